@@ -1,0 +1,322 @@
+/*
+ * oracle.c -- plain, slow, single-threaded fp64 reference for the CSR PCG
+ * solve and its adjoint.  TEST INFRASTRUCTURE ONLY: the library never calls
+ * it.  Only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * load it.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it follows
+ *   - CSR SpMV y = A x: the matvec of torch-sla (arXiv 2601.13994), §3 "sparse
+ *     tensor types" (.matvec) and §4 Figure 2 (scatter-based SpMV), written as
+ *     the plain definition y_i = sum_k A_ik x_k in stored order.
+ *   - Conjugate gradient with a preconditioner (torch-sla §3.3 "Distributed
+ *     CG": the Krylov recurrence with the inner products <r,r> and <p,Ap>;
+ *     §4 Table 3: CG with Jacobi preconditioning), in the Hestenes-Stiefel
+ *     order: q = A p, alpha = rho / p.q, x += alpha p, r -= alpha q,
+ *     z = M^-1 r, beta = r.z / rho, p = z + beta p.
+ *   - Factored sparse approximate inverse M^-1 = G G^T + eps I ("Learning
+ *     Sparse Approximate Inverse Preconditioners for Conjugate Gradient
+ *     Solvers on GPUs", author responses: Reviewer GmV6 Concern 3 for the
+ *     eps I term, Reviewer umir Concern 1 for M^-1 r = G G^T r applied by
+ *     SpMV, Reviewer Rbu2 Concern 3 for A^-1 ~ G G^T with G sparse).  The
+ *     pages learn G with a graph network; here G is the closed-form stand-in
+ *     on the pattern of tril(A): G_ii = A_ii^-1/2,
+ *     G_ij = -A_ij / (2 sqrt(A_ii A_jj)) for j < i.
+ *   - Adjoint (torch-sla §3.3, last paragraph, and §3.2 as summarised in §3):
+ *     solve A^T lambda = dL/dx, then dL/db = lambda and
+ *     dL/dA_ij = -lambda_i x_j on the stored non-zeros.
+ *
+ * Readings where the pages are silent
+ *   - Stopping: ||r||_2 <= tol ||b||_2 on the recursive residual, tested right
+ *     after the r update; when it holds, the true residual of the returned x
+ *     is computed and the solve stops only if that is <= tol ||b|| as well;
+ *     otherwise the iteration continues.  x0 = 0 unless given.  ||b|| = 0
+ *     returns x = 0 after 0 iterations.
+ *   - Iterations = number of products A p inside the loop.
+ *   - Breakdown: p.q <= 0 or not finite, r.z <= 0 or not finite, or a
+ *     non-finite ||r||^2.
+ *   - fp32 systems (f32 != 0): A, b are fp32 values (passed here as the exact
+ *     doubles).  All arithmetic is fp64.  Every working vector of the
+ *     recurrence except x (q, r, z, p and the SPAI intermediate t) is rounded
+ *     to fp32 when it is assigned; x is kept in fp64 and rounded to fp32 when
+ *     returned.  The true-residual test uses that rounded x.
+ *
+ * Build: gcc -O2 -ffp-contract=off -shared -fPIC (no fused multiply-add, so
+ * every product is rounded before it is added).
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_PC_NONE 0
+#define OR_PC_JACOBI 1
+#define OR_PC_SPAI 2
+
+#define OR_OK 0
+#define OR_NOT_CONVERGED 1
+#define OR_BREAKDOWN 2
+#define OR_INVALID 3
+
+static double stor(double v, int f32) { return f32 ? (double)(float)v : v; }
+
+static double dot(int n, const double* u, const double* v) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += u[i] * v[i];
+    return s;
+}
+
+/* y = A x, each row summed in stored order starting from 0. */
+void oracle_spmv(int n, const int* rp, const int* ci, const double* a,
+                 const double* x, double* y) {
+    for (int i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int k = rp[i]; k < rp[i + 1]; ++k) s += a[k] * x[ci[k]];
+        y[i] = s;
+    }
+}
+
+/* Diagonal of A; returns 0 if some A_ii is missing. */
+static int diagonal(int n, const int* rp, const int* ci, const double* a, double* d) {
+    for (int i = 0; i < n; ++i) {
+        int found = 0;
+        for (int k = rp[i]; k < rp[i + 1]; ++k)
+            if (ci[k] == i) { d[i] = a[k]; found = 1; }
+        if (!found) return 0;
+    }
+    return 1;
+}
+
+/* Number of stored entries of tril(A) (columns <= row). */
+long long oracle_spai_nnz(int n, const int* rp, const int* ci) {
+    long long c = 0;
+    for (int i = 0; i < n; ++i)
+        for (int k = rp[i]; k < rp[i + 1]; ++k)
+            if (ci[k] <= i) ++c;
+    return c;
+}
+
+/* G on the pattern of tril(A).  grp[n+1], gci[nnzG], gv[nnzG] are outputs.
+ * Returns OR_INVALID if a diagonal entry is missing or not positive. */
+int oracle_spai_factor(int n, const int* rp, const int* ci, const double* a,
+                       int* grp, int* gci, double* gv) {
+    double* d = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!diagonal(n, rp, ci, a, d)) { free(d); return OR_INVALID; }
+    for (int i = 0; i < n; ++i)
+        if (!(d[i] > 0.0)) { free(d); return OR_INVALID; }
+    int m = 0;
+    grp[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        for (int k = rp[i]; k < rp[i + 1]; ++k) {
+            int j = ci[k];
+            if (j > i) continue;
+            gci[m] = j;
+            if (j == i) gv[m] = 1.0 / sqrt(d[i]);
+            else gv[m] = -a[k] / (2.0 * sqrt(d[i] * d[j]));
+            ++m;
+        }
+        grp[i + 1] = m;
+    }
+    free(d);
+    return OR_OK;
+}
+
+/* z = G (G^T r) + eps r.  t = G^T r is formed by scattering the rows of G
+ * (t_j += G_ij r_i, rows in ascending order), so no transposed copy of G is
+ * built.  t and z are rounded to the storage precision. */
+void oracle_spai_apply(int n, const int* grp, const int* gci, const double* gv,
+                       double eps, int f32, const double* r, double* t, double* z) {
+    for (int j = 0; j < n; ++j) t[j] = 0.0;
+    for (int i = 0; i < n; ++i)
+        for (int k = grp[i]; k < grp[i + 1]; ++k) t[gci[k]] += gv[k] * r[i];
+    for (int j = 0; j < n; ++j) t[j] = stor(t[j], f32);
+    for (int i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int k = grp[i]; k < grp[i + 1]; ++k) s += gv[k] * t[gci[k]];
+        z[i] = stor(s + eps * r[i], f32);
+    }
+}
+
+/* ||b - A xo||^2 with every row sum in fp64. */
+static double true_res2(int n, const int* rp, const int* ci, const double* a,
+                        const double* b, const double* xo) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double y = 0.0;
+        for (int k = rp[i]; k < rp[i + 1]; ++k) y += a[k] * xo[ci[k]];
+        double e = b[i] - y;
+        s += e * e;
+    }
+    return s;
+}
+
+typedef struct {
+    int pc;
+    double eps;
+    int f32;
+    double* dinv_src;      /* Jacobi: A_ii */
+    int* grp; int* gci; double* gv; double* t;   /* SPAI */
+} precond;
+
+static void apply_precond(const precond* M, int n, const double* r, double* z) {
+    if (M->pc == OR_PC_JACOBI) {
+        for (int i = 0; i < n; ++i) z[i] = stor(r[i] / M->dinv_src[i], M->f32);
+    } else if (M->pc == OR_PC_SPAI) {
+        oracle_spai_apply(n, M->grp, M->gci, M->gv, M->eps, M->f32, r, M->t, z);
+    } else {
+        for (int i = 0; i < n; ++i) z[i] = r[i];
+    }
+}
+
+/*
+ * Solve A x = b.  x: on entry the initial guess if use_x0, on exit the
+ * solution (rounded to fp32 values when f32).  Returns a status code; iters,
+ * rel_rec (||r||/||b||, recursive) and rel_true (||b - A x||/||b|| for the
+ * returned x) are written when non-null.
+ */
+int oracle_pcg(int n, const int* rp, const int* ci, const double* a,
+               const double* b, double* x, double tol, int max_iter, int pc,
+               double eps, int f32, int use_x0, int* iters, double* rel_rec,
+               double* rel_true) {
+    if (n < 0 || tol <= 0.0 || max_iter < 0) return OR_INVALID;
+    size_t sz = sizeof(double) * (size_t)(n > 0 ? n : 1);
+    double* xi = (double*)malloc(sz);
+    double* xo = (double*)malloc(sz);
+    double* r = (double*)malloc(sz);
+    double* z = (double*)malloc(sz);
+    double* p = (double*)malloc(sz);
+    double* q = (double*)malloc(sz);
+    precond M;
+    memset(&M, 0, sizeof M);
+    M.pc = pc; M.eps = eps; M.f32 = f32;
+    int status = OR_OK, k = 0;
+    double gamma = 0.0, tr2 = 0.0;
+
+    double bb = dot(n, b, b);
+    if (pc == OR_PC_JACOBI) {
+        M.dinv_src = (double*)malloc(sz);
+        if (!diagonal(n, rp, ci, a, M.dinv_src)) { status = OR_INVALID; goto done; }
+    } else if (pc == OR_PC_SPAI) {
+        long long ng = oracle_spai_nnz(n, rp, ci);
+        M.grp = (int*)malloc(sizeof(int) * (size_t)(n + 1));
+        M.gci = (int*)malloc(sizeof(int) * (size_t)(ng > 0 ? ng : 1));
+        M.gv = (double*)malloc(sizeof(double) * (size_t)(ng > 0 ? ng : 1));
+        M.t = (double*)malloc(sz);
+        if (oracle_spai_factor(n, rp, ci, a, M.grp, M.gci, M.gv) != OR_OK) {
+            status = OR_INVALID; goto done;
+        }
+    }
+
+    if (bb == 0.0) {
+        for (int i = 0; i < n; ++i) x[i] = 0.0;
+        if (iters) *iters = 0;
+        if (rel_rec) *rel_rec = 0.0;
+        if (rel_true) *rel_true = 0.0;
+        goto done;
+    }
+
+    /* r = b - A x0 (or b), z = M^-1 r, p = z, rho = r.z */
+    if (use_x0) {
+        for (int i = 0; i < n; ++i) xi[i] = x[i];
+        oracle_spmv(n, rp, ci, a, xi, q);
+        for (int i = 0; i < n; ++i) r[i] = stor(b[i] - q[i], f32);
+    } else {
+        for (int i = 0; i < n; ++i) { xi[i] = 0.0; r[i] = stor(b[i], f32); }
+    }
+    apply_precond(&M, n, r, z);
+    for (int i = 0; i < n; ++i) p[i] = z[i];
+    double rho = dot(n, r, z);
+    gamma = dot(n, r, r);
+    double tol2bb = tol * tol * bb;
+
+    for (;;) {
+        if (!isfinite(gamma)) { status = OR_BREAKDOWN; break; }
+        if (gamma <= tol2bb) {
+            for (int i = 0; i < n; ++i) xo[i] = stor(xi[i], f32);
+            tr2 = true_res2(n, rp, ci, a, b, xo);
+            if (tr2 <= tol2bb) { status = OR_OK; break; }
+        }
+        if (k >= max_iter) { status = OR_NOT_CONVERGED; break; }
+        if (k > 0) {
+            apply_precond(&M, n, r, z);
+            double rho_new = dot(n, r, z);
+            if (!(rho_new > 0.0) || !isfinite(rho_new)) { status = OR_BREAKDOWN; break; }
+            double beta = rho_new / rho;
+            rho = rho_new;
+            for (int i = 0; i < n; ++i) p[i] = stor(z[i] + beta * p[i], f32);
+        }
+        oracle_spmv(n, rp, ci, a, p, q);
+        for (int i = 0; i < n; ++i) q[i] = stor(q[i], f32);
+        double delta = dot(n, p, q);
+        if (!(delta > 0.0) || !isfinite(delta)) { status = OR_BREAKDOWN; break; }
+        double alpha = rho / delta;
+        for (int i = 0; i < n; ++i) {
+            xi[i] = xi[i] + alpha * p[i];
+            r[i] = stor(r[i] - alpha * q[i], f32);
+        }
+        ++k;
+        gamma = dot(n, r, r);
+    }
+
+    for (int i = 0; i < n; ++i) x[i] = stor(xi[i], f32);
+    if (iters) *iters = k;
+    if (rel_rec) *rel_rec = sqrt(gamma / bb);
+    if (rel_true) *rel_true = sqrt(true_res2(n, rp, ci, a, b, x) / bb);
+
+done:
+    free(xi); free(xo); free(r); free(z); free(p); free(q);
+    free(M.dinv_src); free(M.grp); free(M.gci); free(M.gv); free(M.t);
+    return status;
+}
+
+/* A^T in CSR (columns ascending within each row): a counting pass over the
+ * columns, then rows of A visited in ascending order. */
+static void transpose(int n, const int* rp, const int* ci, const double* a,
+                      int* trp, int* tci, double* ta) {
+    int nnz = rp[n];
+    for (int j = 0; j <= n; ++j) trp[j] = 0;
+    for (int k = 0; k < nnz; ++k) trp[ci[k] + 1]++;
+    for (int j = 0; j < n; ++j) trp[j + 1] += trp[j];
+    int* fill = (int*)malloc(sizeof(int) * (size_t)(n > 0 ? n : 1));
+    for (int j = 0; j < n; ++j) fill[j] = trp[j];
+    for (int i = 0; i < n; ++i)
+        for (int k = rp[i]; k < rp[i + 1]; ++k) {
+            int pos = fill[ci[k]]++;
+            tci[pos] = i;
+            ta[pos] = a[k];
+        }
+    free(fill);
+}
+
+/*
+ * Adjoint of x = A^-1 b for the upstream gradient g = dL/dx:
+ * solve A^T lambda = g (same preconditioner kind, tolerance and iteration
+ * cap), then dL/db = lambda and dL/dA_k = -lambda_row(k) * x_col(k) for every
+ * stored entry k.  In fp32 mode lambda is rounded to fp32 as it is returned
+ * and dL/dA is formed from that rounded lambda, then rounded.
+ */
+int oracle_adjoint(int n, const int* rp, const int* ci, const double* a,
+                   const double* x, const double* g, double tol, int max_iter,
+                   int pc, double eps, int f32, double* dldb, double* dlda,
+                   int* iters, double* rel_rec, double* rel_true) {
+    int nnz = rp[n];
+    int* trp = (int*)malloc(sizeof(int) * (size_t)(n + 1));
+    int* tci = (int*)malloc(sizeof(int) * (size_t)(nnz > 0 ? nnz : 1));
+    double* ta = (double*)malloc(sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+    transpose(n, rp, ci, a, trp, tci, ta);
+    int st = oracle_pcg(n, trp, tci, ta, g, dldb, tol, max_iter, pc, eps, f32, 0,
+                        iters, rel_rec, rel_true);
+    if (st != OR_INVALID) {
+        for (int i = 0; i < n; ++i)
+            for (int k = rp[i]; k < rp[i + 1]; ++k)
+                dlda[k] = stor(-dldb[i] * x[ci[k]], f32);
+    }
+    free(trp); free(tci); free(ta);
+    return st;
+}
+
+/* ||b - A x||_2 / ||b||_2 (0 when b = 0). */
+double oracle_rel_residual(int n, const int* rp, const int* ci, const double* a,
+                           const double* b, const double* x) {
+    double bb = dot(n, b, b);
+    if (bb == 0.0) return 0.0;
+    return sqrt(true_res2(n, rp, ci, a, b, x) / bb);
+}
