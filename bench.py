@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark: preconditioned CG + adjoint on one B300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+
+A step is one pass of the whole hot path on the workload: the forward PCG
+solve A x = b and the backward pass (adjoint solve A^T lambda = g, dL/db,
+dL/dA on the pattern).  The headline metric is PCG iterations per second
+(forward + adjoint iterations / wall time on the device), with the
+per-iteration HBM traffic of the algorithmic byte model, the fused SpMV + dot
+kernel's achieved bandwidth, and the solve time.
+
+Default workload (N = 1): 2D 5-point variable-coefficient diffusion,
+1024 x 1024 grid, k = exp(N(0,1)), fp64, Jacobi-PCG to 1e-8, b ~ N(0,1),
+g ~ N(0,1).  Under torchrun every rank solves its own replica (no data-path
+collective); value = iterations of all ranks / max-over-ranks time.
+`--impl reference` times the plain CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DESCR = {
+    "c1": "2D 5-point Poisson 64x64 Dirichlet (n=4096, nnz=20224), fp64, CG to 1e-10, b = A x*",
+    "c2": "2D 5-point variable-coefficient diffusion 1024x1024 (n=1048576, nnz=5238784), "
+          "k=exp(N(0,1)) harmonic faces, fp64, Jacobi-PCG to 1e-8, b,g ~ N(0,1)",
+    "c3": "64 systems on one 256x256 5-point pattern, k=exp(0.5 N(0,1)), fp32 values, "
+          "Jacobi-PCG to 1e-5 per system, b ~ U(-1,1)",
+    "c4": "3D 7-point Poisson 128^3 (n=2097152, nnz=14581760), fp64, CG to 1e-8, b,g ~ N(0,1)",
+    "c5": "kNN graph Laplacian, 4M points in the unit cube, k=12 union, A = L + 1e-3 I, relabelled, fp64, "
+          "SPAI-PCG (G G^T + 1e-3 I) to 1e-8",
+}
+MAX_ITER = 200000
+L2_BYTES = 126 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def byte_model(w, nnzg=None):
+    """Algorithmic bytes: per CG iteration, per fused SpMV + dot launch, and
+    for the dL/dA pass.  Indices int32; s = value bytes; col_idx/row_ptr of a
+    shared-pattern batch counted once."""
+    A = w.A
+    n, nnz, B = A.n, A.nnz, A.batch
+    s = 4 if w.dtype == "f32" else 8
+    rp = 4 * (n + 1)
+    if w.pc == "spai":
+        it = 12 * nnz + 24 * nnzg + 3 * rp + 128 * n
+    elif w.pc == "jacobi":
+        it = (s * nnz * B + 4 * nnz + rp + 13 * s * n * B)
+    else:
+        it = (s * nnz * B + 4 * nnz + rp + 11 * s * n * B)
+    spmv = s * nnz * B + 4 * nnz + rp + 2 * s * n * B
+    grad = (4 * nnz + rp + s * nnz * B + 2 * s * n * B)
+    return {"per_iteration": it, "spmv_dot_per_launch": spmv, "grad_A": grad}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "sparse_iterative_linear_csr_b300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config, kernel, src_hash):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (profiles/traffic.tsv)."""
+    p = os.path.join(ROOT, "profiles", "traffic.tsv")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.rstrip("\n").split("\t")
+        if len(f) >= 4 and f[0] == config and f[1] == kernel and f[2] == src_hash:
+            return float(f[3])
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.proc = None
+        self.bus_id = bus_id
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def bus_id_of(dev):
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return None
+
+
+def cpu_sample(w, budget_s=12.0):
+    """The oracle as it stands, single-threaded, on a bounded number of PCG
+    iterations of the same workload (first system of a batch)."""
+    import numpy as np
+    import oracle
+    A = w.A
+    b = w.b if w.b.ndim == 1 else w.b[0]
+    if A.vals.ndim == 2:
+        from workloads.matrices import CSR
+        A = CSR(A.n, A.row_ptr, A.col_idx, A.vals[0])
+    t0 = time.perf_counter()
+    _, inf = oracle.pcg(A, b, w.tol, max_iter=3, pc=w.pc, eps=w.eps)
+    t_small = time.perf_counter() - t0
+    per_it = max(t_small / 4.0, 1e-6)
+    cap = int(max(3, min(MAX_ITER, budget_s / per_it)))
+    t0 = time.perf_counter()
+    _, inf = oracle.pcg(A, b, w.tol, max_iter=cap, pc=w.pc, eps=w.eps)
+    dt = time.perf_counter() - t0
+    its = max(inf["iters"], 1)
+    return {"value": its / dt, "unit": "iterations/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {its} PCG iterations of the forward solve (system 0), {dt:.1f} s, "
+                      f"single-threaded fp64 C oracle"}
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    import oracle  # noqa: F401
+    A = w.A
+    b = w.b if w.b.ndim == 1 else w.b[0]
+    if A.vals.ndim == 2:
+        from workloads.matrices import CSR
+        A = CSR(A.n, A.row_ptr, A.col_idx, A.vals[0])
+    import oracle as orc
+    t0 = time.perf_counter()
+    orc.pcg(A, b, w.tol, max_iter=3, pc=w.pc, eps=w.eps)
+    per_it = max((time.perf_counter() - t0) / 4.0, 1e-6)
+    cap = int(max(2, min(MAX_ITER, 4.0 / per_it)))   # ~4 s of CPU work per step
+    for _ in range(args.warmup):
+        orc.pcg(A, b, w.tol, max_iter=max(2, cap // 4), pc=w.pc, eps=w.eps)
+    its = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _, inf = orc.pcg(A, b, w.tol, max_iter=cap, pc=w.pc, eps=w.eps)
+        its += inf["iters"]
+    dt = time.perf_counter() - t0
+    v = its / dt
+    line = {"metric": "PCG iterations/s", "value": v, "unit": "iterations/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64" if w.dtype == "f64" else "f32",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": w.A.n, "nnz": w.A.nnz,
+                       "pc": w.pc, "tol": w.tol},
+            "cpu_baseline": {"value": v, "unit": "iterations/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{cap} PCG iterations per step of the forward solve (system 0)"},
+            "e2e": {"value": v, "unit": "iterations/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c2", choices=sorted(DESCR))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--poll-k", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from workloads import build
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = build(args.config)
+        run_reference(args, w, rank)
+        return
+
+    import numpy as np
+    import torch
+    import sparse_iterative_linear_csr_b300 as sla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = build(args.config)
+    A = w.A
+    stream = torch.cuda.current_stream()
+    rp = torch.from_numpy(A.row_ptr).to(dev)
+    ci = torch.from_numpy(A.col_idx).to(dev)
+    vals = torch.from_numpy(A.vals).to(dev)
+    b = torch.from_numpy(w.b).to(dev)
+    g = torch.from_numpy(w.g).to(dev)
+    M = sla.CSRMatrix(rp, ci, vals)
+    kw = dict(tol=w.tol, max_iter=MAX_ITER, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3,
+              poll_k=args.poll_k)
+
+    def step():
+        x, inf = M.solve(b, **kw)
+        dldb, dlda, ainf = M.adjoint(x, g, **kw)
+        return x, inf, ainf
+
+    for _ in range(max(args.warmup, 0)):
+        x, inf, ainf = step()
+    bad = [i.status for i in inf + ainf if i.status != "ok"]
+    if bad:
+        raise SystemExit(f"solve did not converge: {bad}")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(bus_id_of(dev))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    iters = 0
+    l0 = sla.launch_count()
+    barrier()
+    sampler.start()
+    e0.record(stream)
+    t_wall = time.perf_counter()
+    solve_ms = []
+    for _ in range(args.steps):
+        x, inf, ainf = step()
+        iters += sum(i.iters for i in inf) + sum(i.iters for i in ainf)
+    e1.record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    launches = sla.launch_count() - l0
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+        it = torch.tensor([iters], device=dev, dtype=torch.float64)
+        dist.all_reduce(it, op=dist.ReduceOp.SUM)
+        iters_all = int(it.item())
+    else:
+        iters_all = iters
+    value = iters_all / (ms / 1000.0)
+
+    # forward solve time alone (one extra timed solve, same configuration)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    _, finf = M.solve(b, **kw)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = f0.elapsed_time(f1)
+
+    # dominant kernel: the fused SpMV + dot, timed alone on the same operands
+    nnzg = (A.nnz + A.n) // 2 if w.pc == "spai" else None
+    bm = byte_model(w, nnzg)
+    reps = 50
+    xin = x.contiguous()
+    for _ in range(5):
+        M.matvec_dot(xin)
+    k0 = torch.cuda.Event(enable_timing=True)
+    k1 = torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(reps):
+        M.matvec_dot(xin)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    kern_ms = k0.elapsed_time(k1) / reps
+    peak, peak_kind = peaks()
+    achieved = bm["spmv_dot_per_launch"] / (kern_ms * 1e-3) / 1e9
+    src = kernel_source_hash()
+    traffic = recorded_traffic(args.config, "k_spmv", src)
+
+    per_it_gbs = bm["per_iteration"] * iters / (ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (values, b, g) from pinned memory, solve + adjoint, D2H of x,
+    # dL/db and dL/dA into pinned memory, all inside the timed region.
+    h_vals = vals.cpu().pin_memory()
+    h_b = b.cpu().pin_memory()
+    h_g = g.cpu().pin_memory()
+    d_vals2 = torch.empty_like(vals)
+    o_x = torch.empty_like(h_b).pin_memory()
+    o_lb = torch.empty_like(h_b).pin_memory()
+    o_la = torch.empty_like(h_vals).pin_memory()
+    h2d = h_vals.numel() * h_vals.element_size() + 2 * h_b.numel() * h_b.element_size()
+    d2h = 2 * h_b.numel() * h_b.element_size() + h_vals.numel() * h_vals.element_size()
+    barrier()
+    t0 = time.perf_counter()
+    e2e_iters = 0
+    for _ in range(args.e2e_steps):
+        d_vals2.copy_(h_vals, non_blocking=True)
+        db = h_b.to(dev, non_blocking=True)
+        dg = h_g.to(dev, non_blocking=True)
+        M.update_values(d_vals2)
+        xx, i1 = M.solve(db, **kw)
+        lb, la, i2 = M.adjoint(xx, dg, **kw)
+        o_x.copy_(xx, non_blocking=True)
+        o_lb.copy_(lb, non_blocking=True)
+        o_la.copy_(la, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_iters += sum(i.iters for i in i1) + sum(i.iters for i in i2)
+    e2e_s = time.perf_counter() - t0
+    e2e_value = e2e_iters / e2e_s * world
+    M.update_values(vals)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_sample(w)
+
+    if rank == 0:
+        line = {
+            "metric": "PCG iterations/s (forward + adjoint); HBM GB/s per iteration (fraction of B300 peak); solve ms",
+            "value": value, "unit": "iterations/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": A.n, "nnz": A.nnz,
+                       "batch": A.batch, "pc": w.pc, "tol": w.tol, "poll_k": args.poll_k,
+                       "step": "forward PCG solve + adjoint solve + dL/dA pass",
+                       "l2": f"inputs larger than L2: {bm['per_iteration'] / 1e6:.1f} MB touched per iteration "
+                             f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"},
+            "iterations_per_step": iters // max(args.steps, 1),
+            "forward_iterations": finf[0].iters, "solve_ms": fwd_ms,
+            "hbm_gbs_per_iteration": per_it_gbs,
+            "hbm_frac_per_iteration": {"of_measured": per_it_gbs / peak, "of_nominal_8tbs": per_it_gbs / NOMINAL_HBM_GBS},
+            "bytes_per_iteration_model": bm["per_iteration"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "kernel": "k_spmv (staged CSR SpMV fused with x.Ax), timed alone on the step's matrix",
+                         "algorithmic_bytes_per_launch": bm["spmv_dot_per_launch"], "ms_per_launch": kern_ms,
+                         "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
+            "e2e": {"value": e2e_value, "unit": "iterations/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+            "wall_s_timed": t_wall, "kernel_src": src,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * sla.h -- C ABI of the B300 (sm_103a) sparse iterative linear solver:
+ * preconditioned conjugate gradient on a CSR matrix and its adjoint.
+ *
+ * Sources of the operations (page title, then section):
+ *  - "torch-sla: Differentiable Sparse Linear Algebra with Adjoint Solvers and
+ *    Sparse Tensor Parallelism for PyTorch" (arXiv 2601.13994):
+ *      §3 sparse tensor types: one matrix, or a batch of matrices sharing one
+ *         sparsity pattern whose set-up is reused across the batch; the
+ *         .matvec and .solve methods;
+ *      §3 autograd wrapper: forward stashes (A, x), backward runs one adjoint
+ *         solve;
+ *      §3.3 distributed CG: the CG recurrence with the inner products <r,r>
+ *         and <p,Ap>; the adjoint A^T lambda = dL/dx and the matrix gradient
+ *         -lambda_i x_j on the stored non-zeros;
+ *      §4 Table 3: CG with Jacobi preconditioning; §4 Figure 2: an absolute /
+ *         relative stopping tolerance on the residual.
+ *  - "Learning Sparse Approximate Inverse Preconditioners for Conjugate
+ *    Gradient Solvers on GPUs" (author responses): the factored
+ *    preconditioner M^-1 = G G^T + eps I applied with two SpMVs (Reviewer umir
+ *    Concern 1; Reviewer GmV6 Concern 3 for eps).  G is the closed-form factor
+ *    on the pattern of tril(A): G_ii = A_ii^-1/2,
+ *    G_ij = -A_ij / (2 sqrt(A_ii A_jj)) for j < i.
+ *
+ * Conventions for every call
+ *  - Pointers named d_* are device pointers owned by the caller.  The matrix
+ *    arrays passed to sla_csr_create must stay alive and unchanged for the
+ *    life of the handle (sla_csr_update_values swaps in new values).
+ *  - CSR: row_ptr int32[n+1] with row_ptr[0] = 0 and row_ptr[n] = nnz;
+ *    col_idx int32[nnz], strictly ascending within each row, 0 <= col < n;
+ *    values [batch][nnz] in the handle's dtype (fp64 or fp32), system s at
+ *    offset s*nnz.
+ *  - Vectors of a batch are [batch][n], system s at offset s*n.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
+ *    work of a call is ordered on it.  sla_pcg_solve and sla_adjoint return
+ *    after the solve has finished on the device (they synchronise `stream`);
+ *    sla_spmv and sla_spmv_dot return without synchronising.
+ *  - One call at a time per handle: the handle owns the solver workspace.
+ *  - Every function returns SLA_OK or an error code; sla_last_error() gives
+ *    a message for the calling thread's last error.
+ */
+#ifndef SLA_H
+#define SLA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sla_csr* sla_handle;
+
+typedef enum {
+    SLA_OK = 0,
+    SLA_ERR_INVALID = 1,        /* bad argument or malformed CSR */
+    SLA_ERR_CUDA = 2,           /* a CUDA runtime call failed */
+    SLA_ERR_NOMEM = 3,          /* device or pinned allocation failed */
+    SLA_ERR_NOT_CONVERGED = 4,  /* max_iter reached; x holds the last iterate */
+    SLA_ERR_BREAKDOWN = 5,      /* p.Ap <= 0, r.z <= 0 or a non-finite value */
+    SLA_ERR_TIMEOUT = 6,        /* host wall-clock limit; x holds the last iterate */
+    SLA_ERR_UNSUPPORTED = 7     /* valid request this build does not serve */
+} sla_status;
+
+typedef enum { SLA_F64 = 0, SLA_F32 = 1 } sla_dtype;
+
+typedef enum {
+    SLA_PC_NONE = 0,    /* z = r */
+    SLA_PC_JACOBI = 1,  /* z_i = r_i / A_ii */
+    SLA_PC_SPAI = 2     /* z = G (G^T r) + eps r */
+} sla_pc;
+
+/* sla_csr_create flags */
+#define SLA_VALIDATE 1u   /* check the CSR structure on the device; SLA_ERR_INVALID on failure */
+
+typedef struct {
+    double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
+                          the returned x meets the same bound; tol > 0 */
+    int max_iter;      /* cap on products A p per system; >= 0 */
+    sla_pc pc;         /* preconditioner */
+    double eps;        /* SPAI shift (ignored otherwise), >= 0 */
+    int poll_k;        /* iterations between host checks of the device flag; 0 = default (32) */
+    int use_x0;        /* nonzero: d_x holds the initial guess on entry */
+    double timeout_s;  /* host wall-clock limit per call; <= 0 = none */
+} sla_pcg_opts;
+
+typedef struct {
+    int iters;                 /* products A p performed in the iteration loop */
+    double rel_res_recursive;  /* ||r||_2 / ||b||_2 of the recursively updated r */
+    double rel_res_true;       /* ||b - A x||_2 / ||b||_2 for the returned x */
+    sla_status status;         /* per-system outcome */
+} sla_solve_info;
+
+/* Fill *o with defaults: tol 1e-8, max_iter 10000, SLA_PC_NONE, eps 1e-3,
+ * poll_k 32, use_x0 0, timeout_s 0. */
+void sla_pcg_opts_default(sla_pcg_opts* o);
+
+/*
+ * Create a handle for an n x n CSR matrix (or a batch of `batch` matrices on
+ * one pattern).  Analyses the pattern (row blocks for the SpMV kernels, the
+ * diagonal, the SPAI factor G and its explicit transpose) on the device.
+ * n >= 1, 0 <= nnz < 2^31, batch >= 1.  The handle keeps the three pointers
+ * (it copies nothing but derived data).  With SLA_VALIDATE the structure is
+ * checked first (monotone row_ptr, row_ptr[0] = 0, row_ptr[n] = nnz, columns
+ * in range and strictly ascending).  A missing or non-positive diagonal entry
+ * is reported when a solve asks for a preconditioner that needs it.
+ * Synchronises `stream`.
+ */
+sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
+                          const int* d_row_ptr, const int* d_col_idx, const void* d_vals,
+                          unsigned flags, void* stream, sla_handle* out);
+
+/* Replace the values (same pattern, same dtype, [batch][nnz]); recomputes the
+ * value-dependent set-up (diagonal, G, G^T).  Synchronises `stream`. */
+sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream);
+
+/* y = A x for every system (torch-sla §3, .matvec).  d_x, d_y: [batch][n]. */
+sla_status sla_spmv(sla_handle h, const void* d_x, void* d_y, void* stream);
+
+/* y = A x and d_dot[s] = x_s . y_s (fp64, one per system) in one fused pass:
+ * the q = A p, delta = p.q step of CG. */
+sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot, void* stream);
+
+/*
+ * Solve A x = b by preconditioned CG, every system of a batch independently
+ * (converged systems are frozen while the others continue).  d_b, d_x:
+ * [batch][n].  x0 = 0 unless opts->use_x0.  info: host array of `batch`
+ * entries, filled on return.  Returns SLA_OK when every system converged,
+ * else the first non-OK per-system status (x still holds each system's last
+ * iterate).  ||b|| = 0 gives x = 0 after 0 iterations.  fp32 handles keep
+ * x in fp64 during the solve and round it to fp32 on return.
+ */
+sla_status sla_pcg_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg_opts* opts,
+                         sla_solve_info* info, void* stream);
+
+/*
+ * Adjoint of x = A^-1 b for an upstream gradient g = dL/dx: solves
+ * A^T lambda = g with the same options (A^T = A: CG needs a symmetric
+ * matrix), then writes dL/db = lambda into d_dLdb [batch][n] and
+ * dL/dA_k = -lambda_row(k) * x_col(k) for every stored entry k into d_dLdA
+ * [batch][nnz] (torch-sla §3.3, adjoint paragraph).  d_x is the forward
+ * solution.  d_dLdA may be NULL to skip the matrix gradient.
+ */
+sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla_pcg_opts* opts,
+                       void* d_dLdb, void* d_dLdA, sla_solve_info* info, void* stream);
+
+/* Free the handle and everything it owns (not the caller's arrays). */
+sla_status sla_csr_destroy(sla_handle h);
+
+/* Message for the calling thread's last error ("" if none). */
+const char* sla_last_error(void);
+
+/* Number of kernels this library has launched in the process (graph nodes
+ * count once per graph launch).  Diagnostics for benchmarks. */
+unsigned long long sla_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SLA_H */

@@ -1,0 +1,233 @@
+// setup.cuh -- once-per-pattern (and once-per-values) device set-up:
+// CSR validation, diagonal extraction, row-block partition for the staged
+// SpMV, an exclusive scan, the closed-form SPAI factor G on tril(A) and its
+// explicit transpose, and the [batch][*] <-> [*][batch] layout transposes.
+#pragma once
+
+#include "common.cuh"
+
+namespace sla {
+
+enum : int {
+    ERR_ROWPTR = 1,       // row_ptr[0] != 0, row_ptr[n] != nnz, or decreasing
+    ERR_COL_RANGE = 2,    // a column outside [0, n)
+    ERR_COL_ORDER = 4,    // columns not strictly ascending within a row
+    ERR_NO_DIAG = 8,      // some A_ii not stored
+    ERR_DIAG_SIGN = 16,   // some A_ii <= 0 (or not finite)
+    ERR_ASYM = 32,        // pattern not symmetric (G^T construction)
+};
+
+// Structure check, one thread per row.  Column reads stay inside
+// [row_ptr[i], row_ptr[i+1]) only after that range was found valid.
+__global__ void k_validate(int n, long long nnz, const int* __restrict__ rp, const int* __restrict__ ci,
+                           int* err) {
+    int bits = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int a = rp[i], b = rp[i + 1];
+        if (i == 0 && a != 0) bits |= ERR_ROWPTR;
+        if (i == n - 1 && (long long)b != nnz) bits |= ERR_ROWPTR;
+        if (a < 0 || b < a || (long long)b > nnz) { bits |= ERR_ROWPTR; continue; }
+        int prev = -1;
+        for (int k = a; k < b; ++k) {
+            const int c = ci[k];
+            if (c < 0 || c >= n) bits |= ERR_COL_RANGE;
+            if (c <= prev) bits |= ERR_COL_ORDER;
+            prev = c;
+        }
+    }
+    if (bits) atomicOr(err, bits);
+}
+
+// Position of column c in row i (columns ascending), or -1.
+__device__ __forceinline__ int find_col(const int* __restrict__ ci, int a, int b, int c) {
+    int lo = a, hi = b;
+    while (lo < hi) {
+        const int m = (lo + hi) >> 1;
+        if (ci[m] < c) lo = m + 1; else hi = m;
+    }
+    return (lo < b && ci[lo] == c) ? lo : -1;
+}
+
+// diag[s*n + i] = A_ii of system s (fp64), dpos[i] = its position; error bits
+// for a missing (or non-positive, when checked) diagonal.
+template <typename T>
+__global__ void k_diag(int n, long long nnz, int batch, const int* __restrict__ rp, const int* __restrict__ ci,
+                       const T* __restrict__ av, double* diag, int* err) {
+    int bits = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int k = find_col(ci, rp[i], rp[i + 1], i);
+        for (int s = 0; s < batch; ++s) {
+            if (k < 0) { diag[(size_t)s * n + i] = 0.0; bits |= ERR_NO_DIAG; continue; }
+            const double d = (double)av[(size_t)s * nnz + k];
+            diag[(size_t)s * n + i] = d;
+            if (!(d > 0.0) || !isfinite(d)) bits |= ERR_DIAG_SIGN;
+        }
+    }
+    if (bits) atomicOr(err, bits);
+}
+
+__global__ void k_recip(size_t m, const double* __restrict__ d, double* __restrict__ dinv) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < m; i += (size_t)gridDim.x * blockDim.x)
+        dinv[i] = 1.0 / d[i];
+}
+
+// ----------------------------------------------------------------- row blocks
+// Rows are taken in chunks of MAXR; inside a chunk a block grows while its
+// non-zeros fit `tile`; a row longer than `tile` is a block alone.
+__device__ __forceinline__ int walk_chunk(const int* __restrict__ rp, int n, int c, int tile, int* out) {
+    int r = c * MAXR;
+    const int rend = min(r + MAXR, n);
+    int nb = 0;
+    while (r < rend) {
+        if (out) out[nb] = r;
+        const int k0 = rp[r];
+        if (rp[r + 1] - k0 > tile) ++r;
+        else while (r < rend && rp[r + 1] - k0 <= tile) ++r;
+        ++nb;
+    }
+    return nb;
+}
+
+__global__ void k_rb_count(const int* __restrict__ rp, int n, int tile, int* cnt) {
+    const int nch = (n + MAXR - 1) / MAXR;
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nch; c += gridDim.x * blockDim.x)
+        cnt[c] = walk_chunk(rp, n, c, tile, nullptr);
+}
+
+__global__ void k_rb_fill(const int* __restrict__ rp, int n, int tile, const int* __restrict__ off, int* rbs) {
+    const int nch = (n + MAXR - 1) / MAXR;
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nch; c += gridDim.x * blockDim.x)
+        walk_chunk(rp, n, c, tile, rbs + off[c]);
+    if (blockIdx.x == 0 && threadIdx.x == 0) rbs[off[nch]] = n;
+}
+
+// ----------------------------------------------------------------- scan
+// Exclusive prefix sum, SCAN_T threads x SCAN_V items per CTA; CTA totals go
+// to `sums` and are scanned recursively by the host driver.
+constexpr int SCAN_T = 1024, SCAN_V = 8, SCAN_TILE = SCAN_T * SCAN_V;
+
+__global__ void __launch_bounds__(SCAN_T) k_scan_tile(int* d, long long m, int* sums) {
+    __shared__ int wsum[SCAN_T / 32];
+    const long long base = (long long)blockIdx.x * SCAN_TILE + (long long)threadIdx.x * SCAN_V;
+    int v[SCAN_V], tsum = 0;
+#pragma unroll
+    for (int j = 0; j < SCAN_V; ++j) {
+        v[j] = (base + j < m) ? d[base + j] : 0;
+        const int t = v[j];
+        v[j] = tsum;
+        tsum += t;
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int s = wsum[lane];
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += y;
+        }
+        wsum[lane] = si - s;  // exclusive over warps
+        if (lane == 31 && sums) sums[blockIdx.x] = si;
+    }
+    __syncthreads();
+    const int off = wsum[w] + incl - tsum;
+#pragma unroll
+    for (int j = 0; j < SCAN_V; ++j)
+        if (base + j < m) d[base + j] = v[j] + off;
+}
+
+__global__ void k_scan_add(int* d, long long m, const int* __restrict__ sums) {
+    const long long base = (long long)blockIdx.x * SCAN_TILE;
+    const int add = sums[blockIdx.x];
+    for (int j = threadIdx.x; j < SCAN_TILE; j += blockDim.x)
+        if (base + j < m) d[base + j] += add;
+}
+
+// ----------------------------------------------------------------- SPAI factor
+// Closed-form factor on the pattern of tril(A) ("Learning Sparse Approximate
+// Inverse Preconditioners ...": M^-1 = G G^T + eps I with G sparse lower
+// triangular): G_ii = A_ii^-1/2, G_ij = -A_ij / (2 sqrt(A_ii A_jj)), j < i.
+// Row i of G is the prefix of row i of A with columns <= i; row j of G^T
+// holds G_ij for the columns i >= j of row j of A (the pattern is symmetric),
+// each value read from row i of A, so G^T is a true transpose of G.
+
+// cntG[i] = #{cols <= i in row i}, cntGT[i] = #{cols >= i in row i}
+__global__ void k_tri_count(int n, const int* __restrict__ rp, const int* __restrict__ ci, int* cntG,
+                            int* cntGT) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int a = rp[i], b = rp[i + 1];
+        int lo = a, hi = b;  // first column > i
+        while (lo < hi) {
+            const int m = (lo + hi) >> 1;
+            if (ci[m] <= i) lo = m + 1; else hi = m;
+        }
+        const int le = lo - a;
+        const int has_diag = (lo > a && ci[lo - 1] == i);
+        cntG[i] = le;
+        cntGT[i] = (b - a) - le + has_diag;
+    }
+}
+
+template <typename T>
+__global__ void k_fill_G(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
+                         const double* __restrict__ diag, const int* __restrict__ grp, int* gci, double* gv) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        int m = grp[i];
+        const int end = grp[i + 1];
+        const double di = diag[i];
+        for (int k = rp[i]; m < end; ++k, ++m) {
+            const int j = ci[k];
+            gci[m] = j;
+            gv[m] = (j == i) ? 1.0 / sqrt(di) : -(double)av[k] / (2.0 * sqrt(di * diag[j]));
+        }
+    }
+}
+
+template <typename T>
+__global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
+                          const double* __restrict__ diag, const int* __restrict__ gtrp, int* gtci, double* gtv,
+                          int* err) {
+    int bits = 0;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
+        int m = gtrp[j];
+        const int end = gtrp[j + 1];
+        const double dj = diag[j];
+        const int b = rp[j + 1];
+        for (int k = b - (end - m); k < b; ++k, ++m) {
+            const int i = ci[k];   // i >= j
+            gtci[m] = i;
+            if (i == j) { gtv[m] = 1.0 / sqrt(dj); continue; }
+            const int pos = find_col(ci, rp[i], rp[i + 1], j);
+            if (pos < 0) { bits |= ERR_ASYM; gtv[m] = 0.0; continue; }
+            gtv[m] = -(double)av[pos] / (2.0 * sqrt(diag[i] * dj));
+        }
+    }
+    if (bits) atomicOr(err, bits);
+}
+
+// ----------------------------------------------------------------- layouts
+// out[c][r] = in[r][c] for a rows x cols matrix (32 x 32 tiles).
+template <typename T>
+__global__ void k_transpose(const T* __restrict__ in, T* __restrict__ out, long long rows, long long cols) {
+    __shared__ T tile[32][33];
+    const long long c0 = (long long)blockIdx.x * 32, r0 = (long long)blockIdx.y * 32;
+    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+        const long long r = r0 + dy, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[dy][threadIdx.x] = in[r * cols + c];
+    }
+    __syncthreads();
+    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+        const long long c = c0 + dy, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) out[c * rows + r] = tile[threadIdx.x][dy];
+    }
+}
+
+}  // namespace sla

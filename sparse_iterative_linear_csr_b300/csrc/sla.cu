@@ -1,0 +1,814 @@
+// sla.cu -- C ABI of the sm_103a CSR PCG library (declared in include/sla.h).
+//
+// Host side of the solver: handle life cycle, device set-up, and the
+// iteration driver.  The driver captures `poll_k` CG iterations into one CUDA
+// graph per (preconditioner, eps, k) and launches it repeatedly; every kernel
+// of an iteration returns at once when its system is frozen, so the host
+// only reads the batch-wide "all done" flag (one 4-byte copy to pinned memory
+// per graph launch, two launches kept in flight) instead of synchronising
+// every iteration.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <type_traits>
+#include <vector>
+
+#include "../../include/sla.h"
+#include "common.cuh"
+#include "kernels.cuh"
+#include "setup.cuh"
+
+using namespace sla;
+
+// ===================================================================== errors
+static thread_local std::string g_err;
+static std::atomic<unsigned long long> g_launches{0};
+
+static sla_status fail(sla_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+#define CU(call)                                                                              \
+    do {                                                                                      \
+        cudaError_t e_ = (call);                                                              \
+        if (e_ != cudaSuccess)                                                                \
+            return fail(e_ == cudaErrorMemoryAllocation ? SLA_ERR_NOMEM : SLA_ERR_CUDA,      \
+                        "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__,     \
+                        __LINE__);                                                            \
+    } while (0)
+
+#define TRY(expr)                            \
+    do {                                     \
+        sla_status s_ = (expr);              \
+        if (s_ != SLA_OK) return s_;         \
+    } while (0)
+
+static sla_status launched() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return SLA_OK;
+}
+
+// ===================================================================== handle
+struct DevBuf {
+    void* p = nullptr;
+    size_t bytes = 0;
+    sla_status alloc(size_t b) {
+        release();
+        if (b == 0) b = 16;
+        cudaError_t e = cudaMalloc(&p, b);
+        if (e != cudaSuccess) {
+            p = nullptr;
+            return fail(SLA_ERR_NOMEM, "cudaMalloc(%zu) failed: %s", b, cudaGetErrorString(e));
+        }
+        bytes = b;
+        return SLA_OK;
+    }
+    void release() {
+        if (p) cudaFree(p);
+        p = nullptr;
+        bytes = 0;
+    }
+    template <typename T>
+    T* as() const { return static_cast<T*>(p); }
+};
+
+struct GraphCache {
+    cudaGraphExec_t exec = nullptr;
+    int k = 0;
+    double eps = 0.0;
+    int nodes = 0;
+    void reset() {
+        if (exec) cudaGraphExecDestroy(exec);
+        exec = nullptr;
+        k = 0;
+        nodes = 0;
+    }
+};
+
+struct RowBlocks {
+    DevBuf rbs;
+    int nblk = 0;
+    int tile = 0;
+};
+
+struct sla_csr {
+    int n = 0;
+    long long nnz = 0;
+    int batch = 1;
+    sla_dtype dt = SLA_F64;
+    size_t es = 8;  // bytes per stored value
+    const int* rp = nullptr;
+    const int* ci = nullptr;
+    const void* vals = nullptr;
+    int device = 0;
+    int sms = 0;
+
+    RowBlocks A;
+    int diag_err = 0;  // ERR_NO_DIAG | ERR_DIAG_SIGN
+    DevBuf diag, dinv;
+
+    // SPAI factor (built on first use, per values)
+    bool spai_ready = false;
+    int spai_err = 0;
+    long long nnzg = 0;
+    DevBuf grp, gci, gv, gtrp, gtci, gtv;
+    RowBlocks G, GT;
+
+    // workspace
+    DevBuf x, r, p, q, z, t, bw;
+    DevBuf state, ctl, cnt, part, stat;
+    int pstride = 0;
+    int* h_flag = nullptr;     // pinned [2]
+    Stat* h_stat = nullptr;    // pinned [batch]
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    cudaStream_t cap = nullptr;  // capture stream
+    GraphCache graph[3];
+};
+
+static int pick_tile(long long nnz, int n) {
+    const double per_chunk = (double)MAXR * (double)nnz / (double)(n > 0 ? n : 1) * 1.15;
+    if (per_chunk <= 1024) return 1024;
+    if (per_chunk <= 2048) return 2048;
+    return 4096;
+}
+
+template <class F>
+static void with_tile(int tile, F&& f) {
+    switch (tile) {
+        case 1024: f(std::integral_constant<int, 1024>{}); break;
+        case 2048: f(std::integral_constant<int, 2048>{}); break;
+        default: f(std::integral_constant<int, 4096>{}); break;
+    }
+}
+
+static size_t smem_for(int tile) { return (size_t)tile * 2 * sizeof(double); }
+
+// Opt in to >48 KB dynamic shared memory for every staged-SpMV kernel of one
+// (T, TILE) instantiation.  Runs once per process and instantiation.
+template <typename T, int TILE>
+static sla_status prepare_kernels() {
+    static std::atomic<int> done{0};
+    if (done.load()) return SLA_OK;
+    const int bytes = (int)smem_for(TILE);
+    CU(cudaFuncSetAttribute(k_spmv<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    CU(cudaFuncSetAttribute(k_spmv_iter<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    CU(cudaFuncSetAttribute(k_init_x0<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    CU(cudaFuncSetAttribute(k_final<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    CU(cudaFuncSetAttribute(k_grad_A<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    CU(cudaFuncSetAttribute(k_spai_t<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    CU(cudaFuncSetAttribute(k_spai_z<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    done.store(1);
+    return SLA_OK;
+}
+
+template <typename T>
+static sla_status prepare_all() {
+    TRY((prepare_kernels<T, 1024>()));
+    TRY((prepare_kernels<T, 2048>()));
+    TRY((prepare_kernels<T, 4096>()));
+    return SLA_OK;
+}
+
+// CTAs per system for a kernel walking `units` work units (row blocks or
+// NT-element vector chunks), `per_sm` resident CTAs per SM.
+static int grid_x(const sla_csr* h, long long units, int per_sm) {
+    long long g = (long long)per_sm * h->sms / h->batch;
+    if (g < 1) g = 1;
+    if (g > units) g = units;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+static int per_sm_spmv(int tile) {
+    // 256 threads, 16*TILE bytes of staging: the smaller of the thread and
+    // shared-memory limits (228 KB per SM, 1 KB reserved per CTA).
+    const int by_smem = (int)((228 * 1024) / (smem_for(tile) + 2048));
+    const int by_threads = 2048 / NT;
+    return by_smem < by_threads ? by_smem : by_threads;
+}
+
+static int gx_spmv(const sla_csr* h, const RowBlocks& rb) { return grid_x(h, rb.nblk, per_sm_spmv(rb.tile)); }
+static int gx_vec(const sla_csr* h) { return grid_x(h, ((long long)h->n + NT - 1) / NT, 2048 / NT); }
+
+static Sys sys_of(sla_csr* h) {
+    Sys s;
+    s.n = h->n;
+    s.nnz = h->nnz;
+    s.st = h->state.as<State>();
+    s.ctl = h->ctl.as<Ctrl>();
+    s.cnt = h->cnt.as<unsigned>();
+    s.part = h->part.as<double>();
+    s.pstride = h->pstride;
+    return s;
+}
+
+static Mat mat_of(const int* rp, const int* ci, const RowBlocks& rb) {
+    Mat m;
+    m.rp = rp;
+    m.ci = ci;
+    m.rbs = rb.rbs.as<int>();
+    m.nblk = rb.nblk;
+    return m;
+}
+
+// ===================================================================== set-up helpers
+static sla_status scan_exclusive(int* d, long long m, cudaStream_t s) {
+    const long long nb = (m + SCAN_TILE - 1) / SCAN_TILE;
+    if (nb <= 1) {
+        k_scan_tile<<<1, SCAN_T, 0, s>>>(d, m, nullptr);
+        return launched();
+    }
+    DevBuf sums;
+    TRY(sums.alloc(sizeof(int) * (size_t)nb));
+    k_scan_tile<<<(unsigned)nb, SCAN_T, 0, s>>>(d, m, sums.as<int>());
+    TRY(launched());
+    TRY(scan_exclusive(sums.as<int>(), nb, s));
+    k_scan_add<<<(unsigned)nb, SCAN_T, 0, s>>>(d, m, sums.as<int>());
+    TRY(launched());
+    CU(cudaStreamSynchronize(s));
+    return SLA_OK;
+}
+
+static sla_status read_int(const int* d, int* out, cudaStream_t s) {
+    CU(cudaMemcpyAsync(out, d, sizeof(int), cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+    return SLA_OK;
+}
+
+static sla_status build_row_blocks(const int* rp, int n, int tile, RowBlocks& rb, cudaStream_t s) {
+    const int nch = (n + MAXR - 1) / MAXR;
+    DevBuf cnt;
+    TRY(cnt.alloc(sizeof(int) * (size_t)(nch + 1)));
+    const int g = (nch + 255) / 256;
+    k_rb_count<<<g, 256, 0, s>>>(rp, n, tile, cnt.as<int>());
+    TRY(launched());
+    CU(cudaMemsetAsync(cnt.as<int>() + nch, 0, sizeof(int), s));
+    TRY(scan_exclusive(cnt.as<int>(), nch + 1, s));
+    int total = 0;
+    TRY(read_int(cnt.as<int>() + nch, &total, s));
+    TRY(rb.rbs.alloc(sizeof(int) * (size_t)(total + 1)));
+    k_rb_fill<<<g, 256, 0, s>>>(rp, n, tile, cnt.as<int>(), rb.rbs.as<int>());
+    TRY(launched());
+    CU(cudaStreamSynchronize(s));
+    rb.nblk = total;
+    rb.tile = tile;
+    return SLA_OK;
+}
+
+static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
+    DevBuf err;
+    TRY(err.alloc(sizeof(int)));
+    CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
+    const int g = (h->n + 255) / 256 < 4096 ? (h->n + 255) / 256 : 4096;
+    if (h->dt == SLA_F64)
+        k_diag<double><<<g, 256, 0, s>>>(h->n, h->nnz, h->batch, h->rp, h->ci, (const double*)h->vals,
+                                         h->diag.as<double>(), err.as<int>());
+    else
+        k_diag<float><<<g, 256, 0, s>>>(h->n, h->nnz, h->batch, h->rp, h->ci, (const float*)h->vals,
+                                        h->diag.as<double>(), err.as<int>());
+    TRY(launched());
+    const size_t m = (size_t)h->batch * h->n;
+    k_recip<<<4096, 256, 0, s>>>(m, h->diag.as<double>(), h->dinv.as<double>());
+    TRY(launched());
+    TRY(read_int(err.as<int>(), &h->diag_err, s));
+    return SLA_OK;
+}
+
+static void release_spai(sla_csr* h) {
+    h->spai_ready = false;
+    h->grp.release(); h->gci.release(); h->gv.release();
+    h->gtrp.release(); h->gtci.release(); h->gtv.release();
+    h->G.rbs.release(); h->GT.rbs.release();
+    h->z.release(); h->t.release();
+    for (auto& g : h->graph) g.reset();
+}
+
+static sla_status ensure_pstride(sla_csr* h);
+
+static sla_status build_spai(sla_csr* h, cudaStream_t s) {
+    if (h->diag_err & ERR_NO_DIAG) return fail(SLA_ERR_INVALID, "SPAI needs every diagonal entry stored");
+    if (h->diag_err & ERR_DIAG_SIGN) return fail(SLA_ERR_INVALID, "SPAI needs a positive diagonal");
+    const int n = h->n;
+    TRY(h->grp.alloc(sizeof(int) * (size_t)(n + 1)));
+    TRY(h->gtrp.alloc(sizeof(int) * (size_t)(n + 1)));
+    const int g = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    k_tri_count<<<g, 256, 0, s>>>(n, h->rp, h->ci, h->grp.as<int>(), h->gtrp.as<int>());
+    TRY(launched());
+    CU(cudaMemsetAsync(h->grp.as<int>() + n, 0, sizeof(int), s));
+    CU(cudaMemsetAsync(h->gtrp.as<int>() + n, 0, sizeof(int), s));
+    TRY(scan_exclusive(h->grp.as<int>(), n + 1, s));
+    TRY(scan_exclusive(h->gtrp.as<int>(), n + 1, s));
+    int ng = 0, ngt = 0;
+    TRY(read_int(h->grp.as<int>() + n, &ng, s));
+    TRY(read_int(h->gtrp.as<int>() + n, &ngt, s));
+    if (ng != ngt) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
+    h->nnzg = ng;
+    TRY(h->gci.alloc(sizeof(int) * (size_t)ng));
+    TRY(h->gtci.alloc(sizeof(int) * (size_t)ng));
+    TRY(h->gv.alloc(sizeof(double) * (size_t)ng * h->batch));
+    TRY(h->gtv.alloc(sizeof(double) * (size_t)ng * h->batch));
+    DevBuf err;
+    TRY(err.alloc(sizeof(int)));
+    CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
+    for (int sy = 0; sy < h->batch; ++sy) {
+        const double* dg = h->diag.as<double>() + (size_t)sy * n;
+        double* gv = h->gv.as<double>() + (size_t)sy * ng;
+        double* gtv = h->gtv.as<double>() + (size_t)sy * ng;
+        if (h->dt == SLA_F64) {
+            const double* av = (const double*)h->vals + (size_t)sy * h->nnz;
+            k_fill_G<double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
+            TRY(launched());
+            k_fill_GT<double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(), gtv,
+                                                err.as<int>());
+        } else {
+            const float* av = (const float*)h->vals + (size_t)sy * h->nnz;
+            k_fill_G<float><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
+            TRY(launched());
+            k_fill_GT<float><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(), gtv,
+                                               err.as<int>());
+        }
+        TRY(launched());
+    }
+    int e = 0;
+    TRY(read_int(err.as<int>(), &e, s));
+    if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
+    const int tile = pick_tile(ng, n);
+    TRY(build_row_blocks(h->grp.as<int>(), n, tile, h->G, s));
+    TRY(build_row_blocks(h->gtrp.as<int>(), n, tile, h->GT, s));
+    TRY(h->z.alloc(h->es * (size_t)n * h->batch));
+    TRY(h->t.alloc(h->es * (size_t)n * h->batch));
+    h->spai_ready = true;
+    return ensure_pstride(h);
+}
+
+static sla_status ensure_pstride(sla_csr* h) {
+    int m = gx_vec(h);
+    m = m > gx_spmv(h, h->A) ? m : gx_spmv(h, h->A);
+    if (h->spai_ready) {
+        m = m > gx_spmv(h, h->G) ? m : gx_spmv(h, h->G);
+        m = m > gx_spmv(h, h->GT) ? m : gx_spmv(h, h->GT);
+    }
+    const int need = 2 * m;
+    if (need <= h->pstride) return SLA_OK;
+    TRY(h->part.alloc(sizeof(double) * (size_t)need * h->batch));
+    h->pstride = need;
+    for (auto& g : h->graph) g.reset();
+    return SLA_OK;
+}
+
+// ===================================================================== kernels per iteration
+template <typename T, int TA, int TG>
+static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
+    const Sys S = sys_of(h);
+    const Mat A = mat_of(h->rp, h->ci, h->A);
+    const T* av = (const T*)h->vals;
+    T* r = h->r.as<T>();
+    T* p = h->p.as<T>();
+    T* q = h->q.as<T>();
+    double* x = h->x.as<double>();
+    const double* dinv = h->dinv.as<double>();
+    const dim3 gs(gx_spmv(h, h->A), h->batch), gv(gx_vec(h), h->batch);
+    k_spmv_iter<T, TA><<<gs, NT, smem_for(TA), s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    TRY(launched());
+    if (pc == SLA_PC_SPAI) {
+        k_update<T, 2><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        TRY(launched());
+        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->GT);
+        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->G);
+        k_spai_t<T, TG><<<dim3(gx_spmv(h, h->GT), h->batch), NT, smem_for(TG), s>>>(GT, S, h->nnzg,
+                                                                                    h->gtv.as<double>(), r,
+                                                                                    h->t.as<T>());
+        TRY(launched());
+        k_spai_z<T, TG><<<dim3(gx_spmv(h, h->G), h->batch), NT, smem_for(TG), s>>>(
+            G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+        TRY(launched());
+        k_pupdate<T, 2, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
+        TRY(launched());
+        *nodes += 5;
+    } else if (pc == SLA_PC_JACOBI) {
+        k_update<T, 1><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        TRY(launched());
+        k_pupdate<T, 1, false><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
+        TRY(launched());
+        *nodes += 3;
+    } else {
+        k_update<T, 0><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        TRY(launched());
+        k_pupdate<T, 0, false><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
+        TRY(launched());
+        *nodes += 3;
+    }
+    return SLA_OK;
+}
+
+template <typename T>
+static sla_status enqueue_iteration_any(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
+    sla_status st = SLA_OK;
+    const int tg = h->spai_ready ? h->G.tile : 1024;
+    with_tile(h->A.tile, [&](auto ta) {
+        with_tile(tg, [&](auto tgc) { st = enqueue_iteration<T, decltype(ta)::value, decltype(tgc)::value>(h, pc, eps, s, nodes); });
+    });
+    return st;
+}
+
+template <typename T>
+static sla_status get_graph(sla_csr* h, int pc, double eps, int k, GraphCache** out) {
+    GraphCache& gc = h->graph[pc];
+    if (gc.exec && gc.k == k && gc.eps == eps) { *out = &gc; return SLA_OK; }
+    gc.reset();
+    CU(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
+    int nodes = 0;
+    sla_status st = SLA_OK;
+    for (int i = 0; i < k && st == SLA_OK; ++i) st = enqueue_iteration_any<T>(h, pc, eps, h->cap, &nodes);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
+    // launches made during capture were counted; they only run when the graph does
+    g_launches.fetch_sub((unsigned long long)nodes, std::memory_order_relaxed);
+    if (st != SLA_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&gc.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        gc.exec = nullptr;
+        return fail(SLA_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+    }
+    gc.k = k;
+    gc.eps = eps;
+    gc.nodes = nodes;
+    *out = &gc;
+    return SLA_OK;
+}
+
+// ===================================================================== solve driver
+static sla_status from_code(int c) {
+    switch (c) {
+        case ST_OK: return SLA_OK;
+        case ST_NOT_CONVERGED: return SLA_ERR_NOT_CONVERGED;
+        default: return SLA_ERR_BREAKDOWN;
+    }
+}
+
+template <typename T>
+static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_opts* o, sla_solve_info* info,
+                             cudaStream_t s) {
+    const int pc = (int)o->pc;
+    if (pc == SLA_PC_JACOBI && (h->diag_err & ERR_NO_DIAG))
+        return fail(SLA_ERR_INVALID, "Jacobi needs every diagonal entry stored");
+    if (pc == SLA_PC_SPAI && !h->spai_ready) TRY(build_spai(h, s));
+    TRY(ensure_pstride(h));
+    const int k = o->poll_k > 0 ? o->poll_k : 32;
+    const double eps = pc == SLA_PC_SPAI ? o->eps : 0.0;
+    GraphCache* gc = nullptr;
+    TRY(get_graph<T>(h, pc, eps, k, &gc));
+
+    const Sys S = sys_of(h);
+    const Mat A = mat_of(h->rp, h->ci, h->A);
+    const T* av = (const T*)h->vals;
+    const dim3 gs(gx_spmv(h, h->A), h->batch), gv(gx_vec(h), h->batch);
+    T* r = h->r.as<T>();
+    T* p = h->p.as<T>();
+    double* x = h->x.as<double>();
+    const double* dinv = h->dinv.as<double>();
+
+    CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
+    if (o->use_x0) {
+        with_tile(h->A.tile, [&](auto ta) {
+            constexpr int TA = decltype(ta)::value;
+            k_init_x0<T, TA><<<gs, NT, smem_for(TA), s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
+                                                          o->max_iter);
+        });
+    } else {
+        k_init<T><<<gv, NT, 0, s>>>(S, b, h->bw.as<T>(), x, r, o->tol, o->max_iter);
+    }
+    TRY(launched());
+    if (pc == SLA_PC_SPAI) {
+        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->GT);
+        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->G);
+        sla_status st = SLA_OK;
+        with_tile(h->G.tile, [&](auto tg) {
+            constexpr int TG = decltype(tg)::value;
+            k_spai_t<T, TG><<<dim3(gx_spmv(h, h->GT), h->batch), NT, smem_for(TG), s>>>(GT, S, h->nnzg,
+                                                                                        h->gtv.as<double>(), r,
+                                                                                        h->t.as<T>());
+            st = launched();
+            if (st != SLA_OK) return;
+            k_spai_z<T, TG><<<dim3(gx_spmv(h, h->G), h->batch), NT, smem_for(TG), s>>>(
+                G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+            st = launched();
+        });
+        TRY(st);
+        k_pupdate<T, 2, true><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
+    } else if (pc == SLA_PC_JACOBI) {
+        k_init_dir<T, 1><<<gv, NT, 0, s>>>(S, p, r, dinv);
+    } else {
+        k_init_dir<T, 0><<<gv, NT, 0, s>>>(S, p, r, dinv);
+    }
+    TRY(launched());
+
+    // iterate: graph launches of k iterations, two in flight, poll the flag
+    const auto t0 = std::chrono::steady_clock::now();
+    const long long cap_launches = ((long long)o->max_iter + 2LL * k + 2) / k + 2;
+    int head = 0, inflight = 0;
+    long long issued = 0;
+    bool finished = false, timed_out = false;
+    while (!finished) {
+        if (issued < cap_launches && !timed_out) {
+            const int slot = (head + inflight) & 1;
+            CU(cudaGraphLaunch(gc->exec, s));
+            g_launches.fetch_add((unsigned long long)gc->nodes, std::memory_order_relaxed);
+            CU(cudaMemcpyAsync(&h->h_flag[slot], &h->ctl.as<Ctrl>()->all_done, sizeof(int),
+                               cudaMemcpyDeviceToHost, s));
+            CU(cudaEventRecord(h->ev[slot], s));
+            ++inflight;
+            ++issued;
+            if (inflight < 2) continue;
+        }
+        if (inflight == 0) break;
+        // wait for the oldest launch
+        const int slot = head;
+        if (o->timeout_s > 0) {
+            for (;;) {
+                cudaError_t q = cudaEventQuery(h->ev[slot]);
+                if (q == cudaSuccess) break;
+                if (q != cudaErrorNotReady) return fail(SLA_ERR_CUDA, "event query: %s", cudaGetErrorString(q));
+                const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+                if (el > o->timeout_s) timed_out = true;
+                std::this_thread::sleep_for(std::chrono::microseconds(50));
+            }
+        } else {
+            CU(cudaEventSynchronize(h->ev[slot]));
+        }
+        head ^= 1;
+        --inflight;
+        if (h->h_flag[slot]) finished = true;
+        if ((issued >= cap_launches || timed_out) && inflight == 0) break;
+    }
+    // drain (kernels of a finished batch return at once)
+    CU(cudaStreamSynchronize(s));
+
+    with_tile(h->A.tile, [&](auto ta) {
+        constexpr int TA = decltype(ta)::value;
+        k_final<T, TA><<<gs, NT, smem_for(TA), s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
+    });
+    TRY(launched());
+    CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+
+    sla_status ret = SLA_OK;
+    for (int i = 0; i < h->batch; ++i) {
+        const Stat& st = h->h_stat[i];
+        sla_status si = from_code(st.status);
+        if (!st.done) si = timed_out ? SLA_ERR_TIMEOUT : SLA_ERR_NOT_CONVERGED;  // host stopped first
+        if (info) {
+            info[i].iters = st.iters;
+            info[i].rel_res_recursive = st.rel_rec;
+            info[i].rel_res_true = st.rel_true;
+            info[i].status = si;
+        }
+        if (ret == SLA_OK && si != SLA_OK) ret = si;
+    }
+    if (!finished && !timed_out)
+        return fail(SLA_ERR_NOT_CONVERGED, "iteration launches exhausted before the device froze");
+    if (ret == SLA_ERR_TIMEOUT) return fail(ret, "timeout after %.3f s", o->timeout_s);
+    if (ret != SLA_OK) fail(ret, ret == SLA_ERR_BREAKDOWN ? "breakdown (p.Ap <= 0, r.z <= 0 or non-finite value)"
+                                                          : "not converged within max_iter");
+    return ret;
+}
+
+// ===================================================================== C ABI
+extern "C" {
+
+void sla_pcg_opts_default(sla_pcg_opts* o) {
+    if (!o) return;
+    o->tol = 1e-8;
+    o->max_iter = 10000;
+    o->pc = SLA_PC_NONE;
+    o->eps = 1e-3;
+    o->poll_k = 32;
+    o->use_x0 = 0;
+    o->timeout_s = 0.0;
+}
+
+const char* sla_last_error(void) { return g_err.c_str(); }
+
+unsigned long long sla_launch_count(void) { return g_launches.load(); }
+
+static void destroy_handle(sla_csr* h) {
+    if (!h) return;
+    for (auto& g : h->graph) g.reset();
+    if (h->cap) cudaStreamDestroy(h->cap);
+    for (auto& e : h->ev) if (e) cudaEventDestroy(e);
+    if (h->h_flag) cudaFreeHost(h->h_flag);
+    if (h->h_stat) cudaFreeHost(h->h_stat);
+    delete h;  // DevBuf members free themselves below via release()
+}
+
+sla_status sla_csr_destroy(sla_handle h) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    DevBuf* bufs[] = {&h->A.rbs, &h->diag, &h->dinv, &h->grp, &h->gci, &h->gv, &h->gtrp, &h->gtci, &h->gtv,
+                      &h->G.rbs, &h->GT.rbs, &h->x, &h->r, &h->p, &h->q, &h->z, &h->t, &h->bw, &h->state,
+                      &h->ctl, &h->cnt, &h->part, &h->stat};
+    for (DevBuf* b : bufs) b->release();
+    destroy_handle(h);
+    return SLA_OK;
+}
+
+sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const int* d_row_ptr,
+                          const int* d_col_idx, const void* d_vals, unsigned flags, void* stream,
+                          sla_handle* out) {
+    if (!out) return fail(SLA_ERR_INVALID, "out is null");
+    *out = nullptr;
+    if (n < 1) return fail(SLA_ERR_INVALID, "n must be >= 1 (got %d)", n);
+    if (nnz < 0 || nnz > 2147483647LL) return fail(SLA_ERR_INVALID, "nnz must be in [0, 2^31) (got %lld)", nnz);
+    if (batch < 1) return fail(SLA_ERR_INVALID, "batch must be >= 1 (got %d)", batch);
+    if (dt != SLA_F64 && dt != SLA_F32) return fail(SLA_ERR_INVALID, "unknown dtype %d", (int)dt);
+    if (!d_row_ptr || (nnz > 0 && (!d_col_idx || !d_vals))) return fail(SLA_ERR_INVALID, "null CSR pointer");
+    cudaStream_t s = (cudaStream_t)stream;
+
+    sla_csr* h = new sla_csr();
+    h->n = n;
+    h->nnz = nnz;
+    h->batch = batch;
+    h->dt = dt;
+    h->es = dt == SLA_F64 ? 8 : 4;
+    h->rp = d_row_ptr;
+    h->ci = d_col_idx;
+    h->vals = d_vals;
+    auto bail = [&](sla_status st) {
+        std::string msg = g_err;
+        sla_csr_destroy(h);
+        g_err = msg;
+        return st;
+    };
+#define HTRY(expr)                                 \
+    do {                                           \
+        sla_status s_ = (expr);                    \
+        if (s_ != SLA_OK) return bail(s_);         \
+    } while (0)
+#define HCU(call)                                                                                   \
+    do {                                                                                            \
+        cudaError_t e_ = (call);                                                                    \
+        if (e_ != cudaSuccess)                                                                      \
+            return bail(fail(SLA_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_)));       \
+    } while (0)
+
+    HCU(cudaGetDevice(&h->device));
+    HCU(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device));
+    HTRY(dt == SLA_F64 ? prepare_all<double>() : prepare_all<float>());
+    HCU(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
+    HCU(cudaEventCreateWithFlags(&h->ev[0], cudaEventDisableTiming));
+    HCU(cudaEventCreateWithFlags(&h->ev[1], cudaEventDisableTiming));
+    HCU(cudaHostAlloc((void**)&h->h_flag, 2 * sizeof(int), cudaHostAllocDefault));
+    HCU(cudaHostAlloc((void**)&h->h_stat, sizeof(Stat) * batch, cudaHostAllocDefault));
+    h->h_flag[0] = h->h_flag[1] = 0;
+
+    if (flags & SLA_VALIDATE) {
+        DevBuf err;
+        HTRY(err.alloc(sizeof(int)));
+        HCU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
+        const int g = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+        k_validate<<<g, 256, 0, s>>>(n, nnz, d_row_ptr, d_col_idx, err.as<int>());
+        HTRY(launched());
+        int e = 0;
+        HTRY(read_int(err.as<int>(), &e, s));
+        if (e)
+            return bail(fail(SLA_ERR_INVALID, "malformed CSR:%s%s%s", (e & ERR_ROWPTR) ? " row_ptr" : "",
+                             (e & ERR_COL_RANGE) ? " column out of range" : "",
+                             (e & ERR_COL_ORDER) ? " columns not strictly ascending" : ""));
+    }
+    HTRY(build_row_blocks(d_row_ptr, n, pick_tile(nnz, n), h->A, s));
+    const size_t vn = (size_t)n * batch;
+    HTRY(h->diag.alloc(sizeof(double) * vn));
+    HTRY(h->dinv.alloc(sizeof(double) * vn));
+    HTRY(compute_diag(h, s));
+    HTRY(h->x.alloc(sizeof(double) * vn));
+    HTRY(h->r.alloc(h->es * vn));
+    HTRY(h->p.alloc(h->es * vn));
+    HTRY(h->q.alloc(h->es * vn));
+    HTRY(h->bw.alloc(h->es * vn));
+    HTRY(h->state.alloc(sizeof(State) * batch));
+    HTRY(h->ctl.alloc(sizeof(Ctrl)));
+    HTRY(h->cnt.alloc(sizeof(unsigned) * batch));
+    HTRY(h->stat.alloc(sizeof(Stat) * batch));
+    HCU(cudaMemsetAsync(h->cnt.p, 0, sizeof(unsigned) * batch, s));
+    HCU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
+    HCU(cudaMemsetAsync(h->state.p, 0, sizeof(State) * batch, s));
+    HTRY(ensure_pstride(h));
+    HCU(cudaStreamSynchronize(s));
+#undef HTRY
+#undef HCU
+    *out = h;
+    return SLA_OK;
+}
+
+sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (!d_vals && h->nnz > 0) return fail(SLA_ERR_INVALID, "null values");
+    cudaStream_t s = (cudaStream_t)stream;
+    h->vals = d_vals;
+    release_spai(h);     // rebuilt on the next SPAI solve
+    for (auto& g : h->graph) g.reset();
+    TRY(compute_diag(h, s));
+    CU(cudaStreamSynchronize(s));
+    return SLA_OK;
+}
+
+static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* d_dot, void* stream) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (!d_x || !d_y) return fail(SLA_ERR_INVALID, "null vector");
+    cudaStream_t s = (cudaStream_t)stream;
+    const Sys S = sys_of(h);
+    const Mat A = mat_of(h->rp, h->ci, h->A);
+    const dim3 g(gx_spmv(h, h->A), h->batch);
+    with_tile(h->A.tile, [&](auto ta) {
+        constexpr int TA = decltype(ta)::value;
+        if (h->dt == SLA_F64)
+            k_spmv<double, TA><<<g, NT, smem_for(TA), s>>>(A, S, (const double*)h->vals, (const double*)d_x,
+                                                           (double*)d_y, d_dot);
+        else
+            k_spmv<float, TA><<<g, NT, smem_for(TA), s>>>(A, S, (const float*)h->vals, (const float*)d_x,
+                                                          (float*)d_y, d_dot);
+    });
+    return launched();
+}
+
+sla_status sla_spmv(sla_handle h, const void* d_x, void* d_y, void* stream) {
+    return spmv_common(h, d_x, d_y, nullptr, stream);
+}
+
+sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot, void* stream) {
+    if (!d_dot) return fail(SLA_ERR_INVALID, "null dot");
+    return spmv_common(h, d_x, d_y, d_dot, stream);
+}
+
+static sla_status check_opts(const sla_pcg_opts* o) {
+    if (!o) return fail(SLA_ERR_INVALID, "null options");
+    if (!(o->tol > 0.0)) return fail(SLA_ERR_INVALID, "tol must be > 0");
+    if (o->max_iter < 0) return fail(SLA_ERR_INVALID, "max_iter must be >= 0");
+    if (o->pc != SLA_PC_NONE && o->pc != SLA_PC_JACOBI && o->pc != SLA_PC_SPAI)
+        return fail(SLA_ERR_INVALID, "unknown preconditioner %d", (int)o->pc);
+    if (o->pc == SLA_PC_SPAI && !(o->eps >= 0.0)) return fail(SLA_ERR_INVALID, "eps must be >= 0");
+    if (o->poll_k < 0) return fail(SLA_ERR_INVALID, "poll_k must be >= 0");
+    return SLA_OK;
+}
+
+sla_status sla_pcg_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg_opts* opts,
+                         sla_solve_info* info, void* stream) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (!d_b || !d_x) return fail(SLA_ERR_INVALID, "null vector");
+    TRY(check_opts(opts));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (h->dt == SLA_F64) return solve_impl<double>(h, (const double*)d_b, (double*)d_x, opts, info, s);
+    return solve_impl<float>(h, (const float*)d_b, (float*)d_x, opts, info, s);
+}
+
+sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla_pcg_opts* opts, void* d_dLdb,
+                       void* d_dLdA, sla_solve_info* info, void* stream) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (!d_x || !d_g || !d_dLdb) return fail(SLA_ERR_INVALID, "null vector");
+    TRY(check_opts(opts));
+    cudaStream_t s = (cudaStream_t)stream;
+    sla_pcg_opts o = *opts;
+    o.use_x0 = 0;
+    sla_status st = h->dt == SLA_F64
+                        ? solve_impl<double>(h, (const double*)d_g, (double*)d_dLdb, &o, info, s)
+                        : solve_impl<float>(h, (const float*)d_g, (float*)d_dLdb, &o, info, s);
+    if (st != SLA_OK && st != SLA_ERR_NOT_CONVERGED && st != SLA_ERR_BREAKDOWN && st != SLA_ERR_TIMEOUT) return st;
+    if (d_dLdA && h->nnz > 0) {
+        const Sys S = sys_of(h);
+        const Mat A = mat_of(h->rp, h->ci, h->A);
+        const dim3 g(gx_spmv(h, h->A), h->batch);
+        with_tile(h->A.tile, [&](auto ta) {
+            constexpr int TA = decltype(ta)::value;
+            if (h->dt == SLA_F64)
+                k_grad_A<double, TA><<<g, NT, TA * sizeof(int), s>>>(A, S, (const double*)d_dLdb,
+                                                                     (const double*)d_x, (double*)d_dLdA);
+            else
+                k_grad_A<float, TA><<<g, NT, TA * sizeof(int), s>>>(A, S, (const float*)d_dLdb,
+                                                                    (const float*)d_x, (float*)d_dLdA);
+        });
+        sla_status l = launched();
+        if (l != SLA_OK) return l;
+        CU(cudaStreamSynchronize(s));
+    }
+    return st;
+}
+
+}  // extern "C"

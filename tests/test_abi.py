@@ -1,0 +1,70 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports
+every function include/sla.h declares.  No compute call is made here."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_iterative_linear_csr_b300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ["sla_csr_create", "sla_spmv", "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy",
+              "sla_last_error"]:
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from sparse_iterative_linear_csr_b300 import _lib
+    names = declared_functions()
+    assert sorted(_lib.EXPORTS) == names
+    for f in names:
+        assert hasattr(lib, f), f
+
+
+def test_host_only_calls(lib):
+    from sparse_iterative_linear_csr_b300 import _lib
+    o = _lib.PcgOpts()
+    lib.sla_pcg_opts_default(C.byref(o))
+    assert o.tol == 1e-8 and o.max_iter == 10000 and o.poll_k == 32 and o.pc == 0
+    # argument checks fail before any CUDA call
+    h = C.c_void_p()
+    st = lib.sla_csr_create(0, 0, 1, 0, None, None, None, 0, None, C.byref(h))
+    assert st == _lib.SLA_ERR_INVALID
+    assert b"n must be" in lib.sla_last_error()
+    assert lib.sla_pcg_solve(None, None, None, C.byref(o), None, None) == _lib.SLA_ERR_INVALID
+    assert lib.sla_csr_destroy(None) == _lib.SLA_ERR_INVALID
+
+
+def test_struct_layouts_match_header():
+    from sparse_iterative_linear_csr_b300 import _lib
+    assert C.sizeof(_lib.PcgOpts) == 40
+    assert _lib.PcgOpts.timeout_s.offset == 32
+    assert C.sizeof(_lib.SolveInfo) == 32
+    assert _lib.SolveInfo.status.offset == 24
+
+
+def test_no_oracle_in_product_package():
+    pkg = os.path.join(ROOT, "sparse_iterative_linear_csr_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "oracle.c" not in src, f

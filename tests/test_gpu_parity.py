@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle
+on the same seeded inputs, element by element, at sizes the oracle finishes
+in seconds (several row blocks and a ragged tail), plus edge cases.
+
+Tolerances: SpMV relative error <= 1e-12 (fp64) and <= 1e-5 (fp32);
+||x - x_oracle|| / ||x_oracle|| <= 1e-6; iteration count within 2% of the
+oracle's (at least +-1); true residual of the returned x <= tol."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import build
+from workloads.matrices import CSR, poisson_grid
+
+from gpu_util import make, random_csr, rel
+
+pytestmark = pytest.mark.gpu
+
+SPMV_TOL = {np.float64: 1e-12, np.float32: 1e-5}
+
+
+def _iters_ok(a, b):
+    return abs(a - b) <= max(1, int(0.02 * b))
+
+
+def _spmv_cases():
+    yield "poisson2d_64", poisson_grid((64, 64))
+    yield "poisson3d_24", poisson_grid((24, 24, 24))
+    yield "diffusion_96", build("c2", N=96).A
+    yield "knn_3000", build("c5", npoints=3000).A
+    for n in (1, 2, 31, 33, 257, 1000):
+        yield f"random_{n}", random_csr(n, 6, seed=n)
+    yield "empty_rows", random_csr(500, 4, seed=7, empty_rows=40)
+    # one row far longer than a staging tile, plus short rows around it
+    n = 12001
+    cols = [np.arange(n)] + [np.array([i]) for i in range(1, n)]
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum([c.size for c in cols])
+    g = np.random.default_rng(3)
+    yield "dense_row", CSR(n, rp, np.concatenate(cols).astype(np.int32), g.standard_normal(int(rp[-1])))
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("name,A", list(_spmv_cases()), ids=lambda v: v if isinstance(v, str) else "")
+def test_spmv_parity(cuda_device, name, A, dtype):
+    A = CSR(A.n, A.row_ptr, A.col_idx, A.vals.astype(dtype))
+    x = np.random.default_rng(11).standard_normal(A.n).astype(dtype)
+    M = make(A)
+    xd = torch.from_numpy(x).to(cuda_device)
+    y = M.matvec(xd).cpu().numpy()
+    y_o = oracle.spmv(A, x.astype(np.float64))
+    scale = oracle.spmv(CSR(A.n, A.row_ptr, A.col_idx, np.abs(A.vals)), np.abs(x.astype(np.float64)))
+    tol = SPMV_TOL[dtype]
+    assert np.all(np.abs(y - y_o) <= tol * np.maximum(scale, 1e-300) + (0 if dtype == np.float64 else 1e-30))
+    yd, dot = M.matvec_dot(xd)
+    assert np.array_equal(yd.cpu().numpy(), y)
+    d_o = float(x.astype(np.float64) @ y.astype(np.float64))
+    assert abs(dot.item() - d_o) <= 1e-12 * max(1.0, float(np.abs(x) @ np.abs(y)))
+
+
+def test_spmv_batched(cuda_device):
+    w = build("c3", N=40, batch=3)
+    M = make(w.A)
+    x = torch.from_numpy(w.b).to(cuda_device)
+    y = M.matvec(x).cpu().numpy()
+    for s in range(3):
+        y_o = oracle.spmv(w.A, w.b[s].astype(np.float64), system=s)
+        assert rel(y[s], y_o) <= 1e-6
+    _, dots = M.matvec_dot(x)
+    for s in range(3):
+        assert abs(dots[s].item() - float(w.b[s].astype(np.float64) @ y[s].astype(np.float64))) <= 1e-9
+
+
+SOLVE_CASES = [
+    ("c1", {}, "none"),
+    ("c2", {"N": 96}, "jacobi"),
+    ("c3", {"N": 48, "batch": 5}, "jacobi"),
+    ("c4", {"N": 24}, "none"),
+    ("c5", {"npoints": 20000}, "spai"),
+    ("c5", {"npoints": 20000}, "jacobi"),
+    ("c2", {"N": 64}, "spai"),
+    ("c3", {"N": 32, "batch": 3}, "spai"),
+]
+
+
+@pytest.mark.parametrize("cfg,kw,pc", SOLVE_CASES, ids=[f"{c}-{p}-{k}" for c, k, p in SOLVE_CASES])
+def test_pcg_parity(cuda_device, cfg, kw, pc):
+    w = build(cfg, **kw)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    x, info = M.solve(b, tol=w.tol, max_iter=20000, pc=pc, eps=1e-3, poll_k=16)
+    x = x.cpu().numpy()
+    xo, io = oracle.pcg(w.A, w.b, w.tol, max_iter=20000, pc=pc, eps=1e-3)
+    if M.batch == 1 and w.A.vals.ndim == 1:
+        x, xo, info, io = x[None], xo[None], info, [io]
+    for s in range(len(info)):
+        assert info[s].status == "ok" and io[s]["status"] == "ok"
+        assert _iters_ok(info[s].iters, io[s]["iters"]), (info[s].iters, io[s]["iters"])
+        assert rel(x[s], xo[s]) <= 1e-6
+        assert info[s].rel_res_true <= w.tol
+        # the reported true residual is the residual of the returned x
+        assert abs(oracle.rel_residual(w.A, w.b[s], x[s], system=s) - info[s].rel_res_true) <= 1e-3 * w.tol
+
+
+ADJ_CASES = [("c4", {"N": 24}, "none"), ("c2", {"N": 64}, "jacobi"), ("c5", {"npoints": 20000}, "spai"),
+             ("c3", {"N": 32, "batch": 3}, "jacobi")]
+
+
+@pytest.mark.parametrize("cfg,kw,pc", ADJ_CASES, ids=[f"{c}-{p}" for c, k, p in ADJ_CASES])
+def test_adjoint_parity(cuda_device, cfg, kw, pc):
+    w = build(cfg, **kw)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    g = torch.from_numpy(w.g).to(cuda_device)
+    x, _ = M.solve(b, tol=w.tol, max_iter=20000, pc=pc)
+    dldb, dlda, info = M.adjoint(x, g, tol=w.tol, max_iter=20000, pc=pc)
+    xh = x.cpu().numpy()
+    lb_o, la_o, io = oracle.adjoint(w.A, xh, w.g, w.tol, max_iter=20000, pc=pc, eps=1e-3)
+    lb, la = dldb.cpu().numpy(), dlda.cpu().numpy()
+    if lb.ndim == 1:
+        lb, la, lb_o, la_o, io = lb[None], la[None], lb_o[None], la_o[None], [io]
+    for s in range(lb.shape[0]):
+        assert info[s].status == "ok" and _iters_ok(info[s].iters, io[s]["iters"])
+        assert rel(lb[s], lb_o[s]) <= 1e-6
+        assert rel(la[s], la_o[s]) <= 1e-6
+        # dA is exactly -lambda_i x_j of the returned lambda and x
+        rows = w.A.rows()
+        exact = (-lb[s][rows].astype(np.float64) * xh[s if xh.ndim == 2 else slice(None)][w.A.col_idx]
+                 .astype(np.float64)).astype(la.dtype)
+        assert np.array_equal(la[s], exact)
+
+
+def test_autograd_wrapper(cuda_device):
+    from sparse_iterative_linear_csr_b300 import solve
+    w = build("c2", N=48)
+    M = make(w.A)
+    vals = M.values.clone().requires_grad_(True)
+    b = torch.from_numpy(w.b).to(cuda_device).requires_grad_(True)
+    g = torch.from_numpy(w.g).to(cuda_device)
+    x = solve(M, vals, b, tol=1e-12, pc="jacobi", max_iter=20000)
+    (x * g).sum().backward()
+    xo, _ = oracle.pcg(w.A, w.b, 1e-12, pc="jacobi")
+    lb_o, la_o, _ = oracle.adjoint(w.A, xo, w.g, 1e-12, pc="jacobi")
+    assert rel(x.detach().cpu().numpy(), xo) <= 1e-9
+    assert rel(b.grad.cpu().numpy(), lb_o) <= 1e-9
+    assert rel(vals.grad.cpu().numpy(), la_o) <= 1e-9
+
+
+# ------------------------------------------------------------------ edge cases
+def test_zero_rhs(cuda_device):
+    w = build("c1")
+    M = make(w.A)
+    x, info = M.solve(torch.zeros(w.A.n, dtype=torch.float64, device=cuda_device), tol=1e-8)
+    assert info[0].iters == 0 and info[0].status == "ok" and not x.abs().sum().item()
+    # also with an initial guess
+    x, info = M.solve(torch.zeros(w.A.n, dtype=torch.float64, device=cuda_device), tol=1e-8,
+                      x0=torch.ones(w.A.n, dtype=torch.float64, device=cuda_device))
+    assert info[0].iters == 0 and not x.abs().sum().item()
+
+
+@pytest.mark.parametrize("max_iter", [0, 1, 2, 37])
+def test_max_iter_reached(cuda_device, max_iter):
+    w = build("c2", N=40)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    x, info = M.solve(b, tol=1e-12, max_iter=max_iter, pc="jacobi", poll_k=8)
+    xo, io = oracle.pcg(w.A, w.b, 1e-12, max_iter=max_iter, pc="jacobi")
+    assert info[0].status == "not_converged" == io["status"]
+    assert info[0].iters == io["iters"] == max_iter
+    assert rel(x.cpu().numpy(), xo) <= 1e-9
+
+
+def test_breakdown_nan_and_indefinite(cuda_device):
+    w = build("c1")
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device).clone()
+    b[17] = float("nan")
+    _, info = M.solve(b, tol=1e-8)
+    assert info[0].status == "breakdown"
+    D = CSR(3, np.array([0, 1, 2, 3], np.int32), np.array([0, 1, 2], np.int32), np.array([1.0, -1.0, 2.0]))
+    M2 = make(D)
+    _, info = M2.solve(torch.ones(3, dtype=torch.float64, device=cuda_device), tol=1e-8)
+    assert info[0].status == "breakdown" == oracle.pcg(D, np.ones(3), 1e-8)[1]["status"]
+
+
+def test_initial_guess_parity(cuda_device):
+    w = build("c2", N=64)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    x0 = np.random.default_rng(1).standard_normal(w.A.n)
+    x, info = M.solve(b, tol=1e-9, pc="jacobi", x0=torch.from_numpy(x0).to(cuda_device))
+    xo, io = oracle.pcg(w.A, w.b, 1e-9, pc="jacobi", x0=x0)
+    assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
+
+
+def test_invalid_inputs_rejected(cuda_device):
+    from sparse_iterative_linear_csr_b300 import CSRMatrix, SLAError
+    dev = cuda_device
+    rp = torch.tensor([0, 2, 1, 3], dtype=torch.int32, device=dev)       # decreasing row_ptr
+    ci = torch.tensor([0, 1, 2], dtype=torch.int32, device=dev)
+    v = torch.ones(3, dtype=torch.float64, device=dev)
+    with pytest.raises(SLAError, match="row_ptr"):
+        CSRMatrix(rp, ci, v)
+    rp = torch.tensor([0, 2, 3, 3], dtype=torch.int32, device=dev)
+    with pytest.raises(SLAError, match="ascending"):
+        CSRMatrix(rp, torch.tensor([1, 0, 2], dtype=torch.int32, device=dev), v)
+    with pytest.raises(SLAError, match="range"):
+        CSRMatrix(rp, torch.tensor([0, 5, 2], dtype=torch.int32, device=dev), v)
+    # missing diagonal: fine for plain CG set-up, rejected for Jacobi / SPAI
+    M = CSRMatrix(torch.tensor([0, 1, 2], dtype=torch.int32, device=dev),
+                  torch.tensor([1, 0], dtype=torch.int32, device=dev), torch.ones(2, dtype=torch.float64,
+                                                                                  device=dev))
+    b = torch.ones(2, dtype=torch.float64, device=dev)
+    for pc in ("jacobi", "spai"):
+        with pytest.raises(SLAError, match="diagonal"):
+            M.solve(b, pc=pc)
+    with pytest.raises(SLAError, match="tol"):
+        M.solve(b, tol=0.0)
+
+
+def test_spai_rejects_unsymmetric_pattern(cuda_device):
+    from sparse_iterative_linear_csr_b300 import SLAError
+    A = CSR(3, np.array([0, 2, 3, 4], np.int32), np.array([0, 2, 1, 2], np.int32), np.array([2.0, -1, 2, 2]))
+    M = make(A)
+    with pytest.raises(SLAError, match="symmetric"):
+        M.solve(torch.ones(3, dtype=torch.float64, device=cuda_device), pc="spai")
+
+
+def test_timeout_reports_and_keeps_iterate(cuda_device):
+    w = build("c4", N=48)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    x, info = M.solve(b, tol=1e-14, max_iter=100000, poll_k=1, timeout_s=1e-4)
+    assert info[0].status in ("timeout", "ok")
+    assert info[0].status == "timeout" and info[0].iters < 100000
+    assert np.isfinite(x.cpu().numpy()).all()
+
+
+def test_repeat_solves_are_deterministic(cuda_device):
+    w = build("c5", npoints=20000)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    x1, i1 = M.solve(b, tol=1e-8, pc="spai")
+    x2, i2 = M.solve(b, tol=1e-8, pc="spai", poll_k=7)
+    assert i1[0].iters == i2[0].iters and torch.equal(x1, x2)
+
+
+def test_update_values(cuda_device):
+    w = build("c2", N=48)
+    M = make(w.A)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    v2 = M.values * 2.0
+    M.update_values(v2)
+    x, info = M.solve(b, tol=1e-10, pc="spai")
+    A2 = CSR(w.A.n, w.A.row_ptr, w.A.col_idx, w.A.vals * 2.0)
+    xo, io = oracle.pcg(A2, w.b, 1e-10, pc="spai", eps=1e-3)
+    assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
+
+
+def test_launch_count_advances(cuda_device):
+    from sparse_iterative_linear_csr_b300 import launch_count
+    w = build("c1")
+    M = make(w.A)
+    c0 = launch_count()
+    M.solve(torch.from_numpy(w.b).to(cuda_device), tol=1e-10)
+    assert launch_count() > c0 + 3 * 200
