@@ -10,6 +10,7 @@ namespace sla {
 
 constexpr int NT = 256;          // threads per CTA for every kernel here
 constexpr int NWARP = NT / 32;
+constexpr int SPMV_MIN_CTAS = 4; // resident CTAs per SM the staged-SpMV kernels are compiled for
 constexpr int MAXR = NT;         // rows per row block (one row per thread)
 
 // Outcome codes mirrored from sla_status (kept numerically equal).
@@ -52,6 +53,25 @@ template <typename T>
 __device__ __forceinline__ T ld_nc(const T* p) { return __ldg(p); }        // read-only path
 template <typename T>
 __device__ __forceinline__ T ld_cg(const T* p) { return __ldcg(p); }       // L2 only (coherent)
+
+// Asynchronous global -> shared copies (cp.async, 4 or 8 bytes per thread),
+// cached at L1 with an L2 evict-first policy: the streamed matrix arrays are
+// read once per product and must not push the gathered vector out of L2.
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void* smem, const void* gmem, unsigned long long pol) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], %2, %3;\n" ::"r"(s), "l"(gmem), "n"(BYTES),
+                 "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // Value stored at the system's precision, returned as the fp64 value it holds.
 template <typename T>

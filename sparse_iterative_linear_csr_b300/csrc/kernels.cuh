@@ -5,17 +5,14 @@
 // and arrival counters are offset per system.  A converged system's CTAs
 // return at once, so frozen systems cost no memory traffic.
 //
-// SpMV layout: the rows are cut into row blocks of at most MAXR rows whose
-// non-zeros fit a TILE-entry shared-memory stage (a row longer than TILE is a
-// block of its own).  A CTA streams a block's values and column indices with
-// coalesced, evict-first loads, gathers the vector entries they address, and
-// stages (value, vector entry) pairs in shared memory; then one thread per
-// row forms the row sum with one fp64 fused multiply-add per non-zero.  One
-// FMA per non-zero is the least fp64 work an SpMV can do, which matters on a
-// part whose fp64 rate is low next to its memory bandwidth.
+// SpMV layout (spmv_rows): one warp per group of 32 consecutive rows; the
+// warp stages its non-zeros in shared memory, then each lane forms its row
+// sum with one fp64 fused multiply-add per non-zero.  One FMA per non-zero is
+// the least fp64 work an SpMV can do, which matters on a part whose fp64 rate
+// is low next to its memory bandwidth.
 //
-// Grids are persistent in x (CTAs walk row blocks / vector ranges with a
-// grid stride).  Inner products are reduced in a fixed order (grid_sum) and
+// Grids are persistent in x (warps / CTAs walk row groups / vector ranges
+// with a grid stride).  Inner products are reduced in a fixed order (grid_sum) and
 // the last CTA to finish updates that system's scalars on the device, so no
 // host round trip sits inside an iteration.
 //
@@ -45,8 +42,10 @@ struct Sys {
 struct Mat {
     const int* rp;
     const int* ci;
-    const int* rbs;   // row-block starts [nblk + 1]
-    int nblk;
+    int n;            // rows
+    int cap;          // staged entries per warp (per 32-row group)
+    int async;        // 1: cp.async double-buffered staging (spmv_rows_async)
+    int wstride;      // doubles of shared memory per warp (both staging forms)
 };
 
 #define SYS_PROLOGUE                                            \
@@ -70,57 +69,190 @@ struct GatherRounded {  // fp64 iterate rounded to the returned precision
     __device__ __forceinline__ double operator()(int c) const { return rnd<T>(ld_nc(v + c)); }
 };
 
-// Walk the row blocks of this CTA.  For every row, epi(row, sum) is called by
-// exactly one thread (thread-per-row for normal blocks, thread 0 for a long
-// row).  Must be called by all threads of the CTA.
-template <typename VT, int TILE, class Gather, class Epi>
+// Rows are taken in groups of 32, one warp per group (grid stride over
+// groups).  The warp stages its group's non-zeros -- values streamed with
+// coalesced evict-first loads, the vector entries they address gathered
+// through the read-only path -- as (value, entry) pairs in its own slice of
+// shared memory (`cap` pairs), then each lane sums its own row with one fp64
+// FMA per non-zero.  Only __syncwarp orders the two phases, so warps progress
+// independently and hide each other's memory latency.  A group with more than
+// `cap` non-zeros is summed straight from global memory: rows up to LONG
+// entries by their lane, longer rows by the whole warp.
+// epi(row, sum) is called once per row of the matrix by the row's lane.
+constexpr int STAGE_U = 4;     // entries per lane in flight while staging
+constexpr int LONG_ROW = 64;   // longer rows of an unstaged group go warp-wide
+
+template <typename VT, class Gather, class Epi>
 __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ av, Gather gather, Epi epi,
-                                          double* sa, double* sx, double* red) {
-    constexpr int PER = TILE / NT;
-    for (int b = blockIdx.x; b < A.nblk; b += gridDim.x) {
-        const int r0 = A.rbs[b], r1 = A.rbs[b + 1];
-        const int k0 = A.rp[r0], k1 = A.rp[r1];
+                                          double* wsm) {
+    const int lane = threadIdx.x & 31;
+    const int cap = A.cap;
+    double* sa = wsm + (threadIdx.x >> 5) * A.wstride;
+    double* sx = sa + cap;
+    const int ngroups = (A.n + 31) >> 5;
+    const int nwarps = (gridDim.x * NT) >> 5;
+    for (int grp = (blockIdx.x * NT + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
+        const int row = (grp << 5) + lane;
+        const int rlo = ld_nc(A.rp + min(row, A.n));
+        const int rhi = ld_nc(A.rp + min(row + 1, A.n));
+        const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
+        const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt = k1 - k0;
-        if (cnt <= TILE) {
-            int c[PER];
-            double a[PER], xv[PER];
+        double s = 0.0;
+        if (cnt <= cap) {
+            for (int base = 0; base < cnt; base += 32 * STAGE_U) {
+                int c[STAGE_U];
+                double a[STAGE_U], xv[STAGE_U];
 #pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const int e = threadIdx.x + j * NT;
-                if (e < cnt) {
-                    c[j] = ld_stream(A.ci + k0 + e);
-                    a[j] = (double)ld_stream(av + k0 + e);
+                for (int j = 0; j < STAGE_U; ++j) {
+                    const int e = base + j * 32 + lane;
+                    if (e < cnt) {
+                        c[j] = ld_stream(A.ci + k0 + e);
+                        a[j] = (double)ld_stream(av + k0 + e);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < STAGE_U; ++j) {
+                    const int e = base + j * 32 + lane;
+                    if (e < cnt) xv[j] = gather(c[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < STAGE_U; ++j) {
+                    const int e = base + j * 32 + lane;
+                    if (e < cnt) { sa[e] = a[j]; sx[e] = xv[j]; }
                 }
             }
+            __syncwarp();
+            for (int e = rlo - k0; e < rhi - k0; ++e) s = fma(sa[e], sx[e], s);
+            __syncwarp();
+        } else {
+            if (rhi - rlo <= LONG_ROW)
+                for (int k = rlo; k < rhi; ++k) s = fma((double)ld_stream(av + k), gather(ld_stream(A.ci + k)), s);
+            unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW);
+            while (longs) {
+                const int src = __ffs(longs) - 1;
+                longs &= longs - 1;
+                const int a0 = __shfl_sync(0xffffffffu, rlo, src);
+                const int a1 = __shfl_sync(0xffffffffu, rhi, src);
+                double t = 0.0;
+                for (int k = a0 + lane; k < a1; k += 32)
+                    t = fma((double)ld_stream(av + k), gather(ld_stream(A.ci + k)), t);
 #pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const int e = threadIdx.x + j * NT;
-                if (e < cnt) xv[j] = gather(c[j]);
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == src) s = t;
             }
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const int e = threadIdx.x + j * NT;
-                if (e < cnt) { sa[e] = a[j]; sx[e] = xv[j]; }
-            }
-            __syncthreads();
-            const int row = r0 + threadIdx.x;
-            if (row < r1) {
-                const int e0 = A.rp[row] - k0, e1 = A.rp[row + 1] - k0;
-                double s = 0.0;
-                for (int e = e0; e < e1; ++e) s = fma(sa[e], sx[e], s);
-                epi(row, s);
-            }
-            __syncthreads();
-        } else {  // one long row
-            double s = 0.0;
-            for (int k = k0 + threadIdx.x; k < k1; k += NT)
-                s = fma((double)ld_stream(av + k), gather(ld_stream(A.ci + k)), s);
-            double v[1] = {s};
-            block_sum<1>(v, red);
-            if (threadIdx.x == 0) epi(r0, v[0]);
-            __syncthreads();
         }
+        if (row < A.n) epi(row, s);
     }
+}
+
+// Pipelined form of spmv_rows for a plain vector gather (v[col] at its stored
+// precision).  Each warp double-buffers its groups' values and column
+// indices in shared memory with cp.async: the copies of the next group are in
+// flight while the warp gathers and sums the current one, so every warp keeps
+// ~12 bytes x (entries per group) of streaming traffic outstanding without
+// holding registers for it.  The gathered entries go through registers
+// (GATHER_U per lane in flight) into the warp's slice, then each lane sums
+// its own row with one fp64 FMA per entry.  Shared memory per warp:
+// 2*cap*(sizeof(VT) + 4) + 8*cap bytes (async_smem_per_warp).
+constexpr int GATHER_U = 8;
+
+template <typename VT>
+__host__ __device__ constexpr size_t async_smem_per_warp(int cap) {
+    return (size_t)2 * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(double);
+}
+
+template <typename VT, typename T, class Epi>
+__device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v,
+                                                Epi epi, double* wsm) {
+    const int lane = threadIdx.x & 31;
+    const int cap = A.cap;
+    char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
+    VT* sv = reinterpret_cast<VT*>(base);
+    int* sc = reinterpret_cast<int*>(base + 2 * cap * sizeof(VT));
+    double* sx = reinterpret_cast<double*>(base + 2 * cap * (sizeof(VT) + sizeof(int)));
+    const unsigned long long pol = l2_evict_first();
+    const int ngroups = (A.n + 31) >> 5;
+    const int nwarps = (gridDim.x * NT) >> 5;
+    const int g0 = (blockIdx.x * NT + threadIdx.x) >> 5;
+
+    auto issue = [&](int grp, int stage) {
+        if (grp < ngroups) {
+            const int k0 = ld_nc(A.rp + (grp << 5));
+            const int k1 = ld_nc(A.rp + min((grp << 5) + 32, A.n));
+            if (k1 - k0 <= cap) {
+                VT* dv = sv + stage * cap;
+                int* dc = sc + stage * cap;
+                for (int e = lane; e < k1 - k0; e += 32) {
+                    cp_async<sizeof(VT)>(dv + e, av + k0 + e, pol);
+                    cp_async<4>(dc + e, A.ci + k0 + e, pol);
+                }
+            }
+        }
+        cp_commit();
+    };
+
+    issue(g0, 0);
+    int stage = 0;
+    for (int grp = g0; grp < ngroups; grp += nwarps, stage ^= 1) {
+        issue(grp + nwarps, stage ^ 1);
+        const int row = (grp << 5) + lane;
+        const int rlo = ld_nc(A.rp + min(row, A.n));
+        const int rhi = ld_nc(A.rp + min(row + 1, A.n));
+        const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
+        const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
+        const int cnt = k1 - k0;
+        cp_wait<1>();  // this group's values and columns have landed
+        __syncwarp();
+        double s = 0.0;
+        if (cnt <= cap) {
+            const VT* cv = sv + stage * cap;
+            const int* cc = sc + stage * cap;
+            for (int b0 = 0; b0 < cnt; b0 += 32 * GATHER_U) {
+                double xv[GATHER_U];
+#pragma unroll
+                for (int j = 0; j < GATHER_U; ++j) {
+                    const int e = b0 + j * 32 + lane;
+                    if (e < cnt) xv[j] = (double)ld_nc(v + cc[e]);
+                }
+#pragma unroll
+                for (int j = 0; j < GATHER_U; ++j) {
+                    const int e = b0 + j * 32 + lane;
+                    if (e < cnt) sx[e] = xv[j];
+                }
+            }
+            __syncwarp();
+            for (int e = rlo - k0; e < rhi - k0; ++e) s = fma((double)cv[e], sx[e], s);
+        } else {
+            if (rhi - rlo <= LONG_ROW)
+                for (int k = rlo; k < rhi; ++k) s = fma((double)ld_stream(av + k), (double)ld_nc(v + ld_stream(A.ci + k)), s);
+            unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW);
+            while (longs) {
+                const int src = __ffs(longs) - 1;
+                longs &= longs - 1;
+                const int a0 = __shfl_sync(0xffffffffu, rlo, src);
+                const int a1 = __shfl_sync(0xffffffffu, rhi, src);
+                double t = 0.0;
+                for (int k = a0 + lane; k < a1; k += 32)
+                    t = fma((double)ld_stream(av + k), (double)ld_nc(v + ld_stream(A.ci + k)), t);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == src) s = t;
+            }
+        }
+        __syncwarp();  // this stage and sx are free for reuse
+        if (row < A.n) epi(row, s);
+    }
+    cp_wait<0>();
+}
+
+// Product with a plain vector gather: the pipelined form when the matrix was
+// set up for it, the single-stage form otherwise.
+template <typename VT, typename T, class Epi>
+__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v, Epi epi,
+                                         double* wsm) {
+    if (A.async) spmv_rows_async<VT>(A, av, v, epi, wsm);
+    else spmv_rows<VT>(A, av, GatherVec<T>{v}, epi, wsm);
 }
 
 // ----------------------------------------------------------------- scalar logic
@@ -190,21 +322,21 @@ __device__ __forceinline__ void start_state(State* s, Ctrl* c, double bb, double
 
 // ----------------------------------------------------------------- SpMV API
 // y = A x, and dot[sys] = x.y when dot != nullptr.
-template <typename T, int TILE>
-__global__ void __launch_bounds__(NT) k_spmv(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ x,
+template <typename T>
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ x,
                                              T* __restrict__ y, double* dot) {
     SYS_PROLOGUE
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     av += ao; x += vo; y += vo;
     double acc = 0.0;
-    spmv_rows<T, TILE>(A, av, GatherVec<T>{x},
-                       [&](int i, double s) {
-                           const T yi = (T)s;
-                           y[i] = yi;
-                           acc = fma((double)x[i], (double)yi, acc);
-                       },
-                       dsm, dsm + TILE, red);
+    spmv_vec<T>(A, av, x,
+                 [&](int i, double s) {
+                     const T yi = (T)s;
+                     y[i] = yi;
+                     acc = fma((double)x[i], (double)yi, acc);
+                 },
+                 dsm);
     if (dot) {
         double v[1] = {acc}, tot[1];
         if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) dot[sys] = tot[0];
@@ -213,8 +345,8 @@ __global__ void __launch_bounds__(NT) k_spmv(Mat A, Sys S, const T* __restrict__
 
 // ----------------------------------------------------------------- iteration
 // q = A p, delta = p.q; with `check` set, ||b - A round(x)||^2 first.
-template <typename T, int TILE>
-__global__ void __launch_bounds__(NT) k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ p,
+template <typename T>
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ p,
                                                   T* __restrict__ q, const double* __restrict__ x,
                                                   const T* __restrict__ b) {
     SYS_PROLOGUE
@@ -225,27 +357,43 @@ __global__ void __launch_bounds__(NT) k_spmv_iter(Mat A, Sys S, const T* __restr
     const bool check = ld_cg(&st->check) != 0;
     double tr2 = 0.0, delta = 0.0;
     if (check) {
-        spmv_rows<T, TILE>(A, av, GatherRounded<T>{x},
-                           [&](int i, double s) {
-                               const double e = (double)b[i] - s;
-                               tr2 = fma(e, e, tr2);
-                           },
-                           dsm, dsm + TILE, red);
+        spmv_rows<T>(A, av, GatherRounded<T>{x},
+                     [&](int i, double s) {
+                         const double e = (double)b[i] - s;
+                         tr2 = fma(e, e, tr2);
+                     },
+                     dsm);
     }
-    spmv_rows<T, TILE>(A, av, GatherVec<T>{p},
-                       [&](int i, double s) {
-                           const T qi = (T)s;
-                           q[i] = qi;
-                           delta = fma((double)p[i], (double)qi, delta);
-                       },
-                       dsm, dsm + TILE, red);
+    spmv_vec<T>(A, av, p,
+                 [&](int i, double s) {
+                     const T qi = (T)s;
+                     q[i] = qi;
+                     delta = fma((double)p[i], (double)qi, delta);
+                 },
+                 dsm);
     double v[2] = {delta, tr2}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0) after_spmv(st, S.ctl, tot[0], check, tot[1]);
 }
 
+// Pairs of consecutive entries (8/16-byte vector accesses) for the streaming
+// kernels; used when n is even, so every system's vectors stay aligned.
+template <typename T> struct Pair;
+template <> struct Pair<double> { using type = double2; };
+template <> struct Pair<float> { using type = float2; };
+
 // x += alpha p; r -= alpha q; gamma = r.r; rho' = r.z (PC 0: z = r, PC 1:
 // z = r / A_ii; PC 2: z comes later from the SPAI kernels).
 template <typename T, int PC>
+__device__ __forceinline__ void update_one(double alpha, double& x, T& r, double p, double q, double dinv,
+                                           double& g, double& rz) {
+    x = fma(alpha, p, x);
+    const double ri = rnd<T>(fma(-alpha, q, (double)r));
+    r = (T)ri;
+    g = fma(ri, ri, g);
+    if (PC == 1) rz = fma(ri, rnd<T>(ri * dinv), rz);
+}
+
+template <typename T, int PC, bool PAIRS>
 __global__ void __launch_bounds__(NT) k_update(Sys S, double* __restrict__ x, T* __restrict__ r,
                                                const T* __restrict__ p, const T* __restrict__ q,
                                                const double* __restrict__ dinv) {
@@ -256,14 +404,45 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, double* __restrict__ x, T*
     if (PC == 1) dinv += vo;
     const double alpha = ld_cg(&st->alpha);
     double g = 0.0, rz = 0.0;
-    for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-        const double pi = (double)ld_stream(p + i);
-        const double qi = (double)ld_stream(q + i);
-        x[i] = fma(alpha, pi, x[i]);
-        const double ri = rnd<T>(fma(-alpha, qi, (double)r[i]));
-        r[i] = (T)ri;
-        g = fma(ri, ri, g);
-        if (PC == 1) rz = fma(ri, rnd<T>(ri * dinv[i]), rz);
+    if (PAIRS) {
+        // two pairs per thread per trip, all loads issued before any use
+        using P2 = typename Pair<T>::type;
+        const int n2 = S.n >> 1;
+        const int stride = gridDim.x * NT;
+        for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += 2 * stride) {
+            P2 p2[2], q2[2], r2[2];
+            double2 x2[2], d2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * stride;
+                if (i < n2) {
+                    p2[u] = ld_stream(reinterpret_cast<const P2*>(p) + i);
+                    q2[u] = ld_stream(reinterpret_cast<const P2*>(q) + i);
+                    x2[u] = reinterpret_cast<const double2*>(x)[i];
+                    r2[u] = reinterpret_cast<const P2*>(r)[i];
+                    d2[u] = PC == 1 ? ld_stream(reinterpret_cast<const double2*>(dinv) + i) : make_double2(0.0, 0.0);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * stride;
+                if (i < n2) {
+                    update_one<T, PC>(alpha, x2[u].x, r2[u].x, (double)p2[u].x, (double)q2[u].x, d2[u].x, g, rz);
+                    update_one<T, PC>(alpha, x2[u].y, r2[u].y, (double)p2[u].y, (double)q2[u].y, d2[u].y, g, rz);
+                    reinterpret_cast<double2*>(x)[i] = x2[u];
+                    reinterpret_cast<P2*>(r)[i] = r2[u];
+                }
+            }
+        }
+    } else {
+        for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
+            double xi = x[i];
+            T ri = r[i];
+            update_one<T, PC>(alpha, xi, ri, (double)ld_stream(p + i), (double)ld_stream(q + i),
+                              PC == 1 ? dinv[i] : 0.0, g, rz);
+            x[i] = xi;
+            r[i] = ri;
+        }
     }
     double v[2] = {g, rz}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0)
@@ -272,6 +451,15 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, double* __restrict__ x, T*
 
 // p = z + beta p   (INIT: p = z)
 template <typename T, int PC, bool INIT>
+__device__ __forceinline__ T pnew(double beta, double p, double r, double dinv, double z) {
+    double zi;
+    if (PC == 0) zi = r;
+    else if (PC == 1) zi = rnd<T>(r * dinv);
+    else zi = z;
+    return INIT ? (T)zi : (T)fma(beta, p, zi);
+}
+
+template <typename T, int PC, bool INIT, bool PAIRS>
 __global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const T* __restrict__ r,
                                                 const T* __restrict__ z, const double* __restrict__ dinv) {
     SYS_PROLOGUE
@@ -280,32 +468,55 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const 
     if (PC == 1) dinv += vo;
     if (PC == 2) z += vo;
     const double beta = INIT ? 0.0 : ld_cg(&st->beta);
-    for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-        double zi;
-        if (PC == 0) zi = (double)r[i];
-        else if (PC == 1) zi = rnd<T>((double)r[i] * dinv[i]);
-        else zi = (double)z[i];
-        p[i] = INIT ? (T)zi : (T)fma(beta, (double)p[i], zi);
+    if (PAIRS) {
+        using P2 = typename Pair<T>::type;
+        const int n2 = S.n >> 1;
+        const int stride = gridDim.x * NT;
+        for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += 2 * stride) {
+            P2 r2[2], p2[2], z2[2];
+            double2 d2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * stride;
+                if (i < n2) {
+                    r2[u] = ld_stream(reinterpret_cast<const P2*>(r) + i);
+                    p2[u] = INIT ? P2{} : reinterpret_cast<const P2*>(p)[i];
+                    d2[u] = PC == 1 ? ld_stream(reinterpret_cast<const double2*>(dinv) + i) : make_double2(0.0, 0.0);
+                    z2[u] = PC == 2 ? ld_stream(reinterpret_cast<const P2*>(z) + i) : P2{};
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * stride;
+                if (i < n2) {
+                    p2[u].x = pnew<T, PC, INIT>(beta, (double)p2[u].x, (double)r2[u].x, d2[u].x, (double)z2[u].x);
+                    p2[u].y = pnew<T, PC, INIT>(beta, (double)p2[u].y, (double)r2[u].y, d2[u].y, (double)z2[u].y);
+                    reinterpret_cast<P2*>(p)[i] = p2[u];
+                }
+            }
+        }
+    } else {
+        for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT)
+            p[i] = pnew<T, PC, INIT>(beta, INIT ? 0.0 : (double)p[i], (double)r[i], PC == 1 ? dinv[i] : 0.0,
+                                     PC == 2 ? (double)z[i] : 0.0);
     }
 }
 
 // SPAI, first product: t = G^T r (explicit transposed CSR of G; G values
 // are per system, [batch][nnz(G)]).
-template <typename T, int TILE>
-__global__ void __launch_bounds__(NT) k_spai_t(Mat GT, Sys S, long long nnzg, const double* __restrict__ gtv,
+template <typename T>
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, long long nnzg, const double* __restrict__ gtv,
                                                const T* __restrict__ r, T* __restrict__ t) {
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
-    __shared__ double red[2 * NWARP];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
-    spmv_rows<double, TILE>(GT, gtv, GatherVec<T>{r}, [&](int i, double s) { t[i] = (T)s; }, dsm, dsm + TILE,
-                            red);
+    spmv_vec<double>(GT, gtv, r, [&](int i, double s) { t[i] = (T)s; }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
-template <typename T, int TILE>
-__global__ void __launch_bounds__(NT) k_spai_z(Mat G, Sys S, long long nnzg, const double* __restrict__ gv,
+template <typename T>
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long long nnzg, const double* __restrict__ gv,
                                                const T* __restrict__ t, const T* __restrict__ r,
                                                T* __restrict__ z, double eps) {
     SYS_PROLOGUE
@@ -314,14 +525,14 @@ __global__ void __launch_bounds__(NT) k_spai_z(Mat G, Sys S, long long nnzg, con
     __shared__ double red[2 * NWARP];
     gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
     double rz = 0.0;
-    spmv_rows<double, TILE>(G, gv, GatherVec<T>{t},
-                            [&](int i, double s) {
-                                const double ri = (double)r[i];
-                                const double zi = rnd<T>(fma(eps, ri, s));
-                                z[i] = (T)zi;
-                                rz = fma(ri, zi, rz);
-                            },
-                            dsm, dsm + TILE, red);
+    spmv_vec<double>(G, gv, t,
+                      [&](int i, double s) {
+                          const double ri = (double)r[i];
+                          const double zi = rnd<T>(fma(eps, ri, s));
+                          z[i] = (T)zi;
+                          rz = fma(ri, zi, rz);
+                      },
+                      dsm);
     double v[1] = {rz}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) new_direction(st, S.ctl, tot[0]);
 }
@@ -348,8 +559,8 @@ __global__ void __launch_bounds__(NT) k_init(Sys S, const T* __restrict__ b_user
 }
 
 // With an initial guess: x = x0, r = b - A x0, bb = b.b, gamma = r.r.
-template <typename T, int TILE>
-__global__ void __launch_bounds__(NT) k_init_x0(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ b_user,
+template <typename T>
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_init_x0(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ b_user,
                                                 const T* __restrict__ x0, T* __restrict__ bw,
                                                 double* __restrict__ x, T* __restrict__ r, double tol,
                                                 int max_iter) {
@@ -358,17 +569,17 @@ __global__ void __launch_bounds__(NT) k_init_x0(Mat A, Sys S, const T* __restric
     __shared__ double red[2 * NWARP];
     av += ao; b_user += vo; x0 += vo; bw += vo; x += vo; r += vo;
     double bb = 0.0, g = 0.0;
-    spmv_rows<T, TILE>(A, av, GatherVec<T>{x0},
-                       [&](int i, double s) {
-                           const T bi = b_user[i];
-                           bw[i] = bi;
-                           x[i] = (double)x0[i];
-                           const double ri = rnd<T>((double)bi - s);
-                           r[i] = (T)ri;
-                           bb = fma((double)bi, (double)bi, bb);
-                           g = fma(ri, ri, g);
-                       },
-                       dsm, dsm + TILE, red);
+    spmv_rows<T>(A, av, GatherVec<T>{x0},
+                 [&](int i, double s) {
+                     const T bi = b_user[i];
+                     bw[i] = bi;
+                     x[i] = (double)x0[i];
+                     const double ri = rnd<T>((double)bi - s);
+                     r[i] = (T)ri;
+                     bb = fma((double)bi, (double)bi, bb);
+                     g = fma(ri, ri, g);
+                 },
+                 dsm);
     double v[2] = {bb, g}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0)
         start_state(st, S.ctl, tot[0], tot[1], tol, max_iter);
@@ -404,8 +615,8 @@ struct Stat {
 };
 
 // Returned x = round(x_w) (0 when b = 0); true residual of that x; statistics.
-template <typename T, int TILE>
-__global__ void __launch_bounds__(NT) k_final(Mat A, Sys S, const T* __restrict__ av, const double* __restrict__ x,
+template <typename T>
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_final(Mat A, Sys S, const T* __restrict__ av, const double* __restrict__ x,
                                               const T* __restrict__ bw, T* __restrict__ x_out, Stat* out) {
     SYS_PROLOGUE
     extern __shared__ double dsm[];
@@ -413,13 +624,13 @@ __global__ void __launch_bounds__(NT) k_final(Mat A, Sys S, const T* __restrict_
     av += ao; x += vo; bw += vo; x_out += vo;
     const bool zero_b = ld_cg(&st->bb) == 0.0;
     double tr2 = 0.0;
-    spmv_rows<T, TILE>(A, av, GatherRounded<T>{x},
-                       [&](int i, double s) {
-                           x_out[i] = zero_b ? (T)0 : (T)x[i];
-                           const double e = (double)bw[i] - s;
-                           tr2 = fma(e, e, tr2);
-                       },
-                       dsm, dsm + TILE, red);
+    spmv_rows<T>(A, av, GatherRounded<T>{x},
+                 [&](int i, double s) {
+                     x_out[i] = zero_b ? (T)0 : (T)x[i];
+                     const double e = (double)bw[i] - s;
+                     tr2 = fma(e, e, tr2);
+                 },
+                 dsm);
     double v[1] = {tr2}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) {
         const double bb = st->bb;
@@ -434,37 +645,40 @@ __global__ void __launch_bounds__(NT) k_final(Mat A, Sys S, const T* __restrict_
     }
 }
 
-// dL/dA_k = -lambda_row(k) * x_col(k) over the pattern (row blocks; the row
-// of each staged entry is recorded in shared memory so reads and writes of
-// the nnz-sized arrays stream).
-template <typename T, int TILE>
+// dL/dA_k = -lambda_row(k) * x_col(k) over the pattern.  One warp per group
+// of 32 rows: the row of each of the group's entries is recorded in the
+// warp's shared-memory slice, then the entries stream (coalesced reads of
+// col_idx, coalesced writes of dA).  A group with more than `cap` entries is
+// written row by row from its lanes.
+template <typename T>
 __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict__ lam, const T* __restrict__ x,
                                                T* __restrict__ dA) {
     SYS_PROLOGUE
     extern __shared__ double dsm[];
-    int* srow = reinterpret_cast<int*>(dsm);
+    int* srow = reinterpret_cast<int*>(dsm + (threadIdx.x >> 5) * A.wstride);
+    const int lane = threadIdx.x & 31;
     lam += vo; x += vo; dA += ao;
-    for (int b = blockIdx.x; b < A.nblk; b += gridDim.x) {
-        const int r0 = A.rbs[b], r1 = A.rbs[b + 1];
-        const int k0 = A.rp[r0], k1 = A.rp[r1];
+    const int ngroups = (A.n + 31) >> 5;
+    const int nwarps = (gridDim.x * NT) >> 5;
+    for (int grp = (blockIdx.x * NT + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
+        const int row = (grp << 5) + lane;
+        const int rlo = ld_nc(A.rp + min(row, A.n));
+        const int rhi = ld_nc(A.rp + min(row + 1, A.n));
+        const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
+        const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt_ = k1 - k0;
-        if (cnt_ <= TILE) {
-            const int row = r0 + threadIdx.x;
-            if (row < r1) {
-                const int e0 = A.rp[row] - k0, e1 = A.rp[row + 1] - k0;
-                for (int e = e0; e < e1; ++e) srow[e] = row;
-            }
-            __syncthreads();
-            for (int e = threadIdx.x; e < cnt_; e += NT) {
+        if (cnt_ <= A.cap) {
+            for (int e = rlo - k0; e < rhi - k0; ++e) srow[e] = row;
+            __syncwarp();
+            for (int e = lane; e < cnt_; e += 32) {
                 const int c = ld_stream(A.ci + k0 + e);
                 const double li = (double)ld_nc(lam + srow[e]);
                 __stcs(dA + k0 + e, (T)(-li * (double)ld_nc(x + c)));
             }
-            __syncthreads();
-        } else {
-            const double li = (double)lam[r0];
-            for (int k = k0 + threadIdx.x; k < k1; k += NT)
-                __stcs(dA + k, (T)(-li * (double)ld_nc(x + ld_stream(A.ci + k))));
+            __syncwarp();
+        } else if (row < A.n) {
+            const double li = (double)lam[row];
+            for (int k = rlo; k < rhi; ++k) __stcs(dA + k, (T)(-li * (double)ld_nc(x + ld_stream(A.ci + k))));
         }
     }
 }

@@ -1,7 +1,7 @@
 // setup.cuh -- once-per-pattern (and once-per-values) device set-up:
-// CSR validation, diagonal extraction, row-block partition for the staged
-// SpMV, an exclusive scan, the closed-form SPAI factor G on tril(A) and its
-// explicit transpose, and the [batch][*] <-> [*][batch] layout transposes.
+// CSR validation, diagonal extraction, the per-warp staging capacity of the
+// SpMV, an exclusive scan, and the closed-form SPAI factor G on tril(A) with
+// its explicit transpose.
 #pragma once
 
 #include "common.cuh"
@@ -48,8 +48,8 @@ __device__ __forceinline__ int find_col(const int* __restrict__ ci, int a, int b
     return (lo < b && ci[lo] == c) ? lo : -1;
 }
 
-// diag[s*n + i] = A_ii of system s (fp64), dpos[i] = its position; error bits
-// for a missing (or non-positive, when checked) diagonal.
+// diag[s*n + i] = A_ii of system s (fp64); error bits for a missing or a
+// non-positive diagonal entry.
 template <typename T>
 __global__ void k_diag(int n, long long nnz, int batch, const int* __restrict__ rp, const int* __restrict__ ci,
                        const T* __restrict__ av, double* diag, int* err) {
@@ -71,34 +71,15 @@ __global__ void k_recip(size_t m, const double* __restrict__ d, double* __restri
         dinv[i] = 1.0 / d[i];
 }
 
-// ----------------------------------------------------------------- row blocks
-// Rows are taken in chunks of MAXR; inside a chunk a block grows while its
-// non-zeros fit `tile`; a row longer than `tile` is a block alone.
-__device__ __forceinline__ int walk_chunk(const int* __restrict__ rp, int n, int c, int tile, int* out) {
-    int r = c * MAXR;
-    const int rend = min(r + MAXR, n);
-    int nb = 0;
-    while (r < rend) {
-        if (out) out[nb] = r;
-        const int k0 = rp[r];
-        if (rp[r + 1] - k0 > tile) ++r;
-        else while (r < rend && rp[r + 1] - k0 <= tile) ++r;
-        ++nb;
-    }
-    return nb;
-}
-
-__global__ void k_rb_count(const int* __restrict__ rp, int n, int tile, int* cnt) {
-    const int nch = (n + MAXR - 1) / MAXR;
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nch; c += gridDim.x * blockDim.x)
-        cnt[c] = walk_chunk(rp, n, c, tile, nullptr);
-}
-
-__global__ void k_rb_fill(const int* __restrict__ rp, int n, int tile, const int* __restrict__ off, int* rbs) {
-    const int nch = (n + MAXR - 1) / MAXR;
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nch; c += gridDim.x * blockDim.x)
-        walk_chunk(rp, n, c, tile, rbs + off[c]);
-    if (blockIdx.x == 0 && threadIdx.x == 0) rbs[off[nch]] = n;
+// ----------------------------------------------------------------- row groups
+// Largest number of stored entries in any group of 32 consecutive rows (the
+// shared-memory staging capacity a warp needs for the SpMV).
+__global__ void k_group_max(const int* __restrict__ rp, int n, int* out) {
+    const int ng = (n + 31) >> 5;
+    int m = 0;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < ng; g += gridDim.x * blockDim.x)
+        m = max(m, rp[min((g << 5) + 32, n)] - rp[g << 5]);
+    if (m) atomicMax(out, m);
 }
 
 // ----------------------------------------------------------------- scan
@@ -211,23 +192,6 @@ __global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restri
         }
     }
     if (bits) atomicOr(err, bits);
-}
-
-// ----------------------------------------------------------------- layouts
-// out[c][r] = in[r][c] for a rows x cols matrix (32 x 32 tiles).
-template <typename T>
-__global__ void k_transpose(const T* __restrict__ in, T* __restrict__ out, long long rows, long long cols) {
-    __shared__ T tile[32][33];
-    const long long c0 = (long long)blockIdx.x * 32, r0 = (long long)blockIdx.y * 32;
-    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
-        const long long r = r0 + dy, c = c0 + threadIdx.x;
-        if (r < rows && c < cols) tile[dy][threadIdx.x] = in[r * cols + c];
-    }
-    __syncthreads();
-    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
-        const long long c = c0 + dy, r = r0 + threadIdx.x;
-        if (r < rows && c < cols) out[c * rows + r] = tile[threadIdx.x][dy];
-    }
 }
 
 }  // namespace sla

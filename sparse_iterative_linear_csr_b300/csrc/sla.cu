@@ -99,12 +99,6 @@ struct GraphCache {
     }
 };
 
-struct RowBlocks {
-    DevBuf rbs;
-    int nblk = 0;
-    int tile = 0;
-};
-
 struct sla_csr {
     int n = 0;
     long long nnz = 0;
@@ -117,16 +111,16 @@ struct sla_csr {
     int device = 0;
     int sms = 0;
 
-    RowBlocks A;
+    int capA = 32;     // SpMV staging capacity (entries per 32-row group)
+    int gxA = 1, gxG = 1, gxGT = 1;  // staged-SpMV CTAs per system for A, G, G^T
     int diag_err = 0;  // ERR_NO_DIAG | ERR_DIAG_SIGN
     DevBuf diag, dinv;
 
     // SPAI factor (built on first use, per values)
     bool spai_ready = false;
-    int spai_err = 0;
     long long nnzg = 0;
+    int capG = 32, capGT = 32;
     DevBuf grp, gci, gv, gtrp, gtci, gtv;
-    RowBlocks G, GT;
 
     // workspace
     DevBuf x, r, p, q, z, t, bw;
@@ -139,70 +133,88 @@ struct sla_csr {
     GraphCache graph[3];
 };
 
-static int pick_tile(long long nnz, int n) {
-    const double per_chunk = (double)MAXR * (double)nnz / (double)(n > 0 ? n : 1) * 1.15;
-    if (per_chunk <= 1024) return 1024;
-    if (per_chunk <= 2048) return 2048;
-    return 4096;
+static constexpr int MAX_CAP = 864;        // staging capacity limit (larger groups take the global path)
+static constexpr int ASYNC_MAX_CAP = 320;  // pipelined staging up to this capacity (2+ CTAs per SM)
+
+static bool use_async(int cap) { return cap <= ASYNC_MAX_CAP; }
+// Dynamic shared memory of the staged-SpMV kernels for capacity `cap`.
+static size_t spmv_smem(int cap) {
+    const size_t single = (size_t)cap * 2 * sizeof(double);
+    const size_t piped = async_smem_per_warp<double>(cap);
+    return (size_t)NWARP * (use_async(cap) && piped > single ? piped : single);
 }
+static size_t grad_smem(int cap) { return spmv_smem(cap); }
 
-template <class F>
-static void with_tile(int tile, F&& f) {
-    switch (tile) {
-        case 1024: f(std::integral_constant<int, 1024>{}); break;
-        case 2048: f(std::integral_constant<int, 2048>{}); break;
-        default: f(std::integral_constant<int, 4096>{}); break;
-    }
-}
-
-static size_t smem_for(int tile) { return (size_t)tile * 2 * sizeof(double); }
-
-// Opt in to >48 KB dynamic shared memory for every staged-SpMV kernel of one
-// (T, TILE) instantiation.  Runs once per process and instantiation.
-template <typename T, int TILE>
-static sla_status prepare_kernels() {
-    static std::atomic<int> done{0};
-    if (done.load()) return SLA_OK;
-    const int bytes = (int)smem_for(TILE);
-    CU(cudaFuncSetAttribute(k_spmv<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    CU(cudaFuncSetAttribute(k_spmv_iter<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    CU(cudaFuncSetAttribute(k_init_x0<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    CU(cudaFuncSetAttribute(k_final<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    CU(cudaFuncSetAttribute(k_grad_A<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    CU(cudaFuncSetAttribute(k_spai_t<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    CU(cudaFuncSetAttribute(k_spai_z<T, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-    done.store(1);
+// Resident CTAs per SM of `kern` with `smem` bytes of dynamic shared memory
+// (the kernel must already allow that much: allow_smem).
+template <typename K>
+static sla_status occupancy(K kern, size_t smem, int* out) {
+    int nb = 0;
+    CU(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NT, smem));
+    *out = nb > 0 ? nb : 1;
     return SLA_OK;
 }
 
-template <typename T>
-static sla_status prepare_all() {
-    TRY((prepare_kernels<T, 1024>()));
-    TRY((prepare_kernels<T, 2048>()));
-    TRY((prepare_kernels<T, 4096>()));
-    return SLA_OK;
-}
-
-// CTAs per system for a kernel walking `units` work units (row blocks or
-// NT-element vector chunks), `per_sm` resident CTAs per SM.
+// CTAs per system for a kernel walking `units` work units with `per_sm`
+// resident CTAs per SM (persistent in x: a multiple of the SM count when
+// there is enough work).
 static int grid_x(const sla_csr* h, long long units, int per_sm) {
     long long g = (long long)per_sm * h->sms / h->batch;
-    if (g < 1) g = 1;
     if (g > units) g = units;
     if (g < 1) g = 1;
     return (int)g;
 }
 
-static int per_sm_spmv(int tile) {
-    // 256 threads, 16*TILE bytes of staging: the smaller of the thread and
-    // shared-memory limits (228 KB per SM, 1 KB reserved per CTA).
-    const int by_smem = (int)((228 * 1024) / (smem_for(tile) + 2048));
-    const int by_threads = 2048 / NT;
-    return by_smem < by_threads ? by_smem : by_threads;
+static long long group_ctas(int n) { return (((long long)n + 31) / 32 + NWARP - 1) / NWARP; }
+static bool pairs_ok(const sla_csr* h) { return (h->n & 1) == 0; }
+static long long vec_units(const sla_csr* h) {
+    const long long m = pairs_ok(h) ? h->n / 2 : h->n;
+    return (m + NT - 1) / NT;
 }
 
-static int gx_spmv(const sla_csr* h, const RowBlocks& rb) { return grid_x(h, rb.nblk, per_sm_spmv(rb.tile)); }
-static int gx_vec(const sla_csr* h) { return grid_x(h, ((long long)h->n + NT - 1) / NT, 2048 / NT); }
+// Allow every staged-SpMV kernel of dtype T the largest staging slice.
+template <typename T>
+static sla_status allow_smem() {
+    static std::atomic<int> done{0};
+    if (done.load()) return SLA_OK;
+    const int b = (int)spmv_smem(MAX_CAP);
+    CU(cudaFuncSetAttribute(k_spmv<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_spmv_iter<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_init_x0<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_final<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_spai_t<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_spai_z<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_grad_A<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    done.store(1);
+    return SLA_OK;
+}
+
+// CTAs per system for the staged SpMV kernels with staging capacity `cap`.
+template <typename T>
+static sla_status spmv_grid(const sla_csr* h, int cap, int* gx) {
+    int per = 1;
+    TRY(occupancy(k_spmv_iter<T>, spmv_smem(cap), &per));
+    *gx = grid_x(h, group_ctas(h->n), per);
+    return SLA_OK;
+}
+
+static sla_status spmv_grid_any(const sla_csr* h, int cap, int* gx) {
+    return h->dt == SLA_F64 ? spmv_grid<double>(h, cap, gx) : spmv_grid<float>(h, cap, gx);
+}
+
+// Streaming kernels: two resident CTAs per SM.  Each warp-level fp64
+// reduction step costs a full warp issue on the slow fp64 pipe, so fewer,
+// longer-running threads (each with two pairs in flight per trip) beat a
+// fully occupied grid here.
+static constexpr int VEC_CTAS_PER_SM = 2;
+static int gx_vec(const sla_csr* h) { return grid_x(h, vec_units(h), VEC_CTAS_PER_SM); }
+static int gx_spmv(const sla_csr* h, int cap);
+
+static int gx_spmv(const sla_csr* h, int cap) {
+    if (cap == h->capA) return h->gxA;
+    if (cap == h->capG) return h->gxG;
+    return h->gxGT;
+}
 
 static Sys sys_of(sla_csr* h) {
     Sys s;
@@ -216,12 +228,14 @@ static Sys sys_of(sla_csr* h) {
     return s;
 }
 
-static Mat mat_of(const int* rp, const int* ci, const RowBlocks& rb) {
+static Mat mat_of(const int* rp, const int* ci, int n, int cap) {
     Mat m;
     m.rp = rp;
     m.ci = ci;
-    m.rbs = rb.rbs.as<int>();
-    m.nblk = rb.nblk;
+    m.n = n;
+    m.cap = cap;
+    m.async = use_async(cap) ? 1 : 0;
+    m.wstride = (int)(spmv_smem(cap) / NWARP / sizeof(double));
     return m;
 }
 
@@ -249,23 +263,20 @@ static sla_status read_int(const int* d, int* out, cudaStream_t s) {
     return SLA_OK;
 }
 
-static sla_status build_row_blocks(const int* rp, int n, int tile, RowBlocks& rb, cudaStream_t s) {
-    const int nch = (n + MAXR - 1) / MAXR;
-    DevBuf cnt;
-    TRY(cnt.alloc(sizeof(int) * (size_t)(nch + 1)));
-    const int g = (nch + 255) / 256;
-    k_rb_count<<<g, 256, 0, s>>>(rp, n, tile, cnt.as<int>());
+static sla_status staging_cap(const int* rp, int n, int* cap, cudaStream_t s) {
+    DevBuf m;
+    TRY(m.alloc(sizeof(int)));
+    CU(cudaMemsetAsync(m.p, 0, sizeof(int), s));
+    const int ng = (n + 31) / 32;
+    const int g = (ng + 255) / 256 < 2048 ? (ng + 255) / 256 : 2048;
+    k_group_max<<<g, 256, 0, s>>>(rp, n, m.as<int>());
     TRY(launched());
-    CU(cudaMemsetAsync(cnt.as<int>() + nch, 0, sizeof(int), s));
-    TRY(scan_exclusive(cnt.as<int>(), nch + 1, s));
-    int total = 0;
-    TRY(read_int(cnt.as<int>() + nch, &total, s));
-    TRY(rb.rbs.alloc(sizeof(int) * (size_t)(total + 1)));
-    k_rb_fill<<<g, 256, 0, s>>>(rp, n, tile, cnt.as<int>(), rb.rbs.as<int>());
-    TRY(launched());
-    CU(cudaStreamSynchronize(s));
-    rb.nblk = total;
-    rb.tile = tile;
+    int v = 0;
+    TRY(read_int(m.as<int>(), &v, s));
+    v = (v + 31) / 32 * 32;
+    if (v < 32) v = 32;
+    if (v > MAX_CAP) v = MAX_CAP;
+    *cap = v;
     return SLA_OK;
 }
 
@@ -292,7 +303,6 @@ static void release_spai(sla_csr* h) {
     h->spai_ready = false;
     h->grp.release(); h->gci.release(); h->gv.release();
     h->gtrp.release(); h->gtci.release(); h->gtv.release();
-    h->G.rbs.release(); h->GT.rbs.release();
     h->z.release(); h->t.release();
     for (auto& g : h->graph) g.reset();
 }
@@ -346,9 +356,10 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     int e = 0;
     TRY(read_int(err.as<int>(), &e, s));
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
-    const int tile = pick_tile(ng, n);
-    TRY(build_row_blocks(h->grp.as<int>(), n, tile, h->G, s));
-    TRY(build_row_blocks(h->gtrp.as<int>(), n, tile, h->GT, s));
+    TRY(staging_cap(h->grp.as<int>(), n, &h->capG, s));
+    TRY(staging_cap(h->gtrp.as<int>(), n, &h->capGT, s));
+    TRY(spmv_grid_any(h, h->capG, &h->gxG));
+    TRY(spmv_grid_any(h, h->capGT, &h->gxGT));
     TRY(h->z.alloc(h->es * (size_t)n * h->batch));
     TRY(h->t.alloc(h->es * (size_t)n * h->batch));
     h->spai_ready = true;
@@ -357,10 +368,10 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
 
 static sla_status ensure_pstride(sla_csr* h) {
     int m = gx_vec(h);
-    m = m > gx_spmv(h, h->A) ? m : gx_spmv(h, h->A);
+    m = m > gx_spmv(h, h->capA) ? m : gx_spmv(h, h->capA);
     if (h->spai_ready) {
-        m = m > gx_spmv(h, h->G) ? m : gx_spmv(h, h->G);
-        m = m > gx_spmv(h, h->GT) ? m : gx_spmv(h, h->GT);
+        m = m > gx_spmv(h, h->capG) ? m : gx_spmv(h, h->capG);
+        m = m > gx_spmv(h, h->capGT) ? m : gx_spmv(h, h->capGT);
     }
     const int need = 2 * m;
     if (need <= h->pstride) return SLA_OK;
@@ -371,44 +382,44 @@ static sla_status ensure_pstride(sla_csr* h) {
 }
 
 // ===================================================================== kernels per iteration
-template <typename T, int TA, int TG>
+template <typename T, bool PAIRS>
 static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->A);
+    const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
     const T* av = (const T*)h->vals;
     T* r = h->r.as<T>();
     T* p = h->p.as<T>();
     T* q = h->q.as<T>();
     double* x = h->x.as<double>();
     const double* dinv = h->dinv.as<double>();
-    const dim3 gs(gx_spmv(h, h->A), h->batch), gv(gx_vec(h), h->batch);
-    k_spmv_iter<T, TA><<<gs, NT, smem_for(TA), s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    const dim3 gs(gx_spmv(h, h->capA), h->batch), gv(gx_vec(h), h->batch);
+    k_spmv_iter<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, p, q, x, h->bw.as<T>());
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
-        k_update<T, 2><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        k_update<T, 2, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
         TRY(launched());
-        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->GT);
-        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->G);
-        k_spai_t<T, TG><<<dim3(gx_spmv(h, h->GT), h->batch), NT, smem_for(TG), s>>>(GT, S, h->nnzg,
-                                                                                    h->gtv.as<double>(), r,
-                                                                                    h->t.as<T>());
+        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->capGT);
+        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->capG);
+        k_spai_t<T><<<dim3(gx_spmv(h, h->capGT), h->batch), NT, spmv_smem(h->capGT), s>>>(GT, S, h->nnzg,
+                                                                                        h->gtv.as<double>(), r,
+                                                                                        h->t.as<T>());
         TRY(launched());
-        k_spai_z<T, TG><<<dim3(gx_spmv(h, h->G), h->batch), NT, smem_for(TG), s>>>(
+        k_spai_z<T><<<dim3(gx_spmv(h, h->capG), h->batch), NT, spmv_smem(h->capG), s>>>(
             G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
         TRY(launched());
-        k_pupdate<T, 2, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
+        k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
         TRY(launched());
         *nodes += 5;
     } else if (pc == SLA_PC_JACOBI) {
-        k_update<T, 1><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        k_update<T, 1, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
         TRY(launched());
-        k_pupdate<T, 1, false><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
+        k_pupdate<T, 1, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
         TRY(launched());
         *nodes += 3;
     } else {
-        k_update<T, 0><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        k_update<T, 0, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
         TRY(launched());
-        k_pupdate<T, 0, false><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
+        k_pupdate<T, 0, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
         TRY(launched());
         *nodes += 3;
     }
@@ -417,12 +428,8 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
 
 template <typename T>
 static sla_status enqueue_iteration_any(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
-    sla_status st = SLA_OK;
-    const int tg = h->spai_ready ? h->G.tile : 1024;
-    with_tile(h->A.tile, [&](auto ta) {
-        with_tile(tg, [&](auto tgc) { st = enqueue_iteration<T, decltype(ta)::value, decltype(tgc)::value>(h, pc, eps, s, nodes); });
-    });
-    return st;
+    return pairs_ok(h) ? enqueue_iteration<T, true>(h, pc, eps, s, nodes)
+                       : enqueue_iteration<T, false>(h, pc, eps, s, nodes);
 }
 
 template <typename T>
@@ -479,9 +486,9 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     TRY(get_graph<T>(h, pc, eps, k, &gc));
 
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->A);
+    const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
     const T* av = (const T*)h->vals;
-    const dim3 gs(gx_spmv(h, h->A), h->batch), gv(gx_vec(h), h->batch);
+    const dim3 gs(gx_spmv(h, h->capA), h->batch), gv(gx_vec(h), h->batch);
     T* r = h->r.as<T>();
     T* p = h->p.as<T>();
     double* x = h->x.as<double>();
@@ -489,32 +496,23 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
 
     CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
     if (o->use_x0) {
-        with_tile(h->A.tile, [&](auto ta) {
-            constexpr int TA = decltype(ta)::value;
-            k_init_x0<T, TA><<<gs, NT, smem_for(TA), s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
-                                                          o->max_iter);
-        });
+        k_init_x0<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
+                                                         o->max_iter);
     } else {
         k_init<T><<<gv, NT, 0, s>>>(S, b, h->bw.as<T>(), x, r, o->tol, o->max_iter);
     }
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
-        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->GT);
-        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->G);
-        sla_status st = SLA_OK;
-        with_tile(h->G.tile, [&](auto tg) {
-            constexpr int TG = decltype(tg)::value;
-            k_spai_t<T, TG><<<dim3(gx_spmv(h, h->GT), h->batch), NT, smem_for(TG), s>>>(GT, S, h->nnzg,
-                                                                                        h->gtv.as<double>(), r,
-                                                                                        h->t.as<T>());
-            st = launched();
-            if (st != SLA_OK) return;
-            k_spai_z<T, TG><<<dim3(gx_spmv(h, h->G), h->batch), NT, smem_for(TG), s>>>(
-                G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
-            st = launched();
-        });
-        TRY(st);
-        k_pupdate<T, 2, true><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
+        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->capGT);
+        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->capG);
+        k_spai_t<T><<<dim3(gx_spmv(h, h->capGT), h->batch), NT, spmv_smem(h->capGT), s>>>(GT, S, h->nnzg,
+                                                                                       h->gtv.as<double>(), r,
+                                                                                       h->t.as<T>());
+        TRY(launched());
+        k_spai_z<T><<<dim3(gx_spmv(h, h->capG), h->batch), NT, spmv_smem(h->capG), s>>>(
+            G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+        TRY(launched());
+        k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
     } else if (pc == SLA_PC_JACOBI) {
         k_init_dir<T, 1><<<gv, NT, 0, s>>>(S, p, r, dinv);
     } else {
@@ -563,10 +561,7 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     // drain (kernels of a finished batch return at once)
     CU(cudaStreamSynchronize(s));
 
-    with_tile(h->A.tile, [&](auto ta) {
-        constexpr int TA = decltype(ta)::value;
-        k_final<T, TA><<<gs, NT, smem_for(TA), s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
-    });
+    k_final<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
     TRY(launched());
     CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
     CU(cudaStreamSynchronize(s));
@@ -622,8 +617,8 @@ static void destroy_handle(sla_csr* h) {
 
 sla_status sla_csr_destroy(sla_handle h) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
-    DevBuf* bufs[] = {&h->A.rbs, &h->diag, &h->dinv, &h->grp, &h->gci, &h->gv, &h->gtrp, &h->gtci, &h->gtv,
-                      &h->G.rbs, &h->GT.rbs, &h->x, &h->r, &h->p, &h->q, &h->z, &h->t, &h->bw, &h->state,
+    DevBuf* bufs[] = {&h->diag, &h->dinv, &h->grp, &h->gci, &h->gv, &h->gtrp, &h->gtci, &h->gtv,
+                      &h->x, &h->r, &h->p, &h->q, &h->z, &h->t, &h->bw, &h->state,
                       &h->ctl, &h->cnt, &h->part, &h->stat};
     for (DevBuf* b : bufs) b->release();
     destroy_handle(h);
@@ -671,7 +666,6 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
 
     HCU(cudaGetDevice(&h->device));
     HCU(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device));
-    HTRY(dt == SLA_F64 ? prepare_all<double>() : prepare_all<float>());
     HCU(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
     HCU(cudaEventCreateWithFlags(&h->ev[0], cudaEventDisableTiming));
     HCU(cudaEventCreateWithFlags(&h->ev[1], cudaEventDisableTiming));
@@ -693,7 +687,9 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
                              (e & ERR_COL_RANGE) ? " column out of range" : "",
                              (e & ERR_COL_ORDER) ? " columns not strictly ascending" : ""));
     }
-    HTRY(build_row_blocks(d_row_ptr, n, pick_tile(nnz, n), h->A, s));
+    HTRY(dt == SLA_F64 ? allow_smem<double>() : allow_smem<float>());
+    HTRY(staging_cap(d_row_ptr, n, &h->capA, s));
+    HTRY(spmv_grid_any(h, h->capA, &h->gxA));
     const size_t vn = (size_t)n * batch;
     HTRY(h->diag.alloc(sizeof(double) * vn));
     HTRY(h->dinv.alloc(sizeof(double) * vn));
@@ -735,17 +731,13 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     if (!d_x || !d_y) return fail(SLA_ERR_INVALID, "null vector");
     cudaStream_t s = (cudaStream_t)stream;
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->A);
-    const dim3 g(gx_spmv(h, h->A), h->batch);
-    with_tile(h->A.tile, [&](auto ta) {
-        constexpr int TA = decltype(ta)::value;
-        if (h->dt == SLA_F64)
-            k_spmv<double, TA><<<g, NT, smem_for(TA), s>>>(A, S, (const double*)h->vals, (const double*)d_x,
-                                                           (double*)d_y, d_dot);
-        else
-            k_spmv<float, TA><<<g, NT, smem_for(TA), s>>>(A, S, (const float*)h->vals, (const float*)d_x,
-                                                          (float*)d_y, d_dot);
-    });
+    const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
+    const dim3 g(gx_spmv(h, h->capA), h->batch);
+    const size_t sm = spmv_smem(h->capA);
+    if (h->dt == SLA_F64)
+        k_spmv<double><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_x, (double*)d_y, d_dot);
+    else
+        k_spmv<float><<<g, NT, sm, s>>>(A, S, (const float*)h->vals, (const float*)d_x, (float*)d_y, d_dot);
     return launched();
 }
 
@@ -793,17 +785,14 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
     if (st != SLA_OK && st != SLA_ERR_NOT_CONVERGED && st != SLA_ERR_BREAKDOWN && st != SLA_ERR_TIMEOUT) return st;
     if (d_dLdA && h->nnz > 0) {
         const Sys S = sys_of(h);
-        const Mat A = mat_of(h->rp, h->ci, h->A);
-        const dim3 g(gx_spmv(h, h->A), h->batch);
-        with_tile(h->A.tile, [&](auto ta) {
-            constexpr int TA = decltype(ta)::value;
-            if (h->dt == SLA_F64)
-                k_grad_A<double, TA><<<g, NT, TA * sizeof(int), s>>>(A, S, (const double*)d_dLdb,
-                                                                     (const double*)d_x, (double*)d_dLdA);
-            else
-                k_grad_A<float, TA><<<g, NT, TA * sizeof(int), s>>>(A, S, (const float*)d_dLdb,
-                                                                    (const float*)d_x, (float*)d_dLdA);
-        });
+        const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
+        const dim3 g(gx_spmv(h, h->capA), h->batch);
+        if (h->dt == SLA_F64)
+            k_grad_A<double><<<g, NT, grad_smem(h->capA), s>>>(A, S, (const double*)d_dLdb, (const double*)d_x,
+                                                               (double*)d_dLdA);
+        else
+            k_grad_A<float><<<g, NT, grad_smem(h->capA), s>>>(A, S, (const float*)d_dLdb, (const float*)d_x,
+                                                              (float*)d_dLdA);
         sla_status l = launched();
         if (l != SLA_OK) return l;
         CU(cudaStreamSynchronize(s));

@@ -50,7 +50,8 @@ def c1(N: int = 64) -> Workload:
     A = poisson_grid((N, N))
     x_star = rng.uniform_pm1(seed, 1, A.n)
     b = _csr_matvec_f64(A, x_star)
-    return Workload("c1", A, b, "f64", "none", 1e-10, x_star=x_star,
+    g = rng.normal(seed, 5, A.n)
+    return Workload("c1", A, b, "f64", "none", 1e-10, g=g, x_star=x_star,
                     info={"grid": (N, N)})
 
 
@@ -69,7 +70,7 @@ def c3(N: int = 256, batch: int = 64) -> Workload:
     n = N * N
     kc = np.exp(0.5 * rng.normal(seed, 2, batch * n)).reshape(batch, n)
     A = diffusion2d(N, kc)
-    A.vals = A.vals.astype(np.float32)
+    A.vals = np.ascontiguousarray(A.vals, dtype=np.float32)
     b = rng.uniform_pm1(seed, 1, batch * n).reshape(batch, n).astype(np.float32)
     g = rng.normal(seed, 5, batch * n).reshape(batch, n).astype(np.float32)
     return Workload("c3", A, b, "f32", "jacobi", 1e-5, g=g,

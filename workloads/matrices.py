@@ -124,9 +124,9 @@ def diffusion2d(N: int, k_cell: np.ndarray) -> CSR:
     row_ptr = np.zeros(n + 1, dtype=np.int64)
     np.cumsum(counts, out=row_ptr[1:])
     col_idx = cols[valid].astype(np.int32)
-    v = vals[:, valid]                              # [B, nnz], row-major order
+    v = np.ascontiguousarray(vals[:, valid])        # [B, nnz], row-major order
     if np.asarray(k_cell).ndim == 1:
-        v = v[0]
+        v = np.ascontiguousarray(v[0])
     return CSR(n, row_ptr.astype(np.int32), col_idx, v,
                meta={"kind": "diffusion2d", "dims": (N, N)})
 
