@@ -336,7 +336,8 @@ def main():
     src = kernel_source_hash()
     traffic = recorded_traffic(args.config, "k_spmv", src)
 
-    per_it_gbs = bm["per_iteration"] * iters / (ms * 1e-3) / 1e9
+    # bytes of one system's iteration (a batched iteration moves B of them)
+    per_it_gbs = bm["per_iteration"] / A.batch * iters / (ms * 1e-3) / 1e9
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (values, b, g) from pinned memory, solve + adjoint, D2H of x,

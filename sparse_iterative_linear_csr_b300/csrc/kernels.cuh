@@ -1,20 +1,26 @@
 // kernels.cuh -- the PCG iteration, set-up and adjoint kernels.
 //
-// Batches: blockIdx.y is the system.  All systems share row_ptr / col_idx
-// and the row-block partition; values, vectors, solver state, partial sums
-// and arrival counters are offset per system.  A converged system's CTAs
-// return at once, so frozen systems cost no memory traffic.
+// Batches: blockIdx.y is the system.  All systems share row_ptr / col_idx;
+// values, vectors, solver state, partial sums and arrival counters are
+// offset per system.  A converged system's CTAs return at once, so frozen
+// systems cost no memory traffic.
 //
-// SpMV layout (spmv_rows): one warp per group of 32 consecutive rows; the
-// warp stages its non-zeros in shared memory, then each lane forms its row
-// sum with one fp64 fused multiply-add per non-zero.  One FMA per non-zero is
-// the least fp64 work an SpMV can do, which matters on a part whose fp64 rate
-// is low next to its memory bandwidth.
+// Precision (Prec<T>, T = stored vector type):
+//  * fp64 systems compute in fp64: one fused multiply-add per stored entry
+//    in the SpMV (the least fp64 work an SpMV can do -- B300's fp64 pipe
+//    issues at 1/64 of its fp32 rate), fp64 updates and dot products.
+//  * fp32 systems store A, b, r, p, q, z, t in fp32 and keep x and the
+//    Jacobi reciprocal as double-float pairs (df.cuh).  All element-wise
+//    arithmetic is double-float on the fp32 pipe: products of fp32 values
+//    are exact and sums carry ~48 bits before each stored vector is rounded
+//    to fp32.  Only per-thread totals and the solver scalars use fp64.
 //
-// Grids are persistent in x (warps / CTAs walk row groups / vector ranges
-// with a grid stride).  Inner products are reduced in a fixed order (grid_sum) and
-// the last CTA to finish updates that system's scalars on the device, so no
-// host round trip sits inside an iteration.
+// SpMV layout (spmv_rows / spmv_rows_async): one warp per group of 32
+// consecutive rows; the warp stages its non-zeros in its own shared-memory
+// slice, then each lane sums its own row.  Grids are persistent in x.
+// Inner products are reduced in a fixed order (grid_sum) and the last CTA to
+// finish updates that system's scalars on the device, so no host round trip
+// sits inside an iteration.
 //
 // CG step order (torch-sla §3.3, distributed CG; Hestenes-Stiefel order):
 //   k_spmv_iter:  q = A p, delta = p.q -> alpha = rho / delta  (and, when the
@@ -25,6 +31,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "df.cuh"
 
 namespace sla {
 
@@ -57,38 +64,105 @@ struct Mat {
     const size_t ao = (size_t)sys * S.nnz;                      \
     (void)st; (void)part; (void)cnt; (void)vo; (void)ao;
 
+// ----------------------------------------------------------------- precision
+template <typename T> struct Prec;
+template <> struct Prec<double> {
+    using acc = double;   // row sums and inner products
+    using xw = double;    // stored iterate x and Jacobi reciprocal
+    using gv = double;    // SPAI factor values
+    using sc = double;    // broadcast solver scalars
+    static __device__ __forceinline__ acc zero() { return 0.0; }
+    static __device__ __forceinline__ double total(acc a) { return a; }
+    static __device__ __forceinline__ sc scal(double v) { return v; }
+};
+template <> struct Prec<float> {
+    using acc = DF;
+    using xw = float2;    // (hi, lo) pair in an 8-byte slot
+    using gv = float2;
+    using sc = DF;
+    static __device__ __forceinline__ acc zero() { return DF{0.0f, 0.0f}; }
+    static __device__ __forceinline__ double total(acc a) { return df_to_double(a); }
+    static __device__ __forceinline__ sc scal(double v) { return df_from_double(v); }
+};
+
+// acc += a * v
+__device__ __forceinline__ void mac(double& s, double a, double v) { s = fma(a, v, s); }
+__device__ __forceinline__ void mac(DF& s, float a, float v) { s = df_fma_ff(a, v, s); }
+__device__ __forceinline__ void mac(DF& s, float2 g, float v) { s = df_fma_df(DF{g.x, g.y}, v, s); }
+
+// stored value nearest to an accumulator
+__device__ __forceinline__ double to_store(double s) { return s; }
+__device__ __forceinline__ float to_store(DF s) { return df_round(s); }
+
+// x value seen by the true-residual check (the returned precision)
+__device__ __forceinline__ double x_out_of(double x) { return x; }
+__device__ __forceinline__ float x_out_of(float2 x) { return __fadd_rn(x.x, x.y); }
+
 // ----------------------------------------------------------------- gathers
 template <typename T>
 struct GatherVec {  // vector entry at the system precision
     const T* v;
-    __device__ __forceinline__ double operator()(int c) const { return (double)ld_nc(v + c); }
+    __device__ __forceinline__ T operator()(int c) const { return ld_nc(v + c); }
 };
 template <typename T>
-struct GatherRounded {  // fp64 iterate rounded to the returned precision
-    const double* v;
-    __device__ __forceinline__ double operator()(int c) const { return rnd<T>(ld_nc(v + c)); }
+struct GatherX {    // stored iterate, rounded to the returned precision
+    const typename Prec<T>::xw* v;
+    __device__ __forceinline__ T operator()(int c) const { return x_out_of(ld_nc(v + c)); }
 };
+
+__device__ __forceinline__ double acc_xor(double t, int o) { return __shfl_xor_sync(0xffffffffu, t, o); }
+__device__ __forceinline__ DF acc_xor(DF t, int o) {
+    return DF{__shfl_xor_sync(0xffffffffu, t.hi, o), __shfl_xor_sync(0xffffffffu, t.lo, o)};
+}
+__device__ __forceinline__ void acc_add(double& a, double b) { a += b; }
+__device__ __forceinline__ void acc_add(DF& a, DF b) { a = df_add(a, b); }
 
 // Rows are taken in groups of 32, one warp per group (grid stride over
 // groups).  The warp stages its group's non-zeros -- values streamed with
 // coalesced evict-first loads, the vector entries they address gathered
-// through the read-only path -- as (value, entry) pairs in its own slice of
-// shared memory (`cap` pairs), then each lane sums its own row with one fp64
-// FMA per non-zero.  Only __syncwarp orders the two phases, so warps progress
+// through the read-only path -- in its own slice of shared memory (`cap`
+// entries), then each lane sums its own row (one fp64 FMA per entry for
+// fp64 systems).  Only __syncwarp orders the two phases, so warps progress
 // independently and hide each other's memory latency.  A group with more than
-// `cap` non-zeros is summed straight from global memory: rows up to LONG
+// `cap` non-zeros is summed straight from global memory: rows up to LONG_ROW
 // entries by their lane, longer rows by the whole warp.
 // epi(row, sum) is called once per row of the matrix by the row's lane.
 constexpr int STAGE_U = 4;     // entries per lane in flight while staging
 constexpr int LONG_ROW = 64;   // longer rows of an unstaged group go warp-wide
 
-template <typename VT, class Gather, class Epi>
+// Rows of a group that did not fit the stage, summed from global memory.
+template <typename T, typename VT, class Gather>
+__device__ __forceinline__ typename Prec<T>::acc unstaged_row(const Mat& A, const VT* __restrict__ av,
+                                                              Gather gather, int rlo, int rhi) {
+    using acc_t = typename Prec<T>::acc;
+    const int lane = threadIdx.x & 31;
+    acc_t s = Prec<T>::zero();
+    if (rhi - rlo <= LONG_ROW)
+        for (int k = rlo; k < rhi; ++k) mac(s, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+    unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW);
+    while (longs) {
+        const int src = __ffs(longs) - 1;
+        longs &= longs - 1;
+        const int a0 = __shfl_sync(0xffffffffu, rlo, src);
+        const int a1 = __shfl_sync(0xffffffffu, rhi, src);
+        acc_t t = Prec<T>::zero();
+        for (int k = a0 + lane; k < a1; k += 32) mac(t, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc_add(t, acc_xor(t, o));
+        if (lane == src) s = t;
+    }
+    return s;
+}
+
+template <typename T, typename VT, class Gather, class Epi>
 __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ av, Gather gather, Epi epi,
                                           double* wsm) {
+    using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
     const int cap = A.cap;
-    double* sa = wsm + (threadIdx.x >> 5) * A.wstride;
-    double* sx = sa + cap;
+    char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
+    VT* sa = reinterpret_cast<VT*>(base);
+    T* sx = reinterpret_cast<T*>(base + cap * sizeof(VT));
     const int ngroups = (A.n + 31) >> 5;
     const int nwarps = (gridDim.x * NT) >> 5;
     for (int grp = (blockIdx.x * NT + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
@@ -98,79 +172,65 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
         const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt = k1 - k0;
-        double s = 0.0;
+        acc_t s = Prec<T>::zero();
         if (cnt <= cap) {
-            for (int base = 0; base < cnt; base += 32 * STAGE_U) {
+            for (int b0 = 0; b0 < cnt; b0 += 32 * STAGE_U) {
                 int c[STAGE_U];
-                double a[STAGE_U], xv[STAGE_U];
+                VT a[STAGE_U];
+                T xv[STAGE_U];
 #pragma unroll
                 for (int j = 0; j < STAGE_U; ++j) {
-                    const int e = base + j * 32 + lane;
+                    const int e = b0 + j * 32 + lane;
                     if (e < cnt) {
                         c[j] = ld_stream(A.ci + k0 + e);
-                        a[j] = (double)ld_stream(av + k0 + e);
+                        a[j] = ld_stream(av + k0 + e);
                     }
                 }
 #pragma unroll
                 for (int j = 0; j < STAGE_U; ++j) {
-                    const int e = base + j * 32 + lane;
+                    const int e = b0 + j * 32 + lane;
                     if (e < cnt) xv[j] = gather(c[j]);
                 }
 #pragma unroll
                 for (int j = 0; j < STAGE_U; ++j) {
-                    const int e = base + j * 32 + lane;
+                    const int e = b0 + j * 32 + lane;
                     if (e < cnt) { sa[e] = a[j]; sx[e] = xv[j]; }
                 }
             }
             __syncwarp();
-            for (int e = rlo - k0; e < rhi - k0; ++e) s = fma(sa[e], sx[e], s);
+            for (int e = rlo - k0; e < rhi - k0; ++e) mac(s, sa[e], sx[e]);
             __syncwarp();
         } else {
-            if (rhi - rlo <= LONG_ROW)
-                for (int k = rlo; k < rhi; ++k) s = fma((double)ld_stream(av + k), gather(ld_stream(A.ci + k)), s);
-            unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW);
-            while (longs) {
-                const int src = __ffs(longs) - 1;
-                longs &= longs - 1;
-                const int a0 = __shfl_sync(0xffffffffu, rlo, src);
-                const int a1 = __shfl_sync(0xffffffffu, rhi, src);
-                double t = 0.0;
-                for (int k = a0 + lane; k < a1; k += 32)
-                    t = fma((double)ld_stream(av + k), gather(ld_stream(A.ci + k)), t);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                if (lane == src) s = t;
-            }
+            s = unstaged_row<T>(A, av, gather, rlo, rhi);
         }
         if (row < A.n) epi(row, s);
     }
 }
 
-// Pipelined form of spmv_rows for a plain vector gather (v[col] at its stored
-// precision).  Each warp double-buffers its groups' values and column
-// indices in shared memory with cp.async: the copies of the next group are in
-// flight while the warp gathers and sums the current one, so every warp keeps
-// ~12 bytes x (entries per group) of streaming traffic outstanding without
-// holding registers for it.  The gathered entries go through registers
-// (GATHER_U per lane in flight) into the warp's slice, then each lane sums
-// its own row with one fp64 FMA per entry.  Shared memory per warp:
-// 2*cap*(sizeof(VT) + 4) + 8*cap bytes (async_smem_per_warp).
+// Pipelined form of spmv_rows for a plain vector gather.  Each warp
+// double-buffers its groups' values and column indices in shared memory with
+// cp.async: the copies of the next group are in flight while the warp gathers
+// and sums the current one, so every warp keeps the next group's streaming
+// traffic outstanding without holding registers for it.  The gathered entries
+// go through registers (GATHER_U per lane in flight) into the warp's slice.
+// Shared memory per warp: 2*cap*(sizeof(VT) + 4) + cap*sizeof(T).
 constexpr int GATHER_U = 8;
 
-template <typename VT>
+template <typename VT, typename T>
 __host__ __device__ constexpr size_t async_smem_per_warp(int cap) {
-    return (size_t)2 * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(double);
+    return (size_t)2 * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
-template <typename VT, typename T, class Epi>
+template <typename T, typename VT, class Epi>
 __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v,
                                                 Epi epi, double* wsm) {
+    using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
     const int cap = A.cap;
     char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
     VT* sv = reinterpret_cast<VT*>(base);
     int* sc = reinterpret_cast<int*>(base + 2 * cap * sizeof(VT));
-    double* sx = reinterpret_cast<double*>(base + 2 * cap * (sizeof(VT) + sizeof(int)));
+    T* sx = reinterpret_cast<T*>(base + 2 * cap * (sizeof(VT) + sizeof(int)));
     const unsigned long long pol = l2_evict_first();
     const int ngroups = (A.n + 31) >> 5;
     const int nwarps = (gridDim.x * NT) >> 5;
@@ -204,16 +264,16 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
         const int cnt = k1 - k0;
         cp_wait<1>();  // this group's values and columns have landed
         __syncwarp();
-        double s = 0.0;
+        acc_t s = Prec<T>::zero();
         if (cnt <= cap) {
             const VT* cv = sv + stage * cap;
             const int* cc = sc + stage * cap;
             for (int b0 = 0; b0 < cnt; b0 += 32 * GATHER_U) {
-                double xv[GATHER_U];
+                T xv[GATHER_U];
 #pragma unroll
                 for (int j = 0; j < GATHER_U; ++j) {
                     const int e = b0 + j * 32 + lane;
-                    if (e < cnt) xv[j] = (double)ld_nc(v + cc[e]);
+                    if (e < cnt) xv[j] = ld_nc(v + cc[e]);
                 }
 #pragma unroll
                 for (int j = 0; j < GATHER_U; ++j) {
@@ -222,23 +282,9 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
                 }
             }
             __syncwarp();
-            for (int e = rlo - k0; e < rhi - k0; ++e) s = fma((double)cv[e], sx[e], s);
+            for (int e = rlo - k0; e < rhi - k0; ++e) mac(s, cv[e], sx[e]);
         } else {
-            if (rhi - rlo <= LONG_ROW)
-                for (int k = rlo; k < rhi; ++k) s = fma((double)ld_stream(av + k), (double)ld_nc(v + ld_stream(A.ci + k)), s);
-            unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW);
-            while (longs) {
-                const int src = __ffs(longs) - 1;
-                longs &= longs - 1;
-                const int a0 = __shfl_sync(0xffffffffu, rlo, src);
-                const int a1 = __shfl_sync(0xffffffffu, rhi, src);
-                double t = 0.0;
-                for (int k = a0 + lane; k < a1; k += 32)
-                    t = fma((double)ld_stream(av + k), (double)ld_nc(v + ld_stream(A.ci + k)), t);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                if (lane == src) s = t;
-            }
+            s = unstaged_row<T>(A, av, GatherVec<T>{v}, rlo, rhi);
         }
         __syncwarp();  // this stage and sx are free for reuse
         if (row < A.n) epi(row, s);
@@ -248,11 +294,11 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
 
 // Product with a plain vector gather: the pipelined form when the matrix was
 // set up for it, the single-stage form otherwise.
-template <typename VT, typename T, class Epi>
+template <typename T, typename VT, class Epi>
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v, Epi epi,
                                          double* wsm) {
-    if (A.async) spmv_rows_async<VT>(A, av, v, epi, wsm);
-    else spmv_rows<VT>(A, av, GatherVec<T>{v}, epi, wsm);
+    if (A.async) spmv_rows_async<T, VT>(A, av, v, epi, wsm);
+    else spmv_rows<T, VT>(A, av, GatherVec<T>{v}, epi, wsm);
 }
 
 // ----------------------------------------------------------------- scalar logic
@@ -320,25 +366,76 @@ __device__ __forceinline__ void start_state(State* s, Ctrl* c, double bb, double
     if (!s->check && max_iter <= 0) freeze(s, c, ST_NOT_CONVERGED);
 }
 
+// ----------------------------------------------------------------- element-wise arithmetic
+// acc += a * b for stored values
+__device__ __forceinline__ void dot_acc(double& s, double a, double b) { s = fma(a, b, s); }
+__device__ __forceinline__ void dot_acc(DF& s, float a, float b) { s = df_fma_ff(a, b, s); }
+
+// b - s for a row sum s
+__device__ __forceinline__ double resid(double b, double s) { return b - s; }
+__device__ __forceinline__ DF resid(float b, DF s) { return df_add_f(df_neg(s), b); }
+__device__ __forceinline__ void sq_acc(double& t, double e) { t = fma(e, e, t); }
+__device__ __forceinline__ void sq_acc(DF& t, DF e) { t = df_add(t, df_sqr(e)); }
+
+// One element of the x / r update.  x += alpha p; r = rnd(r - alpha q);
+// g += r^2; (Jacobi) rz += r rnd(r dinv).
+template <int PC>
+__device__ __forceinline__ void update_one(double alpha, double& x, double& r, double p, double q, double dinv,
+                                           double& g, double& rz) {
+    x = fma(alpha, p, x);
+    r = fma(-alpha, q, r);
+    g = fma(r, r, g);
+    if (PC == 1) rz = fma(r, r * dinv, rz);
+}
+template <int PC>
+__device__ __forceinline__ void update_one(DF alpha, float2& x, float& r, float p, float q, float2 dinv, DF& g,
+                                           DF& rz) {
+    const DF xn = df_add(DF{x.x, x.y}, df_mul_f(alpha, p));
+    x = make_float2(xn.hi, xn.lo);
+    r = df_round(df_add_f(df_neg(df_mul_f(alpha, q)), r));
+    g = df_fma_ff(r, r, g);
+    if (PC == 1) {
+        const float z = df_round(df_mul_f(DF{dinv.x, dinv.y}, r));
+        rz = df_fma_ff(r, z, rz);
+    }
+}
+
+// Jacobi z = rnd(r dinv)
+__device__ __forceinline__ double jacobi_z(double r, double dinv) { return r * dinv; }
+__device__ __forceinline__ float jacobi_z(float r, float2 dinv) { return df_round(df_mul_f(DF{dinv.x, dinv.y}, r)); }
+
+// p = rnd(z + beta p)
+__device__ __forceinline__ double p_step(double beta, double p, double z) { return fma(beta, p, z); }
+__device__ __forceinline__ float p_step(DF beta, float p, float z) { return df_round(df_add_f(df_mul_f(beta, p), z)); }
+
+// z = rnd(s + eps r)
+__device__ __forceinline__ double spai_z(double s, double eps, double r) { return fma(eps, r, s); }
+__device__ __forceinline__ float spai_z(DF s, DF eps, float r) { return df_round(df_add(s, df_mul_f(eps, r))); }
+
+// -lambda_i x_j, rounded once
+__device__ __forceinline__ double neg_prod(double l, double x) { return -l * x; }
+__device__ __forceinline__ float neg_prod(float l, float x) { return df_round(two_prod(-l, x)); }
+
 // ----------------------------------------------------------------- SpMV API
 // y = A x, and dot[sys] = x.y when dot != nullptr.
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ x,
-                                             T* __restrict__ y, double* dot) {
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const T* __restrict__ av,
+                                                            const T* __restrict__ x, T* __restrict__ y, double* dot) {
+    using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     av += ao; x += vo; y += vo;
-    double acc = 0.0;
-    spmv_vec<T>(A, av, x,
-                 [&](int i, double s) {
-                     const T yi = (T)s;
-                     y[i] = yi;
-                     acc = fma((double)x[i], (double)yi, acc);
-                 },
-                 dsm);
+    acc_t acc = Prec<T>::zero();
+    spmv_vec<T, T>(A, av, x,
+                   [&](int i, acc_t s) {
+                       const T yi = to_store(s);
+                       y[i] = yi;
+                       dot_acc(acc, x[i], yi);
+                   },
+                   dsm);
     if (dot) {
-        double v[1] = {acc}, tot[1];
+        double v[1] = {Prec<T>::total(acc)}, tot[1];
         if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) dot[sys] = tot[0];
     }
 }
@@ -346,32 +443,28 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
 // ----------------------------------------------------------------- iteration
 // q = A p, delta = p.q; with `check` set, ||b - A round(x)||^2 first.
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ p,
-                                                  T* __restrict__ q, const double* __restrict__ x,
-                                                  const T* __restrict__ b) {
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
+    k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ p, T* __restrict__ q,
+                const typename Prec<T>::xw* __restrict__ x, const T* __restrict__ b) {
+    using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     av += ao; p += vo; q += vo; x += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
-    double tr2 = 0.0, delta = 0.0;
+    acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
     if (check) {
-        spmv_rows<T>(A, av, GatherRounded<T>{x},
-                     [&](int i, double s) {
-                         const double e = (double)b[i] - s;
-                         tr2 = fma(e, e, tr2);
-                     },
-                     dsm);
+        spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i, acc_t s) { sq_acc(tr2, resid(b[i], s)); }, dsm);
     }
-    spmv_vec<T>(A, av, p,
-                 [&](int i, double s) {
-                     const T qi = (T)s;
-                     q[i] = qi;
-                     delta = fma((double)p[i], (double)qi, delta);
-                 },
-                 dsm);
-    double v[2] = {delta, tr2}, tot[2];
+    spmv_vec<T, T>(A, av, p,
+                   [&](int i, acc_t s) {
+                       const T qi = to_store(s);
+                       q[i] = qi;
+                       dot_acc(delta, p[i], qi);
+                   },
+                   dsm);
+    double v[2] = {Prec<T>::total(delta), Prec<T>::total(tr2)}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0) after_spmv(st, S.ctl, tot[0], check, tot[1]);
 }
 
@@ -380,108 +473,120 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv_iter(Mat A, Sys S, c
 template <typename T> struct Pair;
 template <> struct Pair<double> { using type = double2; };
 template <> struct Pair<float> { using type = float2; };
+template <typename X> struct XPair;
+template <> struct XPair<double> { using type = double2; };
+template <> struct XPair<float2> { using type = float4; };
+
+__device__ __forceinline__ void split2(double2 v, double& a, double& b) { a = v.x; b = v.y; }
+__device__ __forceinline__ void split2(float4 v, float2& a, float2& b) {
+    a = make_float2(v.x, v.y);
+    b = make_float2(v.z, v.w);
+}
+__device__ __forceinline__ double2 join2(double a, double b) { return make_double2(a, b); }
+__device__ __forceinline__ float4 join2(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
 
 // x += alpha p; r -= alpha q; gamma = r.r; rho' = r.z (PC 0: z = r, PC 1:
 // z = r / A_ii; PC 2: z comes later from the SPAI kernels).
-template <typename T, int PC>
-__device__ __forceinline__ void update_one(double alpha, double& x, T& r, double p, double q, double dinv,
-                                           double& g, double& rz) {
-    x = fma(alpha, p, x);
-    const double ri = rnd<T>(fma(-alpha, q, (double)r));
-    r = (T)ri;
-    g = fma(ri, ri, g);
-    if (PC == 1) rz = fma(ri, rnd<T>(ri * dinv), rz);
-}
-
 template <typename T, int PC, bool PAIRS>
-__global__ void __launch_bounds__(NT) k_update(Sys S, double* __restrict__ x, T* __restrict__ r,
+__global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __restrict__ x, T* __restrict__ r,
                                                const T* __restrict__ p, const T* __restrict__ q,
-                                               const double* __restrict__ dinv) {
+                                               const typename Prec<T>::xw* __restrict__ dinv) {
+    using acc_t = typename Prec<T>::acc;
+    using XW = typename Prec<T>::xw;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     __shared__ double red[2 * NWARP];
     x += vo; r += vo; p += vo; q += vo;
     if (PC == 1) dinv += vo;
-    const double alpha = ld_cg(&st->alpha);
-    double g = 0.0, rz = 0.0;
+    const typename Prec<T>::sc alpha = Prec<T>::scal(ld_cg(&st->alpha));
+    acc_t g = Prec<T>::zero(), rz = Prec<T>::zero();
     if (PAIRS) {
         // two pairs per thread per trip, all loads issued before any use
         using P2 = typename Pair<T>::type;
+        using X2 = typename XPair<XW>::type;
         const int n2 = S.n >> 1;
         const int stride = gridDim.x * NT;
         for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += 2 * stride) {
             P2 p2[2], q2[2], r2[2];
-            double2 x2[2], d2[2];
+            X2 x2[2], d2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
                     p2[u] = ld_stream(reinterpret_cast<const P2*>(p) + i);
                     q2[u] = ld_stream(reinterpret_cast<const P2*>(q) + i);
-                    x2[u] = reinterpret_cast<const double2*>(x)[i];
+                    x2[u] = reinterpret_cast<const X2*>(x)[i];
                     r2[u] = reinterpret_cast<const P2*>(r)[i];
-                    d2[u] = PC == 1 ? ld_stream(reinterpret_cast<const double2*>(dinv) + i) : make_double2(0.0, 0.0);
+                    if (PC == 1) d2[u] = ld_stream(reinterpret_cast<const X2*>(dinv) + i);
                 }
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    update_one<T, PC>(alpha, x2[u].x, r2[u].x, (double)p2[u].x, (double)q2[u].x, d2[u].x, g, rz);
-                    update_one<T, PC>(alpha, x2[u].y, r2[u].y, (double)p2[u].y, (double)q2[u].y, d2[u].y, g, rz);
-                    reinterpret_cast<double2*>(x)[i] = x2[u];
+                    XW xa, xb, da{}, db{};
+                    split2(x2[u], xa, xb);
+                    if (PC == 1) split2(d2[u], da, db);
+                    T ra = r2[u].x, rb = r2[u].y;
+                    update_one<PC>(alpha, xa, ra, p2[u].x, q2[u].x, da, g, rz);
+                    update_one<PC>(alpha, xb, rb, p2[u].y, q2[u].y, db, g, rz);
+                    reinterpret_cast<X2*>(x)[i] = join2(xa, xb);
+                    r2[u].x = ra;
+                    r2[u].y = rb;
                     reinterpret_cast<P2*>(r)[i] = r2[u];
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-            double xi = x[i];
+            XW xi = x[i];
             T ri = r[i];
-            update_one<T, PC>(alpha, xi, ri, (double)ld_stream(p + i), (double)ld_stream(q + i),
-                              PC == 1 ? dinv[i] : 0.0, g, rz);
+            update_one<PC>(alpha, xi, ri, ld_stream(p + i), ld_stream(q + i), PC == 1 ? dinv[i] : XW{}, g, rz);
             x[i] = xi;
             r[i] = ri;
         }
     }
-    double v[2] = {g, rz}, tot[2];
+    double v[2] = {Prec<T>::total(g), Prec<T>::total(rz)}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0)
         after_update(st, S.ctl, tot[0], PC != 2, PC == 0 ? tot[0] : tot[1]);
 }
 
 // p = z + beta p   (INIT: p = z)
 template <typename T, int PC, bool INIT>
-__device__ __forceinline__ T pnew(double beta, double p, double r, double dinv, double z) {
-    double zi;
+__device__ __forceinline__ T pnew(typename Prec<T>::sc beta, T p, T r, typename Prec<T>::xw dinv, T z) {
+    T zi;
     if (PC == 0) zi = r;
-    else if (PC == 1) zi = rnd<T>(r * dinv);
+    else if (PC == 1) zi = jacobi_z(r, dinv);
     else zi = z;
-    return INIT ? (T)zi : (T)fma(beta, p, zi);
+    return INIT ? zi : p_step(beta, p, zi);
 }
 
 template <typename T, int PC, bool INIT, bool PAIRS>
 __global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const T* __restrict__ r,
-                                                const T* __restrict__ z, const double* __restrict__ dinv) {
+                                                const T* __restrict__ z,
+                                                const typename Prec<T>::xw* __restrict__ dinv) {
+    using XW = typename Prec<T>::xw;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     p += vo; r += vo;
     if (PC == 1) dinv += vo;
     if (PC == 2) z += vo;
-    const double beta = INIT ? 0.0 : ld_cg(&st->beta);
+    const typename Prec<T>::sc beta = Prec<T>::scal(INIT ? 0.0 : ld_cg(&st->beta));
     if (PAIRS) {
         using P2 = typename Pair<T>::type;
+        using X2 = typename XPair<XW>::type;
         const int n2 = S.n >> 1;
         const int stride = gridDim.x * NT;
         for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += 2 * stride) {
             P2 r2[2], p2[2], z2[2];
-            double2 d2[2];
+            X2 d2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
                     r2[u] = ld_stream(reinterpret_cast<const P2*>(r) + i);
                     p2[u] = INIT ? P2{} : reinterpret_cast<const P2*>(p)[i];
-                    d2[u] = PC == 1 ? ld_stream(reinterpret_cast<const double2*>(dinv) + i) : make_double2(0.0, 0.0);
+                    if (PC == 1) d2[u] = ld_stream(reinterpret_cast<const X2*>(dinv) + i);
                     z2[u] = PC == 2 ? ld_stream(reinterpret_cast<const P2*>(z) + i) : P2{};
                 }
             }
@@ -489,51 +594,58 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const 
             for (int u = 0; u < 2; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    p2[u].x = pnew<T, PC, INIT>(beta, (double)p2[u].x, (double)r2[u].x, d2[u].x, (double)z2[u].x);
-                    p2[u].y = pnew<T, PC, INIT>(beta, (double)p2[u].y, (double)r2[u].y, d2[u].y, (double)z2[u].y);
+                    XW da{}, db{};
+                    if (PC == 1) split2(d2[u], da, db);
+                    p2[u].x = pnew<T, PC, INIT>(beta, p2[u].x, r2[u].x, da, z2[u].x);
+                    p2[u].y = pnew<T, PC, INIT>(beta, p2[u].y, r2[u].y, db, z2[u].y);
                     reinterpret_cast<P2*>(p)[i] = p2[u];
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT)
-            p[i] = pnew<T, PC, INIT>(beta, INIT ? 0.0 : (double)p[i], (double)r[i], PC == 1 ? dinv[i] : 0.0,
-                                     PC == 2 ? (double)z[i] : 0.0);
+            p[i] = pnew<T, PC, INIT>(beta, INIT ? T(0) : p[i], r[i], PC == 1 ? dinv[i] : XW{},
+                                     PC == 2 ? z[i] : T(0));
     }
 }
 
 // SPAI, first product: t = G^T r (explicit transposed CSR of G; G values
 // are per system, [batch][nnz(G)]).
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, long long nnzg, const double* __restrict__ gtv,
-                                               const T* __restrict__ r, T* __restrict__ t) {
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, long long nnzg,
+                                                              const typename Prec<T>::gv* __restrict__ gtv,
+                                                              const T* __restrict__ r, T* __restrict__ t) {
+    using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
-    spmv_vec<double>(GT, gtv, r, [&](int i, double s) { t[i] = (T)s; }, dsm);
+    spmv_vec<T, typename Prec<T>::gv>(GT, gtv, r, [&](int i, acc_t s) { t[i] = to_store(s); }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long long nnzg, const double* __restrict__ gv,
-                                               const T* __restrict__ t, const T* __restrict__ r,
-                                               T* __restrict__ z, double eps) {
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long long nnzg,
+                                                              const typename Prec<T>::gv* __restrict__ gv,
+                                                              const T* __restrict__ t, const T* __restrict__ r,
+                                                              T* __restrict__ z, double eps) {
+    using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
-    double rz = 0.0;
-    spmv_vec<double>(G, gv, t,
-                      [&](int i, double s) {
-                          const double ri = (double)r[i];
-                          const double zi = rnd<T>(fma(eps, ri, s));
-                          z[i] = (T)zi;
-                          rz = fma(ri, zi, rz);
-                      },
-                      dsm);
-    double v[1] = {rz}, tot[1];
+    const typename Prec<T>::sc e = Prec<T>::scal(eps);
+    acc_t rz = Prec<T>::zero();
+    spmv_vec<T, typename Prec<T>::gv>(G, gv, t,
+                                      [&](int i, acc_t s) {
+                                          const T ri = r[i];
+                                          const T zi = spai_z(s, e, ri);
+                                          z[i] = zi;
+                                          dot_acc(rz, ri, zi);
+                                      },
+                                      dsm);
+    double v[1] = {Prec<T>::total(rz)}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) new_direction(st, S.ctl, tot[0]);
 }
 
@@ -541,46 +653,50 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long
 // x = 0, r = b, b copied into the workspace, bb = b.b.
 template <typename T>
 __global__ void __launch_bounds__(NT) k_init(Sys S, const T* __restrict__ b_user, T* __restrict__ bw,
-                                             double* __restrict__ x, T* __restrict__ r, double tol, int max_iter) {
+                                             typename Prec<T>::xw* __restrict__ x, T* __restrict__ r, double tol,
+                                             int max_iter) {
     SYS_PROLOGUE
     __shared__ double red[2 * NWARP];
     b_user += vo; bw += vo; x += vo; r += vo;
-    double bb = 0.0;
+    typename Prec<T>::acc bb = Prec<T>::zero();
     for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
         const T bi = b_user[i];
         bw[i] = bi;
         r[i] = bi;
-        x[i] = 0.0;
-        bb = fma((double)bi, (double)bi, bb);
+        x[i] = typename Prec<T>::xw{};
+        dot_acc(bb, bi, bi);
     }
-    double v[1] = {bb}, tot[1];
+    double v[1] = {Prec<T>::total(bb)}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0)
         start_state(st, S.ctl, tot[0], tot[0], tol, max_iter);
 }
 
+__device__ __forceinline__ double x_from(double v) { return v; }
+__device__ __forceinline__ float2 x_from(float v) { return make_float2(v, 0.0f); }
+
 // With an initial guess: x = x0, r = b - A x0, bb = b.b, gamma = r.r.
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_init_x0(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ b_user,
-                                                const T* __restrict__ x0, T* __restrict__ bw,
-                                                double* __restrict__ x, T* __restrict__ r, double tol,
-                                                int max_iter) {
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
+    k_init_x0(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ b_user, const T* __restrict__ x0,
+              T* __restrict__ bw, typename Prec<T>::xw* __restrict__ x, T* __restrict__ r, double tol, int max_iter) {
+    using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     av += ao; b_user += vo; x0 += vo; bw += vo; x += vo; r += vo;
-    double bb = 0.0, g = 0.0;
-    spmv_rows<T>(A, av, GatherVec<T>{x0},
-                 [&](int i, double s) {
-                     const T bi = b_user[i];
-                     bw[i] = bi;
-                     x[i] = (double)x0[i];
-                     const double ri = rnd<T>((double)bi - s);
-                     r[i] = (T)ri;
-                     bb = fma((double)bi, (double)bi, bb);
-                     g = fma(ri, ri, g);
-                 },
-                 dsm);
-    double v[2] = {bb, g}, tot[2];
+    acc_t bb = Prec<T>::zero(), g = Prec<T>::zero();
+    spmv_rows<T, T>(A, av, GatherVec<T>{x0},
+                    [&](int i, acc_t s) {
+                        const T bi = b_user[i];
+                        bw[i] = bi;
+                        x[i] = x_from(x0[i]);
+                        const T ri = to_store(resid(bi, s));
+                        r[i] = ri;
+                        dot_acc(bb, bi, bi);
+                        dot_acc(g, ri, ri);
+                    },
+                    dsm);
+    double v[2] = {Prec<T>::total(bb), Prec<T>::total(g)}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0)
         start_state(st, S.ctl, tot[0], tot[1], tol, max_iter);
 }
@@ -588,20 +704,20 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_init_x0(Mat A, Sys S, con
 // First direction for PC 0 / 1: p = z, rho = r.z.
 template <typename T, int PC>
 __global__ void __launch_bounds__(NT) k_init_dir(Sys S, T* __restrict__ p, const T* __restrict__ r,
-                                                 const double* __restrict__ dinv) {
+                                                 const typename Prec<T>::xw* __restrict__ dinv) {
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     __shared__ double red[2 * NWARP];
     p += vo; r += vo;
     if (PC == 1) dinv += vo;
-    double rz = 0.0;
+    typename Prec<T>::acc rz = Prec<T>::zero();
     for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-        const double ri = (double)r[i];
-        const double zi = PC == 1 ? rnd<T>(ri * dinv[i]) : ri;
-        p[i] = (T)zi;
-        rz = fma(ri, zi, rz);
+        const T ri = r[i];
+        const T zi = PC == 1 ? jacobi_z(ri, dinv[i]) : ri;
+        p[i] = zi;
+        dot_acc(rz, ri, zi);
     }
-    double v[1] = {rz}, tot[1];
+    double v[1] = {Prec<T>::total(rz)}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) new_direction(st, S.ctl, tot[0]);
 }
 
@@ -616,22 +732,23 @@ struct Stat {
 
 // Returned x = round(x_w) (0 when b = 0); true residual of that x; statistics.
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_final(Mat A, Sys S, const T* __restrict__ av, const double* __restrict__ x,
-                                              const T* __restrict__ bw, T* __restrict__ x_out, Stat* out) {
+__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
+    k_final(Mat A, Sys S, const T* __restrict__ av, const typename Prec<T>::xw* __restrict__ x,
+            const T* __restrict__ bw, T* __restrict__ x_out, Stat* out) {
+    using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     av += ao; x += vo; bw += vo; x_out += vo;
     const bool zero_b = ld_cg(&st->bb) == 0.0;
-    double tr2 = 0.0;
-    spmv_rows<T>(A, av, GatherRounded<T>{x},
-                 [&](int i, double s) {
-                     x_out[i] = zero_b ? (T)0 : (T)x[i];
-                     const double e = (double)bw[i] - s;
-                     tr2 = fma(e, e, tr2);
-                 },
-                 dsm);
-    double v[1] = {tr2}, tot[1];
+    acc_t tr2 = Prec<T>::zero();
+    spmv_rows<T, T>(A, av, GatherX<T>{x},
+                    [&](int i, acc_t s) {
+                        x_out[i] = zero_b ? T(0) : x_out_of(x[i]);
+                        sq_acc(tr2, resid(bw[i], s));
+                    },
+                    dsm);
+    double v[1] = {Prec<T>::total(tr2)}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) {
         const double bb = st->bb;
         Stat o;
@@ -672,13 +789,12 @@ __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict
             __syncwarp();
             for (int e = lane; e < cnt_; e += 32) {
                 const int c = ld_stream(A.ci + k0 + e);
-                const double li = (double)ld_nc(lam + srow[e]);
-                __stcs(dA + k0 + e, (T)(-li * (double)ld_nc(x + c)));
+                __stcs(dA + k0 + e, neg_prod(ld_nc(lam + srow[e]), ld_nc(x + c)));
             }
             __syncwarp();
         } else if (row < A.n) {
-            const double li = (double)lam[row];
-            for (int k = rlo; k < rhi; ++k) __stcs(dA + k, (T)(-li * (double)ld_nc(x + ld_stream(A.ci + k))));
+            const T li = lam[row];
+            for (int k = rlo; k < rhi; ++k) __stcs(dA + k, neg_prod(li, ld_nc(x + ld_stream(A.ci + k))));
         }
     }
 }

@@ -5,6 +5,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "df.cuh"
 
 namespace sla {
 
@@ -66,9 +67,18 @@ __global__ void k_diag(int n, long long nnz, int batch, const int* __restrict__ 
     if (bits) atomicOr(err, bits);
 }
 
-__global__ void k_recip(size_t m, const double* __restrict__ d, double* __restrict__ dinv) {
+// Stored form of an fp64 set-up value: fp64 itself, or a double-float pair
+// for fp32 systems.
+__device__ __forceinline__ void put(double* dst, double v) { *dst = v; }
+__device__ __forceinline__ void put(float2* dst, double v) {
+    const DF d = df_from_double(v);
+    *dst = make_float2(d.hi, d.lo);
+}
+
+template <typename W>
+__global__ void k_recip(size_t m, const double* __restrict__ d, W* __restrict__ dinv) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < m; i += (size_t)gridDim.x * blockDim.x)
-        dinv[i] = 1.0 / d[i];
+        put(dinv + i, 1.0 / d[i]);
 }
 
 // ----------------------------------------------------------------- row groups
@@ -157,9 +167,9 @@ __global__ void k_tri_count(int n, const int* __restrict__ rp, const int* __rest
     }
 }
 
-template <typename T>
+template <typename T, typename GV>
 __global__ void k_fill_G(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
-                         const double* __restrict__ diag, const int* __restrict__ grp, int* gci, double* gv) {
+                         const double* __restrict__ diag, const int* __restrict__ grp, int* gci, GV* gv) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         int m = grp[i];
         const int end = grp[i + 1];
@@ -167,14 +177,14 @@ __global__ void k_fill_G(int n, const int* __restrict__ rp, const int* __restric
         for (int k = rp[i]; m < end; ++k, ++m) {
             const int j = ci[k];
             gci[m] = j;
-            gv[m] = (j == i) ? 1.0 / sqrt(di) : -(double)av[k] / (2.0 * sqrt(di * diag[j]));
+            put(gv + m, (j == i) ? 1.0 / sqrt(di) : -(double)av[k] / (2.0 * sqrt(di * diag[j])));
         }
     }
 }
 
-template <typename T>
+template <typename T, typename GV>
 __global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
-                          const double* __restrict__ diag, const int* __restrict__ gtrp, int* gtci, double* gtv,
+                          const double* __restrict__ diag, const int* __restrict__ gtrp, int* gtci, GV* gtv,
                           int* err) {
     int bits = 0;
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
@@ -185,10 +195,10 @@ __global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restri
         for (int k = b - (end - m); k < b; ++k, ++m) {
             const int i = ci[k];   // i >= j
             gtci[m] = i;
-            if (i == j) { gtv[m] = 1.0 / sqrt(dj); continue; }
+            if (i == j) { put(gtv + m, 1.0 / sqrt(dj)); continue; }
             const int pos = find_col(ci, rp[i], rp[i + 1], j);
-            if (pos < 0) { bits |= ERR_ASYM; gtv[m] = 0.0; continue; }
-            gtv[m] = -(double)av[pos] / (2.0 * sqrt(diag[i] * dj));
+            if (pos < 0) { bits |= ERR_ASYM; put(gtv + m, 0.0); continue; }
+            put(gtv + m, -(double)av[pos] / (2.0 * sqrt(diag[i] * dj)));
         }
     }
     if (bits) atomicOr(err, bits);

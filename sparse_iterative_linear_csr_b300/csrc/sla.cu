@@ -140,7 +140,7 @@ static bool use_async(int cap) { return cap <= ASYNC_MAX_CAP; }
 // Dynamic shared memory of the staged-SpMV kernels for capacity `cap`.
 static size_t spmv_smem(int cap) {
     const size_t single = (size_t)cap * 2 * sizeof(double);
-    const size_t piped = async_smem_per_warp<double>(cap);
+    const size_t piped = async_smem_per_warp<double, double>(cap);  // largest value and vector types
     return (size_t)NWARP * (use_async(cap) && piped > single ? piped : single);
 }
 static size_t grad_smem(int cap) { return spmv_smem(cap); }
@@ -293,7 +293,8 @@ static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
                                         h->diag.as<double>(), err.as<int>());
     TRY(launched());
     const size_t m = (size_t)h->batch * h->n;
-    k_recip<<<4096, 256, 0, s>>>(m, h->diag.as<double>(), h->dinv.as<double>());
+    if (h->dt == SLA_F64) k_recip<double><<<4096, 256, 0, s>>>(m, h->diag.as<double>(), h->dinv.as<double>());
+    else k_recip<float2><<<4096, 256, 0, s>>>(m, h->diag.as<double>(), h->dinv.as<float2>());
     TRY(launched());
     TRY(read_int(err.as<int>(), &h->diag_err, s));
     return SLA_OK;
@@ -336,19 +337,21 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
     for (int sy = 0; sy < h->batch; ++sy) {
         const double* dg = h->diag.as<double>() + (size_t)sy * n;
-        double* gv = h->gv.as<double>() + (size_t)sy * ng;
-        double* gtv = h->gtv.as<double>() + (size_t)sy * ng;
+        double* gv = h->gv.as<double>() + (size_t)sy * ng;     // 8-byte slots: fp64, or a
+        double* gtv = h->gtv.as<double>() + (size_t)sy * ng;   // double-float pair for fp32
         if (h->dt == SLA_F64) {
             const double* av = (const double*)h->vals + (size_t)sy * h->nnz;
-            k_fill_G<double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
+            k_fill_G<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
             TRY(launched());
-            k_fill_GT<double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(), gtv,
+            k_fill_GT<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(), gtv,
                                                 err.as<int>());
         } else {
             const float* av = (const float*)h->vals + (size_t)sy * h->nnz;
-            k_fill_G<float><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
+            k_fill_G<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(),
+                                                      reinterpret_cast<float2*>(gv));
             TRY(launched());
-            k_fill_GT<float><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(), gtv,
+            k_fill_GT<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(),
+                                                       reinterpret_cast<float2*>(gtv),
                                                err.as<int>());
         }
         TRY(launched());
@@ -390,8 +393,10 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     T* r = h->r.as<T>();
     T* p = h->p.as<T>();
     T* q = h->q.as<T>();
-    double* x = h->x.as<double>();
-    const double* dinv = h->dinv.as<double>();
+    using XW = typename Prec<T>::xw;
+    using GV = typename Prec<T>::gv;
+    XW* x = h->x.as<XW>();
+    const XW* dinv = h->dinv.as<XW>();
     const dim3 gs(gx_spmv(h, h->capA), h->batch), gv(gx_vec(h), h->batch);
     k_spmv_iter<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, p, q, x, h->bw.as<T>());
     TRY(launched());
@@ -401,11 +406,11 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
         const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->capGT);
         const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->capG);
         k_spai_t<T><<<dim3(gx_spmv(h, h->capGT), h->batch), NT, spmv_smem(h->capGT), s>>>(GT, S, h->nnzg,
-                                                                                        h->gtv.as<double>(), r,
+                                                                                        h->gtv.as<GV>(), r,
                                                                                         h->t.as<T>());
         TRY(launched());
         k_spai_z<T><<<dim3(gx_spmv(h, h->capG), h->batch), NT, spmv_smem(h->capG), s>>>(
-            G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<T>(), r, h->z.as<T>(), eps);
         TRY(launched());
         k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
         TRY(launched());
@@ -491,8 +496,10 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     const dim3 gs(gx_spmv(h, h->capA), h->batch), gv(gx_vec(h), h->batch);
     T* r = h->r.as<T>();
     T* p = h->p.as<T>();
-    double* x = h->x.as<double>();
-    const double* dinv = h->dinv.as<double>();
+    using XW = typename Prec<T>::xw;
+    using GV = typename Prec<T>::gv;
+    XW* x = h->x.as<XW>();
+    const XW* dinv = h->dinv.as<XW>();
 
     CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
     if (o->use_x0) {
@@ -506,11 +513,11 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
         const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->capGT);
         const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->capG);
         k_spai_t<T><<<dim3(gx_spmv(h, h->capGT), h->batch), NT, spmv_smem(h->capGT), s>>>(GT, S, h->nnzg,
-                                                                                       h->gtv.as<double>(), r,
+                                                                                       h->gtv.as<GV>(), r,
                                                                                        h->t.as<T>());
         TRY(launched());
         k_spai_z<T><<<dim3(gx_spmv(h, h->capG), h->batch), NT, spmv_smem(h->capG), s>>>(
-            G, S, h->nnzg, h->gv.as<double>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<T>(), r, h->z.as<T>(), eps);
         TRY(launched());
         k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
     } else if (pc == SLA_PC_JACOBI) {
