@@ -141,6 +141,32 @@ sla_status sla_pcg_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg
 sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla_pcg_opts* opts,
                        void* d_dLdb, void* d_dLdA, sla_solve_info* info, void* stream);
 
+/*
+ * Allocation-free y = A x and d_dot[s] = x_s . y_s (the same fused kernel as
+ * sla_spmv_dot), without a handle.  The paper has no counterpart: this entry
+ * point exists for callers that cannot let a library allocate device
+ * memory -- programs that own all device memory through their own allocator
+ * or memory budget, and latency-critical loops where cudaMalloc / cudaFree
+ * would synchronise the device.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine; the caller passes every input and output.
+ *  - Arguments as for sla_csr_create plus the vectors of sla_spmv_dot:
+ *    CSR arrays (structure not checked here), d_x and d_y [batch][n] in the
+ *    dtype, d_dot double[batch].  1 <= batch <= 64; a larger batch returns
+ *    SLA_ERR_INVALID.
+ *  - Its scratch (64 arrival counters and 4096 partial sums, about 33 KB) is
+ *    a fixed array in device memory that every GPU loading this library
+ *    holds until the process exits.  Every call shares it: each call first
+ *    clears the counters on `stream`, so calls that overlap on the GPU (on
+ *    different streams, or from several threads) race and must not be used.
+ *  - The first call with a given device current looks up the scratch's
+ *    device address (cudaGetSymbolAddress) and caches it; make that first
+ *    call before any stream capture.
+ *  - Returns without synchronising `stream`.
+ */
+sla_status sla_spmv_dot_static(int n, long long nnz, int batch, sla_dtype dt, const int* d_row_ptr,
+                               const int* d_col_idx, const void* d_vals, const void* d_x, void* d_y,
+                               double* d_dot, void* stream);
+
 /* Free the handle and everything it owns (not the caller's arrays). */
 sla_status sla_csr_destroy(sla_handle h);
 

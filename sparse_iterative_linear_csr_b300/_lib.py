@@ -20,7 +20,8 @@ SLA_VALIDATE = 1
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
-           "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count"]
+           "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
+           "sla_spmv_dot_static"]
 
 
 class PcgOpts(C.Structure):
@@ -58,6 +59,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_csr_destroy.argtypes = [_vp]
     lib.sla_last_error.argtypes = []
     lib.sla_last_error.restype = C.c_char_p
+    # allocation-free fused SpMV + dot (no handle; fixed device scratch)
+    lib.sla_spmv_dot_static.argtypes = [C.c_int, C.c_longlong, C.c_int, C.c_int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _vp]
+    lib.sla_spmv_dot_static.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
     for f in ["sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",

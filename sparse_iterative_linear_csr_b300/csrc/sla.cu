@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <type_traits>
@@ -808,3 +809,91 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
 }
 
 }  // extern "C"
+
+// ===================================================================== allocation-free SpMV + dot
+// Scratch of sla_spmv_dot_static, in file-scope device memory instead of a
+// handle: one arrival counter per system (first STATIC_COUNTER_BYTES) and the
+// per-CTA partial sums of x.y (the rest).  Every GPU that loads this library
+// holds these bytes until the process exits.  Host code must not pass the
+// symbol itself to a kernel (on the host it names a host-side stand-in):
+// static_scratch() looks up its device address once per device.
+static constexpr int STATIC_MAX_BATCH = 64;
+static constexpr int STATIC_COUNTER_BYTES = 256;                 // 64 counters, one per system
+static constexpr int STATIC_PARTIALS = 4096;                     // partial sums shared by all systems
+static constexpr size_t STATIC_SCRATCH_BYTES = STATIC_COUNTER_BYTES + STATIC_PARTIALS * sizeof(double);
+static constexpr int STATIC_CAP = 256;                           // staged entries per 32-row group
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+static constexpr int STATIC_MAX_DEVICES = 64;
+static std::mutex g_static_mu;
+static void* g_static_ptr[STATIC_MAX_DEVICES] = {};
+
+// Device address of g_static_scratch on the current device (looked up on the
+// first call made with that device current, then cached).
+static sla_status static_scratch(void** out) {
+    int dev = 0;
+    CU(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= STATIC_MAX_DEVICES) return fail(SLA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess || !ptr)
+            return fail(SLA_ERR_CUDA, "cudaGetSymbolAddress(scratch) failed: %s", cudaGetErrorString(e));
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return SLA_OK;
+}
+
+template <typename T>
+static sla_status spmv_dot_static_impl(int n, long long nnz, int batch, const int* rp, const int* ci,
+                                       const T* vals, const T* x, T* y, double* dot, cudaStream_t s) {
+    void* scratch = nullptr;
+    TRY(static_scratch(&scratch));
+    TRY(allow_smem<T>());
+    int dev = 0, sms = 0, per = 0;
+    CU(cudaGetDevice(&dev));
+    CU(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const size_t smem = spmv_smem(STATIC_CAP);
+    TRY(occupancy(k_spmv<T>, smem, &per));
+    long long gx = (long long)per * sms / batch;
+    if (gx > group_ctas(n)) gx = group_ctas(n);
+    if (gx > STATIC_PARTIALS / batch) gx = STATIC_PARTIALS / batch;
+    if (gx < 1) gx = 1;
+    unsigned* counters = static_cast<unsigned*>(scratch);
+    double* partials = reinterpret_cast<double*>(static_cast<unsigned char*>(scratch) + STATIC_COUNTER_BYTES);
+    // The counters must start at zero; the partial sums are always written before they are read.
+    CU(cudaMemsetAsync(counters, 0, sizeof(unsigned) * batch, s));
+    Sys S;
+    S.n = n;
+    S.nnz = nnz;
+    S.st = nullptr;    // k_spmv keeps no solver state
+    S.ctl = nullptr;
+    S.cnt = counters;
+    S.part = partials;
+    S.pstride = (int)gx;
+    const Mat A = mat_of(rp, ci, n, STATIC_CAP);
+    k_spmv<T><<<dim3((unsigned)gx, batch), NT, smem, s>>>(A, S, vals, x, y, dot);
+    return launched();
+}
+
+extern "C" sla_status sla_spmv_dot_static(int n, long long nnz, int batch, sla_dtype dt, const int* d_row_ptr,
+                                          const int* d_col_idx, const void* d_vals, const void* d_x, void* d_y,
+                                          double* d_dot, void* stream) {
+    if (n < 1) return fail(SLA_ERR_INVALID, "n must be >= 1 (got %d)", n);
+    if (nnz < 0 || nnz > 2147483647LL) return fail(SLA_ERR_INVALID, "nnz must be in [0, 2^31) (got %lld)", nnz);
+    if (batch < 1 || batch > STATIC_MAX_BATCH)
+        return fail(SLA_ERR_INVALID, "batch must be in [1, %d] for the allocation-free entry point (got %d)",
+                    STATIC_MAX_BATCH, batch);
+    if (dt != SLA_F64 && dt != SLA_F32) return fail(SLA_ERR_INVALID, "unknown dtype %d", (int)dt);
+    if (!d_row_ptr || (nnz > 0 && (!d_col_idx || !d_vals)) || !d_x || !d_y || !d_dot)
+        return fail(SLA_ERR_INVALID, "null pointer");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dt == SLA_F64)
+        return spmv_dot_static_impl<double>(n, nnz, batch, d_row_ptr, d_col_idx, (const double*)d_vals,
+                                            (const double*)d_x, (double*)d_y, d_dot, s);
+    return spmv_dot_static_impl<float>(n, nnz, batch, d_row_ptr, d_col_idx, (const float*)d_vals,
+                                       (const float*)d_x, (float*)d_y, d_dot, s);
+}
+
