@@ -41,6 +41,7 @@ DESCR = {
           "SPAI-PCG (G G^T + 1e-3 I) to 1e-8",
 }
 MAX_ITER = 200000
+METRIC = "PCG iterations/s (forward + adjoint); HBM GB/s per iteration (fraction of B300 peak); solve ms"
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0
 
@@ -201,7 +202,7 @@ def run_reference(args, w, rank):
         its += inf["iters"]
     dt = time.perf_counter() - t0
     v = its / dt
-    line = {"metric": "PCG iterations/s", "value": v, "unit": "iterations/s", "n_gpus": args.gpus,
+    line = {"metric": METRIC, "value": v, "unit": "iterations/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64" if w.dtype == "f64" else "f32",
             "data": "synthetic", "impl": "reference",
@@ -376,7 +377,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": "PCG iterations/s (forward + adjoint); HBM GB/s per iteration (fraction of B300 peak); solve ms",
+            "metric": METRIC,
             "value": value, "unit": "iterations/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
