@@ -15,9 +15,10 @@
 //    are exact and sums carry ~48 bits before each stored vector is rounded
 //    to fp32.  Only per-thread totals and the solver scalars use fp64.
 //
-// SpMV layout (spmv_rows / spmv_rows_async): one warp per group of 32
-// consecutive rows; the warp stages its non-zeros in its own shared-memory
-// slice, then each lane sums its own row.  Grids are persistent in x.
+// SpMV layout (spmv_rows / spmv_rows_async): one warp per group of 32 / L
+// consecutive rows (L = 1, 2 or 4 lanes per row, from the row lengths); the
+// warp stages its non-zeros in its own shared-memory slice, then the lanes of
+// each row sum it.  Grids are persistent in x.
 // Inner products are reduced in a fixed order (grid_sum) and the last CTA to
 // finish updates that system's scalars on the device, so no host round trip
 // sits inside an iteration.
@@ -50,9 +51,11 @@ struct Mat {
     const int* rp;
     const int* ci;
     int n;            // rows
-    int cap;          // staged entries per warp (per 32-row group)
+    int cap;          // staged entries per warp (per group of 32 / lanes rows)
     int async;        // 1: cp.async double-buffered staging (spmv_rows_async)
     int wstride;      // doubles of shared memory per warp (both staging forms)
+    int lanes;        // lanes per row: 1, 2 or 4 (a group holds 32 / lanes rows)
+    int lshift;       // log2(lanes)
 };
 
 #define SYS_PROLOGUE                                            \
@@ -117,18 +120,38 @@ __device__ __forceinline__ DF acc_xor(DF t, int o) {
 __device__ __forceinline__ void acc_add(double& a, double b) { a += b; }
 __device__ __forceinline__ void acc_add(DF& a, DF b) { a = df_add(a, b); }
 
-// Rows are taken in groups of 32, one warp per group (grid stride over
-// groups).  The warp stages its group's non-zeros -- values streamed with
+// Rows are taken in groups of R = 32 / L consecutive rows, one warp per group
+// (grid stride over groups), L = A.lanes lanes per row chosen from the row
+// lengths so that a group's entries fit the warp's stage.  The warp stages
+// the group's non-zeros -- values and column indices streamed with
 // coalesced evict-first loads, the vector entries they address gathered
 // through the read-only path -- in its own slice of shared memory (`cap`
-// entries), then each lane sums its own row (one fp64 FMA per entry for
-// fp64 systems).  Only __syncwarp orders the two phases, so warps progress
-// independently and hide each other's memory latency.  A group with more than
-// `cap` non-zeros is summed straight from global memory: rows up to LONG_ROW
-// entries by their lane, longer rows by the whole warp.
-// epi(row, sum) is called once per row of the matrix by the row's lane.
+// entries), then the L lanes of each row sum interleaved entries (one fp64
+// FMA per entry for fp64 systems) and combine with log2(L) shuffle adds.
+// Only __syncwarp orders the phases, so warps progress independently and
+// hide each other's memory latency.  A group with more than `cap` non-zeros
+// is summed straight from global memory (rows longer than LONG_ROW by the
+// whole warp).
+// For every row, pre(row) is called early by the row's first lane (its result
+// is carried to the epilogue, so that load overlaps the gathers) and
+// epi(row, sum, carried) once the sum is complete.
 constexpr int STAGE_U = 4;     // entries per lane in flight while staging
 constexpr int LONG_ROW = 64;   // longer rows of an unstaged group go warp-wide
+
+// Bounds of this lane's row in group grp (empty past the last row).
+__device__ __forceinline__ void row_bounds(const Mat& A, int grp, int& row, int& rlo, int& rhi) {
+    const int lane = threadIdx.x & 31;
+    const long long r = ((((long long)grp) << 5) + lane) >> A.lshift;
+    row = (int)(r < A.n ? r : A.n);
+    rlo = ld_nc(A.rp + row);
+    rhi = ld_nc(A.rp + min(row + 1, A.n));
+}
+
+// Sum of the lanes of each row's segment (every lane of the segment gets it).
+template <typename ACC>
+__device__ __forceinline__ void segment_sum(ACC& s, int lanes) {
+    for (int o = lanes >> 1; o > 0; o >>= 1) acc_add(s, acc_xor(s, o));
+}
 
 // Rows of a group that did not fit the stage, summed from global memory.
 template <typename T, typename VT, class Gather>
@@ -136,10 +159,11 @@ __device__ __forceinline__ typename Prec<T>::acc unstaged_row(const Mat& A, cons
                                                               Gather gather, int rlo, int rhi) {
     using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
+    const int sub = lane & (A.lanes - 1);
     acc_t s = Prec<T>::zero();
     if (rhi - rlo <= LONG_ROW)
-        for (int k = rlo; k < rhi; ++k) mac(s, ld_stream(av + k), gather(ld_stream(A.ci + k)));
-    unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW);
+        for (int k = rlo + sub; k < rhi; k += A.lanes) mac(s, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+    unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW && sub == 0);
     while (longs) {
         const int src = __ffs(longs) - 1;
         longs &= longs - 1;
@@ -154,21 +178,23 @@ __device__ __forceinline__ typename Prec<T>::acc unstaged_row(const Mat& A, cons
     return s;
 }
 
-template <typename T, typename VT, class Gather, class Epi>
-__device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ av, Gather gather, Epi epi,
-                                          double* wsm) {
+template <typename T, typename VT, class Gather, class Pre, class Epi>
+__device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ av, Gather gather, Pre pre,
+                                          Epi epi, double* wsm) {
     using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
+    const int sub = lane & (A.lanes - 1);
     const int cap = A.cap;
     char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
     VT* sa = reinterpret_cast<VT*>(base);
     T* sx = reinterpret_cast<T*>(base + cap * sizeof(VT));
-    const int ngroups = (A.n + 31) >> 5;
+    const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
     const int nwarps = (gridDim.x * NT) >> 5;
     for (int grp = (blockIdx.x * NT + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
-        const int row = (grp << 5) + lane;
-        const int rlo = ld_nc(A.rp + min(row, A.n));
-        const int rhi = ld_nc(A.rp + min(row + 1, A.n));
+        int row, rlo, rhi;
+        row_bounds(A, grp, row, rlo, rhi);
+        const bool own = sub == 0 && row < A.n;
+        const auto carried = own ? pre(row) : decltype(pre(0))(0);
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
         const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt = k1 - k0;
@@ -198,12 +224,13 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
                 }
             }
             __syncwarp();
-            for (int e = rlo - k0; e < rhi - k0; ++e) mac(s, sa[e], sx[e]);
+            for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, sa[e], sx[e]);
             __syncwarp();
         } else {
             s = unstaged_row<T>(A, av, gather, rlo, rhi);
         }
-        if (row < A.n) epi(row, s);
+        segment_sum(s, A.lanes);
+        if (own) epi(row, s, carried);
     }
 }
 
@@ -211,54 +238,58 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
 // double-buffers its groups' values and column indices in shared memory with
 // cp.async: the copies of the next group are in flight while the warp gathers
 // and sums the current one, so every warp keeps the next group's streaming
-// traffic outstanding without holding registers for it.  The gathered entries
-// go through registers (GATHER_U per lane in flight) into the warp's slice.
+// traffic outstanding without holding registers for it.  Row bounds are
+// loaded one group ahead, so issuing the next group's copies never waits on
+// them.  The gathered entries go through registers (GATHER_U per lane in
+// flight) into the warp's slice.
 // Shared memory per warp: 2*cap*(sizeof(VT) + 4) + cap*sizeof(T).
-constexpr int GATHER_U = 8;
+constexpr int GATHER_U = 4;
 
 template <typename VT, typename T>
 __host__ __device__ constexpr size_t async_smem_per_warp(int cap) {
     return (size_t)2 * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
-template <typename T, typename VT, class Epi>
+template <typename T, typename VT, class Pre, class Epi>
 __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v,
-                                                Epi epi, double* wsm) {
+                                                Pre pre, Epi epi, double* wsm) {
     using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
+    const int sub = lane & (A.lanes - 1);
     const int cap = A.cap;
     char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
     VT* sv = reinterpret_cast<VT*>(base);
     int* sc = reinterpret_cast<int*>(base + 2 * cap * sizeof(VT));
     T* sx = reinterpret_cast<T*>(base + 2 * cap * (sizeof(VT) + sizeof(int)));
     const unsigned long long pol = l2_evict_first();
-    const int ngroups = (A.n + 31) >> 5;
+    const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
     const int nwarps = (gridDim.x * NT) >> 5;
     const int g0 = (blockIdx.x * NT + threadIdx.x) >> 5;
 
-    auto issue = [&](int grp, int stage) {
-        if (grp < ngroups) {
-            const int k0 = ld_nc(A.rp + (grp << 5));
-            const int k1 = ld_nc(A.rp + min((grp << 5) + 32, A.n));
-            if (k1 - k0 <= cap) {
-                VT* dv = sv + stage * cap;
-                int* dc = sc + stage * cap;
-                for (int e = lane; e < k1 - k0; e += 32) {
-                    cp_async<sizeof(VT)>(dv + e, av + k0 + e, pol);
-                    cp_async<4>(dc + e, A.ci + k0 + e, pol);
-                }
+    // copies of a group's values and columns into `stage` (k0, k1: its entry range)
+    auto issue = [&](int grp, int stage, int k0, int k1) {
+        if (grp < ngroups && k1 - k0 <= cap) {
+            VT* dv = sv + stage * cap;
+            int* dc = sc + stage * cap;
+            for (int e = lane; e < k1 - k0; e += 32) {
+                cp_async<sizeof(VT)>(dv + e, av + k0 + e, pol);
+                cp_async<4>(dc + e, A.ci + k0 + e, pol);
             }
         }
         cp_commit();
     };
 
-    issue(g0, 0);
+    int row, rlo, rhi, nrow, nlo, nhi;
+    row_bounds(A, g0, row, rlo, rhi);
+    issue(g0, 0, __shfl_sync(0xffffffffu, rlo, 0), __shfl_sync(0xffffffffu, rhi, 31));
+    row_bounds(A, g0 + nwarps, nrow, nlo, nhi);
     int stage = 0;
     for (int grp = g0; grp < ngroups; grp += nwarps, stage ^= 1) {
-        issue(grp + nwarps, stage ^ 1);
-        const int row = (grp << 5) + lane;
-        const int rlo = ld_nc(A.rp + min(row, A.n));
-        const int rhi = ld_nc(A.rp + min(row + 1, A.n));
+        const bool own = sub == 0 && row < A.n;
+        const auto carried = own ? pre(row) : decltype(pre(0))(0);
+        issue(grp + nwarps, stage ^ 1, __shfl_sync(0xffffffffu, nlo, 0), __shfl_sync(0xffffffffu, nhi, 31));
+        int frow, flo, fhi;
+        row_bounds(A, grp + 2 * nwarps, frow, flo, fhi);
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
         const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt = k1 - k0;
@@ -282,23 +313,26 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
                 }
             }
             __syncwarp();
-            for (int e = rlo - k0; e < rhi - k0; ++e) mac(s, cv[e], sx[e]);
+            for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, cv[e], sx[e]);
         } else {
             s = unstaged_row<T>(A, av, GatherVec<T>{v}, rlo, rhi);
         }
+        segment_sum(s, A.lanes);
         __syncwarp();  // this stage and sx are free for reuse
-        if (row < A.n) epi(row, s);
+        if (own) epi(row, s, carried);
+        row = nrow; rlo = nlo; rhi = nhi;
+        nrow = frow; nlo = flo; nhi = fhi;
     }
     cp_wait<0>();
 }
 
 // Product with a plain vector gather: the pipelined form when the matrix was
 // set up for it, the single-stage form otherwise.
-template <typename T, typename VT, class Epi>
-__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v, Epi epi,
-                                         double* wsm) {
-    if (A.async) spmv_rows_async<T, VT>(A, av, v, epi, wsm);
-    else spmv_rows<T, VT>(A, av, GatherVec<T>{v}, epi, wsm);
+template <typename T, typename VT, class Pre, class Epi>
+__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v, Pre pre,
+                                         Epi epi, double* wsm) {
+    if (A.async) spmv_rows_async<T, VT>(A, av, v, pre, epi, wsm);
+    else spmv_rows<T, VT>(A, av, GatherVec<T>{v}, pre, epi, wsm);
 }
 
 // ----------------------------------------------------------------- scalar logic
@@ -427,11 +461,11 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
     __shared__ double red[2 * NWARP];
     av += ao; x += vo; y += vo;
     acc_t acc = Prec<T>::zero();
-    spmv_vec<T, T>(A, av, x,
-                   [&](int i, acc_t s) {
+    spmv_vec<T, T>(A, av, x, [&](int i) { return x[i]; },
+                   [&](int i, acc_t s, T xi) {
                        const T yi = to_store(s);
                        y[i] = yi;
-                       dot_acc(acc, x[i], yi);
+                       dot_acc(acc, xi, yi);
                    },
                    dsm);
     if (dot) {
@@ -455,13 +489,14 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
     if (check) {
-        spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i, acc_t s) { sq_acc(tr2, resid(b[i], s)); }, dsm);
+        spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i) { return b[i]; },
+                        [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
     }
-    spmv_vec<T, T>(A, av, p,
-                   [&](int i, acc_t s) {
+    spmv_vec<T, T>(A, av, p, [&](int i) { return p[i]; },
+                   [&](int i, acc_t s, T pi) {
                        const T qi = to_store(s);
                        q[i] = qi;
-                       dot_acc(delta, p[i], qi);
+                       dot_acc(delta, pi, qi);
                    },
                    dsm);
     double v[2] = {Prec<T>::total(delta), Prec<T>::total(tr2)}, tot[2];
@@ -620,7 +655,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, lon
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
-    spmv_vec<T, typename Prec<T>::gv>(GT, gtv, r, [&](int i, acc_t s) { t[i] = to_store(s); }, dsm);
+    spmv_vec<T, typename Prec<T>::gv>(GT, gtv, r, [](int) { return T(0); },
+                                      [&](int i, acc_t s, T) { t[i] = to_store(s); }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
@@ -637,9 +673,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long
     gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
     const typename Prec<T>::sc e = Prec<T>::scal(eps);
     acc_t rz = Prec<T>::zero();
-    spmv_vec<T, typename Prec<T>::gv>(G, gv, t,
-                                      [&](int i, acc_t s) {
-                                          const T ri = r[i];
+    spmv_vec<T, typename Prec<T>::gv>(G, gv, t, [&](int i) { return r[i]; },
+                                      [&](int i, acc_t s, T ri) {
                                           const T zi = spai_z(s, e, ri);
                                           z[i] = zi;
                                           dot_acc(rz, ri, zi);
@@ -685,9 +720,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     __shared__ double red[2 * NWARP];
     av += ao; b_user += vo; x0 += vo; bw += vo; x += vo; r += vo;
     acc_t bb = Prec<T>::zero(), g = Prec<T>::zero();
-    spmv_rows<T, T>(A, av, GatherVec<T>{x0},
-                    [&](int i, acc_t s) {
-                        const T bi = b_user[i];
+    spmv_rows<T, T>(A, av, GatherVec<T>{x0}, [&](int i) { return b_user[i]; },
+                    [&](int i, acc_t s, T bi) {
                         bw[i] = bi;
                         x[i] = x_from(x0[i]);
                         const T ri = to_store(resid(bi, s));
@@ -742,10 +776,10 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     av += ao; x += vo; bw += vo; x_out += vo;
     const bool zero_b = ld_cg(&st->bb) == 0.0;
     acc_t tr2 = Prec<T>::zero();
-    spmv_rows<T, T>(A, av, GatherX<T>{x},
-                    [&](int i, acc_t s) {
+    spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i) { return bw[i]; },
+                    [&](int i, acc_t s, T bi) {
                         x_out[i] = zero_b ? T(0) : x_out_of(x[i]);
-                        sq_acc(tr2, resid(bw[i], s));
+                        sq_acc(tr2, resid(bi, s));
                     },
                     dsm);
     double v[1] = {Prec<T>::total(tr2)}, tot[1];
@@ -762,8 +796,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     }
 }
 
-// dL/dA_k = -lambda_row(k) * x_col(k) over the pattern.  One warp per group
-// of 32 rows: the row of each of the group's entries is recorded in the
+// dL/dA_k = -lambda_row(k) * x_col(k) over the pattern.  One warp per row
+// group (as in the SpMV): the row of each of the group's entries is recorded in the
 // warp's shared-memory slice, then the entries stream (coalesced reads of
 // col_idx, coalesced writes of dA).  A group with more than `cap` entries is
 // written row by row from its lanes.
@@ -775,17 +809,17 @@ __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict
     int* srow = reinterpret_cast<int*>(dsm + (threadIdx.x >> 5) * A.wstride);
     const int lane = threadIdx.x & 31;
     lam += vo; x += vo; dA += ao;
-    const int ngroups = (A.n + 31) >> 5;
+    const int sub = lane & (A.lanes - 1);
+    const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
     const int nwarps = (gridDim.x * NT) >> 5;
     for (int grp = (blockIdx.x * NT + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
-        const int row = (grp << 5) + lane;
-        const int rlo = ld_nc(A.rp + min(row, A.n));
-        const int rhi = ld_nc(A.rp + min(row + 1, A.n));
+        int row, rlo, rhi;
+        row_bounds(A, grp, row, rlo, rhi);
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
         const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt_ = k1 - k0;
         if (cnt_ <= A.cap) {
-            for (int e = rlo - k0; e < rhi - k0; ++e) srow[e] = row;
+            for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) srow[e] = row;
             __syncwarp();
             for (int e = lane; e < cnt_; e += 32) {
                 const int c = ld_stream(A.ci + k0 + e);
@@ -794,7 +828,7 @@ __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict
             __syncwarp();
         } else if (row < A.n) {
             const T li = lam[row];
-            for (int k = rlo; k < rhi; ++k) __stcs(dA + k, neg_prod(li, ld_nc(x + ld_stream(A.ci + k))));
+            for (int k = rlo + sub; k < rhi; k += A.lanes) __stcs(dA + k, neg_prod(li, ld_nc(x + ld_stream(A.ci + k))));
         }
     }
 }

@@ -82,13 +82,16 @@ __global__ void k_recip(size_t m, const double* __restrict__ d, W* __restrict__ 
 }
 
 // ----------------------------------------------------------------- row groups
-// Largest number of stored entries in any group of 32 consecutive rows (the
+// Largest number of stored entries in any group of R consecutive rows (the
 // shared-memory staging capacity a warp needs for the SpMV).
-__global__ void k_group_max(const int* __restrict__ rp, int n, int* out) {
-    const int ng = (n + 31) >> 5;
+__global__ void k_group_max(const int* __restrict__ rp, int n, int R, int* out) {
+    const long long ng = ((long long)n + R - 1) / R;
     int m = 0;
-    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < ng; g += gridDim.x * blockDim.x)
-        m = max(m, rp[min((g << 5) + 32, n)] - rp[g << 5]);
+    for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < ng; g += (long long)gridDim.x * blockDim.x) {
+        const long long r0 = g * R;
+        const long long r1 = r0 + R < n ? r0 + R : n;
+        m = max(m, rp[r1] - rp[r0]);
+    }
     if (m) atomicMax(out, m);
 }
 

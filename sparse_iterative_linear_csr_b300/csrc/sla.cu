@@ -100,6 +100,14 @@ struct GraphCache {
     }
 };
 
+// Staged-SpMV layout of one matrix: staging capacity (entries per group of
+// 32 / lanes rows), lanes per row, and CTAs per system.
+struct Layout {
+    int cap = 32;
+    int lanes = 1;
+    int gx = 1;
+};
+
 struct sla_csr {
     int n = 0;
     long long nnz = 0;
@@ -112,15 +120,14 @@ struct sla_csr {
     int device = 0;
     int sms = 0;
 
-    int capA = 32;     // SpMV staging capacity (entries per 32-row group)
-    int gxA = 1, gxG = 1, gxGT = 1;  // staged-SpMV CTAs per system for A, G, G^T
+    Layout LA;         // staged-SpMV layout of A
     int diag_err = 0;  // ERR_NO_DIAG | ERR_DIAG_SIGN
     DevBuf diag, dinv;
 
     // SPAI factor (built on first use, per values)
     bool spai_ready = false;
     long long nnzg = 0;
-    int capG = 32, capGT = 32;
+    Layout LG, LGT;    // ... of G and G^T
     DevBuf grp, gci, gv, gtrp, gtci, gtv;
 
     // workspace
@@ -166,7 +173,10 @@ static int grid_x(const sla_csr* h, long long units, int per_sm) {
     return (int)g;
 }
 
-static long long group_ctas(int n) { return (((long long)n + 31) / 32 + NWARP - 1) / NWARP; }
+static long long group_ctas(int n, int lanes) {
+    const long long rows = 32 / lanes;
+    return (((long long)n + rows - 1) / rows + NWARP - 1) / NWARP;
+}
 static bool pairs_ok(const sla_csr* h) { return (h->n & 1) == 0; }
 static long long vec_units(const sla_csr* h) {
     const long long m = pairs_ok(h) ? h->n / 2 : h->n;
@@ -192,15 +202,15 @@ static sla_status allow_smem() {
 
 // CTAs per system for the staged SpMV kernels with staging capacity `cap`.
 template <typename T>
-static sla_status spmv_grid(const sla_csr* h, int cap, int* gx) {
+static sla_status spmv_grid(const sla_csr* h, Layout* L) {
     int per = 1;
-    TRY(occupancy(k_spmv_iter<T>, spmv_smem(cap), &per));
-    *gx = grid_x(h, group_ctas(h->n), per);
+    TRY(occupancy(k_spmv_iter<T>, spmv_smem(L->cap), &per));
+    L->gx = grid_x(h, group_ctas(h->n, L->lanes), per);
     return SLA_OK;
 }
 
-static sla_status spmv_grid_any(const sla_csr* h, int cap, int* gx) {
-    return h->dt == SLA_F64 ? spmv_grid<double>(h, cap, gx) : spmv_grid<float>(h, cap, gx);
+static sla_status spmv_grid_any(const sla_csr* h, Layout* L) {
+    return h->dt == SLA_F64 ? spmv_grid<double>(h, L) : spmv_grid<float>(h, L);
 }
 
 // Streaming kernels: two resident CTAs per SM.  Each warp-level fp64
@@ -209,13 +219,6 @@ static sla_status spmv_grid_any(const sla_csr* h, int cap, int* gx) {
 // fully occupied grid here.
 static constexpr int VEC_CTAS_PER_SM = 2;
 static int gx_vec(const sla_csr* h) { return grid_x(h, vec_units(h), VEC_CTAS_PER_SM); }
-static int gx_spmv(const sla_csr* h, int cap);
-
-static int gx_spmv(const sla_csr* h, int cap) {
-    if (cap == h->capA) return h->gxA;
-    if (cap == h->capG) return h->gxG;
-    return h->gxGT;
-}
 
 static Sys sys_of(sla_csr* h) {
     Sys s;
@@ -229,14 +232,16 @@ static Sys sys_of(sla_csr* h) {
     return s;
 }
 
-static Mat mat_of(const int* rp, const int* ci, int n, int cap) {
+static Mat mat_of(const int* rp, const int* ci, int n, const Layout& L) {
     Mat m;
     m.rp = rp;
     m.ci = ci;
     m.n = n;
-    m.cap = cap;
-    m.async = use_async(cap) ? 1 : 0;
-    m.wstride = (int)(spmv_smem(cap) / NWARP / sizeof(double));
+    m.cap = L.cap;
+    m.async = use_async(L.cap) ? 1 : 0;
+    m.wstride = (int)(spmv_smem(L.cap) / NWARP / sizeof(double));
+    m.lanes = L.lanes;
+    m.lshift = L.lanes == 4 ? 2 : (L.lanes == 2 ? 1 : 0);
     return m;
 }
 
@@ -264,21 +269,36 @@ static sla_status read_int(const int* d, int* out, cudaStream_t s) {
     return SLA_OK;
 }
 
-static sla_status staging_cap(const int* rp, int n, int* cap, cudaStream_t s) {
+static sla_status group_max(const int* rp, int n, int rows, int* out, cudaStream_t s) {
     DevBuf m;
     TRY(m.alloc(sizeof(int)));
     CU(cudaMemsetAsync(m.p, 0, sizeof(int), s));
-    const int ng = (n + 31) / 32;
-    const int g = (ng + 255) / 256 < 2048 ? (ng + 255) / 256 : 2048;
-    k_group_max<<<g, 256, 0, s>>>(rp, n, m.as<int>());
+    const long long ng = ((long long)n + rows - 1) / rows;
+    const int g = (ng + 255) / 256 < 2048 ? (int)((ng + 255) / 256) : 2048;
+    k_group_max<<<g, 256, 0, s>>>(rp, n, rows, m.as<int>());
     TRY(launched());
-    int v = 0;
-    TRY(read_int(m.as<int>(), &v, s));
-    v = (v + 31) / 32 * 32;
-    if (v < 32) v = 32;
-    if (v > MAX_CAP) v = MAX_CAP;
-    *cap = v;
+    TRY(read_int(m.as<int>(), out, s));
     return SLA_OK;
+}
+
+// One lane per row whenever a 32-row group fits a stage (pipelined up to
+// ASYNC_MAX_CAP entries, single-stage up to MAX_CAP); otherwise the fewest
+// lanes per row whose groups fit.  Measured on B300: for ~15-entry rows
+// (kNN graphs) one lane per row with single-stage staging beats two lanes
+// per row with pipelined staging.
+static sla_status choose_layout(const sla_csr* h, const int* rp, Layout* L, cudaStream_t s) {
+    for (int lanes = 1; lanes <= 4; lanes *= 2) {
+        int m = 0;
+        TRY(group_max(rp, h->n, 32 / lanes, &m, s));
+        int cap = (m + 31) / 32 * 32;
+        if (cap < 32) cap = 32;
+        if (cap <= MAX_CAP || lanes == 4) {
+            L->cap = cap > MAX_CAP ? MAX_CAP : cap;
+            L->lanes = lanes;
+            break;
+        }
+    }
+    return spmv_grid_any(h, L);
 }
 
 static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
@@ -360,10 +380,8 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     int e = 0;
     TRY(read_int(err.as<int>(), &e, s));
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
-    TRY(staging_cap(h->grp.as<int>(), n, &h->capG, s));
-    TRY(staging_cap(h->gtrp.as<int>(), n, &h->capGT, s));
-    TRY(spmv_grid_any(h, h->capG, &h->gxG));
-    TRY(spmv_grid_any(h, h->capGT, &h->gxGT));
+    TRY(choose_layout(h, h->grp.as<int>(), &h->LG, s));
+    TRY(choose_layout(h, h->gtrp.as<int>(), &h->LGT, s));
     TRY(h->z.alloc(h->es * (size_t)n * h->batch));
     TRY(h->t.alloc(h->es * (size_t)n * h->batch));
     h->spai_ready = true;
@@ -372,10 +390,10 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
 
 static sla_status ensure_pstride(sla_csr* h) {
     int m = gx_vec(h);
-    m = m > gx_spmv(h, h->capA) ? m : gx_spmv(h, h->capA);
+    m = m > h->LA.gx ? m : h->LA.gx;
     if (h->spai_ready) {
-        m = m > gx_spmv(h, h->capG) ? m : gx_spmv(h, h->capG);
-        m = m > gx_spmv(h, h->capGT) ? m : gx_spmv(h, h->capGT);
+        m = m > h->LG.gx ? m : h->LG.gx;
+        m = m > h->LGT.gx ? m : h->LGT.gx;
     }
     const int need = 2 * m;
     if (need <= h->pstride) return SLA_OK;
@@ -389,7 +407,7 @@ static sla_status ensure_pstride(sla_csr* h) {
 template <typename T, bool PAIRS>
 static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
+    const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
     const T* av = (const T*)h->vals;
     T* r = h->r.as<T>();
     T* p = h->p.as<T>();
@@ -398,19 +416,19 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     using GV = typename Prec<T>::gv;
     XW* x = h->x.as<XW>();
     const XW* dinv = h->dinv.as<XW>();
-    const dim3 gs(gx_spmv(h, h->capA), h->batch), gv(gx_vec(h), h->batch);
-    k_spmv_iter<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
+    k_spmv_iter<T><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, p, q, x, h->bw.as<T>());
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
         k_update<T, 2, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
         TRY(launched());
-        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->capGT);
-        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->capG);
-        k_spai_t<T><<<dim3(gx_spmv(h, h->capGT), h->batch), NT, spmv_smem(h->capGT), s>>>(GT, S, h->nnzg,
+        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->LGT);
+        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
+        k_spai_t<T><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
                                                                                         h->gtv.as<GV>(), r,
                                                                                         h->t.as<T>());
         TRY(launched());
-        k_spai_z<T><<<dim3(gx_spmv(h, h->capG), h->batch), NT, spmv_smem(h->capG), s>>>(
+        k_spai_z<T><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
             G, S, h->nnzg, h->gv.as<GV>(), h->t.as<T>(), r, h->z.as<T>(), eps);
         TRY(launched());
         k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
@@ -492,9 +510,9 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     TRY(get_graph<T>(h, pc, eps, k, &gc));
 
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
+    const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
     const T* av = (const T*)h->vals;
-    const dim3 gs(gx_spmv(h, h->capA), h->batch), gv(gx_vec(h), h->batch);
+    const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
     T* r = h->r.as<T>();
     T* p = h->p.as<T>();
     using XW = typename Prec<T>::xw;
@@ -504,20 +522,20 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
 
     CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
     if (o->use_x0) {
-        k_init_x0<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
+        k_init_x0<T><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
                                                          o->max_iter);
     } else {
         k_init<T><<<gv, NT, 0, s>>>(S, b, h->bw.as<T>(), x, r, o->tol, o->max_iter);
     }
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
-        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->capGT);
-        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->capG);
-        k_spai_t<T><<<dim3(gx_spmv(h, h->capGT), h->batch), NT, spmv_smem(h->capGT), s>>>(GT, S, h->nnzg,
+        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->LGT);
+        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
+        k_spai_t<T><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
                                                                                        h->gtv.as<GV>(), r,
                                                                                        h->t.as<T>());
         TRY(launched());
-        k_spai_z<T><<<dim3(gx_spmv(h, h->capG), h->batch), NT, spmv_smem(h->capG), s>>>(
+        k_spai_z<T><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
             G, S, h->nnzg, h->gv.as<GV>(), h->t.as<T>(), r, h->z.as<T>(), eps);
         TRY(launched());
         k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
@@ -569,7 +587,7 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     // drain (kernels of a finished batch return at once)
     CU(cudaStreamSynchronize(s));
 
-    k_final<T><<<gs, NT, spmv_smem(h->capA), s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
+    k_final<T><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
     TRY(launched());
     CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
     CU(cudaStreamSynchronize(s));
@@ -696,8 +714,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
                              (e & ERR_COL_ORDER) ? " columns not strictly ascending" : ""));
     }
     HTRY(dt == SLA_F64 ? allow_smem<double>() : allow_smem<float>());
-    HTRY(staging_cap(d_row_ptr, n, &h->capA, s));
-    HTRY(spmv_grid_any(h, h->capA, &h->gxA));
+    HTRY(choose_layout(h, d_row_ptr, &h->LA, s));
     const size_t vn = (size_t)n * batch;
     HTRY(h->diag.alloc(sizeof(double) * vn));
     HTRY(h->dinv.alloc(sizeof(double) * vn));
@@ -739,9 +756,9 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     if (!d_x || !d_y) return fail(SLA_ERR_INVALID, "null vector");
     cudaStream_t s = (cudaStream_t)stream;
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
-    const dim3 g(gx_spmv(h, h->capA), h->batch);
-    const size_t sm = spmv_smem(h->capA);
+    const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
+    const dim3 g(h->LA.gx, h->batch);
+    const size_t sm = spmv_smem(h->LA.cap);
     if (h->dt == SLA_F64)
         k_spmv<double><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_x, (double*)d_y, d_dot);
     else
@@ -793,13 +810,13 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
     if (st != SLA_OK && st != SLA_ERR_NOT_CONVERGED && st != SLA_ERR_BREAKDOWN && st != SLA_ERR_TIMEOUT) return st;
     if (d_dLdA && h->nnz > 0) {
         const Sys S = sys_of(h);
-        const Mat A = mat_of(h->rp, h->ci, h->n, h->capA);
-        const dim3 g(gx_spmv(h, h->capA), h->batch);
+        const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
+        const dim3 g(h->LA.gx, h->batch);
         if (h->dt == SLA_F64)
-            k_grad_A<double><<<g, NT, grad_smem(h->capA), s>>>(A, S, (const double*)d_dLdb, (const double*)d_x,
+            k_grad_A<double><<<g, NT, grad_smem(h->LA.cap), s>>>(A, S, (const double*)d_dLdb, (const double*)d_x,
                                                                (double*)d_dLdA);
         else
-            k_grad_A<float><<<g, NT, grad_smem(h->capA), s>>>(A, S, (const float*)d_dLdb, (const float*)d_x,
+            k_grad_A<float><<<g, NT, grad_smem(h->LA.cap), s>>>(A, S, (const float*)d_dLdb, (const float*)d_x,
                                                               (float*)d_dLdA);
         sla_status l = launched();
         if (l != SLA_OK) return l;
@@ -858,7 +875,7 @@ static sla_status spmv_dot_static_impl(int n, long long nnz, int batch, const in
     const size_t smem = spmv_smem(STATIC_CAP);
     TRY(occupancy(k_spmv<T>, smem, &per));
     long long gx = (long long)per * sms / batch;
-    if (gx > group_ctas(n)) gx = group_ctas(n);
+    if (gx > group_ctas(n, 1)) gx = group_ctas(n, 1);
     if (gx > STATIC_PARTIALS / batch) gx = STATIC_PARTIALS / batch;
     if (gx < 1) gx = 1;
     unsigned* counters = static_cast<unsigned*>(scratch);
@@ -873,7 +890,10 @@ static sla_status spmv_dot_static_impl(int n, long long nnz, int batch, const in
     S.cnt = counters;
     S.part = partials;
     S.pstride = (int)gx;
-    const Mat A = mat_of(rp, ci, n, STATIC_CAP);
+    Layout L;
+    L.cap = STATIC_CAP;
+    L.lanes = 1;
+    const Mat A = mat_of(rp, ci, n, L);
     k_spmv<T><<<dim3((unsigned)gx, batch), NT, smem, s>>>(A, S, vals, x, y, dot);
     return launched();
 }
