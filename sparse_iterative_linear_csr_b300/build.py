@@ -4,6 +4,7 @@
 
 The library is one translation unit (csrc/sla.cu) with the CUDA runtime
 linked statically, so it loads next to PyTorch without sharing its runtime.
+SLA_NVCC_EXTRA adds nvcc flags (e.g. -DSLA_ITER_MIN_CTAS=3 for tuning runs).
 """
 from __future__ import annotations
 
@@ -44,7 +45,8 @@ def stale() -> bool:
 def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     if not force and not stale():
         return LIB
-    cmd = [nvcc()] + ARCH + FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + \
+    extra = os.environ.get("SLA_NVCC_EXTRA", "").split()
+    cmd = [nvcc()] + ARCH + FLAGS + extra + (["-Xptxas", "-v"] if ptxas_verbose else []) + \
         ["-o", LIB + ".tmp", os.path.join(SRC_DIR, "sla.cu")]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:

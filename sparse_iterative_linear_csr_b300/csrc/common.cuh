@@ -11,6 +11,10 @@ namespace sla {
 constexpr int NT = 256;          // threads per CTA for every kernel here
 constexpr int NWARP = NT / 32;
 constexpr int SPMV_MIN_CTAS = 4; // resident CTAs per SM the staged-SpMV kernels are compiled for
+#ifndef SLA_ITER_MIN_CTAS
+#define SLA_ITER_MIN_CTAS 3      // ... and the CG product kernel (which also carries the residual check;
+                                 // measured faster unspilled at 3 than spilled at 4)
+#endif
 constexpr int MAXR = NT;         // rows per row block (one row per thread)
 
 // Outcome codes mirrored from sla_status (kept numerically equal).
@@ -60,6 +64,12 @@ __device__ __forceinline__ T ld_cg(const T* p) { return __ldcg(p); }       // L2
 __device__ __forceinline__ unsigned long long l2_evict_first() {
     unsigned long long pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+// For gathered vector entries, which every product re-reads: keep them in L2.
+__device__ __forceinline__ unsigned long long l2_evict_last() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
     return pol;
 }
 template <int BYTES>

@@ -31,6 +31,8 @@
 //   k_pupdate:    p = z + beta p
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "df.cuh"
 
@@ -52,10 +54,13 @@ struct Mat {
     const int* ci;
     int n;            // rows
     int cap;          // staged entries per warp (per group of 32 / lanes rows)
-    int async;        // 1: cp.async double-buffered staging (spmv_rows_async)
+    int async;        // 0: register staging (spmv_rows); 1 / 2: cp.async staging, value/column
+                      //    copies single / double buffered (spmv_rows_async)
     int wstride;      // doubles of shared memory per warp (both staging forms)
     int lanes;        // lanes per row: 1, 2 or 4 (a group holds 32 / lanes rows)
     int lshift;       // log2(lanes)
+    int gasync;       // 1: gathers by cp.async (scattered columns); 0: through registers
+                      //    (columns near the row: the gathers mostly hit L1)
 };
 
 #define SYS_PROLOGUE                                            \
@@ -234,20 +239,25 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
     }
 }
 
-// Pipelined form of spmv_rows for a plain vector gather.  Each warp
-// double-buffers its groups' values and column indices in shared memory with
-// cp.async: the copies of the next group are in flight while the warp gathers
-// and sums the current one, so every warp keeps the next group's streaming
-// traffic outstanding without holding registers for it.  Row bounds are
-// loaded one group ahead, so issuing the next group's copies never waits on
-// them.  The gathered entries go through registers (GATHER_U per lane in
-// flight) into the warp's slice.
-// Shared memory per warp: 2*cap*(sizeof(VT) + 4) + cap*sizeof(T).
-constexpr int GATHER_U = 4;
+// Asynchronous form of spmv_rows for a plain vector gather.  A group's
+// values and column indices are copied into the warp's slice with cp.async
+// (L2 evict-first), then the vector entries they address are gathered into
+// the slice with cp.async as well (L2 evict-last: the vector is re-read by
+// every product), so a warp keeps a whole group of gathers in flight without
+// holding a register for any of them.  With A.async == 2 the value/column
+// copies are double-buffered: the next group's copies are issued as soon as
+// the current group's gathers are, so only the gather latency is exposed per
+// group; with A.async == 1 (large groups) they are single-buffered.  For
+// matrices whose columns stay near the row (A.gasync == 0) the gathers go
+// through registers instead, GATHER_U per lane in flight: they mostly hit L1,
+// which the asynchronous copies serve less well.  Row bounds are loaded one
+// group ahead.
+// Shared memory per warp: async*cap*(sizeof(VT) + 4) + cap*sizeof(T).
+constexpr int GATHER_U = 4;   // register gathers per lane in flight
 
 template <typename VT, typename T>
-__host__ __device__ constexpr size_t async_smem_per_warp(int cap) {
-    return (size_t)2 * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
+__host__ __device__ constexpr size_t async_smem_per_warp(int cap, int bufs) {
+    return (size_t)bufs * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
 template <typename T, typename VT, class Pre, class Epi>
@@ -257,23 +267,25 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
     const int lane = threadIdx.x & 31;
     const int sub = lane & (A.lanes - 1);
     const int cap = A.cap;
+    const int bufs = A.async;
     char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
     VT* sv = reinterpret_cast<VT*>(base);
-    int* sc = reinterpret_cast<int*>(base + 2 * cap * sizeof(VT));
-    T* sx = reinterpret_cast<T*>(base + 2 * cap * (sizeof(VT) + sizeof(int)));
-    const unsigned long long pol = l2_evict_first();
+    int* sc = reinterpret_cast<int*>(base + bufs * cap * sizeof(VT));
+    T* sx = reinterpret_cast<T*>(base + bufs * cap * (sizeof(VT) + sizeof(int)));
+    const unsigned long long stream_pol = l2_evict_first();
+    const unsigned long long keep_pol = l2_evict_last();
     const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
     const int nwarps = (gridDim.x * NT) >> 5;
     const int g0 = (blockIdx.x * NT + threadIdx.x) >> 5;
 
-    // copies of a group's values and columns into `stage` (k0, k1: its entry range)
-    auto issue = [&](int grp, int stage, int k0, int k1) {
+    // copies of a group's values and columns into buffer `b` (k0, k1: its entry range)
+    auto issue_vc = [&](int grp, int b, int k0, int k1) {
         if (grp < ngroups && k1 - k0 <= cap) {
-            VT* dv = sv + stage * cap;
-            int* dc = sc + stage * cap;
+            VT* dv = sv + b * cap;
+            int* dc = sc + b * cap;
             for (int e = lane; e < k1 - k0; e += 32) {
-                cp_async<sizeof(VT)>(dv + e, av + k0 + e, pol);
-                cp_async<4>(dc + e, A.ci + k0 + e, pol);
+                cp_async<sizeof(VT)>(dv + e, av + k0 + e, stream_pol);
+                cp_async<4>(dc + e, A.ci + k0 + e, stream_pol);
             }
         }
         cp_commit();
@@ -281,44 +293,67 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
 
     int row, rlo, rhi, nrow, nlo, nhi;
     row_bounds(A, g0, row, rlo, rhi);
-    issue(g0, 0, __shfl_sync(0xffffffffu, rlo, 0), __shfl_sync(0xffffffffu, rhi, 31));
+    issue_vc(g0, 0, __shfl_sync(0xffffffffu, rlo, 0), __shfl_sync(0xffffffffu, rhi, 31));
     row_bounds(A, g0 + nwarps, nrow, nlo, nhi);
-    int stage = 0;
-    for (int grp = g0; grp < ngroups; grp += nwarps, stage ^= 1) {
+    int b = 0;
+    for (int grp = g0; grp < ngroups; grp += nwarps) {
         const bool own = sub == 0 && row < A.n;
         const auto carried = own ? pre(row) : decltype(pre(0))(0);
-        issue(grp + nwarps, stage ^ 1, __shfl_sync(0xffffffffu, nlo, 0), __shfl_sync(0xffffffffu, nhi, 31));
         int frow, flo, fhi;
         row_bounds(A, grp + 2 * nwarps, frow, flo, fhi);
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
         const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt = k1 - k0;
-        cp_wait<1>();  // this group's values and columns have landed
+        const int nk0 = __shfl_sync(0xffffffffu, nlo, 0);
+        const int nk1 = __shfl_sync(0xffffffffu, nhi, 31);
+        // With register gathers and two buffers the next group's copies can
+        // start before this group's have landed.
+        const bool early = bufs == 2 && !A.gasync;
+        if (early) {
+            issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
+            cp_wait<1>();  // this group's values and columns have landed
+        } else {
+            cp_wait<0>();
+        }
         __syncwarp();
         acc_t s = Prec<T>::zero();
         if (cnt <= cap) {
-            const VT* cv = sv + stage * cap;
-            const int* cc = sc + stage * cap;
-            for (int b0 = 0; b0 < cnt; b0 += 32 * GATHER_U) {
-                T xv[GATHER_U];
-#pragma unroll
-                for (int j = 0; j < GATHER_U; ++j) {
-                    const int e = b0 + j * 32 + lane;
-                    if (e < cnt) xv[j] = ld_nc(v + cc[e]);
+            const int* cc = sc + b * cap;
+            if (A.gasync) {
+                for (int e = lane; e < cnt; e += 32) cp_async<sizeof(T)>(sx + e, v + cc[e], keep_pol);
+                cp_commit();
+                if (bufs == 2) {
+                    issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
+                    cp_wait<1>();  // gathers done; the next group's copies may still fly
+                } else {
+                    cp_wait<0>();
                 }
+            } else {
+                for (int b0 = 0; b0 < cnt; b0 += 32 * GATHER_U) {
+                    T xv[GATHER_U];
 #pragma unroll
-                for (int j = 0; j < GATHER_U; ++j) {
-                    const int e = b0 + j * 32 + lane;
-                    if (e < cnt) sx[e] = xv[j];
+                    for (int j = 0; j < GATHER_U; ++j) {
+                        const int e = b0 + j * 32 + lane;
+                        if (e < cnt) xv[j] = ld_nc(v + cc[e]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < GATHER_U; ++j) {
+                        const int e = b0 + j * 32 + lane;
+                        if (e < cnt) sx[e] = xv[j];
+                    }
                 }
             }
             __syncwarp();
+            const VT* cv = sv + b * cap;
             for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, cv[e], sx[e]);
         } else {
+            if (bufs == 2 && !early) issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
             s = unstaged_row<T>(A, av, GatherVec<T>{v}, rlo, rhi);
         }
         segment_sum(s, A.lanes);
-        __syncwarp();  // this stage and sx are free for reuse
+        __syncwarp();  // buffers free for reuse
+        if (bufs == 1) issue_vc(grp + nwarps, 0, nk0, nk1);
+        else b ^= 1;
         if (own) epi(row, s, carried);
         row = nrow; rlo = nlo; rhi = nhi;
         nrow = frow; nlo = flo; nhi = fhi;
@@ -475,9 +510,23 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
 }
 
 // ----------------------------------------------------------------- iteration
+// ||b - A round(x)||^2 over this CTA's rows (the true-residual check).  Kept
+// out of line: it runs only when the recursive residual has met the
+// tolerance, and inlining it would cost the main product registers.
+template <typename T>
+__device__ __noinline__ typename Prec<T>::acc residual_pass(const Mat& A, const T* __restrict__ av,
+                                                            const typename Prec<T>::xw* __restrict__ x,
+                                                            const T* __restrict__ b, double* dsm) {
+    using acc_t = typename Prec<T>::acc;
+    acc_t tr2 = Prec<T>::zero();
+    spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i) { return b[i]; },
+                    [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
+    return tr2;
+}
+
 // q = A p, delta = p.q; with `check` set, ||b - A round(x)||^2 first.
 template <typename T>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
+__global__ void __launch_bounds__(NT, SLA_ITER_MIN_CTAS)
     k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ p, T* __restrict__ q,
                 const typename Prec<T>::xw* __restrict__ x, const T* __restrict__ b) {
     using acc_t = typename Prec<T>::acc;
@@ -488,10 +537,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     av += ao; p += vo; q += vo; x += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
-    if (check) {
-        spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i) { return b[i]; },
-                        [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
-    }
+    if (check) tr2 = residual_pass<T>(A, av, x, b, dsm);
     spmv_vec<T, T>(A, av, p, [&](int i) { return p[i]; },
                    [&](int i, acc_t s, T pi) {
                        const T qi = to_store(s);

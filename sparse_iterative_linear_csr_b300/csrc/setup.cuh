@@ -95,6 +95,15 @@ __global__ void k_group_max(const int* __restrict__ rp, int n, int R, int* out) 
     if (m) atomicMax(out, m);
 }
 
+// Number of stored entries whose column is more than `w` away from the row.
+__global__ void k_far_count(const int* __restrict__ rp, const int* __restrict__ ci, int n, int w,
+                            unsigned long long* out) {
+    unsigned long long c = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        for (int k = rp[i]; k < rp[i + 1]; ++k) c += (abs(ci[k] - i) > w);
+    if (c) atomicAdd(out, c);
+}
+
 // ----------------------------------------------------------------- scan
 // Exclusive prefix sum, SCAN_T threads x SCAN_V items per CTA; CTA totals go
 // to `sums` and are scanned recursively by the host driver.

@@ -106,6 +106,7 @@ struct Layout {
     int cap = 32;
     int lanes = 1;
     int gx = 1;
+    int gasync = 0;   // gathers by cp.async (scattered columns)
 };
 
 struct sla_csr {
@@ -141,18 +142,26 @@ struct sla_csr {
     GraphCache graph[3];
 };
 
-static constexpr int MAX_CAP = 864;        // staging capacity limit (larger groups take the global path)
-static constexpr int ASYNC_MAX_CAP = 320;  // pipelined staging up to this capacity (2+ CTAs per SM)
+static constexpr int MAX_CAP = 864;  // staging capacity limit (larger groups take the global path)
 
-static bool use_async(int cap) { return cap <= ASYNC_MAX_CAP; }
-// Dynamic shared memory of the staged-SpMV kernels for capacity `cap`.
+// Staging form for capacity `cap`: 2 (cp.async, double-buffered values and
+// columns) while that fits three CTAs per SM, else 1 (single-buffered) while
+// it fits two, else 0 (register staging).
+static int staging_form(int cap) {
+    const size_t per_sm = 228 * 1024;
+    if ((size_t)NWARP * async_smem_per_warp<double, double>(cap, 2) * 3 <= per_sm) return 2;
+    if ((size_t)NWARP * async_smem_per_warp<double, double>(cap, 1) * 2 <= per_sm) return 1;
+    return 0;
+}
+// Dynamic shared memory of the staged-SpMV kernels for capacity `cap`
+// (enough for the register form too, which the true-residual pass uses).
 static size_t spmv_smem(int cap) {
     const size_t single = (size_t)cap * 2 * sizeof(double);
-    const size_t piped = async_smem_per_warp<double, double>(cap);  // largest value and vector types
-    return (size_t)NWARP * (use_async(cap) && piped > single ? piped : single);
+    const int f = staging_form(cap);
+    const size_t piped = f ? async_smem_per_warp<double, double>(cap, f) : 0;
+    return (size_t)NWARP * (piped > single ? piped : single);
 }
 static size_t grad_smem(int cap) { return spmv_smem(cap); }
-
 // Resident CTAs per SM of `kern` with `smem` bytes of dynamic shared memory
 // (the kernel must already allow that much: allow_smem).
 template <typename K>
@@ -238,10 +247,11 @@ static Mat mat_of(const int* rp, const int* ci, int n, const Layout& L) {
     m.ci = ci;
     m.n = n;
     m.cap = L.cap;
-    m.async = use_async(L.cap) ? 1 : 0;
+    m.async = staging_form(L.cap);
     m.wstride = (int)(spmv_smem(L.cap) / NWARP / sizeof(double));
     m.lanes = L.lanes;
     m.lshift = L.lanes == 4 ? 2 : (L.lanes == 2 ? 1 : 0);
+    m.gasync = L.gasync;
     return m;
 }
 
@@ -281,12 +291,29 @@ static sla_status group_max(const int* rp, int n, int rows, int* out, cudaStream
     return SLA_OK;
 }
 
-// One lane per row whenever a 32-row group fits a stage (pipelined up to
-// ASYNC_MAX_CAP entries, single-stage up to MAX_CAP); otherwise the fewest
+// One lane per row whenever a 32-row group fits a stage (up to MAX_CAP
+// entries; the staging form follows from the capacity); otherwise the fewest
 // lanes per row whose groups fit.  Measured on B300: for ~15-entry rows
 // (kNN graphs) one lane per row with single-stage staging beats two lanes
 // per row with pipelined staging.
-static sla_status choose_layout(const sla_csr* h, const int* rp, Layout* L, cudaStream_t s) {
+// Scattered columns: more than 10% of the entries lie farther than 64K
+// columns from their row (a 512 KB window of an fp64 vector).
+static constexpr int NEAR_WINDOW = 65536;
+
+static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, long long nnz, Layout* L,
+                                cudaStream_t s) {
+    {
+        DevBuf far;
+        TRY(far.alloc(sizeof(unsigned long long)));
+        CU(cudaMemsetAsync(far.p, 0, sizeof(unsigned long long), s));
+        const int g = (h->n + 255) / 256 < 2048 ? (h->n + 255) / 256 : 2048;
+        k_far_count<<<g, 256, 0, s>>>(rp, ci, h->n, NEAR_WINDOW, far.as<unsigned long long>());
+        TRY(launched());
+        unsigned long long f = 0;
+        CU(cudaMemcpyAsync(&f, far.p, sizeof f, cudaMemcpyDeviceToHost, s));
+        CU(cudaStreamSynchronize(s));
+        L->gasync = (double)f > 0.1 * (double)nnz ? 1 : 0;
+    }
     for (int lanes = 1; lanes <= 4; lanes *= 2) {
         int m = 0;
         TRY(group_max(rp, h->n, 32 / lanes, &m, s));
@@ -380,8 +407,8 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     int e = 0;
     TRY(read_int(err.as<int>(), &e, s));
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
-    TRY(choose_layout(h, h->grp.as<int>(), &h->LG, s));
-    TRY(choose_layout(h, h->gtrp.as<int>(), &h->LGT, s));
+    TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, s));
+    TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, s));
     TRY(h->z.alloc(h->es * (size_t)n * h->batch));
     TRY(h->t.alloc(h->es * (size_t)n * h->batch));
     h->spai_ready = true;
@@ -714,7 +741,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
                              (e & ERR_COL_ORDER) ? " columns not strictly ascending" : ""));
     }
     HTRY(dt == SLA_F64 ? allow_smem<double>() : allow_smem<float>());
-    HTRY(choose_layout(h, d_row_ptr, &h->LA, s));
+    HTRY(choose_layout(h, d_row_ptr, d_col_idx, nnz, &h->LA, s));
     const size_t vn = (size_t)n * batch;
     HTRY(h->diag.alloc(sizeof(double) * vn));
     HTRY(h->dinv.alloc(sizeof(double) * vn));
