@@ -34,11 +34,12 @@
  *   - Iterations = number of products A p inside the loop.
  *   - Breakdown: p.q <= 0 or not finite, r.z <= 0 or not finite, or a
  *     non-finite ||r||^2.
- *   - fp32 systems (f32 != 0): A, b are fp32 values (passed here as the exact
- *     doubles).  All arithmetic is fp64.  Every working vector of the
- *     recurrence except x (q, r, z, p and the SPAI intermediate t) is rounded
- *     to fp32 when it is assigned; x is kept in fp64 and rounded to fp32 when
- *     returned.  The true-residual test uses that rounded x.
+ *   - fp32 systems (f32 != 0): "fp32 values" are the matrix values, b and
+ *     the returned x (A, b passed here as the exact doubles).  The recurrence
+ *     itself runs at fp64 precision: all arithmetic is fp64 and the working
+ *     vectors (q, r, z, p, t) are not rounded; x is rounded to fp32 when it
+ *     is returned, and the true-residual test uses that rounded x (as do the
+ *     returned lambda and dL/dA of the adjoint).
  *
  * Build: gcc -O2 -ffp-contract=off -shared -fPIC (no fused multiply-add, so
  * every product is rounded before it is added).
@@ -56,6 +57,7 @@
 #define OR_BREAKDOWN 2
 #define OR_INVALID 3
 
+/* Value as returned to the caller: rounded to fp32 for fp32 systems. */
 static double stor(double v, int f32) { return f32 ? (double)(float)v : v; }
 
 static double dot(int n, const double* u, const double* v) {
@@ -121,17 +123,17 @@ int oracle_spai_factor(int n, const int* rp, const int* ci, const double* a,
 
 /* z = G (G^T r) + eps r.  t = G^T r is formed by scattering the rows of G
  * (t_j += G_ij r_i, rows in ascending order), so no transposed copy of G is
- * built.  t and z are rounded to the storage precision. */
+ * built.  (f32 is accepted for symmetry with the solver; working vectors are
+ * fp64 in both modes.) */
 void oracle_spai_apply(int n, const int* grp, const int* gci, const double* gv,
                        double eps, int f32, const double* r, double* t, double* z) {
     for (int j = 0; j < n; ++j) t[j] = 0.0;
     for (int i = 0; i < n; ++i)
         for (int k = grp[i]; k < grp[i + 1]; ++k) t[gci[k]] += gv[k] * r[i];
-    for (int j = 0; j < n; ++j) t[j] = stor(t[j], f32);
     for (int i = 0; i < n; ++i) {
         double s = 0.0;
         for (int k = grp[i]; k < grp[i + 1]; ++k) s += gv[k] * t[gci[k]];
-        z[i] = stor(s + eps * r[i], f32);
+        z[i] = s + eps * r[i];
     }
 }
 
@@ -158,7 +160,7 @@ typedef struct {
 
 static void apply_precond(const precond* M, int n, const double* r, double* z) {
     if (M->pc == OR_PC_JACOBI) {
-        for (int i = 0; i < n; ++i) z[i] = stor(r[i] / M->dinv_src[i], M->f32);
+        for (int i = 0; i < n; ++i) z[i] = r[i] / M->dinv_src[i];
     } else if (M->pc == OR_PC_SPAI) {
         oracle_spai_apply(n, M->grp, M->gci, M->gv, M->eps, M->f32, r, M->t, z);
     } else {
@@ -217,9 +219,9 @@ int oracle_pcg(int n, const int* rp, const int* ci, const double* a,
     if (use_x0) {
         for (int i = 0; i < n; ++i) xi[i] = x[i];
         oracle_spmv(n, rp, ci, a, xi, q);
-        for (int i = 0; i < n; ++i) r[i] = stor(b[i] - q[i], f32);
+        for (int i = 0; i < n; ++i) r[i] = b[i] - q[i];
     } else {
-        for (int i = 0; i < n; ++i) { xi[i] = 0.0; r[i] = stor(b[i], f32); }
+        for (int i = 0; i < n; ++i) { xi[i] = 0.0; r[i] = b[i]; }
     }
     apply_precond(&M, n, r, z);
     for (int i = 0; i < n; ++i) p[i] = z[i];
@@ -241,16 +243,15 @@ int oracle_pcg(int n, const int* rp, const int* ci, const double* a,
             if (!(rho_new > 0.0) || !isfinite(rho_new)) { status = OR_BREAKDOWN; break; }
             double beta = rho_new / rho;
             rho = rho_new;
-            for (int i = 0; i < n; ++i) p[i] = stor(z[i] + beta * p[i], f32);
+            for (int i = 0; i < n; ++i) p[i] = z[i] + beta * p[i];
         }
         oracle_spmv(n, rp, ci, a, p, q);
-        for (int i = 0; i < n; ++i) q[i] = stor(q[i], f32);
         double delta = dot(n, p, q);
         if (!(delta > 0.0) || !isfinite(delta)) { status = OR_BREAKDOWN; break; }
         double alpha = rho / delta;
         for (int i = 0; i < n; ++i) {
             xi[i] = xi[i] + alpha * p[i];
-            r[i] = stor(r[i] - alpha * q[i], f32);
+            r[i] = r[i] - alpha * q[i];
         }
         ++k;
         gamma = dot(n, r, r);
