@@ -61,14 +61,15 @@ def byte_model(w, nnzg=None):
     shared-pattern batch counted once."""
     A = w.A
     n, nnz, B = A.n, A.nnz, A.batch
-    s = 4 if w.dtype == "f32" else 8
+    s = 4 if w.dtype == "f32" else 8   # matrix values and caller vectors
+    v = 8                              # working vectors of the recurrence (fp64 or fp32 pairs)
     rp = 4 * (n + 1)
     if w.pc == "spai":
         it = 12 * nnz + 24 * nnzg + 3 * rp + 128 * n
     elif w.pc == "jacobi":
-        it = (s * nnz * B + 4 * nnz + rp + 13 * s * n * B)
+        it = (s * nnz * B + 4 * nnz + rp + 13 * v * n * B)
     else:
-        it = (s * nnz * B + 4 * nnz + rp + 11 * s * n * B)
+        it = (s * nnz * B + 4 * nnz + rp + 11 * v * n * B)
     spmv = s * nnz * B + 4 * nnz + rp + 2 * s * n * B
     grad = (4 * nnz + rp + s * nnz * B + 2 * s * n * B)
     return {"per_iteration": it, "spmv_dot_per_launch": spmv, "grad_A": grad}

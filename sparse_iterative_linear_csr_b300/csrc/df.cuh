@@ -65,6 +65,14 @@ __device__ __forceinline__ DF df_mul_f(DF x, float b) {
     return fast_two_sum(p.hi, p.lo);
 }
 
+// (a.hi + a.lo) * (b.hi + b.lo)
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+    DF p = two_prod(a.hi, b.hi);
+    p.lo = __fmaf_rn(a.hi, b.lo, p.lo);
+    p.lo = __fmaf_rn(a.lo, b.hi, p.lo);
+    return fast_two_sum(p.hi, p.lo);
+}
+
 // x * x
 __device__ __forceinline__ DF df_sqr(DF x) {
     DF p = two_prod(x.hi, x.hi);

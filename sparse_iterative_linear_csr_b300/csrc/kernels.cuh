@@ -76,6 +76,7 @@ struct Mat {
 template <typename T> struct Prec;
 template <> struct Prec<double> {
     using acc = double;   // row sums and inner products
+    using w = double;     // working vectors of the recurrence (r, p, q, z, t)
     using xw = double;    // stored iterate x and Jacobi reciprocal
     using gv = double;    // SPAI factor values
     using sc = double;    // broadcast solver scalars
@@ -85,7 +86,8 @@ template <> struct Prec<double> {
 };
 template <> struct Prec<float> {
     using acc = DF;
-    using xw = float2;    // (hi, lo) pair in an 8-byte slot
+    using w = float2;     // double-float pair in an 8-byte slot
+    using xw = float2;
     using gv = float2;
     using sc = DF;
     static __device__ __forceinline__ acc zero() { return DF{0.0f, 0.0f}; }
@@ -93,10 +95,26 @@ template <> struct Prec<float> {
     static __device__ __forceinline__ sc scal(double v) { return df_from_double(v); }
 };
 
+// working value <-> accumulator form
+__device__ __forceinline__ double ld_w(double v) { return v; }
+__device__ __forceinline__ DF ld_w(float2 v) { return DF{v.x, v.y}; }
+__device__ __forceinline__ DF ld_w(float v) { return DF{v, 0.0f}; }
+__device__ __forceinline__ double to_w(double s) { return s; }
+__device__ __forceinline__ float2 to_w(DF s) { return make_float2(s.hi, s.lo); }
+
+// accumulator arithmetic
+__device__ __forceinline__ double amul(double a, double b) { return a * b; }
+__device__ __forceinline__ DF amul(DF a, DF b) { return df_mul(a, b); }
+__device__ __forceinline__ double afma(double a, double b, double c) { return fma(a, b, c); }
+__device__ __forceinline__ DF afma(DF a, DF b, DF c) { return df_add(df_mul(a, b), c); }
+__device__ __forceinline__ double aneg(double a) { return -a; }
+__device__ __forceinline__ DF aneg(DF a) { return df_neg(a); }
+
 // acc += a * v
 __device__ __forceinline__ void mac(double& s, double a, double v) { s = fma(a, v, s); }
 __device__ __forceinline__ void mac(DF& s, float a, float v) { s = df_fma_ff(a, v, s); }
-__device__ __forceinline__ void mac(DF& s, float2 g, float v) { s = df_fma_df(DF{g.x, g.y}, v, s); }
+__device__ __forceinline__ void mac(DF& s, float a, float2 v) { s = df_fma_df(DF{v.x, v.y}, a, s); }
+__device__ __forceinline__ void mac(DF& s, float2 g, float2 v) { s = df_add(s, df_mul(DF{g.x, g.y}, DF{v.x, v.y})); }
 
 // stored value nearest to an accumulator
 __device__ __forceinline__ double to_store(double s) { return s; }
@@ -190,16 +208,17 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
     const int lane = threadIdx.x & 31;
     const int sub = lane & (A.lanes - 1);
     const int cap = A.cap;
+    using XT = decltype(gather(0));
     char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
     VT* sa = reinterpret_cast<VT*>(base);
-    T* sx = reinterpret_cast<T*>(base + cap * sizeof(VT));
+    XT* sx = reinterpret_cast<XT*>(base + cap * sizeof(VT));
     const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
     const int nwarps = (gridDim.x * NT) >> 5;
     for (int grp = (blockIdx.x * NT + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
         int row, rlo, rhi;
         row_bounds(A, grp, row, rlo, rhi);
         const bool own = sub == 0 && row < A.n;
-        const auto carried = own ? pre(row) : decltype(pre(0))(0);
+        const auto carried = own ? pre(row) : decltype(pre(0)){};
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
         const int k1 = __shfl_sync(0xffffffffu, rhi, 31);
         const int cnt = k1 - k0;
@@ -208,7 +227,7 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
             for (int b0 = 0; b0 < cnt; b0 += 32 * STAGE_U) {
                 int c[STAGE_U];
                 VT a[STAGE_U];
-                T xv[STAGE_U];
+                XT xv[STAGE_U];
 #pragma unroll
                 for (int j = 0; j < STAGE_U; ++j) {
                     const int e = b0 + j * 32 + lane;
@@ -260,8 +279,8 @@ __host__ __device__ constexpr size_t async_smem_per_warp(int cap, int bufs) {
     return (size_t)bufs * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
-template <typename T, typename VT, class Pre, class Epi>
-__device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v,
+template <typename T, typename VT, typename XT, class Pre, class Epi>
+__device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v,
                                                 Pre pre, Epi epi, double* wsm) {
     using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
@@ -271,7 +290,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
     char* base = reinterpret_cast<char*>(wsm + (threadIdx.x >> 5) * A.wstride);
     VT* sv = reinterpret_cast<VT*>(base);
     int* sc = reinterpret_cast<int*>(base + bufs * cap * sizeof(VT));
-    T* sx = reinterpret_cast<T*>(base + bufs * cap * (sizeof(VT) + sizeof(int)));
+    XT* sx = reinterpret_cast<XT*>(base + bufs * cap * (sizeof(VT) + sizeof(int)));
     const unsigned long long stream_pol = l2_evict_first();
     const unsigned long long keep_pol = l2_evict_last();
     const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
@@ -298,7 +317,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
     int b = 0;
     for (int grp = g0; grp < ngroups; grp += nwarps) {
         const bool own = sub == 0 && row < A.n;
-        const auto carried = own ? pre(row) : decltype(pre(0))(0);
+        const auto carried = own ? pre(row) : decltype(pre(0)){};
         int frow, flo, fhi;
         row_bounds(A, grp + 2 * nwarps, frow, flo, fhi);
         const int k0 = __shfl_sync(0xffffffffu, rlo, 0);
@@ -320,7 +339,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
         if (cnt <= cap) {
             const int* cc = sc + b * cap;
             if (A.gasync) {
-                for (int e = lane; e < cnt; e += 32) cp_async<sizeof(T)>(sx + e, v + cc[e], keep_pol);
+                for (int e = lane; e < cnt; e += 32) cp_async<sizeof(XT)>(sx + e, v + cc[e], keep_pol);
                 cp_commit();
                 if (bufs == 2) {
                     issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
@@ -330,7 +349,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
                 }
             } else {
                 for (int b0 = 0; b0 < cnt; b0 += 32 * GATHER_U) {
-                    T xv[GATHER_U];
+                    XT xv[GATHER_U];
 #pragma unroll
                     for (int j = 0; j < GATHER_U; ++j) {
                         const int e = b0 + j * 32 + lane;
@@ -348,7 +367,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
             for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, cv[e], sx[e]);
         } else {
             if (bufs == 2 && !early) issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
-            s = unstaged_row<T>(A, av, GatherVec<T>{v}, rlo, rhi);
+            s = unstaged_row<T>(A, av, GatherVec<XT>{v}, rlo, rhi);
         }
         segment_sum(s, A.lanes);
         __syncwarp();  // buffers free for reuse
@@ -363,11 +382,11 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
 
 // Product with a plain vector gather: the pipelined form when the matrix was
 // set up for it, the single-stage form otherwise.
-template <typename T, typename VT, class Pre, class Epi>
-__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const T* __restrict__ v, Pre pre,
+template <typename T, typename VT, typename XT, class Pre, class Epi>
+__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v, Pre pre,
                                          Epi epi, double* wsm) {
-    if (A.async) spmv_rows_async<T, VT>(A, av, v, pre, epi, wsm);
-    else spmv_rows<T, VT>(A, av, GatherVec<T>{v}, pre, epi, wsm);
+    if (A.async) spmv_rows_async<T, VT, XT>(A, av, v, pre, epi, wsm);
+    else spmv_rows<T, VT>(A, av, GatherVec<XT>{v}, pre, epi, wsm);
 }
 
 // ----------------------------------------------------------------- scalar logic
@@ -436,9 +455,10 @@ __device__ __forceinline__ void start_state(State* s, Ctrl* c, double bb, double
 }
 
 // ----------------------------------------------------------------- element-wise arithmetic
-// acc += a * b for stored values
+// acc += a * b
 __device__ __forceinline__ void dot_acc(double& s, double a, double b) { s = fma(a, b, s); }
 __device__ __forceinline__ void dot_acc(DF& s, float a, float b) { s = df_fma_ff(a, b, s); }
+__device__ __forceinline__ void dot_acc(DF& s, float2 a, float2 b) { s = afma(ld_w(a), ld_w(b), s); }
 
 // b - s for a row sum s
 __device__ __forceinline__ double resid(double b, double s) { return b - s; }
@@ -446,40 +466,16 @@ __device__ __forceinline__ DF resid(float b, DF s) { return df_add_f(df_neg(s), 
 __device__ __forceinline__ void sq_acc(double& t, double e) { t = fma(e, e, t); }
 __device__ __forceinline__ void sq_acc(DF& t, DF e) { t = df_add(t, df_sqr(e)); }
 
-// One element of the x / r update.  x += alpha p; r = rnd(r - alpha q);
-// g += r^2; (Jacobi) rz += r rnd(r dinv).
-template <int PC>
-__device__ __forceinline__ void update_one(double alpha, double& x, double& r, double p, double q, double dinv,
-                                           double& g, double& rz) {
-    x = fma(alpha, p, x);
-    r = fma(-alpha, q, r);
-    g = fma(r, r, g);
-    if (PC == 1) rz = fma(r, r * dinv, rz);
+// One element of the x / r update: x += alpha p; r -= alpha q; g += r^2;
+// (Jacobi) rz += r (r dinv).  A = accumulator type, W = working value type.
+template <int PC, typename A, typename W, typename XW>
+__device__ __forceinline__ void update_one(A alpha, XW& x, W& r, W p, W q, XW dinv, A& g, A& rz) {
+    x = to_w(afma(alpha, ld_w(p), ld_w(x)));
+    const A rn = afma(aneg(alpha), ld_w(q), ld_w(r));
+    r = to_w(rn);
+    g = afma(rn, rn, g);
+    if (PC == 1) rz = afma(rn, amul(rn, ld_w(dinv)), rz);
 }
-template <int PC>
-__device__ __forceinline__ void update_one(DF alpha, float2& x, float& r, float p, float q, float2 dinv, DF& g,
-                                           DF& rz) {
-    const DF xn = df_add(DF{x.x, x.y}, df_mul_f(alpha, p));
-    x = make_float2(xn.hi, xn.lo);
-    r = df_round(df_add_f(df_neg(df_mul_f(alpha, q)), r));
-    g = df_fma_ff(r, r, g);
-    if (PC == 1) {
-        const float z = df_round(df_mul_f(DF{dinv.x, dinv.y}, r));
-        rz = df_fma_ff(r, z, rz);
-    }
-}
-
-// Jacobi z = rnd(r dinv)
-__device__ __forceinline__ double jacobi_z(double r, double dinv) { return r * dinv; }
-__device__ __forceinline__ float jacobi_z(float r, float2 dinv) { return df_round(df_mul_f(DF{dinv.x, dinv.y}, r)); }
-
-// p = rnd(z + beta p)
-__device__ __forceinline__ double p_step(double beta, double p, double z) { return fma(beta, p, z); }
-__device__ __forceinline__ float p_step(DF beta, float p, float z) { return df_round(df_add_f(df_mul_f(beta, p), z)); }
-
-// z = rnd(s + eps r)
-__device__ __forceinline__ double spai_z(double s, double eps, double r) { return fma(eps, r, s); }
-__device__ __forceinline__ float spai_z(DF s, DF eps, float r) { return df_round(df_add(s, df_mul_f(eps, r))); }
 
 // -lambda_i x_j, rounded once
 __device__ __forceinline__ double neg_prod(double l, double x) { return -l * x; }
@@ -496,7 +492,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
     __shared__ double red[2 * NWARP];
     av += ao; x += vo; y += vo;
     acc_t acc = Prec<T>::zero();
-    spmv_vec<T, T>(A, av, x, [&](int i) { return x[i]; },
+    spmv_vec<T, T, T>(A, av, x, [&](int i) { return x[i]; },
                    [&](int i, acc_t s, T xi) {
                        const T yi = to_store(s);
                        y[i] = yi;
@@ -527,9 +523,11 @@ __device__ __noinline__ typename Prec<T>::acc residual_pass(const Mat& A, const 
 // q = A p, delta = p.q; with `check` set, ||b - A round(x)||^2 first.
 template <typename T>
 __global__ void __launch_bounds__(NT, SLA_ITER_MIN_CTAS)
-    k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ p, T* __restrict__ q,
-                const typename Prec<T>::xw* __restrict__ x, const T* __restrict__ b) {
+    k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const typename Prec<T>::w* __restrict__ p,
+                typename Prec<T>::w* __restrict__ q, const typename Prec<T>::xw* __restrict__ x,
+                const T* __restrict__ b) {
     using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
@@ -538,22 +536,19 @@ __global__ void __launch_bounds__(NT, SLA_ITER_MIN_CTAS)
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
     if (check) tr2 = residual_pass<T>(A, av, x, b, dsm);
-    spmv_vec<T, T>(A, av, p, [&](int i) { return p[i]; },
-                   [&](int i, acc_t s, T pi) {
-                       const T qi = to_store(s);
-                       q[i] = qi;
-                       dot_acc(delta, pi, qi);
-                   },
-                   dsm);
+    spmv_vec<T, T, W>(A, av, p, [&](int i) { return p[i]; },
+                      [&](int i, acc_t s, W pi) {
+                          const W qi = to_w(s);
+                          q[i] = qi;
+                          dot_acc(delta, pi, qi);
+                      },
+                      dsm);
     double v[2] = {Prec<T>::total(delta), Prec<T>::total(tr2)}, tot[2];
     if (grid_sum<2>(v, part, cnt, tot, red) && threadIdx.x == 0) after_spmv(st, S.ctl, tot[0], check, tot[1]);
 }
 
-// Pairs of consecutive entries (8/16-byte vector accesses) for the streaming
+// Pairs of consecutive 8-byte entries (16-byte accesses) for the streaming
 // kernels; used when n is even, so every system's vectors stay aligned.
-template <typename T> struct Pair;
-template <> struct Pair<double> { using type = double2; };
-template <> struct Pair<float> { using type = float2; };
 template <typename X> struct XPair;
 template <> struct XPair<double> { using type = double2; };
 template <> struct XPair<float2> { using type = float4; };
@@ -569,21 +564,24 @@ __device__ __forceinline__ float4 join2(float2 a, float2 b) { return make_float4
 // x += alpha p; r -= alpha q; gamma = r.r; rho' = r.z (PC 0: z = r, PC 1:
 // z = r / A_ii; PC 2: z comes later from the SPAI kernels).
 template <typename T, int PC, bool PAIRS>
-__global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __restrict__ x, T* __restrict__ r,
-                                               const T* __restrict__ p, const T* __restrict__ q,
+__global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __restrict__ x,
+                                               typename Prec<T>::w* __restrict__ r,
+                                               const typename Prec<T>::w* __restrict__ p,
+                                               const typename Prec<T>::w* __restrict__ q,
                                                const typename Prec<T>::xw* __restrict__ dinv) {
     using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     using XW = typename Prec<T>::xw;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     __shared__ double red[2 * NWARP];
     x += vo; r += vo; p += vo; q += vo;
     if (PC == 1) dinv += vo;
-    const typename Prec<T>::sc alpha = Prec<T>::scal(ld_cg(&st->alpha));
+    const acc_t alpha = Prec<T>::scal(ld_cg(&st->alpha));
     acc_t g = Prec<T>::zero(), rz = Prec<T>::zero();
     if (PAIRS) {
         // two pairs per thread per trip, all loads issued before any use
-        using P2 = typename Pair<T>::type;
+        using P2 = typename XPair<W>::type;
         using X2 = typename XPair<XW>::type;
         const int n2 = S.n >> 1;
         const int stride = gridDim.x * NT;
@@ -606,22 +604,23 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __re
                 const int i = i0 + u * stride;
                 if (i < n2) {
                     XW xa, xb, da{}, db{};
+                    W pa, pb, qa, qb, ra, rb;
                     split2(x2[u], xa, xb);
+                    split2(p2[u], pa, pb);
+                    split2(q2[u], qa, qb);
+                    split2(r2[u], ra, rb);
                     if (PC == 1) split2(d2[u], da, db);
-                    T ra = r2[u].x, rb = r2[u].y;
-                    update_one<PC>(alpha, xa, ra, p2[u].x, q2[u].x, da, g, rz);
-                    update_one<PC>(alpha, xb, rb, p2[u].y, q2[u].y, db, g, rz);
+                    update_one<PC>(alpha, xa, ra, pa, qa, da, g, rz);
+                    update_one<PC>(alpha, xb, rb, pb, qb, db, g, rz);
                     reinterpret_cast<X2*>(x)[i] = join2(xa, xb);
-                    r2[u].x = ra;
-                    r2[u].y = rb;
-                    reinterpret_cast<P2*>(r)[i] = r2[u];
+                    reinterpret_cast<P2*>(r)[i] = join2(ra, rb);
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
             XW xi = x[i];
-            T ri = r[i];
+            W ri = r[i];
             update_one<PC>(alpha, xi, ri, ld_stream(p + i), ld_stream(q + i), PC == 1 ? dinv[i] : XW{}, g, rz);
             x[i] = xi;
             r[i] = ri;
@@ -633,28 +632,31 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __re
 }
 
 // p = z + beta p   (INIT: p = z)
-template <typename T, int PC, bool INIT>
-__device__ __forceinline__ T pnew(typename Prec<T>::sc beta, T p, T r, typename Prec<T>::xw dinv, T z) {
-    T zi;
-    if (PC == 0) zi = r;
-    else if (PC == 1) zi = jacobi_z(r, dinv);
-    else zi = z;
-    return INIT ? zi : p_step(beta, p, zi);
+template <int PC, bool INIT, typename A, typename W, typename XW>
+__device__ __forceinline__ W pnew(A beta, W p, W r, XW dinv, W z) {
+    A zi;
+    if (PC == 0) zi = ld_w(r);
+    else if (PC == 1) zi = amul(ld_w(r), ld_w(dinv));
+    else zi = ld_w(z);
+    return INIT ? to_w(zi) : to_w(afma(beta, ld_w(p), zi));
 }
 
 template <typename T, int PC, bool INIT, bool PAIRS>
-__global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const T* __restrict__ r,
-                                                const T* __restrict__ z,
+__global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __restrict__ p,
+                                                const typename Prec<T>::w* __restrict__ r,
+                                                const typename Prec<T>::w* __restrict__ z,
                                                 const typename Prec<T>::xw* __restrict__ dinv) {
+    using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     using XW = typename Prec<T>::xw;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     p += vo; r += vo;
     if (PC == 1) dinv += vo;
     if (PC == 2) z += vo;
-    const typename Prec<T>::sc beta = Prec<T>::scal(INIT ? 0.0 : ld_cg(&st->beta));
+    const acc_t beta = Prec<T>::scal(INIT ? 0.0 : ld_cg(&st->beta));
     if (PAIRS) {
-        using P2 = typename Pair<T>::type;
+        using P2 = typename XPair<W>::type;
         using X2 = typename XPair<XW>::type;
         const int n2 = S.n >> 1;
         const int stride = gridDim.x * NT;
@@ -676,17 +678,19 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const 
                 const int i = i0 + u * stride;
                 if (i < n2) {
                     XW da{}, db{};
+                    W ra, rb, pa, pb, za, zb;
+                    split2(r2[u], ra, rb);
+                    split2(p2[u], pa, pb);
+                    split2(z2[u], za, zb);
                     if (PC == 1) split2(d2[u], da, db);
-                    p2[u].x = pnew<T, PC, INIT>(beta, p2[u].x, r2[u].x, da, z2[u].x);
-                    p2[u].y = pnew<T, PC, INIT>(beta, p2[u].y, r2[u].y, db, z2[u].y);
-                    reinterpret_cast<P2*>(p)[i] = p2[u];
+                    reinterpret_cast<P2*>(p)[i] =
+                        join2(pnew<PC, INIT>(beta, pa, ra, da, za), pnew<PC, INIT>(beta, pb, rb, db, zb));
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT)
-            p[i] = pnew<T, PC, INIT>(beta, INIT ? T(0) : p[i], r[i], PC == 1 ? dinv[i] : XW{},
-                                     PC == 2 ? z[i] : T(0));
+            p[i] = pnew<PC, INIT>(beta, INIT ? W{} : p[i], r[i], PC == 1 ? dinv[i] : XW{}, PC == 2 ? z[i] : W{});
     }
 }
 
@@ -695,37 +699,41 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, T* __restrict__ p, const 
 template <typename T>
 __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gtv,
-                                                              const T* __restrict__ r, T* __restrict__ t) {
+                                                              const typename Prec<T>::w* __restrict__ r,
+                                                              typename Prec<T>::w* __restrict__ t) {
     using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
-    spmv_vec<T, typename Prec<T>::gv>(GT, gtv, r, [](int) { return T(0); },
-                                      [&](int i, acc_t s, T) { t[i] = to_store(s); }, dsm);
+    spmv_vec<T, typename Prec<T>::gv, W>(GT, gtv, r, [](int) { return W{}; },
+                                         [&](int i, acc_t s, W) { t[i] = to_w(s); }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
 template <typename T>
 __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gv,
-                                                              const T* __restrict__ t, const T* __restrict__ r,
-                                                              T* __restrict__ z, double eps) {
+                                                              const typename Prec<T>::w* __restrict__ t,
+                                                              const typename Prec<T>::w* __restrict__ r,
+                                                              typename Prec<T>::w* __restrict__ z, double eps) {
     using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
     gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
-    const typename Prec<T>::sc e = Prec<T>::scal(eps);
+    const acc_t e = Prec<T>::scal(eps);
     acc_t rz = Prec<T>::zero();
-    spmv_vec<T, typename Prec<T>::gv>(G, gv, t, [&](int i) { return r[i]; },
-                                      [&](int i, acc_t s, T ri) {
-                                          const T zi = spai_z(s, e, ri);
-                                          z[i] = zi;
-                                          dot_acc(rz, ri, zi);
-                                      },
-                                      dsm);
+    spmv_vec<T, typename Prec<T>::gv, W>(G, gv, t, [&](int i) { return r[i]; },
+                                         [&](int i, acc_t s, W ri) {
+                                             const W zi = to_w(afma(e, ld_w(ri), s));
+                                             z[i] = zi;
+                                             dot_acc(rz, ri, zi);
+                                         },
+                                         dsm);
     double v[1] = {Prec<T>::total(rz)}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) new_direction(st, S.ctl, tot[0]);
 }
@@ -734,8 +742,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long
 // x = 0, r = b, b copied into the workspace, bb = b.b.
 template <typename T>
 __global__ void __launch_bounds__(NT) k_init(Sys S, const T* __restrict__ b_user, T* __restrict__ bw,
-                                             typename Prec<T>::xw* __restrict__ x, T* __restrict__ r, double tol,
-                                             int max_iter) {
+                                             typename Prec<T>::xw* __restrict__ x, typename Prec<T>::w* __restrict__ r,
+                                             double tol, int max_iter) {
     SYS_PROLOGUE
     __shared__ double red[2 * NWARP];
     b_user += vo; bw += vo; x += vo; r += vo;
@@ -743,7 +751,7 @@ __global__ void __launch_bounds__(NT) k_init(Sys S, const T* __restrict__ b_user
     for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
         const T bi = b_user[i];
         bw[i] = bi;
-        r[i] = bi;
+        r[i] = to_w(ld_w(bi));
         x[i] = typename Prec<T>::xw{};
         dot_acc(bb, bi, bi);
     }
@@ -759,8 +767,10 @@ __device__ __forceinline__ float2 x_from(float v) { return make_float2(v, 0.0f);
 template <typename T>
 __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     k_init_x0(Mat A, Sys S, const T* __restrict__ av, const T* __restrict__ b_user, const T* __restrict__ x0,
-              T* __restrict__ bw, typename Prec<T>::xw* __restrict__ x, T* __restrict__ r, double tol, int max_iter) {
+              T* __restrict__ bw, typename Prec<T>::xw* __restrict__ x, typename Prec<T>::w* __restrict__ r,
+              double tol, int max_iter) {
     using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     SYS_PROLOGUE
     extern __shared__ double dsm[];
     __shared__ double red[2 * NWARP];
@@ -770,10 +780,10 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
                     [&](int i, acc_t s, T bi) {
                         bw[i] = bi;
                         x[i] = x_from(x0[i]);
-                        const T ri = to_store(resid(bi, s));
-                        r[i] = ri;
+                        const acc_t ri = resid(bi, s);
+                        r[i] = to_w(ri);
                         dot_acc(bb, bi, bi);
-                        dot_acc(g, ri, ri);
+                        g = afma(ri, ri, g);
                     },
                     dsm);
     double v[2] = {Prec<T>::total(bb), Prec<T>::total(g)}, tot[2];
@@ -783,19 +793,22 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
 
 // First direction for PC 0 / 1: p = z, rho = r.z.
 template <typename T, int PC>
-__global__ void __launch_bounds__(NT) k_init_dir(Sys S, T* __restrict__ p, const T* __restrict__ r,
+__global__ void __launch_bounds__(NT) k_init_dir(Sys S, typename Prec<T>::w* __restrict__ p,
+                                                 const typename Prec<T>::w* __restrict__ r,
                                                  const typename Prec<T>::xw* __restrict__ dinv) {
+    using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     __shared__ double red[2 * NWARP];
     p += vo; r += vo;
     if (PC == 1) dinv += vo;
-    typename Prec<T>::acc rz = Prec<T>::zero();
+    acc_t rz = Prec<T>::zero();
     for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-        const T ri = r[i];
-        const T zi = PC == 1 ? jacobi_z(ri, dinv[i]) : ri;
-        p[i] = zi;
-        dot_acc(rz, ri, zi);
+        const W ri = r[i];
+        const acc_t zi = PC == 1 ? amul(ld_w(ri), ld_w(dinv[i])) : ld_w(ri);
+        p[i] = to_w(zi);
+        rz = afma(ld_w(ri), zi, rz);
     }
     double v[1] = {Prec<T>::total(rz)}, tot[1];
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) new_direction(st, S.ctl, tot[0]);

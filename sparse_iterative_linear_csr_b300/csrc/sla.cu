@@ -142,6 +142,7 @@ struct sla_csr {
     GraphCache graph[3];
 };
 
+static constexpr size_t WORK_BYTES = 8;  // working vectors: fp64, or a double-float pair
 static constexpr int MAX_CAP = 864;  // staging capacity limit (larger groups take the global path)
 
 // Staging form for capacity `cap`: 2 (cp.async, double-buffered values and
@@ -409,8 +410,8 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
     TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, s));
     TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, s));
-    TRY(h->z.alloc(h->es * (size_t)n * h->batch));
-    TRY(h->t.alloc(h->es * (size_t)n * h->batch));
+    TRY(h->z.alloc(WORK_BYTES * (size_t)n * h->batch));
+    TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
     h->spai_ready = true;
     return ensure_pstride(h);
 }
@@ -436,9 +437,10 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     const Sys S = sys_of(h);
     const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
     const T* av = (const T*)h->vals;
-    T* r = h->r.as<T>();
-    T* p = h->p.as<T>();
-    T* q = h->q.as<T>();
+    using W = typename Prec<T>::w;
+    W* r = h->r.as<W>();
+    W* p = h->p.as<W>();
+    W* q = h->q.as<W>();
     using XW = typename Prec<T>::xw;
     using GV = typename Prec<T>::gv;
     XW* x = h->x.as<XW>();
@@ -453,12 +455,12 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
         const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
         k_spai_t<T><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
                                                                                         h->gtv.as<GV>(), r,
-                                                                                        h->t.as<T>());
+                                                                                        h->t.as<W>());
         TRY(launched());
         k_spai_z<T><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
-            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
         TRY(launched());
-        k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
+        k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<W>(), dinv);
         TRY(launched());
         *nodes += 5;
     } else if (pc == SLA_PC_JACOBI) {
@@ -540,8 +542,9 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
     const T* av = (const T*)h->vals;
     const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
-    T* r = h->r.as<T>();
-    T* p = h->p.as<T>();
+    using W = typename Prec<T>::w;
+    W* r = h->r.as<W>();
+    W* p = h->p.as<W>();
     using XW = typename Prec<T>::xw;
     using GV = typename Prec<T>::gv;
     XW* x = h->x.as<XW>();
@@ -560,12 +563,12 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
         const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
         k_spai_t<T><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
                                                                                        h->gtv.as<GV>(), r,
-                                                                                       h->t.as<T>());
+                                                                                       h->t.as<W>());
         TRY(launched());
         k_spai_z<T><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
-            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<T>(), r, h->z.as<T>(), eps);
+            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
         TRY(launched());
-        k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<T>(), dinv);
+        k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<W>(), dinv);
     } else if (pc == SLA_PC_JACOBI) {
         k_init_dir<T, 1><<<gv, NT, 0, s>>>(S, p, r, dinv);
     } else {
@@ -747,9 +750,9 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     HTRY(h->dinv.alloc(sizeof(double) * vn));
     HTRY(compute_diag(h, s));
     HTRY(h->x.alloc(sizeof(double) * vn));
-    HTRY(h->r.alloc(h->es * vn));
-    HTRY(h->p.alloc(h->es * vn));
-    HTRY(h->q.alloc(h->es * vn));
+    HTRY(h->r.alloc(WORK_BYTES * vn));
+    HTRY(h->p.alloc(WORK_BYTES * vn));
+    HTRY(h->q.alloc(WORK_BYTES * vn));
     HTRY(h->bw.alloc(h->es * vn));
     HTRY(h->state.alloc(sizeof(State) * batch));
     HTRY(h->ctl.alloc(sizeof(Ctrl)));
