@@ -4,7 +4,7 @@
 
 The library is one translation unit (csrc/sla.cu) with the CUDA runtime
 linked statically, so it loads next to PyTorch without sharing its runtime.
-SLA_NVCC_EXTRA adds nvcc flags (e.g. -DSLA_ITER_MIN_CTAS=3 for tuning runs).
+SLA_NVCC_EXTRA adds nvcc flags for tuning runs.
 """
 from __future__ import annotations
 

@@ -11,10 +11,11 @@ namespace sla {
 constexpr int NT = 256;          // threads per CTA for every kernel here
 constexpr int NWARP = NT / 32;
 constexpr int SPMV_MIN_CTAS = 4; // resident CTAs per SM the staged-SpMV kernels are compiled for
-#ifndef SLA_ITER_MIN_CTAS
-#define SLA_ITER_MIN_CTAS 3      // ... and the CG product kernel (which also carries the residual check;
-                                 // measured faster unspilled at 3 than spilled at 4)
-#endif
+// Resident CTAs per SM the CG product kernel (which also carries the residual
+// check) is compiled for: fp64 measured faster unspilled at 3 than spilled
+// at 4; fp32 fits 4 unspilled.
+template <typename T> struct IterMinCtas { static constexpr int value = 3; };
+template <> struct IterMinCtas<float> { static constexpr int value = 4; };
 constexpr int MAXR = NT;         // rows per row block (one row per thread)
 
 // Outcome codes mirrored from sla_status (kept numerically equal).

@@ -59,8 +59,6 @@ struct Mat {
     int wstride;      // doubles of shared memory per warp (both staging forms)
     int lanes;        // lanes per row: 1, 2 or 4 (a group holds 32 / lanes rows)
     int lshift;       // log2(lanes)
-    int gasync;       // 1: gathers by cp.async (scattered columns); 0: through registers
-                      //    (columns near the row: the gathers mostly hit L1)
 };
 
 #define SYS_PROLOGUE                                            \
@@ -267,7 +265,7 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
 // copies are double-buffered: the next group's copies are issued as soon as
 // the current group's gathers are, so only the gather latency is exposed per
 // group; with A.async == 1 (large groups) they are single-buffered.  For
-// matrices whose columns stay near the row (A.gasync == 0) the gathers go
+// matrices whose columns stay near the row (GASYNC false) the gathers go
 // through registers instead, GATHER_U per lane in flight: they mostly hit L1,
 // which the asynchronous copies serve less well.  Row bounds are loaded one
 // group ahead.
@@ -279,7 +277,7 @@ __host__ __device__ constexpr size_t async_smem_per_warp(int cap, int bufs) {
     return (size_t)bufs * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
-template <typename T, typename VT, typename XT, class Pre, class Epi>
+template <typename T, typename VT, typename XT, bool GASYNC, class Pre, class Epi>
 __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v,
                                                 Pre pre, Epi epi, double* wsm) {
     using acc_t = typename Prec<T>::acc;
@@ -327,7 +325,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
         const int nk1 = __shfl_sync(0xffffffffu, nhi, 31);
         // With register gathers and two buffers the next group's copies can
         // start before this group's have landed.
-        const bool early = bufs == 2 && !A.gasync;
+        const bool early = bufs == 2 && !GASYNC;
         if (early) {
             issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
             cp_wait<1>();  // this group's values and columns have landed
@@ -338,7 +336,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
         acc_t s = Prec<T>::zero();
         if (cnt <= cap) {
             const int* cc = sc + b * cap;
-            if (A.gasync) {
+            if (GASYNC) {
                 for (int e = lane; e < cnt; e += 32) cp_async<sizeof(XT)>(sx + e, v + cc[e], keep_pol);
                 cp_commit();
                 if (bufs == 2) {
@@ -380,13 +378,15 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
     cp_wait<0>();
 }
 
-// Product with a plain vector gather: the pipelined form when the matrix was
-// set up for it, the single-stage form otherwise.
-template <typename T, typename VT, typename XT, class Pre, class Epi>
+// Product with a plain vector gather in one of three compiled forms (the
+// host picks one per matrix, so each kernel instantiation carries a single
+// path): FORM 0 register staging (spmv_rows); FORM 1 cp.async value/column
+// staging with register gathers; FORM 2 cp.async staging and gathers.
+template <typename T, int FORM, typename VT, typename XT, class Pre, class Epi>
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v, Pre pre,
                                          Epi epi, double* wsm) {
-    if (A.async) spmv_rows_async<T, VT, XT>(A, av, v, pre, epi, wsm);
-    else spmv_rows<T, VT>(A, av, GatherVec<XT>{v}, pre, epi, wsm);
+    if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT>{v}, pre, epi, wsm);
+    else spmv_rows_async<T, VT, XT, FORM == 2>(A, av, v, pre, epi, wsm);
 }
 
 // ----------------------------------------------------------------- scalar logic
@@ -483,7 +483,7 @@ __device__ __forceinline__ float neg_prod(float l, float x) { return df_round(tw
 
 // ----------------------------------------------------------------- SpMV API
 // y = A x, and dot[sys] = x.y when dot != nullptr.
-template <typename T>
+template <typename T, int FORM>
 __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const T* __restrict__ av,
                                                             const T* __restrict__ x, T* __restrict__ y, double* dot) {
     using acc_t = typename Prec<T>::acc;
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
     __shared__ double red[2 * NWARP];
     av += ao; x += vo; y += vo;
     acc_t acc = Prec<T>::zero();
-    spmv_vec<T, T, T>(A, av, x, [&](int i) { return x[i]; },
+    spmv_vec<T, FORM, T, T>(A, av, x, [&](int i) { return x[i]; },
                    [&](int i, acc_t s, T xi) {
                        const T yi = to_store(s);
                        y[i] = yi;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
 // ||b - A round(x)||^2 over this CTA's rows (the true-residual check).  Kept
 // out of line: it runs only when the recursive residual has met the
 // tolerance, and inlining it would cost the main product registers.
-template <typename T>
+template <typename T, int FORM>
 __device__ __noinline__ typename Prec<T>::acc residual_pass(const Mat& A, const T* __restrict__ av,
                                                             const typename Prec<T>::xw* __restrict__ x,
                                                             const T* __restrict__ b, double* dsm) {
@@ -521,8 +521,8 @@ __device__ __noinline__ typename Prec<T>::acc residual_pass(const Mat& A, const 
 }
 
 // q = A p, delta = p.q; with `check` set, ||b - A round(x)||^2 first.
-template <typename T>
-__global__ void __launch_bounds__(NT, SLA_ITER_MIN_CTAS)
+template <typename T, int FORM>
+__global__ void __launch_bounds__(NT, IterMinCtas<T>::value)
     k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const typename Prec<T>::w* __restrict__ p,
                 typename Prec<T>::w* __restrict__ q, const typename Prec<T>::xw* __restrict__ x,
                 const T* __restrict__ b) {
@@ -535,8 +535,8 @@ __global__ void __launch_bounds__(NT, SLA_ITER_MIN_CTAS)
     av += ao; p += vo; q += vo; x += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
-    if (check) tr2 = residual_pass<T>(A, av, x, b, dsm);
-    spmv_vec<T, T, W>(A, av, p, [&](int i) { return p[i]; },
+    if (check) tr2 = residual_pass<T, FORM>(A, av, x, b, dsm);
+    spmv_vec<T, FORM, T, W>(A, av, p, [&](int i) { return p[i]; },
                       [&](int i, acc_t s, W pi) {
                           const W qi = to_w(s);
                           q[i] = qi;
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __re
 
 // SPAI, first product: t = G^T r (explicit transposed CSR of G; G values
 // are per system, [batch][nnz(G)]).
-template <typename T>
+template <typename T, int FORM>
 __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gtv,
                                                               const typename Prec<T>::w* __restrict__ r,
@@ -707,12 +707,12 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, lon
     if (ld_cg(&st->done)) return;
     extern __shared__ double dsm[];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
-    spmv_vec<T, typename Prec<T>::gv, W>(GT, gtv, r, [](int) { return W{}; },
+    spmv_vec<T, FORM, typename Prec<T>::gv, W>(GT, gtv, r, [](int) { return W{}; },
                                          [&](int i, acc_t s, W) { t[i] = to_w(s); }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
-template <typename T>
+template <typename T, int FORM>
 __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gv,
                                                               const typename Prec<T>::w* __restrict__ t,
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long
     gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
     const acc_t e = Prec<T>::scal(eps);
     acc_t rz = Prec<T>::zero();
-    spmv_vec<T, typename Prec<T>::gv, W>(G, gv, t, [&](int i) { return r[i]; },
+    spmv_vec<T, FORM, typename Prec<T>::gv, W>(G, gv, t, [&](int i) { return r[i]; },
                                          [&](int i, acc_t s, W ri) {
                                              const W zi = to_w(afma(e, ld_w(ri), s));
                                              z[i] = zi;

@@ -193,28 +193,56 @@ static long long vec_units(const sla_csr* h) {
     return (m + NT - 1) / NT;
 }
 
-// Allow every staged-SpMV kernel of dtype T the largest staging slice.
+// Allow every staged-SpMV kernel of dtype T (all three staging forms) the
+// largest staging slice.
+template <typename T, int F>
+static sla_status allow_smem_form(int b) {
+    CU(cudaFuncSetAttribute(k_spmv<T, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_spmv_iter<T, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_spai_t<T, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_spai_z<T, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    return SLA_OK;
+}
+
 template <typename T>
 static sla_status allow_smem() {
     static std::atomic<int> done{0};
     if (done.load()) return SLA_OK;
     const int b = (int)spmv_smem(MAX_CAP);
-    CU(cudaFuncSetAttribute(k_spmv<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
-    CU(cudaFuncSetAttribute(k_spmv_iter<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    TRY((allow_smem_form<T, 0>(b)));
+    TRY((allow_smem_form<T, 1>(b)));
+    TRY((allow_smem_form<T, 2>(b)));
     CU(cudaFuncSetAttribute(k_init_x0<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
     CU(cudaFuncSetAttribute(k_final<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
-    CU(cudaFuncSetAttribute(k_spai_t<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
-    CU(cudaFuncSetAttribute(k_spai_z<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
     CU(cudaFuncSetAttribute(k_grad_A<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
     done.store(1);
     return SLA_OK;
+}
+
+// Compiled form of the staged product for a layout (see spmv_vec).
+static int form_of(const Layout& L) {
+    if (staging_form(L.cap) == 0) return 0;
+    return L.gasync ? 2 : 1;
+}
+
+template <class F>
+static void with_form(int form, F&& f) {
+    switch (form) {
+        case 0: f(std::integral_constant<int, 0>{}); break;
+        case 1: f(std::integral_constant<int, 1>{}); break;
+        default: f(std::integral_constant<int, 2>{}); break;
+    }
 }
 
 // CTAs per system for the staged SpMV kernels with staging capacity `cap`.
 template <typename T>
 static sla_status spmv_grid(const sla_csr* h, Layout* L) {
     int per = 1;
-    TRY(occupancy(k_spmv_iter<T>, spmv_smem(L->cap), &per));
+    sla_status st = SLA_OK;
+    with_form(form_of(*L), [&](auto f) {
+        st = occupancy(k_spmv_iter<T, decltype(f)::value>, spmv_smem(L->cap), &per);
+    });
+    TRY(st);
     L->gx = grid_x(h, group_ctas(h->n, L->lanes), per);
     return SLA_OK;
 }
@@ -252,7 +280,6 @@ static Mat mat_of(const int* rp, const int* ci, int n, const Layout& L) {
     m.wstride = (int)(spmv_smem(L.cap) / NWARP / sizeof(double));
     m.lanes = L.lanes;
     m.lshift = L.lanes == 4 ? 2 : (L.lanes == 2 ? 1 : 0);
-    m.gasync = L.gasync;
     return m;
 }
 
@@ -446,19 +473,25 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     XW* x = h->x.as<XW>();
     const XW* dinv = h->dinv.as<XW>();
     const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
-    k_spmv_iter<T><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    with_form(form_of(h->LA), [&](auto f) {
+        k_spmv_iter<T, decltype(f)::value><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    });
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
         k_update<T, 2, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
         TRY(launched());
         const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->LGT);
         const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
-        k_spai_t<T><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
+        with_form(form_of(h->LGT), [&](auto f) {
+        k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
                                                                                         h->gtv.as<GV>(), r,
                                                                                         h->t.as<W>());
+        });
         TRY(launched());
-        k_spai_z<T><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
+        with_form(form_of(h->LG), [&](auto f) {
+        k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
             G, S, h->nnzg, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
+        });
         TRY(launched());
         k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<W>(), dinv);
         TRY(launched());
@@ -561,12 +594,16 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     if (pc == SLA_PC_SPAI) {
         const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->LGT);
         const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
-        k_spai_t<T><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
+        with_form(form_of(h->LGT), [&](auto f) {
+        k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
                                                                                        h->gtv.as<GV>(), r,
                                                                                        h->t.as<W>());
+        });
         TRY(launched());
-        k_spai_z<T><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
+        with_form(form_of(h->LG), [&](auto f) {
+        k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
             G, S, h->nnzg, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
+        });
         TRY(launched());
         k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<W>(), dinv);
     } else if (pc == SLA_PC_JACOBI) {
@@ -789,10 +826,14 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
     const dim3 g(h->LA.gx, h->batch);
     const size_t sm = spmv_smem(h->LA.cap);
-    if (h->dt == SLA_F64)
-        k_spmv<double><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_x, (double*)d_y, d_dot);
-    else
-        k_spmv<float><<<g, NT, sm, s>>>(A, S, (const float*)h->vals, (const float*)d_x, (float*)d_y, d_dot);
+    with_form(form_of(h->LA), [&](auto f) {
+        constexpr int F = decltype(f)::value;
+        if (h->dt == SLA_F64)
+            k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_x, (double*)d_y,
+                                                d_dot);
+        else
+            k_spmv<float, F><<<g, NT, sm, s>>>(A, S, (const float*)h->vals, (const float*)d_x, (float*)d_y, d_dot);
+    });
     return launched();
 }
 
@@ -903,7 +944,7 @@ static sla_status spmv_dot_static_impl(int n, long long nnz, int batch, const in
     CU(cudaGetDevice(&dev));
     CU(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const size_t smem = spmv_smem(STATIC_CAP);
-    TRY(occupancy(k_spmv<T>, smem, &per));
+    TRY(occupancy(k_spmv<T, 1>, smem, &per));   // STATIC_CAP fits the pipelined form
     long long gx = (long long)per * sms / batch;
     if (gx > group_ctas(n, 1)) gx = group_ctas(n, 1);
     if (gx > STATIC_PARTIALS / batch) gx = STATIC_PARTIALS / batch;
@@ -923,8 +964,9 @@ static sla_status spmv_dot_static_impl(int n, long long nnz, int batch, const in
     Layout L;
     L.cap = STATIC_CAP;
     L.lanes = 1;
+    L.gasync = 0;
     const Mat A = mat_of(rp, ci, n, L);
-    k_spmv<T><<<dim3((unsigned)gx, batch), NT, smem, s>>>(A, S, vals, x, y, dot);
+    k_spmv<T, 1><<<dim3((unsigned)gx, batch), NT, smem, s>>>(A, S, vals, x, y, dot);
     return launched();
 }
 
