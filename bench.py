@@ -64,12 +64,17 @@ def byte_model(w, nnzg=None):
     s = 4 if w.dtype == "f32" else 8   # matrix values and caller vectors
     v = 8                              # working vectors of the recurrence (fp64 or fp32 pairs)
     rp = 4 * (n + 1)
+    # vector passes per iteration: product (p gathered once, q written) 2;
+    # residual update (r, q [, dinv] read; r [, z] written) 3 or 5;
+    # direction update (p, x, z read; p, x written) 5; SPAI adds t = G^T r
+    # (r gathered, t written) 2 and z = G t + eps r (t gathered, r read,
+    # z written) 3.
     if w.pc == "spai":
-        it = 12 * nnz + 24 * nnzg + 3 * rp + 128 * n
+        it = 12 * nnz + 24 * nnzg + 3 * rp + 15 * 8 * n
     elif w.pc == "jacobi":
-        it = (s * nnz * B + 4 * nnz + rp + 13 * v * n * B)
+        it = (s * nnz * B + 4 * nnz + rp + 12 * v * n * B)
     else:
-        it = (s * nnz * B + 4 * nnz + rp + 11 * v * n * B)
+        it = (s * nnz * B + 4 * nnz + rp + 10 * v * n * B)
     spmv = s * nnz * B + 4 * nnz + rp + 2 * s * n * B
     grad = (4 * nnz + rp + s * nnz * B + 2 * s * n * B)
     return {"per_iteration": it, "spmv_dot_per_launch": spmv, "grad_A": grad}
@@ -225,6 +230,10 @@ def main():
     ap.add_argument("--poll-k", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--warp-pipeline", action="store_true",
+                    help="use the warp-pipeline product where it applies")
+    ap.add_argument("--persistent", action="store_true",
+                    help="CG / Jacobi-PCG as the persistent iteration kernel (not a graph of kernels)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -257,7 +266,7 @@ def main():
     vals = torch.from_numpy(A.vals).to(dev)
     b = torch.from_numpy(w.b).to(dev)
     g = torch.from_numpy(w.g).to(dev)
-    M = sla.CSRMatrix(rp, ci, vals)
+    M = sla.CSRMatrix(rp, ci, vals, pipeline=args.warp_pipeline, fused=args.persistent)
     kw = dict(tol=w.tol, max_iter=MAX_ITER, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3,
               poll_k=args.poll_k)
 
@@ -400,7 +409,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "iterations/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
-            "wall_s_timed": t_wall, "kernel_src": src,
+            "wall_s_timed": t_wall, "kernel_src": src, "product_form": M.layout()[0],
         }
         print(json.dumps(line), flush=True)
     if world > 1:

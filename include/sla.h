@@ -68,7 +68,10 @@ typedef enum {
 } sla_pc;
 
 /* sla_csr_create flags */
-#define SLA_VALIDATE 1u   /* check the CSR structure on the device; SLA_ERR_INVALID on failure */
+#define SLA_VALIDATE 1u     /* check the CSR structure on the device; SLA_ERR_INVALID on failure */
+#define SLA_WARP_PIPELINE 2u /* use the warp-pipeline product where it applies (see sla_csr_layout) */
+#define SLA_PERSISTENT 4u    /* CG / Jacobi-PCG: one persistent iteration kernel per poll interval
+                                instead of a CUDA graph of one kernel per step (see sla_pcg_solve) */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -94,8 +97,9 @@ void sla_pcg_opts_default(sla_pcg_opts* o);
 
 /*
  * Create a handle for an n x n CSR matrix (or a batch of `batch` matrices on
- * one pattern).  Analyses the pattern (row blocks for the SpMV kernels, the
- * diagonal, the SPAI factor G and its explicit transpose) on the device.
+ * one pattern).  Analyses the pattern on the device: the product layout
+ * (sla_csr_layout), the diagonal, and on first SPAI use the factor G and its
+ * explicit transpose.
  * n >= 1, 0 <= nnz < 2^31, batch >= 1.  The handle keeps the three pointers
  * (it copies nothing but derived data).  With SLA_VALIDATE the structure is
  * checked first (monotone row_ptr, row_ptr[0] = 0, row_ptr[n] = nnz, columns
@@ -106,6 +110,18 @@ void sla_pcg_opts_default(sla_pcg_opts* o);
 sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
                           const int* d_row_ptr, const int* d_col_idx, const void* d_vals,
                           unsigned flags, void* stream, sla_handle* out);
+
+/*
+ * Product layout chosen for the handle's matrix A (diagnostics):
+ *  *form: 0 register-staged warp groups, 1 warp groups with asynchronous
+ *         value/column staging, 2 the same with asynchronous gathers,
+ *         3 the chunk pipeline (bulk copies of NT-row chunks; needs 16-byte
+ *         aligned row_ptr, col_idx and values of every system, and groups
+ *         that fit shared memory; only with SLA_WARP_PIPELINE);
+ *  *ctas: CTAs per system of the product kernels.
+ * Either pointer may be NULL.  SLA_ERR_INVALID for a null handle.
+ */
+sla_status sla_csr_layout(sla_handle h, int* form, int* ctas);
 
 /* Replace the values (same pattern, same dtype, [batch][nnz]); recomputes the
  * value-dependent set-up (diagonal, G, G^T).  Synchronises `stream`. */

@@ -73,10 +73,13 @@ class CSRMatrix:
 
     row_ptr: int32 [n+1], col_idx: int32 [nnz] (ascending per row), values:
     float64 or float32 [nnz] or [batch, nnz]; all CUDA tensors, kept alive by
-    this object.  validate=True checks the structure on the device."""
+    this object.  validate=True checks the structure on the device;
+    pipeline=True uses the warp-pipeline product where it applies;
+    fused=True runs CG / Jacobi-PCG as the persistent iteration kernel
+    instead of a CUDA graph of one kernel per step."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
-                 validate: bool = True, stream=None):
+                 validate: bool = True, pipeline: bool = False, fused: bool = False, stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -97,7 +100,9 @@ class CSRMatrix:
         self._h = C.c_void_p()
         dt = _lib.SLA_F64 if values.dtype == torch.float64 else _lib.SLA_F32
         _check(lib.sla_csr_create(self.n, self.nnz, self.batch, dt, _ptr(row_ptr), _ptr(col_idx),
-                                  _ptr(values), _lib.SLA_VALIDATE if validate else 0, _stream(stream),
+                                  _ptr(values), (_lib.SLA_VALIDATE if validate else 0) |
+                                  (_lib.SLA_WARP_PIPELINE if pipeline else 0) |
+                                  (_lib.SLA_PERSISTENT if fused else 0), _stream(stream),
                                   C.byref(self._h)))
 
     # -------------------------------------------------------------- lifetime
@@ -139,6 +144,12 @@ class CSRMatrix:
         return [SolveInfo(a.iters, a.rel_res_recursive, a.rel_res_true, STATUS_NAMES[a.status]) for a in arr]
 
     # -------------------------------------------------------------- API
+    def layout(self) -> tuple[int, int]:
+        """(product form 0..3, CTAs per system) the library chose for A."""
+        f, g = C.c_int(), C.c_int()
+        _check(_lib_handle().sla_csr_layout(self._h, C.byref(f), C.byref(g)))
+        return f.value, g.value
+
     def update_values(self, values: torch.Tensor, stream=None):
         if values.dtype != self.dtype or values.numel() != self.batch * self.nnz or not values.is_cuda:
             raise ValueError("values must match the handle's dtype and size")

@@ -17,11 +17,13 @@ STATUS_NAMES = {SLA_OK: "ok", SLA_ERR_INVALID: "invalid", SLA_ERR_CUDA: "cuda", 
 SLA_F64, SLA_F32 = 0, 1
 PC = {"none": 0, "jacobi": 1, "spai": 2}
 SLA_VALIDATE = 1
+SLA_WARP_PIPELINE = 2
+SLA_PERSISTENT = 4
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
-           "sla_spmv_dot_static"]
+           "sla_spmv_dot_static", "sla_csr_layout"]
 
 
 class PcgOpts(C.Structure):
@@ -52,6 +54,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_csr_create.argtypes = [C.c_int, C.c_longlong, C.c_int, C.c_int, _vp, _vp, _vp, C.c_uint, _vp,
                                    C.POINTER(_vp)]
     lib.sla_csr_update_values.argtypes = [_vp, _vp, _vp]
+    lib.sla_csr_layout.argtypes = [_vp, C.POINTER(C.c_int), C.POINTER(C.c_int)]
     lib.sla_spmv.argtypes = [_vp, _vp, _vp, _vp]
     lib.sla_spmv_dot.argtypes = [_vp, _vp, _vp, _vp, _vp]
     lib.sla_pcg_solve.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), C.POINTER(SolveInfo), _vp]
@@ -65,7 +68,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_spmv_dot_static.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
-    for f in ["sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
+    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
               "sla_adjoint", "sla_csr_destroy"]:
         getattr(lib, f).restype = C.c_int
     _lib = lib

@@ -20,6 +20,16 @@ constexpr int MAXR = NT;         // rows per row block (one row per thread)
 
 // Outcome codes mirrored from sla_status (kept numerically equal).
 enum : int { ST_OK = 0, ST_NOT_CONVERGED = 4, ST_BREAKDOWN = 5 };
+// Device error bit in Ctrl::err.
+enum : int { ERR_WAIT = 1 << 8, ERR_GRID = 1 << 9 };
+// Record where the first wait gave up (diagnostics for the host's message).
+__device__ __forceinline__ void note_wait(int* diag, int who, int a, int b, int c) {
+    if (atomicCAS(diag, 0, who) == 0) {
+        diag[1] = a;
+        diag[2] = b;
+        diag[3] = c;
+    }
+}
 
 // Solver state of one system, in device memory.  Written only by the last
 // CTA of a kernel (thread 0), read by every CTA of the following kernels.
@@ -39,7 +49,7 @@ struct State {
     int check;        // 1: the recursive residual met tol; next SpMV pass checks the true residual
     int rho_bad;      // r.z <= 0 seen while a check was pending
     int phase;        // 0 = set-up (p = z), 1 = iterating
-    int pad;
+    int xpend;        // x += alpha p of the current iteration not yet applied
 };
 
 // Batch-wide control block (per-system CTA arrival counters live in a
@@ -47,8 +57,9 @@ struct State {
 struct Ctrl {
     int all_done;     // every system frozen
     int ndone;        // systems frozen so far
-    int err;          // set-up / validation error bits
+    int err;          // error bits (ERR_WAIT: a bulk-copy wait gave up; ERR_GRID: a grid barrier did)
     int pad;
+    int diag[4];      // where the first wait gave up: CTA + 1 (negative for a copy wait), then details
 };
 
 // ----------------------------------------------------------------- loads
@@ -58,6 +69,24 @@ template <typename T>
 __device__ __forceinline__ T ld_nc(const T* p) { return __ldg(p); }        // read-only path
 template <typename T>
 __device__ __forceinline__ T ld_cg(const T* p) { return __ldcg(p); }       // L2 only (coherent)
+// Plain (weak, L1-cached) loads the compiler cannot turn into read-only-path
+// loads: for vectors a persistent kernel rewrites between grid barriers
+// (the read-only path may only serve data no thread writes during the kernel).
+__device__ __forceinline__ double ld_coh(const double* p) {
+    double v;
+    asm volatile("ld.global.f64 %0, [%1];\n" : "=d"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_coh(const float* p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float2 ld_coh(const float2* p) {
+    float2 v;
+    asm volatile("ld.global.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
 
 // Asynchronous global -> shared copies (cp.async, 4 or 8 bytes per thread),
 // cached at L1 with an L2 evict-first policy: the streamed matrix arrays are
@@ -84,6 +113,72 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
+// ----------------------------------------------------------------- bulk copies
+// One-shot mbarriers (one arrival per phase, completion counted in bytes)
+// and bulk asynchronous global -> shared copies (cp.async.bulk): the copy
+// engine moves a contiguous range of 16-byte units and signals the
+// barrier when its bytes have landed.
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Ends a barrier's life: required before its memory is used for anything
+// else (including another mbar_init), once no arrival or copy is pending.
+__device__ __forceinline__ void mbar_inval(unsigned long long* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// Makes initialised barriers visible to the asynchronous (copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Orders this thread's earlier shared-memory accesses before later
+// asynchronous-proxy accesses (a stage is refilled after it was read).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect(unsigned long long* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Wait for phase `parity` of `bar` to complete; gives up (returns false)
+// after about WAIT_LIMIT_NS, so a copy that never lands cannot hang the GPU.
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (unsigned k = 1; k < (1u << 30); ++k) {
+        if (mbar_test(bar, parity)) return true;
+        if ((k & 255u) == 0 && global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+    return false;
+}
+// `bytes` (a multiple of 16) from global `src` to shared `dst`, both 16-byte
+// aligned; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, unsigned bytes, unsigned long long* bar,
+                                          unsigned long long pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 // Value stored at the system's precision, returned as the fp64 value it holds.
 template <typename T>
 __device__ __forceinline__ double rnd(double v) { return (double)(T)v; }
@@ -96,24 +191,25 @@ __device__ __forceinline__ double warp_sum(double v) {
 }
 
 // Sum NV values over the CTA in a fixed order; the result is valid in thread 0.
+// Every thread parks its values in shared memory and warp 0 alone adds
+// them up (NT / 32 per lane, then a shuffle tree): on B300 every fp64 add
+// of every lane costs issue slots of the narrow fp64 pipe, so a shuffle
+// tree in all warps (5 adds per value per thread) was measurably slower.
+constexpr int RED_DOUBLES = 2 * NT;   // shared memory of block_sum<2>
 template <int NV>
-__device__ __forceinline__ void block_sum(double (&v)[NV], double* sm /* [NV][NWARP] */) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __forceinline__ void block_sum(double (&v)[NV], double* sm /* [NV][NT] */) {
+    static_assert(NV * NT <= RED_DOUBLES, "reduction buffer too small");
+    __syncthreads();   // the buffer may still be read by an earlier reduction
 #pragma unroll
-    for (int j = 0; j < NV; ++j) v[j] = warp_sum(v[j]);
+    for (int j = 0; j < NV; ++j) sm[j * NT + threadIdx.x] = v[j];
     __syncthreads();
-    if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) sm[j * NWARP + w] = v[j];
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             double s = 0.0;
 #pragma unroll
-            for (int k = 0; k < NWARP; ++k) s += sm[j * NWARP + k];
-            v[j] = s;
+            for (int k = 0; k < NT / 32; ++k) s += sm[j * NT + k * 32 + threadIdx.x];
+            v[j] = warp_sum(s);
         }
     }
     __syncthreads();

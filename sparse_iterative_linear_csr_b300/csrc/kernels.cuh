@@ -59,6 +59,10 @@ struct Mat {
     int wstride;      // doubles of shared memory per warp (both staging forms)
     int lanes;        // lanes per row: 1, 2 or 4 (a group holds 32 / lanes rows)
     int lshift;       // log2(lanes)
+    long long nnz;    // stored entries of the pattern
+    int ccap;         // warp pipeline: entries per stage (multiple of 4)
+    int stages;       // warp pipeline: ring stages
+    int* err;         // device error bits (Ctrl::err; Ctrl::diag follows at err + 2)
 };
 
 #define SYS_PROLOGUE                                            \
@@ -123,15 +127,24 @@ __device__ __forceinline__ double x_out_of(double x) { return x; }
 __device__ __forceinline__ float x_out_of(float2 x) { return __fadd_rn(x.x, x.y); }
 
 // ----------------------------------------------------------------- gathers
-template <typename T>
+// COH: the vector is rewritten during the kernel (the fused iteration), so
+// gathers use plain loads instead of the read-only path.
+template <typename T, bool COH = false>
+__device__ __forceinline__ T ld_gather(const T* p) {
+    if constexpr (COH) return ld_coh(p);
+    else return ld_nc(p);
+}
+template <typename T, bool COH = false>
 struct GatherVec {  // vector entry at the system precision
     const T* v;
-    __device__ __forceinline__ T operator()(int c) const { return ld_nc(v + c); }
+    __device__ __forceinline__ T operator()(int c) const { return ld_gather<T, COH>(v + c); }
 };
-template <typename T>
+template <typename T, bool COH = false>
 struct GatherX {    // stored iterate, rounded to the returned precision
     const typename Prec<T>::xw* v;
-    __device__ __forceinline__ T operator()(int c) const { return x_out_of(ld_nc(v + c)); }
+    __device__ __forceinline__ T operator()(int c) const {
+        return x_out_of(ld_gather<typename Prec<T>::xw, COH>(v + c));
+    }
 };
 
 __device__ __forceinline__ double acc_xor(double t, int o) { return __shfl_xor_sync(0xffffffffu, t, o); }
@@ -277,7 +290,7 @@ __host__ __device__ constexpr size_t async_smem_per_warp(int cap, int bufs) {
     return (size_t)bufs * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
-template <typename T, typename VT, typename XT, bool GASYNC, class Pre, class Epi>
+template <typename T, typename VT, typename XT, bool GASYNC, bool COH, class Pre, class Epi>
 __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v,
                                                 Pre pre, Epi epi, double* wsm) {
     using acc_t = typename Prec<T>::acc;
@@ -351,7 +364,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
 #pragma unroll
                     for (int j = 0; j < GATHER_U; ++j) {
                         const int e = b0 + j * 32 + lane;
-                        if (e < cnt) xv[j] = ld_nc(v + cc[e]);
+                        if (e < cnt) xv[j] = ld_gather<XT, COH>(v + cc[e]);
                     }
 #pragma unroll
                     for (int j = 0; j < GATHER_U; ++j) {
@@ -365,7 +378,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
             for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, cv[e], sx[e]);
         } else {
             if (bufs == 2 && !early) issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
-            s = unstaged_row<T>(A, av, GatherVec<XT>{v}, rlo, rhi);
+            s = unstaged_row<T>(A, av, GatherVec<XT, COH>{v}, rlo, rhi);
         }
         segment_sum(s, A.lanes);
         __syncwarp();  // buffers free for reuse
@@ -378,28 +391,211 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
     cp_wait<0>();
 }
 
-// Product with a plain vector gather in one of three compiled forms (the
+// Warp pipeline.  As in spmv_rows, a warp takes groups of 32 consecutive
+// rows (one row per lane; grid stride over groups), but it moves each
+// group's values and column indices into its own ring of A.stages
+// shared-memory stages with two bulk asynchronous copies (cp.async.bulk,
+// L2 evict-first), whose completion is counted in bytes on the stage's
+// mbarrier, issued by lane 0 stages - 1 groups ahead of the group being
+// summed.  Once a group's columns have landed the lanes gather the vector
+// entries they address into one of two gather buffers with cp.async (L2
+// evict-last), one group ahead of the arithmetic.  So while a warp sums
+// group t, the gathers of group t+1 and the copies of groups t+2 ..
+// t+stages-1 are in flight, and no warp ever waits for another.  Each lane
+// then sums its row from shared memory (one fp64 FMA per entry for fp64
+// systems).  Copies run from the group's first entry rounded down to a
+// multiple of 4 to its end rounded up (bulk copies move 16-byte units
+// between 16-byte aligned addresses); entries past the pattern's last
+// multiple of 4 are copied with plain loads.  The host uses this form only
+// when every group fits a stage (A.ccap entries) and the arrays are 16-byte
+// aligned.
+// Shared memory per warp (A.wstride doubles): PipeHdr, stages * ccap values,
+// stages * ccap columns, 2 * ccap gathered entries.
+constexpr int MAX_STAGES = 4;
+struct PipeHdr {
+    unsigned long long bar[MAX_STAGES];   // one mbarrier per stage
+    int k0[MAX_STAGES];                   // first staged entry (multiple of 4)
+    int cnt[MAX_STAGES];                  // staged entries
+};
+
+template <typename VT, typename XT>
+__host__ __device__ constexpr size_t pipe_smem_per_warp(int ccap, int stages) {
+    return sizeof(PipeHdr) + (size_t)stages * ccap * (sizeof(VT) + sizeof(int)) + 2 * (size_t)ccap * sizeof(XT);
+}
+
+template <typename T, typename VT, typename XT, class Pre, class Epi>
+__device__ __forceinline__ void spmv_pipe(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v,
+                                          Pre pre, Epi epi, double* dsm) {
+    using acc_t = typename Prec<T>::acc;
+    using car_t = decltype(pre(0));
+    const int S = A.stages, cap = A.ccap;
+    const int lane = threadIdx.x & 31;
+    char* base = reinterpret_cast<char*>(dsm + (threadIdx.x >> 5) * A.wstride);
+    PipeHdr* hd = reinterpret_cast<PipeHdr*>(base);
+    VT* sv = reinterpret_cast<VT*>(base + sizeof(PipeHdr));
+    int* sc = reinterpret_cast<int*>(sv + (size_t)S * cap);
+    XT* sx = reinterpret_cast<XT*>(sc + (size_t)S * cap);
+    const int ngroups = (A.n + 31) >> 5;
+    const int g0 = (blockIdx.x * NT + threadIdx.x) >> 5;
+    const int gstep = (gridDim.x * NT) >> 5;
+    const int m = g0 < ngroups ? (ngroups - 1 - g0) / gstep + 1 : 0;   // groups of this warp
+    __syncwarp();   // the warp's slice may still be in use by an earlier pass
+    if (m == 0) return;
+    const long long nnz4 = A.nnz & ~3LL;
+
+    // Lane 0: copies of the warp's j-th group into stage j % S, given the
+    // group's entry range [e0, e1).
+    auto issue = [&](int j, int e0, int e1) {
+        const int st = j % S;
+        const long long k0 = (long long)e0 & ~3LL;
+        const long long k1 = ((long long)e1 + 3) & ~3LL;
+        const long long kb = k1 < nnz4 ? k1 : (nnz4 > k0 ? nnz4 : k0);   // end of the bulk part
+        const long long ke = k1 < A.nnz ? k1 : A.nnz;                      // end of the staged range
+        hd->k0[st] = (int)k0;
+        hd->cnt[st] = (int)(ke - k0);
+        VT* dv = sv + (size_t)st * cap;
+        int* dc = sc + (size_t)st * cap;
+        for (long long k = kb; k < ke; ++k) {   // ragged end of the pattern
+            dv[k - k0] = av[k];
+            dc[k - k0] = A.ci[k];
+        }
+        const unsigned nb = (unsigned)(kb - k0);
+        fence_proxy_async();
+        mbar_arrive_expect(&hd->bar[st], nb * (unsigned)(sizeof(VT) + sizeof(int)));
+        if (nb) {
+            const unsigned long long pol = l2_evict_first();
+            bulk_copy(dv, av + k0, nb * (unsigned)sizeof(VT), &hd->bar[st], pol);
+            bulk_copy(dc, A.ci + k0, nb * (unsigned)sizeof(int), &hd->bar[st], pol);
+        }
+    };
+    // Entry range of the warp's j-th group (lane 0).
+    auto bounds = [&](int j, int& e0, int& e1) {
+        const int r0 = (g0 + j * gstep) << 5;
+        const int r1 = r0 + 32 < A.n ? r0 + 32 : A.n;
+        e0 = ld_nc(A.rp + r0);
+        e1 = ld_nc(A.rp + r1);
+    };
+
+    int ne0 = 0, ne1 = 0;   // lane 0: range of the next group to issue
+    if (lane == 0) {
+        for (int st = 0; st < S; ++st) mbar_init(&hd->bar[st], 1);
+        fence_barrier_init();
+        const int pre_n = S < m ? S : m;
+        for (int j = 0; j < pre_n; ++j) {
+            int e0, e1;
+            bounds(j, e0, e1);
+            issue(j, e0, e1);
+        }
+        if (S < m) bounds(S, ne0, ne1);
+    }
+    __syncwarp();
+    const unsigned long long keep = l2_evict_last();
+    auto gather = [&](int st, int gb) {
+        const int* cc = sc + (size_t)st * cap;
+        XT* dx = sx + (size_t)gb * cap;
+        const int cnt = hd->cnt[st];
+        for (int e = lane; e < cnt; e += 32) cp_async<sizeof(XT)>(dx + e, v + cc[e], keep);
+    };
+    // this lane's row of group 0
+    int row = (g0 << 5) + lane, rlo = 0, rhi = 0;
+    car_t car{};
+    if (row < A.n) {
+        rlo = ld_nc(A.rp + row);
+        rhi = ld_nc(A.rp + row + 1);
+        car = pre(row);
+    }
+    bool ok = mbar_wait(&hd->bar[0], 0);
+    if (ok) gather(0, 0);
+    cp_commit();
+    for (int i = 0; i < m; ++i) {
+        const int st = i % S, gb = i & 1;
+        int nrow = row + (gstep << 5), nlo = 0, nhi = 0;
+        car_t ncar{};
+        if (i + 1 < m) {
+            if (nrow < A.n) {
+                nlo = ld_nc(A.rp + nrow);
+                nhi = ld_nc(A.rp + nrow + 1);
+                ncar = pre(nrow);
+            }
+            const int ns = (i + 1) % S;
+            const bool w = mbar_wait(&hd->bar[ns], (unsigned)(((i + 1) / S) & 1));
+            ok = ok && w;
+            if (ok) gather(ns, gb ^ 1);
+            cp_commit();
+            cp_wait<1>();   // this group's gathers (the next group's may fly)
+        } else {
+            cp_wait<0>();
+        }
+        if (__any_sync(0xffffffffu, !ok)) {
+            // A copy never landed: record it, let copies still in flight
+            // settle (bounded), and leave the stages alone.
+            if (lane == 0) {
+                atomicOr(A.err, ERR_WAIT);
+                note_wait(A.err + 2, -1 - (int)blockIdx.x, i, m, (int)(threadIdx.x >> 5));
+                bool settled = true;
+                for (int j = i; j < i + S && j < m; ++j)
+                    settled = mbar_wait(&hd->bar[j % S], (unsigned)((j / S) & 1)) && settled;
+                if (settled)
+                    for (int st = 0; st < S; ++st) mbar_inval(&hd->bar[st]);
+            }
+            cp_wait<0>();
+            __syncwarp();
+            return;
+        }
+        __syncwarp();   // every lane's gathers of this group have landed
+        acc_t s = Prec<T>::zero();
+        if (row < A.n) {
+            const int k0 = hd->k0[st];
+            const VT* cv = sv + (size_t)st * cap;
+            const XT* cx = sx + (size_t)gb * cap;
+            for (int e = rlo - k0; e < rhi - k0; ++e) mac(s, cv[e], cx[e]);
+        }
+        __syncwarp();   // stage st and gather buffer gb are free
+        if (lane == 0 && i + S < m) {
+            issue(i + S, ne0, ne1);
+            if (i + S + 1 < m) bounds(i + S + 1, ne0, ne1);
+        }
+        if (row < A.n) epi(row, s, car);
+        row = nrow; rlo = nlo; rhi = nhi; car = ncar;
+    }
+    // every copy has landed: retire the barriers so the slice may be reused
+    // (by the register-staged passes, or by the next pass's mbar_init)
+    __syncwarp();
+    if (lane == 0)
+        for (int st = 0; st < S; ++st) mbar_inval(&hd->bar[st]);
+    __syncwarp();
+}
+
+// Product with a plain vector gather in one of four compiled forms (the
 // host picks one per matrix, so each kernel instantiation carries a single
 // path): FORM 0 register staging (spmv_rows); FORM 1 cp.async value/column
-// staging with register gathers; FORM 2 cp.async staging and gathers.
-template <typename T, int FORM, typename VT, typename XT, class Pre, class Epi>
-__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v, Pre pre,
+// staging with register gathers; FORM 2 cp.async staging and gathers; FORM 3
+// the warp pipeline (spmv_pipe).
+template <typename T, int FORM, typename VT, typename XT, bool COH = false, class Pre, class Epi>
+__device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
-    if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT>{v}, pre, epi, wsm);
-    else spmv_rows_async<T, VT, XT, FORM == 2>(A, av, v, pre, epi, wsm);
+    if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
+    else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
+    else spmv_rows_async<T, VT, XT, FORM == 2, COH>(A, av, v, pre, epi, wsm);
 }
 
 // ----------------------------------------------------------------- scalar logic
-// All of these run in thread 0 of the last CTA of one system.
+// These run in thread 0 of the last CTA of one system on the system's State
+// in device memory, or (c == nullptr) in thread 0 of every CTA of the fused
+// kernel on the CTA's shared copy, which CTA 0 publishes afterwards.
+__device__ __forceinline__ void count_frozen(Ctrl* c) {
+    __threadfence();
+    if (atomicAdd(&c->ndone, 1) + 1 == (int)gridDim.y) c->all_done = 1;
+}
 __device__ __forceinline__ void freeze(State* s, Ctrl* c, int status) {
     s->status = status;
     s->done = 1;
-    __threadfence();
-    if (atomicAdd(&c->ndone, 1) + 1 == (int)gridDim.y) c->all_done = 1;
+    if (c) count_frozen(c);
 }
 
 // After the p.q reduction (and the optional true-residual check).
 __device__ __forceinline__ void after_spmv(State* s, Ctrl* c, double delta, bool checked, double tr2) {
+    s->xpend = 0;   // the previous iteration's x update has been applied
     if (checked) {
         s->tr2 = tr2;
         if (tr2 <= s->tol2bb) { freeze(s, c, ST_OK); return; }
@@ -411,6 +607,7 @@ __device__ __forceinline__ void after_spmv(State* s, Ctrl* c, double delta, bool
     if (!(delta > 0.0) || !finite(delta)) { freeze(s, c, ST_BREAKDOWN); return; }
     s->alpha = s->rho / delta;
     s->iter += 1;
+    s->xpend = 1;
 }
 
 // beta from the new r.z (or, in the set-up phase, the first rho).
@@ -447,6 +644,7 @@ __device__ __forceinline__ void start_state(State* s, Ctrl* c, double bb, double
     s->check = 0;
     s->rho_bad = 0;
     s->phase = 0;
+    s->xpend = 0;
     s->alpha = s->beta = s->rho = s->delta = s->tr2 = 0.0;
     if (bb == 0.0) { freeze(s, c, ST_OK); return; }   // x = 0 is exact
     if (!finite(gamma)) { freeze(s, c, ST_BREAKDOWN); return; }
@@ -466,17 +664,6 @@ __device__ __forceinline__ DF resid(float b, DF s) { return df_add_f(df_neg(s), 
 __device__ __forceinline__ void sq_acc(double& t, double e) { t = fma(e, e, t); }
 __device__ __forceinline__ void sq_acc(DF& t, DF e) { t = df_add(t, df_sqr(e)); }
 
-// One element of the x / r update: x += alpha p; r -= alpha q; g += r^2;
-// (Jacobi) rz += r (r dinv).  A = accumulator type, W = working value type.
-template <int PC, typename A, typename W, typename XW>
-__device__ __forceinline__ void update_one(A alpha, XW& x, W& r, W p, W q, XW dinv, A& g, A& rz) {
-    x = to_w(afma(alpha, ld_w(p), ld_w(x)));
-    const A rn = afma(aneg(alpha), ld_w(q), ld_w(r));
-    r = to_w(rn);
-    g = afma(rn, rn, g);
-    if (PC == 1) rz = afma(rn, amul(rn, ld_w(dinv)), rz);
-}
-
 // -lambda_i x_j, rounded once
 __device__ __forceinline__ double neg_prod(double l, double x) { return -l * x; }
 __device__ __forceinline__ float neg_prod(float l, float x) { return df_round(two_prod(-l, x)); }
@@ -488,8 +675,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
                                                             const T* __restrict__ x, T* __restrict__ y, double* dot) {
     using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
-    extern __shared__ double dsm[];
-    __shared__ double red[2 * NWARP];
+    extern __shared__ __align__(16) double dsm[];
+    __shared__ double red[RED_DOUBLES];
     av += ao; x += vo; y += vo;
     acc_t acc = Prec<T>::zero();
     spmv_vec<T, FORM, T, T>(A, av, x, [&](int i) { return x[i]; },
@@ -509,13 +696,13 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
 // ||b - A round(x)||^2 over this CTA's rows (the true-residual check).  Kept
 // out of line: it runs only when the recursive residual has met the
 // tolerance, and inlining it would cost the main product registers.
-template <typename T, int FORM>
+template <typename T, int FORM, bool COH = false>
 __device__ __noinline__ typename Prec<T>::acc residual_pass(const Mat& A, const T* __restrict__ av,
-                                                            const typename Prec<T>::xw* __restrict__ x,
+                                                            const typename Prec<T>::xw* x,
                                                             const T* __restrict__ b, double* dsm) {
     using acc_t = typename Prec<T>::acc;
     acc_t tr2 = Prec<T>::zero();
-    spmv_rows<T, T>(A, av, GatherX<T>{x}, [&](int i) { return b[i]; },
+    spmv_rows<T, T>(A, av, GatherX<T, COH>{x}, [&](int i) { return b[i]; },
                     [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
     return tr2;
 }
@@ -529,9 +716,13 @@ __global__ void __launch_bounds__(NT, IterMinCtas<T>::value)
     using acc_t = typename Prec<T>::acc;
     using W = typename Prec<T>::w;
     SYS_PROLOGUE
-    if (ld_cg(&st->done)) return;
-    extern __shared__ double dsm[];
-    __shared__ double red[2 * NWARP];
+    if (ld_cg(&st->done)) {
+        // a system frozen in k_update had its last x update applied by k_pupdate
+        if (blockIdx.x == 0 && threadIdx.x == 0 && ld_cg(&st->xpend)) st->xpend = 0;
+        return;
+    }
+    extern __shared__ __align__(16) double dsm[];
+    __shared__ double red[RED_DOUBLES];
     av += ao; p += vo; q += vo; x += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
@@ -561,69 +752,82 @@ __device__ __forceinline__ void split2(float4 v, float2& a, float2& b) {
 __device__ __forceinline__ double2 join2(double a, double b) { return make_double2(a, b); }
 __device__ __forceinline__ float4 join2(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
 
-// x += alpha p; r -= alpha q; gamma = r.r; rho' = r.z (PC 0: z = r, PC 1:
-// z = r / A_ii; PC 2: z comes later from the SPAI kernels).
+// One element of the residual update: r -= alpha q; gamma += r^2; and for
+// Jacobi z = r / A_ii (stored for the direction update) with rho' += r z.
+template <int PC, typename A, typename W, typename XW>
+__device__ __forceinline__ void update_r(A alpha, W& ri, W qi, XW di, W& zi, A& g, A& rz) {
+    const A rn = afma(aneg(alpha), ld_w(qi), ld_w(ri));
+    ri = to_w(rn);
+    g = afma(rn, rn, g);
+    if (PC == 1) {
+        const A zz = amul(rn, ld_w(di));
+        zi = to_w(zz);
+        rz = afma(rn, zz, rz);
+    }
+}
+
+// Pairs per thread per trip of the streaming kernels (measured on B300:
+// one pair with two resident CTAs per SM beats deeper unrolling).
+constexpr int VU = 1;
+
+// r -= alpha q; gamma = r.r; rho' = r.z (PC 0: z = r; PC 1: z = r / A_ii,
+// stored; PC 2: z comes later from the SPAI kernels).  x is advanced by
+// k_pupdate, which reads p anyway, so this kernel touches r, q (and dinv, z).
 template <typename T, int PC, bool PAIRS>
-__global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __restrict__ x,
-                                               typename Prec<T>::w* __restrict__ r,
-                                               const typename Prec<T>::w* __restrict__ p,
+__global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::w* __restrict__ r,
                                                const typename Prec<T>::w* __restrict__ q,
-                                               const typename Prec<T>::xw* __restrict__ dinv) {
+                                               const typename Prec<T>::xw* __restrict__ dinv,
+                                               typename Prec<T>::w* __restrict__ z) {
     using acc_t = typename Prec<T>::acc;
     using W = typename Prec<T>::w;
     using XW = typename Prec<T>::xw;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
-    __shared__ double red[2 * NWARP];
-    x += vo; r += vo; p += vo; q += vo;
-    if (PC == 1) dinv += vo;
+    __shared__ double red[RED_DOUBLES];
+    r += vo; q += vo;
+    if (PC == 1) { dinv += vo; z += vo; }
     const acc_t alpha = Prec<T>::scal(ld_cg(&st->alpha));
     acc_t g = Prec<T>::zero(), rz = Prec<T>::zero();
     if (PAIRS) {
-        // two pairs per thread per trip, all loads issued before any use
+        // VU pairs per thread per trip, all loads issued before any use
         using P2 = typename XPair<W>::type;
         using X2 = typename XPair<XW>::type;
         const int n2 = S.n >> 1;
         const int stride = gridDim.x * NT;
-        for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += 2 * stride) {
-            P2 p2[2], q2[2], r2[2];
-            X2 x2[2], d2[2];
+        for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += VU * stride) {
+            P2 q2[VU], r2[VU];
+            X2 d2[VU];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < VU; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    p2[u] = ld_stream(reinterpret_cast<const P2*>(p) + i);
                     q2[u] = ld_stream(reinterpret_cast<const P2*>(q) + i);
-                    x2[u] = reinterpret_cast<const X2*>(x)[i];
                     r2[u] = reinterpret_cast<const P2*>(r)[i];
-                    if (PC == 1) d2[u] = ld_stream(reinterpret_cast<const X2*>(dinv) + i);
+                    if (PC == 1) d2[u] = ld_nc(reinterpret_cast<const X2*>(dinv) + i);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < VU; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    XW xa, xb, da{}, db{};
-                    W pa, pb, qa, qb, ra, rb;
-                    split2(x2[u], xa, xb);
-                    split2(p2[u], pa, pb);
-                    split2(q2[u], qa, qb);
+                    W ra, rb, qa, qb, za{}, zb{};
+                    XW da{}, db{};
                     split2(r2[u], ra, rb);
+                    split2(q2[u], qa, qb);
                     if (PC == 1) split2(d2[u], da, db);
-                    update_one<PC>(alpha, xa, ra, pa, qa, da, g, rz);
-                    update_one<PC>(alpha, xb, rb, pb, qb, db, g, rz);
-                    reinterpret_cast<X2*>(x)[i] = join2(xa, xb);
+                    update_r<PC>(alpha, ra, qa, da, za, g, rz);
+                    update_r<PC>(alpha, rb, qb, db, zb, g, rz);
                     reinterpret_cast<P2*>(r)[i] = join2(ra, rb);
+                    if (PC == 1) reinterpret_cast<P2*>(z)[i] = join2(za, zb);
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-            XW xi = x[i];
-            W ri = r[i];
-            update_one<PC>(alpha, xi, ri, ld_stream(p + i), ld_stream(q + i), PC == 1 ? dinv[i] : XW{}, g, rz);
-            x[i] = xi;
+            W ri = r[i], zi{};
+            update_r<PC>(alpha, ri, ld_stream(q + i), PC == 1 ? dinv[i] : XW{}, zi, g, rz);
             r[i] = ri;
+            if (PC == 1) z[i] = zi;
         }
     }
     double v[2] = {Prec<T>::total(g), Prec<T>::total(rz)}, tot[2];
@@ -631,66 +835,70 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::xw* __re
         after_update(st, S.ctl, tot[0], PC != 2, PC == 0 ? tot[0] : tot[1]);
 }
 
-// p = z + beta p   (INIT: p = z)
-template <int PC, bool INIT, typename A, typename W, typename XW>
-__device__ __forceinline__ W pnew(A beta, W p, W r, XW dinv, W z) {
-    A zi;
-    if (PC == 0) zi = ld_w(r);
-    else if (PC == 1) zi = amul(ld_w(r), ld_w(dinv));
-    else zi = ld_w(z);
-    return INIT ? to_w(zi) : to_w(afma(beta, ld_w(p), zi));
-}
-
-template <typename T, int PC, bool INIT, bool PAIRS>
+// The iteration's pending x += alpha p (applied even when the system froze
+// in k_update), then, while iterating, p = z + beta p, with z = r for
+// PC 0.  INIT: p = z only (set-up of SPAI).
+template <typename T, bool INIT, bool PAIRS>
 __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __restrict__ p,
-                                                const typename Prec<T>::w* __restrict__ r,
-                                                const typename Prec<T>::w* __restrict__ z,
-                                                const typename Prec<T>::xw* __restrict__ dinv) {
+                                                typename Prec<T>::xw* __restrict__ x,
+                                                const typename Prec<T>::w* __restrict__ zs) {
     using acc_t = typename Prec<T>::acc;
     using W = typename Prec<T>::w;
     using XW = typename Prec<T>::xw;
     SYS_PROLOGUE
-    if (ld_cg(&st->done)) return;
-    p += vo; r += vo;
-    if (PC == 1) dinv += vo;
-    if (PC == 2) z += vo;
+    const bool done = ld_cg(&st->done) != 0;
+    const bool xp = !INIT && ld_cg(&st->xpend) != 0;
+    if (done && !xp) return;
+    p += vo; x += vo; zs += vo;
+    const acc_t alpha = Prec<T>::scal(xp ? ld_cg(&st->alpha) : 0.0);
     const acc_t beta = Prec<T>::scal(INIT ? 0.0 : ld_cg(&st->beta));
+    const bool more = !done;
     if (PAIRS) {
         using P2 = typename XPair<W>::type;
         using X2 = typename XPair<XW>::type;
         const int n2 = S.n >> 1;
         const int stride = gridDim.x * NT;
-        for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += 2 * stride) {
-            P2 r2[2], p2[2], z2[2];
-            X2 d2[2];
+        for (int i0 = blockIdx.x * NT + threadIdx.x; i0 < n2; i0 += VU * stride) {
+            P2 p2[VU], z2[VU];
+            X2 x2[VU];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < VU; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    r2[u] = ld_stream(reinterpret_cast<const P2*>(r) + i);
                     p2[u] = INIT ? P2{} : reinterpret_cast<const P2*>(p)[i];
-                    if (PC == 1) d2[u] = ld_stream(reinterpret_cast<const X2*>(dinv) + i);
-                    z2[u] = PC == 2 ? ld_stream(reinterpret_cast<const P2*>(z) + i) : P2{};
+                    if (xp) x2[u] = reinterpret_cast<const X2*>(x)[i];
+                    if (more) z2[u] = ld_stream(reinterpret_cast<const P2*>(zs) + i);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < VU; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    XW da{}, db{};
-                    W ra, rb, pa, pb, za, zb;
-                    split2(r2[u], ra, rb);
+                    W pa, pb;
                     split2(p2[u], pa, pb);
-                    split2(z2[u], za, zb);
-                    if (PC == 1) split2(d2[u], da, db);
-                    reinterpret_cast<P2*>(p)[i] =
-                        join2(pnew<PC, INIT>(beta, pa, ra, da, za), pnew<PC, INIT>(beta, pb, rb, db, zb));
+                    if (xp) {
+                        XW xa, xb;
+                        split2(x2[u], xa, xb);
+                        xa = to_w(afma(alpha, ld_w(pa), ld_w(xa)));
+                        xb = to_w(afma(alpha, ld_w(pb), ld_w(xb)));
+                        reinterpret_cast<X2*>(x)[i] = join2(xa, xb);
+                    }
+                    if (more) {
+                        W za, zb;
+                        split2(z2[u], za, zb);
+                        reinterpret_cast<P2*>(p)[i] =
+                            INIT ? join2(za, zb)
+                                 : join2(to_w(afma(beta, ld_w(pa), ld_w(za))), to_w(afma(beta, ld_w(pb), ld_w(zb))));
+                    }
                 }
             }
         }
     } else {
-        for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT)
-            p[i] = pnew<PC, INIT>(beta, INIT ? W{} : p[i], r[i], PC == 1 ? dinv[i] : XW{}, PC == 2 ? z[i] : W{});
+        for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
+            const W pi = INIT ? W{} : p[i];
+            if (xp) x[i] = to_w(afma(alpha, ld_w(pi), ld_w(x[i])));
+            if (more) p[i] = INIT ? zs[i] : to_w(afma(beta, ld_w(pi), ld_w(zs[i])));
+        }
     }
 }
 
@@ -705,7 +913,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, lon
     using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
-    extern __shared__ double dsm[];
+    extern __shared__ __align__(16) double dsm[];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
     spmv_vec<T, FORM, typename Prec<T>::gv, W>(GT, gtv, r, [](int) { return W{}; },
                                          [&](int i, acc_t s, W) { t[i] = to_w(s); }, dsm);
@@ -722,8 +930,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long
     using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
-    extern __shared__ double dsm[];
-    __shared__ double red[2 * NWARP];
+    extern __shared__ __align__(16) double dsm[];
+    __shared__ double red[RED_DOUBLES];
     gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
     const acc_t e = Prec<T>::scal(eps);
     acc_t rz = Prec<T>::zero();
@@ -738,6 +946,217 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) new_direction(st, S.ctl, tot[0]);
 }
 
+// ----------------------------------------------------------------- fused iteration
+// A persistent form of the iteration for CG and Jacobi-PCG: one cooperative
+// launch (every CTA resident) runs up to `iters` iterations, the CTAs of a
+// system meeting at grid barriers instead of kernel boundaries:
+//   A  q = A p, delta = p.q (and ||b - A round(x)||^2 when checking)
+//      -> all-reduce -> alpha
+//   B  r -= alpha q, z = M^-1 r (stored), gamma = r.r, rho' = r.z
+//      -> all-reduce -> beta, convergence test
+//   C  x += alpha p, p = z + beta p -> barrier
+// x is advanced in C, where p is read anyway, so B reads three vectors and
+// C three.  Every CTA sums the partial sums of all CTAs itself, in CTA
+// order, so all CTAs hold identical scalars (a shared-memory copy of the
+// State, advanced by the same scalar logic as the kernel-per-step path) and
+// take identical decisions; CTA 0 publishes the State when the launch ends.
+struct GridSync {
+    unsigned count;   // arrivals at the current barrier
+    unsigned gen;     // completed barriers
+};
+
+// Thread 0 of every CTA of a system: arrive and wait for the others.
+// Returns false (and records ERR_WAIT) after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool grid_arrive_wait(GridSync* g, int* err) {
+    volatile unsigned* vgen = &g->gen;
+    const unsigned gen = *vgen;   // read before arriving: the last arrival advances it
+    __threadfence();
+    const unsigned arrived = atomicAdd(&g->count, 1u);
+    if (arrived == gridDim.x - 1) {
+        atomicExch(&g->count, 0u);
+        __threadfence();
+        atomicAdd(&g->gen, 1u);
+        return true;
+    }
+    const unsigned long long t0 = global_ns();
+    for (unsigned k = 0; k < (1u << 31); ++k) {
+        if (*vgen != gen) {
+            __threadfence();
+            return true;
+        }
+        if (k > 32) __nanosleep(64);
+        if ((k & 63u) == 63u && global_ns() - t0 > WAIT_LIMIT_NS) break;
+    }
+    atomicOr(err, ERR_GRID);
+    note_wait(err + 2, 1 + (int)blockIdx.x, (int)gen, (int)arrived, (int)*((volatile unsigned*)&g->count));
+    return false;
+}
+
+__device__ __forceinline__ bool grid_barrier(GridSync* g, int* err) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) s_ok = grid_arrive_wait(g, err);
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// Sum NV values over the system's CTAs (in CTA order, in every CTA; valid
+// in thread 0).  part: [gridDim.x][NV] slots of this reduction.
+template <int NV>
+__device__ __forceinline__ bool grid_allreduce(double (&v)[NV], double* part, GridSync* g, int* err, double* sm) {
+    __shared__ int s_ok;
+    block_sum<NV>(v, sm);
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) part[blockIdx.x * NV + j] = v[j];
+        s_ok = grid_arrive_wait(g, err);
+    }
+    __syncthreads();
+    if (!s_ok) return false;
+    double acc[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) acc[j] = 0.0;
+    for (int bk = threadIdx.x; bk < (int)gridDim.x; bk += NT) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) acc[j] += ld_cg(part + bk * NV + j);
+    }
+    block_sum<NV>(acc, sm);
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) v[j] = acc[j];
+    }
+    return true;
+}
+
+#ifndef SLA_FUSED_MIN_CTAS
+#define SLA_FUSED_MIN_CTAS IterMinCtas<T>::value
+#endif
+template <typename T, int FORM, int PC, bool PAIRS>
+__global__ void __launch_bounds__(NT, SLA_FUSED_MIN_CTAS)
+    k_cg_fused(Mat A, Sys S, const T* __restrict__ av, typename Prec<T>::w* __restrict__ p,
+               typename Prec<T>::w* __restrict__ q, typename Prec<T>::w* __restrict__ r,
+               typename Prec<T>::w* __restrict__ z, typename Prec<T>::xw* __restrict__ x,
+               const typename Prec<T>::xw* __restrict__ dinv, const T* __restrict__ b, GridSync* gsync,
+               int iters) {
+    using acc_t = typename Prec<T>::acc;
+    using W = typename Prec<T>::w;
+    using XW = typename Prec<T>::xw;
+    SYS_PROLOGUE
+    __shared__ State ls;
+    __shared__ int s_was_done;
+    extern __shared__ __align__(16) double dsm[];
+    __shared__ double red[RED_DOUBLES];
+    av += ao; p += vo; q += vo; r += vo; z += vo; x += vo; b += vo;
+    if (PC == 1) dinv += vo;
+    GridSync* gs = gsync + sys;
+    double* partA = part;                   // [gridDim.x][2]: delta, ||b - A x||^2
+    double* partB = part + 2 * gridDim.x;   // [gridDim.x][2]: gamma, rho'
+    int* err = &S.ctl->err;
+    if (threadIdx.x == 0) {
+        ls = *st;
+        s_was_done = ls.done;
+    }
+    __syncthreads();
+    const int stride = gridDim.x * NT;
+    for (int it = 0; it < iters && !ls.done; ++it) {
+        // A
+        const bool check = ls.check != 0;
+        acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
+        if (check) tr2 = residual_pass<T, FORM, true>(A, av, x, b, dsm);
+        spmv_vec<T, FORM, T, W, true>(A, av, p, [&](int i) { return p[i]; },
+                                [&](int i, acc_t s, W pi) {
+                                    const W qi = to_w(s);
+                                    q[i] = qi;
+                                    dot_acc(delta, pi, qi);
+                                },
+                                dsm);
+        double va[2] = {Prec<T>::total(delta), Prec<T>::total(tr2)};
+        if (!grid_allreduce<2>(va, partA, gs, err, red)) break;
+        if (threadIdx.x == 0) after_spmv(&ls, nullptr, va[0], check, va[1]);
+        __syncthreads();
+        if (ls.done) break;
+        // B
+        {
+            const acc_t alpha = Prec<T>::scal(ls.alpha);
+            acc_t g = Prec<T>::zero(), rz = Prec<T>::zero();
+            auto one = [&](W& ri, W qi, XW di, W& zi) { update_r<PC>(alpha, ri, qi, di, zi, g, rz); };
+            if (PAIRS) {
+                using P2 = typename XPair<W>::type;
+                using X2 = typename XPair<XW>::type;
+                const int n2 = S.n >> 1;
+                for (int i = blockIdx.x * NT + threadIdx.x; i < n2; i += stride) {
+                    const P2 q2 = ld_stream(reinterpret_cast<const P2*>(q) + i);
+                    P2 r2 = reinterpret_cast<const P2*>(r)[i];
+                    X2 d2{};
+                    if (PC == 1) d2 = ld_nc(reinterpret_cast<const X2*>(dinv) + i);
+                    W ra, rb, qa, qb, za{}, zb{};
+                    XW da{}, db{};
+                    split2(r2, ra, rb);
+                    split2(q2, qa, qb);
+                    if (PC == 1) split2(d2, da, db);
+                    one(ra, qa, da, za);
+                    one(rb, qb, db, zb);
+                    reinterpret_cast<P2*>(r)[i] = join2(ra, rb);
+                    if (PC == 1) reinterpret_cast<P2*>(z)[i] = join2(za, zb);
+                }
+            } else {
+                for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += stride) {
+                    W ri = r[i], zi{};
+                    one(ri, ld_stream(q + i), PC == 1 ? dinv[i] : XW{}, zi);
+                    r[i] = ri;
+                    if (PC == 1) z[i] = zi;
+                }
+            }
+            double vb[2] = {Prec<T>::total(g), Prec<T>::total(rz)};
+            if (!grid_allreduce<2>(vb, partB, gs, err, red)) break;
+            if (threadIdx.x == 0) after_update(&ls, nullptr, vb[0], true, PC == 0 ? vb[0] : vb[1]);
+            __syncthreads();
+        }
+        // C (x always advances; p only while iterating)
+        {
+            const acc_t alpha = Prec<T>::scal(ls.alpha);
+            const acc_t beta = Prec<T>::scal(ls.beta);
+            const bool more = !ls.done;
+            const W* zs = PC == 1 ? z : r;
+            if (PAIRS) {
+                using P2 = typename XPair<W>::type;
+                using X2 = typename XPair<XW>::type;
+                const int n2 = S.n >> 1;
+                for (int i = blockIdx.x * NT + threadIdx.x; i < n2; i += stride) {
+                    const P2 p2 = reinterpret_cast<const P2*>(p)[i];
+                    const X2 x2 = reinterpret_cast<const X2*>(x)[i];
+                    const P2 z2 = reinterpret_cast<const P2*>(zs)[i];
+                    W pa, pb, za, zb;
+                    XW xa, xb;
+                    split2(p2, pa, pb);
+                    split2(x2, xa, xb);
+                    split2(z2, za, zb);
+                    xa = to_w(afma(alpha, ld_w(pa), ld_w(xa)));
+                    xb = to_w(afma(alpha, ld_w(pb), ld_w(xb)));
+                    reinterpret_cast<X2*>(x)[i] = join2(xa, xb);
+                    if (more)
+                        reinterpret_cast<P2*>(p)[i] =
+                            join2(to_w(afma(beta, ld_w(pa), ld_w(za))), to_w(afma(beta, ld_w(pb), ld_w(zb))));
+                }
+            } else {
+                for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += stride) {
+                    const W pi = p[i];
+                    x[i] = to_w(afma(alpha, ld_w(pi), ld_w(x[i])));
+                    if (more) p[i] = to_w(afma(beta, ld_w(pi), ld_w(zs[i])));
+                }
+            }
+        }
+        if (threadIdx.x == 0) ls.xpend = 0;   // applied in C
+        if (ls.done) break;
+        if (!grid_barrier(gs, err)) break;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *st = ls;
+        if (ls.done && !s_was_done) count_frozen(S.ctl);
+    }
+}
+
 // ----------------------------------------------------------------- set-up / final
 // x = 0, r = b, b copied into the workspace, bb = b.b.
 template <typename T>
@@ -745,7 +1164,7 @@ __global__ void __launch_bounds__(NT) k_init(Sys S, const T* __restrict__ b_user
                                              typename Prec<T>::xw* __restrict__ x, typename Prec<T>::w* __restrict__ r,
                                              double tol, int max_iter) {
     SYS_PROLOGUE
-    __shared__ double red[2 * NWARP];
+    __shared__ double red[RED_DOUBLES];
     b_user += vo; bw += vo; x += vo; r += vo;
     typename Prec<T>::acc bb = Prec<T>::zero();
     for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
@@ -772,8 +1191,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
     using acc_t = typename Prec<T>::acc;
     using W = typename Prec<T>::w;
     SYS_PROLOGUE
-    extern __shared__ double dsm[];
-    __shared__ double red[2 * NWARP];
+    extern __shared__ __align__(16) double dsm[];
+    __shared__ double red[RED_DOUBLES];
     av += ao; b_user += vo; x0 += vo; bw += vo; x += vo; r += vo;
     acc_t bb = Prec<T>::zero(), g = Prec<T>::zero();
     spmv_rows<T, T>(A, av, GatherVec<T>{x0}, [&](int i) { return b_user[i]; },
@@ -800,7 +1219,7 @@ __global__ void __launch_bounds__(NT) k_init_dir(Sys S, typename Prec<T>::w* __r
     using W = typename Prec<T>::w;
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
-    __shared__ double red[2 * NWARP];
+    __shared__ double red[RED_DOUBLES];
     p += vo; r += vo;
     if (PC == 1) dinv += vo;
     acc_t rz = Prec<T>::zero();
@@ -830,8 +1249,8 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
             const T* __restrict__ bw, T* __restrict__ x_out, Stat* out) {
     using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
-    extern __shared__ double dsm[];
-    __shared__ double red[2 * NWARP];
+    extern __shared__ __align__(16) double dsm[];
+    __shared__ double red[RED_DOUBLES];
     av += ao; x += vo; bw += vo; x_out += vo;
     const bool zero_b = ld_cg(&st->bb) == 0.0;
     acc_t tr2 = Prec<T>::zero();
@@ -864,7 +1283,7 @@ template <typename T>
 __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict__ lam, const T* __restrict__ x,
                                                T* __restrict__ dA) {
     SYS_PROLOGUE
-    extern __shared__ double dsm[];
+    extern __shared__ __align__(16) double dsm[];
     int* srow = reinterpret_cast<int*>(dsm + (threadIdx.x >> 5) * A.wstride);
     const int lane = threadIdx.x & 31;
     lam += vo; x += vo; dA += ao;

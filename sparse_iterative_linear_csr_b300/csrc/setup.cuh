@@ -95,6 +95,21 @@ __global__ void k_group_max(const int* __restrict__ rp, int n, int R, int* out) 
     if (m) atomicMax(out, m);
 }
 
+// Largest staged range of a chunk of R consecutive rows, the range's ends
+// rounded out to multiples of 4 entries (as the chunk pipeline copies it).
+__global__ void k_chunk_max(const int* __restrict__ rp, int n, int R, int* out) {
+    const long long nc = ((long long)n + R - 1) / R;
+    int m = 0;
+    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < nc; c += (long long)gridDim.x * blockDim.x) {
+        const long long r0 = c * R;
+        const long long r1 = r0 + R < n ? r0 + R : n;
+        const long long k0 = (long long)rp[r0] & ~3LL;
+        const long long k1 = ((long long)rp[r1] + 3) & ~3LL;
+        m = max(m, (int)(k1 - k0));
+    }
+    if (m) atomicMax(out, m);
+}
+
 // Number of stored entries whose column is more than `w` away from the row.
 __global__ void k_far_count(const int* __restrict__ rp, const int* __restrict__ ci, int n, int w,
                             unsigned long long* out) {

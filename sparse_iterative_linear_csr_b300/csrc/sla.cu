@@ -9,6 +9,7 @@
 // every iteration.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <cstdarg>
@@ -100,13 +101,19 @@ struct GraphCache {
     }
 };
 
-// Staged-SpMV layout of one matrix: staging capacity (entries per group of
-// 32 / lanes rows), lanes per row, and CTAs per system.
+// Product layout of one matrix: warp staging capacity (entries per group of
+// 32 / lanes rows), lanes per row, chunk-pipeline capacity and stages, the
+// compiled form the product kernels use, their dynamic shared memory, and
+// CTAs per system.
 struct Layout {
     int cap = 32;
     int lanes = 1;
     int gx = 1;
     int gasync = 0;   // gathers by cp.async (scattered columns)
+    int ccap = 0;     // chunk pipeline: entries per stage (0: a chunk would not fit)
+    int stages = 0;   // chunk pipeline: ring stages
+    int form = 0;     // compiled form of the product kernels (spmv_vec)
+    size_t smem = 0;  // their dynamic shared memory
 };
 
 struct sla_csr {
@@ -121,13 +128,19 @@ struct sla_csr {
     int device = 0;
     int sms = 0;
 
-    Layout LA;         // staged-SpMV layout of A
+    Layout LA;         // product layout of A
+    bool vals_aligned = false;  // values 16-byte aligned for every system (chunk pipeline)
+    bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
+    bool persistent = false;    // SLA_PERSISTENT: persistent iteration kernel for CG / Jacobi-PCG
+    bool coop = false;          // device supports cooperative launches
+    DevBuf gsync;               // GridSync per system (fused iteration kernel)
     int diag_err = 0;  // ERR_NO_DIAG | ERR_DIAG_SIGN
     DevBuf diag, dinv;
 
     // SPAI factor (built on first use, per values)
     bool spai_ready = false;
     long long nnzg = 0;
+    long long gstride = 0;  // per-system stride of the G values (nnzg rounded up to even: 16-byte aligned)
     Layout LG, LGT;    // ... of G and G^T
     DevBuf grp, gci, gv, gtrp, gtci, gtv;
 
@@ -162,7 +175,6 @@ static size_t spmv_smem(int cap) {
     const size_t piped = f ? async_smem_per_warp<double, double>(cap, f) : 0;
     return (size_t)NWARP * (piped > single ? piped : single);
 }
-static size_t grad_smem(int cap) { return spmv_smem(cap); }
 // Resident CTAs per SM of `kern` with `smem` bytes of dynamic shared memory
 // (the kernel must already allow that much: allow_smem).
 template <typename K>
@@ -204,6 +216,19 @@ static sla_status allow_smem_form(int b) {
     return SLA_OK;
 }
 
+static constexpr int SMEM_CTA_MAX = 222 * 1024;   // dynamic shared memory a CTA may use (227 KB less static)
+static constexpr size_t SMEM_SM = 228 * 1024;     // shared memory per SM
+static constexpr size_t SMEM_CTA_RESERVE = 6144;  // per-CTA system reserve + static shared memory
+
+template <typename T, int F>
+static sla_status allow_smem_fused() {
+    CU(cudaFuncSetAttribute(k_cg_fused<T, F, 0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    CU(cudaFuncSetAttribute(k_cg_fused<T, F, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    CU(cudaFuncSetAttribute(k_cg_fused<T, F, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    CU(cudaFuncSetAttribute(k_cg_fused<T, F, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    return SLA_OK;
+}
+
 template <typename T>
 static sla_status allow_smem() {
     static std::atomic<int> done{0};
@@ -212,17 +237,37 @@ static sla_status allow_smem() {
     TRY((allow_smem_form<T, 0>(b)));
     TRY((allow_smem_form<T, 1>(b)));
     TRY((allow_smem_form<T, 2>(b)));
-    CU(cudaFuncSetAttribute(k_init_x0<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
-    CU(cudaFuncSetAttribute(k_final<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
-    CU(cudaFuncSetAttribute(k_grad_A<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    TRY((allow_smem_form<T, 3>(SMEM_CTA_MAX)));
+    TRY((allow_smem_fused<T, 0>()));
+    TRY((allow_smem_fused<T, 1>()));
+    TRY((allow_smem_fused<T, 2>()));
+    TRY((allow_smem_fused<T, 3>()));
+    CU(cudaFuncSetAttribute(k_init_x0<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    CU(cudaFuncSetAttribute(k_final<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    CU(cudaFuncSetAttribute(k_grad_A<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
     done.store(1);
     return SLA_OK;
 }
 
-// Compiled form of the staged product for a layout (see spmv_vec).
-static int form_of(const Layout& L) {
-    if (staging_form(L.cap) == 0) return 0;
-    return L.gasync ? 2 : 1;
+// Warp pipeline (FORM 3): shared memory per warp for capacity `ccap`, S
+// stages and `vb`-byte values (gathered entries sized at 8 bytes, the
+// largest).
+#ifndef SLA_PIPE_CTAS
+#define SLA_PIPE_CTAS 3   // most resident CTAs per SM the warp pipeline aims for
+#endif
+static size_t pipe_bytes(int ccap, int S, size_t vb) {
+    return sizeof(PipeHdr) + (size_t)S * ccap * (vb + sizeof(int)) + 2 * (size_t)ccap * sizeof(double);
+}
+// Most stages (3 or 4) that fit the most resident CTAs per SM (3 or 2); 0
+// when not even two CTAs of three stages fit (the warp-staged forms then
+// serve the matrix).
+static int pipe_stages(int ccap, size_t vb) {
+    for (int ctas = SLA_PIPE_CTAS; ctas >= 2; --ctas)
+        for (int S = MAX_STAGES; S >= 3; --S) {
+            const size_t b = (size_t)NWARP * pipe_bytes(ccap, S, vb);
+            if (b <= (size_t)SMEM_CTA_MAX && (b + SMEM_CTA_RESERVE) * ctas <= SMEM_SM) return S;
+        }
+    return 0;
 }
 
 template <class F>
@@ -230,25 +275,41 @@ static void with_form(int form, F&& f) {
     switch (form) {
         case 0: f(std::integral_constant<int, 0>{}); break;
         case 1: f(std::integral_constant<int, 1>{}); break;
-        default: f(std::integral_constant<int, 2>{}); break;
+        case 2: f(std::integral_constant<int, 2>{}); break;
+        default: f(std::integral_constant<int, 3>{}); break;
     }
 }
 
-// CTAs per system for the staged SpMV kernels with staging capacity `cap`.
+// Compiled form, shared memory and CTAs per system of a layout's kernels.
+// The warp pipeline needs a group capacity (pattern) and 16-byte aligned
+// values (`aligned`); `vb` is the value size in bytes.  Every kernel that
+// takes the layout's Mat is launched with L->smem.
 template <typename T>
-static sla_status spmv_grid(const sla_csr* h, Layout* L) {
+static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb) {
+    L->stages = L->ccap > 0 && aligned && h->pipeline ? pipe_stages(L->ccap, vb) : 0;
+    if (L->stages > 0) {
+        L->form = 3;
+        L->smem = (size_t)NWARP * pipe_bytes(L->ccap, L->stages, vb);
+    } else {
+        L->form = staging_form(L->cap) == 0 ? 0 : (L->gasync ? 2 : 1);
+        L->smem = spmv_smem(L->cap);
+    }
     int per = 1;
     sla_status st = SLA_OK;
-    with_form(form_of(*L), [&](auto f) {
-        st = occupancy(k_spmv_iter<T, decltype(f)::value>, spmv_smem(L->cap), &per);
-    });
+    with_form(L->form, [&](auto f) { st = occupancy(k_spmv_iter<T, decltype(f)::value>, L->smem, &per); });
     TRY(st);
-    L->gx = grid_x(h, group_ctas(h->n, L->lanes), per);
+    L->gx = grid_x(h, group_ctas(h->n, L->form == 3 ? 1 : L->lanes), per);
     return SLA_OK;
 }
 
-static sla_status spmv_grid_any(const sla_csr* h, Layout* L) {
-    return h->dt == SLA_F64 ? spmv_grid<double>(h, L) : spmv_grid<float>(h, L);
+static sla_status set_form_any(const sla_csr* h, Layout* L, bool aligned, size_t vb) {
+    return h->dt == SLA_F64 ? set_form<double>(h, L, aligned, vb) : set_form<float>(h, L, aligned, vb);
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+// Values of every system 16-byte aligned (chunk pipeline bulk copies).
+static bool vals_aligned(const sla_csr* h, const void* vals) {
+    return aligned16(vals) && (h->batch == 1 || ((size_t)h->nnz * h->es) % 16 == 0);
 }
 
 // Streaming kernels: two resident CTAs per SM.  Each warp-level fp64
@@ -270,17 +331,30 @@ static Sys sys_of(sla_csr* h) {
     return s;
 }
 
-static Mat mat_of(const int* rp, const int* ci, int n, const Layout& L) {
+static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layout& L, int* err) {
     Mat m;
     m.rp = rp;
     m.ci = ci;
     m.n = n;
     m.cap = L.cap;
     m.async = staging_form(L.cap);
-    m.wstride = (int)(spmv_smem(L.cap) / NWARP / sizeof(double));
-    m.lanes = L.lanes;
-    m.lshift = L.lanes == 4 ? 2 : (L.lanes == 2 ? 1 : 0);
+    // doubles of shared memory per warp (L.smem / NWARP)
+    m.wstride = (int)(L.smem / NWARP / sizeof(double));
+    m.lanes = L.form == 3 ? 1 : L.lanes;
+    m.lshift = m.lanes == 4 ? 2 : (m.lanes == 2 ? 1 : 0);
+    if (L.form == 3) m.cap = L.ccap;   // every group stages in the register-staged passes too
+    m.nnz = nnz;
+    m.ccap = L.ccap;
+    m.stages = L.stages;
+    m.err = err;
     return m;
+}
+static Mat mat_A(const sla_csr* h) { return mat_of(h->rp, h->ci, h->n, h->nnz, h->LA, &h->ctl.as<Ctrl>()->err); }
+static Mat mat_G(const sla_csr* h) {
+    return mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->nnzg, h->LG, &h->ctl.as<Ctrl>()->err);
+}
+static Mat mat_GT(const sla_csr* h) {
+    return mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->nnzg, h->LGT, &h->ctl.as<Ctrl>()->err);
 }
 
 // ===================================================================== set-up helpers
@@ -329,7 +403,7 @@ static sla_status group_max(const int* rp, int n, int rows, int* out, cudaStream
 static constexpr int NEAR_WINDOW = 65536;
 
 static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, long long nnz, Layout* L,
-                                cudaStream_t s) {
+                                bool aligned, size_t vb, cudaStream_t s) {
     {
         DevBuf far;
         TRY(far.alloc(sizeof(unsigned long long)));
@@ -353,7 +427,21 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
             break;
         }
     }
-    return spmv_grid_any(h, L);
+    // warp pipeline: largest group of 32 rows, as staged
+    L->ccap = 0;
+    if (aligned16(rp) && aligned16(ci)) {
+        DevBuf m;
+        TRY(m.alloc(sizeof(int)));
+        CU(cudaMemsetAsync(m.p, 0, sizeof(int), s));
+        const long long nc = ((long long)h->n + 31) / 32;
+        const int g = (nc + 255) / 256 < 2048 ? (int)((nc + 255) / 256) : 2048;
+        k_chunk_max<<<g, 256, 0, s>>>(rp, h->n, 32, m.as<int>());
+        TRY(launched());
+        int cc = 0;
+        TRY(read_int(m.as<int>(), &cc, s));
+        L->ccap = cc < 4 ? 4 : cc;
+    }
+    return set_form_any(h, L, aligned, vb);
 }
 
 static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
@@ -380,7 +468,7 @@ static void release_spai(sla_csr* h) {
     h->spai_ready = false;
     h->grp.release(); h->gci.release(); h->gv.release();
     h->gtrp.release(); h->gtci.release(); h->gtv.release();
-    h->z.release(); h->t.release();
+    h->t.release();
     for (auto& g : h->graph) g.reset();
 }
 
@@ -404,17 +492,18 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     TRY(read_int(h->gtrp.as<int>() + n, &ngt, s));
     if (ng != ngt) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
     h->nnzg = ng;
+    h->gstride = ((long long)ng + 1) & ~1LL;
     TRY(h->gci.alloc(sizeof(int) * (size_t)ng));
     TRY(h->gtci.alloc(sizeof(int) * (size_t)ng));
-    TRY(h->gv.alloc(sizeof(double) * (size_t)ng * h->batch));
-    TRY(h->gtv.alloc(sizeof(double) * (size_t)ng * h->batch));
+    TRY(h->gv.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
+    TRY(h->gtv.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
     DevBuf err;
     TRY(err.alloc(sizeof(int)));
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
     for (int sy = 0; sy < h->batch; ++sy) {
         const double* dg = h->diag.as<double>() + (size_t)sy * n;
-        double* gv = h->gv.as<double>() + (size_t)sy * ng;     // 8-byte slots: fp64, or a
-        double* gtv = h->gtv.as<double>() + (size_t)sy * ng;   // double-float pair for fp32
+        double* gv = h->gv.as<double>() + (size_t)sy * h->gstride;     // 8-byte slots: fp64, or a
+        double* gtv = h->gtv.as<double>() + (size_t)sy * h->gstride;   // double-float pair for fp32
         if (h->dt == SLA_F64) {
             const double* av = (const double*)h->vals + (size_t)sy * h->nnz;
             k_fill_G<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
@@ -435,9 +524,8 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     int e = 0;
     TRY(read_int(err.as<int>(), &e, s));
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
-    TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, s));
-    TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, s));
-    TRY(h->z.alloc(WORK_BYTES * (size_t)n * h->batch));
+    TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, true, sizeof(double), s));
+    TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s));
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
     h->spai_ready = true;
     return ensure_pstride(h);
@@ -446,11 +534,15 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
 static sla_status ensure_pstride(sla_csr* h) {
     int m = gx_vec(h);
     m = m > h->LA.gx ? m : h->LA.gx;
+    // the fused iteration kernel: two reductions of two values per CTA, at
+    // most as many CTAs as fit resident (2048 threads per SM)
+    const int fused = (int)((long long)(2048 / NT) * h->sms / h->batch) + 1;
+    m = m > fused ? m : fused;
     if (h->spai_ready) {
         m = m > h->LG.gx ? m : h->LG.gx;
         m = m > h->LGT.gx ? m : h->LGT.gx;
     }
-    const int need = 2 * m;
+    const int need = 4 * m;
     if (need <= h->pstride) return SLA_OK;
     TRY(h->part.alloc(sizeof(double) * (size_t)need * h->batch));
     h->pstride = need;
@@ -462,7 +554,7 @@ static sla_status ensure_pstride(sla_csr* h) {
 template <typename T, bool PAIRS>
 static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
+    const Mat A = mat_A(h);
     const T* av = (const T*)h->vals;
     using W = typename Prec<T>::w;
     W* r = h->r.as<W>();
@@ -473,39 +565,39 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     XW* x = h->x.as<XW>();
     const XW* dinv = h->dinv.as<XW>();
     const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
-    with_form(form_of(h->LA), [&](auto f) {
-        k_spmv_iter<T, decltype(f)::value><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    with_form(h->LA.form, [&](auto f) {
+        k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LA.smem, s>>>(A, S, av, p, q, x, h->bw.as<T>());
     });
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
-        k_update<T, 2, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        k_update<T, 2, PAIRS><<<gv, NT, 0, s>>>(S, r, q, dinv, h->z.as<W>());
         TRY(launched());
-        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->LGT);
-        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
-        with_form(form_of(h->LGT), [&](auto f) {
-        k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
+        const Mat GT = mat_GT(h);
+        const Mat G = mat_G(h);
+        with_form(h->LGT.form, [&](auto f) {
+        k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, h->LGT.smem, s>>>(GT, S, h->gstride,
                                                                                         h->gtv.as<GV>(), r,
                                                                                         h->t.as<W>());
         });
         TRY(launched());
-        with_form(form_of(h->LG), [&](auto f) {
-        k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
-            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
+        with_form(h->LG.form, [&](auto f) {
+        k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, h->LG.smem, s>>>(
+            G, S, h->gstride, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
         });
         TRY(launched());
-        k_pupdate<T, 2, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, h->z.as<W>(), dinv);
+        k_pupdate<T, false, PAIRS><<<gv, NT, 0, s>>>(S, p, x, h->z.as<W>());
         TRY(launched());
         *nodes += 5;
     } else if (pc == SLA_PC_JACOBI) {
-        k_update<T, 1, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        k_update<T, 1, PAIRS><<<gv, NT, 0, s>>>(S, r, q, dinv, h->z.as<W>());
         TRY(launched());
-        k_pupdate<T, 1, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
+        k_pupdate<T, false, PAIRS><<<gv, NT, 0, s>>>(S, p, x, h->z.as<W>());
         TRY(launched());
         *nodes += 3;
     } else {
-        k_update<T, 0, PAIRS><<<gv, NT, 0, s>>>(S, x, r, p, q, dinv);
+        k_update<T, 0, PAIRS><<<gv, NT, 0, s>>>(S, r, q, dinv, h->z.as<W>());
         TRY(launched());
-        k_pupdate<T, 0, false, PAIRS><<<gv, NT, 0, s>>>(S, p, r, nullptr, dinv);
+        k_pupdate<T, false, PAIRS><<<gv, NT, 0, s>>>(S, p, x, r);
         TRY(launched());
         *nodes += 3;
     }
@@ -549,6 +641,66 @@ static sla_status get_graph(sla_csr* h, int pc, double eps, int k, GraphCache** 
     return SLA_OK;
 }
 
+// ===================================================================== fused iteration
+// Grid of the persistent iteration kernel: every CTA must be resident (a
+// cooperative launch), so at most the occupancy times the SM count, spread
+// over the batch; 0 when not even one CTA per system fits.
+template <typename T, int PC, bool PAIRS>
+static sla_status fused_grid(const sla_csr* h, int* gx) {
+    int per = 0;
+    cudaError_t e = cudaSuccess;
+    with_form(h->LA.form, [&](auto f) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_cg_fused<T, decltype(f)::value, PC, PAIRS>, NT,
+                                                          h->LA.smem);
+    });
+    if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
+    long long g = (long long)per * h->sms / h->batch;
+    const long long work = std::max(group_ctas(h->n, h->LA.form == 3 ? 1 : h->LA.lanes), vec_units(h));
+    if (g > work) g = work;
+    *gx = (int)g;
+    return SLA_OK;
+}
+
+template <typename T, int PC, bool PAIRS>
+static sla_status launch_fused(sla_csr* h, int gx, int iters, cudaStream_t s) {
+    using W = typename Prec<T>::w;
+    using XW = typename Prec<T>::xw;
+    Mat A = mat_A(h);
+    Sys S = sys_of(h);
+    const T* av = (const T*)h->vals;
+    W* p = h->p.as<W>();
+    W* q = h->q.as<W>();
+    W* r = h->r.as<W>();
+    W* z = h->z.as<W>();
+    XW* x = h->x.as<XW>();
+    const XW* dinv = h->dinv.as<XW>();
+    const T* b = h->bw.as<T>();
+    GridSync* gsy = h->gsync.as<GridSync>();
+    void* args[] = {&A, &S, &av, &p, &q, &r, &z, &x, &dinv, &b, &gsy, &iters};
+    cudaError_t e = cudaSuccess;
+    with_form(h->LA.form, [&](auto f) {
+        e = cudaLaunchCooperativeKernel((const void*)k_cg_fused<T, decltype(f)::value, PC, PAIRS>,
+                                        dim3((unsigned)gx, (unsigned)h->batch), dim3(NT), args, h->LA.smem, s);
+    });
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "cooperative launch failed: %s", cudaGetErrorString(e));
+    return SLA_OK;
+}
+
+template <typename T>
+static sla_status fused_grid_any(const sla_csr* h, int pc, int* gx) {
+    const bool pr = pairs_ok(h);
+    if (pc == SLA_PC_JACOBI) return pr ? fused_grid<T, 1, true>(h, gx) : fused_grid<T, 1, false>(h, gx);
+    return pr ? fused_grid<T, 0, true>(h, gx) : fused_grid<T, 0, false>(h, gx);
+}
+template <typename T>
+static sla_status launch_fused_any(sla_csr* h, int pc, int gx, int iters, cudaStream_t s) {
+    const bool pr = pairs_ok(h);
+    if (pc == SLA_PC_JACOBI)
+        return pr ? launch_fused<T, 1, true>(h, gx, iters, s) : launch_fused<T, 1, false>(h, gx, iters, s);
+    return pr ? launch_fused<T, 0, true>(h, gx, iters, s) : launch_fused<T, 0, false>(h, gx, iters, s);
+}
+
 // ===================================================================== solve driver
 static sla_status from_code(int c) {
     switch (c) {
@@ -568,11 +720,17 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     TRY(ensure_pstride(h));
     const int k = o->poll_k > 0 ? o->poll_k : 32;
     const double eps = pc == SLA_PC_SPAI ? o->eps : 0.0;
+    // A CUDA graph of k iterations of one kernel per step; with
+    // SLA_PERSISTENT, CG and Jacobi-PCG instead run as the persistent
+    // iteration kernel wherever every CTA can be resident.
+    int gxf = 0;
+    if (pc != SLA_PC_SPAI && h->coop && h->persistent) TRY(fused_grid_any<T>(h, pc, &gxf));
+    const bool fused = gxf >= 1;
     GraphCache* gc = nullptr;
-    TRY(get_graph<T>(h, pc, eps, k, &gc));
+    if (!fused) TRY(get_graph<T>(h, pc, eps, k, &gc));
 
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
+    const Mat A = mat_A(h);
     const T* av = (const T*)h->vals;
     const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
     using W = typename Prec<T>::w;
@@ -584,28 +742,29 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     const XW* dinv = h->dinv.as<XW>();
 
     CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
+    CU(cudaMemsetAsync(h->gsync.p, 0, sizeof(GridSync) * h->batch, s));
     if (o->use_x0) {
-        k_init_x0<T><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
+        k_init_x0<T><<<gs, NT, h->LA.smem, s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
                                                          o->max_iter);
     } else {
         k_init<T><<<gv, NT, 0, s>>>(S, b, h->bw.as<T>(), x, r, o->tol, o->max_iter);
     }
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
-        const Mat GT = mat_of(h->gtrp.as<int>(), h->gtci.as<int>(), h->n, h->LGT);
-        const Mat G = mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->LG);
-        with_form(form_of(h->LGT), [&](auto f) {
-        k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, spmv_smem(h->LGT.cap), s>>>(GT, S, h->nnzg,
+        const Mat GT = mat_GT(h);
+        const Mat G = mat_G(h);
+        with_form(h->LGT.form, [&](auto f) {
+        k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, h->LGT.smem, s>>>(GT, S, h->gstride,
                                                                                        h->gtv.as<GV>(), r,
                                                                                        h->t.as<W>());
         });
         TRY(launched());
-        with_form(form_of(h->LG), [&](auto f) {
-        k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, spmv_smem(h->LG.cap), s>>>(
-            G, S, h->nnzg, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
+        with_form(h->LG.form, [&](auto f) {
+        k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, h->LG.smem, s>>>(
+            G, S, h->gstride, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
         });
         TRY(launched());
-        k_pupdate<T, 2, true, false><<<gv, NT, 0, s>>>(S, p, r, h->z.as<W>(), dinv);
+        k_pupdate<T, true, false><<<gv, NT, 0, s>>>(S, p, x, h->z.as<W>());
     } else if (pc == SLA_PC_JACOBI) {
         k_init_dir<T, 1><<<gv, NT, 0, s>>>(S, p, r, dinv);
     } else {
@@ -622,8 +781,12 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     while (!finished) {
         if (issued < cap_launches && !timed_out) {
             const int slot = (head + inflight) & 1;
-            CU(cudaGraphLaunch(gc->exec, s));
-            g_launches.fetch_add((unsigned long long)gc->nodes, std::memory_order_relaxed);
+            if (fused) {
+                TRY(launch_fused_any<T>(h, pc, gxf, k, s));
+            } else {
+                CU(cudaGraphLaunch(gc->exec, s));
+                g_launches.fetch_add((unsigned long long)gc->nodes, std::memory_order_relaxed);
+            }
             CU(cudaMemcpyAsync(&h->h_flag[slot], &h->ctl.as<Ctrl>()->all_done, sizeof(int),
                                cudaMemcpyDeviceToHost, s));
             CU(cudaEventRecord(h->ev[slot], s));
@@ -654,10 +817,16 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     // drain (kernels of a finished batch return at once)
     CU(cudaStreamSynchronize(s));
 
-    k_final<T><<<gs, NT, spmv_smem(h->LA.cap), s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
+    k_final<T><<<gs, NT, h->LA.smem, s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
     TRY(launched());
     CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
+    Ctrl dc;
+    CU(cudaMemcpyAsync(&dc, h->ctl.p, sizeof(Ctrl), cudaMemcpyDeviceToHost, s));
     CU(cudaStreamSynchronize(s));
+    if (dc.err & (ERR_WAIT | ERR_GRID))
+        return fail(SLA_ERR_CUDA, "a device wait gave up (%s; at %d: %d %d %d); results invalid",
+                    (dc.err & ERR_GRID) ? "grid barrier" : "bulk copy", dc.diag[0], dc.diag[1], dc.diag[2],
+                    dc.diag[3]);
 
     sla_status ret = SLA_OK;
     for (int i = 0; i < h->batch; ++i) {
@@ -712,7 +881,7 @@ sla_status sla_csr_destroy(sla_handle h) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
     DevBuf* bufs[] = {&h->diag, &h->dinv, &h->grp, &h->gci, &h->gv, &h->gtrp, &h->gtci, &h->gtv,
                       &h->x, &h->r, &h->p, &h->q, &h->z, &h->t, &h->bw, &h->state,
-                      &h->ctl, &h->cnt, &h->part, &h->stat};
+                      &h->ctl, &h->cnt, &h->part, &h->stat, &h->gsync};
     for (DevBuf* b : bufs) b->release();
     destroy_handle(h);
     return SLA_OK;
@@ -781,7 +950,15 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
                              (e & ERR_COL_ORDER) ? " columns not strictly ascending" : ""));
     }
     HTRY(dt == SLA_F64 ? allow_smem<double>() : allow_smem<float>());
-    HTRY(choose_layout(h, d_row_ptr, d_col_idx, nnz, &h->LA, s));
+    h->vals_aligned = vals_aligned(h, d_vals);
+    h->pipeline = (flags & SLA_WARP_PIPELINE) != 0;
+    h->persistent = (flags & SLA_PERSISTENT) != 0;
+    {
+        int coop = 0;
+        HCU(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
+        h->coop = coop != 0;
+    }
+    HTRY(choose_layout(h, d_row_ptr, d_col_idx, nnz, &h->LA, h->vals_aligned, h->es, s));
     const size_t vn = (size_t)n * batch;
     HTRY(h->diag.alloc(sizeof(double) * vn));
     HTRY(h->dinv.alloc(sizeof(double) * vn));
@@ -790,6 +967,9 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     HTRY(h->r.alloc(WORK_BYTES * vn));
     HTRY(h->p.alloc(WORK_BYTES * vn));
     HTRY(h->q.alloc(WORK_BYTES * vn));
+    HTRY(h->z.alloc(WORK_BYTES * vn));
+    HTRY(h->gsync.alloc(sizeof(GridSync) * batch));
+    HCU(cudaMemsetAsync(h->gsync.p, 0, sizeof(GridSync) * batch, s));
     HTRY(h->bw.alloc(h->es * vn));
     HTRY(h->state.alloc(sizeof(State) * batch));
     HTRY(h->ctl.alloc(sizeof(Ctrl)));
@@ -806,6 +986,13 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     return SLA_OK;
 }
 
+sla_status sla_csr_layout(sla_handle h, int* form, int* ctas) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (form) *form = h->LA.form;
+    if (ctas) *ctas = h->LA.gx;
+    return SLA_OK;
+}
+
 sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
     if (!d_vals && h->nnz > 0) return fail(SLA_ERR_INVALID, "null values");
@@ -813,6 +1000,11 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
     h->vals = d_vals;
     release_spai(h);     // rebuilt on the next SPAI solve
     for (auto& g : h->graph) g.reset();
+    if (vals_aligned(h, d_vals) != h->vals_aligned) {
+        h->vals_aligned = !h->vals_aligned;
+        TRY(set_form_any(h, &h->LA, h->vals_aligned, h->es));
+        TRY(ensure_pstride(h));
+    }
     TRY(compute_diag(h, s));
     CU(cudaStreamSynchronize(s));
     return SLA_OK;
@@ -823,10 +1015,10 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     if (!d_x || !d_y) return fail(SLA_ERR_INVALID, "null vector");
     cudaStream_t s = (cudaStream_t)stream;
     const Sys S = sys_of(h);
-    const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
+    const Mat A = mat_A(h);
     const dim3 g(h->LA.gx, h->batch);
-    const size_t sm = spmv_smem(h->LA.cap);
-    with_form(form_of(h->LA), [&](auto f) {
+    const size_t sm = h->LA.smem;
+    with_form(h->LA.form, [&](auto f) {
         constexpr int F = decltype(f)::value;
         if (h->dt == SLA_F64)
             k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_x, (double*)d_y,
@@ -881,13 +1073,13 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
     if (st != SLA_OK && st != SLA_ERR_NOT_CONVERGED && st != SLA_ERR_BREAKDOWN && st != SLA_ERR_TIMEOUT) return st;
     if (d_dLdA && h->nnz > 0) {
         const Sys S = sys_of(h);
-        const Mat A = mat_of(h->rp, h->ci, h->n, h->LA);
+        const Mat A = mat_A(h);
         const dim3 g(h->LA.gx, h->batch);
         if (h->dt == SLA_F64)
-            k_grad_A<double><<<g, NT, grad_smem(h->LA.cap), s>>>(A, S, (const double*)d_dLdb, (const double*)d_x,
+            k_grad_A<double><<<g, NT, h->LA.smem, s>>>(A, S, (const double*)d_dLdb, (const double*)d_x,
                                                                (double*)d_dLdA);
         else
-            k_grad_A<float><<<g, NT, grad_smem(h->LA.cap), s>>>(A, S, (const float*)d_dLdb, (const float*)d_x,
+            k_grad_A<float><<<g, NT, h->LA.smem, s>>>(A, S, (const float*)d_dLdb, (const float*)d_x,
                                                               (float*)d_dLdA);
         sla_status l = launched();
         if (l != SLA_OK) return l;
@@ -965,7 +1157,9 @@ static sla_status spmv_dot_static_impl(int n, long long nnz, int batch, const in
     L.cap = STATIC_CAP;
     L.lanes = 1;
     L.gasync = 0;
-    const Mat A = mat_of(rp, ci, n, L);
+    L.form = 1;
+    L.smem = smem;
+    const Mat A = mat_of(rp, ci, n, nnz, L, nullptr);
     k_spmv<T, 1><<<dim3((unsigned)gx, batch), NT, smem, s>>>(A, S, vals, x, y, dot);
     return launched();
 }

@@ -2,6 +2,12 @@
 on the same seeded inputs, element by element, at sizes the oracle finishes
 in seconds (several row blocks and a ragged tail), plus edge cases.
 
+Every product test runs with the warp-staged forms (the default) and with
+the warp pipeline (pipeline=True, wherever a group fits its stages); the
+solve tests run with one kernel per step in a CUDA graph (the default) and
+with the persistent iteration kernel (fused=True), the latter with either
+product form.
+
 Tolerances: SpMV relative error <= 1e-12 (fp64) and <= 1e-5 (fp32);
 ||x - x_oracle|| / ||x_oracle|| <= 1e-6; iteration count within 2% of the
 oracle's (at least +-1); true residual of the returned x <= tol."""
@@ -41,12 +47,23 @@ def _spmv_cases():
     yield "dense_row", CSR(n, rp, np.concatenate(cols).astype(np.int32), g.standard_normal(int(rp[-1])))
 
 
+PIPE = pytest.mark.parametrize("pipeline", [False, True], ids=["warp", "pipe"])
+MODES = pytest.mark.parametrize("pipeline,fused", [(False, False), (True, False), (False, True), (True, True)],
+                                ids=["steps", "pipe-steps", "fused", "pipe-fused"])
+
+
+@PIPE
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 @pytest.mark.parametrize("name,A", list(_spmv_cases()), ids=lambda v: v if isinstance(v, str) else "")
-def test_spmv_parity(cuda_device, name, A, dtype):
+def test_spmv_parity(cuda_device, name, A, dtype, pipeline):
     A = CSR(A.n, A.row_ptr, A.col_idx, A.vals.astype(dtype))
     x = np.random.default_rng(11).standard_normal(A.n).astype(dtype)
-    M = make(A)
+    M = make(A, pipeline=pipeline)
+    form = M.layout()[0]
+    if not pipeline:
+        assert form in (0, 1, 2)
+    elif name not in ("dense_row", "knn_3000"):   # groups of 32 short rows fit the warp pipeline
+        assert form == 3, form
     xd = torch.from_numpy(x).to(cuda_device)
     y = M.matvec(xd).cpu().numpy()
     y_o = oracle.spmv(A, x.astype(np.float64))
@@ -59,9 +76,10 @@ def test_spmv_parity(cuda_device, name, A, dtype):
     assert abs(dot.item() - d_o) <= 1e-12 * max(1.0, float(np.abs(x) @ np.abs(y)))
 
 
-def test_spmv_batched(cuda_device):
+@PIPE
+def test_spmv_batched(cuda_device, pipeline):
     w = build("c3", N=40, batch=3)
-    M = make(w.A)
+    M = make(w.A, pipeline=pipeline)
     x = torch.from_numpy(w.b).to(cuda_device)
     y = M.matvec(x).cpu().numpy()
     for s in range(3):
@@ -84,10 +102,11 @@ SOLVE_CASES = [
 ]
 
 
+@MODES
 @pytest.mark.parametrize("cfg,kw,pc", SOLVE_CASES, ids=[f"{c}-{p}-{k}" for c, k, p in SOLVE_CASES])
-def test_pcg_parity(cuda_device, cfg, kw, pc):
+def test_pcg_parity(cuda_device, cfg, kw, pc, pipeline, fused):
     w = build(cfg, **kw)
-    M = make(w.A)
+    M = make(w.A, pipeline=pipeline, fused=fused)
     b = torch.from_numpy(w.b).to(cuda_device)
     x, info = M.solve(b, tol=w.tol, max_iter=20000, pc=pc, eps=1e-3, poll_k=16)
     x = x.cpu().numpy()
@@ -108,10 +127,11 @@ ADJ_CASES = [("c4", {"N": 24}, "none"), ("c2", {"N": 64}, "jacobi"), ("c5", {"np
              ("c3", {"N": 32, "batch": 3}, "jacobi")]
 
 
+@MODES
 @pytest.mark.parametrize("cfg,kw,pc", ADJ_CASES, ids=[f"{c}-{p}" for c, k, p in ADJ_CASES])
-def test_adjoint_parity(cuda_device, cfg, kw, pc):
+def test_adjoint_parity(cuda_device, cfg, kw, pc, pipeline, fused):
     w = build(cfg, **kw)
-    M = make(w.A)
+    M = make(w.A, pipeline=pipeline, fused=fused)
     b = torch.from_numpy(w.b).to(cuda_device)
     g = torch.from_numpy(w.g).to(cuda_device)
     x, _ = M.solve(b, tol=w.tol, max_iter=20000, pc=pc)
@@ -160,10 +180,14 @@ def test_zero_rhs(cuda_device):
     assert info[0].iters == 0 and not x.abs().sum().item()
 
 
+FUSED = pytest.mark.parametrize("fused", [True, False], ids=["fused", "steps"])
+
+
+@FUSED
 @pytest.mark.parametrize("max_iter", [0, 1, 2, 37])
-def test_max_iter_reached(cuda_device, max_iter):
+def test_max_iter_reached(cuda_device, max_iter, fused):
     w = build("c2", N=40)
-    M = make(w.A)
+    M = make(w.A, fused=fused)
     b = torch.from_numpy(w.b).to(cuda_device)
     x, info = M.solve(b, tol=1e-12, max_iter=max_iter, pc="jacobi", poll_k=8)
     xo, io = oracle.pcg(w.A, w.b, 1e-12, max_iter=max_iter, pc="jacobi")
@@ -172,22 +196,24 @@ def test_max_iter_reached(cuda_device, max_iter):
     assert rel(x.cpu().numpy(), xo) <= 1e-9
 
 
-def test_breakdown_nan_and_indefinite(cuda_device):
+@FUSED
+def test_breakdown_nan_and_indefinite(cuda_device, fused):
     w = build("c1")
-    M = make(w.A)
+    M = make(w.A, fused=fused)
     b = torch.from_numpy(w.b).to(cuda_device).clone()
     b[17] = float("nan")
     _, info = M.solve(b, tol=1e-8)
     assert info[0].status == "breakdown"
     D = CSR(3, np.array([0, 1, 2, 3], np.int32), np.array([0, 1, 2], np.int32), np.array([1.0, -1.0, 2.0]))
-    M2 = make(D)
+    M2 = make(D, fused=fused)
     _, info = M2.solve(torch.ones(3, dtype=torch.float64, device=cuda_device), tol=1e-8)
     assert info[0].status == "breakdown" == oracle.pcg(D, np.ones(3), 1e-8)[1]["status"]
 
 
-def test_initial_guess_parity(cuda_device):
+@FUSED
+def test_initial_guess_parity(cuda_device, fused):
     w = build("c2", N=64)
-    M = make(w.A)
+    M = make(w.A, fused=fused)
     b = torch.from_numpy(w.b).to(cuda_device)
     x0 = np.random.default_rng(1).standard_normal(w.A.n)
     x, info = M.solve(b, tol=1e-9, pc="jacobi", x0=torch.from_numpy(x0).to(cuda_device))
@@ -228,9 +254,10 @@ def test_spai_rejects_unsymmetric_pattern(cuda_device):
         M.solve(torch.ones(3, dtype=torch.float64, device=cuda_device), pc="spai")
 
 
-def test_timeout_reports_and_keeps_iterate(cuda_device):
+@FUSED
+def test_timeout_reports_and_keeps_iterate(cuda_device, fused):
     w = build("c4", N=48)
-    M = make(w.A)
+    M = make(w.A, fused=fused)
     b = torch.from_numpy(w.b).to(cuda_device)
     x, info = M.solve(b, tol=1e-14, max_iter=100000, poll_k=1, timeout_s=1e-4)
     assert info[0].status in ("timeout", "ok")
@@ -238,12 +265,13 @@ def test_timeout_reports_and_keeps_iterate(cuda_device):
     assert np.isfinite(x.cpu().numpy()).all()
 
 
-def test_repeat_solves_are_deterministic(cuda_device):
+@pytest.mark.parametrize("pc", ["spai", "jacobi"])
+def test_repeat_solves_are_deterministic(cuda_device, pc):
     w = build("c5", npoints=20000)
     M = make(w.A)
     b = torch.from_numpy(w.b).to(cuda_device)
-    x1, i1 = M.solve(b, tol=1e-8, pc="spai")
-    x2, i2 = M.solve(b, tol=1e-8, pc="spai", poll_k=7)
+    x1, i1 = M.solve(b, tol=1e-8, pc=pc)
+    x2, i2 = M.solve(b, tol=1e-8, pc=pc, poll_k=7)
     assert i1[0].iters == i2[0].iters and torch.equal(x1, x2)
 
 
@@ -259,10 +287,44 @@ def test_update_values(cuda_device):
     assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
 
 
-def test_launch_count_advances(cuda_device):
+@FUSED
+def test_launch_count_advances(cuda_device, fused):
+    """Kernel-per-step solves launch three kernels per iteration; the
+    persistent kernel one per poll interval (plus set-up and the final pass)."""
     from sparse_iterative_linear_csr_b300 import launch_count
     w = build("c1")
-    M = make(w.A)
+    M = make(w.A, fused=fused)
     c0 = launch_count()
-    M.solve(torch.from_numpy(w.b).to(cuda_device), tol=1e-10)
-    assert launch_count() > c0 + 3 * 200
+    _, info = M.solve(torch.from_numpy(w.b).to(cuda_device), tol=1e-10, poll_k=16)
+    it = info[0].iters
+    if fused:
+        assert c0 + it // 16 + 2 <= launch_count() <= c0 + it // 16 + 8
+    else:
+        assert launch_count() >= c0 + 3 * it
+
+
+def test_unaligned_values_leave_the_pipeline(cuda_device):
+    """Values at an 8-byte offset cannot be bulk-copied: the handle falls
+    back to a warp-staged form, and returns to the pipeline once aligned
+    values are swapped in; products agree with the oracle throughout."""
+    A = poisson_grid((40, 40))
+    from gpu_util import to_device
+    from sparse_iterative_linear_csr_b300 import CSRMatrix
+    rp, ci, v = to_device(A, cuda_device)
+    buf = torch.zeros(A.nnz + 1, dtype=torch.float64, device=cuda_device)
+    off = buf[1:]
+    off.copy_(v)
+    assert off.data_ptr() % 16 == 8
+    x = np.random.default_rng(5).standard_normal(A.n)
+    xd = torch.from_numpy(x).to(cuda_device)
+    y_o = oracle.spmv(A, x)
+    M = CSRMatrix(rp, ci, off, pipeline=True)
+    assert M.layout()[0] != 3
+    assert rel(M.matvec(xd).cpu().numpy(), y_o) <= 1e-13
+    M.update_values(v)
+    assert M.layout()[0] == 3
+    assert rel(M.matvec(xd).cpu().numpy(), y_o) <= 1e-13
+    M.update_values(off)
+    assert M.layout()[0] != 3
+    xs, info = M.solve(torch.from_numpy(y_o).to(cuda_device), tol=1e-10, pc="jacobi")
+    assert info[0].status == "ok" and rel(xs.cpu().numpy(), x) <= 1e-6
