@@ -72,6 +72,7 @@ typedef enum {
 #define SLA_WARP_PIPELINE 2u /* use the warp-pipeline product where it applies (see sla_csr_layout) */
 #define SLA_PERSISTENT 4u    /* CG / Jacobi-PCG: one persistent iteration kernel per poll interval
                                 instead of a CUDA graph of one kernel per step (see sla_pcg_solve) */
+#define SLA_TIME_PRODUCT 8u  /* time one CG product kernel per graph launch (sla_product_time) */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -122,6 +123,21 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  * Either pointer may be NULL.  SLA_ERR_INVALID for a null handle.
  */
 sla_status sla_csr_layout(sla_handle h, int* form, int* ctas);
+
+/*
+ * Live duration of the CG product kernel (q = A p fused with p.q and the
+ * pending true-residual check), for handles created with SLA_TIME_PRODUCT:
+ * every graph launch of sla_pcg_solve / sla_adjoint records CUDA events on
+ * the solve's stream around the product kernel of its middle iteration,
+ * and the solve adds that duration once the launch has finished, for
+ * launches that neither start nor end with every system frozen (a system
+ * that freezes within a launch makes its later kernels return at once).  Returns the summed duration in
+ * milliseconds and the number of launches timed since creation or the last
+ * reset; nonzero `reset` clears both after reading.  The persistent
+ * iteration kernel (SLA_PERSISTENT) is not timed.  Either output pointer
+ * may be NULL.  SLA_ERR_INVALID for a null handle.
+ */
+sla_status sla_product_time(sla_handle h, double* total_ms, long long* samples, int reset);
 
 /* Replace the values (same pattern, same dtype, [batch][nnz]); recomputes the
  * value-dependent set-up (diagonal, G, G^T).  Synchronises `stream`. */

@@ -76,10 +76,13 @@ class CSRMatrix:
     this object.  validate=True checks the structure on the device;
     pipeline=True uses the warp-pipeline product where it applies;
     fused=True runs CG / Jacobi-PCG as the persistent iteration kernel
-    instead of a CUDA graph of one kernel per step."""
+    instead of a CUDA graph of one kernel per step; time_product=True
+    records the live duration of one product kernel per graph launch
+    (product_time)."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
-                 validate: bool = True, pipeline: bool = False, fused: bool = False, stream=None):
+                 validate: bool = True, pipeline: bool = False, fused: bool = False,
+                 time_product: bool = False, stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -102,7 +105,8 @@ class CSRMatrix:
         _check(lib.sla_csr_create(self.n, self.nnz, self.batch, dt, _ptr(row_ptr), _ptr(col_idx),
                                   _ptr(values), (_lib.SLA_VALIDATE if validate else 0) |
                                   (_lib.SLA_WARP_PIPELINE if pipeline else 0) |
-                                  (_lib.SLA_PERSISTENT if fused else 0), _stream(stream),
+                                  (_lib.SLA_PERSISTENT if fused else 0) |
+                                  (_lib.SLA_TIME_PRODUCT if time_product else 0), _stream(stream),
                                   C.byref(self._h)))
 
     # -------------------------------------------------------------- lifetime
@@ -144,6 +148,12 @@ class CSRMatrix:
         return [SolveInfo(a.iters, a.rel_res_recursive, a.rel_res_true, STATUS_NAMES[a.status]) for a in arr]
 
     # -------------------------------------------------------------- API
+    def product_time(self, reset: bool = True) -> tuple[float, int]:
+        """(summed ms, launches timed) of the live CG product kernel (time_product=True)."""
+        ms, n = C.c_double(), C.c_longlong()
+        _check(_lib_handle().sla_product_time(self._h, C.byref(ms), C.byref(n), int(reset)))
+        return ms.value, n.value
+
     def layout(self) -> tuple[int, int]:
         """(product form 0..3, CTAs per system) the library chose for A."""
         f, g = C.c_int(), C.c_int()

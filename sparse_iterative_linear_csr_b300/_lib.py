@@ -19,11 +19,12 @@ PC = {"none": 0, "jacobi": 1, "spai": 2}
 SLA_VALIDATE = 1
 SLA_WARP_PIPELINE = 2
 SLA_PERSISTENT = 4
+SLA_TIME_PRODUCT = 8
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
-           "sla_spmv_dot_static", "sla_csr_layout"]
+           "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time"]
 
 
 class PcgOpts(C.Structure):
@@ -55,6 +56,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                    C.POINTER(_vp)]
     lib.sla_csr_update_values.argtypes = [_vp, _vp, _vp]
     lib.sla_csr_layout.argtypes = [_vp, C.POINTER(C.c_int), C.POINTER(C.c_int)]
+    lib.sla_product_time.argtypes = [_vp, C.POINTER(C.c_double), C.POINTER(C.c_longlong), C.c_int]
     lib.sla_spmv.argtypes = [_vp, _vp, _vp, _vp]
     lib.sla_spmv_dot.argtypes = [_vp, _vp, _vp, _vp, _vp]
     lib.sla_pcg_solve.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), C.POINTER(SolveInfo), _vp]
@@ -68,7 +70,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_spmv_dot_static.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
-    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
+    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
               "sla_adjoint", "sla_csr_destroy"]:
         getattr(lib, f).restype = C.c_int
     _lib = lib

@@ -42,13 +42,17 @@ static sla_status fail(sla_status st, const char* fmt, ...) {
     return st;
 }
 
+// A failed runtime call is reported here and cleared from the runtime's
+// last-error slot, so the next launch check does not report it again.
 #define CU(call)                                                                              \
     do {                                                                                      \
         cudaError_t e_ = (call);                                                              \
-        if (e_ != cudaSuccess)                                                                \
+        if (e_ != cudaSuccess) {                                                              \
+            (void)cudaGetLastError();                                                         \
             return fail(e_ == cudaErrorMemoryAllocation ? SLA_ERR_NOMEM : SLA_ERR_CUDA,      \
                         "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__,     \
                         __LINE__);                                                            \
+        }                                                                                     \
     } while (0)
 
 #define TRY(expr)                            \
@@ -88,14 +92,24 @@ struct DevBuf {
     T* as() const { return static_cast<T*>(p); }
 };
 
+// Captured iterations for one (preconditioner, eps, k).  With product
+// timing there is one instance per launch slot, each recording its own
+// pair of events around its first product kernel (two launches are in
+// flight, so one pair of events could be overwritten before it is read).
 struct GraphCache {
-    cudaGraphExec_t exec = nullptr;
+    cudaGraphExec_t exec[2] = {nullptr, nullptr};
+    cudaEvent_t t0[2] = {nullptr, nullptr}, t1[2] = {nullptr, nullptr};
     int k = 0;
     double eps = 0.0;
     int nodes = 0;
     void reset() {
-        if (exec) cudaGraphExecDestroy(exec);
-        exec = nullptr;
+        for (int i = 0; i < 2; ++i) {
+            if (exec[i]) cudaGraphExecDestroy(exec[i]);
+            if (t0[i]) cudaEventDestroy(t0[i]);
+            if (t1[i]) cudaEventDestroy(t1[i]);
+            exec[i] = nullptr;
+            t0[i] = t1[i] = nullptr;
+        }
         k = 0;
         nodes = 0;
     }
@@ -131,6 +145,9 @@ struct sla_csr {
     Layout LA;         // product layout of A
     bool vals_aligned = false;  // values 16-byte aligned for every system (chunk pipeline)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
+    bool time_product = false;  // SLA_TIME_PRODUCT: events around one product kernel per graph launch
+    double prod_ms = 0.0;       // summed product-kernel durations (sla_product_time)
+    long long prod_n = 0;
     bool persistent = false;    // SLA_PERSISTENT: persistent iteration kernel for CG / Jacobi-PCG
     bool coop = false;          // device supports cooperative launches
     DevBuf gsync;               // GridSync per system (fused iteration kernel)
@@ -552,7 +569,8 @@ static sla_status ensure_pstride(sla_csr* h) {
 
 // ===================================================================== kernels per iteration
 template <typename T, bool PAIRS>
-static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
+static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes, cudaEvent_t ev0,
+                                    cudaEvent_t ev1) {
     const Sys S = sys_of(h);
     const Mat A = mat_A(h);
     const T* av = (const T*)h->vals;
@@ -565,10 +583,14 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     XW* x = h->x.as<XW>();
     const XW* dinv = h->dinv.as<XW>();
     const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
+    // external event-record nodes (a plain record inside a capture only
+    // orders streams within the graph)
+    if (ev0) CU(cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal));
     with_form(h->LA.form, [&](auto f) {
         k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LA.smem, s>>>(A, S, av, p, q, x, h->bw.as<T>());
     });
     TRY(launched());
+    if (ev1) CU(cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal));
     if (pc == SLA_PC_SPAI) {
         k_update<T, 2, PAIRS><<<gv, NT, 0, s>>>(S, r, q, dinv, h->z.as<W>());
         TRY(launched());
@@ -605,34 +627,52 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
 }
 
 template <typename T>
-static sla_status enqueue_iteration_any(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes) {
-    return pairs_ok(h) ? enqueue_iteration<T, true>(h, pc, eps, s, nodes)
-                       : enqueue_iteration<T, false>(h, pc, eps, s, nodes);
+static sla_status enqueue_iteration_any(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes,
+                                        cudaEvent_t ev0 = nullptr, cudaEvent_t ev1 = nullptr) {
+    return pairs_ok(h) ? enqueue_iteration<T, true>(h, pc, eps, s, nodes, ev0, ev1)
+                       : enqueue_iteration<T, false>(h, pc, eps, s, nodes, ev0, ev1);
 }
 
 template <typename T>
 static sla_status get_graph(sla_csr* h, int pc, double eps, int k, GraphCache** out) {
     GraphCache& gc = h->graph[pc];
-    if (gc.exec && gc.k == k && gc.eps == eps) { *out = &gc; return SLA_OK; }
+    if (gc.exec[0] && gc.k == k && gc.eps == eps) { *out = &gc; return SLA_OK; }
     gc.reset();
-    CU(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
+    const int inst = h->time_product ? 2 : 1;
     int nodes = 0;
-    sla_status st = SLA_OK;
-    for (int i = 0; i < k && st == SLA_OK; ++i) st = enqueue_iteration_any<T>(h, pc, eps, h->cap, &nodes);
-    cudaGraph_t graph = nullptr;
-    cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
-    // launches made during capture were counted; they only run when the graph does
-    g_launches.fetch_sub((unsigned long long)nodes, std::memory_order_relaxed);
-    if (st != SLA_OK) {
-        if (graph) cudaGraphDestroy(graph);
-        return st;
-    }
-    if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
-    e = cudaGraphInstantiate(&gc.exec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (e != cudaSuccess) {
-        gc.exec = nullptr;
-        return fail(SLA_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+    for (int slot = 0; slot < inst; ++slot) {
+        if (h->time_product) {
+            CU(cudaEventCreate(&gc.t0[slot]));
+            CU(cudaEventCreate(&gc.t1[slot]));
+        }
+        CU(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
+        nodes = 0;
+        sla_status st = SLA_OK;
+        // the timed product is the middle iteration's, clear of the graph
+        // launch's own start-up
+        for (int i = 0; i < k && st == SLA_OK; ++i)
+            st = enqueue_iteration_any<T>(h, pc, eps, h->cap, &nodes, i == k / 2 ? gc.t0[slot] : nullptr,
+                                          i == k / 2 ? gc.t1[slot] : nullptr);
+        cudaGraph_t graph = nullptr;
+        cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
+        // launches made during capture were counted; they only run when the graph does
+        g_launches.fetch_sub((unsigned long long)nodes, std::memory_order_relaxed);
+        if (st != SLA_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            gc.reset();
+            return st;
+        }
+        if (e != cudaSuccess) {
+            gc.reset();
+            return fail(SLA_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+        }
+        e = cudaGraphInstantiate(&gc.exec[slot], graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            gc.exec[slot] = nullptr;
+            gc.reset();
+            return fail(SLA_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+        }
     }
     gc.k = k;
     gc.eps = eps;
@@ -778,13 +818,15 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     int head = 0, inflight = 0;
     long long issued = 0;
     bool finished = false, timed_out = false;
+    const bool timing = !fused && h->time_product;
+    bool prev_done = false;   // the launch before the oldest in flight left every system frozen
     while (!finished) {
         if (issued < cap_launches && !timed_out) {
             const int slot = (head + inflight) & 1;
             if (fused) {
                 TRY(launch_fused_any<T>(h, pc, gxf, k, s));
             } else {
-                CU(cudaGraphLaunch(gc->exec, s));
+                CU(cudaGraphLaunch(gc->exec[timing ? slot : 0], s));
                 g_launches.fetch_add((unsigned long long)gc->nodes, std::memory_order_relaxed);
             }
             CU(cudaMemcpyAsync(&h->h_flag[slot], &h->ctl.as<Ctrl>()->all_done, sizeof(int),
@@ -809,6 +851,13 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
         } else {
             CU(cudaEventSynchronize(h->ev[slot]));
         }
+        if (timing && !prev_done && !h->h_flag[slot]) {   // live systems from start to end
+            float ms = 0.0f;
+            CU(cudaEventElapsedTime(&ms, gc->t0[slot], gc->t1[slot]));
+            h->prod_ms += ms;
+            h->prod_n += 1;
+        }
+        prev_done = h->h_flag[slot] != 0;
         head ^= 1;
         --inflight;
         if (h->h_flag[slot]) finished = true;
@@ -952,6 +1001,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     HTRY(dt == SLA_F64 ? allow_smem<double>() : allow_smem<float>());
     h->vals_aligned = vals_aligned(h, d_vals);
     h->pipeline = (flags & SLA_WARP_PIPELINE) != 0;
+    h->time_product = (flags & SLA_TIME_PRODUCT) != 0;
     h->persistent = (flags & SLA_PERSISTENT) != 0;
     {
         int coop = 0;
@@ -983,6 +1033,17 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
 #undef HTRY
 #undef HCU
     *out = h;
+    return SLA_OK;
+}
+
+sla_status sla_product_time(sla_handle h, double* total_ms, long long* samples, int reset) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (total_ms) *total_ms = h->prod_ms;
+    if (samples) *samples = h->prod_n;
+    if (reset) {
+        h->prod_ms = 0.0;
+        h->prod_n = 0;
+    }
     return SLA_OK;
 }
 

@@ -328,3 +328,22 @@ def test_unaligned_values_leave_the_pipeline(cuda_device):
     assert M.layout()[0] != 3
     xs, info = M.solve(torch.from_numpy(y_o).to(cuda_device), tol=1e-10, pc="jacobi")
     assert info[0].status == "ok" and rel(xs.cpu().numpy(), x) <= 1e-6
+
+
+def test_product_time_records_live_launches(cuda_device):
+    """With time_product the solve times one product kernel per graph
+    launch; the per-launch time is positive and far below the solve time."""
+    w = build("c2", N=96)
+    from gpu_util import to_device
+    from sparse_iterative_linear_csr_b300 import CSRMatrix
+    rp, ci, v = to_device(w.A, cuda_device)
+    M = CSRMatrix(rp, ci, v, time_product=True)
+    b = torch.from_numpy(w.b).to(cuda_device)
+    assert M.product_time() == (0.0, 0)
+    _, info = M.solve(b, tol=w.tol, pc="jacobi", poll_k=8)
+    ms, n = M.product_time(reset=False)
+    assert n >= info[0].iters // 8 - 2 and ms > 0.0
+    assert M.product_time(reset=True)[1] == n and M.product_time() == (0.0, 0)
+    plain = CSRMatrix(rp, ci, v)
+    plain.solve(b, tol=w.tol, pc="jacobi", poll_k=8)
+    assert plain.product_time() == (0.0, 0)
