@@ -156,8 +156,14 @@ sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot,
  * [batch][n].  x0 = 0 unless opts->use_x0.  info: host array of `batch`
  * entries, filled on return.  Returns SLA_OK when every system converged,
  * else the first non-OK per-system status (x still holds each system's last
- * iterate).  ||b|| = 0 gives x = 0 after 0 iterations.  fp32 handles keep
- * x in fp64 during the solve and round it to fp32 on return.
+ * iterate).  ||b|| = 0 gives x = 0 after 0 iterations.  fp32 handles run
+ * the recurrence at fp64-equivalent precision (working vectors as
+ * double-float pairs) and round x to fp32 on return.  The host issues
+ * opts->poll_k iterations per launch -- a CUDA graph of one kernel per CG
+ * step, or with SLA_PERSISTENT (CG and Jacobi only) one persistent
+ * cooperative kernel -- keeps two launches in flight and reads one device
+ * flag per launch; a device wait that gives up (never expected) returns
+ * SLA_ERR_CUDA with its location in sla_last_error().
  */
 sla_status sla_pcg_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg_opts* opts,
                          sla_solve_info* info, void* stream);
@@ -175,7 +181,7 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
 
 /*
  * Allocation-free y = A x and d_dot[s] = x_s . y_s (the same fused kernel as
- * sla_spmv_dot), without a handle.  The paper has no counterpart: this entry
+ * sla_spmv_dot), without a handle.  The pages have no counterpart: this entry
  * point exists for callers that cannot let a library allocate device
  * memory -- programs that own all device memory through their own allocator
  * or memory budget, and latency-critical loops where cudaMalloc / cudaFree
