@@ -251,6 +251,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--warp-pipeline", action="store_true",
                     help="use the warp-pipeline product where it applies")
+    ap.add_argument("--producer-consumer", action="store_true",
+                    help="use the producer/consumer product where it applies")
     ap.add_argument("--persistent", action="store_true",
                     help="CG / Jacobi-PCG as the persistent iteration kernel (not a graph of kernels)")
     args = ap.parse_args()
@@ -285,7 +287,8 @@ def main():
     vals = torch.from_numpy(A.vals).to(dev)
     b = torch.from_numpy(w.b).to(dev)
     g = torch.from_numpy(w.g).to(dev)
-    M = sla.CSRMatrix(rp, ci, vals, pipeline=args.warp_pipeline, fused=args.persistent, time_product=True)
+    M = sla.CSRMatrix(rp, ci, vals, pipeline=args.warp_pipeline, fused=args.persistent, time_product=True,
+                      producer_consumer=args.producer_consumer)
     kw = dict(tol=w.tol, max_iter=MAX_ITER, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3,
               poll_k=args.poll_k)
 

@@ -73,6 +73,7 @@ typedef enum {
 #define SLA_PERSISTENT 4u    /* CG / Jacobi-PCG: one persistent iteration kernel per poll interval
                                 instead of a CUDA graph of one kernel per step (see sla_pcg_solve) */
 #define SLA_TIME_PRODUCT 8u  /* time one CG product kernel per graph launch (sla_product_time) */
+#define SLA_PRODUCER_CONSUMER 16u /* use the producer/consumer product where it applies (see sla_csr_layout) */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -119,6 +120,10 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         3 the chunk pipeline (bulk copies of NT-row chunks; needs 16-byte
  *         aligned row_ptr, col_idx and values of every system, and groups
  *         that fit shared memory; only with SLA_WARP_PIPELINE);
+ *         4 producer/consumer warps (2 warps bulk-copy and gather tiles of
+ *         192 rows into a ring of shared-memory stages, 6 warps add; same
+ *         alignment conditions; only with SLA_PRODUCER_CONSUMER, which
+ *         takes precedence over SLA_WARP_PIPELINE);
  *  *ctas: CTAs per system of the product kernels.
  * Either pointer may be NULL.  SLA_ERR_INVALID for a null handle.
  */

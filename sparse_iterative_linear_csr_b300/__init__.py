@@ -78,11 +78,12 @@ class CSRMatrix:
     fused=True runs CG / Jacobi-PCG as the persistent iteration kernel
     instead of a CUDA graph of one kernel per step; time_product=True
     records the live duration of one product kernel per graph launch
-    (product_time)."""
+    (product_time); producer_consumer=True uses the producer/consumer
+    product where it applies."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
                  validate: bool = True, pipeline: bool = False, fused: bool = False,
-                 time_product: bool = False, stream=None):
+                 time_product: bool = False, producer_consumer: bool = False, stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -106,7 +107,8 @@ class CSRMatrix:
                                   _ptr(values), (_lib.SLA_VALIDATE if validate else 0) |
                                   (_lib.SLA_WARP_PIPELINE if pipeline else 0) |
                                   (_lib.SLA_PERSISTENT if fused else 0) |
-                                  (_lib.SLA_TIME_PRODUCT if time_product else 0), _stream(stream),
+                                  (_lib.SLA_TIME_PRODUCT if time_product else 0) |
+                                  (_lib.SLA_PRODUCER_CONSUMER if producer_consumer else 0), _stream(stream),
                                   C.byref(self._h)))
 
     # -------------------------------------------------------------- lifetime

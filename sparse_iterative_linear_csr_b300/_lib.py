@@ -20,6 +20,7 @@ SLA_VALIDATE = 1
 SLA_WARP_PIPELINE = 2
 SLA_PERSISTENT = 4
 SLA_TIME_PRODUCT = 8
+SLA_PRODUCER_CONSUMER = 16
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",

@@ -14,14 +14,17 @@ constexpr int SPMV_MIN_CTAS = 4; // resident CTAs per SM the staged-SpMV kernels
 // Resident CTAs per SM the CG product kernel (which also carries the residual
 // check) is compiled for: fp64 measured faster unspilled at 3 than spilled
 // at 4; fp32 fits 4 unspilled.
-template <typename T> struct IterMinCtas { static constexpr int value = 3; };
+#ifndef SLA_ITER_CTAS_F64
+#define SLA_ITER_CTAS_F64 3
+#endif
+template <typename T> struct IterMinCtas { static constexpr int value = SLA_ITER_CTAS_F64; };
 template <> struct IterMinCtas<float> { static constexpr int value = 4; };
 constexpr int MAXR = NT;         // rows per row block (one row per thread)
 
 // Outcome codes mirrored from sla_status (kept numerically equal).
 enum : int { ST_OK = 0, ST_NOT_CONVERGED = 4, ST_BREAKDOWN = 5 };
 // Device error bit in Ctrl::err.
-enum : int { ERR_WAIT = 1 << 8, ERR_GRID = 1 << 9 };
+enum : int { ERR_WAIT = 1 << 8, ERR_GRID = 1 << 9, ERR_STAGE = 1 << 10 };
 // Record where the first wait gave up (diagnostics for the host's message).
 __device__ __forceinline__ void note_wait(int* diag, int who, int a, int b, int c) {
     if (atomicCAS(diag, 0, who) == 0) {
@@ -134,11 +137,27 @@ __device__ __forceinline__ void fence_barrier_init() {
 }
 // Orders this thread's earlier shared-memory accesses before later
 // asynchronous-proxy accesses (a stage is refilled after it was read).
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+#ifndef SLA_PROXY_FENCE
+#define SLA_PROXY_FENCE 1
+#endif
+__device__ __forceinline__ void fence_proxy_async() {
+#if SLA_PROXY_FENCE
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+#endif
+}
 
 __device__ __forceinline__ void mbar_arrive_expect(unsigned long long* bar, unsigned bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+// One arrival (count 1).
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// An arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes these arrivals).
+__device__ __forceinline__ void cp_async_arrive(unsigned long long* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned parity) {
     unsigned ok;

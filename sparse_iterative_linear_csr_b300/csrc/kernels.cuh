@@ -283,7 +283,10 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
 // which the asynchronous copies serve less well.  Row bounds are loaded one
 // group ahead.
 // Shared memory per warp: async*cap*(sizeof(VT) + 4) + cap*sizeof(T).
-constexpr int GATHER_U = 4;   // register gathers per lane in flight
+#ifndef SLA_GATHER_U
+#define SLA_GATHER_U 8
+#endif
+constexpr int GATHER_U = SLA_GATHER_U;   // register gathers per lane in flight
 
 template <typename VT, typename T>
 __host__ __device__ constexpr size_t async_smem_per_warp(int cap, int bufs) {
@@ -449,8 +452,12 @@ __device__ __forceinline__ void spmv_pipe(const Mat& A, const VT* __restrict__ a
         const int st = j % S;
         const long long k0 = (long long)e0 & ~3LL;
         const long long k1 = ((long long)e1 + 3) & ~3LL;
-        const long long kb = k1 < nnz4 ? k1 : (nnz4 > k0 ? nnz4 : k0);   // end of the bulk part
-        const long long ke = k1 < A.nnz ? k1 : A.nnz;                      // end of the staged range
+        long long kb = k1 < nnz4 ? k1 : (nnz4 > k0 ? nnz4 : k0);   // end of the bulk part
+        long long ke = k1 < A.nnz ? k1 : A.nnz;                      // end of the staged range
+        if (ke - k0 > cap) {   // never expected: the host sized the stages for every group
+            atomicOr(A.err, ERR_STAGE);
+            kb = ke = k0;
+        }
         hd->k0[st] = (int)k0;
         hd->cnt[st] = (int)(ke - k0);
         VT* dv = sv + (size_t)st * cap;
@@ -548,7 +555,9 @@ __device__ __forceinline__ void spmv_pipe(const Mat& A, const VT* __restrict__ a
             const int k0 = hd->k0[st];
             const VT* cv = sv + (size_t)st * cap;
             const XT* cx = sx + (size_t)gb * cap;
-            for (int e = rlo - k0; e < rhi - k0; ++e) mac(s, cv[e], cx[e]);
+            const int lo = rlo - k0, hi = rhi - k0;
+            if (lo >= 0 && hi <= hd->cnt[st])   // inside the staged range (always, unless ERR_STAGE)
+                for (int e = lo; e < hi; ++e) mac(s, cv[e], cx[e]);
         }
         __syncwarp();   // stage st and gather buffer gb are free
         if (lane == 0 && i + S < m) {
@@ -566,16 +575,195 @@ __device__ __forceinline__ void spmv_pipe(const Mat& A, const VT* __restrict__ a
     __syncwarp();
 }
 
-// Product with a plain vector gather in one of four compiled forms (the
+// Producer/consumer product (FORM 4).  Warps specialise: WS_PROD producer
+// warps move data, the other WS_CONS warps only add.  Rows are taken in
+// tiles of WS_ROWS consecutive rows (a system's tile c belongs to CTA
+// c mod gridDim.x), staged in a ring of A.stages shared-memory stages.  For
+// each tile one producer lane bulk-copies the values and column indices
+// (cp.async.bulk, L2 evict-first, completion counted in bytes on the
+// stage's `full_vc` barrier) up to `stages` tiles ahead; once the columns
+// have landed all producer threads gather the vector entries they address
+// with cp.async (L2 evict-last) and have the stage's `full_x` barrier
+// count their completion (cp.async.mbarrier.arrive).  Each consumer lane
+// owns one row of the tile: it waits for both barriers, sums its row from
+// shared memory (one fp64 FMA per entry for fp64 systems), runs the
+// epilogue and, warp by warp, releases the stage on `empty`.  The fp64 pipe
+// is thus fed by warps that never wait on global memory, while the memory
+// system is kept busy by warps that never wait on the fp64 pipe.  Copies
+// are rounded out to 16-byte units as in spmv_pipe; the host uses this form
+// only where every tile fits a stage and the arrays are 16-byte aligned.
+// Every wait gives up after WAIT_LIMIT_NS, recording ERR_WAIT.
+#ifndef SLA_WS_PROD
+#define SLA_WS_PROD 2
+#endif
+constexpr int WS_PROD = SLA_WS_PROD;
+constexpr int WS_CONS = NWARP - WS_PROD;
+constexpr int WS_ROWS = 32 * WS_CONS;
+struct WsHdr {
+    unsigned long long full_vc[MAX_STAGES];
+    unsigned long long full_x[MAX_STAGES];
+    unsigned long long empty[MAX_STAGES];
+    int k0[MAX_STAGES];    // first staged entry (multiple of 4)
+    int cnt[MAX_STAGES];   // staged entries
+};
+
+template <typename VT, typename XT>
+__host__ __device__ constexpr size_t ws_smem_bytes(int tcap, int stages) {
+    return sizeof(WsHdr) + (size_t)stages * tcap * (sizeof(VT) + sizeof(int) + sizeof(XT));
+}
+
+template <typename T, typename VT, typename XT, class Pre, class Epi>
+__device__ __forceinline__ void spmv_ws(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v, Pre pre,
+                                        Epi epi, double* dsm) {
+    using acc_t = typename Prec<T>::acc;
+    using car_t = decltype(pre(0));
+    const int S = A.stages, cap = A.ccap;
+    char* base = reinterpret_cast<char*>(dsm);
+    WsHdr* hd = reinterpret_cast<WsHdr*>(base);
+    VT* sv = reinterpret_cast<VT*>(base + sizeof(WsHdr));
+    int* sc = reinterpret_cast<int*>(sv + (size_t)S * cap);
+    XT* sx = reinterpret_cast<XT*>(sc + (size_t)S * cap);
+    const int ntiles = (A.n + WS_ROWS - 1) / WS_ROWS;
+    const int c0 = blockIdx.x, cstep = gridDim.x;
+    const int m = c0 < ntiles ? (ntiles - 1 - c0) / cstep + 1 : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();   // shared memory may still be in use by an earlier pass
+    if (m == 0) return;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < S; ++st) {
+            mbar_init(&hd->full_vc[st], 1);
+            mbar_init(&hd->full_x[st], 32 * WS_PROD);
+            mbar_init(&hd->empty[st], WS_CONS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    bool ok = true;
+    if (warp >= WS_CONS) {
+        // ------------------------------------------------ producers
+        const int pt = threadIdx.x - 32 * WS_CONS;
+        const long long nnz4 = A.nnz & ~3LL;
+        const unsigned long long keep = l2_evict_last();
+        const unsigned long long strm = l2_evict_first();
+        // entry range of the CTA's j-th tile (thread pt == 0)
+        auto bounds = [&](int j, int& e0, int& e1) {
+            const int r0 = (c0 + j * cstep) * WS_ROWS;
+            const int r1 = r0 + WS_ROWS < A.n ? r0 + WS_ROWS : A.n;
+            e0 = ld_nc(A.rp + r0);
+            e1 = ld_nc(A.rp + r1);
+        };
+        int ne0 = 0, ne1 = 0;
+        if (pt == 0) bounds(0, ne0, ne1);
+        int tb = 0, bst = 0, bpar = 1;   // next tile to copy, its stage, the parity of its stage's release
+        int gst = 0, gpar = 0;           // stage and parity of the tile being gathered
+        for (int t = 0; t < m; ++t) {
+            while (tb < m && tb < t + S) {
+                if (!mbar_wait(&hd->empty[bst], (unsigned)bpar)) { ok = false; break; }
+                if (pt == 0) {
+                    const long long k0 = (long long)ne0 & ~3LL;
+                    const long long k1 = ((long long)ne1 + 3) & ~3LL;
+                    long long kb = k1 < nnz4 ? k1 : (nnz4 > k0 ? nnz4 : k0);
+                    long long ke = k1 < A.nnz ? k1 : A.nnz;
+                    if (ke - k0 > cap) {   // never expected: the host sized the stages for every tile
+                        atomicOr(A.err, ERR_STAGE);
+                        kb = ke = k0;
+                    }
+                    hd->k0[bst] = (int)k0;
+                    hd->cnt[bst] = (int)(ke - k0);
+                    VT* dv = sv + (size_t)bst * cap;
+                    int* dc = sc + (size_t)bst * cap;
+                    for (long long k = kb; k < ke; ++k) {   // ragged end of the pattern
+                        dv[k - k0] = av[k];
+                        dc[k - k0] = A.ci[k];
+                    }
+                    const unsigned nb = (unsigned)(kb - k0);
+                    fence_proxy_async();
+                    mbar_arrive_expect(&hd->full_vc[bst], nb * (unsigned)(sizeof(VT) + sizeof(int)));
+                    if (nb) {
+                        bulk_copy(dv, av + k0, nb * (unsigned)sizeof(VT), &hd->full_vc[bst], strm);
+                        bulk_copy(dc, A.ci + k0, nb * (unsigned)sizeof(int), &hd->full_vc[bst], strm);
+                    }
+                    if (tb + 1 < m) bounds(tb + 1, ne0, ne1);
+                }
+                ++tb;
+                if (++bst == S) { bst = 0; bpar ^= 1; }
+            }
+            if (!ok) break;
+            if (!mbar_wait(&hd->full_vc[gst], (unsigned)gpar)) { ok = false; break; }
+            const int* cc = sc + (size_t)gst * cap;
+            XT* dx = sx + (size_t)gst * cap;
+            const int cnt = hd->cnt[gst];
+#pragma unroll 4
+            for (int e = pt; e < cnt; e += 32 * WS_PROD) cp_async<sizeof(XT)>(dx + e, v + cc[e], keep);
+            cp_async_arrive(&hd->full_x[gst]);
+            if (++gst == S) { gst = 0; gpar ^= 1; }
+        }
+    } else {
+        // ------------------------------------------------ consumers
+        const int rofs = warp * 32 + lane;
+        int row = c0 * WS_ROWS + rofs, rlo = 0, rhi = 0;
+        car_t car{};
+        if (row < A.n) {
+            rlo = ld_nc(A.rp + row);
+            rhi = ld_nc(A.rp + row + 1);
+            car = pre(row);
+        }
+        int st = 0, par = 0;
+        for (int t = 0; t < m; ++t) {
+            const int nrow = row + cstep * WS_ROWS;
+            int nlo = 0, nhi = 0;
+            car_t ncar{};
+            if (t + 1 < m && nrow < A.n) {
+                nlo = ld_nc(A.rp + nrow);
+                nhi = ld_nc(A.rp + nrow + 1);
+                ncar = pre(nrow);
+            }
+            const bool w = mbar_wait(&hd->full_vc[st], (unsigned)par) && mbar_wait(&hd->full_x[st], (unsigned)par);
+            if (__any_sync(0xffffffffu, !w)) { ok = false; break; }
+            if (row < A.n) {
+                const int k0 = hd->k0[st];
+                const VT* cv = sv + (size_t)st * cap;
+                const XT* cx = sx + (size_t)st * cap;
+                acc_t s = Prec<T>::zero();
+                const int lo = rlo - k0, hi = rhi - k0;
+                if (lo >= 0 && hi <= hd->cnt[st]) {   // inside the staged range (always, unless ERR_STAGE)
+#pragma unroll 4
+                    for (int e = lo; e < hi; ++e) mac(s, cv[e], cx[e]);
+                }
+                epi(row, s, car);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&hd->empty[st]);
+            if (++st == S) { st = 0; par ^= 1; }
+            row = nrow; rlo = nlo; rhi = nhi; car = ncar;
+        }
+    }
+    if (!ok) {
+        atomicOr(A.err, ERR_WAIT);
+        note_wait(A.err + 2, -1 - (int)blockIdx.x, m, warp, lane);
+    }
+    cp_wait<0>();
+    const int all_ok = __syncthreads_and(ok ? 1 : 0);
+    if (threadIdx.x == 0 && all_ok)
+        for (int st = 0; st < S; ++st) {
+            mbar_inval(&hd->full_vc[st]);
+            mbar_inval(&hd->full_x[st]);
+            mbar_inval(&hd->empty[st]);
+        }
+    __syncthreads();
+}
+
+// Product with a plain vector gather in one of five compiled forms (the
 // host picks one per matrix, so each kernel instantiation carries a single
 // path): FORM 0 register staging (spmv_rows); FORM 1 cp.async value/column
 // staging with register gathers; FORM 2 cp.async staging and gathers; FORM 3
-// the warp pipeline (spmv_pipe).
+// the warp pipeline (spmv_pipe); FORM 4 producer/consumer warps (spmv_ws).
 template <typename T, int FORM, typename VT, typename XT, bool COH = false, class Pre, class Epi>
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
     if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
     else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
+    else if constexpr (FORM == 4) spmv_ws<T, VT, XT>(A, av, v, pre, epi, wsm);
     else spmv_rows_async<T, VT, XT, FORM == 2, COH>(A, av, v, pre, epi, wsm);
 }
 

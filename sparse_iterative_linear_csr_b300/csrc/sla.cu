@@ -124,7 +124,8 @@ struct Layout {
     int lanes = 1;
     int gx = 1;
     int gasync = 0;   // gathers by cp.async (scattered columns)
-    int ccap = 0;     // chunk pipeline: entries per stage (0: a chunk would not fit)
+    int ccap = 0;     // warp pipeline: entries per stage (0: a group would not fit)
+    int tcap = 0;     // producer/consumer form: entries per tile stage (0: unusable)
     int stages = 0;   // chunk pipeline: ring stages
     int form = 0;     // compiled form of the product kernels (spmv_vec)
     size_t smem = 0;  // their dynamic shared memory
@@ -145,6 +146,7 @@ struct sla_csr {
     Layout LA;         // product layout of A
     bool vals_aligned = false;  // values 16-byte aligned for every system (chunk pipeline)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
+    bool ws = false;            // SLA_PRODUCER_CONSUMER: producer/consumer product where it applies
     bool time_product = false;  // SLA_TIME_PRODUCT: events around one product kernel per graph launch
     double prod_ms = 0.0;       // summed product-kernel durations (sla_product_time)
     long long prod_n = 0;
@@ -255,10 +257,12 @@ static sla_status allow_smem() {
     TRY((allow_smem_form<T, 1>(b)));
     TRY((allow_smem_form<T, 2>(b)));
     TRY((allow_smem_form<T, 3>(SMEM_CTA_MAX)));
+    TRY((allow_smem_form<T, 4>(SMEM_CTA_MAX)));
     TRY((allow_smem_fused<T, 0>()));
     TRY((allow_smem_fused<T, 1>()));
     TRY((allow_smem_fused<T, 2>()));
     TRY((allow_smem_fused<T, 3>()));
+    TRY((allow_smem_fused<T, 4>()));
     CU(cudaFuncSetAttribute(k_init_x0<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
     CU(cudaFuncSetAttribute(k_final<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
     CU(cudaFuncSetAttribute(k_grad_A<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
@@ -293,7 +297,8 @@ static void with_form(int form, F&& f) {
         case 0: f(std::integral_constant<int, 0>{}); break;
         case 1: f(std::integral_constant<int, 1>{}); break;
         case 2: f(std::integral_constant<int, 2>{}); break;
-        default: f(std::integral_constant<int, 3>{}); break;
+        case 3: f(std::integral_constant<int, 3>{}); break;
+        default: f(std::integral_constant<int, 4>{}); break;
     }
 }
 
@@ -301,10 +306,33 @@ static void with_form(int form, F&& f) {
 // The warp pipeline needs a group capacity (pattern) and 16-byte aligned
 // values (`aligned`); `vb` is the value size in bytes.  Every kernel that
 // takes the layout's Mat is launched with L->smem.
+// Producer/consumer form (FORM 4): shared memory of a CTA for tile capacity
+// `tcap`, S stages, `vb`-byte values (gathered entries sized at 8 bytes).
+static size_t ws_bytes(int tcap, int S, size_t vb) {
+    return sizeof(WsHdr) + (size_t)S * tcap * (vb + sizeof(int) + sizeof(double));
+}
+// Most stages (4..2) with two resident CTAs per SM, else three or more stages
+// with one; 0 when none fits.
+static int ws_stages(int tcap, size_t vb) {
+    for (int ctas = 2; ctas >= 1; --ctas)
+        for (int S = MAX_STAGES; S >= (ctas == 2 ? 2 : 3); --S) {
+            const size_t b = ws_bytes(tcap, S, vb);
+            if (b <= (size_t)SMEM_CTA_MAX && (b + SMEM_CTA_RESERVE) * ctas <= SMEM_SM) return S;
+        }
+    return 0;
+}
+
 template <typename T>
 static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb) {
-    L->stages = L->ccap > 0 && aligned && h->pipeline ? pipe_stages(L->ccap, vb) : 0;
-    if (L->stages > 0) {
+    const int wss = L->tcap > 0 && aligned && h->ws ? ws_stages(L->tcap, vb) : 0;
+    L->stages = wss == 0 && L->ccap > 0 && aligned && h->pipeline ? pipe_stages(L->ccap, vb) : 0;
+    if (wss > 0) {
+        L->form = 4;
+        L->stages = wss;
+        const size_t rows = (size_t)NWARP * L->cap * 2 * sizeof(double);   // warp staging of the check pass
+        const size_t b = ws_bytes(L->tcap, wss, vb);
+        L->smem = b > rows ? b : rows;
+    } else if (L->stages > 0) {
         L->form = 3;
         L->smem = (size_t)NWARP * pipe_bytes(L->ccap, L->stages, vb);
     } else {
@@ -315,7 +343,9 @@ static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb)
     sla_status st = SLA_OK;
     with_form(L->form, [&](auto f) { st = occupancy(k_spmv_iter<T, decltype(f)::value>, L->smem, &per); });
     TRY(st);
-    L->gx = grid_x(h, group_ctas(h->n, L->form == 3 ? 1 : L->lanes), per);
+    const long long units = L->form == 4 ? ((long long)h->n + WS_ROWS - 1) / WS_ROWS
+                                         : group_ctas(h->n, L->form == 3 ? 1 : L->lanes);
+    L->gx = grid_x(h, units, per);
     return SLA_OK;
 }
 
@@ -361,7 +391,7 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     m.lshift = m.lanes == 4 ? 2 : (m.lanes == 2 ? 1 : 0);
     if (L.form == 3) m.cap = L.ccap;   // every group stages in the register-staged passes too
     m.nnz = nnz;
-    m.ccap = L.ccap;
+    m.ccap = L.form == 4 ? L.tcap : L.ccap;   // entries per stage of the bulk-copy forms
     m.stages = L.stages;
     m.err = err;
     return m;
@@ -457,6 +487,15 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
         int cc = 0;
         TRY(read_int(m.as<int>(), &cc, s));
         L->ccap = cc < 4 ? 4 : cc;
+        // producer/consumer form: largest tile of WS_ROWS rows, as staged
+        CU(cudaMemsetAsync(m.p, 0, sizeof(int), s));
+        const long long nt = ((long long)h->n + WS_ROWS - 1) / WS_ROWS;
+        const int gt = (nt + 255) / 256 < 2048 ? (int)((nt + 255) / 256) : 2048;
+        k_chunk_max<<<gt, 256, 0, s>>>(rp, h->n, WS_ROWS, m.as<int>());
+        TRY(launched());
+        int tc = 0;
+        TRY(read_int(m.as<int>(), &tc, s));
+        L->tcap = tc < 4 ? 4 : tc;
     }
     return set_form_any(h, L, aligned, vb);
 }
@@ -872,6 +911,7 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     Ctrl dc;
     CU(cudaMemcpyAsync(&dc, h->ctl.p, sizeof(Ctrl), cudaMemcpyDeviceToHost, s));
     CU(cudaStreamSynchronize(s));
+    if (dc.err & ERR_STAGE) return fail(SLA_ERR_CUDA, "a staged range exceeded its stage; results invalid");
     if (dc.err & (ERR_WAIT | ERR_GRID))
         return fail(SLA_ERR_CUDA, "a device wait gave up (%s; at %d: %d %d %d); results invalid",
                     (dc.err & ERR_GRID) ? "grid barrier" : "bulk copy", dc.diag[0], dc.diag[1], dc.diag[2],
@@ -1001,6 +1041,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     HTRY(dt == SLA_F64 ? allow_smem<double>() : allow_smem<float>());
     h->vals_aligned = vals_aligned(h, d_vals);
     h->pipeline = (flags & SLA_WARP_PIPELINE) != 0;
+    h->ws = (flags & SLA_PRODUCER_CONSUMER) != 0;
     h->time_product = (flags & SLA_TIME_PRODUCT) != 0;
     h->persistent = (flags & SLA_PERSISTENT) != 0;
     {

@@ -13,10 +13,10 @@ def to_device(A: CSR, device="cuda:0"):
     return rp, ci, v
 
 
-def make(A: CSR, device="cuda:0", validate=True, pipeline=False, fused=False):
+def make(A: CSR, device="cuda:0", validate=True, **opts):
     from sparse_iterative_linear_csr_b300 import CSRMatrix
     rp, ci, v = to_device(A, device)
-    return CSRMatrix(rp, ci, v, validate=validate, pipeline=pipeline, fused=fused)
+    return CSRMatrix(rp, ci, v, validate=validate, **opts)
 
 
 def rel(a, b):

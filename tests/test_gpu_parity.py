@@ -2,11 +2,12 @@
 on the same seeded inputs, element by element, at sizes the oracle finishes
 in seconds (several row blocks and a ragged tail), plus edge cases.
 
-Every product test runs with the warp-staged forms (the default) and with
-the warp pipeline (pipeline=True, wherever a group fits its stages); the
-solve tests run with one kernel per step in a CUDA graph (the default) and
-with the persistent iteration kernel (fused=True), the latter with either
-product form.
+Every product test runs with the warp-staged forms (the default), the warp
+pipeline (pipeline=True) and the producer/consumer form
+(producer_consumer=True), the last two wherever the matrix fits their
+stages; the solve tests run with one kernel per step in a CUDA graph (the
+default) and with the persistent iteration kernel (fused=True), each with
+every product form.
 
 Tolerances: SpMV relative error <= 1e-12 (fp64) and <= 1e-5 (fp32);
 ||x - x_oracle|| / ||x_oracle|| <= 1e-6; iteration count within 2% of the
@@ -47,23 +48,26 @@ def _spmv_cases():
     yield "dense_row", CSR(n, rp, np.concatenate(cols).astype(np.int32), g.standard_normal(int(rp[-1])))
 
 
-PIPE = pytest.mark.parametrize("pipeline", [False, True], ids=["warp", "pipe"])
-MODES = pytest.mark.parametrize("pipeline,fused", [(False, False), (True, False), (False, True), (True, True)],
-                                ids=["steps", "pipe-steps", "fused", "pipe-fused"])
+FORMS = {"warp": {}, "pipe": {"pipeline": True}, "pc": {"producer_consumer": True}}
+PIPE = pytest.mark.parametrize("mode", list(FORMS))
+MODES = pytest.mark.parametrize("mode,fused", [(m, f) for f in (False, True) for m in FORMS],
+                                ids=[f"{m}-{'fused' if f else 'steps'}" for f in (False, True) for m in FORMS])
 
 
 @PIPE
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 @pytest.mark.parametrize("name,A", list(_spmv_cases()), ids=lambda v: v if isinstance(v, str) else "")
-def test_spmv_parity(cuda_device, name, A, dtype, pipeline):
+def test_spmv_parity(cuda_device, name, A, dtype, mode):
     A = CSR(A.n, A.row_ptr, A.col_idx, A.vals.astype(dtype))
     x = np.random.default_rng(11).standard_normal(A.n).astype(dtype)
-    M = make(A, pipeline=pipeline)
+    M = make(A, **FORMS[mode])
     form = M.layout()[0]
-    if not pipeline:
+    if mode == "warp" or name == "dense_row":   # the dense row fits neither staged form
         assert form in (0, 1, 2)
-    elif name not in ("dense_row", "knn_3000"):   # groups of 32 short rows fit the warp pipeline
+    elif mode == "pipe" and name != "knn_3000":   # groups of 32 short rows fit the warp pipeline
         assert form == 3, form
+    elif mode == "pc":
+        assert form == 4, form
     xd = torch.from_numpy(x).to(cuda_device)
     y = M.matvec(xd).cpu().numpy()
     y_o = oracle.spmv(A, x.astype(np.float64))
@@ -77,9 +81,9 @@ def test_spmv_parity(cuda_device, name, A, dtype, pipeline):
 
 
 @PIPE
-def test_spmv_batched(cuda_device, pipeline):
+def test_spmv_batched(cuda_device, mode):
     w = build("c3", N=40, batch=3)
-    M = make(w.A, pipeline=pipeline)
+    M = make(w.A, **FORMS[mode])
     x = torch.from_numpy(w.b).to(cuda_device)
     y = M.matvec(x).cpu().numpy()
     for s in range(3):
@@ -104,9 +108,9 @@ SOLVE_CASES = [
 
 @MODES
 @pytest.mark.parametrize("cfg,kw,pc", SOLVE_CASES, ids=[f"{c}-{p}-{k}" for c, k, p in SOLVE_CASES])
-def test_pcg_parity(cuda_device, cfg, kw, pc, pipeline, fused):
+def test_pcg_parity(cuda_device, cfg, kw, pc, mode, fused):
     w = build(cfg, **kw)
-    M = make(w.A, pipeline=pipeline, fused=fused)
+    M = make(w.A, fused=fused, **FORMS[mode])
     b = torch.from_numpy(w.b).to(cuda_device)
     x, info = M.solve(b, tol=w.tol, max_iter=20000, pc=pc, eps=1e-3, poll_k=16)
     x = x.cpu().numpy()
@@ -129,9 +133,9 @@ ADJ_CASES = [("c4", {"N": 24}, "none"), ("c2", {"N": 64}, "jacobi"), ("c5", {"np
 
 @MODES
 @pytest.mark.parametrize("cfg,kw,pc", ADJ_CASES, ids=[f"{c}-{p}" for c, k, p in ADJ_CASES])
-def test_adjoint_parity(cuda_device, cfg, kw, pc, pipeline, fused):
+def test_adjoint_parity(cuda_device, cfg, kw, pc, mode, fused):
     w = build(cfg, **kw)
-    M = make(w.A, pipeline=pipeline, fused=fused)
+    M = make(w.A, fused=fused, **FORMS[mode])
     b = torch.from_numpy(w.b).to(cuda_device)
     g = torch.from_numpy(w.g).to(cuda_device)
     x, _ = M.solve(b, tol=w.tol, max_iter=20000, pc=pc)
@@ -303,10 +307,11 @@ def test_launch_count_advances(cuda_device, fused):
         assert launch_count() >= c0 + 3 * it
 
 
-def test_unaligned_values_leave_the_pipeline(cuda_device):
+@pytest.mark.parametrize("form,opt", [(3, "pipeline"), (4, "producer_consumer")])
+def test_unaligned_values_leave_the_pipeline(cuda_device, form, opt):
     """Values at an 8-byte offset cannot be bulk-copied: the handle falls
-    back to a warp-staged form, and returns to the pipeline once aligned
-    values are swapped in; products agree with the oracle throughout."""
+    back to a warp-staged form, and returns to the bulk-copy form once
+    aligned values are swapped in; products agree with the oracle."""
     A = poisson_grid((40, 40))
     from gpu_util import to_device
     from sparse_iterative_linear_csr_b300 import CSRMatrix
@@ -318,14 +323,14 @@ def test_unaligned_values_leave_the_pipeline(cuda_device):
     x = np.random.default_rng(5).standard_normal(A.n)
     xd = torch.from_numpy(x).to(cuda_device)
     y_o = oracle.spmv(A, x)
-    M = CSRMatrix(rp, ci, off, pipeline=True)
-    assert M.layout()[0] != 3
+    M = CSRMatrix(rp, ci, off, **{opt: True})
+    assert M.layout()[0] in (0, 1, 2)
     assert rel(M.matvec(xd).cpu().numpy(), y_o) <= 1e-13
     M.update_values(v)
-    assert M.layout()[0] == 3
+    assert M.layout()[0] == form
     assert rel(M.matvec(xd).cpu().numpy(), y_o) <= 1e-13
     M.update_values(off)
-    assert M.layout()[0] != 3
+    assert M.layout()[0] in (0, 1, 2)
     xs, info = M.solve(torch.from_numpy(y_o).to(cuda_device), tol=1e-10, pc="jacobi")
     assert info[0].status == "ok" and rel(xs.cpu().numpy(), x) <= 1e-6
 
