@@ -74,6 +74,8 @@ typedef enum {
                                 instead of a CUDA graph of one kernel per step (see sla_pcg_solve) */
 #define SLA_TIME_PRODUCT 8u  /* time one CG product kernel per graph launch (sla_product_time) */
 #define SLA_PRODUCER_CONSUMER 16u /* use the producer/consumer product where it applies (see sla_csr_layout) */
+#define SLA_REORDER 32u      /* always iterate on the reordered matrix (see sla_pcg_solve) */
+#define SLA_NO_REORDER 64u   /* never reorder */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -114,7 +116,8 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
                           unsigned flags, void* stream, sla_handle* out);
 
 /*
- * Product layout chosen for the handle's matrix A (diagnostics):
+ * Product layout of the matrix the solves iterate on -- A, or P A P^T when
+ * the handle reorders (see sla_pcg_solve) -- for diagnostics:
  *  *form: 0 register-staged warp groups, 1 warp groups with asynchronous
  *         value/column staging, 2 the same with asynchronous gathers,
  *         3 the chunk pipeline (bulk copies of NT-row chunks; needs 16-byte
@@ -124,10 +127,11 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         192 rows into a ring of shared-memory stages, 6 warps add; same
  *         alignment conditions; only with SLA_PRODUCER_CONSUMER, which
  *         takes precedence over SLA_WARP_PIPELINE);
- *  *ctas: CTAs per system of the product kernels.
- * Either pointer may be NULL.  SLA_ERR_INVALID for a null handle.
+ *  *ctas: CTAs per system of the product kernels;
+ *  *reordered: 1 when the solves iterate on P A P^T.
+ * Any pointer may be NULL.  SLA_ERR_INVALID for a null handle.
  */
-sla_status sla_csr_layout(sla_handle h, int* form, int* ctas);
+sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered);
 
 /*
  * Live duration of the CG product kernel (q = A p fused with p.q and the
@@ -161,7 +165,15 @@ sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot,
  * [batch][n].  x0 = 0 unless opts->use_x0.  info: host array of `batch`
  * entries, filled on return.  Returns SLA_OK when every system converged,
  * else the first non-OK per-system status (x still holds each system's last
- * iterate).  ||b|| = 0 gives x = 0 after 0 iterations.  fp32 handles run
+ * iterate).  ||b|| = 0 gives x = 0 after 0 iterations.  Reordering: when
+ * the pattern is scattered (more than 10% of its entries lie farther than
+ * 65536 columns from their row) or SLA_REORDER is given, and SLA_NO_REORDER
+ * is not, the handle iterates on P A P^T with P a reverse Cuthill-McKee
+ * permutation of the pattern (computed on the host at creation), P b and
+ * P x0, and returns P^T x: the same method (the SPAI factor is still built
+ * on the caller's ordering and then permuted), rounded in a different
+ * order.  sla_spmv and the dL/dA pass always use the caller's arrays.
+ * fp32 handles run
  * the recurrence at fp64-equivalent precision (working vectors as
  * double-float pairs) and round x to fp32 on return.  The host issues
  * opts->poll_k iterations per launch -- a CUDA graph of one kernel per CG

@@ -79,11 +79,14 @@ class CSRMatrix:
     instead of a CUDA graph of one kernel per step; time_product=True
     records the live duration of one product kernel per graph launch
     (product_time); producer_consumer=True uses the producer/consumer
-    product where it applies."""
+    product where it applies; reorder=True / False forces / forbids
+    iterating on a reverse Cuthill-McKee reordering (default: reorder
+    scattered patterns)."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
                  validate: bool = True, pipeline: bool = False, fused: bool = False,
-                 time_product: bool = False, producer_consumer: bool = False, stream=None):
+                 time_product: bool = False, producer_consumer: bool = False, reorder: bool | None = None,
+                 stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -108,7 +111,9 @@ class CSRMatrix:
                                   (_lib.SLA_WARP_PIPELINE if pipeline else 0) |
                                   (_lib.SLA_PERSISTENT if fused else 0) |
                                   (_lib.SLA_TIME_PRODUCT if time_product else 0) |
-                                  (_lib.SLA_PRODUCER_CONSUMER if producer_consumer else 0), _stream(stream),
+                                  (_lib.SLA_PRODUCER_CONSUMER if producer_consumer else 0) |
+                                  ({None: 0, True: _lib.SLA_REORDER, False: _lib.SLA_NO_REORDER}[reorder]),
+                                  _stream(stream),
                                   C.byref(self._h)))
 
     # -------------------------------------------------------------- lifetime
@@ -156,11 +161,11 @@ class CSRMatrix:
         _check(_lib_handle().sla_product_time(self._h, C.byref(ms), C.byref(n), int(reset)))
         return ms.value, n.value
 
-    def layout(self) -> tuple[int, int]:
-        """(product form 0..3, CTAs per system) the library chose for A."""
-        f, g = C.c_int(), C.c_int()
-        _check(_lib_handle().sla_csr_layout(self._h, C.byref(f), C.byref(g)))
-        return f.value, g.value
+    def layout(self) -> tuple[int, int, bool]:
+        """(product form 0..4, CTAs per system, reordered) of the matrix the solves iterate on."""
+        f, g, r = C.c_int(), C.c_int(), C.c_int()
+        _check(_lib_handle().sla_csr_layout(self._h, C.byref(f), C.byref(g), C.byref(r)))
+        return f.value, g.value, bool(r.value)
 
     def update_values(self, values: torch.Tensor, stream=None):
         if values.dtype != self.dtype or values.numel() != self.batch * self.nnz or not values.is_cuda:

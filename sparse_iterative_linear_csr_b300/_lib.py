@@ -21,6 +21,8 @@ SLA_WARP_PIPELINE = 2
 SLA_PERSISTENT = 4
 SLA_TIME_PRODUCT = 8
 SLA_PRODUCER_CONSUMER = 16
+SLA_REORDER = 32
+SLA_NO_REORDER = 64
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
@@ -56,7 +58,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_csr_create.argtypes = [C.c_int, C.c_longlong, C.c_int, C.c_int, _vp, _vp, _vp, C.c_uint, _vp,
                                    C.POINTER(_vp)]
     lib.sla_csr_update_values.argtypes = [_vp, _vp, _vp]
-    lib.sla_csr_layout.argtypes = [_vp, C.POINTER(C.c_int), C.POINTER(C.c_int)]
+    lib.sla_csr_layout.argtypes = [_vp, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_int)]
     lib.sla_product_time.argtypes = [_vp, C.POINTER(C.c_double), C.POINTER(C.c_longlong), C.c_int]
     lib.sla_spmv.argtypes = [_vp, _vp, _vp, _vp]
     lib.sla_spmv_dot.argtypes = [_vp, _vp, _vp, _vp, _vp]

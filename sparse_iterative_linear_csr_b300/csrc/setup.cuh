@@ -110,6 +110,20 @@ __global__ void k_chunk_max(const int* __restrict__ rp, int n, int R, int* out) 
     if (m) atomicMax(out, m);
 }
 
+// out[s * os + i] = in[s * is + map[i]] for i < m and every system s:
+// permuted vectors (map = permutation) and permuted values (map = source
+// entry of each permuted entry).
+template <typename T>
+__global__ void k_gather_map(long long m, int batch, const int* __restrict__ map, const T* __restrict__ in,
+                             long long is, T* __restrict__ out, long long os) {
+    const long long total = m * batch;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long s = t / m, i = t - s * m;
+        out[s * os + i] = in[s * is + map[i]];
+    }
+}
+
 // Number of stored entries whose column is more than `w` away from the row.
 __global__ void k_far_count(const int* __restrict__ rp, const int* __restrict__ ci, int n, int w,
                             unsigned long long* out) {

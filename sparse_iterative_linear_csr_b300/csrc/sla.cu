@@ -72,6 +72,10 @@ static sla_status launched() {
 struct DevBuf {
     void* p = nullptr;
     size_t bytes = 0;
+    DevBuf() = default;
+    DevBuf(const DevBuf&) = delete;
+    DevBuf& operator=(const DevBuf&) = delete;
+    ~DevBuf() { release(); }
     sla_status alloc(size_t b) {
         release();
         if (b == 0) b = 16;
@@ -143,7 +147,18 @@ struct sla_csr {
     int device = 0;
     int sms = 0;
 
-    Layout LA;         // product layout of A
+    Layout LA;         // product layout of A (sla_spmv, the dL/dA pass)
+    // The matrix the solve iterates on: A itself, or P A P^T when the handle
+    // reorders a scattered pattern (reverse Cuthill-McKee).
+    const int* irp = nullptr;
+    const int* ici = nullptr;
+    const void* ivals = nullptr;
+    Layout LI;
+    bool reordered = false;
+    DevBuf perm, iperm;        // int[n]: new -> old row, old -> new row
+    DevBuf prp, pci, psrc;     // permuted pattern; source entry of every permuted entry
+    DevBuf pvals;              // permuted values [batch][nnz]
+    DevBuf ptmp;               // 2 x [batch][n] values: permuted right-hand side / initial guess, result
     bool vals_aligned = false;  // values 16-byte aligned for every system (chunk pipeline)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
     bool ws = false;            // SLA_PRODUCER_CONSUMER: producer/consumer product where it applies
@@ -397,6 +412,7 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     return m;
 }
 static Mat mat_A(const sla_csr* h) { return mat_of(h->rp, h->ci, h->n, h->nnz, h->LA, &h->ctl.as<Ctrl>()->err); }
+static Mat mat_I(const sla_csr* h) { return mat_of(h->irp, h->ici, h->n, h->nnz, h->LI, &h->ctl.as<Ctrl>()->err); }
 static Mat mat_G(const sla_csr* h) {
     return mat_of(h->grp.as<int>(), h->gci.as<int>(), h->n, h->nnzg, h->LG, &h->ctl.as<Ctrl>()->err);
 }
@@ -500,16 +516,176 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
     return set_form_any(h, L, aligned, vb);
 }
 
+// ===================================================================== reordering
+// Reverse Cuthill-McKee order of a pattern read as a graph (row i adjacent
+// to the columns of its stored entries): each connected part is walked
+// breadth-first from a pseudo-peripheral row (George-Liu search from a row
+// of least degree), unvisited neighbours in order of increasing degree,
+// and the whole order is reversed.  perm[new] = old.
+static void rcm_order(int n, const std::vector<int>& rp, const std::vector<int>& ci, std::vector<int>& perm) {
+    std::vector<int> deg(n);
+    for (int i = 0; i < n; ++i) deg[i] = rp[i + 1] - rp[i];
+    std::vector<int> by_deg(n);
+    for (int i = 0; i < n; ++i) by_deg[i] = i;
+    std::stable_sort(by_deg.begin(), by_deg.end(), [&](int a, int b) { return deg[a] < deg[b]; });
+    std::vector<char> seen(n, 0);
+    std::vector<int> stamp(n, -1), queue;
+    queue.reserve(n);
+    std::vector<int> order;
+    order.reserve(n);
+    int pass = 0;
+    // breadth-first levels from `root` inside its part (without marking
+    // `seen`); returns the depth and a least-degree row of the last level
+    auto last_level = [&](int root, int& far) {
+        ++pass;
+        queue.clear();
+        queue.push_back(root);
+        stamp[root] = pass;
+        size_t head = 0;
+        int depth = 0;
+        while (head < queue.size()) {
+            const size_t end = queue.size();
+            far = queue[head];
+            for (size_t k = head; k < end; ++k)
+                if (deg[queue[k]] < deg[far]) far = queue[k];
+            for (; head < end; ++head) {
+                const int u = queue[head];
+                for (int k = rp[u]; k < rp[u + 1]; ++k) {
+                    const int v = ci[k];
+                    if (stamp[v] != pass && !seen[v]) {
+                        stamp[v] = pass;
+                        queue.push_back(v);
+                    }
+                }
+            }
+            if (queue.size() > end) ++depth;
+        }
+        return depth;
+    };
+    std::vector<std::pair<int, int>> nb;
+    for (int start : by_deg) {
+        if (seen[start]) continue;
+        int root = start, far = start;
+        int depth = last_level(root, far);
+        for (int it = 0; it < 4; ++it) {   // move to a farther row while the depth grows
+            int far2 = far;
+            const int d2 = last_level(far, far2);
+            if (d2 <= depth) break;
+            root = far;
+            depth = d2;
+            far = far2;
+        }
+        const size_t base = order.size();
+        order.push_back(root);
+        seen[root] = 1;
+        for (size_t head = base; head < order.size(); ++head) {
+            const int u = order[head];
+            nb.clear();
+            for (int k = rp[u]; k < rp[u + 1]; ++k) {
+                const int v = ci[k];
+                if (!seen[v]) {
+                    seen[v] = 1;
+                    nb.emplace_back(deg[v], v);
+                }
+            }
+            std::sort(nb.begin(), nb.end());
+            for (const auto& e : nb) order.push_back(e.second);
+        }
+    }
+    perm.assign(order.rbegin(), order.rend());
+}
+
+// Pattern of P M P^T for perm[new] = old: row i' is old row perm[i'] with
+// every column c renamed iperm[c], columns ascending; src[k'] = the entry
+// of M that permuted entry k' holds.  Rows are filled by several threads.
+static void permute_pattern(int n, const std::vector<int>& rp, const std::vector<int>& ci,
+                            const std::vector<int>& perm, const std::vector<int>& iperm, std::vector<int>& rp2,
+                            std::vector<int>& ci2, std::vector<int>& src) {
+    rp2.assign(n + 1, 0);
+    for (int i = 0; i < n; ++i) rp2[i + 1] = rp2[i] + (rp[perm[i] + 1] - rp[perm[i]]);
+    ci2.resize(ci.size());
+    src.resize(ci.size());
+    const int nt = std::max(1, std::min(16, (int)std::thread::hardware_concurrency()));
+    std::vector<std::thread> pool;
+    for (int t = 0; t < nt; ++t)
+        pool.emplace_back([&, t] {
+            std::vector<std::pair<int, int>> row;
+            for (int i = t; i < n; i += nt) {
+                const int o = perm[i];
+                row.clear();
+                for (int k = rp[o]; k < rp[o + 1]; ++k) row.emplace_back(iperm[ci[k]], k);
+                std::sort(row.begin(), row.end());
+                for (size_t j = 0; j < row.size(); ++j) {
+                    ci2[rp2[i] + j] = row[j].first;
+                    src[rp2[i] + j] = row[j].second;
+                }
+            }
+        });
+    for (auto& th : pool) th.join();
+}
+
+static sla_status to_host(std::vector<int>& out, const int* d, size_t m) {
+    out.resize(m);
+    if (m) CU(cudaMemcpy(out.data(), d, sizeof(int) * m, cudaMemcpyDeviceToHost));
+    return SLA_OK;
+}
+static sla_status to_device(DevBuf& buf, const std::vector<int>& v) {
+    TRY(buf.alloc(sizeof(int) * (v.empty() ? 1 : v.size())));
+    if (!v.empty()) CU(cudaMemcpy(buf.p, v.data(), sizeof(int) * v.size(), cudaMemcpyHostToDevice));
+    return SLA_OK;
+}
+
+// out[s][k] = in[s][map[k]] for k < m, systems strided by `is` / `os`
+// elements of `eb` bytes (8: fp64 or a double-float pair; 4: fp32).
+static sla_status gather_map(size_t eb, long long m, int batch, const int* map, const void* in, long long is,
+                             void* out, long long os, cudaStream_t s) {
+    if (m == 0) return SLA_OK;
+    const long long tot = m * batch;
+    const int g = (int)std::min<long long>((tot + 255) / 256, 8192);
+    if (eb == 8)
+        k_gather_map<double><<<g, 256, 0, s>>>(m, batch, map, (const double*)in, is, (double*)out, os);
+    else
+        k_gather_map<float><<<g, 256, 0, s>>>(m, batch, map, (const float*)in, is, (float*)out, os);
+    return launched();
+}
+
+// Iterate on P A P^T (reverse Cuthill-McKee): permuted pattern and values
+// owned by the handle, with the permutation both ways.
+static sla_status make_reordered(sla_csr* h, cudaStream_t s) {
+    const int n = h->n;
+    std::vector<int> rp, ci, perm, iperm, rp2, ci2, src;
+    CU(cudaStreamSynchronize(s));
+    TRY(to_host(rp, h->rp, (size_t)n + 1));
+    TRY(to_host(ci, h->ci, (size_t)h->nnz));
+    rcm_order(n, rp, ci, perm);
+    iperm.resize(n);
+    for (int i = 0; i < n; ++i) iperm[perm[i]] = i;
+    permute_pattern(n, rp, ci, perm, iperm, rp2, ci2, src);
+    TRY(to_device(h->perm, perm));
+    TRY(to_device(h->iperm, iperm));
+    TRY(to_device(h->prp, rp2));
+    TRY(to_device(h->pci, ci2));
+    TRY(to_device(h->psrc, src));
+    TRY(h->pvals.alloc(h->es * (size_t)h->nnz * h->batch));
+    TRY(gather_map(h->es, h->nnz, h->batch, h->psrc.as<int>(), h->vals, h->nnz, h->pvals.p, h->nnz, s));
+    TRY(h->ptmp.alloc(2 * h->es * (size_t)n * h->batch));
+    h->irp = h->prp.as<int>();
+    h->ici = h->pci.as<int>();
+    h->ivals = h->pvals.p;
+    h->reordered = true;
+    return SLA_OK;
+}
+
 static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
     DevBuf err;
     TRY(err.alloc(sizeof(int)));
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
     const int g = (h->n + 255) / 256 < 4096 ? (h->n + 255) / 256 : 4096;
     if (h->dt == SLA_F64)
-        k_diag<double><<<g, 256, 0, s>>>(h->n, h->nnz, h->batch, h->rp, h->ci, (const double*)h->vals,
+        k_diag<double><<<g, 256, 0, s>>>(h->n, h->nnz, h->batch, h->irp, h->ici, (const double*)h->ivals,
                                          h->diag.as<double>(), err.as<int>());
     else
-        k_diag<float><<<g, 256, 0, s>>>(h->n, h->nnz, h->batch, h->rp, h->ci, (const float*)h->vals,
+        k_diag<float><<<g, 256, 0, s>>>(h->n, h->nnz, h->batch, h->irp, h->ici, (const float*)h->ivals,
                                         h->diag.as<double>(), err.as<int>());
     TRY(launched());
     const size_t m = (size_t)h->batch * h->n;
@@ -556,8 +732,17 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     DevBuf err;
     TRY(err.alloc(sizeof(int)));
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
+    // G is defined on the caller's ordering (tril of A); with a reordered
+    // handle it is built there and then permuted like A.
+    DevBuf dorig;
+    const double* dbase = h->diag.as<double>();
+    if (h->reordered) {
+        TRY(dorig.alloc(sizeof(double) * (size_t)n * h->batch));
+        TRY(gather_map(8, n, h->batch, h->iperm.as<int>(), h->diag.p, n, dorig.p, n, s));
+        dbase = dorig.as<double>();
+    }
     for (int sy = 0; sy < h->batch; ++sy) {
-        const double* dg = h->diag.as<double>() + (size_t)sy * n;
+        const double* dg = dbase + (size_t)sy * n;
         double* gv = h->gv.as<double>() + (size_t)sy * h->gstride;     // 8-byte slots: fp64, or a
         double* gtv = h->gtv.as<double>() + (size_t)sy * h->gstride;   // double-float pair for fp32
         if (h->dt == SLA_F64) {
@@ -580,6 +765,28 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     int e = 0;
     TRY(read_int(err.as<int>(), &e, s));
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
+    if (h->reordered) {
+        std::vector<int> perm, iperm;
+        TRY(to_host(perm, h->perm.as<int>(), (size_t)n));
+        iperm.resize(n);
+        for (int i = 0; i < n; ++i) iperm[perm[i]] = i;
+        DevBuf* pats[2][3] = {{&h->grp, &h->gci, &h->gv}, {&h->gtrp, &h->gtci, &h->gtv}};
+        for (auto& pt : pats) {
+            std::vector<int> rp, ci, rp2, ci2, src;
+            TRY(to_host(rp, pt[0]->as<int>(), (size_t)n + 1));
+            TRY(to_host(ci, pt[1]->as<int>(), (size_t)ng));
+            permute_pattern(n, rp, ci, perm, iperm, rp2, ci2, src);
+            DevBuf dsrc, vals2;
+            TRY(to_device(dsrc, src));
+            TRY(vals2.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
+            TRY(gather_map(8, ng, h->batch, dsrc.as<int>(), pt[2]->p, h->gstride, vals2.p, h->gstride, s));
+            CU(cudaStreamSynchronize(s));
+            TRY(to_device(*pt[0], rp2));
+            TRY(to_device(*pt[1], ci2));
+            std::swap(pt[2]->p, vals2.p);
+            std::swap(pt[2]->bytes, vals2.bytes);
+        }
+    }
     TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, true, sizeof(double), s));
     TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s));
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
@@ -590,6 +797,7 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
 static sla_status ensure_pstride(sla_csr* h) {
     int m = gx_vec(h);
     m = m > h->LA.gx ? m : h->LA.gx;
+    m = m > h->LI.gx ? m : h->LI.gx;
     // the fused iteration kernel: two reductions of two values per CTA, at
     // most as many CTAs as fit resident (2048 threads per SM)
     const int fused = (int)((long long)(2048 / NT) * h->sms / h->batch) + 1;
@@ -611,8 +819,8 @@ template <typename T, bool PAIRS>
 static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t s, int* nodes, cudaEvent_t ev0,
                                     cudaEvent_t ev1) {
     const Sys S = sys_of(h);
-    const Mat A = mat_A(h);
-    const T* av = (const T*)h->vals;
+    const Mat A = mat_I(h);
+    const T* av = (const T*)h->ivals;
     using W = typename Prec<T>::w;
     W* r = h->r.as<W>();
     W* p = h->p.as<W>();
@@ -621,12 +829,12 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     using GV = typename Prec<T>::gv;
     XW* x = h->x.as<XW>();
     const XW* dinv = h->dinv.as<XW>();
-    const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
+    const dim3 gs(h->LI.gx, h->batch), gv(gx_vec(h), h->batch);
     // external event-record nodes (a plain record inside a capture only
     // orders streams within the graph)
     if (ev0) CU(cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal));
-    with_form(h->LA.form, [&](auto f) {
-        k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LA.smem, s>>>(A, S, av, p, q, x, h->bw.as<T>());
+    with_form(h->LI.form, [&](auto f) {
+        k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LI.smem, s>>>(A, S, av, p, q, x, h->bw.as<T>());
     });
     TRY(launched());
     if (ev1) CU(cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal));
@@ -728,13 +936,13 @@ template <typename T, int PC, bool PAIRS>
 static sla_status fused_grid(const sla_csr* h, int* gx) {
     int per = 0;
     cudaError_t e = cudaSuccess;
-    with_form(h->LA.form, [&](auto f) {
+    with_form(h->LI.form, [&](auto f) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_cg_fused<T, decltype(f)::value, PC, PAIRS>, NT,
-                                                          h->LA.smem);
+                                                          h->LI.smem);
     });
     if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
     long long g = (long long)per * h->sms / h->batch;
-    const long long work = std::max(group_ctas(h->n, h->LA.form == 3 ? 1 : h->LA.lanes), vec_units(h));
+    const long long work = std::max(group_ctas(h->n, h->LI.form == 3 ? 1 : h->LI.lanes), vec_units(h));
     if (g > work) g = work;
     *gx = (int)g;
     return SLA_OK;
@@ -744,9 +952,9 @@ template <typename T, int PC, bool PAIRS>
 static sla_status launch_fused(sla_csr* h, int gx, int iters, cudaStream_t s) {
     using W = typename Prec<T>::w;
     using XW = typename Prec<T>::xw;
-    Mat A = mat_A(h);
+    Mat A = mat_I(h);
     Sys S = sys_of(h);
-    const T* av = (const T*)h->vals;
+    const T* av = (const T*)h->ivals;
     W* p = h->p.as<W>();
     W* q = h->q.as<W>();
     W* r = h->r.as<W>();
@@ -757,9 +965,9 @@ static sla_status launch_fused(sla_csr* h, int gx, int iters, cudaStream_t s) {
     GridSync* gsy = h->gsync.as<GridSync>();
     void* args[] = {&A, &S, &av, &p, &q, &r, &z, &x, &dinv, &b, &gsy, &iters};
     cudaError_t e = cudaSuccess;
-    with_form(h->LA.form, [&](auto f) {
+    with_form(h->LI.form, [&](auto f) {
         e = cudaLaunchCooperativeKernel((const void*)k_cg_fused<T, decltype(f)::value, PC, PAIRS>,
-                                        dim3((unsigned)gx, (unsigned)h->batch), dim3(NT), args, h->LA.smem, s);
+                                        dim3((unsigned)gx, (unsigned)h->batch), dim3(NT), args, h->LI.smem, s);
     });
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "cooperative launch failed: %s", cudaGetErrorString(e));
@@ -809,9 +1017,9 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     if (!fused) TRY(get_graph<T>(h, pc, eps, k, &gc));
 
     const Sys S = sys_of(h);
-    const Mat A = mat_A(h);
-    const T* av = (const T*)h->vals;
-    const dim3 gs(h->LA.gx, h->batch), gv(gx_vec(h), h->batch);
+    const Mat A = mat_I(h);
+    const T* av = (const T*)h->ivals;
+    const dim3 gs(h->LI.gx, h->batch), gv(gx_vec(h), h->batch);
     using W = typename Prec<T>::w;
     W* r = h->r.as<W>();
     W* p = h->p.as<W>();
@@ -822,11 +1030,23 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
 
     CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
     CU(cudaMemsetAsync(h->gsync.p, 0, sizeof(GridSync) * h->batch, s));
+    // a reordered handle iterates on P b (and P x0) and returns P^T x
+    const T* b_it = b;
+    const T* x0_it = x_user;
+    T* x_it = x_user;
+    if (h->reordered) {
+        T* tb = h->ptmp.as<T>();
+        T* tx = tb + (size_t)h->batch * h->n;
+        TRY(gather_map(sizeof(T), h->n, h->batch, h->perm.as<int>(), b, h->n, tb, h->n, s));
+        if (o->use_x0) TRY(gather_map(sizeof(T), h->n, h->batch, h->perm.as<int>(), x_user, h->n, tx, h->n, s));
+        b_it = tb;
+        x0_it = tx;
+        x_it = tx;
+    }
     if (o->use_x0) {
-        k_init_x0<T><<<gs, NT, h->LA.smem, s>>>(A, S, av, b, x_user, h->bw.as<T>(), x, r, o->tol,
-                                                         o->max_iter);
+        k_init_x0<T><<<gs, NT, h->LI.smem, s>>>(A, S, av, b_it, x0_it, h->bw.as<T>(), x, r, o->tol, o->max_iter);
     } else {
-        k_init<T><<<gv, NT, 0, s>>>(S, b, h->bw.as<T>(), x, r, o->tol, o->max_iter);
+        k_init<T><<<gv, NT, 0, s>>>(S, b_it, h->bw.as<T>(), x, r, o->tol, o->max_iter);
     }
     TRY(launched());
     if (pc == SLA_PC_SPAI) {
@@ -905,8 +1125,9 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     // drain (kernels of a finished batch return at once)
     CU(cudaStreamSynchronize(s));
 
-    k_final<T><<<gs, NT, h->LA.smem, s>>>(A, S, av, x, h->bw.as<T>(), x_user, h->stat.as<Stat>());
+    k_final<T><<<gs, NT, h->LI.smem, s>>>(A, S, av, x, h->bw.as<T>(), x_it, h->stat.as<Stat>());
     TRY(launched());
+    if (h->reordered) TRY(gather_map(sizeof(T), h->n, h->batch, h->iperm.as<int>(), x_it, h->n, x_user, h->n, s));
     CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
     Ctrl dc;
     CU(cudaMemcpyAsync(&dc, h->ctl.p, sizeof(Ctrl), cudaMemcpyDeviceToHost, s));
@@ -970,7 +1191,8 @@ sla_status sla_csr_destroy(sla_handle h) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
     DevBuf* bufs[] = {&h->diag, &h->dinv, &h->grp, &h->gci, &h->gv, &h->gtrp, &h->gtci, &h->gtv,
                       &h->x, &h->r, &h->p, &h->q, &h->z, &h->t, &h->bw, &h->state,
-                      &h->ctl, &h->cnt, &h->part, &h->stat, &h->gsync};
+                      &h->ctl, &h->cnt, &h->part, &h->stat, &h->gsync, &h->perm, &h->iperm,
+                      &h->prp, &h->pci, &h->psrc, &h->pvals, &h->ptmp};
     for (DevBuf* b : bufs) b->release();
     destroy_handle(h);
     return SLA_OK;
@@ -1050,6 +1272,18 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
         h->coop = coop != 0;
     }
     HTRY(choose_layout(h, d_row_ptr, d_col_idx, nnz, &h->LA, h->vals_aligned, h->es, s));
+    // the matrix the solve iterates on: A, or P A P^T for a scattered
+    // pattern (its gathers then stay near the row)
+    h->irp = d_row_ptr;
+    h->ici = d_col_idx;
+    h->ivals = d_vals;
+    h->LI = h->LA;
+    const bool reorder = nnz > 0 && !(flags & SLA_NO_REORDER) && ((flags & SLA_REORDER) || h->LA.gasync);
+    if (reorder) {
+        HTRY(make_reordered(h, s));
+        const bool al = h->batch == 1 || ((size_t)nnz * h->es) % 16 == 0;
+        HTRY(choose_layout(h, h->irp, h->ici, nnz, &h->LI, al, h->es, s));
+    }
     const size_t vn = (size_t)n * batch;
     HTRY(h->diag.alloc(sizeof(double) * vn));
     HTRY(h->dinv.alloc(sizeof(double) * vn));
@@ -1088,10 +1322,11 @@ sla_status sla_product_time(sla_handle h, double* total_ms, long long* samples, 
     return SLA_OK;
 }
 
-sla_status sla_csr_layout(sla_handle h, int* form, int* ctas) {
+sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
-    if (form) *form = h->LA.form;
-    if (ctas) *ctas = h->LA.gx;
+    if (form) *form = h->LI.form;
+    if (ctas) *ctas = h->LI.gx;
+    if (reordered) *reordered = h->reordered ? 1 : 0;
     return SLA_OK;
 }
 
@@ -1105,8 +1340,11 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
     if (vals_aligned(h, d_vals) != h->vals_aligned) {
         h->vals_aligned = !h->vals_aligned;
         TRY(set_form_any(h, &h->LA, h->vals_aligned, h->es));
+        if (!h->reordered) h->LI = h->LA;
         TRY(ensure_pstride(h));
     }
+    if (h->reordered) TRY(gather_map(h->es, h->nnz, h->batch, h->psrc.as<int>(), d_vals, h->nnz, h->pvals.p, h->nnz, s));
+    else h->ivals = d_vals;
     TRY(compute_diag(h, s));
     CU(cudaStreamSynchronize(s));
     return SLA_OK;

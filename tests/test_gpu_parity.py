@@ -352,3 +352,79 @@ def test_product_time_records_live_launches(cuda_device):
     plain = CSRMatrix(rp, ci, v)
     plain.solve(b, tol=w.tol, pc="jacobi", poll_k=8)
     assert plain.product_time() == (0.0, 0)
+
+
+# --------------------------------------------------------------- reordering
+REORDER_CASES = [
+    ("c2", {"N": 64}, "jacobi"),
+    ("c5", {"npoints": 20000}, "spai"),
+    ("c5", {"npoints": 20000}, "jacobi"),
+    ("c3", {"N": 32, "batch": 3}, "jacobi"),
+    ("c1", {}, "none"),
+]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["steps", "fused"])
+@pytest.mark.parametrize("cfg,kw,pc", REORDER_CASES, ids=[f"{c}-{p}" for c, k, p in REORDER_CASES])
+def test_reordered_solve_and_adjoint_parity(cuda_device, cfg, kw, pc, fused):
+    """Iterating on P A P^T (reverse Cuthill-McKee) solves the caller's
+    system: x, iterations and the adjoint match the oracle on A itself."""
+    w = build(cfg, **kw)
+    M = make(w.A, reorder=True, fused=fused)
+    assert M.layout()[2]
+    b = torch.from_numpy(w.b).to(cuda_device)
+    g = torch.from_numpy(w.g).to(cuda_device)
+    x, info = M.solve(b, tol=w.tol, max_iter=20000, pc=pc, eps=1e-3, poll_k=16)
+    xh = x.cpu().numpy()
+    xo, io = oracle.pcg(w.A, w.b, w.tol, max_iter=20000, pc=pc, eps=1e-3)
+    X, XO, IO = (xh, xo, io) if M.batch > 1 or w.A.vals.ndim == 2 else (xh[None], xo[None], [io])
+    bs = w.b if w.b.ndim == 2 else w.b[None]
+    for s in range(len(info)):
+        assert info[s].status == "ok" and _iters_ok(info[s].iters, IO[s]["iters"]), (info[s].iters, IO[s]["iters"])
+        assert rel(X[s], XO[s]) <= 1e-6
+        assert abs(oracle.rel_residual(w.A, bs[s], X[s], system=s) - info[s].rel_res_true) <= 1e-3 * w.tol
+    lb, la, ainfo = M.adjoint(x, g, tol=w.tol, max_iter=20000, pc=pc, eps=1e-3)
+    lb_o, la_o, aio = oracle.adjoint(w.A, xh, w.g, w.tol, max_iter=20000, pc=pc, eps=1e-3)
+    lb, la = lb.cpu().numpy(), la.cpu().numpy()
+    if lb.ndim == 1:
+        lb, la, lb_o, la_o, aio = lb[None], la[None], lb_o[None], la_o[None], [aio]
+    for s in range(lb.shape[0]):
+        assert ainfo[s].status == "ok" and _iters_ok(ainfo[s].iters, aio[s]["iters"])
+        assert rel(lb[s], lb_o[s]) <= 1e-6 and rel(la[s], la_o[s]) <= 1e-6
+
+
+def test_scattered_pattern_is_reordered(cuda_device):
+    """A grid relabelled at random is detected as scattered and reordered;
+    the solve still matches the oracle, the SpMV API still works on A, and
+    an initial guess and new values pass through the permutation."""
+    base = poisson_grid((400, 400))
+    n = base.n
+    perm = np.random.default_rng(4).permutation(n)
+    inv = np.empty(n, np.int64)
+    inv[perm] = np.arange(n)
+    rows = base.rows()
+    r2, c2 = inv[rows], inv[base.col_idx]
+    order = np.lexsort((c2, r2))
+    rp = np.zeros(n + 1, np.int64)
+    np.cumsum(np.bincount(r2, minlength=n), out=rp[1:])
+    A = CSR(n, rp.astype(np.int32), c2[order].astype(np.int32), base.vals[order])
+    M = make(A)
+    assert M.layout()[2], "a randomly relabelled grid should be reordered"
+    assert not make(A, reorder=False).layout()[2]
+    x_true = np.random.default_rng(2).standard_normal(n)
+    b = oracle.spmv(A, x_true)
+    bt = torch.from_numpy(b).to(cuda_device)
+    assert rel(M.matvec(torch.from_numpy(x_true).to(cuda_device)).cpu().numpy(), b) <= 1e-13
+    x, info = M.solve(bt, tol=1e-9, pc="jacobi", max_iter=20000)
+    xo, io = oracle.pcg(A, b, 1e-9, pc="jacobi", max_iter=20000)
+    assert info[0].status == "ok" and _iters_ok(info[0].iters, io["iters"])
+    assert rel(x.cpu().numpy(), xo) <= 1e-6
+    x0 = np.random.default_rng(3).standard_normal(n)
+    x1, i1 = M.solve(bt, tol=1e-9, pc="jacobi", max_iter=20000, x0=torch.from_numpy(x0).to(cuda_device))
+    xo1, io1 = oracle.pcg(A, b, 1e-9, pc="jacobi", max_iter=20000, x0=x0)
+    assert _iters_ok(i1[0].iters, io1["iters"]) and rel(x1.cpu().numpy(), xo1) <= 1e-6
+    M.update_values(M.values * 3.0)
+    A3 = CSR(n, A.row_ptr, A.col_idx, A.vals * 3.0)
+    x3, i3 = M.solve(bt, tol=1e-9, pc="jacobi", max_iter=20000)
+    xo3, io3 = oracle.pcg(A3, b, 1e-9, pc="jacobi", max_iter=20000)
+    assert _iters_ok(i3[0].iters, io3["iters"]) and rel(x3.cpu().numpy(), xo3) <= 1e-6
