@@ -195,9 +195,15 @@ static constexpr int MAX_CAP = 864;  // staging capacity limit (larger groups ta
 // Staging form for capacity `cap`: 2 (cp.async, double-buffered values and
 // columns) while that fits three CTAs per SM, else 1 (single-buffered) while
 // it fits two, else 0 (register staging).
+#ifndef SLA_STAGE_CTAS
+#define SLA_STAGE_CTAS 3   // resident CTAs per SM double buffering must still allow
+#endif
+#ifndef SLA_MIN_LANES
+#define SLA_MIN_LANES 1    // fewest lanes per row the layout considers
+#endif
 static int staging_form(int cap) {
     const size_t per_sm = 228 * 1024;
-    if ((size_t)NWARP * async_smem_per_warp<double, double>(cap, 2) * 3 <= per_sm) return 2;
+    if ((size_t)NWARP * async_smem_per_warp<double, double>(cap, 2) * SLA_STAGE_CTAS <= per_sm) return 2;
     if ((size_t)NWARP * async_smem_per_warp<double, double>(cap, 1) * 2 <= per_sm) return 1;
     return 0;
 }
@@ -479,7 +485,7 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
         CU(cudaStreamSynchronize(s));
         L->gasync = (double)f > 0.1 * (double)nnz ? 1 : 0;
     }
-    for (int lanes = 1; lanes <= 4; lanes *= 2) {
+    for (int lanes = SLA_MIN_LANES; lanes <= 4; lanes *= 2) {
         int m = 0;
         TRY(group_max(rp, h->n, 32 / lanes, &m, s));
         int cap = (m + 31) / 32 * 32;
