@@ -160,6 +160,15 @@ sla_status sla_spmv(sla_handle h, const void* d_x, void* d_y, void* stream);
 sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot, void* stream);
 
 /*
+ * Block product: Y[:, j] = A X[:, j] for the k columns of a block stored
+ * column after column (d_X, d_Y: [k][n], column j at offset j*n), in the
+ * handle's dtype.  Needs a single-system handle (batch = 1); 0 <= k <= 65535.
+ * Same product kernels as sla_spmv, with every column reading the same
+ * values (the block eigensolver's A times a block).  Does not synchronise.
+ */
+sla_status sla_spmm(sla_handle h, const void* d_X, void* d_Y, int k, void* stream);
+
+/*
  * Solve A x = b by preconditioned CG, every system of a batch independently
  * (converged systems are frozen while the others continue).  d_b, d_x:
  * [batch][n].  x0 = 0 unless opts->use_x0.  info: host array of `batch`

@@ -202,3 +202,18 @@ def rel_residual(A, b, x, system: int = 0) -> float:
     bb, bp = _d(b)
     xx, xp = _d(x)
     return lib.oracle_rel_residual(A.n, rpp, cip, vp, bp, xp)
+
+
+def eigsh_dense(A, k, largest=False, system: int = 0):
+    """The k smallest (largest) eigenpairs of the symmetric matrix A, by the
+    plain definition: a dense symmetric eigendecomposition (LAPACK through
+    numpy.linalg.eigh) of the matrix the CSR arrays describe.  Returns
+    (eigenvalues ascending [k] (descending when largest), eigenvectors [k, n])."""
+    n = A.n
+    D = np.zeros((n, n))
+    rows = np.repeat(np.arange(n), np.diff(A.row_ptr))
+    D[rows, A.col_idx] = _system_vals(A, system)
+    w, V = np.linalg.eigh((D + D.T) / 2)
+    if largest:
+        w, V = w[::-1], V[:, ::-1]
+    return w[:k].copy(), V[:, :k].T.copy()

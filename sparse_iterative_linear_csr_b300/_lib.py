@@ -27,7 +27,7 @@ SLA_NO_REORDER = 64
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
-           "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time"]
+           "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time", "sla_spmm"]
 
 
 class PcgOpts(C.Structure):
@@ -61,6 +61,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_csr_layout.argtypes = [_vp, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_int)]
     lib.sla_product_time.argtypes = [_vp, C.POINTER(C.c_double), C.POINTER(C.c_longlong), C.c_int]
     lib.sla_spmv.argtypes = [_vp, _vp, _vp, _vp]
+    lib.sla_spmm.argtypes = [_vp, _vp, _vp, C.c_int, _vp]
     lib.sla_spmv_dot.argtypes = [_vp, _vp, _vp, _vp, _vp]
     lib.sla_pcg_solve.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), C.POINTER(SolveInfo), _vp]
     lib.sla_adjoint.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), _vp, _vp, C.POINTER(SolveInfo), _vp]
@@ -73,7 +74,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_spmv_dot_static.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
-    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
+    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
               "sla_adjoint", "sla_csr_destroy"]:
         getattr(lib, f).restype = C.c_int
     _lib = lib

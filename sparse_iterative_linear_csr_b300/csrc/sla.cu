@@ -1375,6 +1375,31 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     return launched();
 }
 
+sla_status sla_spmm(sla_handle h, const void* d_X, void* d_Y, int k, void* stream) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (h->batch != 1) return fail(SLA_ERR_INVALID, "sla_spmm needs a single-system handle (batch = 1)");
+    if (k < 0) return fail(SLA_ERR_INVALID, "k must be >= 0 (got %d)", k);
+    if (k == 0) return SLA_OK;
+    if (!d_X || !d_Y) return fail(SLA_ERR_INVALID, "null block");
+    if (k > 65535) return fail(SLA_ERR_INVALID, "k must be <= 65535 (got %d)", k);
+    cudaStream_t s = (cudaStream_t)stream;
+    Sys S = sys_of(h);
+    S.nnz = 0;   // every column of the block is multiplied by the same values
+    const Mat A = mat_A(h);
+    const dim3 g(h->LA.gx, k);
+    const size_t sm = h->LA.smem;
+    with_form(h->LA.form, [&](auto f) {
+        constexpr int F = decltype(f)::value;
+        if (h->dt == SLA_F64)
+            k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_X, (double*)d_Y,
+                                                nullptr);
+        else
+            k_spmv<float, F><<<g, NT, sm, s>>>(A, S, (const float*)h->vals, (const float*)d_X, (float*)d_Y,
+                                               nullptr);
+    });
+    return launched();
+}
+
 sla_status sla_spmv(sla_handle h, const void* d_x, void* d_y, void* stream) {
     return spmv_common(h, d_x, d_y, nullptr, stream);
 }
