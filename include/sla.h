@@ -120,9 +120,10 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  * the handle reorders (see sla_pcg_solve) -- for diagnostics:
  *  *form: 0 register-staged warp groups, 1 warp groups with asynchronous
  *         value/column staging, 2 the same with asynchronous gathers,
- *         3 the chunk pipeline (bulk copies of NT-row chunks; needs 16-byte
- *         aligned row_ptr, col_idx and values of every system, and groups
- *         that fit shared memory; only with SLA_WARP_PIPELINE);
+ *         3 the warp pipeline (each warp bulk-copies its 32-row groups into
+ *         a ring of shared-memory stages; needs 16-byte aligned row_ptr,
+ *         col_idx and values of every system, and groups that fit shared
+ *         memory; only with SLA_WARP_PIPELINE);
  *         4 producer/consumer warps (2 warps bulk-copy and gather tiles of
  *         192 rows into a ring of shared-memory stages, 6 warps add; same
  *         alignment conditions; only with SLA_PRODUCER_CONSUMER, which

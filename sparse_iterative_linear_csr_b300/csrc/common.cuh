@@ -19,7 +19,6 @@ constexpr int SPMV_MIN_CTAS = 4; // resident CTAs per SM the staged-SpMV kernels
 #endif
 template <typename T> struct IterMinCtas { static constexpr int value = SLA_ITER_CTAS_F64; };
 template <> struct IterMinCtas<float> { static constexpr int value = 4; };
-constexpr int MAXR = NT;         // rows per row block (one row per thread)
 
 // Outcome codes mirrored from sla_status (kept numerically equal).
 enum : int { ST_OK = 0, ST_NOT_CONVERGED = 4, ST_BREAKDOWN = 5 };

@@ -95,8 +95,9 @@ __global__ void k_group_max(const int* __restrict__ rp, int n, int R, int* out) 
     if (m) atomicMax(out, m);
 }
 
-// Largest staged range of a chunk of R consecutive rows, the range's ends
-// rounded out to multiples of 4 entries (as the chunk pipeline copies it).
+// Largest staged range of a run of R consecutive rows (a warp-pipeline group
+// or a producer/consumer tile), the range's ends rounded out to multiples of
+// 4 entries as the bulk copies move it.
 __global__ void k_chunk_max(const int* __restrict__ rp, int n, int R, int* out) {
     const long long nc = ((long long)n + R - 1) / R;
     int m = 0;

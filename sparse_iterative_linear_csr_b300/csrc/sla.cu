@@ -120,7 +120,7 @@ struct GraphCache {
 };
 
 // Product layout of one matrix: warp staging capacity (entries per group of
-// 32 / lanes rows), lanes per row, chunk-pipeline capacity and stages, the
+// 32 / lanes rows), lanes per row, bulk-copy capacities and stages, the
 // compiled form the product kernels use, their dynamic shared memory, and
 // CTAs per system.
 struct Layout {
@@ -130,7 +130,7 @@ struct Layout {
     int gasync = 0;   // gathers by cp.async (scattered columns)
     int ccap = 0;     // warp pipeline: entries per stage (0: a group would not fit)
     int tcap = 0;     // producer/consumer form: entries per tile stage (0: unusable)
-    int stages = 0;   // chunk pipeline: ring stages
+    int stages = 0;   // bulk-copy forms: ring stages
     int form = 0;     // compiled form of the product kernels (spmv_vec)
     size_t smem = 0;  // their dynamic shared memory
 };
@@ -159,7 +159,7 @@ struct sla_csr {
     DevBuf prp, pci, psrc;     // permuted pattern; source entry of every permuted entry
     DevBuf pvals;              // permuted values [batch][nnz]
     DevBuf ptmp;               // 2 x [batch][n] values: permuted right-hand side / initial guess, result
-    bool vals_aligned = false;  // values 16-byte aligned for every system (chunk pipeline)
+    bool vals_aligned = false;  // values 16-byte aligned for every system (bulk-copy forms)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
     bool ws = false;            // SLA_PRODUCER_CONSUMER: producer/consumer product where it applies
     bool time_product = false;  // SLA_TIME_PRODUCT: events around one product kernel per graph launch
@@ -375,7 +375,7 @@ static sla_status set_form_any(const sla_csr* h, Layout* L, bool aligned, size_t
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-// Values of every system 16-byte aligned (chunk pipeline bulk copies).
+// Values of every system 16-byte aligned (bulk copies of the forms 3 and 4).
 static bool vals_aligned(const sla_csr* h, const void* vals) {
     return aligned16(vals) && (h->batch == 1 || ((size_t)h->nnz * h->es) % 16 == 0);
 }

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle
 on the same seeded inputs, element by element, at sizes the oracle finishes
-in seconds (several row blocks and a ragged tail), plus edge cases.
+in seconds (many warp groups and CTAs and a ragged tail), plus edge cases.
 
 Every product test runs with the warp-staged forms (the default), the warp
 pipeline (pipeline=True) and the producer/consumer form
