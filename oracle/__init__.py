@@ -65,6 +65,12 @@ def _load():
             lib.oracle_adjoint.restype = C.c_int
             lib.oracle_rel_residual.argtypes = [C.c_int, _ip, _ip, _dp, _dp, _dp]
             lib.oracle_rel_residual.restype = C.c_double
+            lib.oracle_bicgstab.argtypes = [C.c_int, _ip, _ip, _dp, _dp, _dp, C.c_double, C.c_int,
+                                            C.c_int, C.c_int, _ip, _dp, _dp]
+            lib.oracle_bicgstab.restype = C.c_int
+            lib.oracle_bicgstab_adjoint.argtypes = [C.c_int, _ip, _ip, _dp, _dp, _dp, C.c_double,
+                                                    C.c_int, C.c_int, _dp, _dp, _ip, _dp, _dp]
+            lib.oracle_bicgstab_adjoint.restype = C.c_int
             _lib = lib
     return _lib
 
@@ -189,6 +195,64 @@ def adjoint(A, x, g, tol, max_iter=100000, pc="none", eps=0.0, f32=None):
     if A.vals.ndim == 1:
         return _adjoint_one(A, 0, x, g, tol, max_iter, pc, eps, f32)
     out = [_adjoint_one(A, s, x[s], g[s], tol, max_iter, pc, eps, f32)
+           for s in range(A.vals.shape[0])]
+    return (np.stack([o[0] for o in out]), np.stack([o[1] for o in out]),
+            [o[2] for o in out])
+
+
+def _bicgstab_one(A, s, b, tol, max_iter, pc, x0):
+    if pc not in ("none", "jacobi"):
+        raise ValueError("BiCGStab takes pc 'none' or 'jacobi'")
+    lib = _load()
+    rp, rpp = _i(A.row_ptr)
+    ci, cip = _i(A.col_idx)
+    v, vp = _d(_system_vals(A, s))
+    bb, bp = _d(b)
+    x = np.zeros(A.n, dtype=np.float64) if x0 is None else np.array(x0, dtype=np.float64)
+    it = C.c_int(0)
+    rr = C.c_double(0)
+    rt = C.c_double(0)
+    st = lib.oracle_bicgstab(A.n, rpp, cip, vp, bp, x.ctypes.data_as(_dp), float(tol), int(max_iter),
+                             PC[pc], int(x0 is not None), C.byref(it), C.byref(rr), C.byref(rt))
+    return x, dict(iters=it.value, rel_res_recursive=rr.value, rel_res_true=rt.value,
+                   status=STATUS[st])
+
+
+def bicgstab(A, b, tol, max_iter=100000, pc="none", x0=None):
+    """Solve a general (nonsymmetric) A x = b by right-preconditioned
+    BiCGStab in fp64; batched like pcg."""
+    if A.vals.ndim == 1:
+        return _bicgstab_one(A, 0, b, tol, max_iter, pc, x0)
+    out = [_bicgstab_one(A, s, b[s], tol, max_iter, pc, None if x0 is None else x0[s])
+           for s in range(A.vals.shape[0])]
+    return np.stack([o[0] for o in out]), [o[1] for o in out]
+
+
+def _bicgstab_adjoint_one(A, s, x, g, tol, max_iter, pc):
+    lib = _load()
+    rp, rpp = _i(A.row_ptr)
+    ci, cip = _i(A.col_idx)
+    v, vp = _d(_system_vals(A, s))
+    xx, xp = _d(x)
+    gg, gp = _d(g)
+    dldb = np.zeros(A.n, dtype=np.float64)
+    dlda = np.zeros(A.nnz, dtype=np.float64)
+    it = C.c_int(0)
+    rr = C.c_double(0)
+    rt = C.c_double(0)
+    st = lib.oracle_bicgstab_adjoint(A.n, rpp, cip, vp, xp, gp, float(tol), int(max_iter), PC[pc],
+                                     dldb.ctypes.data_as(_dp), dlda.ctypes.data_as(_dp),
+                                     C.byref(it), C.byref(rr), C.byref(rt))
+    return dldb, dlda, dict(iters=it.value, rel_res_recursive=rr.value,
+                            rel_res_true=rt.value, status=STATUS[st])
+
+
+def bicgstab_adjoint(A, x, g, tol, max_iter=100000, pc="none"):
+    """(dL/db, dL/dA on the pattern, info) for a general A: A^T lambda = g
+    solved by BiCGStab on the explicit transpose."""
+    if A.vals.ndim == 1:
+        return _bicgstab_adjoint_one(A, 0, x, g, tol, max_iter, pc)
+    out = [_bicgstab_adjoint_one(A, s, x[s], g[s], tol, max_iter, pc)
            for s in range(A.vals.shape[0])]
     return (np.stack([o[0] for o in out]), np.stack([o[1] for o in out]),
             [o[2] for o in out])

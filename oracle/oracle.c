@@ -321,3 +321,114 @@ double oracle_rel_residual(int n, const int* rp, const int* ci, const double* a,
     if (bb == 0.0) return 0.0;
     return sqrt(true_res2(n, rp, ci, a, b, x) / bb);
 }
+
+/*
+ * BiCGStab for a general (nonsymmetric) A x = b, right-preconditioned
+ * (M = diag(A) for pc = OR_PC_JACOBI, M = I for OR_PC_NONE): the algorithm
+ * of van der Vorst (SIAM J. Sci. Stat. Comput. 13(2), 1992) as laid out in
+ * Barrett et al., "Templates for the Solution of Linear Systems" (SIAM,
+ * 1994), section 2.3.8, with the shadow residual r^ = r0.  One iteration is
+ * the pair of products A p^ and A s^.  Stopping as in oracle_pcg: the
+ * recursive residual ||r|| <= tol ||b|| (tested after the x / r update, and
+ * before the first iteration), confirmed on the true residual of the
+ * returned x, otherwise the iteration continues.  omega = (t.s)/(t.t), or 0
+ * when t = 0.  Breakdown: rho = r^.r or sigma = r^.v zero or not finite, a
+ * non-finite ||r||^2, or omega = 0 while the residual test fails.
+ */
+int oracle_bicgstab(int n, const int* rp, const int* ci, const double* a,
+                    const double* b, double* x, double tol, int max_iter, int pc,
+                    int use_x0, int* iters, double* rel_rec, double* rel_true) {
+    if (n < 0 || tol <= 0.0 || max_iter < 0 || (pc != OR_PC_NONE && pc != OR_PC_JACOBI)) return OR_INVALID;
+    size_t sz = sizeof(double) * (size_t)(n > 0 ? n : 1);
+    double *xi = (double*)malloc(sz), *r = (double*)malloc(sz), *rh = (double*)malloc(sz);
+    double *p = (double*)malloc(sz), *ph = (double*)malloc(sz), *v = (double*)malloc(sz);
+    double *s = (double*)malloc(sz), *sh = (double*)malloc(sz), *t = (double*)malloc(sz);
+    double *d = (double*)malloc(sz), *xo = (double*)malloc(sz);
+    int status = OR_OK, k = 0;
+    double gamma = 0.0;
+    double bb = dot(n, b, b);
+    if (pc == OR_PC_JACOBI && !diagonal(n, rp, ci, a, d)) { status = OR_INVALID; goto done; }
+    if (bb == 0.0) {
+        for (int i = 0; i < n; ++i) x[i] = 0.0;
+        if (iters) *iters = 0;
+        if (rel_rec) *rel_rec = 0.0;
+        if (rel_true) *rel_true = 0.0;
+        goto done;
+    }
+    if (use_x0) {
+        for (int i = 0; i < n; ++i) xi[i] = x[i];
+        oracle_spmv(n, rp, ci, a, xi, v);
+        for (int i = 0; i < n; ++i) r[i] = b[i] - v[i];
+    } else {
+        for (int i = 0; i < n; ++i) { xi[i] = 0.0; r[i] = b[i]; }
+    }
+    for (int i = 0; i < n; ++i) { rh[i] = r[i]; p[i] = 0.0; v[i] = 0.0; }
+    gamma = dot(n, r, r);
+    double tol2bb = tol * tol * bb, rho_prev = 1.0, alpha = 1.0, omega = 1.0;
+    for (;;) {
+        if (!isfinite(gamma)) { status = OR_BREAKDOWN; break; }
+        if (gamma <= tol2bb) {
+            for (int i = 0; i < n; ++i) xo[i] = xi[i];
+            if (true_res2(n, rp, ci, a, b, xo) <= tol2bb) { status = OR_OK; break; }
+        } else if (k > 0 && omega == 0.0) {
+            status = OR_BREAKDOWN;
+            break;
+        }
+        if (k >= max_iter) { status = OR_NOT_CONVERGED; break; }
+        double rho = dot(n, rh, r);
+        if (rho == 0.0 || !isfinite(rho)) { status = OR_BREAKDOWN; break; }
+        if (k == 0) {
+            for (int i = 0; i < n; ++i) p[i] = r[i];
+        } else {
+            double beta = (rho / rho_prev) * (alpha / omega);
+            for (int i = 0; i < n; ++i) p[i] = r[i] + beta * (p[i] - omega * v[i]);
+        }
+        for (int i = 0; i < n; ++i) ph[i] = pc == OR_PC_JACOBI ? p[i] / d[i] : p[i];
+        oracle_spmv(n, rp, ci, a, ph, v);
+        double sigma = dot(n, rh, v);
+        if (sigma == 0.0 || !isfinite(sigma)) { status = OR_BREAKDOWN; break; }
+        alpha = rho / sigma;
+        for (int i = 0; i < n; ++i) {
+            s[i] = r[i] - alpha * v[i];
+            sh[i] = pc == OR_PC_JACOBI ? s[i] / d[i] : s[i];
+        }
+        oracle_spmv(n, rp, ci, a, sh, t);
+        double tt = dot(n, t, t), ts = dot(n, t, s);
+        omega = tt > 0.0 ? ts / tt : 0.0;
+        if (!isfinite(omega)) { status = OR_BREAKDOWN; break; }
+        for (int i = 0; i < n; ++i) {
+            xi[i] = xi[i] + alpha * ph[i] + omega * sh[i];
+            r[i] = s[i] - omega * t[i];
+        }
+        gamma = dot(n, r, r);
+        rho_prev = rho;
+        ++k;
+    }
+    for (int i = 0; i < n; ++i) x[i] = xi[i];
+    if (iters) *iters = k;
+    if (rel_rec) *rel_rec = sqrt(gamma / bb);
+    if (rel_true) *rel_true = sqrt(true_res2(n, rp, ci, a, b, x) / bb);
+done:
+    free(xi); free(r); free(rh); free(p); free(ph); free(v); free(s); free(sh); free(t); free(d); free(xo);
+    return status;
+}
+
+/* Adjoint of x = A^-1 b for a general A: solve A^T lambda = g by BiCGStab on
+ * the explicit transpose, then dL/db = lambda and dL/dA_k = -lambda_row(k)
+ * x_col(k) on the stored entries (torch-sla §3.3, adjoint paragraph). */
+int oracle_bicgstab_adjoint(int n, const int* rp, const int* ci, const double* a,
+                            const double* x, const double* g, double tol, int max_iter,
+                            int pc, double* dldb, double* dlda, int* iters,
+                            double* rel_rec, double* rel_true) {
+    int nnz = rp[n];
+    int* trp = (int*)malloc(sizeof(int) * (size_t)(n + 1));
+    int* tci = (int*)malloc(sizeof(int) * (size_t)(nnz > 0 ? nnz : 1));
+    double* ta = (double*)malloc(sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+    transpose(n, rp, ci, a, trp, tci, ta);
+    int st = oracle_bicgstab(n, trp, tci, ta, g, dldb, tol, max_iter, pc, 0, iters, rel_rec, rel_true);
+    if (st != OR_INVALID)
+        for (int i = 0; i < n; ++i)
+            for (int k = rp[i]; k < rp[i + 1]; ++k) dlda[k] = -dldb[i] * x[ci[k]];
+    free(trp); free(tci); free(ta);
+    return st;
+}

@@ -183,3 +183,49 @@ def knn_graph_laplacian(points: np.ndarray, k: int, shift: float, workers: int =
     vals[~is_diag] = -w
     return CSR(n, row_ptr.astype(np.int32), col_idx.astype(np.int32), vals,
                meta={"kind": "knn", "k": k, "h": h, "shift": shift})
+
+
+def convection_diffusion(dims: tuple[int, ...], wind) -> CSR:
+    """Nonsymmetric (2d+1)-point convection-diffusion operator on an interior
+    grid: the unscaled Dirichlet Laplacian plus first-order upwind convection.
+
+    wind[a] is the scaled velocity h * beta_a along axis a, a scalar or an
+    array [n] (one value per unknown).  Along axis a the upwind neighbour
+    (the one at -1 for wind >= 0, at +1 for wind < 0) gets -1 - |wind_a|, the
+    other neighbour -1, and the diagonal 2d + sum_a |wind_a|.  Rows are
+    weakly diagonally dominant with strict dominance next to the boundary,
+    so A is a nonsingular M-matrix; wind = 0 gives poisson_grid exactly."""
+    d = len(dims)
+    n = int(np.prod(dims))
+    idx = np.arange(n, dtype=np.int64)
+    coords = np.unravel_index(idx, dims[::-1])[::-1]
+    strides = [int(np.prod(dims[:a])) for a in range(d)]
+    w = [np.broadcast_to(np.asarray(wind[a], dtype=np.float64), (n,)) for a in range(d)]
+    offs = _grid_offsets(dims)
+    cols, vals, valid = [], [], []
+
+    def entry(a, s):
+        upwind = np.where(w[a] >= 0.0, s < 0, s > 0)
+        return np.where(upwind, -1.0 - np.abs(w[a]), -1.0)
+
+    lower = [(a, s) for (a, s) in offs if s * strides[a] < 0]
+    upper = [(a, s) for (a, s) in offs if s * strides[a] > 0]
+    for (a, s) in lower:
+        cols.append(idx + s * strides[a]); vals.append(entry(a, s)); valid.append(coords[a] + s >= 0)
+    cols.append(idx); vals.append(2.0 * d + sum(np.abs(wa) for wa in w)); valid.append(np.ones(n, bool))
+    for (a, s) in upper:
+        cols.append(idx + s * strides[a]); vals.append(entry(a, s)); valid.append(coords[a] + s < dims[a])
+    rp, ci, v = _from_masked_stencil(n, np.stack(cols, 1), np.stack(vals, 1), np.stack(valid, 1))
+    return CSR(n, rp, ci, np.ascontiguousarray(v), meta={"kind": "convdiff", "dims": tuple(dims)})
+
+
+def rotating_wind(dims: tuple[int, int], peclet: float) -> tuple[np.ndarray, np.ndarray]:
+    """Scaled velocity (h beta_x, h beta_y) of the solid-body rotation about
+    the centre of an N x M grid, |h beta| up to `peclet` at the corners' mid
+    edges: beta = (-(y - 1/2), x - 1/2) * 2 peclet."""
+    Nx, Ny = dims
+    n = Nx * Ny
+    idx = np.arange(n, dtype=np.int64)
+    x = (idx % Nx + 1.0) / (Nx + 1.0)
+    y = (idx // Nx + 1.0) / (Ny + 1.0)
+    return -(y - 0.5) * 2.0 * peclet, (x - 0.5) * 2.0 * peclet
