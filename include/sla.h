@@ -207,6 +207,41 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
                        void* d_dLdb, void* d_dLdA, sla_solve_info* info, void* stream);
 
 /*
+ * Solve a general (nonsymmetric) A x = b by BiCGStab (van der Vorst 1992;
+ * the right-preconditioned form of Barrett et al., "Templates for the
+ * Solution of Linear Systems", §2.3.8, shadow residual r^ = r0) -- the
+ * nonsymmetric Krylov solver of torch-sla's iterative backends (§3.1).
+ *  - fp64 handles only (SLA_ERR_UNSUPPORTED for fp32).  opts->pc is
+ *    SLA_PC_NONE or SLA_PC_JACOBI (right preconditioning by diag(A), which
+ *    must be stored; applied as the column scaling A diag(A)^-1 of a
+ *    handle-owned copy of the values); SLA_PC_SPAI is SLA_ERR_INVALID.
+ *    opts->eps is ignored.
+ *  - Layout, batching, x0, polling, reordering and timeout as for
+ *    sla_pcg_solve; info[s].iters counts BiCGStab iterations (two products
+ *    each).  Stopping: ||r|| <= tol ||b|| on the recursive residual,
+ *    confirmed on the true residual of x before returning SLA_OK.
+ *  - SLA_ERR_BREAKDOWN when r^.r or r^.v is zero or not finite, or when
+ *    omega = (t.s)/(t.t) is zero while the residual test fails.
+ *  - The first call allocates the shadow residual (and, for Jacobi, a copy
+ *    of the values: batch x nnz doubles); later calls allocate nothing.
+ */
+sla_status sla_bicgstab_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg_opts* opts,
+                              sla_solve_info* info, void* stream);
+
+/*
+ * Adjoint of x = A^-1 b for a general A (torch-sla §3.3, adjoint
+ * paragraph): solves A^T lambda = g by BiCGStab on an explicit transpose of
+ * A -- its pattern built on the host at the first call and kept by the
+ * handle, its values gathered from the current values on every call -- then
+ * writes dL/db = lambda into d_dLdb and dL/dA_k = -lambda_row(k) x_col(k)
+ * into d_dLdA (NULL skips it), as sla_adjoint.  Options and errors as for
+ * sla_bicgstab_solve (use_x0 is ignored).  The transpose costs
+ * nnz ints x 3 plus batch x nnz doubles of device memory.
+ */
+sla_status sla_bicgstab_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla_pcg_opts* opts,
+                                void* d_dLdb, void* d_dLdA, sla_solve_info* info, void* stream);
+
+/*
  * Allocation-free y = A x and d_dot[s] = x_s . y_s (the same fused kernel as
  * sla_spmv_dot), without a handle.  The pages have no counterpart: this entry
  * point exists for callers that cannot let a library allocate device

@@ -68,6 +68,12 @@ def launch_count() -> int:
     return int(_lib_handle().sla_launch_count())
 
 
+def _method(method: str, cg: str, bicgstab: str):
+    if method not in ("cg", "bicgstab"):
+        raise ValueError(f"method must be 'cg' or 'bicgstab', not {method!r}")
+    return getattr(_lib_handle(), cg if method == "cg" else bicgstab)
+
+
 class CSRMatrix:
     """A CSR matrix (or a batch of matrices sharing one pattern) on the GPU.
 
@@ -191,8 +197,10 @@ class CSRMatrix:
 
     def solve(self, b: torch.Tensor, tol: float = 1e-8, max_iter: int = 10000, pc: str = "none",
               eps: float = 1e-3, poll_k: int = 32, x0: torch.Tensor | None = None,
-              timeout_s: float = 0.0, raise_on_fail: bool = False, stream=None):
-        """Solve A x = b by PCG; returns (x, [SolveInfo per system])."""
+              timeout_s: float = 0.0, raise_on_fail: bool = False, method: str = "cg", stream=None):
+        """Solve A x = b; returns (x, [SolveInfo per system]).  method "cg":
+        preconditioned CG (symmetric positive definite A); "bicgstab":
+        BiCGStab for a general A (fp64; pc "none" or "jacobi")."""
         self._check_vec(b, "b")
         if x0 is not None:
             self._check_vec(x0, "x0")
@@ -201,23 +209,26 @@ class CSRMatrix:
             x = torch.empty_like(b)
         o = self._opts(tol, max_iter, pc, eps, poll_k, x0 is not None, timeout_s)
         info = (_lib.SolveInfo * self.batch)()
-        st = _lib_handle().sla_pcg_solve(self._h, _ptr(b), _ptr(x), C.byref(o), info, _stream(stream))
+        fn = _method(method, "sla_pcg_solve", "sla_bicgstab_solve")
+        st = fn(self._h, _ptr(b), _ptr(x), C.byref(o), info, _stream(stream))
         _check(st, allow=() if raise_on_fail else (_lib.SLA_ERR_NOT_CONVERGED, _lib.SLA_ERR_BREAKDOWN,
                                                    _lib.SLA_ERR_TIMEOUT))
         return x, self._infos(info)
 
     def adjoint(self, x: torch.Tensor, g: torch.Tensor, tol: float = 1e-8, max_iter: int = 10000,
                 pc: str = "none", eps: float = 1e-3, poll_k: int = 32, want_dA: bool = True,
-                timeout_s: float = 0.0, stream=None):
-        """(dL/db, dL/dA on the pattern or None, [SolveInfo]) for g = dL/dx."""
+                timeout_s: float = 0.0, method: str = "cg", stream=None):
+        """(dL/db, dL/dA on the pattern or None, [SolveInfo]) for g = dL/dx.
+        method "bicgstab" solves A^T lambda = g on an explicit transpose."""
         self._check_vec(x, "x")
         self._check_vec(g, "g")
         dldb = torch.empty_like(g)
         dlda = torch.empty_like(self.values) if want_dA else None
         o = self._opts(tol, max_iter, pc, eps, poll_k, False, timeout_s)
         info = (_lib.SolveInfo * self.batch)()
-        st = _lib_handle().sla_adjoint(self._h, _ptr(x), _ptr(g), C.byref(o), _ptr(dldb),
-                                       _ptr(dlda) if dlda is not None else None, info, _stream(stream))
+        fn = _method(method, "sla_adjoint", "sla_bicgstab_adjoint")
+        st = fn(self._h, _ptr(x), _ptr(g), C.byref(o), _ptr(dldb), _ptr(dlda) if dlda is not None else None, info,
+                _stream(stream))
         _check(st, allow=(_lib.SLA_ERR_NOT_CONVERGED, _lib.SLA_ERR_BREAKDOWN, _lib.SLA_ERR_TIMEOUT))
         return dldb, dlda, self._infos(info)
 
@@ -236,7 +247,8 @@ class _Solve(torch.autograd.Function):
     @staticmethod
     def backward(ctx, gx):
         (x,) = ctx.saved_tensors
-        kw = {k: v for k, v in ctx.kw.items() if k in ("tol", "max_iter", "pc", "eps", "poll_k", "timeout_s")}
+        kw = {k: v for k, v in ctx.kw.items()
+              if k in ("tol", "max_iter", "pc", "eps", "poll_k", "timeout_s", "method")}
         dldb, dlda, _ = ctx.A.adjoint(x, gx.contiguous(), want_dA=ctx.needs_input_grad[0], **kw)
         return (dlda if ctx.needs_input_grad[0] else None,
                 dldb if ctx.needs_input_grad[1] else None, None, None)
@@ -245,5 +257,6 @@ class _Solve(torch.autograd.Function):
 def solve(A: CSRMatrix, values: torch.Tensor, b: torch.Tensor, **kw) -> torch.Tensor:
     """x = A(values)^-1 b, differentiable with respect to values and b: the
     backward pass is one adjoint solve (A^T lambda = dL/dx) plus
-    dL/dA_ij = -lambda_i x_j on the stored entries."""
+    dL/dA_ij = -lambda_i x_j on the stored entries.  method="bicgstab"
+    (keyword) serves a nonsymmetric A, forward and adjoint."""
     return _Solve.apply(values, b, A, kw)

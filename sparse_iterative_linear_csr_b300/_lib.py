@@ -27,7 +27,8 @@ SLA_NO_REORDER = 64
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
-           "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time", "sla_spmm"]
+           "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_bicgstab_solve",
+           "sla_bicgstab_adjoint"]
 
 
 class PcgOpts(C.Structure):
@@ -65,6 +66,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_spmv_dot.argtypes = [_vp, _vp, _vp, _vp, _vp]
     lib.sla_pcg_solve.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), C.POINTER(SolveInfo), _vp]
     lib.sla_adjoint.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), _vp, _vp, C.POINTER(SolveInfo), _vp]
+    lib.sla_bicgstab_solve.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), C.POINTER(SolveInfo), _vp]
+    lib.sla_bicgstab_adjoint.argtypes = [_vp, _vp, _vp, C.POINTER(PcgOpts), _vp, _vp, C.POINTER(SolveInfo),
+                                         _vp]
     lib.sla_csr_destroy.argtypes = [_vp]
     lib.sla_last_error.argtypes = []
     lib.sla_last_error.restype = C.c_char_p
@@ -75,7 +79,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
     for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
-              "sla_adjoint", "sla_csr_destroy"]:
+              "sla_adjoint", "sla_bicgstab_solve", "sla_bicgstab_adjoint", "sla_csr_destroy"]:
         getattr(lib, f).restype = C.c_int
     _lib = lib
     return lib

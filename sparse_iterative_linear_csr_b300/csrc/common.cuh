@@ -43,7 +43,8 @@ struct State {
     double bb;        // b.b
     double tol2bb;    // tol^2 * b.b
     double tr2;       // ||b - A x||^2 of the last true-residual check
-    double delta;     // p.q of the last iteration
+    double delta;     // p.q of the last iteration (BiCGStab: r^.v)
+    double omega;     // BiCGStab: the stabilising step (t.s) / (t.t)
     int iter;         // products A p done in the loop
     int max_iter;
     int done;         // 1: frozen (converged, not converged at cap, or breakdown)

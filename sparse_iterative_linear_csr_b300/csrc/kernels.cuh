@@ -833,7 +833,7 @@ __device__ __forceinline__ void start_state(State* s, Ctrl* c, double bb, double
     s->rho_bad = 0;
     s->phase = 0;
     s->xpend = 0;
-    s->alpha = s->beta = s->rho = s->delta = s->tr2 = 0.0;
+    s->alpha = s->beta = s->rho = s->delta = s->tr2 = s->omega = 0.0;
     if (bb == 0.0) { freeze(s, c, ST_OK); return; }   // x = 0 is exact
     if (!finite(gamma)) { freeze(s, c, ST_BREAKDOWN); return; }
     s->check = (gamma <= s->tol2bb);

@@ -24,6 +24,7 @@
 #include "../../include/sla.h"
 #include "common.cuh"
 #include "kernels.cuh"
+#include "bicgstab.cuh"
 #include "setup.cuh"
 
 using namespace sla;
@@ -186,7 +187,21 @@ struct sla_csr {
     Stat* h_stat = nullptr;    // pinned [batch]
     cudaEvent_t ev[2] = {nullptr, nullptr};
     cudaStream_t cap = nullptr;  // capture stream
-    GraphCache graph[3];
+    // graphs: CG per preconditioner (0..2), BiCGStab on A / A^T per
+    // preconditioner (3 + 2 * transposed + pc)
+    GraphCache graph[7];
+
+    // BiCGStab (built on first use): the iteration matrix's layout with the
+    // register / cp.async forms only (its values may be a handle-owned
+    // scaled copy), the shadow residual, the column-scaled values A D^-1;
+    // for the adjoint the explicit transpose of the iteration matrix (pattern,
+    // source entry of every transposed entry, values per system) and its layout.
+    bool bicg_ready = false;
+    Layout LB;
+    DevBuf rh, bvals;
+    bool tr_ready = false;
+    Layout LT;
+    DevBuf trp, tci, tsrc, tvals;
 };
 
 static constexpr size_t WORK_BYTES = 8;  // working vectors: fp64, or a double-float pair
@@ -256,6 +271,14 @@ static sla_status allow_smem_form(int b) {
     return SLA_OK;
 }
 
+// BiCGStab product kernels (fp64; register and cp.async staging forms).
+template <int F>
+static sla_status allow_smem_bicg(int b) {
+    CU(cudaFuncSetAttribute(k_bicg_v<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    CU(cudaFuncSetAttribute(k_bicg_t<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+    return SLA_OK;
+}
+
 static constexpr int SMEM_CTA_MAX = 222 * 1024;   // dynamic shared memory a CTA may use (227 KB less static)
 static constexpr size_t SMEM_SM = 228 * 1024;     // shared memory per SM
 static constexpr size_t SMEM_CTA_RESERVE = 6144;  // per-CTA system reserve + static shared memory
@@ -287,6 +310,11 @@ static sla_status allow_smem() {
     CU(cudaFuncSetAttribute(k_init_x0<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
     CU(cudaFuncSetAttribute(k_final<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
     CU(cudaFuncSetAttribute(k_grad_A<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CTA_MAX));
+    if constexpr (std::is_same<T, double>::value) {
+        TRY((allow_smem_bicg<0>(b)));
+        TRY((allow_smem_bicg<1>(b)));
+        TRY((allow_smem_bicg<2>(b)));
+    }
     done.store(1);
     return SLA_OK;
 }
@@ -812,6 +840,8 @@ static sla_status ensure_pstride(sla_csr* h) {
         m = m > h->LG.gx ? m : h->LG.gx;
         m = m > h->LGT.gx ? m : h->LGT.gx;
     }
+    if (h->bicg_ready) m = m > h->LB.gx ? m : h->LB.gx;
+    if (h->tr_ready) m = m > h->LT.gx ? m : h->LT.gx;
     const int need = 4 * m;
     if (need <= h->pstride) return SLA_OK;
     TRY(h->part.alloc(sizeof(double) * (size_t)need * h->batch));
@@ -886,26 +916,26 @@ static sla_status enqueue_iteration_any(sla_csr* h, int pc, double eps, cudaStre
                        : enqueue_iteration<T, false>(h, pc, eps, s, nodes, ev0, ev1);
 }
 
-template <typename T>
-static sla_status get_graph(sla_csr* h, int pc, double eps, int k, GraphCache** out) {
-    GraphCache& gc = h->graph[pc];
-    if (gc.exec[0] && gc.k == k && gc.eps == eps) { *out = &gc; return SLA_OK; }
+// Capture k iterations into gc (enq(stream, &nodes, ev0, ev1) enqueues one,
+// recording ev0 / ev1 around its product kernel when they are given): one
+// instance per launch slot when `timed`, with events around the middle
+// iteration's product (clear of the graph launch's own start-up), else one.
+template <class Enq>
+static sla_status capture_graph(sla_csr* h, GraphCache& gc, int k, double eps, bool timed, Enq enq) {
+    if (gc.exec[0] && gc.k == k && gc.eps == eps) return SLA_OK;
     gc.reset();
-    const int inst = h->time_product ? 2 : 1;
+    const int inst = timed ? 2 : 1;
     int nodes = 0;
     for (int slot = 0; slot < inst; ++slot) {
-        if (h->time_product) {
+        if (timed) {
             CU(cudaEventCreate(&gc.t0[slot]));
             CU(cudaEventCreate(&gc.t1[slot]));
         }
         CU(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal));
         nodes = 0;
         sla_status st = SLA_OK;
-        // the timed product is the middle iteration's, clear of the graph
-        // launch's own start-up
         for (int i = 0; i < k && st == SLA_OK; ++i)
-            st = enqueue_iteration_any<T>(h, pc, eps, h->cap, &nodes, i == k / 2 ? gc.t0[slot] : nullptr,
-                                          i == k / 2 ? gc.t1[slot] : nullptr);
+            st = enq(h->cap, &nodes, i == k / 2 ? gc.t0[slot] : nullptr, i == k / 2 ? gc.t1[slot] : nullptr);
         cudaGraph_t graph = nullptr;
         cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
         // launches made during capture were counted; they only run when the graph does
@@ -930,6 +960,16 @@ static sla_status get_graph(sla_csr* h, int pc, double eps, int k, GraphCache** 
     gc.k = k;
     gc.eps = eps;
     gc.nodes = nodes;
+    return SLA_OK;
+}
+
+template <typename T>
+static sla_status get_graph(sla_csr* h, int pc, double eps, int k, GraphCache** out) {
+    GraphCache& gc = h->graph[pc];
+    TRY(capture_graph(h, gc, k, eps, h->time_product,
+                      [&](cudaStream_t s, int* nodes, cudaEvent_t e0, cudaEvent_t e1) {
+                          return enqueue_iteration_any<T>(h, pc, eps, s, nodes, e0, e1);
+                      }));
     *out = &gc;
     return SLA_OK;
 }
@@ -1001,6 +1041,99 @@ static sla_status from_code(int c) {
         case ST_NOT_CONVERGED: return SLA_ERR_NOT_CONVERGED;
         default: return SLA_ERR_BREAKDOWN;
     }
+}
+
+// Run the iteration in batches -- launch(slot) issues one: a graph of k
+// iterations or one persistent kernel -- two in flight, reading the
+// device's all-frozen flag after each, until it is set, cap_launches
+// batches have run or the host timeout has passed; then drain the stream.
+// With gc set, the product-kernel time of every launch during which some
+// system stayed live throughout is summed into the handle.
+template <class Launch>
+static sla_status poll_loop(sla_csr* h, const sla_pcg_opts* o, long long cap_launches, GraphCache* gc,
+                            cudaStream_t s, bool* finished_out, bool* timed_out_out, Launch launch) {
+    const auto t0 = std::chrono::steady_clock::now();
+    int head = 0, inflight = 0;
+    long long issued = 0;
+    bool finished = false, timed_out = false;
+    bool prev_done = false;   // the launch before the oldest in flight left every system frozen
+    while (!finished) {
+        if (issued < cap_launches && !timed_out) {
+            const int slot = (head + inflight) & 1;
+            TRY(launch(slot));
+            CU(cudaMemcpyAsync(&h->h_flag[slot], &h->ctl.as<Ctrl>()->all_done, sizeof(int),
+                               cudaMemcpyDeviceToHost, s));
+            CU(cudaEventRecord(h->ev[slot], s));
+            ++inflight;
+            ++issued;
+            if (inflight < 2) continue;
+        }
+        if (inflight == 0) break;
+        // wait for the oldest launch
+        const int slot = head;
+        if (o->timeout_s > 0) {
+            for (;;) {
+                cudaError_t q = cudaEventQuery(h->ev[slot]);
+                if (q == cudaSuccess) break;
+                if (q != cudaErrorNotReady) return fail(SLA_ERR_CUDA, "event query: %s", cudaGetErrorString(q));
+                const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+                if (el > o->timeout_s) timed_out = true;
+                std::this_thread::sleep_for(std::chrono::microseconds(50));
+            }
+        } else {
+            CU(cudaEventSynchronize(h->ev[slot]));
+        }
+        if (gc && !prev_done && !h->h_flag[slot]) {   // live systems from start to end
+            float ms = 0.0f;
+            CU(cudaEventElapsedTime(&ms, gc->t0[slot], gc->t1[slot]));
+            h->prod_ms += ms;
+            h->prod_n += 1;
+        }
+        prev_done = h->h_flag[slot] != 0;
+        head ^= 1;
+        --inflight;
+        if (h->h_flag[slot]) finished = true;
+        if ((issued >= cap_launches || timed_out) && inflight == 0) break;
+    }
+    // drain (kernels of a finished batch return at once)
+    CU(cudaStreamSynchronize(s));
+    *finished_out = finished;
+    *timed_out_out = timed_out;
+    return SLA_OK;
+}
+
+// After the final pass (k_final) is enqueued: device error bits, then the
+// per-system statistics into info[] and the call's status.
+static sla_status collect(sla_csr* h, bool finished, bool timed_out, const sla_pcg_opts* o, sla_solve_info* info,
+                          cudaStream_t s, const char* breakdown_msg) {
+    CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
+    Ctrl dc;
+    CU(cudaMemcpyAsync(&dc, h->ctl.p, sizeof(Ctrl), cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+    if (dc.err & ERR_STAGE) return fail(SLA_ERR_CUDA, "a staged range exceeded its stage; results invalid");
+    if (dc.err & (ERR_WAIT | ERR_GRID))
+        return fail(SLA_ERR_CUDA, "a device wait gave up (%s; at %d: %d %d %d); results invalid",
+                    (dc.err & ERR_GRID) ? "grid barrier" : "bulk copy", dc.diag[0], dc.diag[1], dc.diag[2],
+                    dc.diag[3]);
+
+    sla_status ret = SLA_OK;
+    for (int i = 0; i < h->batch; ++i) {
+        const Stat& st = h->h_stat[i];
+        sla_status si = from_code(st.status);
+        if (!st.done) si = timed_out ? SLA_ERR_TIMEOUT : SLA_ERR_NOT_CONVERGED;  // host stopped first
+        if (info) {
+            info[i].iters = st.iters;
+            info[i].rel_res_recursive = st.rel_rec;
+            info[i].rel_res_true = st.rel_true;
+            info[i].status = si;
+        }
+        if (ret == SLA_OK && si != SLA_OK) ret = si;
+    }
+    if (!finished && !timed_out)
+        return fail(SLA_ERR_NOT_CONVERGED, "iteration launches exhausted before the device froze");
+    if (ret == SLA_ERR_TIMEOUT) return fail(ret, "timeout after %.3f s", o->timeout_s);
+    if (ret != SLA_OK) fail(ret, ret == SLA_ERR_BREAKDOWN ? breakdown_msg : "not converged within max_iter");
+    return ret;
 }
 
 template <typename T>
@@ -1077,92 +1210,192 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     }
     TRY(launched());
 
-    // iterate: graph launches of k iterations, two in flight, poll the flag
-    const auto t0 = std::chrono::steady_clock::now();
     const long long cap_launches = ((long long)o->max_iter + 2LL * k + 2) / k + 2;
-    int head = 0, inflight = 0;
-    long long issued = 0;
-    bool finished = false, timed_out = false;
     const bool timing = !fused && h->time_product;
-    bool prev_done = false;   // the launch before the oldest in flight left every system frozen
-    while (!finished) {
-        if (issued < cap_launches && !timed_out) {
-            const int slot = (head + inflight) & 1;
-            if (fused) {
-                TRY(launch_fused_any<T>(h, pc, gxf, k, s));
-            } else {
-                CU(cudaGraphLaunch(gc->exec[timing ? slot : 0], s));
-                g_launches.fetch_add((unsigned long long)gc->nodes, std::memory_order_relaxed);
-            }
-            CU(cudaMemcpyAsync(&h->h_flag[slot], &h->ctl.as<Ctrl>()->all_done, sizeof(int),
-                               cudaMemcpyDeviceToHost, s));
-            CU(cudaEventRecord(h->ev[slot], s));
-            ++inflight;
-            ++issued;
-            if (inflight < 2) continue;
-        }
-        if (inflight == 0) break;
-        // wait for the oldest launch
-        const int slot = head;
-        if (o->timeout_s > 0) {
-            for (;;) {
-                cudaError_t q = cudaEventQuery(h->ev[slot]);
-                if (q == cudaSuccess) break;
-                if (q != cudaErrorNotReady) return fail(SLA_ERR_CUDA, "event query: %s", cudaGetErrorString(q));
-                const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
-                if (el > o->timeout_s) timed_out = true;
-                std::this_thread::sleep_for(std::chrono::microseconds(50));
-            }
-        } else {
-            CU(cudaEventSynchronize(h->ev[slot]));
-        }
-        if (timing && !prev_done && !h->h_flag[slot]) {   // live systems from start to end
-            float ms = 0.0f;
-            CU(cudaEventElapsedTime(&ms, gc->t0[slot], gc->t1[slot]));
-            h->prod_ms += ms;
-            h->prod_n += 1;
-        }
-        prev_done = h->h_flag[slot] != 0;
-        head ^= 1;
-        --inflight;
-        if (h->h_flag[slot]) finished = true;
-        if ((issued >= cap_launches || timed_out) && inflight == 0) break;
-    }
-    // drain (kernels of a finished batch return at once)
-    CU(cudaStreamSynchronize(s));
+    bool finished = false, timed_out = false;
+    TRY(poll_loop(h, o, cap_launches, timing ? gc : nullptr, s, &finished, &timed_out, [&](int slot) {
+        if (fused) return launch_fused_any<T>(h, pc, gxf, k, s);
+        CU(cudaGraphLaunch(gc->exec[timing ? slot : 0], s));
+        g_launches.fetch_add((unsigned long long)gc->nodes, std::memory_order_relaxed);
+        return SLA_OK;
+    }));
 
     k_final<T><<<gs, NT, h->LI.smem, s>>>(A, S, av, x, h->bw.as<T>(), x_it, h->stat.as<Stat>());
     TRY(launched());
     if (h->reordered) TRY(gather_map(sizeof(T), h->n, h->batch, h->iperm.as<int>(), x_it, h->n, x_user, h->n, s));
-    CU(cudaMemcpyAsync(h->h_stat, h->stat.p, sizeof(Stat) * h->batch, cudaMemcpyDeviceToHost, s));
-    Ctrl dc;
-    CU(cudaMemcpyAsync(&dc, h->ctl.p, sizeof(Ctrl), cudaMemcpyDeviceToHost, s));
-    CU(cudaStreamSynchronize(s));
-    if (dc.err & ERR_STAGE) return fail(SLA_ERR_CUDA, "a staged range exceeded its stage; results invalid");
-    if (dc.err & (ERR_WAIT | ERR_GRID))
-        return fail(SLA_ERR_CUDA, "a device wait gave up (%s; at %d: %d %d %d); results invalid",
-                    (dc.err & ERR_GRID) ? "grid barrier" : "bulk copy", dc.diag[0], dc.diag[1], dc.diag[2],
-                    dc.diag[3]);
+    return collect(h, finished, timed_out, o, info, s, "breakdown (p.Ap <= 0, r.z <= 0 or non-finite value)");
+}
 
-    sla_status ret = SLA_OK;
-    for (int i = 0; i < h->batch; ++i) {
-        const Stat& st = h->h_stat[i];
-        sla_status si = from_code(st.status);
-        if (!st.done) si = timed_out ? SLA_ERR_TIMEOUT : SLA_ERR_NOT_CONVERGED;  // host stopped first
-        if (info) {
-            info[i].iters = st.iters;
-            info[i].rel_res_recursive = st.rel_rec;
-            info[i].rel_res_true = st.rel_true;
-            info[i].status = si;
-        }
-        if (ret == SLA_OK && si != SLA_OK) ret = si;
+// ===================================================================== BiCGStab
+// Dispatch over the register / cp.async staging forms (the BiCGStab product
+// kernels are built for these only).
+template <class F>
+static void with_form_rc(int form, F&& f) {
+    switch (form) {
+        case 0: f(std::integral_constant<int, 0>{}); break;
+        case 1: f(std::integral_constant<int, 1>{}); break;
+        default: f(std::integral_constant<int, 2>{}); break;
     }
-    if (!finished && !timed_out)
-        return fail(SLA_ERR_NOT_CONVERGED, "iteration launches exhausted before the device froze");
-    if (ret == SLA_ERR_TIMEOUT) return fail(ret, "timeout after %.3f s", o->timeout_s);
-    if (ret != SLA_OK) fail(ret, ret == SLA_ERR_BREAKDOWN ? "breakdown (p.Ap <= 0, r.z <= 0 or non-finite value)"
-                                                          : "not converged within max_iter");
-    return ret;
+}
+
+// Pattern of M^T: row j lists the rows i of the entries (i, j) of M in
+// ascending order; src[k'] = the entry of M that transposed entry k' holds.
+static void transpose_pattern(int n, const std::vector<int>& rp, const std::vector<int>& ci, std::vector<int>& trp,
+                              std::vector<int>& tci, std::vector<int>& src) {
+    trp.assign(n + 1, 0);
+    for (size_t k = 0; k < ci.size(); ++k) trp[ci[k] + 1] += 1;
+    for (int j = 0; j < n; ++j) trp[j + 1] += trp[j];
+    std::vector<int> next(trp.begin(), trp.end() - 1);
+    tci.resize(ci.size());
+    src.resize(ci.size());
+    for (int i = 0; i < n; ++i)
+        for (int k = rp[i]; k < rp[i + 1]; ++k) {
+            const int d = next[ci[k]]++;
+            tci[d] = i;
+            src[d] = k;
+        }
+}
+
+// Workspace of BiCGStab (and, for `transposed`, the explicit transpose of
+// the iteration matrix); built once per handle.
+static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
+    if (!h->bicg_ready) {
+        TRY(h->rh.alloc(sizeof(double) * (size_t)h->n * h->batch));
+        h->LB = h->LI;
+        TRY(set_form_any(h, &h->LB, false, sizeof(double)));
+        h->bicg_ready = true;
+    }
+    if (transposed && !h->tr_ready) {
+        std::vector<int> rp, ci, trp, tci, src;
+        CU(cudaStreamSynchronize(s));
+        TRY(to_host(rp, h->irp, (size_t)h->n + 1));
+        TRY(to_host(ci, h->ici, (size_t)h->nnz));
+        transpose_pattern(h->n, rp, ci, trp, tci, src);
+        TRY(to_device(h->trp, trp));
+        TRY(to_device(h->tci, tci));
+        TRY(to_device(h->tsrc, src));
+        TRY(h->tvals.alloc(sizeof(double) * (size_t)h->nnz * h->batch));
+        TRY(choose_layout(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, &h->LT, false, sizeof(double), s));
+        h->tr_ready = true;
+    }
+    return ensure_pstride(h);
+}
+
+// One BiCGStab iteration on the matrix (M, av): five kernels.
+template <int W>
+static sla_status enqueue_bicg(sla_csr* h, const Mat& M, const Layout& L, const double* av, cudaStream_t s,
+                               int* nodes) {
+    const Sys S = sys_of(h);
+    double* y = h->x.as<double>();
+    double* r = h->r.as<double>();   // r, and s over it
+    double* p = h->p.as<double>();
+    double* v = h->q.as<double>();
+    double* t = h->z.as<double>();
+    const double* rh = h->rh.as<double>();
+    const dim3 gs(L.gx, h->batch), gv(gx_vec(h), h->batch);
+    with_form_rc(L.form, [&](auto f) {
+        k_bicg_v<decltype(f)::value><<<gs, NT, L.smem, s>>>(M, S, av, p, v, rh, y, h->bw.as<double>());
+    });
+    TRY(launched());
+    k_bicg_s<W><<<gv, NT, 0, s>>>(S, r, v);
+    TRY(launched());
+    with_form_rc(L.form, [&](auto f) { k_bicg_t<decltype(f)::value><<<gs, NT, L.smem, s>>>(M, S, av, r, t); });
+    TRY(launched());
+    k_bicg_xr<W><<<gv, NT, 0, s>>>(S, y, p, r, t, rh);
+    TRY(launched());
+    k_bicg_p<W><<<gv, NT, 0, s>>>(S, p, r, v);
+    TRY(launched());
+    *nodes += 5;
+    return SLA_OK;
+}
+
+// Solve A x = b (transposed: A^T x = b) by BiCGStab on the iteration matrix
+// (P A P^T when the handle reorders; b and x are permuted in and out).
+static sla_status bicg_impl(sla_csr* h, bool transposed, const double* b, double* x_user, const sla_pcg_opts* o,
+                            sla_solve_info* info, cudaStream_t s) {
+    const int pc = (int)o->pc;
+    if (pc == SLA_PC_JACOBI && (h->diag_err & ERR_NO_DIAG))
+        return fail(SLA_ERR_INVALID, "Jacobi needs every diagonal entry stored");
+    TRY(ensure_bicg(h, transposed, s));
+    const int k = o->poll_k > 0 ? o->poll_k : 32;
+    const Sys S = sys_of(h);
+    int* err = &h->ctl.as<Ctrl>()->err;
+    // the matrix as stored (initial residual, final check) and as iterated
+    const int* mrp = transposed ? h->trp.as<int>() : h->irp;
+    const int* mci = transposed ? h->tci.as<int>() : h->ici;
+    const Layout& L = transposed ? h->LT : h->LB;
+    const Mat M = mat_of(mrp, mci, h->n, h->nnz, L, err);
+    const double* uv = (const double*)h->ivals;
+    if (transposed) {
+        TRY(gather_map(8, h->nnz, h->batch, h->tsrc.as<int>(), h->ivals, h->nnz, h->tvals.p, h->nnz, s));
+        uv = h->tvals.as<double>();
+    }
+    const double* itv = uv;
+    if (pc == SLA_PC_JACOBI) {
+        if (!h->bvals.p) {
+            TRY(h->bvals.alloc(sizeof(double) * (size_t)h->nnz * h->batch));
+            for (int g = 3; g < 7; ++g) h->graph[g].reset();
+        }
+        if (h->nnz > 0) {
+            const long long blocks = (h->nnz + NT - 1) / NT;
+            const dim3 gsc((unsigned)std::min<long long>(blocks, 4096), h->batch);
+            k_bicg_colscale<<<gsc, NT, 0, s>>>(h->nnz, h->n, mci, uv, h->diag.as<double>(), h->bvals.as<double>());
+            TRY(launched());
+        }
+        itv = h->bvals.as<double>();
+    }
+    GraphCache& gc = h->graph[3 + 2 * (transposed ? 1 : 0) + (pc == SLA_PC_JACOBI ? 1 : 0)];
+    TRY(capture_graph(h, gc, k, 0.0, false, [&](cudaStream_t cs, int* nodes, cudaEvent_t, cudaEvent_t) {
+        return pairs_ok(h) ? enqueue_bicg<2>(h, M, L, itv, cs, nodes) : enqueue_bicg<1>(h, M, L, itv, cs, nodes);
+    }));
+
+    const dim3 gs(L.gx, h->batch), gv(gx_vec(h), h->batch);
+    double* x = h->x.as<double>();
+    double* r = h->r.as<double>();
+    CU(cudaMemsetAsync(h->ctl.p, 0, sizeof(Ctrl), s));
+    const double* b_it = b;
+    const double* x0_it = x_user;
+    double* x_it = x_user;
+    if (h->reordered) {
+        double* tb = h->ptmp.as<double>();
+        double* tx = tb + (size_t)h->batch * h->n;
+        TRY(gather_map(8, h->n, h->batch, h->perm.as<int>(), b, h->n, tb, h->n, s));
+        if (o->use_x0) TRY(gather_map(8, h->n, h->batch, h->perm.as<int>(), x_user, h->n, tx, h->n, s));
+        b_it = tb;
+        x0_it = tx;
+        x_it = tx;
+    }
+    if (o->use_x0) {
+        k_init_x0<double><<<gs, NT, L.smem, s>>>(M, S, uv, b_it, x0_it, h->bw.as<double>(), x, r, o->tol,
+                                                 o->max_iter);
+    } else {
+        k_init<double><<<gv, NT, 0, s>>>(S, b_it, h->bw.as<double>(), x, r, o->tol, o->max_iter);
+    }
+    TRY(launched());
+    if (pc == SLA_PC_JACOBI && o->use_x0) {   // y = D x0
+        k_bicg_scale<true><<<gv, NT, 0, s>>>(S, x, h->diag.as<double>());
+        TRY(launched());
+    }
+    if (pairs_ok(h)) k_bicg_dir<2><<<gv, NT, 0, s>>>(S, r, h->rh.as<double>(), h->p.as<double>());
+    else k_bicg_dir<1><<<gv, NT, 0, s>>>(S, r, h->rh.as<double>(), h->p.as<double>());
+    TRY(launched());
+
+    const long long cap_launches = ((long long)o->max_iter + 2LL * k + 2) / k + 2;
+    bool finished = false, timed_out = false;
+    TRY(poll_loop(h, o, cap_launches, nullptr, s, &finished, &timed_out, [&](int) {
+        CU(cudaGraphLaunch(gc.exec[0], s));
+        g_launches.fetch_add((unsigned long long)gc.nodes, std::memory_order_relaxed);
+        return SLA_OK;
+    }));
+
+    if (pc == SLA_PC_JACOBI) {   // x = D^-1 y
+        k_bicg_scale<false><<<gv, NT, 0, s>>>(S, x, h->diag.as<double>());
+        TRY(launched());
+    }
+    k_final<double><<<gs, NT, L.smem, s>>>(M, S, uv, x, h->bw.as<double>(), x_it, h->stat.as<Stat>());
+    TRY(launched());
+    if (h->reordered) TRY(gather_map(8, h->n, h->batch, h->iperm.as<int>(), x_it, h->n, x_user, h->n, s));
+    return collect(h, finished, timed_out, o, info, s, "breakdown (r^.r or r^.v zero, omega zero or non-finite value)");
 }
 
 // ===================================================================== C ABI
@@ -1430,6 +1663,26 @@ sla_status sla_pcg_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg
     return solve_impl<float>(h, (const float*)d_b, (float*)d_x, opts, info, s);
 }
 
+// dL/dA_k = -lambda_row(k) x_col(k) on A's own pattern and ordering.
+static sla_status grad_A(sla_csr* h, const void* d_x, const void* d_lam, void* d_dLdA, cudaStream_t s) {
+    if (!d_dLdA || h->nnz == 0) return SLA_OK;
+    const Sys S = sys_of(h);
+    const Mat A = mat_A(h);
+    const dim3 g(h->LA.gx, h->batch);
+    if (h->dt == SLA_F64)
+        k_grad_A<double><<<g, NT, h->LA.smem, s>>>(A, S, (const double*)d_lam, (const double*)d_x, (double*)d_dLdA);
+    else
+        k_grad_A<float><<<g, NT, h->LA.smem, s>>>(A, S, (const float*)d_lam, (const float*)d_x, (float*)d_dLdA);
+    TRY(launched());
+    CU(cudaStreamSynchronize(s));
+    return SLA_OK;
+}
+
+// A solve status after which the gradient is still formed (x holds the last iterate).
+static bool solved_or_stopped(sla_status st) {
+    return st == SLA_OK || st == SLA_ERR_NOT_CONVERGED || st == SLA_ERR_BREAKDOWN || st == SLA_ERR_TIMEOUT;
+}
+
 sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla_pcg_opts* opts, void* d_dLdb,
                        void* d_dLdA, sla_solve_info* info, void* stream) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
@@ -1441,21 +1694,36 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
     sla_status st = h->dt == SLA_F64
                         ? solve_impl<double>(h, (const double*)d_g, (double*)d_dLdb, &o, info, s)
                         : solve_impl<float>(h, (const float*)d_g, (float*)d_dLdb, &o, info, s);
-    if (st != SLA_OK && st != SLA_ERR_NOT_CONVERGED && st != SLA_ERR_BREAKDOWN && st != SLA_ERR_TIMEOUT) return st;
-    if (d_dLdA && h->nnz > 0) {
-        const Sys S = sys_of(h);
-        const Mat A = mat_A(h);
-        const dim3 g(h->LA.gx, h->batch);
-        if (h->dt == SLA_F64)
-            k_grad_A<double><<<g, NT, h->LA.smem, s>>>(A, S, (const double*)d_dLdb, (const double*)d_x,
-                                                               (double*)d_dLdA);
-        else
-            k_grad_A<float><<<g, NT, h->LA.smem, s>>>(A, S, (const float*)d_dLdb, (const float*)d_x,
-                                                              (float*)d_dLdA);
-        sla_status l = launched();
-        if (l != SLA_OK) return l;
-        CU(cudaStreamSynchronize(s));
-    }
+    if (!solved_or_stopped(st)) return st;
+    TRY(grad_A(h, d_x, d_dLdb, d_dLdA, s));
+    return st;
+}
+
+static sla_status check_bicg(sla_handle h, const sla_pcg_opts* o) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    TRY(check_opts(o));
+    if (o->pc == SLA_PC_SPAI) return fail(SLA_ERR_INVALID, "BiCGStab takes SLA_PC_NONE or SLA_PC_JACOBI");
+    if (h->dt != SLA_F64) return fail(SLA_ERR_UNSUPPORTED, "BiCGStab is built for fp64 systems only");
+    return SLA_OK;
+}
+
+sla_status sla_bicgstab_solve(sla_handle h, const void* d_b, void* d_x, const sla_pcg_opts* opts,
+                              sla_solve_info* info, void* stream) {
+    TRY(check_bicg(h, opts));
+    if (!d_b || !d_x) return fail(SLA_ERR_INVALID, "null vector");
+    return bicg_impl(h, false, (const double*)d_b, (double*)d_x, opts, info, (cudaStream_t)stream);
+}
+
+sla_status sla_bicgstab_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla_pcg_opts* opts,
+                                void* d_dLdb, void* d_dLdA, sla_solve_info* info, void* stream) {
+    TRY(check_bicg(h, opts));
+    if (!d_x || !d_g || !d_dLdb) return fail(SLA_ERR_INVALID, "null vector");
+    cudaStream_t s = (cudaStream_t)stream;
+    sla_pcg_opts o = *opts;
+    o.use_x0 = 0;
+    sla_status st = bicg_impl(h, true, (const double*)d_g, (double*)d_dLdb, &o, info, s);
+    if (!solved_or_stopped(st)) return st;
+    TRY(grad_A(h, d_x, d_dLdb, d_dLdA, s));
     return st;
 }
 

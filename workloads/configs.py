@@ -17,6 +17,11 @@ Streams: 1 = b (or the manufactured x*), 2 = cell coefficients, 3 = points,
       union-symmetrised, weights exp(-d^2/h^2), A = L + 1e-3 I, points relabelled
       by a seeded permutation, fp64; b ~ N(0,1); factored-SPAI PCG
       (M^-1 = G G^T + 1e-3 I) to 1e-8.
+  cd3 3D upwind convection-diffusion, 128^3, fp64 (nonsymmetric): the 7-point
+      Laplacian plus first-order upwind convection by a solid-body rotation
+      about the z axis (scaled speed up to 2 at the side midpoints) and a
+      constant 0.5 along z; b ~ N(0,1); Jacobi-BiCGStab to 1e-8, then the
+      adjoint (A^T lambda = g) with g ~ N(0,1).  Seed 1006.
 
 `scale` shrinks a workload for tests the oracle finishes in seconds: the grid
 side (or point count) is replaced while the recipe is kept.
@@ -28,7 +33,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 from . import rng
-from .matrices import CSR, diffusion2d, knn_graph_laplacian, poisson_grid
+from .matrices import CSR, convection_diffusion, diffusion2d, knn_graph_laplacian, poisson_grid
 
 
 @dataclass
@@ -97,6 +102,20 @@ def c5(npoints: int = 4 * 1024 * 1024, k: int = 12) -> Workload:
                     info={"points": npoints, "k": k})
 
 
+def cd3(N: int = 128, peclet: float = 2.0) -> Workload:
+    seed = 1006
+    n = N * N * N
+    idx = np.arange(n, dtype=np.int64)
+    x = (idx % N + 1.0) / (N + 1.0)
+    y = ((idx // N) % N + 1.0) / (N + 1.0)
+    wind = (-(y - 0.5) * 2.0 * peclet, (x - 0.5) * 2.0 * peclet, 0.5)
+    A = convection_diffusion((N, N, N), wind)
+    b = rng.normal(seed, 1, n)
+    g = rng.normal(seed, 5, n)
+    return Workload("cd3", A, b, "f64", "jacobi", 1e-8, g=g,
+                    info={"grid": (N, N, N), "peclet": peclet, "method": "bicgstab"})
+
+
 def _csr_matvec_f64(A: CSR, x: np.ndarray) -> np.ndarray:
     """b = A x*, used only to manufacture the right-hand side of c1.  Summed
     with numpy (np.add.reduceat), which is neither the oracle nor the GPU code."""
@@ -104,13 +123,13 @@ def _csr_matvec_f64(A: CSR, x: np.ndarray) -> np.ndarray:
     return np.add.reduceat(prod, A.row_ptr[:-1].astype(np.int64))
 
 
-BUILDERS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5}
+BUILDERS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5, "cd3": cd3}
 
 # Full sizes of each workload (the shapes the benchmark and the
 # full-size parity tests use) and small shapes the oracle solves in seconds.
-FULL = {"c1": {}, "c2": {}, "c3": {}, "c4": {}, "c5": {}}
+FULL = {"c1": {}, "c2": {}, "c3": {}, "c4": {}, "c5": {}, "cd3": {}}
 SMALL = {"c1": {"N": 64}, "c2": {"N": 96}, "c3": {"N": 48, "batch": 5},
-         "c4": {"N": 24}, "c5": {"npoints": 20000}}
+         "c4": {"N": 24}, "c5": {"npoints": 20000}, "cd3": {"N": 24}}
 
 
 def build(name: str, **kw) -> Workload:
