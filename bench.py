@@ -15,6 +15,10 @@ Default workload (N = 1): 2D 5-point variable-coefficient diffusion,
 g ~ N(0,1).  Under torchrun every rank solves its own replica (no data-path
 collective); value = iterations of all ranks / max-over-ranks time.
 `--impl reference` times the plain CPU oracle on the host cores instead.
+
+`--config cd3` measures BiCGStab instead: a nonsymmetric 3D
+convection-diffusion system, forward solve plus the adjoint solve on the
+explicit transpose, reported as BiCGStab iterations per second.
 """
 from __future__ import annotations
 
@@ -39,9 +43,30 @@ DESCR = {
     "c4": "3D 7-point Poisson 128^3 (n=2097152, nnz=14581760), fp64, CG to 1e-8, b,g ~ N(0,1)",
     "c5": "kNN graph Laplacian, 4M points in the unit cube, k=12 union, A = L + 1e-3 I, relabelled, fp64, "
           "SPAI-PCG (G G^T + 1e-3 I) to 1e-8",
+    "cd3": "3D 7-point upwind convection-diffusion 128^3 (n=2097152, nnz=14581760), rotating wind about z "
+           "(scaled speed <= 2) + 0.5 along z, fp64, nonsymmetric, Jacobi-BiCGStab to 1e-8, b,g ~ N(0,1)",
 }
 MAX_ITER = 200000
 METRIC = "PCG iterations/s (forward + adjoint); HBM GB/s per iteration (fraction of B300 peak); solve ms"
+METRIC_BICG = ("BiCGStab iterations/s (forward + transpose adjoint); HBM GB/s per iteration "
+               "(fraction of B300 peak); solve ms")
+
+
+def method_of(w):
+    return w.info.get("method", "cg")
+
+
+def metric_of(w):
+    return METRIC_BICG if method_of(w) == "bicgstab" else METRIC
+
+
+def oracle_solve(w, A, b, max_iter):
+    """The oracle's solver for the workload's method (test infrastructure,
+    used only by the CPU legs)."""
+    import oracle
+    if method_of(w) == "bicgstab":
+        return oracle.bicgstab(A, b, w.tol, max_iter=max_iter, pc=w.pc)
+    return oracle.pcg(A, b, w.tol, max_iter=max_iter, pc=w.pc, eps=w.eps)
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0
 
@@ -64,6 +89,17 @@ def byte_model(w, nnzg=None):
     s = 4 if w.dtype == "f32" else 8   # matrix values and caller vectors
     v = 8                              # working vectors of the recurrence (fp64 or fp32 pairs)
     rp = 4 * (n + 1)
+    if method_of(w) == "bicgstab":
+        # BiCGStab: two products (values, columns, row pointers, the source
+        # vector gathered once) and 19 vector passes: v = A p (p, r^ read, v
+        # written), s = r - alpha v (3), t = A s (s, t), the x/r update (x, p,
+        # s, t, r^ read; x, r written) and the direction update (r, p, v
+        # read; p written).
+        mat = s * nnz * B + 4 * nnz + rp
+        return {"per_iteration": 2 * mat + 19 * v * n * B,
+                "spmv_dot_per_launch": mat + 2 * s * n * B,
+                "product_per_launch": mat + 3 * v * n * B,
+                "grad_A": 4 * nnz + rp + s * nnz * B + 2 * s * n * B}
     # The per-iteration model is fixed in advance for the three-kernel
     # schedule (product: p read once, q written; x/r update: x, r, p, q
     # [, dinv] read, x, r written; p update: r, p [, dinv] read, p written),
@@ -88,7 +124,7 @@ def kernel_source_hash():
     traffic figure is reported only while these sources are unchanged)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sparse_iterative_linear_csr_b300", "csrc")
-    for f in ("common.cuh", "df.cuh", "kernels.cuh"):
+    for f in ("common.cuh", "df.cuh", "kernels.cuh", "bicgstab.cuh"):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -167,60 +203,58 @@ def bus_id_of(dev):
 
 
 def cpu_sample(w, budget_s=12.0):
-    """The oracle as it stands, single-threaded, on a bounded number of PCG
-    iterations of the same workload (first system of a batch)."""
-    import numpy as np
-    import oracle
+    """The oracle as it stands, single-threaded, on a bounded number of
+    iterations of the same workload's method (first system of a batch)."""
     A = w.A
     b = w.b if w.b.ndim == 1 else w.b[0]
     if A.vals.ndim == 2:
         from workloads.matrices import CSR
         A = CSR(A.n, A.row_ptr, A.col_idx, A.vals[0])
     t0 = time.perf_counter()
-    _, inf = oracle.pcg(A, b, w.tol, max_iter=3, pc=w.pc, eps=w.eps)
+    _, inf = oracle_solve(w, A, b, 3)
     t_small = time.perf_counter() - t0
     per_it = max(t_small / 4.0, 1e-6)
     cap = int(max(3, min(MAX_ITER, budget_s / per_it)))
     t0 = time.perf_counter()
-    _, inf = oracle.pcg(A, b, w.tol, max_iter=cap, pc=w.pc, eps=w.eps)
+    _, inf = oracle_solve(w, A, b, cap)
     dt = time.perf_counter() - t0
     its = max(inf["iters"], 1)
+    name = "BiCGStab" if method_of(w) == "bicgstab" else "PCG"
     return {"value": its / dt, "unit": "iterations/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {its} PCG iterations of the forward solve (system 0), {dt:.1f} s, "
+            "sample": f"first {its} {name} iterations of the forward solve (system 0), {dt:.1f} s, "
                       f"single-threaded fp64 C oracle"}
 
 
 def run_reference(args, w, rank):
     if rank != 0:
         return
-    import oracle  # noqa: F401
     A = w.A
     b = w.b if w.b.ndim == 1 else w.b[0]
     if A.vals.ndim == 2:
         from workloads.matrices import CSR
         A = CSR(A.n, A.row_ptr, A.col_idx, A.vals[0])
-    import oracle as orc
     t0 = time.perf_counter()
-    orc.pcg(A, b, w.tol, max_iter=3, pc=w.pc, eps=w.eps)
+    oracle_solve(w, A, b, 3)
     per_it = max((time.perf_counter() - t0) / 4.0, 1e-6)
     cap = int(max(2, min(MAX_ITER, 4.0 / per_it)))   # ~4 s of CPU work per step
     for _ in range(args.warmup):
-        orc.pcg(A, b, w.tol, max_iter=max(2, cap // 4), pc=w.pc, eps=w.eps)
+        oracle_solve(w, A, b, max(2, cap // 4))
     its = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, inf = orc.pcg(A, b, w.tol, max_iter=cap, pc=w.pc, eps=w.eps)
+        _, inf = oracle_solve(w, A, b, cap)
         its += inf["iters"]
     dt = time.perf_counter() - t0
     v = its / dt
-    line = {"metric": METRIC, "value": v, "unit": "iterations/s", "n_gpus": args.gpus,
+    name = "BiCGStab" if method_of(w) == "bicgstab" else "PCG"
+    line = {"metric": metric_of(w), "value": v, "unit": "iterations/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64" if w.dtype == "f64" else "f32",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": w.A.n, "nnz": w.A.nnz,
                        "pc": w.pc, "tol": w.tol},
             "cpu_baseline": {"value": v, "unit": "iterations/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{cap} PCG iterations per step of the forward solve (system 0)"},
+                             "sample": f"{cap} {name} iterations per step of the forward solve (system 0)"},
             "e2e": {"value": v, "unit": "iterations/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -289,8 +323,9 @@ def main():
     g = torch.from_numpy(w.g).to(dev)
     M = sla.CSRMatrix(rp, ci, vals, pipeline=args.warp_pipeline, fused=args.persistent, time_product=True,
                       producer_consumer=args.producer_consumer)
+    method = method_of(w)
     kw = dict(tol=w.tol, max_iter=MAX_ITER, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3,
-              poll_k=args.poll_k)
+              poll_k=args.poll_k, method=method)
 
     def step():
         x, inf = M.solve(b, **kw)
@@ -348,7 +383,13 @@ def main():
     # so the fused SpMV + dot API kernel is timed alone on the same operands.
     nnzg = (A.nnz + A.n) // 2 if w.pc == "spai" else None
     bm = byte_model(w, nnzg)
-    if prod_n > 0:
+    if prod_n > 0 and method == "bicgstab":
+        kern_ms = prod_ms / prod_n
+        kern_bytes = bm["product_per_launch"]
+        kern_desc = (f"k_bicg_v (BiCGStab product v = A p fused with r^.v), live in the timed solves: "
+                     f"{prod_n} launches timed with CUDA events on the solve stream")
+        kern_name = "k_bicg_v"
+    elif prod_n > 0:
         kern_ms = prod_ms / prod_n
         kern_bytes = bm["product_per_launch"]
         kern_desc = (f"k_spmv_iter (CG product q = A p fused with p.q), live in the timed solves: "
@@ -421,13 +462,14 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC,
+            "metric": metric_of(w),
             "value": value, "unit": "iterations/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": A.n, "nnz": A.nnz,
                        "batch": A.batch, "pc": w.pc, "tol": w.tol, "poll_k": args.poll_k,
-                       "step": "forward PCG solve + adjoint solve + dL/dA pass",
+                       "step": ("forward BiCGStab solve + adjoint BiCGStab solve on the explicit A^T + dL/dA pass"
+                                if method == "bicgstab" else "forward PCG solve + adjoint solve + dL/dA pass"),
                        "l2": f"inputs larger than L2: {bm['per_iteration'] / 1e6:.1f} MB touched per iteration "
                              f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"},
             "iterations_per_step": iters // max(args.steps, 1),

@@ -1,6 +1,7 @@
 /*
  * sla.h -- C ABI of the B300 (sm_103a) sparse iterative linear solver:
- * preconditioned conjugate gradient on a CSR matrix and its adjoint.
+ * preconditioned conjugate gradient on a CSR matrix and its adjoint, and
+ * BiCGStab with its transpose adjoint for nonsymmetric systems.
  *
  * Sources of the operations (page title, then section):
  *  - "torch-sla: Differentiable Sparse Linear Algebra with Adjoint Solvers and
@@ -14,7 +15,11 @@
  *         and <p,Ap>; the adjoint A^T lambda = dL/dx and the matrix gradient
  *         -lambda_i x_j on the stored non-zeros;
  *      §4 Table 3: CG with Jacobi preconditioning; §4 Figure 2: an absolute /
- *         relative stopping tolerance on the residual.
+ *         relative stopping tolerance on the residual;
+ *      §3 backends paragraph: BiCGStab beside CG among the iterative methods.
+ *  - BiCGStab itself: van der Vorst, SIAM J. Sci. Stat. Comput. 13(2), 1992,
+ *    as laid out in Barrett et al., "Templates for the Solution of Linear
+ *    Systems" (SIAM, 1994), §2.3.8.
  *  - "Learning Sparse Approximate Inverse Preconditioners for Conjugate
  *    Gradient Solvers on GPUs" (author responses): the factored
  *    preconditioner M^-1 = G G^T + eps I applied with two SpMVs (Reviewer umir
@@ -32,7 +37,7 @@
  *    offset s*nnz.
  *  - Vectors of a batch are [batch][n], system s at offset s*n.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
- *    work of a call is ordered on it.  sla_pcg_solve and sla_adjoint return
+ *    work of a call is ordered on it.  The solve and adjoint calls return
  *    after the solve has finished on the device (they synchronise `stream`);
  *    sla_spmv and sla_spmv_dot return without synchronising.
  *  - One call at a time per handle: the handle owns the solver workspace.
@@ -72,7 +77,7 @@ typedef enum {
 #define SLA_WARP_PIPELINE 2u /* use the warp-pipeline product where it applies (see sla_csr_layout) */
 #define SLA_PERSISTENT 4u    /* CG / Jacobi-PCG: one persistent iteration kernel per poll interval
                                 instead of a CUDA graph of one kernel per step (see sla_pcg_solve) */
-#define SLA_TIME_PRODUCT 8u  /* time one CG product kernel per graph launch (sla_product_time) */
+#define SLA_TIME_PRODUCT 8u  /* time one product kernel per graph launch (sla_product_time) */
 #define SLA_PRODUCER_CONSUMER 16u /* use the producer/consumer product where it applies (see sla_csr_layout) */
 #define SLA_REORDER 32u      /* always iterate on the reordered matrix (see sla_pcg_solve) */
 #define SLA_NO_REORDER 64u   /* never reorder */
@@ -135,9 +140,11 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
 sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered);
 
 /*
- * Live duration of the CG product kernel (q = A p fused with p.q and the
+ * Live duration of the first product kernel of an iteration (CG: q = A p
+ * fused with p.q; BiCGStab: v = A p fused with r^.v; either with the
  * pending true-residual check), for handles created with SLA_TIME_PRODUCT:
- * every graph launch of sla_pcg_solve / sla_adjoint records CUDA events on
+ * every graph launch of sla_pcg_solve / sla_adjoint / sla_bicgstab_solve /
+ * sla_bicgstab_adjoint records CUDA events on
  * the solve's stream around the product kernel of its middle iteration,
  * and the solve adds that duration once the launch has finished, for
  * launches that neither start nor end with every system frozen (a system
@@ -210,7 +217,8 @@ sla_status sla_adjoint(sla_handle h, const void* d_x, const void* d_g, const sla
  * Solve a general (nonsymmetric) A x = b by BiCGStab (van der Vorst 1992;
  * the right-preconditioned form of Barrett et al., "Templates for the
  * Solution of Linear Systems", §2.3.8, shadow residual r^ = r0) -- the
- * nonsymmetric Krylov solver of torch-sla's iterative backends (§3.1).
+ * nonsymmetric Krylov solver of torch-sla's iterative backends (§3, backends
+ * paragraph).
  *  - fp64 handles only (SLA_ERR_UNSUPPORTED for fp32).  opts->pc is
  *    SLA_PC_NONE or SLA_PC_JACOBI (right preconditioning by diag(A), which
  *    must be stored; applied as the column scaling A diag(A)^-1 of a

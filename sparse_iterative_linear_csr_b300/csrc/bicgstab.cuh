@@ -4,8 +4,8 @@
 // Sci. Stat. Comput. 13(2), 1992), in the right-preconditioned form of
 // Barrett et al., "Templates for the Solution of Linear Systems", §2.3.8,
 // with the shadow residual r^ = r0 -- the nonsymmetric Krylov solver that
-// torch-sla's native iterative backend offers beside CG (torch-sla, §3.1
-// backends).  Right Jacobi preconditioning is applied as a column scaling
+// torch-sla's native iterative backend offers beside CG (torch-sla, §3
+// backends paragraph).  Right Jacobi preconditioning is applied as a column scaling
 // of the stored values, A^ = A D^-1 (D = diag(A)), built once per solve: the
 // iteration runs unpreconditioned on A^ y = b and returns x = D^-1 y, which
 // is the right-preconditioned iteration with p^ = D^-1 p and s^ = D^-1 s

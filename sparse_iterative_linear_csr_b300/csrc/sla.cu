@@ -1284,7 +1284,7 @@ static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
 // One BiCGStab iteration on the matrix (M, av): five kernels.
 template <int W>
 static sla_status enqueue_bicg(sla_csr* h, const Mat& M, const Layout& L, const double* av, cudaStream_t s,
-                               int* nodes) {
+                               int* nodes, cudaEvent_t ev0, cudaEvent_t ev1) {
     const Sys S = sys_of(h);
     double* y = h->x.as<double>();
     double* r = h->r.as<double>();   // r, and s over it
@@ -1293,10 +1293,12 @@ static sla_status enqueue_bicg(sla_csr* h, const Mat& M, const Layout& L, const 
     double* t = h->z.as<double>();
     const double* rh = h->rh.as<double>();
     const dim3 gs(L.gx, h->batch), gv(gx_vec(h), h->batch);
+    if (ev0) CU(cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal));
     with_form_rc(L.form, [&](auto f) {
         k_bicg_v<decltype(f)::value><<<gs, NT, L.smem, s>>>(M, S, av, p, v, rh, y, h->bw.as<double>());
     });
     TRY(launched());
+    if (ev1) CU(cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal));
     k_bicg_s<W><<<gv, NT, 0, s>>>(S, r, v);
     TRY(launched());
     with_form_rc(L.form, [&](auto f) { k_bicg_t<decltype(f)::value><<<gs, NT, L.smem, s>>>(M, S, av, r, t); });
@@ -1345,8 +1347,10 @@ static sla_status bicg_impl(sla_csr* h, bool transposed, const double* b, double
         itv = h->bvals.as<double>();
     }
     GraphCache& gc = h->graph[3 + 2 * (transposed ? 1 : 0) + (pc == SLA_PC_JACOBI ? 1 : 0)];
-    TRY(capture_graph(h, gc, k, 0.0, false, [&](cudaStream_t cs, int* nodes, cudaEvent_t, cudaEvent_t) {
-        return pairs_ok(h) ? enqueue_bicg<2>(h, M, L, itv, cs, nodes) : enqueue_bicg<1>(h, M, L, itv, cs, nodes);
+    TRY(capture_graph(h, gc, k, 0.0, h->time_product, [&](cudaStream_t cs, int* nodes, cudaEvent_t e0,
+                                                            cudaEvent_t e1) {
+        return pairs_ok(h) ? enqueue_bicg<2>(h, M, L, itv, cs, nodes, e0, e1)
+                           : enqueue_bicg<1>(h, M, L, itv, cs, nodes, e0, e1);
     }));
 
     const dim3 gs(L.gx, h->batch), gv(gx_vec(h), h->batch);
@@ -1382,8 +1386,8 @@ static sla_status bicg_impl(sla_csr* h, bool transposed, const double* b, double
 
     const long long cap_launches = ((long long)o->max_iter + 2LL * k + 2) / k + 2;
     bool finished = false, timed_out = false;
-    TRY(poll_loop(h, o, cap_launches, nullptr, s, &finished, &timed_out, [&](int) {
-        CU(cudaGraphLaunch(gc.exec[0], s));
+    TRY(poll_loop(h, o, cap_launches, h->time_product ? &gc : nullptr, s, &finished, &timed_out, [&](int slot) {
+        CU(cudaGraphLaunch(gc.exec[h->time_product ? slot : 0], s));
         g_launches.fetch_add((unsigned long long)gc.nodes, std::memory_order_relaxed);
         return SLA_OK;
     }));

@@ -1,5 +1,6 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the
-benchmark times (same options, poll interval 32, forward solve then adjoint).
+"""Parity at the workloads' full sizes (the five CG workloads and the
+BiCGStab workload cd3), in the launch configuration the benchmark times (same
+options, poll interval 32, forward solve then adjoint).
 
 The oracle cannot solve the large systems in seconds, so the checks are the
 ones that hold at any size plus outputs the oracle computes one by one:
@@ -9,8 +10,11 @@ ones that hold at any size plus outputs the oracle computes one by one:
     the 64x64 Poisson problem and two systems of the 64-system batch are also
     solved by the oracle and compared element by element;
   * adjoint: g.x = lambda.b and sum_k A_k dL/dA_k = -g.x (fp64 on the host),
-    the adjoint's own true residual, and sampled dL/dA entries exactly equal
-    to -lambda_i x_j of the returned vectors."""
+    the adjoint's own true residual ||g - A^T lambda||, and sampled dL/dA
+    entries exactly equal to -lambda_i x_j of the returned vectors.
+BiCGStab's Jacobi form stops on the residual of the column-scaled system,
+which equals b - A x up to rounding: its bound carries a 1e-6 relative
+slack."""
 import numpy as np
 import pytest
 import scipy.sparse as sp
@@ -32,8 +36,10 @@ def _system(A, s):
     return sp.csr_matrix((v.astype(np.float64), A.col_idx, A.row_ptr), shape=(A.n, A.n))
 
 
-def _true_rel(A, s, b, x):
+def _true_rel(A, s, b, x, transpose=False):
     M = _system(A, s)
+    if transpose:
+        M = M.T.tocsr()
     b = b.astype(np.float64)
     return float(np.linalg.norm(b - M @ x.astype(np.float64)) / np.linalg.norm(b))
 
@@ -48,7 +54,7 @@ def _workload(name):
     return _cache[name]
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5", "cd3"])
 def test_fullsize_spmv_sampled_rows(cuda_device, name):
     w = _workload(name)
     A = w.A
@@ -75,14 +81,16 @@ def test_fullsize_spmv_sampled_rows(cuda_device, name):
         assert np.all(np.abs(ys[rows].astype(np.float64) - y_o) <= tol * np.maximum(scale, 1e-300))
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5", "cd3"])
 def test_fullsize_solve_and_adjoint(cuda_device, name):
     w = _workload(name)
     A = w.A
     M = make(A)
     b = torch.from_numpy(w.b).to(cuda_device)
     g = torch.from_numpy(w.g).to(cuda_device)
-    kw = dict(tol=w.tol, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3, **BENCH_KW)
+    method = w.info.get("method", "cg")
+    kw = dict(tol=w.tol, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3, method=method, **BENCH_KW)
+    slack = 1.0 + 1e-6 if method == "bicgstab" else 1.0
     x, info = M.solve(b, **kw)
     dldb, dlda, ainfo = M.adjoint(x, g, **kw)
     xh, lb, la = x.cpu().numpy(), dldb.cpu().numpy(), dlda.cpu().numpy()
@@ -98,9 +106,9 @@ def test_fullsize_solve_and_adjoint(cuda_device, name):
         assert info[s].status == "ok" and ainfo[s].status == "ok"
         # true residuals recomputed on the host in fp64
         tr = _true_rel(A, s, B[s], X[s])
-        assert tr <= w.tol
+        assert tr <= w.tol * slack
         assert abs(tr - info[s].rel_res_true) <= 1e-3 * w.tol
-        assert _true_rel(A, s, G[s], L[s]) <= w.tol
+        assert _true_rel(A, s, G[s], L[s], transpose=True) <= w.tol * slack
         # adjoint identities
         gx = float(G[s].astype(np.float64) @ X[s].astype(np.float64))
         lbb = float(L[s].astype(np.float64) @ B[s].astype(np.float64))
