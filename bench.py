@@ -287,6 +287,8 @@ def main():
                     help="use the warp-pipeline product where it applies")
     ap.add_argument("--producer-consumer", action="store_true",
                     help="use the producer/consumer product where it applies")
+    ap.add_argument("--staged", action="store_true",
+                    help="keep the warp-staged product forms where the direct form would be the default")
     ap.add_argument("--persistent", action="store_true",
                     help="CG / Jacobi-PCG as the persistent iteration kernel (not a graph of kernels)")
     args = ap.parse_args()
@@ -322,7 +324,7 @@ def main():
     b = torch.from_numpy(w.b).to(dev)
     g = torch.from_numpy(w.g).to(dev)
     M = sla.CSRMatrix(rp, ci, vals, pipeline=args.warp_pipeline, fused=args.persistent, time_product=True,
-                      producer_consumer=args.producer_consumer)
+                      producer_consumer=args.producer_consumer, staged=args.staged)
     method = method_of(w)
     kw = dict(tol=w.tol, max_iter=MAX_ITER, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3,
               poll_k=args.poll_k, method=method)
@@ -486,6 +488,7 @@ def main():
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
             "wall_s_timed": t_wall, "kernel_src": src, "product_form": M.layout()[0],
+            "product_ctas_per_system": M.layout()[1],
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -81,6 +81,7 @@ typedef enum {
 #define SLA_PRODUCER_CONSUMER 16u /* use the producer/consumer product where it applies (see sla_csr_layout) */
 #define SLA_REORDER 32u      /* always iterate on the reordered matrix (see sla_pcg_solve) */
 #define SLA_NO_REORDER 64u   /* never reorder */
+#define SLA_STAGED 128u      /* never use the direct product form (see sla_csr_layout) */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -133,6 +134,10 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         192 rows into a ring of shared-memory stages, 6 warps add; same
  *         alignment conditions; only with SLA_PRODUCER_CONSUMER, which
  *         takes precedence over SLA_WARP_PIPELINE);
+ *         5 direct: one thread per row, no shared-memory staging, kernels
+ *         built for high occupancy -- the default whenever no row has more
+ *         than 16 entries, unless SLA_STAGED, SLA_WARP_PIPELINE or
+ *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2;
  *  *ctas: CTAs per system of the product kernels;
  *  *reordered: 1 when the solves iterate on P A P^T.
  * Any pointer may be NULL.  SLA_ERR_INVALID for a null handle.

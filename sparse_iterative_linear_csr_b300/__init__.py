@@ -87,12 +87,13 @@ class CSRMatrix:
     (product_time); producer_consumer=True uses the producer/consumer
     product where it applies; reorder=True / False forces / forbids
     iterating on a reverse Cuthill-McKee reordering (default: reorder
-    scattered patterns)."""
+    scattered patterns); staged=True keeps the warp-staged product forms
+    where the direct (thread-per-row) form would be the default."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
                  validate: bool = True, pipeline: bool = False, fused: bool = False,
                  time_product: bool = False, producer_consumer: bool = False, reorder: bool | None = None,
-                 stream=None):
+                 staged: bool = False, stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -118,6 +119,7 @@ class CSRMatrix:
                                   (_lib.SLA_PERSISTENT if fused else 0) |
                                   (_lib.SLA_TIME_PRODUCT if time_product else 0) |
                                   (_lib.SLA_PRODUCER_CONSUMER if producer_consumer else 0) |
+                                  (_lib.SLA_STAGED if staged else 0) |
                                   ({None: 0, True: _lib.SLA_REORDER, False: _lib.SLA_NO_REORDER}[reorder]),
                                   _stream(stream),
                                   C.byref(self._h)))
@@ -162,13 +164,13 @@ class CSRMatrix:
 
     # -------------------------------------------------------------- API
     def product_time(self, reset: bool = True) -> tuple[float, int]:
-        """(summed ms, launches timed) of the live CG product kernel (time_product=True)."""
+        """(summed ms, launches timed) of the live product kernel (time_product=True)."""
         ms, n = C.c_double(), C.c_longlong()
         _check(_lib_handle().sla_product_time(self._h, C.byref(ms), C.byref(n), int(reset)))
         return ms.value, n.value
 
     def layout(self) -> tuple[int, int, bool]:
-        """(product form 0..4, CTAs per system, reordered) of the matrix the solves iterate on."""
+        """(product form 0..5, CTAs per system, reordered) of the matrix the solves iterate on."""
         f, g, r = C.c_int(), C.c_int(), C.c_int()
         _check(_lib_handle().sla_csr_layout(self._h, C.byref(f), C.byref(g), C.byref(r)))
         return f.value, g.value, bool(r.value)

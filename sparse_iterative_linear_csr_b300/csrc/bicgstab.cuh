@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(NT) k_bicg_dir(Sys S, const double* __restrict
 
 // v = A p, sigma = r^.v; with `check` set, ||b - A y||^2 first.
 template <int FORM>
-__global__ void __launch_bounds__(NT, IterMinCtas<double>::value)
+__global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     k_bicg_v(Mat A, Sys S, const double* __restrict__ av, const double* __restrict__ p, double* __restrict__ v,
              const double* __restrict__ rh, const double* __restrict__ y, const double* __restrict__ b) {
     SYS_PROLOGUE
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(NT) k_bicg_s(Sys S, double* __restrict__ r, co
 
 // t = A s, t.t and t.s -> omega.
 template <int FORM>
-__global__ void __launch_bounds__(NT, IterMinCtas<double>::value)
+__global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     k_bicg_t(Mat A, Sys S, const double* __restrict__ av, const double* __restrict__ s, double* __restrict__ t) {
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;

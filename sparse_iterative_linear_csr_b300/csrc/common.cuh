@@ -19,6 +19,16 @@ constexpr int SPMV_MIN_CTAS = 4; // resident CTAs per SM the staged-SpMV kernels
 #endif
 template <typename T> struct IterMinCtas { static constexpr int value = SLA_ITER_CTAS_F64; };
 template <> struct IterMinCtas<float> { static constexpr int value = 4; };
+// Resident CTAs per SM the product kernels are compiled for in the direct
+// form (thread per row, no staging): occupancy is what hides its latency.
+// Measured on B300 inside the running iteration (c4, c2): 4 beats 6 and 8,
+// which thrash the caches the iteration's other kernels leave filled.
+#ifndef SLA_DIRECT_CTAS
+#define SLA_DIRECT_CTAS 4
+#endif
+template <typename T, int FORM> struct ProductCtas {
+    static constexpr int value = FORM == 5 ? SLA_DIRECT_CTAS : IterMinCtas<T>::value;
+};
 
 // Outcome codes mirrored from sla_status (kept numerically equal).
 enum : int { ST_OK = 0, ST_NOT_CONVERGED = 4, ST_BREAKDOWN = 5 };

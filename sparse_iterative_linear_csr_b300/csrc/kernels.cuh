@@ -63,6 +63,7 @@ struct Mat {
     int ccap;         // warp pipeline: entries per stage (multiple of 4)
     int stages;       // warp pipeline: ring stages
     int* err;         // device error bits (Ctrl::err; Ctrl::diag follows at err + 2)
+    int direct;       // 1: the layout's kernels run the direct form (no shared-memory staging)
 };
 
 #define SYS_PROLOGUE                                            \
@@ -212,10 +213,36 @@ __device__ __forceinline__ typename Prec<T>::acc unstaged_row(const Mat& A, cons
     return s;
 }
 
+// Direct form: one thread per row (grid stride over rows).  The thread
+// loads its row's values and column indices (evict-first; the warp's rows
+// are consecutive, so the lines its loads touch are shared through L1),
+// gathers the vector entries they address through the read-only path and
+// sums them (one fp64 FMA per entry for fp64 systems).  No shared memory:
+// the kernels carrying it are built for high occupancy (many resident warps
+// per SM hide the load latency), which on B300 beats staging a warp's rows
+// for patterns with short rows.
+template <typename T, typename VT, class Gather, class Pre, class Epi>
+__device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__ av, Gather gather, Pre pre,
+                                            Epi epi) {
+    using acc_t = typename Prec<T>::acc;
+    const int stride = gridDim.x * NT;
+    for (int row = blockIdx.x * NT + threadIdx.x; row < A.n; row += stride) {
+        const int lo = ld_nc(A.rp + row), hi = ld_nc(A.rp + row + 1);
+        const auto carried = pre(row);
+        acc_t s = Prec<T>::zero();
+        for (int k = lo; k < hi; ++k) mac(s, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+        epi(row, s, carried);
+    }
+}
+
 template <typename T, typename VT, class Gather, class Pre, class Epi>
 __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ av, Gather gather, Pre pre,
                                           Epi epi, double* wsm) {
     using acc_t = typename Prec<T>::acc;
+    if (A.direct) {   // a direct-form layout gives its kernels no shared memory
+        spmv_direct<T, VT>(A, av, gather, pre, epi);
+        return;
+    }
     const int lane = threadIdx.x & 31;
     const int sub = lane & (A.lanes - 1);
     const int cap = A.cap;
@@ -753,15 +780,17 @@ __device__ __forceinline__ void spmv_ws(const Mat& A, const VT* __restrict__ av,
     __syncthreads();
 }
 
-// Product with a plain vector gather in one of five compiled forms (the
+// Product with a plain vector gather in one of six compiled forms (the
 // host picks one per matrix, so each kernel instantiation carries a single
 // path): FORM 0 register staging (spmv_rows); FORM 1 cp.async value/column
 // staging with register gathers; FORM 2 cp.async staging and gathers; FORM 3
-// the warp pipeline (spmv_pipe); FORM 4 producer/consumer warps (spmv_ws).
+// the warp pipeline (spmv_pipe); FORM 4 producer/consumer warps (spmv_ws);
+// FORM 5 the direct form (spmv_direct).
 template <typename T, int FORM, typename VT, typename XT, bool COH = false, class Pre, class Epi>
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
-    if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
+    if constexpr (FORM == 5) spmv_direct<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
+    else if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
     else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
     else if constexpr (FORM == 4) spmv_ws<T, VT, XT>(A, av, v, pre, epi, wsm);
     else spmv_rows_async<T, VT, XT, FORM == 2, COH>(A, av, v, pre, epi, wsm);
@@ -859,7 +888,7 @@ __device__ __forceinline__ float neg_prod(float l, float x) { return df_round(tw
 // ----------------------------------------------------------------- SpMV API
 // y = A x, and dot[sys] = x.y when dot != nullptr.
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const T* __restrict__ av,
+__global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spmv(Mat A, Sys S, const T* __restrict__ av,
                                                             const T* __restrict__ x, T* __restrict__ y, double* dot) {
     using acc_t = typename Prec<T>::acc;
     SYS_PROLOGUE
@@ -881,23 +910,44 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spmv(Mat A, Sys S, const 
 }
 
 // ----------------------------------------------------------------- iteration
-// ||b - A round(x)||^2 over this CTA's rows (the true-residual check).  Kept
-// out of line: it runs only when the recursive residual has met the
-// tolerance, and inlining it would cost the main product registers.
+// ||b - A round(x)||^2 over this CTA's rows (the true-residual check).  For
+// the staged forms it is kept out of line: it runs only when the recursive
+// residual has met the tolerance, and inlining it would cost the main
+// product registers.  The direct form inlines it: there the out-of-line call
+// (its stack frame) slowed the product in the running iteration by half
+// (measured on B300 at six resident CTAs per SM), while the inlined pass
+// fits the same registers.
+template <typename T, bool COH>
+__device__ __forceinline__ typename Prec<T>::acc residual_direct(const Mat& A, const T* __restrict__ av,
+                                                                 const typename Prec<T>::xw* x,
+                                                                 const T* __restrict__ b) {
+    using acc_t = typename Prec<T>::acc;
+    acc_t tr2 = Prec<T>::zero();
+    spmv_direct<T, T>(A, av, GatherX<T, COH>{x}, [&](int i) { return b[i]; },
+                      [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); });
+    return tr2;
+}
 template <typename T, int FORM, bool COH = false>
-__device__ __noinline__ typename Prec<T>::acc residual_pass(const Mat& A, const T* __restrict__ av,
-                                                            const typename Prec<T>::xw* x,
-                                                            const T* __restrict__ b, double* dsm) {
+__device__ __noinline__ typename Prec<T>::acc residual_staged(const Mat& A, const T* __restrict__ av,
+                                                              const typename Prec<T>::xw* x,
+                                                              const T* __restrict__ b, double* dsm) {
     using acc_t = typename Prec<T>::acc;
     acc_t tr2 = Prec<T>::zero();
     spmv_rows<T, T>(A, av, GatherX<T, COH>{x}, [&](int i) { return b[i]; },
                     [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
     return tr2;
 }
+template <typename T, int FORM, bool COH = false>
+__device__ __forceinline__ typename Prec<T>::acc residual_pass(const Mat& A, const T* __restrict__ av,
+                                                               const typename Prec<T>::xw* x,
+                                                               const T* __restrict__ b, double* dsm) {
+    if constexpr (FORM == 5) return residual_direct<T, COH>(A, av, x, b);
+    else return residual_staged<T, FORM, COH>(A, av, x, b, dsm);
+}
 
 // q = A p, delta = p.q; with `check` set, ||b - A round(x)||^2 first.
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, IterMinCtas<T>::value)
+__global__ void __launch_bounds__(NT, (ProductCtas<T, FORM>::value))
     k_spmv_iter(Mat A, Sys S, const T* __restrict__ av, const typename Prec<T>::w* __restrict__ p,
                 typename Prec<T>::w* __restrict__ q, const typename Prec<T>::xw* __restrict__ x,
                 const T* __restrict__ b) {
@@ -1093,7 +1143,7 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __re
 // SPAI, first product: t = G^T r (explicit transposed CSR of G; G values
 // are per system, [batch][nnz(G)]).
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, long long nnzg,
+__global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_t(Mat GT, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gtv,
                                                               const typename Prec<T>::w* __restrict__ r,
                                                               typename Prec<T>::w* __restrict__ t) {
@@ -1109,7 +1159,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_t(Mat GT, Sys S, lon
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, SPMV_MIN_CTAS) k_spai_z(Mat G, Sys S, long long nnzg,
+__global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_z(Mat G, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gv,
                                                               const typename Prec<T>::w* __restrict__ t,
                                                               const typename Prec<T>::w* __restrict__ r,
@@ -1472,9 +1522,17 @@ __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict
                                                T* __restrict__ dA) {
     SYS_PROLOGUE
     extern __shared__ __align__(16) double dsm[];
+    lam += vo; x += vo; dA += ao;
+    if (A.direct) {   // thread per row (the layout gives no shared memory)
+        for (int row = blockIdx.x * NT + threadIdx.x; row < A.n; row += gridDim.x * NT) {
+            const int lo = ld_nc(A.rp + row), hi = ld_nc(A.rp + row + 1);
+            const T li = lam[row];
+            for (int k = lo; k < hi; ++k) __stcs(dA + k, neg_prod(li, ld_nc(x + ld_stream(A.ci + k))));
+        }
+        return;
+    }
     int* srow = reinterpret_cast<int*>(dsm + (threadIdx.x >> 5) * A.wstride);
     const int lane = threadIdx.x & 31;
-    lam += vo; x += vo; dA += ao;
     const int sub = lane & (A.lanes - 1);
     const int ngroups = (A.n + (32 >> A.lshift) - 1) >> (5 - A.lshift);
     const int nwarps = (gridDim.x * NT) >> 5;

@@ -134,6 +134,7 @@ struct Layout {
     int stages = 0;   // bulk-copy forms: ring stages
     int form = 0;     // compiled form of the product kernels (spmv_vec)
     size_t smem = 0;  // their dynamic shared memory
+    int maxrow = 0;   // longest row
 };
 
 struct sla_csr {
@@ -163,6 +164,7 @@ struct sla_csr {
     bool vals_aligned = false;  // values 16-byte aligned for every system (bulk-copy forms)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
     bool ws = false;            // SLA_PRODUCER_CONSUMER: producer/consumer product where it applies
+    bool staged = false;        // SLA_STAGED: never the direct form
     bool time_product = false;  // SLA_TIME_PRODUCT: events around one product kernel per graph launch
     double prod_ms = 0.0;       // summed product-kernel durations (sla_product_time)
     long long prod_n = 0;
@@ -347,7 +349,8 @@ static void with_form(int form, F&& f) {
         case 1: f(std::integral_constant<int, 1>{}); break;
         case 2: f(std::integral_constant<int, 2>{}); break;
         case 3: f(std::integral_constant<int, 3>{}); break;
-        default: f(std::integral_constant<int, 4>{}); break;
+        case 4: f(std::integral_constant<int, 4>{}); break;
+        default: f(std::integral_constant<int, 5>{}); break;
     }
 }
 
@@ -371,11 +374,23 @@ static int ws_stages(int tcap, size_t vb) {
     return 0;
 }
 
+// Longest row the direct form (FORM 5, thread per row) takes; a matrix with
+// longer rows uses the staged forms, whose warps share long rows (measured:
+// the kNN Laplacian with 13-28 entries per row runs its product in half the
+// time staged).
+#ifndef SLA_DIRECT_MAXROW
+#define SLA_DIRECT_MAXROW 16
+#endif
+
 template <typename T>
-static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb) {
+static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb, bool allow_direct = true) {
     const int wss = L->tcap > 0 && aligned && h->ws ? ws_stages(L->tcap, vb) : 0;
     L->stages = wss == 0 && L->ccap > 0 && aligned && h->pipeline ? pipe_stages(L->ccap, vb) : 0;
-    if (wss > 0) {
+    const bool direct = allow_direct && !h->staged && L->maxrow <= SLA_DIRECT_MAXROW;
+    if (wss == 0 && L->stages == 0 && direct) {
+        L->form = 5;
+        L->smem = 0;
+    } else if (wss > 0) {
         L->form = 4;
         L->stages = wss;
         const size_t rows = (size_t)NWARP * L->cap * 2 * sizeof(double);   // warp staging of the check pass
@@ -392,14 +407,16 @@ static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb)
     sla_status st = SLA_OK;
     with_form(L->form, [&](auto f) { st = occupancy(k_spmv_iter<T, decltype(f)::value>, L->smem, &per); });
     TRY(st);
-    const long long units = L->form == 4 ? ((long long)h->n + WS_ROWS - 1) / WS_ROWS
-                                         : group_ctas(h->n, L->form == 3 ? 1 : L->lanes);
+    const long long units = L->form == 5   ? ((long long)h->n + NT - 1) / NT
+                            : L->form == 4 ? ((long long)h->n + WS_ROWS - 1) / WS_ROWS
+                                           : group_ctas(h->n, L->form == 3 ? 1 : L->lanes);
     L->gx = grid_x(h, units, per);
     return SLA_OK;
 }
 
-static sla_status set_form_any(const sla_csr* h, Layout* L, bool aligned, size_t vb) {
-    return h->dt == SLA_F64 ? set_form<double>(h, L, aligned, vb) : set_form<float>(h, L, aligned, vb);
+static sla_status set_form_any(const sla_csr* h, Layout* L, bool aligned, size_t vb, bool allow_direct = true) {
+    return h->dt == SLA_F64 ? set_form<double>(h, L, aligned, vb, allow_direct)
+                            : set_form<float>(h, L, aligned, vb, allow_direct);
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -412,7 +429,10 @@ static bool vals_aligned(const sla_csr* h, const void* vals) {
 // reduction step costs a full warp issue on the slow fp64 pipe, so fewer,
 // longer-running threads (each with two pairs in flight per trip) beat a
 // fully occupied grid here.
-static constexpr int VEC_CTAS_PER_SM = 2;
+#ifndef SLA_VEC_CTAS
+#define SLA_VEC_CTAS 2
+#endif
+static constexpr int VEC_CTAS_PER_SM = SLA_VEC_CTAS;
 static int gx_vec(const sla_csr* h) { return grid_x(h, vec_units(h), VEC_CTAS_PER_SM); }
 
 static Sys sys_of(sla_csr* h) {
@@ -443,6 +463,7 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     m.ccap = L.form == 4 ? L.tcap : L.ccap;   // entries per stage of the bulk-copy forms
     m.stages = L.stages;
     m.err = err;
+    m.direct = L.form == 5 ? 1 : 0;
     return m;
 }
 static Mat mat_A(const sla_csr* h) { return mat_of(h->rp, h->ci, h->n, h->nnz, h->LA, &h->ctl.as<Ctrl>()->err); }
@@ -500,7 +521,7 @@ static sla_status group_max(const int* rp, int n, int rows, int* out, cudaStream
 static constexpr int NEAR_WINDOW = 65536;
 
 static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, long long nnz, Layout* L,
-                                bool aligned, size_t vb, cudaStream_t s) {
+                                bool aligned, size_t vb, cudaStream_t s, bool allow_direct = true) {
     {
         DevBuf far;
         TRY(far.alloc(sizeof(unsigned long long)));
@@ -513,6 +534,7 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
         CU(cudaStreamSynchronize(s));
         L->gasync = (double)f > 0.1 * (double)nnz ? 1 : 0;
     }
+    TRY(group_max(rp, h->n, 1, &L->maxrow, s));
     for (int lanes = SLA_MIN_LANES; lanes <= 4; lanes *= 2) {
         int m = 0;
         TRY(group_max(rp, h->n, 32 / lanes, &m, s));
@@ -547,7 +569,7 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
         TRY(read_int(m.as<int>(), &tc, s));
         L->tcap = tc < 4 ? 4 : tc;
     }
-    return set_form_any(h, L, aligned, vb);
+    return set_form_any(h, L, aligned, vb, allow_direct);
 }
 
 // ===================================================================== reordering
@@ -988,7 +1010,9 @@ static sla_status fused_grid(const sla_csr* h, int* gx) {
     });
     if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
     long long g = (long long)per * h->sms / h->batch;
-    const long long work = std::max(group_ctas(h->n, h->LI.form == 3 ? 1 : h->LI.lanes), vec_units(h));
+    const long long rows_work = h->LI.form == 5 ? ((long long)h->n + NT - 1) / NT
+                                                : group_ctas(h->n, h->LI.form == 3 ? 1 : h->LI.lanes);
+    const long long work = std::max(rows_work, vec_units(h));
     if (g > work) g = work;
     *gx = (int)g;
     return SLA_OK;
@@ -1227,13 +1251,14 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
 }
 
 // ===================================================================== BiCGStab
-// Dispatch over the register / cp.async staging forms (the BiCGStab product
-// kernels are built for these only).
+// Dispatch over the register / cp.async staging forms and the direct form
+// (the BiCGStab product kernels are built for these only).
 template <class F>
 static void with_form_rc(int form, F&& f) {
     switch (form) {
         case 0: f(std::integral_constant<int, 0>{}); break;
         case 1: f(std::integral_constant<int, 1>{}); break;
+        case 5: f(std::integral_constant<int, 5>{}); break;
         default: f(std::integral_constant<int, 2>{}); break;
     }
 }
@@ -1257,12 +1282,15 @@ static void transpose_pattern(int n, const std::vector<int>& rp, const std::vect
 }
 
 // Workspace of BiCGStab (and, for `transposed`, the explicit transpose of
-// the iteration matrix); built once per handle.
+// the iteration matrix); built once per handle.  Its products take the
+// staged forms: on the 3D convection-diffusion system the direct form's
+// product was slower inside the BiCGStab iteration (71.9 against 65.1 us,
+// measured on B300), unlike in the CG iteration.
 static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
     if (!h->bicg_ready) {
         TRY(h->rh.alloc(sizeof(double) * (size_t)h->n * h->batch));
         h->LB = h->LI;
-        TRY(set_form_any(h, &h->LB, false, sizeof(double)));
+        TRY(set_form_any(h, &h->LB, false, sizeof(double), false));
         h->bicg_ready = true;
     }
     if (transposed && !h->tr_ready) {
@@ -1275,7 +1303,7 @@ static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
         TRY(to_device(h->tci, tci));
         TRY(to_device(h->tsrc, src));
         TRY(h->tvals.alloc(sizeof(double) * (size_t)h->nnz * h->batch));
-        TRY(choose_layout(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, &h->LT, false, sizeof(double), s));
+        TRY(choose_layout(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, &h->LT, false, sizeof(double), s, false));
         h->tr_ready = true;
     }
     return ensure_pstride(h);
@@ -1507,6 +1535,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     h->vals_aligned = vals_aligned(h, d_vals);
     h->pipeline = (flags & SLA_WARP_PIPELINE) != 0;
     h->ws = (flags & SLA_PRODUCER_CONSUMER) != 0;
+    h->staged = (flags & SLA_STAGED) != 0;
     h->time_product = (flags & SLA_TIME_PRODUCT) != 0;
     h->persistent = (flags & SLA_PERSISTENT) != 0;
     {
