@@ -94,31 +94,31 @@ template <int W>
 __device__ __forceinline__ Vd<W> vld(const double* p, int i) {
     Vd<W> o;
     if constexpr (W == 2) {
-        const double2 t = reinterpret_cast<const double2*>(p)[i];
+        const double2 t = ld_vec(reinterpret_cast<const double2*>(p) + i);
         o.e[0] = t.x;
         o.e[1] = t.y;
     } else {
-        o.e[0] = p[i];
+        o.e[0] = ld_vec(p + i);
     }
     return o;
 }
-// evict-first load, for a vector read for the last time in the iteration
+// a vector read for the last time in the iteration
 template <int W>
 __device__ __forceinline__ Vd<W> vld_last(const double* p, int i) {
     Vd<W> o;
     if constexpr (W == 2) {
-        const double2 t = __ldcs(reinterpret_cast<const double2*>(p) + i);
+        const double2 t = ld_vec_last(reinterpret_cast<const double2*>(p) + i);
         o.e[0] = t.x;
         o.e[1] = t.y;
     } else {
-        o.e[0] = __ldcs(p + i);
+        o.e[0] = ld_vec_last(p + i);
     }
     return o;
 }
 template <int W>
 __device__ __forceinline__ void vst(double* p, int i, const Vd<W>& v) {
-    if constexpr (W == 2) reinterpret_cast<double2*>(p)[i] = make_double2(v.e[0], v.e[1]);
-    else p[i] = v.e[0];
+    if constexpr (W == 2) st_vec(reinterpret_cast<double2*>(p) + i, make_double2(v.e[0], v.e[1]));
+    else st_vec(p + i, v.e[0]);
 }
 
 #define BICG_LOOP(W) for (int i = blockIdx.x * NT + threadIdx.x; i < S.n / (W); i += gridDim.x * NT)
@@ -157,9 +157,9 @@ __global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     const bool check = ld_cg(&st->check) != 0;
     double tr2 = 0.0, sigma = 0.0;
     if (check) tr2 = residual_pass<double, FORM>(A, av, y, b, dsm);
-    spmv_vec<double, FORM, double, double>(A, av, p, [&](int i) { return rh[i]; },
+    spmv_vec<double, FORM, double, double>(A, av, p, [&](int i) { return ld_vec(rh + i); },
                                            [&](int i, double s, double rhi) {
-                                               v[i] = s;
+                                               st_vec(v + i, s);
                                                sigma = fma(rhi, s, sigma);
                                            },
                                            dsm);
@@ -194,9 +194,9 @@ __global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     __shared__ double red[RED_DOUBLES];
     av += ao; s += vo; t += vo;
     double tt = 0.0, ts = 0.0;
-    spmv_vec<double, FORM, double, double>(A, av, s, [&](int i) { return s[i]; },
+    spmv_vec<double, FORM, double, double>(A, av, s, [&](int i) { return ld_vec(s + i); },
                                            [&](int i, double q, double si) {
-                                               t[i] = q;
+                                               st_vec(t + i, q);
                                                tt = fma(q, q, tt);
                                                ts = fma(q, si, ts);
                                            },

@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace sla {
 
@@ -115,6 +116,93 @@ __device__ __forceinline__ unsigned long long l2_evict_last() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
     return pol;
 }
+// SLA_L2_KEEP = 1 marks every working-vector access L2 evict-last and the
+// matrix stream evict-first, so that the vectors (read and rewritten every
+// iteration) would stay resident in L2.  Measured on B300 (c2, c4, the 3D
+// convection-diffusion BiCGStab): no change in iterations per second, since
+// the iteration is bound by fp64 throughput and load latency rather than by
+// the vectors' HBM traffic; off by default.  Policies come from a pure asm,
+// so the compiler hoists them out of loops.
+#ifndef SLA_L2_KEEP
+#define SLA_L2_KEEP 0
+#endif
+__device__ __forceinline__ unsigned long long pol_keep() {
+    unsigned long long pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ unsigned long long pol_stream() {
+    unsigned long long pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+// 4-, 8- and 16-byte loads and stores with an L2 policy (any trivially
+// copyable type of that size).  NC: read-only path (data not written during
+// the kernel).
+template <bool NC, typename T>
+__device__ __forceinline__ T ld_pol(const T* p, unsigned long long pol) {
+    static_assert(sizeof(T) == 4 || sizeof(T) == 8 || sizeof(T) == 16, "size");
+    T out;
+    if constexpr (sizeof(T) == 4) {
+        unsigned v;
+        if (NC) asm("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;\n" : "=r"(v) : "l"(p), "l"(pol));
+        else asm("ld.global.L2::cache_hint.b32 %0, [%1], %2;\n" : "=r"(v) : "l"(p), "l"(pol));
+        memcpy(&out, &v, 4);
+    } else if constexpr (sizeof(T) == 8) {
+        unsigned long long v;
+        if (NC) asm("ld.global.nc.L2::cache_hint.b64 %0, [%1], %2;\n" : "=l"(v) : "l"(p), "l"(pol));
+        else asm("ld.global.L2::cache_hint.b64 %0, [%1], %2;\n" : "=l"(v) : "l"(p), "l"(pol));
+        memcpy(&out, &v, 8);
+    } else {
+        unsigned long long a, b;
+        if (NC) asm("ld.global.nc.L2::cache_hint.v2.b64 {%0, %1}, [%2], %3;\n" : "=l"(a), "=l"(b) : "l"(p), "l"(pol));
+        else asm("ld.global.L2::cache_hint.v2.b64 {%0, %1}, [%2], %3;\n" : "=l"(a), "=l"(b) : "l"(p), "l"(pol));
+        unsigned long long v[2] = {a, b};
+        memcpy(&out, v, 16);
+    }
+    return out;
+}
+template <typename T>
+__device__ __forceinline__ void st_pol(T* p, const T& val, unsigned long long pol) {
+    static_assert(sizeof(T) == 4 || sizeof(T) == 8 || sizeof(T) == 16, "size");
+    if constexpr (sizeof(T) == 4) {
+        unsigned v;
+        memcpy(&v, &val, 4);
+        asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;\n" :: "l"(p), "r"(v), "l"(pol) : "memory");
+    } else if constexpr (sizeof(T) == 8) {
+        unsigned long long v;
+        memcpy(&v, &val, 8);
+        asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;\n" :: "l"(p), "l"(v), "l"(pol) : "memory");
+    } else {
+        unsigned long long v[2];
+        memcpy(v, &val, 16);
+        asm volatile("st.global.L2::cache_hint.v2.b64 [%0], {%1, %2}, %3;\n" :: "l"(p), "l"(v[0]), "l"(v[1]), "l"(pol)
+                     : "memory");
+    }
+}
+// A working-vector load / store (kept in L2 when SLA_L2_KEEP) and a matrix
+// stream load (evict-first).
+template <typename T>
+__device__ __forceinline__ T ld_vec(const T* p) {
+    if constexpr (SLA_L2_KEEP) return ld_pol<false>(p, pol_keep());
+    else return *p;
+}
+template <typename T>
+__device__ __forceinline__ T ld_vec_last(const T* p) {   // last read of the vector in this kernel
+    if constexpr (SLA_L2_KEEP) return ld_pol<false>(p, pol_keep());
+    else return __ldcs(p);
+}
+template <typename T>
+__device__ __forceinline__ void st_vec(T* p, const T& v) {
+    if constexpr (SLA_L2_KEEP) st_pol(p, v, pol_keep());
+    else *p = v;
+}
+template <typename T>
+__device__ __forceinline__ T ld_mat(const T* p) {
+    if constexpr (SLA_L2_KEEP) return ld_pol<true>(p, pol_stream());
+    else return __ldcs(p);
+}
+
 template <int BYTES>
 __device__ __forceinline__ void cp_async(void* smem, const void* gmem, unsigned long long pol) {
     const unsigned s = (unsigned)__cvta_generic_to_shared(smem);

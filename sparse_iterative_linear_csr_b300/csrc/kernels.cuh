@@ -133,6 +133,7 @@ __device__ __forceinline__ float x_out_of(float2 x) { return __fadd_rn(x.x, x.y)
 template <typename T, bool COH = false>
 __device__ __forceinline__ T ld_gather(const T* p) {
     if constexpr (COH) return ld_coh(p);
+    else if constexpr (SLA_L2_KEEP) return ld_pol<true>(p, pol_keep());
     else return ld_nc(p);
 }
 template <typename T, bool COH = false>
@@ -230,7 +231,7 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
         const int lo = ld_nc(A.rp + row), hi = ld_nc(A.rp + row + 1);
         const auto carried = pre(row);
         acc_t s = Prec<T>::zero();
-        for (int k = lo; k < hi; ++k) mac(s, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+        for (int k = lo; k < hi; ++k) mac(s, ld_mat(av + k), gather(ld_mat(A.ci + k)));
         epi(row, s, carried);
     }
 }
@@ -965,10 +966,10 @@ __global__ void __launch_bounds__(NT, (ProductCtas<T, FORM>::value))
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
     if (check) tr2 = residual_pass<T, FORM>(A, av, x, b, dsm);
-    spmv_vec<T, FORM, T, W>(A, av, p, [&](int i) { return p[i]; },
+    spmv_vec<T, FORM, T, W>(A, av, p, [&](int i) { return ld_vec(p + i); },
                       [&](int i, acc_t s, W pi) {
                           const W qi = to_w(s);
-                          q[i] = qi;
+                          st_vec(q + i, qi);
                           dot_acc(delta, pi, qi);
                       },
                       dsm);
@@ -1039,9 +1040,9 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::w* __res
             for (int u = 0; u < VU; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    q2[u] = ld_stream(reinterpret_cast<const P2*>(q) + i);
-                    r2[u] = reinterpret_cast<const P2*>(r)[i];
-                    if (PC == 1) d2[u] = ld_nc(reinterpret_cast<const X2*>(dinv) + i);
+                    q2[u] = ld_vec_last(reinterpret_cast<const P2*>(q) + i);
+                    r2[u] = ld_vec(reinterpret_cast<const P2*>(r) + i);
+                    if (PC == 1) d2[u] = ld_gather(reinterpret_cast<const X2*>(dinv) + i);
                 }
             }
 #pragma unroll
@@ -1055,17 +1056,17 @@ __global__ void __launch_bounds__(NT) k_update(Sys S, typename Prec<T>::w* __res
                     if (PC == 1) split2(d2[u], da, db);
                     update_r<PC>(alpha, ra, qa, da, za, g, rz);
                     update_r<PC>(alpha, rb, qb, db, zb, g, rz);
-                    reinterpret_cast<P2*>(r)[i] = join2(ra, rb);
-                    if (PC == 1) reinterpret_cast<P2*>(z)[i] = join2(za, zb);
+                    st_vec(reinterpret_cast<P2*>(r) + i, join2(ra, rb));
+                    if (PC == 1) st_vec(reinterpret_cast<P2*>(z) + i, join2(za, zb));
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-            W ri = r[i], zi{};
-            update_r<PC>(alpha, ri, ld_stream(q + i), PC == 1 ? dinv[i] : XW{}, zi, g, rz);
-            r[i] = ri;
-            if (PC == 1) z[i] = zi;
+            W ri = ld_vec(r + i), zi{};
+            update_r<PC>(alpha, ri, ld_vec_last(q + i), PC == 1 ? ld_gather(dinv + i) : XW{}, zi, g, rz);
+            st_vec(r + i, ri);
+            if (PC == 1) st_vec(z + i, zi);
         }
     }
     double v[2] = {Prec<T>::total(g), Prec<T>::total(rz)}, tot[2];
@@ -1103,9 +1104,9 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __re
             for (int u = 0; u < VU; ++u) {
                 const int i = i0 + u * stride;
                 if (i < n2) {
-                    p2[u] = INIT ? P2{} : reinterpret_cast<const P2*>(p)[i];
-                    if (xp) x2[u] = reinterpret_cast<const X2*>(x)[i];
-                    if (more) z2[u] = ld_stream(reinterpret_cast<const P2*>(zs) + i);
+                    p2[u] = INIT ? P2{} : ld_vec(reinterpret_cast<const P2*>(p) + i);
+                    if (xp) x2[u] = ld_vec(reinterpret_cast<const X2*>(x) + i);
+                    if (more) z2[u] = ld_vec_last(reinterpret_cast<const P2*>(zs) + i);
                 }
             }
 #pragma unroll
@@ -1119,23 +1120,23 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __re
                         split2(x2[u], xa, xb);
                         xa = to_w(afma(alpha, ld_w(pa), ld_w(xa)));
                         xb = to_w(afma(alpha, ld_w(pb), ld_w(xb)));
-                        reinterpret_cast<X2*>(x)[i] = join2(xa, xb);
+                        st_vec(reinterpret_cast<X2*>(x) + i, join2(xa, xb));
                     }
                     if (more) {
                         W za, zb;
                         split2(z2[u], za, zb);
-                        reinterpret_cast<P2*>(p)[i] =
-                            INIT ? join2(za, zb)
-                                 : join2(to_w(afma(beta, ld_w(pa), ld_w(za))), to_w(afma(beta, ld_w(pb), ld_w(zb))));
+                        st_vec(reinterpret_cast<P2*>(p) + i,
+                               INIT ? join2(za, zb)
+                                    : join2(to_w(afma(beta, ld_w(pa), ld_w(za))), to_w(afma(beta, ld_w(pb), ld_w(zb)))));
                     }
                 }
             }
         }
     } else {
         for (int i = blockIdx.x * NT + threadIdx.x; i < S.n; i += gridDim.x * NT) {
-            const W pi = INIT ? W{} : p[i];
-            if (xp) x[i] = to_w(afma(alpha, ld_w(pi), ld_w(x[i])));
-            if (more) p[i] = INIT ? zs[i] : to_w(afma(beta, ld_w(pi), ld_w(zs[i])));
+            const W pi = INIT ? W{} : ld_vec(p + i);
+            if (xp) st_vec(x + i, to_w(afma(alpha, ld_w(pi), ld_w(ld_vec(x + i)))));
+            if (more) st_vec(p + i, INIT ? ld_vec_last(zs + i) : to_w(afma(beta, ld_w(pi), ld_w(ld_vec_last(zs + i)))));
         }
     }
 }
@@ -1154,7 +1155,7 @@ __global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CT
     extern __shared__ __align__(16) double dsm[];
     gtv += (size_t)sys * nnzg; r += vo; t += vo;
     spmv_vec<T, FORM, typename Prec<T>::gv, W>(GT, gtv, r, [](int) { return W{}; },
-                                         [&](int i, acc_t s, W) { t[i] = to_w(s); }, dsm);
+                                         [&](int i, acc_t s, W) { st_vec(t + i, to_w(s)); }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
@@ -1176,7 +1177,7 @@ __global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CT
     spmv_vec<T, FORM, typename Prec<T>::gv, W>(G, gv, t, [&](int i) { return r[i]; },
                                          [&](int i, acc_t s, W ri) {
                                              const W zi = to_w(afma(e, ld_w(ri), s));
-                                             z[i] = zi;
+                                             st_vec(z + i, zi);
                                              dot_acc(rz, ri, zi);
                                          },
                                          dsm);
