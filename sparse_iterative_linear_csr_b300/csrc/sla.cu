@@ -381,12 +381,17 @@ static int ws_stages(int tcap, size_t vb) {
 #ifndef SLA_DIRECT_MAXROW
 #define SLA_DIRECT_MAXROW 16
 #endif
+// The same bound for the SPAI factors G and G^T.
+#ifndef SLA_DIRECT_MAXROW_G
+#define SLA_DIRECT_MAXROW_G SLA_DIRECT_MAXROW
+#endif
 
 template <typename T>
-static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb, bool allow_direct = true) {
+static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb,
+                           int direct_maxrow = SLA_DIRECT_MAXROW) {
     const int wss = L->tcap > 0 && aligned && h->ws ? ws_stages(L->tcap, vb) : 0;
     L->stages = wss == 0 && L->ccap > 0 && aligned && h->pipeline ? pipe_stages(L->ccap, vb) : 0;
-    const bool direct = allow_direct && !h->staged && L->maxrow <= SLA_DIRECT_MAXROW;
+    const bool direct = !h->staged && L->maxrow <= direct_maxrow;
     if (wss == 0 && L->stages == 0 && direct) {
         L->form = 5;
         L->smem = 0;
@@ -414,9 +419,11 @@ static sla_status set_form(const sla_csr* h, Layout* L, bool aligned, size_t vb,
     return SLA_OK;
 }
 
-static sla_status set_form_any(const sla_csr* h, Layout* L, bool aligned, size_t vb, bool allow_direct = true) {
-    return h->dt == SLA_F64 ? set_form<double>(h, L, aligned, vb, allow_direct)
-                            : set_form<float>(h, L, aligned, vb, allow_direct);
+// direct_maxrow: longest row for which the direct form may be chosen (0: never).
+static sla_status set_form_any(const sla_csr* h, Layout* L, bool aligned, size_t vb,
+                               int direct_maxrow = SLA_DIRECT_MAXROW) {
+    return h->dt == SLA_F64 ? set_form<double>(h, L, aligned, vb, direct_maxrow)
+                            : set_form<float>(h, L, aligned, vb, direct_maxrow);
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -521,7 +528,7 @@ static sla_status group_max(const int* rp, int n, int rows, int* out, cudaStream
 static constexpr int NEAR_WINDOW = 65536;
 
 static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, long long nnz, Layout* L,
-                                bool aligned, size_t vb, cudaStream_t s, bool allow_direct = true) {
+                                bool aligned, size_t vb, cudaStream_t s, int direct_maxrow = SLA_DIRECT_MAXROW) {
     {
         DevBuf far;
         TRY(far.alloc(sizeof(unsigned long long)));
@@ -569,7 +576,7 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
         TRY(read_int(m.as<int>(), &tc, s));
         L->tcap = tc < 4 ? 4 : tc;
     }
-    return set_form_any(h, L, aligned, vb, allow_direct);
+    return set_form_any(h, L, aligned, vb, direct_maxrow);
 }
 
 // ===================================================================== reordering
@@ -843,8 +850,10 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
             std::swap(pt[2]->bytes, vals2.bytes);
         }
     }
-    TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, true, sizeof(double), s));
-    TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s));
+    TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, true, sizeof(double), s,
+                      SLA_DIRECT_MAXROW_G));
+    TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s,
+                      SLA_DIRECT_MAXROW_G));
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
     h->spai_ready = true;
     return ensure_pstride(h);
@@ -1290,7 +1299,7 @@ static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
     if (!h->bicg_ready) {
         TRY(h->rh.alloc(sizeof(double) * (size_t)h->n * h->batch));
         h->LB = h->LI;
-        TRY(set_form_any(h, &h->LB, false, sizeof(double), false));
+        TRY(set_form_any(h, &h->LB, false, sizeof(double), 0));
         h->bicg_ready = true;
     }
     if (transposed && !h->tr_ready) {
@@ -1303,7 +1312,7 @@ static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
         TRY(to_device(h->tci, tci));
         TRY(to_device(h->tsrc, src));
         TRY(h->tvals.alloc(sizeof(double) * (size_t)h->nnz * h->batch));
-        TRY(choose_layout(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, &h->LT, false, sizeof(double), s, false));
+        TRY(choose_layout(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, &h->LT, false, sizeof(double), s, 0));
         h->tr_ready = true;
     }
     return ensure_pstride(h);
