@@ -1,0 +1,60 @@
+"""The benchmark's algorithmic byte model and method dispatch (CPU only):
+the per-iteration and per-launch byte counts equal the stated formulas
+(values and indices of a shared pattern counted once, 8-byte working
+vectors), and each workload is timed on the oracle's solver for its own
+method."""
+import numpy as np
+
+import bench
+from workloads import build
+
+
+def _mat(w, s):
+    A = w.A
+    return s * A.nnz * A.batch + 4 * A.nnz + 4 * (A.n + 1)
+
+
+def test_cg_and_jacobi_models():
+    w = build("c4", N=12)                       # CG, fp64
+    bm = bench.byte_model(w)
+    n = w.A.n
+    assert bm["per_iteration"] == 12 * w.A.nnz + 4 * (n + 1) + 11 * 8 * n
+    assert bm["product_per_launch"] == 12 * w.A.nnz + 4 * (n + 1) + 16 * n
+    w = build("c2", N=20)                       # Jacobi-PCG, fp64
+    assert bench.byte_model(w)["per_iteration"] == _mat(w, 8) + 13 * 8 * w.A.n
+    w = build("c3", N=16, batch=3)              # batched fp32 values, 8-byte working vectors
+    bm = bench.byte_model(w)
+    assert bm["per_iteration"] == _mat(w, 4) + 13 * 8 * w.A.n * 3
+    assert bm["spmv_dot_per_launch"] == _mat(w, 4) + 2 * 4 * w.A.n * 3
+
+
+def test_bicgstab_model():
+    w = build("cd3", N=10)
+    bm = bench.byte_model(w)
+    n, nnz = w.A.n, w.A.nnz
+    mat = 12 * nnz + 4 * (n + 1)
+    assert bench.method_of(w) == "bicgstab"
+    assert bm["per_iteration"] == 2 * mat + 19 * 8 * n
+    assert bm["product_per_launch"] == mat + 3 * 8 * n
+    assert bench.metric_of(w) == bench.METRIC_BICG
+    assert bench.metric_of(build("c1", N=8)) == bench.METRIC
+
+
+def test_full_size_models_match_the_stated_figures():
+    # c4 at 128^3: 367.9 MB per CG iteration, 216.9 MB per product launch
+    w = build("c4")
+    bm = bench.byte_model(w)
+    assert round(bm["per_iteration"] / 1e6, 1) == 367.9
+    assert round(bm["product_per_launch"] / 1e6, 1) == 216.9
+
+
+def test_oracle_dispatch_follows_the_method():
+    w = build("cd3", N=8)
+    x, info = bench.oracle_solve(w, w.A, w.b, 10000)
+    assert info["status"] == "ok"
+    D = w.A.dense()
+    assert np.linalg.norm(D @ x - w.b) <= 2 * w.tol * np.linalg.norm(w.b)
+    assert np.abs(D - D.T).max() > 0.1          # nonsymmetric: CG would not apply
+    w = build("c1", N=8)
+    x, info = bench.oracle_solve(w, w.A, w.b, 10000)
+    assert info["status"] == "ok"
