@@ -202,6 +202,24 @@ def bus_id_of(dev):
         return None
 
 
+def host_cpu():
+    """Model name of the host's cores and the number the process may use."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except AttributeError:
+        avail = os.cpu_count() or 1
+    return {"model": model, "available_cores": avail}
+
+
 def cpu_sample(w, budget_s=12.0):
     """The oracle as it stands, single-threaded, on a bounded number of
     iterations of the same workload's method (first system of a batch)."""
@@ -222,7 +240,7 @@ def cpu_sample(w, budget_s=12.0):
     name = "BiCGStab" if method_of(w) == "bicgstab" else "PCG"
     return {"value": its / dt, "unit": "iterations/s", "cores": 1, "kind": "oracle",
             "sample": f"first {its} {name} iterations of the forward solve (system 0), {dt:.1f} s, "
-                      f"single-threaded fp64 C oracle"}
+                      f"single-threaded fp64 C oracle", "host": host_cpu()}
 
 
 def run_reference(args, w, rank):
@@ -254,7 +272,8 @@ def run_reference(args, w, rank):
             "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": w.A.n, "nnz": w.A.nnz,
                        "pc": w.pc, "tol": w.tol},
             "cpu_baseline": {"value": v, "unit": "iterations/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{cap} {name} iterations per step of the forward solve (system 0)"},
+                             "sample": f"{cap} {name} iterations per step of the forward solve (system 0)",
+                             "host": host_cpu()},
             "e2e": {"value": v, "unit": "iterations/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
