@@ -99,3 +99,43 @@ def test_knn_laplacian_small():
     assert np.all(off <= 0)
     np.testing.assert_allclose(np.diag(D), -off.sum(axis=1) + 1e-3, rtol=1e-13)
     assert np.linalg.eigvalsh(D).min() > 0
+
+
+# ---------------------------------------------------------------- convection-diffusion (BiCGStab inputs)
+def test_convection_diffusion_reduces_to_poisson_without_wind():
+    from workloads.matrices import convection_diffusion
+    for dims in ((7, 5), (4, 3, 5)):
+        A = convection_diffusion(dims, (0.0,) * len(dims))
+        P = poisson_grid(dims)
+        assert np.array_equal(A.row_ptr, P.row_ptr) and np.array_equal(A.col_idx, P.col_idx)
+        assert np.array_equal(A.vals, P.vals)
+
+
+def test_convection_diffusion_upwinding():
+    """Constant wind (+w along x, -u along y): the upstream neighbour gets
+    -1 - |wind|, the downstream one -1, the diagonal 2d + sum |wind|; rows
+    away from the boundary sum to zero and the matrix is nonsymmetric."""
+    from workloads.matrices import convection_diffusion
+    N, w, u = 6, 0.75, 0.4
+    A = convection_diffusion((N, N), (w, -u))
+    D = A.dense()
+    i = 2 + N * 2                               # interior unknown (x = 2, y = 2)
+    assert D[i, i] == 4.0 + w + u
+    assert D[i, i - 1] == -1.0 - w and D[i, i + 1] == -1.0    # x: wind from -x
+    assert D[i, i + N] == -1.0 - u and D[i, i - N] == -1.0    # y: wind from +y
+    interior = [x + N * y for y in range(1, N - 1) for x in range(1, N - 1)]
+    assert np.allclose(D[interior].sum(axis=1), 0.0)
+    assert np.all(D.sum(axis=1) >= -1e-15)                   # weakly diagonally dominant rows
+    assert np.abs(D - D.T).max() > 0.1
+
+
+def test_workload_cd3_recipe():
+    from workloads import build
+    w = build("cd3", N=10)
+    n = 1000
+    assert w.A.n == n and w.A.nnz == 7 * n - 6 * 100       # 7-point pattern, Dirichlet faces dropped
+    assert w.pc == "jacobi" and w.tol == 1e-8 and w.info["method"] == "bicgstab"
+    w2 = build("cd3", N=10)
+    assert np.array_equal(w.A.vals, w2.A.vals) and np.array_equal(w.b, w2.b)   # seeded
+    D = w.A.dense()
+    assert np.all(np.diag(D) > 0) and np.abs(D - D.T).max() > 0.1
