@@ -59,7 +59,8 @@ typedef enum {
     SLA_ERR_CUDA = 2,           /* a CUDA runtime call failed */
     SLA_ERR_NOMEM = 3,          /* device or pinned allocation failed */
     SLA_ERR_NOT_CONVERGED = 4,  /* max_iter reached; x holds the last iterate */
-    SLA_ERR_BREAKDOWN = 5,      /* p.Ap <= 0, r.z <= 0 or a non-finite value */
+    SLA_ERR_BREAKDOWN = 5,      /* CG: p.Ap <= 0, r.z <= 0; BiCGStab: r^.r or r^.v = 0, omega = 0;
+                                   or a non-finite value */
     SLA_ERR_TIMEOUT = 6,        /* host wall-clock limit; x holds the last iterate */
     SLA_ERR_UNSUPPORTED = 7     /* valid request this build does not serve */
 } sla_status;
@@ -86,7 +87,8 @@ typedef enum {
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
                           the returned x meets the same bound; tol > 0 */
-    int max_iter;      /* cap on products A p per system; >= 0 */
+    int max_iter;      /* cap on iterations per system (CG: products A p; BiCGStab:
+                          iterations of two products); >= 0 */
     sla_pc pc;         /* preconditioner */
     double eps;        /* SPAI shift (ignored otherwise), >= 0 */
     int poll_k;        /* iterations between host checks of the device flag; 0 = default (32) */
@@ -137,7 +139,9 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         5 direct: one thread per row, no shared-memory staging, kernels
  *         built for high occupancy -- the default whenever no row has more
  *         than 16 entries, unless SLA_STAGED, SLA_WARP_PIPELINE or
- *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2;
+ *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2.
+ *         The SPAI factors G and G^T take their forms by the same rule;
+ *         the BiCGStab products always take a staged form (0, 1 or 2);
  *  *ctas: CTAs per system of the product kernels;
  *  *reordered: 1 when the solves iterate on P A P^T.
  * Any pointer may be NULL.  SLA_ERR_INVALID for a null handle.
