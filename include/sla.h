@@ -97,7 +97,8 @@ typedef struct {
 } sla_pcg_opts;
 
 typedef struct {
-    int iters;                 /* products A p performed in the iteration loop */
+    int iters;                 /* iterations performed in the loop (CG: products A p;
+                                  BiCGStab: iterations of two products) */
     double rel_res_recursive;  /* ||r||_2 / ||b||_2 of the recursively updated r */
     double rel_res_true;       /* ||b - A x||_2 / ||b||_2 for the returned x */
     sla_status status;         /* per-system outcome */
