@@ -188,3 +188,17 @@ def test_three_distinct_eigenvalues_terminate_in_three_steps():
     assert info["status"] == "ok" and info["iters"] <= 3
     xs = np.linalg.solve(T, b)
     assert np.linalg.norm(x - xs) / np.linalg.norm(xs) <= 1e-9
+
+
+def test_batched_systems_are_solved_independently():
+    """A batch on one pattern (values [batch][nnz]) gives each system's own
+    solution, as the single-system calls do."""
+    dims = (6, 5)
+    mats = [convection_diffusion(dims, w) for w in ((0.5, 0.2), (-1.0, 0.7), rotating_wind(dims, 2.0))]
+    A = CSR(mats[0].n, mats[0].row_ptr, mats[0].col_idx, np.stack([m.vals for m in mats]))
+    b = np.stack([_rhs(A.n, 20 + s) for s in range(3)])
+    x, infos = oracle.bicgstab(A, b, 1e-12, pc="jacobi")
+    for s, M in enumerate(mats):
+        xs, inf = oracle.bicgstab(M, b[s], 1e-12, pc="jacobi")
+        assert np.array_equal(x[s], xs) and infos[s] == inf
+        assert np.linalg.norm(M.dense() @ x[s] - b[s]) <= 1e-11 * np.linalg.norm(b[s])
