@@ -63,6 +63,8 @@ def _load():
                                            C.c_int, C.c_int, C.c_double, C.c_int, _dp, _dp,
                                            _ip, _dp, _dp]
             lib.oracle_adjoint.restype = C.c_int
+            lib.oracle_grad_A.argtypes = [C.c_int, _ip, _ip, _dp, _dp, C.c_int, _dp]
+            lib.oracle_grad_A.restype = None
             lib.oracle_rel_residual.argtypes = [C.c_int, _ip, _ip, _dp, _dp, _dp]
             lib.oracle_rel_residual.restype = C.c_double
             lib.oracle_bicgstab.argtypes = [C.c_int, _ip, _ip, _dp, _dp, _dp, C.c_double, C.c_int,
@@ -169,35 +171,56 @@ def pcg(A, b, tol, max_iter=100000, pc="none", eps=0.0, f32=None, x0=None):
     return np.stack(xs), infos
 
 
-def _adjoint_one(A, s, x, g, tol, max_iter, pc, eps, f32):
+def _adjoint_one(A, s, x, g, tol, max_iter, pc, eps, f32, with_dA=True):
     lib = _load()
     rp, rpp = _i(A.row_ptr)
     ci, cip = _i(A.col_idx)
     v, vp = _d(_system_vals(A, s))
-    xx, xp = _d(x)
     gg, gp = _d(g)
+    if with_dA:
+        xx, xp = _d(x)
+        dlda = np.zeros(A.nnz, dtype=np.float64)
+        dp = dlda.ctypes.data_as(_dp)
+    else:
+        xp = dlda = dp = None
     dldb = np.zeros(A.n, dtype=np.float64)
-    dlda = np.zeros(A.nnz, dtype=np.float64)
     it = C.c_int(0)
     rr = C.c_double(0)
     rt = C.c_double(0)
     st = lib.oracle_adjoint(A.n, rpp, cip, vp, xp, gp, float(tol), int(max_iter), PC[pc],
                             float(eps), int(f32), dldb.ctypes.data_as(_dp),
-                            dlda.ctypes.data_as(_dp), C.byref(it), C.byref(rr), C.byref(rt))
+                            dp, C.byref(it), C.byref(rr), C.byref(rt))
     return dldb, dlda, dict(iters=it.value, rel_res_recursive=rr.value,
                             rel_res_true=rt.value, status=STATUS[st])
 
 
-def adjoint(A, x, g, tol, max_iter=100000, pc="none", eps=0.0, f32=None):
-    """(dL/db, dL/dA on the pattern, info) for upstream gradient g = dL/dx."""
+def adjoint(A, x, g, tol, max_iter=100000, pc="none", eps=0.0, f32=None, with_dA=True):
+    """(dL/db, dL/dA on the pattern, info) for upstream gradient g = dL/dx.
+    with_dA=False solves for lambda only (x is not read; dL/dA is None)."""
     if f32 is None:
         f32 = A.vals.dtype == np.float32
     if A.vals.ndim == 1:
-        return _adjoint_one(A, 0, x, g, tol, max_iter, pc, eps, f32)
-    out = [_adjoint_one(A, s, x[s], g[s], tol, max_iter, pc, eps, f32)
+        return _adjoint_one(A, 0, x, g, tol, max_iter, pc, eps, f32, with_dA)
+    out = [_adjoint_one(A, s, None if x is None else x[s], g[s], tol, max_iter, pc, eps, f32, with_dA)
            for s in range(A.vals.shape[0])]
-    return (np.stack([o[0] for o in out]), np.stack([o[1] for o in out]),
+    return (np.stack([o[0] for o in out]),
+            np.stack([o[1] for o in out]) if with_dA else None,
             [o[2] for o in out])
+
+
+def grad_A(A, lam, x, f32=None, system: int = 0) -> np.ndarray:
+    """dL/dA_k = -lambda_row(k) x_col(k) on the stored pattern (rounded to
+    fp32 in fp32 mode), for one system."""
+    if f32 is None:
+        f32 = A.vals.dtype == np.float32
+    lib = _load()
+    rp, rpp = _i(A.row_ptr)
+    ci, cip = _i(A.col_idx)
+    ll, lp = _d(lam)
+    xx, xp = _d(x)
+    out = np.empty(max(A.nnz, 1), dtype=np.float64)
+    lib.oracle_grad_A(A.n, rpp, cip, lp, xp, int(f32), out.ctypes.data_as(_dp))
+    return out[:A.nnz]
 
 
 def _bicgstab_one(A, s, b, tol, max_iter, pc, x0):

@@ -288,11 +288,24 @@ static void transpose(int n, const int* rp, const int* ci, const double* a,
 }
 
 /*
+ * Matrix gradient on the stored pattern (torch-sla §3.3, adjoint paragraph):
+ * dL/dA_k = -lambda_row(k) * x_col(k) for every stored entry k, rounded to
+ * fp32 in fp32 mode.
+ */
+void oracle_grad_A(int n, const int* rp, const int* ci, const double* lam,
+                   const double* x, int f32, double* dlda) {
+    for (int i = 0; i < n; ++i)
+        for (int k = rp[i]; k < rp[i + 1]; ++k)
+            dlda[k] = stor(-lam[i] * x[ci[k]], f32);
+}
+
+/*
  * Adjoint of x = A^-1 b for the upstream gradient g = dL/dx:
  * solve A^T lambda = g (same preconditioner kind, tolerance and iteration
  * cap), then dL/db = lambda and dL/dA_k = -lambda_row(k) * x_col(k) for every
  * stored entry k.  In fp32 mode lambda is rounded to fp32 as it is returned
- * and dL/dA is formed from that rounded lambda, then rounded.
+ * and dL/dA is formed from that rounded lambda, then rounded.  dlda = NULL
+ * skips the matrix gradient (x is then not read).
  */
 int oracle_adjoint(int n, const int* rp, const int* ci, const double* a,
                    const double* x, const double* g, double tol, int max_iter,
@@ -305,11 +318,7 @@ int oracle_adjoint(int n, const int* rp, const int* ci, const double* a,
     transpose(n, rp, ci, a, trp, tci, ta);
     int st = oracle_pcg(n, trp, tci, ta, g, dldb, tol, max_iter, pc, eps, f32, 0,
                         iters, rel_rec, rel_true);
-    if (st != OR_INVALID) {
-        for (int i = 0; i < n; ++i)
-            for (int k = rp[i]; k < rp[i + 1]; ++k)
-                dlda[k] = stor(-dldb[i] * x[ci[k]], f32);
-    }
+    if (st != OR_INVALID && dlda) oracle_grad_A(n, rp, ci, dldb, x, f32, dlda);
     free(trp); free(tci); free(ta);
     return st;
 }

@@ -370,3 +370,54 @@ def test_f32_mode_solution_and_residual():
         x64, i64 = oracle.pcg(CSR(w.A.n, w.A.row_ptr, w.A.col_idx, w.A.vals[s].astype(np.float64)),
                               w.b[s].astype(np.float64), w.tol, pc="jacobi", f32=False)
         assert abs(infos[s]["iters"] - i64["iters"]) <= max(2, 0.05 * i64["iters"])
+
+
+def _f32_cases():
+    """fp32-representable systems: the c3 recipe at a small size (two
+    systems) and a random diagonally dominant SPD matrix, with fp32 b and g."""
+    w = build("c3", N=24, batch=2)
+    cases = [(CSR(w.A.n, w.A.row_ptr, w.A.col_idx, w.A.vals[s]), w.b[s], w.g[s], w.tol, "jacobi")
+             for s in range(2)]
+    g = np.random.default_rng(21)
+    R = random_csr(120, 0.05, g, spd=True)
+    R32 = CSR(R.n, R.row_ptr, R.col_idx, R.vals.astype(np.float32))
+    cases.append((R32, g.standard_normal(R.n).astype(np.float32),
+                  g.standard_normal(R.n).astype(np.float32), 1e-5, "none"))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_f32_mode_is_the_fp64_recurrence_rounded_on_return(case):
+    """The reading of "fp32 values": the matrix, b and the returned x (and
+    lambda, dL/dA) are fp32, while the CG recurrence itself runs in fp64.  So
+    on fp32-representable A and b the fp32 mode must take exactly the fp64
+    mode's iterations and return exactly float32 of the fp64 mode's x; the
+    adjoint likewise returns float32 of the fp64 lambda and dL/dA formed from
+    those fp32 vectors, rounded once.  A reading that rounds the working
+    vectors (r, p, q, z) to fp32 changes the iterates and fails this."""
+    A32, b, gv, tol, pc = _f32_cases()[case]
+    A64 = CSR(A32.n, A32.row_ptr, A32.col_idx, A32.vals.astype(np.float64))
+    x32, i32 = oracle.pcg(A32, b, tol, pc=pc, f32=True)
+    x64, i64 = oracle.pcg(A64, b.astype(np.float64), tol, pc=pc, f32=False)
+    assert i32["status"] == i64["status"] == "ok"
+    assert i32["iters"] == i64["iters"]
+    assert np.array_equal(x32, x64.astype(np.float32).astype(np.float64))
+    l32, d32, a32 = oracle.adjoint(A32, x32, gv, tol, pc=pc, f32=True)
+    l64, _, a64 = oracle.adjoint(A64, x64, gv.astype(np.float64), tol, pc=pc, f32=False)
+    assert a32["iters"] == a64["iters"]
+    assert np.array_equal(l32, l64.astype(np.float32).astype(np.float64))
+    rows = A32.rows()
+    # the product of two fp32 values is exact in fp64; one rounding to fp32
+    exact = (-l32[rows] * x32[A32.col_idx]).astype(np.float32).astype(np.float64)
+    assert np.array_equal(d32, exact)
+
+
+def test_grad_A_is_the_stored_pattern_outer_product():
+    """oracle.grad_A: dL/dA_k = -lambda_row(k) x_col(k), by brute force over
+    a dense outer product restricted to the pattern."""
+    g = np.random.default_rng(5)
+    A = random_csr(40, 0.2, g)
+    lam, x = g.standard_normal(A.n), g.standard_normal(A.n)
+    D = -np.outer(lam, x)
+    rows = A.rows()
+    assert np.array_equal(oracle.grad_A(A, lam, x), D[rows, A.col_idx])
