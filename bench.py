@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark: preconditioned CG + adjoint on one B300, one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--also c4] [--impl ours|reference]
 
 A step is one pass of the whole hot path on the workload: the forward PCG
 solve A x = b and the backward pass (adjoint solve A^T lambda = g, dL/db,
@@ -10,10 +10,13 @@ dL/dA on the pattern).  The headline metric is PCG iterations per second
 per-iteration HBM traffic of the algorithmic byte model, the fused SpMV + dot
 kernel's achieved bandwidth, and the solve time.
 
-Default workload (N = 1): 2D 5-point variable-coefficient diffusion,
-1024 x 1024 grid, k = exp(N(0,1)), fp64, Jacobi-PCG to 1e-8, b ~ N(0,1),
-g ~ N(0,1).  Under torchrun every rank solves its own replica (no data-path
-collective); value = iterations of all ranks / max-over-ranks time.
+Default workload (N = 1): the largest single-GPU configuration, the kNN
+graph Laplacian of 4M points (k = 12, union-symmetrised, relabelled), fp64,
+SPAI-PCG (M^-1 = G G^T + 1e-3 I) to 1e-8, b, g ~ N(0,1); the 3D 7-point
+Poisson problem on 128^3 (CG to 1e-8) is measured after it and reported under
+"secondary" (--also).  Other workloads: --config c1..c5, cd3.  Under
+torchrun every rank solves its own replica (no data-path collective); value
+= iterations of all ranks / max-over-ranks time.
 `--impl reference` times the plain CPU oracle on the host cores instead.
 
 `--config cd3` measures BiCGStab instead: a nonsymmetric 3D
@@ -220,61 +223,105 @@ def host_cpu():
     return {"model": model, "available_cores": avail}
 
 
-def cpu_sample(w, budget_s=12.0):
-    """The oracle as it stands, single-threaded, on a bounded number of
-    iterations of the same workload's method (first system of a batch)."""
+def _single_system(w):
     A = w.A
     b = w.b if w.b.ndim == 1 else w.b[0]
     if A.vals.ndim == 2:
         from workloads.matrices import CSR
         A = CSR(A.n, A.row_ptr, A.col_idx, A.vals[0])
-    t0 = time.perf_counter()
-    _, inf = oracle_solve(w, A, b, 3)
-    t_small = time.perf_counter() - t0
-    per_it = max(t_small / 4.0, 1e-6)
-    cap = int(max(3, min(MAX_ITER, budget_s / per_it)))
-    t0 = time.perf_counter()
-    _, inf = oracle_solve(w, A, b, cap)
-    dt = time.perf_counter() - t0
-    its = max(inf["iters"], 1)
+    return A, b
+
+
+def oracle_calibrate(w, budget_s):
+    """Iterations of the oracle's forward solve that take about budget_s
+    seconds on one host core beyond the solve's own set-up (the time per
+    iteration from a 1- and a 3-iteration solve)."""
+    A, b = _single_system(w)
+    t = []
+    for k in (1, 3):
+        t0 = time.perf_counter()
+        oracle_solve(w, A, b, k)
+        t.append(time.perf_counter() - t0)
+    per_it = max((t[1] - t[0]) / 2.0, 1e-6)
+    return int(max(2, min(MAX_ITER, budget_s / per_it)))
+
+
+def oracle_calls(w, cap, calls):
+    """The oracle as it stands, single-threaded: `calls` forward solves of at
+    most `cap` iterations each (first system of a batch).  Returns the
+    iterations and seconds of every call and the host core it ran on."""
+    A, b = _single_system(w)
+    out = []
+    for _ in range(calls):
+        t0 = time.perf_counter()
+        _, inf = oracle_solve(w, A, b, cap)
+        out.append((int(inf["iters"]), time.perf_counter() - t0))
+    try:
+        cpu = os.sched_getcpu()
+    except AttributeError:
+        cpu = None
+    return out, cpu
+
+
+def oracle_summary(w, calls, cpu_id, what):
+    its = sum(c[0] for c in calls)
+    dt = sum(c[1] for c in calls)
     name = "BiCGStab" if method_of(w) == "bicgstab" else "PCG"
     return {"value": its / dt, "unit": "iterations/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {its} {name} iterations of the forward solve (system 0), {dt:.1f} s, "
-                      f"single-threaded fp64 C oracle", "host": host_cpu()}
+            "sample": f"{what}: {len(calls)} call(s) of the oracle's forward {name} solve (system 0), "
+                      f"{calls[0][0]} iterations each, {its} iterations in {dt:.1f} s, "
+                      f"single-threaded fp64 C oracle",
+            "per_call_iterations_per_s": [round(c[0] / c[1], 2) for c in calls],
+            "host_cpu_id": cpu_id, "host": host_cpu()}
+
+
+# Both oracle legs time the same thing: calls of the forward solve capped
+# at ORACLE_CALL_S seconds of iterations each.
+ORACLE_CALL_S = 4.0
+
+
+def cpu_sample(w, calls=3):
+    """cpu_baseline of the main line: the oracle timed on the host cores."""
+    cap = oracle_calibrate(w, ORACLE_CALL_S)
+    res, cpu = oracle_calls(w, cap, calls)
+    return oracle_summary(w, res, cpu, "bounded sample")
+
+
+def config_of(name, w, poll_k, bm):
+    """The `config` object, the same for both arms."""
+    method = method_of(w)
+    return {"workload": f"{name}: {DESCR[name]}", "n": w.A.n, "nnz": w.A.nnz, "batch": w.A.batch,
+            "pc": w.pc, "tol": w.tol, "poll_k": poll_k,
+            "step": ("forward BiCGStab solve + adjoint BiCGStab solve on the explicit A^T + dL/dA pass"
+                     if method == "bicgstab" else "forward PCG solve + adjoint solve + dL/dA pass"),
+            "l2": f"inputs larger than L2: {bm['per_iteration'] / 1e6:.1f} MB touched per iteration "
+                  f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
+
+
+def nnzg_of(w):
+    return (w.A.nnz + w.A.n) // 2 if w.pc == "spai" else None
 
 
 def run_reference(args, w, rank):
     if rank != 0:
         return
-    A = w.A
-    b = w.b if w.b.ndim == 1 else w.b[0]
-    if A.vals.ndim == 2:
-        from workloads.matrices import CSR
-        A = CSR(A.n, A.row_ptr, A.col_idx, A.vals[0])
+    cap = oracle_calibrate(w, ORACLE_CALL_S)
+    if args.warmup > 0:
+        oracle_calls(w, max(2, cap // 4), args.warmup)
     t0 = time.perf_counter()
-    oracle_solve(w, A, b, 3)
-    per_it = max((time.perf_counter() - t0) / 4.0, 1e-6)
-    cap = int(max(2, min(MAX_ITER, 4.0 / per_it)))   # ~4 s of CPU work per step
-    for _ in range(args.warmup):
-        oracle_solve(w, A, b, max(2, cap // 4))
-    its = 0
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        _, inf = oracle_solve(w, A, b, cap)
-        its += inf["iters"]
+    res, cpu = oracle_calls(w, cap, args.steps)
     dt = time.perf_counter() - t0
+    its = sum(c[0] for c in res)
     v = its / dt
-    name = "BiCGStab" if method_of(w) == "bicgstab" else "PCG"
+    bm = byte_model(w, nnzg_of(w))
     line = {"metric": metric_of(w), "value": v, "unit": "iterations/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64" if w.dtype == "f64" else "f32",
-            "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": w.A.n, "nnz": w.A.nnz,
-                       "pc": w.pc, "tol": w.tol},
-            "cpu_baseline": {"value": v, "unit": "iterations/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{cap} {name} iterations per step of the forward solve (system 0)",
-                             "host": host_cpu()},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64" if w.dtype == "f64" else "f32", "data": "synthetic", "impl": "reference",
+            "config": config_of(args.config, w, args.poll_k, bm),
+            "cpu_baseline": oracle_summary(w, res, cpu, "one step = one call"),
             "e2e": {"value": v, "unit": "iterations/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    line["cpu_baseline"]["value"] = v
     print(json.dumps(line), flush=True)
 
 
@@ -292,51 +339,15 @@ def aggregate(ms, iters, world, device):
     return t.item(), int(it.item())
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="c2", choices=sorted(DESCR))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--poll-k", type=int, default=32)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=2)
-    ap.add_argument("--warp-pipeline", action="store_true",
-                    help="use the warp-pipeline product where it applies")
-    ap.add_argument("--producer-consumer", action="store_true",
-                    help="use the producer/consumer product where it applies")
-    ap.add_argument("--staged", action="store_true",
-                    help="keep the warp-staged product forms where the direct form would be the default")
-    ap.add_argument("--persistent", action="store_true",
-                    help="CG / Jacobi-PCG as the persistent iteration kernel (not a graph of kernels)")
-    args = ap.parse_args()
-
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-
-    from workloads import build
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        w = build(args.config)
-        run_reference(args, w, rank)
-        return
-
-    import numpy as np
+def measure(args, name, dev, world, rank, stream, lib, with_cpu, e2e_steps, fma_rate):
+    """Time `args.steps` steps of workload `name` (after `args.warmup`) and
+    return the fields of its JSON line."""
     import torch
     import sparse_iterative_linear_csr_b300 as sla
+    from workloads import build
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    w = build(args.config)
+    w = build(name)
     A = w.A
-    stream = torch.cuda.current_stream()
     rp = torch.from_numpy(A.row_ptr).to(dev)
     ci = torch.from_numpy(A.col_idx).to(dev)
     vals = torch.from_numpy(A.vals).to(dev)
@@ -357,7 +368,7 @@ def main():
         x, inf, ainf = step()
     bad = [i.status for i in inf + ainf if i.status != "ok"]
     if bad:
-        raise SystemExit(f"solve did not converge: {bad}")
+        raise SystemExit(f"{name}: solve did not converge: {bad}")
 
     def barrier():
         if world > 1:
@@ -375,7 +386,6 @@ def main():
     sampler.start()
     e0.record(stream)
     t_wall = time.perf_counter()
-    solve_ms = []
     for _ in range(args.steps):
         x, inf, ainf = step()
         iters += sum(i.iters for i in inf) + sum(i.iters for i in ainf)
@@ -397,28 +407,26 @@ def main():
     torch.cuda.synchronize()
     fwd_ms = f0.elapsed_time(f1)
 
-    # dominant kernel: the CG product kernel (q = A p fused with p.q), timed
-    # live inside the timed region (CUDA events the solve records on its
-    # stream around the first product kernel of every graph launch); with
-    # the persistent iteration kernel there is no separate product launch,
-    # so the fused SpMV + dot API kernel is timed alone on the same operands.
-    nnzg = (A.nnz + A.n) // 2 if w.pc == "spai" else None
-    bm = byte_model(w, nnzg)
-    if prod_n > 0 and method == "bicgstab":
+    # dominant kernel: the product kernel (CG: q = A p fused with p.q;
+    # BiCGStab: v = A p fused with r^.v), timed live inside the timed region
+    # (CUDA events the solve records on its stream around the first product
+    # kernel of every graph launch); with the persistent iteration kernel
+    # there is no separate product launch, so the fused SpMV + dot API kernel
+    # is timed alone on the same operands.
+    bm = byte_model(w, nnzg_of(w))
+    if prod_n > 0:
         kern_ms = prod_ms / prod_n
         kern_bytes = bm["product_per_launch"]
-        kern_desc = (f"k_bicg_v (BiCGStab product v = A p fused with r^.v), live in the timed solves: "
-                     f"{prod_n} launches timed with CUDA events on the solve stream")
-        kern_name = "k_bicg_v"
-    elif prod_n > 0:
-        kern_ms = prod_ms / prod_n
-        kern_bytes = bm["product_per_launch"]
-        kern_desc = (f"k_spmv_iter (CG product q = A p fused with p.q), live in the timed solves: "
-                     f"{prod_n} launches timed with CUDA events on the solve stream")
-        kern_name = "k_spmv_iter"
+        if method == "bicgstab":
+            kern_desc = (f"k_bicg_v (BiCGStab product v = A p fused with r^.v), live in the timed solves: "
+                         f"{prod_n} launches timed with CUDA events on the solve stream")
+            kern_name = "k_bicg_v"
+        else:
+            kern_desc = (f"k_spmv_iter (CG product q = A p fused with p.q), live in the timed solves: "
+                         f"{prod_n} launches timed with CUDA events on the solve stream")
+            kern_name = "k_spmv_iter"
     else:
         import ctypes as C
-        lib = sla._lib.load()
         xin = x.contiguous()
         yout = torch.empty_like(xin)
         dout = torch.empty(A.batch, dtype=torch.float64, device=dev)
@@ -441,74 +449,169 @@ def main():
     peak, peak_kind = peaks()
     achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
     src = kernel_source_hash()
-    traffic = recorded_traffic(args.config, kern_name, src)
+    traffic = recorded_traffic(name, kern_name, src)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+            "kernel": kern_desc, "algorithmic_bytes_per_launch": kern_bytes, "ms_per_launch": kern_ms,
+            "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
+    # The fp64 roof: one fp64 FMA per stored entry plus one per row for the
+    # fused dot (fp64 systems; fp32 systems run double-float arithmetic on
+    # the fp32 pipe), against the fp64 FMA rate measured on this GPU.
+    hbm_us = kern_bytes / (peak * 1e9) * 1e6
+    if w.dtype == "f64" and fma_rate:
+        fma = (A.nnz + A.n) * A.batch
+        fp64_us = fma / fma_rate * 1e6
+        roof["fp64"] = {"fma_per_launch": fma, "fma_rate_per_s": fma_rate,
+                        "rate_method": "sla_fp64_fma_rate: independent fp64 FMA chains on every SM, CUDA events, "
+                                       "best of 3 launches",
+                        "time_us_at_rate": fp64_us, "achieved_fma_per_s": fma / (kern_ms * 1e-3),
+                        "frac": fma / (kern_ms * 1e-3) / fma_rate}
+        bind = "fp64" if fp64_us > hbm_us else "hbm"
+        roof["binding_roof"] = {"bound": bind, "time_us": max(hbm_us, fp64_us),
+                                "frac": max(hbm_us, fp64_us) / (kern_ms * 1e3)}
+    else:
+        roof["binding_roof"] = {"bound": "hbm", "time_us": hbm_us, "frac": hbm_us / (kern_ms * 1e3)}
 
     # bytes of one system's iteration (a batched iteration moves B of them)
     per_it_gbs = bm["per_iteration"] / A.batch * iters / (ms * 1e-3) / 1e9
+    out = {
+        "value": value, "ms_per_step": ms / args.steps, "dtype": w.dtype,
+        "config": config_of(name, w, args.poll_k, bm),
+        "iterations_per_step": iters // max(args.steps, 1),
+        "forward_iterations": finf[0].iters, "solve_ms": fwd_ms,
+        "hbm_gbs_per_iteration": per_it_gbs,
+        "hbm_frac_per_iteration": {"of_measured": per_it_gbs / peak, "of_nominal_8tbs": per_it_gbs / NOMINAL_HBM_GBS},
+        "bytes_per_iteration_model": bm["per_iteration"],
+        "roofline": roof, "gpu_launches": int(launches), "clocks": clocks,
+        "wall_s_timed": t_wall, "kernel_src": src, "product_form": M.layout()[0],
+        "product_ctas_per_system": M.layout()[1], "metric": metric_of(w),
+    }
+    if w.dtype == "f32":
+        # the working vectors are 8-byte double-float slots; the same
+        # iteration counted with 4-byte working vectors (fp32 storage)
+        n, nnz, B = A.n, A.nnz, A.batch
+        it4 = 4 * nnz * B + 4 * nnz + 4 * (n + 1) + 13 * 4 * n * B
+        out["hbm_frac_per_iteration"]["of_measured_4byte_vectors"] = (
+            it4 / A.batch * iters / (ms * 1e-3) / 1e9) / peak
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs (values, b, g) from pinned memory, solve + adjoint, D2H of x,
-    # dL/db and dL/dA into pinned memory, all inside the timed region.
-    h_vals = vals.cpu().pin_memory()
-    h_b = b.cpu().pin_memory()
-    h_g = g.cpu().pin_memory()
-    d_vals2 = torch.empty_like(vals)
-    o_x = torch.empty_like(h_b).pin_memory()
-    o_lb = torch.empty_like(h_b).pin_memory()
-    o_la = torch.empty_like(h_vals).pin_memory()
-    h2d = h_vals.numel() * h_vals.element_size() + 2 * h_b.numel() * h_b.element_size()
-    d2h = 2 * h_b.numel() * h_b.element_size() + h_vals.numel() * h_vals.element_size()
-    barrier()
-    t0 = time.perf_counter()
-    e2e_iters = 0
-    for _ in range(args.e2e_steps):
-        d_vals2.copy_(h_vals, non_blocking=True)
-        db = h_b.to(dev, non_blocking=True)
-        dg = h_g.to(dev, non_blocking=True)
-        M.update_values(d_vals2)
-        xx, i1 = M.solve(db, **kw)
-        lb, la, i2 = M.adjoint(xx, dg, **kw)
-        o_x.copy_(xx, non_blocking=True)
-        o_lb.copy_(lb, non_blocking=True)
-        o_la.copy_(la, non_blocking=True)
-        torch.cuda.synchronize()
-        e2e_iters += sum(i.iters for i in i1) + sum(i.iters for i in i2)
-    e2e_ms, e2e_iters_all = aggregate((time.perf_counter() - t0) * 1000.0, e2e_iters, world, dev)
-    e2e_value = e2e_iters_all / (e2e_ms / 1000.0)
-    M.update_values(vals)
+    if e2e_steps > 0:
+        # end to end through the public API with host buffers: H2D of the
+        # step's inputs (values, b, g) from pinned memory, solve + adjoint,
+        # D2H of x, dL/db and dL/dA into pinned memory, all inside the timed
+        # region.
+        h_vals = vals.cpu().pin_memory()
+        h_b = b.cpu().pin_memory()
+        h_g = g.cpu().pin_memory()
+        d_vals2 = torch.empty_like(vals)
+        o_x = torch.empty_like(h_b).pin_memory()
+        o_lb = torch.empty_like(h_b).pin_memory()
+        o_la = torch.empty_like(h_vals).pin_memory()
+        h2d = h_vals.numel() * h_vals.element_size() + 2 * h_b.numel() * h_b.element_size()
+        d2h = 2 * h_b.numel() * h_b.element_size() + h_vals.numel() * h_vals.element_size()
+        barrier()
+        t0 = time.perf_counter()
+        e2e_iters = 0
+        for _ in range(e2e_steps):
+            d_vals2.copy_(h_vals, non_blocking=True)
+            db = h_b.to(dev, non_blocking=True)
+            dg = h_g.to(dev, non_blocking=True)
+            M.update_values(d_vals2)
+            xx, i1 = M.solve(db, **kw)
+            lb, la, i2 = M.adjoint(xx, dg, **kw)
+            o_x.copy_(xx, non_blocking=True)
+            o_lb.copy_(lb, non_blocking=True)
+            o_la.copy_(la, non_blocking=True)
+            torch.cuda.synchronize()
+            e2e_iters += sum(i.iters for i in i1) + sum(i.iters for i in i2)
+        e2e_ms, e2e_iters_all = aggregate((time.perf_counter() - t0) * 1000.0, e2e_iters, world, dev)
+        out["e2e"] = {"value": e2e_iters_all / (e2e_ms / 1000.0), "unit": "iterations/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        M.update_values(vals)
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_sample(w)
+    out["cpu_baseline"] = cpu_sample(w) if (rank == 0 and with_cpu) else None
+    M.close()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c5", choices=sorted(DESCR))
+    ap.add_argument("--also", default=None,
+                    help="comma-separated workloads measured after the main one and reported under "
+                         "'secondary' (default: c4 when the main workload is c5; 'none' for none)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--poll-k", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--warp-pipeline", action="store_true",
+                    help="use the warp-pipeline product where it applies")
+    ap.add_argument("--producer-consumer", action="store_true",
+                    help="use the producer/consumer product where it applies")
+    ap.add_argument("--staged", action="store_true",
+                    help="keep the warp-staged product forms where the direct form would be the default")
+    ap.add_argument("--persistent", action="store_true",
+                    help="CG / Jacobi-PCG as the persistent iteration kernel (not a graph of kernels)")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from workloads import build
+        run_reference(args, build(args.config), rank)
+        return
+
+    import ctypes as C
+    import torch
+    import sparse_iterative_linear_csr_b300 as sla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    lib = sla._lib.load()
+    rate = C.c_double(0.0)
+    st = lib.sla_fp64_fma_rate(C.byref(rate), C.c_void_p(stream.cuda_stream))
+    fma_rate = rate.value if st == 0 else None
+
+    main_line = measure(args, args.config, dev, world, rank, stream, lib, not args.no_cpu_baseline,
+                        args.e2e_steps, fma_rate)
+    also = args.also if args.also is not None else ("c4" if args.config == "c5" else "none")
+    secondary = {}
+    for name in [a for a in also.split(",") if a and a != "none"]:
+        sec = measure(args, name, dev, world, rank, stream, lib, False, 0, fma_rate)
+        secondary[name] = {k: sec[k] for k in ("value", "ms_per_step", "config", "iterations_per_step",
+                                               "forward_iterations", "solve_ms", "hbm_gbs_per_iteration",
+                                               "hbm_frac_per_iteration", "roofline", "clocks",
+                                               "product_form", "gpu_launches")}
+        secondary[name]["unit"] = "iterations/s"
 
     if rank == 0:
+        m = main_line
         line = {
-            "metric": metric_of(w),
-            "value": value, "unit": "iterations/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": f"{args.config}: {DESCR[args.config]}", "n": A.n, "nnz": A.nnz,
-                       "batch": A.batch, "pc": w.pc, "tol": w.tol, "poll_k": args.poll_k,
-                       "step": ("forward BiCGStab solve + adjoint BiCGStab solve on the explicit A^T + dL/dA pass"
-                                if method == "bicgstab" else "forward PCG solve + adjoint solve + dL/dA pass"),
-                       "l2": f"inputs larger than L2: {bm['per_iteration'] / 1e6:.1f} MB touched per iteration "
-                             f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"},
-            "iterations_per_step": iters // max(args.steps, 1),
-            "forward_iterations": finf[0].iters, "solve_ms": fwd_ms,
-            "hbm_gbs_per_iteration": per_it_gbs,
-            "hbm_frac_per_iteration": {"of_measured": per_it_gbs / peak, "of_nominal_8tbs": per_it_gbs / NOMINAL_HBM_GBS},
-            "bytes_per_iteration_model": bm["per_iteration"],
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                         "kernel": kern_desc,
-                         "algorithmic_bytes_per_launch": kern_bytes, "ms_per_launch": kern_ms,
-                         "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
-            "e2e": {"value": e2e_value, "unit": "iterations/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
-            "wall_s_timed": t_wall, "kernel_src": src, "product_form": M.layout()[0],
-            "product_ctas_per_system": M.layout()[1],
+            "metric": m["metric"], "value": m["value"], "unit": "iterations/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": m["dtype"],
+            "data": "synthetic", "config": m["config"],
+            "iterations_per_step": m["iterations_per_step"], "forward_iterations": m["forward_iterations"],
+            "solve_ms": m["solve_ms"], "hbm_gbs_per_iteration": m["hbm_gbs_per_iteration"],
+            "hbm_frac_per_iteration": m["hbm_frac_per_iteration"],
+            "bytes_per_iteration_model": m["bytes_per_iteration_model"], "roofline": m["roofline"],
+            "e2e": m.get("e2e"), "gpu_launches": m["gpu_launches"], "clocks": m["clocks"],
+            "cpu_baseline": m["cpu_baseline"], "wall_s_timed": m["wall_s_timed"], "kernel_src": m["kernel_src"],
+            "product_form": m["product_form"], "product_ctas_per_system": m["product_ctas_per_system"],
+            "fp64_fma_rate_per_s": fma_rate,
         }
+        if secondary:
+            line["secondary"] = secondary
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

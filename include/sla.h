@@ -105,12 +105,18 @@ typedef struct {
 } sla_solve_info;
 
 /* Fill *o with defaults: tol 1e-8, max_iter 10000, SLA_PC_NONE, eps 1e-3,
- * poll_k 32, use_x0 0, timeout_s 0. */
+ * poll_k 32, use_x0 0, timeout_s 0.  The keyword defaults of torch-sla §3
+ * (.solve with per-call overrides); eps = 1e-3 is the learned-SPAI shift
+ * (Reviewer GmV6 Concern 3). */
 void sla_pcg_opts_default(sla_pcg_opts* o);
 
 /*
  * Create a handle for an n x n CSR matrix (or a batch of `batch` matrices on
- * one pattern).  Analyses the pattern on the device: the product layout
+ * one pattern).  Defined by torch-sla §3, sparse tensor types: one sparse
+ * matrix, or a batch of matrices that share one sparsity pattern so that the
+ * set-up done once (here the analysis below; there the symbolic
+ * factorisation or communication buffers) is reused across the batch and
+ * across solves.  Analyses the pattern on the device: the product layout
  * (sla_csr_layout), the diagonal, and on first SPAI use the factor G and its
  * explicit transpose.
  * n >= 1, 0 <= nnz < 2^31, batch >= 1.  The handle keeps the three pointers
@@ -126,7 +132,8 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
 
 /*
  * Product layout of the matrix the solves iterate on -- A, or P A P^T when
- * the handle reorders (see sla_pcg_solve) -- for diagnostics:
+ * the handle reorders (see sla_pcg_solve) -- for diagnostics.  The pages have
+ * no counterpart (it reports this implementation's choices):
  *  *form: 0 register-staged warp groups, 1 warp groups with asynchronous
  *         value/column staging, 2 the same with asynchronous gathers,
  *         3 the warp pipeline (each warp bulk-copies its 32-row groups into
@@ -150,6 +157,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
 sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered);
 
 /*
+ * Measurement hook; the pages have no counterpart.
  * Live duration of the first product kernel of an iteration (CG: q = A p
  * fused with p.q; BiCGStab: v = A p fused with r^.v; either with the
  * pending true-residual check), for handles created with SLA_TIME_PRODUCT:
@@ -167,18 +175,23 @@ sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered);
 sla_status sla_product_time(sla_handle h, double* total_ms, long long* samples, int reset);
 
 /* Replace the values (same pattern, same dtype, [batch][nnz]); recomputes the
- * value-dependent set-up (diagonal, G, G^T).  Synchronises `stream`. */
+ * value-dependent set-up (diagonal, G, G^T).  torch-sla §3, sparse tensor
+ * types: the pattern-dependent set-up is kept and reused when only the
+ * values change (the shared-pattern case).  Synchronises `stream`.  The
+ * handle keeps d_vals as it kept the values passed to sla_csr_create. */
 sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream);
 
 /* y = A x for every system (torch-sla §3, .matvec).  d_x, d_y: [batch][n]. */
 sla_status sla_spmv(sla_handle h, const void* d_x, void* d_y, void* stream);
 
 /* y = A x and d_dot[s] = x_s . y_s (fp64, one per system) in one fused pass:
- * the q = A p, delta = p.q step of CG. */
+ * the q = A p, delta = <p,Ap> step of CG (torch-sla §3.3, distributed CG).
+ * d_dot: device double[batch].  Does not synchronise. */
 sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot, void* stream);
 
 /*
- * Block product: Y[:, j] = A X[:, j] for the k columns of a block stored
+ * Block product (the A-times-a-block step of torch-sla §3's .eigsh, here
+ * LOBPCG): Y[:, j] = A X[:, j] for the k columns of a block stored
  * column after column (d_X, d_Y: [k][n], column j at offset j*n), in the
  * handle's dtype.  Needs a single-system handle (batch = 1); 0 <= k <= 65535.
  * Same product kernels as sla_spmv, with every column reading the same
@@ -187,7 +200,13 @@ sla_status sla_spmv_dot(sla_handle h, const void* d_x, void* d_y, double* d_dot,
 sla_status sla_spmm(sla_handle h, const void* d_X, void* d_Y, int k, void* stream);
 
 /*
- * Solve A x = b by preconditioned CG, every system of a batch independently
+ * Solve A x = b by preconditioned CG (torch-sla §3.3, distributed CG: the CG
+ * recurrence with the inner products <r,r> and <p,Ap>; torch-sla §4 Table 3:
+ * CG with Jacobi preconditioning, opts->pc = SLA_PC_JACOBI; the learned-SPAI
+ * author responses, Reviewer umir Concern 1 and Reviewer GmV6 Concern 3:
+ * M^-1 = G G^T + eps I applied by two SpMVs, opts->pc = SLA_PC_SPAI; torch-sla
+ * §4 Figure 2: the stopping tolerance on the residual), every system of a
+ * batch independently
  * (converged systems are frozen while the others continue).  d_b, d_x:
  * [batch][n].  x0 = 0 unless opts->use_x0.  info: host array of `batch`
  * entries, filled on return.  Returns SLA_OK when every system converged,
@@ -285,14 +304,30 @@ sla_status sla_spmv_dot_static(int n, long long nnz, int batch, sla_dtype dt, co
                                const int* d_col_idx, const void* d_vals, const void* d_x, void* d_y,
                                double* d_dot, void* stream);
 
-/* Free the handle and everything it owns (not the caller's arrays). */
+/*
+ * Measurement hook; the pages have no counterpart.  Measures the device's
+ * fp64 fused multiply-add rate (thread FMAs per second): a kernel of
+ * independent fp64 FMA chains on every SM at full occupancy, timed with CUDA
+ * events on `stream` (best of three launches after one warm-up).  This is
+ * the fp64 roof beside the HBM roof: an fp64 SpMV spends one FMA per stored
+ * entry.  Allocates a small output buffer; synchronises `stream`.
+ */
+sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream);
+
+/* Free the handle and everything it owns (not the caller's arrays).  The
+ * pages have no counterpart (a resource-release call of this C interface).
+ * A NULL handle returns SLA_ERR_INVALID.  Must not run while a call on the
+ * handle is in flight on another thread. */
 sla_status sla_csr_destroy(sla_handle h);
 
-/* Message for the calling thread's last error ("" if none). */
+/* Message for the calling thread's last error ("" if none).  The pages have
+ * no counterpart (error reporting of this C interface).  The string belongs
+ * to the library and stays valid until the thread's next failing call. */
 const char* sla_last_error(void);
 
 /* Number of kernels this library has launched in the process (graph nodes
- * count once per graph launch).  Diagnostics for benchmarks. */
+ * count once per graph launch).  Diagnostics for benchmarks; the pages have
+ * no counterpart. */
 unsigned long long sla_launch_count(void);
 
 #ifdef __cplusplus

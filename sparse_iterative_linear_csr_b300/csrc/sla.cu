@@ -294,10 +294,19 @@ static sla_status allow_smem_fused() {
     return SLA_OK;
 }
 
+// cudaFuncSetAttribute acts on the current device's context, so the
+// attributes are set once per device ordinal (and per dtype).
+static constexpr int SMEM_MAX_DEVICES = 64;
+static std::mutex g_smem_mu;
+
 template <typename T>
 static sla_status allow_smem() {
-    static std::atomic<int> done{0};
-    if (done.load()) return SLA_OK;
+    static bool done[SMEM_MAX_DEVICES] = {};
+    int dev = 0;
+    CU(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= SMEM_MAX_DEVICES) return fail(SLA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    if (done[dev]) return SLA_OK;
     const int b = (int)spmv_smem(MAX_CAP);
     TRY((allow_smem_form<T, 0>(b)));
     TRY((allow_smem_form<T, 1>(b)));
@@ -317,7 +326,7 @@ static sla_status allow_smem() {
         TRY((allow_smem_bicg<1>(b)));
         TRY((allow_smem_bicg<2>(b)));
     }
-    done.store(1);
+    done[dev] = true;
     return SLA_OK;
 }
 
@@ -1767,6 +1776,61 @@ sla_status sla_bicgstab_adjoint(sla_handle h, const void* d_x, const void* d_g, 
     if (!solved_or_stopped(st)) return st;
     TRY(grad_A(h, d_x, d_dLdb, d_dLdA, s));
     return st;
+}
+
+// Thread-FMA rate of the fp64 pipe: every thread runs PROBE_CHAINS
+// independent chains of dependent fp64 FMAs (enough in flight to keep the
+// pipe issuing), on a grid of every SM at full occupancy.  The result is
+// stored so the chains are not optimised away.
+static constexpr int PROBE_CHAINS = 8;
+__global__ void __launch_bounds__(NT) k_fp64_probe(double* out, int iters, double m, double c) {
+    double a[PROBE_CHAINS];
+#pragma unroll
+    for (int j = 0; j < PROBE_CHAINS; ++j) a[j] = 1e-3 * (threadIdx.x + j);
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int j = 0; j < PROBE_CHAINS; ++j) a[j] = fma(a[j], m, c);
+    }
+    double t = 0.0;
+#pragma unroll
+    for (int j = 0; j < PROBE_CHAINS; ++j) t += a[j];
+    out[blockIdx.x * NT + threadIdx.x] = t;
+}
+
+sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream) {
+    if (!fma_per_s) return fail(SLA_ERR_INVALID, "null output");
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0, sms = 0, per = 0;
+    CU(cudaGetDevice(&dev));
+    CU(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    CU(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_fp64_probe, NT, 0));
+    if (per < 1) per = 1;
+    const int grid = per * sms;
+    DevBuf out;
+    TRY(out.alloc(sizeof(double) * (size_t)grid * NT));
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    CU(cudaEventCreate(&e0));
+    CU(cudaEventCreate(&e1));
+    const int iters = 4096;
+    float best = 0.0f;
+    sla_status st = SLA_OK;
+    for (int rep = 0; rep < 4 && st == SLA_OK; ++rep) {   // the first launch warms up
+        cudaEventRecord(e0, s);
+        k_fp64_probe<<<grid, NT, 0, s>>>(out.as<double>(), iters, 0.999999, 1e-7);
+        st = launched();
+        cudaEventRecord(e1, s);
+        if (st == SLA_OK && cudaEventSynchronize(e1) == cudaSuccess) {
+            float ms = 0.0f;
+            cudaEventElapsedTime(&ms, e0, e1);
+            if (rep > 0 && (best == 0.0f || ms < best)) best = ms;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    TRY(st);
+    if (!(best > 0.0f)) return fail(SLA_ERR_CUDA, "fp64 probe could not be timed");
+    *fma_per_s = (double)grid * NT * iters * PROBE_CHAINS / (best * 1e-3);
+    return SLA_OK;
 }
 
 }  // extern "C"

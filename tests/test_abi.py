@@ -68,3 +68,38 @@ def test_no_oracle_in_product_package():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "oracle.c" not in src, f
+
+
+@pytest.mark.parametrize("case", ["n0", "nnz_neg", "null_x", "null_dot", "null_rowptr", "batch_big",
+                                  "dtype"])
+def test_static_entry_rejects_bad_arguments_without_launching(lib, case):
+    """sla_spmv_dot_static checks its arguments before any CUDA call: each
+    bad argument returns SLA_ERR_INVALID and launches nothing."""
+    from sparse_iterative_linear_csr_b300 import _lib
+    p = C.c_void_p(16)   # never dereferenced: the checks fail first
+    args = dict(n=4, nnz=4, batch=1, dt=0, rp=p, ci=p, v=p, x=p, y=p, dot=p)
+    if case == "n0":
+        args["n"] = 0
+    elif case == "nnz_neg":
+        args["nnz"] = -1
+    elif case == "null_x":
+        args["x"] = None
+    elif case == "null_dot":
+        args["dot"] = None
+    elif case == "null_rowptr":
+        args["rp"] = None
+    elif case == "batch_big":
+        args["batch"] = 65
+    else:
+        args["dt"] = 7
+    before = lib.sla_launch_count()
+    st = lib.sla_spmv_dot_static(args["n"], args["nnz"], args["batch"], args["dt"], args["rp"], args["ci"],
+                                 args["v"], args["x"], args["y"], args["dot"], None)
+    assert st == _lib.SLA_ERR_INVALID
+    assert lib.sla_last_error()
+    assert lib.sla_launch_count() == before
+
+
+def test_fp64_probe_rejects_null_output(lib):
+    from sparse_iterative_linear_csr_b300 import _lib
+    assert lib.sla_fp64_fma_rate(None, None) == _lib.SLA_ERR_INVALID

@@ -81,3 +81,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["cpu_baseline"]["host"]["available_cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    # the same config keys as the main arm's line (bench.config_of)
+    for key in ("workload", "n", "nnz", "batch", "pc", "tol", "poll_k", "step", "l2"):
+        assert key in d["config"], key
+    assert d["config"]["workload"].startswith("c1:")

@@ -2,8 +2,13 @@
 BiCGStab workload cd3), in the launch configuration the benchmark times (same
 options, poll interval 32, forward solve then adjoint).
 
-The oracle cannot solve the large systems in seconds, so the checks are the
-ones that hold at any size plus outputs the oracle computes one by one:
+The large CG workloads c2, c4 and c5 are compared with the oracle's own
+full-size solves (computed once by tests/fullsize_oracle.py and cached, or in
+spawned processes started at the beginning of the session): x and lambda
+within 1e-6 relative, dL/dA against the oracle's -lambda_i x_j on the pattern
+within 1e-6 relative, forward and adjoint iteration counts within 2%.
+Besides, the checks that hold at any size and outputs the oracle computes
+one by one:
   * SpMV: 2000 sampled rows against the oracle's row sums of those rows;
   * solve: status, and the true residual ||b - A x|| / ||b|| <= tol
     recomputed on the host in fp64 from the returned x (scipy, not the GPU);
@@ -24,6 +29,7 @@ import oracle
 from workloads import build
 from workloads.matrices import CSR
 
+import fullsize_oracle
 from gpu_util import make, rel
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -142,3 +148,46 @@ def test_fullsize_c3_two_systems_match_oracle(cuda_device):
         xo, io = oracle.pcg(A1, w.b[s], w.tol, pc="jacobi", f32=True)
         assert abs(info[s].iters - io["iters"]) <= max(1, int(0.02 * io["iters"]))
         assert rel(xh[s], xo) <= 1e-6
+
+
+def _oracle_results(name, w):
+    """The oracle's full-size (x, info, lambda, info) for workload `name`:
+    from the cache, else from the solves the session started (conftest), else
+    computed here in spawned processes."""
+    key = fullsize_oracle.key_of(w)
+    got = fullsize_oracle.load(name, key)
+    if got is None:
+        pending = getattr(fullsize_oracle, "PENDING", None)
+        if pending is None:
+            pool, pending = fullsize_oracle.start((name,))
+        for r in pending:
+            r.get(timeout=3600)
+        got = fullsize_oracle.load(name, key)
+    assert got is not None, f"oracle results for {name} missing"
+    return got
+
+
+@pytest.mark.parametrize("name", ["c2", "c4", "c5"])
+def test_fullsize_matches_oracle(cuda_device, name):
+    """x, iterations, lambda and dL/dA against the oracle at full size, in
+    the benchmark's launch configuration."""
+    w = _workload(name)
+    A = w.A
+    M = make(A)
+    kw = dict(tol=w.tol, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3, **BENCH_KW)
+    x, info = M.solve(torch.from_numpy(w.b).to(cuda_device), **kw)
+    lam, dA, ainfo = M.adjoint(x, torch.from_numpy(w.g).to(cuda_device), **kw)
+    xo, fo, lo, ao = _oracle_results(name, w)
+    assert fo["status"] == "ok" and ao["status"] == "ok"
+    assert info[0].status == "ok" and ainfo[0].status == "ok"
+    assert abs(info[0].iters - fo["iters"]) <= max(1, int(0.02 * fo["iters"])), (info[0].iters, fo["iters"])
+    assert abs(ainfo[0].iters - ao["iters"]) <= max(1, int(0.02 * ao["iters"])), (ainfo[0].iters, ao["iters"])
+    xh = x.cpu().numpy()
+    lh = lam.cpu().numpy()
+    ex, el = rel(xh, xo), rel(lh, lo)
+    assert ex <= 1e-6, ex
+    assert el <= 1e-6, el
+    del lam, x
+    dAo = oracle.grad_A(A, lo, xo)
+    ed = rel(dA.cpu().numpy(), dAo)
+    assert ed <= 1e-6, ed
