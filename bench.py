@@ -50,6 +50,9 @@ DESCR = {
            "(scaled speed <= 2) + 0.5 along z, fp64, nonsymmetric, Jacobi-BiCGStab to 1e-8, b,g ~ N(0,1)",
 }
 MAX_ITER = 200000
+# full sizes (grid side / point count) of the workloads
+FULL_SIZE = {"c1": (64, 64), "c2": (1024, 1024), "c3": (256, 256), "c4": (128, 128, 128),
+             "cd3": (128, 128, 128), "c5_points": 4 * 1024 * 1024}
 METRIC = "PCG iterations/s (forward + adjoint); HBM GB/s per iteration (fraction of B300 peak); solve ms"
 METRIC_BICG = ("BiCGStab iterations/s (forward + transpose adjoint); HBM GB/s per iteration "
                "(fraction of B300 peak); solve ms")
@@ -290,12 +293,26 @@ def cpu_sample(w, calls=3):
 def config_of(name, w, poll_k, bm):
     """The `config` object, the same for both arms."""
     method = method_of(w)
-    return {"workload": f"{name}: {DESCR[name]}", "n": w.A.n, "nnz": w.A.nnz, "batch": w.A.batch,
+    scaled = w.info.get("grid") != FULL_SIZE.get(name, w.info.get("grid")) or \
+        w.info.get("points") != FULL_SIZE.get(name + "_points", w.info.get("points"))
+    tag = " (SCALED DOWN: a profiler-capture size, not the workload)" if scaled else ""
+    return {"workload": f"{name}: {DESCR[name]}{tag}", "n": w.A.n, "nnz": w.A.nnz, "batch": w.A.batch,
             "pc": w.pc, "tol": w.tol, "poll_k": poll_k,
             "step": ("forward BiCGStab solve + adjoint BiCGStab solve on the explicit A^T + dL/dA pass"
                      if method == "bicgstab" else "forward PCG solve + adjoint solve + dL/dA pass"),
             "l2": f"inputs larger than L2: {bm['per_iteration'] / 1e6:.1f} MB touched per iteration "
                   f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
+
+
+def size_override(args, name):
+    """Smaller versions of a workload (same recipe) for profiler captures
+    that must hold only a few GB on the device: --grid N (grid side of
+    c1-c4, cd3), --points P (c5)."""
+    if name == "c5" and args.points:
+        return {"npoints": args.points}
+    if name != "c5" and args.grid:
+        return {"N": args.grid}
+    return {}
 
 
 def nnzg_of(w):
@@ -346,7 +363,7 @@ def measure(args, name, dev, world, rank, stream, lib, with_cpu, e2e_steps, fma_
     import sparse_iterative_linear_csr_b300 as sla
     from workloads import build
 
-    w = build(name)
+    w = build(name, **size_override(args, name))
     A = w.A
     rp = torch.from_numpy(A.row_ptr).to(dev)
     ci = torch.from_numpy(A.col_idx).to(dev)
@@ -354,7 +371,7 @@ def measure(args, name, dev, world, rank, stream, lib, with_cpu, e2e_steps, fma_
     b = torch.from_numpy(w.b).to(dev)
     g = torch.from_numpy(w.g).to(dev)
     M = sla.CSRMatrix(rp, ci, vals, pipeline=args.warp_pipeline, fused=args.persistent, time_product=True,
-                      producer_consumer=args.producer_consumer, staged=args.staged)
+                      producer_consumer=args.producer_consumer, staged=args.staged, sliced=args.sliced)
     method = method_of(w)
     kw = dict(tol=w.tol, max_iter=MAX_ITER, pc=w.pc, eps=w.eps if w.pc == "spai" else 1e-3,
               poll_k=args.poll_k, method=method)
@@ -552,6 +569,12 @@ def main():
                     help="use the producer/consumer product where it applies")
     ap.add_argument("--staged", action="store_true",
                     help="keep the warp-staged product forms where the direct form would be the default")
+    ap.add_argument("--grid", type=int, default=0,
+                    help="grid side of a smaller c1-c4/cd3 (profiler captures; the line is then not the workload's)")
+    ap.add_argument("--points", type=int, default=0,
+                    help="point count of a smaller c5 (profiler captures; the line is then not the workload's)")
+    ap.add_argument("--sliced", action="store_true",
+                    help="use the sliced product form where it applies")
     ap.add_argument("--persistent", action="store_true",
                     help="CG / Jacobi-PCG as the persistent iteration kernel (not a graph of kernels)")
     args = ap.parse_args()

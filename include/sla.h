@@ -83,6 +83,8 @@ typedef enum {
 #define SLA_REORDER 32u      /* always iterate on the reordered matrix (see sla_pcg_solve) */
 #define SLA_NO_REORDER 64u   /* never reorder */
 #define SLA_STAGED 128u      /* never use the direct product form (see sla_csr_layout) */
+#define SLA_SLICED 256u      /* use the sliced product form wherever it pads little, also for the
+                                SPAI factors (see sla_csr_layout) */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -147,7 +149,18 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         5 direct: one thread per row, no shared-memory staging, kernels
  *         built for high occupancy -- the default whenever no row has more
  *         than 16 entries, unless SLA_STAGED, SLA_WARP_PIPELINE or
- *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2.
+ *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2;
+ *         6 sliced (not with SLA_STAGED, SLA_WARP_PIPELINE or
+ *         SLA_PRODUCER_CONSUMER): a handle-owned copy of the iteration
+ *         matrix in slices of 32 rows stored column by column (rows
+ *         reordered by length within windows of 256, 1024 or 4096 rows when
+ *         that pads less), used when padding adds at most 15% entries; one
+ *         thread per row, coalesced value and column loads.  The default
+ *         for the iteration matrix when some row has more than 16 entries
+ *         and rows hold at least 12 on average; with SLA_SLICED wherever it
+ *         applies, the SPAI factors included.  Costs (8 + value size) bytes
+ *         per sliced entry of device memory, and the values are copied again
+ *         by sla_csr_update_values.
  *         The SPAI factors G and G^T take their forms by the same rule;
  *         the BiCGStab products always take a staged form (0, 1 or 2);
  *  *ctas: CTAs per system of the product kernels;

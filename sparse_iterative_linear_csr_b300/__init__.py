@@ -88,12 +88,15 @@ class CSRMatrix:
     product where it applies; reorder=True / False forces / forbids
     iterating on a reverse Cuthill-McKee reordering (default: reorder
     scattered patterns); staged=True keeps the warp-staged product forms
-    where the direct (thread-per-row) form would be the default."""
+    where the direct (thread-per-row) form would be the default;
+    sliced=True uses the sliced product form (a handle-owned copy of the
+    iteration matrix and of the SPAI factors in 32-row slices) where it
+    applies."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
                  validate: bool = True, pipeline: bool = False, fused: bool = False,
                  time_product: bool = False, producer_consumer: bool = False, reorder: bool | None = None,
-                 staged: bool = False, stream=None):
+                 staged: bool = False, sliced: bool = False, stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -120,6 +123,7 @@ class CSRMatrix:
                                   (_lib.SLA_TIME_PRODUCT if time_product else 0) |
                                   (_lib.SLA_PRODUCER_CONSUMER if producer_consumer else 0) |
                                   (_lib.SLA_STAGED if staged else 0) |
+                                  (_lib.SLA_SLICED if sliced else 0) |
                                   ({None: 0, True: _lib.SLA_REORDER, False: _lib.SLA_NO_REORDER}[reorder]),
                                   _stream(stream),
                                   C.byref(self._h)))

@@ -24,6 +24,7 @@ SLA_PRODUCER_CONSUMER = 16
 SLA_REORDER = 32
 SLA_NO_REORDER = 64
 SLA_STAGED = 128
+SLA_SLICED = 256
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",

@@ -27,8 +27,12 @@ template <> struct IterMinCtas<float> { static constexpr int value = 4; };
 #ifndef SLA_DIRECT_CTAS
 #define SLA_DIRECT_CTAS 4
 #endif
+// The sliced form (no staging either) is compiled for SLA_SLICED_CTAS.
+#ifndef SLA_SLICED_CTAS
+#define SLA_SLICED_CTAS 4
+#endif
 template <typename T, int FORM> struct ProductCtas {
-    static constexpr int value = FORM == 5 ? SLA_DIRECT_CTAS : IterMinCtas<T>::value;
+    static constexpr int value = FORM == 5 ? SLA_DIRECT_CTAS : FORM == 6 ? SLA_SLICED_CTAS : IterMinCtas<T>::value;
 };
 
 // Outcome codes mirrored from sla_status (kept numerically equal).

@@ -64,6 +64,14 @@ struct Mat {
     int stages;       // warp pipeline: ring stages
     int* err;         // device error bits (Ctrl::err; Ctrl::diag follows at err + 2)
     int direct;       // 1: the layout's kernels run the direct form (no shared-memory staging)
+    // Sliced form (FORM 6): the rows in slices of 32, each slice stored
+    // column by column (entry j of the slice's 32 rows side by side), padded
+    // to the slice's longest row.
+    const int* sptr;     // [nslices + 1] first entry of every slice (multiples of 32)
+    const int* sperm;    // [nslices * 32] row held by every slot (>= n: empty), or nullptr (slot = row)
+    const int* scol;     // [sptr[nslices]] column of every sliced entry (padding: a valid column)
+    int nslices;
+    long long vstride;   // per-system stride of the sliced values
 };
 
 #define SYS_PROLOGUE                                            \
@@ -234,6 +242,65 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
         for (int k = lo; k < hi; ++k) mac(s, ld_mat(av + k), gather(ld_mat(A.ci + k)));
         epi(row, s, carried);
     }
+}
+
+// Sliced form: one warp per slice of 32 rows (grid stride over slices;
+// the 8 warps of a CTA take 8 consecutive slices).  Lane l owns the slice's
+// l-th row: its entry j sits at sptr[slice] + 32 j + l, so each value and
+// column load of the warp reads 32 consecutive entries (coalesced), and
+// every lane of a slice runs the same trip count (the slice's width).  The
+// entries go in batches of SLICE_U -- all loads of a batch issued before its
+// gathers -- then one at a time.  Padding entries hold the value 0 and a
+// valid column.  Rows are summed in stored order (one fp64 FMA per entry
+// for fp64 systems).  No shared memory.
+// Measured on B300 inside the running iteration (kNN Laplacian; 3D and 2D
+// grids): plain batches of 4 beat batches of 6 or 8 predicated on the
+// width, batches of 3 or 4 software-pipelined (the next batch's values and
+// columns loaded before this batch's FMAs), and 3 resident CTAs per SM
+// (kNN product 191 us against 204-282 us).
+#ifndef SLA_SLICE_U
+#define SLA_SLICE_U 4
+#endif
+constexpr int SLICE_U = SLA_SLICE_U;
+
+template <typename T, typename VT, class Gather, class Pre, class Epi>
+__device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__ sv, Gather gather, Pre pre,
+                                            Epi epi) {
+    using acc_t = typename Prec<T>::acc;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * NT) >> 5;
+    for (int sl = (blockIdx.x * NT + threadIdx.x) >> 5; sl < A.nslices; sl += nwarps) {
+        const int base = ld_nc(A.sptr + sl);
+        const int w = (ld_nc(A.sptr + sl + 1) - base) >> 5;
+        const int slot = (sl << 5) + lane;
+        const int row = A.sperm ? ld_nc(A.sperm + slot) : slot;
+        const bool live = row < A.n;
+        const auto carried = live ? pre(row) : decltype(pre(0)){};
+        acc_t s = Prec<T>::zero();
+        const VT* v = sv + base + lane;
+        const int* c = A.scol + base + lane;
+        int j = 0;
+        for (; j + SLICE_U <= w; j += SLICE_U) {
+            VT a[SLICE_U];
+            int cc[SLICE_U];
+#pragma unroll
+            for (int u = 0; u < SLICE_U; ++u) {
+                a[u] = ld_mat(v + (j + u) * 32);
+                cc[u] = ld_mat(c + (j + u) * 32);
+            }
+#pragma unroll
+            for (int u = 0; u < SLICE_U; ++u) mac(s, a[u], gather(cc[u]));
+        }
+        for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
+        if (live) epi(row, s, carried);
+    }
+}
+
+// Offset of system `sys`'s values: the CSR values ([batch][nnz]) or, for
+// the sliced form, the sliced values ([batch][vstride]).
+template <int FORM>
+__device__ __forceinline__ size_t val_offset(const Mat& A, int sys, long long nnz) {
+    return (size_t)sys * (size_t)(FORM == 6 ? A.vstride : nnz);
 }
 
 template <typename T, typename VT, class Gather, class Pre, class Epi>
@@ -781,16 +848,18 @@ __device__ __forceinline__ void spmv_ws(const Mat& A, const VT* __restrict__ av,
     __syncthreads();
 }
 
-// Product with a plain vector gather in one of six compiled forms (the
+// Product with a plain vector gather in one of seven compiled forms (the
 // host picks one per matrix, so each kernel instantiation carries a single
 // path): FORM 0 register staging (spmv_rows); FORM 1 cp.async value/column
 // staging with register gathers; FORM 2 cp.async staging and gathers; FORM 3
 // the warp pipeline (spmv_pipe); FORM 4 producer/consumer warps (spmv_ws);
-// FORM 5 the direct form (spmv_direct).
+// FORM 5 the direct form (spmv_direct); FORM 6 the sliced form
+// (spmv_sliced, on the layout's sliced copy of the values).
 template <typename T, int FORM, typename VT, typename XT, bool COH = false, class Pre, class Epi>
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
     if constexpr (FORM == 5) spmv_direct<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
+    else if constexpr (FORM == 6) spmv_sliced<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
     else if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
     else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
     else if constexpr (FORM == 4) spmv_ws<T, VT, XT>(A, av, v, pre, epi, wsm);
@@ -895,7 +964,7 @@ __global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CT
     SYS_PROLOGUE
     extern __shared__ __align__(16) double dsm[];
     __shared__ double red[RED_DOUBLES];
-    av += ao; x += vo; y += vo;
+    av += val_offset<FORM>(A, sys, S.nnz); x += vo; y += vo;
     acc_t acc = Prec<T>::zero();
     spmv_vec<T, FORM, T, T>(A, av, x, [&](int i) { return x[i]; },
                    [&](int i, acc_t s, T xi) {
@@ -938,11 +1007,22 @@ __device__ __noinline__ typename Prec<T>::acc residual_staged(const Mat& A, cons
                     [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
     return tr2;
 }
+template <typename T, bool COH>
+__device__ __forceinline__ typename Prec<T>::acc residual_sliced(const Mat& A, const T* __restrict__ sv,
+                                                                 const typename Prec<T>::xw* x,
+                                                                 const T* __restrict__ b) {
+    using acc_t = typename Prec<T>::acc;
+    acc_t tr2 = Prec<T>::zero();
+    spmv_sliced<T, T>(A, sv, GatherX<T, COH>{x}, [&](int i) { return b[i]; },
+                      [&](int, acc_t s, T bi) { sq_acc(tr2, resid(bi, s)); });
+    return tr2;
+}
 template <typename T, int FORM, bool COH = false>
 __device__ __forceinline__ typename Prec<T>::acc residual_pass(const Mat& A, const T* __restrict__ av,
                                                                const typename Prec<T>::xw* x,
                                                                const T* __restrict__ b, double* dsm) {
     if constexpr (FORM == 5) return residual_direct<T, COH>(A, av, x, b);
+    else if constexpr (FORM == 6) return residual_sliced<T, COH>(A, av, x, b);
     else return residual_staged<T, FORM, COH>(A, av, x, b, dsm);
 }
 
@@ -962,7 +1042,7 @@ __global__ void __launch_bounds__(NT, (ProductCtas<T, FORM>::value))
     }
     extern __shared__ __align__(16) double dsm[];
     __shared__ double red[RED_DOUBLES];
-    av += ao; p += vo; q += vo; x += vo; b += vo;
+    av += val_offset<FORM>(A, sys, S.nnz); p += vo; q += vo; x += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
     acc_t tr2 = Prec<T>::zero(), delta = Prec<T>::zero();
     if (check) tr2 = residual_pass<T, FORM>(A, av, x, b, dsm);
@@ -1005,9 +1085,14 @@ __device__ __forceinline__ void update_r(A alpha, W& ri, W qi, XW di, W& zi, A& 
     }
 }
 
-// Pairs per thread per trip of the streaming kernels (measured on B300:
-// one pair with two resident CTAs per SM beats deeper unrolling).
-constexpr int VU = 1;
+// Pairs per thread per trip of the streaming kernels (measured on B300
+// inside the running iteration: one pair per thread with two resident CTAs
+// per SM beats two pairs, or four and eight CTAs per SM, on the 2D, 3D and
+// kNN workloads).
+#ifndef SLA_VU
+#define SLA_VU 1
+#endif
+constexpr int VU = SLA_VU;
 
 // r -= alpha q; gamma = r.r; rho' = r.z (PC 0: z = r; PC 1: z = r / A_ii,
 // stored; PC 2: z comes later from the SPAI kernels).  x is advanced by
@@ -1144,7 +1229,7 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __re
 // SPAI, first product: t = G^T r (explicit transposed CSR of G; G values
 // are per system, [batch][nnz(G)]).
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_t(Mat GT, Sys S, long long nnzg,
+__global__ void __launch_bounds__(NT, (FORM >= 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_t(Mat GT, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gtv,
                                                               const typename Prec<T>::w* __restrict__ r,
                                                               typename Prec<T>::w* __restrict__ t) {
@@ -1153,14 +1238,14 @@ __global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CT
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ __align__(16) double dsm[];
-    gtv += (size_t)sys * nnzg; r += vo; t += vo;
+    gtv += val_offset<FORM>(GT, sys, nnzg); r += vo; t += vo;
     spmv_vec<T, FORM, typename Prec<T>::gv, W>(GT, gtv, r, [](int) { return W{}; },
                                          [&](int i, acc_t s, W) { st_vec(t + i, to_w(s)); }, dsm);
 }
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_z(Mat G, Sys S, long long nnzg,
+__global__ void __launch_bounds__(NT, (FORM >= 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_z(Mat G, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gv,
                                                               const typename Prec<T>::w* __restrict__ t,
                                                               const typename Prec<T>::w* __restrict__ r,
@@ -1171,7 +1256,7 @@ __global__ void __launch_bounds__(NT, (FORM == 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CT
     if (ld_cg(&st->done)) return;
     extern __shared__ __align__(16) double dsm[];
     __shared__ double red[RED_DOUBLES];
-    gv += (size_t)sys * nnzg; t += vo; r += vo; z += vo;
+    gv += val_offset<FORM>(G, sys, nnzg); t += vo; r += vo; z += vo;
     const acc_t e = Prec<T>::scal(eps);
     acc_t rz = Prec<T>::zero();
     spmv_vec<T, FORM, typename Prec<T>::gv, W>(G, gv, t, [&](int i) { return r[i]; },

@@ -125,6 +125,46 @@ __global__ void k_gather_map(long long m, int batch, const int* __restrict__ map
     }
 }
 
+// out[s * os + i] = in[s * is + map[i]], or 0 where map[i] < 0: the sliced
+// copy of the values (map = source CSR entry of every sliced entry, -1 for
+// padding).  T is an unsigned type of the value's size (bits are copied).
+template <typename T>
+__global__ void k_gather_map_pad(long long m, int batch, const int* __restrict__ map, const T* __restrict__ in,
+                                 long long is, T* __restrict__ out, long long os) {
+    const long long total = m * batch;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long s = t / m, i = t - s * m;
+        const int k = map[i];
+        out[s * os + i] = k >= 0 ? in[s * is + k] : T(0);
+    }
+}
+
+// Sliced pattern: slot t = 32 * slice + lane holds row perm[t] (t itself
+// when perm is null; >= n: an empty slot); its entry j (j < the slice's
+// width) goes to sptr[slice] + 32 j + lane.  Entries past the row's length
+// are padding: column = the row itself (0 for an empty slot), source -1.
+__global__ void k_sell_fill(int n, int nslices, const int* __restrict__ rp, const int* __restrict__ ci,
+                            const int* __restrict__ sptr, const int* __restrict__ perm, int* __restrict__ scol,
+                            int* __restrict__ smap) {
+    const long long slots = (long long)nslices * 32;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < slots;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int sl = (int)(t >> 5), lane = (int)(t & 31);
+        const int base = sptr[sl];
+        const int w = (sptr[sl + 1] - base) >> 5;
+        const int row = perm ? perm[t] : (int)t;
+        const int lo = row < n ? rp[row] : 0;
+        const int len = row < n ? rp[row + 1] - lo : 0;
+        const int fill = row < n ? row : 0;
+        for (int j = 0; j < w; ++j) {
+            const int idx = base + 32 * j + lane;
+            scol[idx] = j < len ? ci[lo + j] : fill;
+            smap[idx] = j < len ? lo + j : -1;
+        }
+    }
+}
+
 // Number of stored entries whose column is more than `w` away from the row.
 __global__ void k_far_count(const int* __restrict__ rp, const int* __restrict__ ci, int n, int w,
                             unsigned long long* out) {

@@ -135,6 +135,28 @@ struct Layout {
     int form = 0;     // compiled form of the product kernels (spmv_vec)
     size_t smem = 0;  // their dynamic shared memory
     int maxrow = 0;   // longest row
+    // sliced copy (form 6), owned by the handle's SellBufs
+    const int* sptr = nullptr;
+    const int* sperm = nullptr;
+    const int* scol = nullptr;
+    const void* sval = nullptr;
+    int nslices = 0;
+    long long vstride = 0;
+};
+
+// Sliced copy of a matrix (form 6): slice pointers, the row of every slot
+// (when rows are reordered within windows), columns, the source CSR entry
+// of every sliced entry (-1: padding) and the sliced values [batch][vstride].
+struct SellBufs {
+    DevBuf sptr, perm, scol, smap, sval;
+    long long npad = 0;
+    long long vstride = 0;
+    int nslices = 0;
+    void release() {
+        sptr.release(); perm.release(); scol.release(); smap.release(); sval.release();
+        npad = vstride = 0;
+        nslices = 0;
+    }
 };
 
 struct sla_csr {
@@ -192,6 +214,10 @@ struct sla_csr {
     // graphs: CG per preconditioner (0..2), BiCGStab on A / A^T per
     // preconditioner (3 + 2 * transposed + pc)
     GraphCache graph[7];
+
+    // sliced copies (form 6) of the iteration matrix and of G, G^T
+    bool sliced = false;        // SLA_SLICED: sliced product form where it applies
+    SellBufs sI, sG, sGT;
 
     // BiCGStab (built on first use): the iteration matrix's layout with the
     // register / cp.async forms only (its values may be a handle-owned
@@ -359,9 +385,13 @@ static void with_form(int form, F&& f) {
         case 2: f(std::integral_constant<int, 2>{}); break;
         case 3: f(std::integral_constant<int, 3>{}); break;
         case 4: f(std::integral_constant<int, 4>{}); break;
+        case 6: f(std::integral_constant<int, 6>{}); break;
         default: f(std::integral_constant<int, 5>{}); break;
     }
 }
+// The persistent iteration kernel runs on the CSR arrays: a sliced layout
+// (whose rows are also short) takes the direct form there.
+static int fused_form(int form) { return form == 6 ? 5 : form; }
 
 // Compiled form, shared memory and CTAs per system of a layout's kernels.
 // The warp pipeline needs a group capacity (pattern) and 16-byte aligned
@@ -479,7 +509,13 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     m.ccap = L.form == 4 ? L.tcap : L.ccap;   // entries per stage of the bulk-copy forms
     m.stages = L.stages;
     m.err = err;
-    m.direct = L.form == 5 ? 1 : 0;
+    // kernels on the CSR arrays take the direct form under a sliced layout
+    m.direct = (L.form == 5 || L.form == 6) ? 1 : 0;
+    m.sptr = L.sptr;
+    m.sperm = L.sperm;
+    m.scol = L.scol;
+    m.nslices = L.nslices;
+    m.vstride = L.vstride;
     return m;
 }
 static Mat mat_A(const sla_csr* h) { return mat_of(h->rp, h->ci, h->n, h->nnz, h->LA, &h->ctl.as<Ctrl>()->err); }
@@ -721,6 +757,142 @@ static sla_status gather_map(size_t eb, long long m, int batch, const int* map, 
     return launched();
 }
 
+// ===================================================================== sliced copies
+// Rows per window whose slots may be reordered by length: the smallest of
+// one, four or sixteen CTAs' slices in one trip of the sliced kernels
+// (NWARP slices of 32 rows each) that pads at most SLICE_GOOD_PAD (else the
+// least padding), so the rows a window's results go to are written by few
+// CTAs at about the same time.  On the kNN Laplacian one CTA's 256 rows pad
+// A by 4%, but the SPAI factor (whose row lengths vary most) by 15.5%; 1024
+// rows pad it by 4%.
+static constexpr int SLICE_WINDOWS[3] = {NWARP * 32, 4 * NWARP * 32, 16 * NWARP * 32};
+static constexpr double SLICE_GOOD_PAD = 1.06;
+// Largest padding (sliced entries / stored entries) for which the sliced
+// form is used.
+#ifndef SLA_SLICED_MAXPAD
+#define SLA_SLICED_MAXPAD 1.15
+#endif
+
+// values: the CSR values the sliced copy mirrors ([batch][is] of eb bytes).
+static sla_status sliced_values(const sla_csr* h, SellBufs& B, const void* vals, long long is, size_t eb,
+                                cudaStream_t s) {
+    if (B.npad == 0) return SLA_OK;
+    const long long tot = B.npad * h->batch;
+    const int g = (int)std::min<long long>((tot + 255) / 256, 8192);
+    if (eb == 8)
+        k_gather_map_pad<unsigned long long><<<g, 256, 0, s>>>(B.npad, h->batch, B.smap.as<int>(),
+                                                               (const unsigned long long*)vals, is,
+                                                               B.sval.as<unsigned long long>(), B.vstride);
+    else
+        k_gather_map_pad<unsigned><<<g, 256, 0, s>>>(B.npad, h->batch, B.smap.as<int>(), (const unsigned*)vals, is,
+                                                     B.sval.as<unsigned>(), B.vstride);
+    return launched();
+}
+
+// Build the sliced copy of the pattern (rp, ci; nnz entries) and its values
+// and switch L to form 6, when the padding stays within SLA_SLICED_MAXPAD;
+// otherwise leave L as it is.  Within every window of SLICE_WINDOWS rows the
+// rows are ordered by decreasing length when that pads less (the slot ->
+// row map is then kept); the kernels write each row's result to its own
+// row, so the iteration order is unchanged.
+template <typename T>
+static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long long nnz, const void* vals,
+                              long long is, size_t eb, Layout* L, SellBufs& B, cudaStream_t s) {
+    const int n = h->n;
+    if (nnz == 0 || n < 1) return SLA_OK;
+    std::vector<int> rp;
+    CU(cudaStreamSynchronize(s));
+    TRY(to_host(rp, d_rp, (size_t)n + 1));
+    const int nslices = (int)(((long long)n + 31) / 32);
+    const long long slots = (long long)nslices * 32;
+    auto len = [&](long long r) { return r < n ? rp[r + 1] - rp[r] : 0; };
+    // padding of the identity order and of the window-sorted order
+    long long pad_id = 0;
+    for (int sl = 0; sl < nslices; ++sl) {
+        int w = 0;
+        for (int l = 0; l < 32; ++l) w = std::max(w, len((long long)sl * 32 + l));
+        pad_id += 32LL * w;
+    }
+    std::vector<int> perm, sptr;
+    long long pad_sorted = 0;
+    for (int wi = 0; wi < 3; ++wi) {
+        const int window = SLICE_WINDOWS[wi];
+        std::vector<int> pw(slots), sw(nslices + 1, 0);
+        for (long long t = 0; t < slots; ++t) pw[t] = t < n ? (int)t : n;
+        for (long long w0 = 0; w0 < n; w0 += window) {
+            const long long w1 = std::min<long long>(w0 + window, n);
+            std::stable_sort(pw.begin() + w0, pw.begin() + w1, [&](int a, int b) { return len(a) > len(b); });
+        }
+        for (int sl = 0; sl < nslices; ++sl) {
+            int w = 0;
+            for (int l = 0; l < 32; ++l) w = std::max(w, len(pw[(size_t)sl * 32 + l]));
+            sw[sl + 1] = (int)std::min<long long>((long long)sw[sl] + 32LL * w, 0x7fffffffLL);
+        }
+        if (perm.empty() || sw[nslices] < pad_sorted) {
+            perm.swap(pw);
+            sptr.swap(sw);
+            pad_sorted = sptr[nslices];
+        }
+        if ((double)pad_sorted <= SLICE_GOOD_PAD * (double)nnz) break;
+    }
+    const bool sorted = pad_sorted < pad_id && (double)pad_id > 1.02 * (double)nnz;
+    const long long npad = sorted ? pad_sorted : pad_id;
+    if ((double)npad > SLA_SLICED_MAXPAD * (double)nnz || npad >= 0x7fffffffLL) return SLA_OK;
+    if (!sorted) {
+        for (int sl = 0; sl < nslices; ++sl) {
+            int w = 0;
+            for (int l = 0; l < 32; ++l) w = std::max(w, len((long long)sl * 32 + l));
+            sptr[sl + 1] = sptr[sl] + 32 * w;
+        }
+    }
+    B.release();
+    TRY(to_device(B.sptr, sptr));
+    if (sorted) TRY(to_device(B.perm, perm));
+    TRY(B.scol.alloc(sizeof(int) * (size_t)npad));
+    TRY(B.smap.alloc(sizeof(int) * (size_t)npad));
+    B.npad = npad;
+    B.vstride = (npad + 1) & ~1LL;   // 16-byte aligned systems
+    B.nslices = nslices;
+    {
+        const int g = (int)std::min<long long>((slots + 255) / 256, 8192);
+        k_sell_fill<<<g, 256, 0, s>>>(n, nslices, d_rp, d_ci, B.sptr.as<int>(), sorted ? B.perm.as<int>() : nullptr,
+                                      B.scol.as<int>(), B.smap.as<int>());
+        TRY(launched());
+    }
+    TRY(B.sval.alloc(eb * (size_t)B.vstride * h->batch));
+    TRY(sliced_values(h, B, vals, is, eb, s));
+    int per = 1;
+    TRY(occupancy(k_spmv_iter<T, 6>, 0, &per));
+    L->form = 6;
+    L->smem = 0;
+    L->sptr = B.sptr.as<int>();
+    L->sperm = sorted ? B.perm.as<int>() : nullptr;
+    L->scol = B.scol.as<int>();
+    L->sval = B.sval.p;
+    L->nslices = nslices;
+    L->vstride = B.vstride;
+    L->gx = grid_x(h, (slots + NT - 1) / NT, per);
+    return SLA_OK;
+}
+
+// Default choice of the sliced form for the iteration matrix: rows too
+// long for the direct form and long enough on average (measured on B300:
+// the kNN Laplacian, 14.6 entries per row, 192 against 238 us staged; on
+// the 2D and 3D grids, 5 and 7 per row, the direct form is as fast; the
+// SPAI factor of the kNN Laplacian, 7.8 per row, runs faster staged).
+#ifndef SLA_SLICED_MINAVG
+#define SLA_SLICED_MINAVG 12.0
+#endif
+static bool sliced_by_default(const sla_csr* h, const Layout& L, long long nnz) {
+    return L.maxrow > SLA_DIRECT_MAXROW && (double)nnz >= SLA_SLICED_MINAVG * (double)h->n;
+}
+
+static sla_status make_sliced_any(sla_csr* h, const int* d_rp, const int* d_ci, long long nnz, const void* vals,
+                                  long long is, size_t eb, Layout* L, SellBufs& B, cudaStream_t s) {
+    return h->dt == SLA_F64 ? make_sliced<double>(h, d_rp, d_ci, nnz, vals, is, eb, L, B, s)
+                            : make_sliced<float>(h, d_rp, d_ci, nnz, vals, is, eb, L, B, s);
+}
+
 // Iterate on P A P^T (reverse Cuthill-McKee): permuted pattern and values
 // owned by the handle, with the permutation both ways.
 static sla_status make_reordered(sla_csr* h, cudaStream_t s) {
@@ -772,6 +944,7 @@ static void release_spai(sla_csr* h) {
     h->spai_ready = false;
     h->grp.release(); h->gci.release(); h->gv.release();
     h->gtrp.release(); h->gtci.release(); h->gtv.release();
+    h->sG.release(); h->sGT.release();
     h->t.release();
     for (auto& g : h->graph) g.reset();
 }
@@ -863,6 +1036,11 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
                       SLA_DIRECT_MAXROW_G));
     TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s,
                       SLA_DIRECT_MAXROW_G));
+    if (h->sliced) {   // only when asked: staged G and G^T measured faster (kNN Laplacian)
+        TRY(make_sliced_any(h, h->grp.as<int>(), h->gci.as<int>(), ng, h->gv.p, h->gstride, 8, &h->LG, h->sG, s));
+        TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
+                            s));
+    }
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
     h->spai_ready = true;
     return ensure_pstride(h);
@@ -909,8 +1087,9 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     // external event-record nodes (a plain record inside a capture only
     // orders streams within the graph)
     if (ev0) CU(cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal));
+    const T* avi = h->LI.form == 6 ? (const T*)h->LI.sval : av;
     with_form(h->LI.form, [&](auto f) {
-        k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LI.smem, s>>>(A, S, av, p, q, x, h->bw.as<T>());
+        k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LI.smem, s>>>(A, S, avi, p, q, x, h->bw.as<T>());
     });
     TRY(launched());
     if (ev1) CU(cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal));
@@ -919,15 +1098,16 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
         TRY(launched());
         const Mat GT = mat_GT(h);
         const Mat G = mat_G(h);
+        const GV* gtv = h->LGT.form == 6 ? (const GV*)h->LGT.sval : h->gtv.as<GV>();
+        const GV* gvv = h->LG.form == 6 ? (const GV*)h->LG.sval : h->gv.as<GV>();
         with_form(h->LGT.form, [&](auto f) {
         k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, h->LGT.smem, s>>>(GT, S, h->gstride,
-                                                                                        h->gtv.as<GV>(), r,
-                                                                                        h->t.as<W>());
+                                                                                        gtv, r, h->t.as<W>());
         });
         TRY(launched());
         with_form(h->LG.form, [&](auto f) {
         k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, h->LG.smem, s>>>(
-            G, S, h->gstride, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
+            G, S, h->gstride, gvv, h->t.as<W>(), r, h->z.as<W>(), eps);
         });
         TRY(launched());
         k_pupdate<T, false, PAIRS><<<gv, NT, 0, s>>>(S, p, x, h->z.as<W>());
@@ -1022,13 +1202,13 @@ template <typename T, int PC, bool PAIRS>
 static sla_status fused_grid(const sla_csr* h, int* gx) {
     int per = 0;
     cudaError_t e = cudaSuccess;
-    with_form(h->LI.form, [&](auto f) {
+    with_form(fused_form(h->LI.form), [&](auto f) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_cg_fused<T, decltype(f)::value, PC, PAIRS>, NT,
                                                           h->LI.smem);
     });
     if (e != cudaSuccess) return fail(SLA_ERR_CUDA, "occupancy query failed: %s", cudaGetErrorString(e));
     long long g = (long long)per * h->sms / h->batch;
-    const long long rows_work = h->LI.form == 5 ? ((long long)h->n + NT - 1) / NT
+    const long long rows_work = fused_form(h->LI.form) == 5 ? ((long long)h->n + NT - 1) / NT
                                                 : group_ctas(h->n, h->LI.form == 3 ? 1 : h->LI.lanes);
     const long long work = std::max(rows_work, vec_units(h));
     if (g > work) g = work;
@@ -1053,7 +1233,7 @@ static sla_status launch_fused(sla_csr* h, int gx, int iters, cudaStream_t s) {
     GridSync* gsy = h->gsync.as<GridSync>();
     void* args[] = {&A, &S, &av, &p, &q, &r, &z, &x, &dinv, &b, &gsy, &iters};
     cudaError_t e = cudaSuccess;
-    with_form(h->LI.form, [&](auto f) {
+    with_form(fused_form(h->LI.form), [&](auto f) {
         e = cudaLaunchCooperativeKernel((const void*)k_cg_fused<T, decltype(f)::value, PC, PAIRS>,
                                         dim3((unsigned)gx, (unsigned)h->batch), dim3(NT), args, h->LI.smem, s);
     });
@@ -1233,15 +1413,16 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     if (pc == SLA_PC_SPAI) {
         const Mat GT = mat_GT(h);
         const Mat G = mat_G(h);
+        const GV* gtv = h->LGT.form == 6 ? (const GV*)h->LGT.sval : h->gtv.as<GV>();
+        const GV* gvv = h->LG.form == 6 ? (const GV*)h->LG.sval : h->gv.as<GV>();
         with_form(h->LGT.form, [&](auto f) {
         k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, h->LGT.smem, s>>>(GT, S, h->gstride,
-                                                                                       h->gtv.as<GV>(), r,
-                                                                                       h->t.as<W>());
+                                                                                       gtv, r, h->t.as<W>());
         });
         TRY(launched());
         with_form(h->LG.form, [&](auto f) {
         k_spai_z<T, decltype(f)::value><<<dim3(h->LG.gx, h->batch), NT, h->LG.smem, s>>>(
-            G, S, h->gstride, h->gv.as<GV>(), h->t.as<W>(), r, h->z.as<W>(), eps);
+            G, S, h->gstride, gvv, h->t.as<W>(), r, h->z.as<W>(), eps);
         });
         TRY(launched());
         k_pupdate<T, true, false><<<gv, NT, 0, s>>>(S, p, x, h->z.as<W>());
@@ -1556,6 +1737,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     h->staged = (flags & SLA_STAGED) != 0;
     h->time_product = (flags & SLA_TIME_PRODUCT) != 0;
     h->persistent = (flags & SLA_PERSISTENT) != 0;
+    h->sliced = (flags & SLA_SLICED) != 0;
     {
         int coop = 0;
         HCU(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
@@ -1574,6 +1756,8 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
         const bool al = h->batch == 1 || ((size_t)nnz * h->es) % 16 == 0;
         HTRY(choose_layout(h, h->irp, h->ici, nnz, &h->LI, al, h->es, s));
     }
+    if (!h->pipeline && !h->ws && !h->staged && (h->sliced || sliced_by_default(h, h->LI, nnz)))
+        HTRY(make_sliced_any(h, h->irp, h->ici, nnz, h->ivals, nnz, h->es, &h->LI, h->sI, s));
     const size_t vn = (size_t)n * batch;
     HTRY(h->diag.alloc(sizeof(double) * vn));
     HTRY(h->dinv.alloc(sizeof(double) * vn));
@@ -1630,11 +1814,16 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
     if (vals_aligned(h, d_vals) != h->vals_aligned) {
         h->vals_aligned = !h->vals_aligned;
         TRY(set_form_any(h, &h->LA, h->vals_aligned, h->es));
-        if (!h->reordered) h->LI = h->LA;
+        if (!h->reordered) {
+            const bool was_sliced = h->LI.form == 6;
+            h->LI = h->LA;
+            if (was_sliced) TRY(make_sliced_any(h, h->irp, h->ici, h->nnz, d_vals, h->nnz, h->es, &h->LI, h->sI, s));
+        }
         TRY(ensure_pstride(h));
     }
     if (h->reordered) TRY(gather_map(h->es, h->nnz, h->batch, h->psrc.as<int>(), d_vals, h->nnz, h->pvals.p, h->nnz, s));
     else h->ivals = d_vals;
+    if (h->LI.form == 6) TRY(sliced_values(h, h->sI, h->ivals, h->nnz, h->es, s));
     TRY(compute_diag(h, s));
     CU(cudaStreamSynchronize(s));
     return SLA_OK;
@@ -1645,16 +1834,20 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     if (!d_x || !d_y) return fail(SLA_ERR_INVALID, "null vector");
     cudaStream_t s = (cudaStream_t)stream;
     const Sys S = sys_of(h);
-    const Mat A = mat_A(h);
-    const dim3 g(h->LA.gx, h->batch);
-    const size_t sm = h->LA.smem;
-    with_form(h->LA.form, [&](auto f) {
+    // the sliced copy of the iteration matrix serves A itself when the
+    // handle does not reorder
+    const bool sl = !h->reordered && h->LI.form == 6;
+    const Layout& L = sl ? h->LI : h->LA;
+    const Mat A = sl ? mat_I(h) : mat_A(h);
+    const void* vals = sl ? L.sval : h->vals;
+    const dim3 g(L.gx, h->batch);
+    const size_t sm = L.smem;
+    with_form(L.form, [&](auto f) {
         constexpr int F = decltype(f)::value;
         if (h->dt == SLA_F64)
-            k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_x, (double*)d_y,
-                                                d_dot);
+            k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)vals, (const double*)d_x, (double*)d_y, d_dot);
         else
-            k_spmv<float, F><<<g, NT, sm, s>>>(A, S, (const float*)h->vals, (const float*)d_x, (float*)d_y, d_dot);
+            k_spmv<float, F><<<g, NT, sm, s>>>(A, S, (const float*)vals, (const float*)d_x, (float*)d_y, d_dot);
     });
     return launched();
 }

@@ -5,8 +5,8 @@ in seconds (many warp groups and CTAs and a ragged tail), plus edge cases.
 Every product test runs with the default form (the direct, thread-per-row
 form for patterns whose rows have at most 16 entries, else a warp-staged
 form), the warp-staged forms (staged=True), the warp pipeline
-(pipeline=True) and the producer/consumer form (producer_consumer=True),
-the last two wherever the matrix fits their stages; the solve tests run with one kernel per step in a CUDA graph (the
+(pipeline=True), the producer/consumer form (producer_consumer=True) and
+the sliced form (sliced=True), the last three wherever they apply; the solve tests run with one kernel per step in a CUDA graph (the
 default) and with the persistent iteration kernel (fused=True), each with
 every product form.
 
@@ -50,7 +50,9 @@ def _spmv_cases():
 
 
 FORMS = {"default": {}, "staged": {"staged": True}, "pipe": {"pipeline": True},
-         "pc": {"producer_consumer": True}}
+         "pc": {"producer_consumer": True}, "sliced": {"sliced": True}}
+# patterns whose sliced copy pads by at most 15% (the sliced form applies)
+SLICED = ("poisson2d_64", "poisson3d_24", "diffusion_96", "knn_3000")
 PIPE = pytest.mark.parametrize("mode", list(FORMS))
 MODES = pytest.mark.parametrize("mode,fused", [(m, f) for f in (False, True) for m in FORMS],
                                 ids=[f"{m}-{'fused' if f else 'steps'}" for f in (False, True) for m in FORMS])
@@ -72,6 +74,8 @@ def test_spmv_parity(cuda_device, name, A, dtype, mode):
         assert form == 3, form
     elif mode == "pc":
         assert form == 4, form
+    elif mode == "sliced" and name in SLICED:
+        assert form == 6, form
     xd = torch.from_numpy(x).to(cuda_device)
     y = M.matvec(xd).cpu().numpy()
     y_o = oracle.spmv(A, x.astype(np.float64))
