@@ -150,17 +150,19 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         built for high occupancy -- the default whenever no row has more
  *         than 16 entries, unless SLA_STAGED, SLA_WARP_PIPELINE or
  *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2;
- *         6 sliced (not with SLA_STAGED, SLA_WARP_PIPELINE or
+ *         6 and 7 sliced (not with SLA_STAGED, SLA_WARP_PIPELINE or
  *         SLA_PRODUCER_CONSUMER): a handle-owned copy of the iteration
  *         matrix in slices of 32 rows stored column by column (rows
  *         reordered by length within windows of 256, 1024 or 4096 rows when
  *         that pads less), used when padding adds at most 15% entries; one
- *         thread per row, coalesced value and column loads.  The default
- *         for the iteration matrix when some row has more than 16 entries
- *         and rows hold at least 12 on average; with SLA_SLICED wherever it
- *         applies, the SPAI factors included.  Costs (8 + value size) bytes
- *         per sliced entry of device memory, and the values are copied again
- *         by sla_csr_update_values.
+ *         thread per row, coalesced value and column loads; 6 for rows of
+ *         at least 12 entries on average, 7 (more resident CTAs) for
+ *         shorter ones.  The default for the iteration matrix when some row
+ *         has more than 16 entries and rows hold at least 12 on average, or
+ *         when no row has more than 16 and rows hold at least 6 on average;
+ *         with SLA_SLICED wherever it applies, the SPAI factors included.
+ *         Costs (8 + value size) bytes per sliced entry of device memory,
+ *         and the values are copied again by sla_csr_update_values.
  *         The SPAI factors G and G^T take their forms by the same rule;
  *         the BiCGStab products always take a staged form (0, 1 or 2);
  *  *ctas: CTAs per system of the product kernels;

@@ -27,12 +27,23 @@ template <> struct IterMinCtas<float> { static constexpr int value = 4; };
 #ifndef SLA_DIRECT_CTAS
 #define SLA_DIRECT_CTAS 4
 #endif
-// The sliced form (no staging either) is compiled for SLA_SLICED_CTAS.
+// The sliced form (no staging either) is compiled twice: FORM 6 for
+// SLA_SLICED_CTAS resident CTAs per SM (long rows, whose scattered gathers
+// want the caches to themselves: on the kNN Laplacian 5 and 6 CTAs per SM
+// took 270 and 303 us against 191 us at 4) and FORM 7 for SLA_SLICED_CTAS_SHORT
+// (short rows: the 3D 7-point product 51.4 us at 5 against 55.6 us at 4).
 #ifndef SLA_SLICED_CTAS
 #define SLA_SLICED_CTAS 4
 #endif
+#ifndef SLA_SLICED_CTAS_SHORT
+#define SLA_SLICED_CTAS_SHORT 5
+#endif
+__host__ __device__ constexpr bool sliced_form(int form) { return form == 6 || form == 7; }
 template <typename T, int FORM> struct ProductCtas {
-    static constexpr int value = FORM == 5 ? SLA_DIRECT_CTAS : FORM == 6 ? SLA_SLICED_CTAS : IterMinCtas<T>::value;
+    static constexpr int value = FORM == 5   ? SLA_DIRECT_CTAS
+                                 : FORM == 6 ? SLA_SLICED_CTAS
+                                 : FORM == 7 ? SLA_SLICED_CTAS_SHORT
+                                             : IterMinCtas<T>::value;
 };
 
 // Outcome codes mirrored from sla_status (kept numerically equal).

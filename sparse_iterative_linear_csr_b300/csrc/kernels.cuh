@@ -262,6 +262,9 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
 #define SLA_SLICE_U 4
 #endif
 constexpr int SLICE_U = SLA_SLICE_U;
+#ifndef SLA_SLICE_TAIL
+#define SLA_SLICE_TAIL 0
+#endif
 
 template <typename T, typename VT, class Gather, class Pre, class Epi>
 __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__ sv, Gather gather, Pre pre,
@@ -279,6 +282,7 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
         acc_t s = Prec<T>::zero();
         const VT* v = sv + base + lane;
         const int* c = A.scol + base + lane;
+#if SLA_SLICE_TAIL == 0
         int j = 0;
         for (; j + SLICE_U <= w; j += SLICE_U) {
             VT a[SLICE_U];
@@ -292,15 +296,38 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
             for (int u = 0; u < SLICE_U; ++u) mac(s, a[u], gather(cc[u]));
         }
         for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
+#else
+        // the last batch loads its missing entries again from the slice's
+        // last entry (an L1 hit) and drops them, so no entry is summed alone
+        for (int j = 0; j < w; j += SLICE_U) {
+            VT a[SLICE_U];
+            int cc[SLICE_U];
+#pragma unroll
+            for (int u = 0; u < SLICE_U; ++u) {
+                const int k = min(j + u, w - 1);
+                a[u] = ld_mat(v + k * 32);
+                cc[u] = ld_mat(c + k * 32);
+            }
+#pragma unroll
+            for (int u = 0; u < SLICE_U; ++u) {
+#if SLA_SLICE_TAIL == 1
+                mac(s, j + u < w ? a[u] : VT{}, gather(cc[u]));
+#else
+                const auto xv = gather(cc[u]);
+                if (j + u < w) mac(s, a[u], xv);
+#endif
+            }
+        }
+#endif
         if (live) epi(row, s, carried);
     }
 }
 
 // Offset of system `sys`'s values: the CSR values ([batch][nnz]) or, for
-// the sliced form, the sliced values ([batch][vstride]).
+// the sliced forms, the sliced values ([batch][vstride]).
 template <int FORM>
 __device__ __forceinline__ size_t val_offset(const Mat& A, int sys, long long nnz) {
-    return (size_t)sys * (size_t)(FORM == 6 ? A.vstride : nnz);
+    return (size_t)sys * (size_t)(sliced_form(FORM) ? A.vstride : nnz);
 }
 
 template <typename T, typename VT, class Gather, class Pre, class Epi>
@@ -853,13 +880,14 @@ __device__ __forceinline__ void spmv_ws(const Mat& A, const VT* __restrict__ av,
 // path): FORM 0 register staging (spmv_rows); FORM 1 cp.async value/column
 // staging with register gathers; FORM 2 cp.async staging and gathers; FORM 3
 // the warp pipeline (spmv_pipe); FORM 4 producer/consumer warps (spmv_ws);
-// FORM 5 the direct form (spmv_direct); FORM 6 the sliced form
-// (spmv_sliced, on the layout's sliced copy of the values).
+// FORM 5 the direct form (spmv_direct); FORMs 6 and 7 the sliced form
+// (spmv_sliced, on the layout's sliced copy of the values; compiled for 4
+// and 5 resident CTAs per SM).
 template <typename T, int FORM, typename VT, typename XT, bool COH = false, class Pre, class Epi>
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
     if constexpr (FORM == 5) spmv_direct<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
-    else if constexpr (FORM == 6) spmv_sliced<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
+    else if constexpr (sliced_form(FORM)) spmv_sliced<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
     else if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
     else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
     else if constexpr (FORM == 4) spmv_ws<T, VT, XT>(A, av, v, pre, epi, wsm);
@@ -1022,7 +1050,7 @@ __device__ __forceinline__ typename Prec<T>::acc residual_pass(const Mat& A, con
                                                                const typename Prec<T>::xw* x,
                                                                const T* __restrict__ b, double* dsm) {
     if constexpr (FORM == 5) return residual_direct<T, COH>(A, av, x, b);
-    else if constexpr (FORM == 6) return residual_sliced<T, COH>(A, av, x, b);
+    else if constexpr (sliced_form(FORM)) return residual_sliced<T, COH>(A, av, x, b);
     else return residual_staged<T, FORM, COH>(A, av, x, b, dsm);
 }
 

@@ -386,12 +386,13 @@ static void with_form(int form, F&& f) {
         case 3: f(std::integral_constant<int, 3>{}); break;
         case 4: f(std::integral_constant<int, 4>{}); break;
         case 6: f(std::integral_constant<int, 6>{}); break;
+        case 7: f(std::integral_constant<int, 7>{}); break;
         default: f(std::integral_constant<int, 5>{}); break;
     }
 }
 // The persistent iteration kernel runs on the CSR arrays: a sliced layout
 // (whose rows are also short) takes the direct form there.
-static int fused_form(int form) { return form == 6 ? 5 : form; }
+static int fused_form(int form) { return sliced_form(form) ? 5 : form; }
 
 // Compiled form, shared memory and CTAs per system of a layout's kernels.
 // The warp pipeline needs a group capacity (pattern) and 16-byte aligned
@@ -510,7 +511,7 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     m.stages = L.stages;
     m.err = err;
     // kernels on the CSR arrays take the direct form under a sliced layout
-    m.direct = (L.form == 5 || L.form == 6) ? 1 : 0;
+    m.direct = (L.form == 5 || sliced_form(L.form)) ? 1 : 0;
     m.sptr = L.sptr;
     m.sperm = L.sperm;
     m.scol = L.scol;
@@ -767,6 +768,11 @@ static sla_status gather_map(size_t eb, long long m, int batch, const int* map, 
 // rows pad it by 4%.
 static constexpr int SLICE_WINDOWS[3] = {NWARP * 32, 4 * NWARP * 32, 16 * NWARP * 32};
 static constexpr double SLICE_GOOD_PAD = 1.06;
+// Rows of at least this many entries on average take the sliced form for 4
+// resident CTAs per SM (6), shorter ones the one for 5 (7).
+#ifndef SLA_SLICED_MINAVG
+#define SLA_SLICED_MINAVG 12.0
+#endif
 // Largest padding (sliced entries / stored entries) for which the sliced
 // form is used.
 #ifndef SLA_SLICED_MAXPAD
@@ -861,9 +867,13 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     }
     TRY(B.sval.alloc(eb * (size_t)B.vstride * h->batch));
     TRY(sliced_values(h, B, vals, is, eb, s));
+    // the sliced form for 4 resident CTAs per SM (6) for long rows, for 5 (7)
+    // for rows of fewer than 12 entries on average
+    const int form = (double)nnz >= SLA_SLICED_MINAVG * (double)n ? 6 : 7;
     int per = 1;
-    TRY(occupancy(k_spmv_iter<T, 6>, 0, &per));
-    L->form = 6;
+    if (form == 6) TRY(occupancy(k_spmv_iter<T, 6>, 0, &per));
+    else TRY(occupancy(k_spmv_iter<T, 7>, 0, &per));
+    L->form = form;
     L->smem = 0;
     L->sptr = B.sptr.as<int>();
     L->sperm = sorted ? B.perm.as<int>() : nullptr;
@@ -875,16 +885,21 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     return SLA_OK;
 }
 
-// Default choice of the sliced form for the iteration matrix: rows too
-// long for the direct form and long enough on average (measured on B300:
-// the kNN Laplacian, 14.6 entries per row, 192 against 238 us staged; on
-// the 2D and 3D grids, 5 and 7 per row, the direct form is as fast; the
-// SPAI factor of the kNN Laplacian, 7.8 per row, runs faster staged).
-#ifndef SLA_SLICED_MINAVG
-#define SLA_SLICED_MINAVG 12.0
+// Default choice of the sliced form for the iteration matrix (measured on
+// B300 inside the running iteration): rows too long for the direct form and
+// long enough on average (the kNN Laplacian, 14.6 entries per row: 192
+// against 238 us staged), or short rows of at least 6 on average (the 3D
+// 7-point grid: 51.4 against 55.7 us direct, at 5 CTAs per SM); the direct
+// form stays for shorter rows (the 2D 5-point grid: 26.2 against 26.9 us),
+// and the SPAI factors stay staged (the kNN Laplacian's, 7.8 per row, runs
+// faster staged).
+#ifndef SLA_SLICED_MINAVG_SHORT
+#define SLA_SLICED_MINAVG_SHORT 6.0
 #endif
 static bool sliced_by_default(const sla_csr* h, const Layout& L, long long nnz) {
-    return L.maxrow > SLA_DIRECT_MAXROW && (double)nnz >= SLA_SLICED_MINAVG * (double)h->n;
+    const double avg = (double)nnz / (double)h->n;
+    if (L.maxrow > SLA_DIRECT_MAXROW) return avg >= SLA_SLICED_MINAVG;
+    return avg >= SLA_SLICED_MINAVG_SHORT;
 }
 
 static sla_status make_sliced_any(sla_csr* h, const int* d_rp, const int* d_ci, long long nnz, const void* vals,
@@ -1087,7 +1102,7 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
     // external event-record nodes (a plain record inside a capture only
     // orders streams within the graph)
     if (ev0) CU(cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal));
-    const T* avi = h->LI.form == 6 ? (const T*)h->LI.sval : av;
+    const T* avi = sliced_form(h->LI.form) ? (const T*)h->LI.sval : av;
     with_form(h->LI.form, [&](auto f) {
         k_spmv_iter<T, decltype(f)::value><<<gs, NT, h->LI.smem, s>>>(A, S, avi, p, q, x, h->bw.as<T>());
     });
@@ -1098,8 +1113,8 @@ static sla_status enqueue_iteration(sla_csr* h, int pc, double eps, cudaStream_t
         TRY(launched());
         const Mat GT = mat_GT(h);
         const Mat G = mat_G(h);
-        const GV* gtv = h->LGT.form == 6 ? (const GV*)h->LGT.sval : h->gtv.as<GV>();
-        const GV* gvv = h->LG.form == 6 ? (const GV*)h->LG.sval : h->gv.as<GV>();
+        const GV* gtv = sliced_form(h->LGT.form) ? (const GV*)h->LGT.sval : h->gtv.as<GV>();
+        const GV* gvv = sliced_form(h->LG.form) ? (const GV*)h->LG.sval : h->gv.as<GV>();
         with_form(h->LGT.form, [&](auto f) {
         k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, h->LGT.smem, s>>>(GT, S, h->gstride,
                                                                                         gtv, r, h->t.as<W>());
@@ -1413,8 +1428,8 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     if (pc == SLA_PC_SPAI) {
         const Mat GT = mat_GT(h);
         const Mat G = mat_G(h);
-        const GV* gtv = h->LGT.form == 6 ? (const GV*)h->LGT.sval : h->gtv.as<GV>();
-        const GV* gvv = h->LG.form == 6 ? (const GV*)h->LG.sval : h->gv.as<GV>();
+        const GV* gtv = sliced_form(h->LGT.form) ? (const GV*)h->LGT.sval : h->gtv.as<GV>();
+        const GV* gvv = sliced_form(h->LG.form) ? (const GV*)h->LG.sval : h->gv.as<GV>();
         with_form(h->LGT.form, [&](auto f) {
         k_spai_t<T, decltype(f)::value><<<dim3(h->LGT.gx, h->batch), NT, h->LGT.smem, s>>>(GT, S, h->gstride,
                                                                                        gtv, r, h->t.as<W>());
@@ -1815,7 +1830,7 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
         h->vals_aligned = !h->vals_aligned;
         TRY(set_form_any(h, &h->LA, h->vals_aligned, h->es));
         if (!h->reordered) {
-            const bool was_sliced = h->LI.form == 6;
+            const bool was_sliced = sliced_form(h->LI.form);
             h->LI = h->LA;
             if (was_sliced) TRY(make_sliced_any(h, h->irp, h->ici, h->nnz, d_vals, h->nnz, h->es, &h->LI, h->sI, s));
         }
@@ -1823,7 +1838,7 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
     }
     if (h->reordered) TRY(gather_map(h->es, h->nnz, h->batch, h->psrc.as<int>(), d_vals, h->nnz, h->pvals.p, h->nnz, s));
     else h->ivals = d_vals;
-    if (h->LI.form == 6) TRY(sliced_values(h, h->sI, h->ivals, h->nnz, h->es, s));
+    if (sliced_form(h->LI.form)) TRY(sliced_values(h, h->sI, h->ivals, h->nnz, h->es, s));
     TRY(compute_diag(h, s));
     CU(cudaStreamSynchronize(s));
     return SLA_OK;
@@ -1836,7 +1851,7 @@ static sla_status spmv_common(sla_handle h, const void* d_x, void* d_y, double* 
     const Sys S = sys_of(h);
     // the sliced copy of the iteration matrix serves A itself when the
     // handle does not reorder
-    const bool sl = !h->reordered && h->LI.form == 6;
+    const bool sl = !h->reordered && sliced_form(h->LI.form);
     const Layout& L = sl ? h->LI : h->LA;
     const Mat A = sl ? mat_I(h) : mat_A(h);
     const void* vals = sl ? L.sval : h->vals;
