@@ -329,6 +329,21 @@ sla_status sla_spmv_dot_static(int n, long long nnz, int batch, sla_dtype dt, co
  */
 sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream);
 
+/*
+ * Self-test of the bounded device waits; the pages have no counterpart.
+ * Every wait of this library's kernels (on an mbarrier phase, or on the
+ * other CTAs at a grid barrier) gives up after a time limit, records where,
+ * and lets its kernel return, so a wait that never ends cannot hang the GPU;
+ * the call that launched it then returns SLA_ERR_CUDA with the location in
+ * sla_last_error().  This call makes one such wait run out on purpose with
+ * a short limit: which = 0 waits on an mbarrier nothing arrives at, which =
+ * 1 on a two-CTA grid barrier that one CTA never reaches.  0 < limit_s <= 1.
+ * Returns SLA_ERR_CUDA with the wait's message (the expected outcome), or
+ * SLA_OK if the wait ended (never expected); the device stays usable.
+ * Allocates a few bytes of device memory; synchronises `stream`.
+ */
+sla_status sla_wait_selftest(int which, double limit_s, void* stream);
+
 /* Free the handle and everything it owns (not the caller's arrays).  The
  * pages have no counterpart (a resource-release call of this C interface).
  * A NULL handle returns SLA_ERR_INVALID.  Must not run while a call on the

@@ -30,7 +30,7 @@ SLA_SLICED = 256
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
            "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_bicgstab_solve",
-           "sla_bicgstab_adjoint", "sla_fp64_fma_rate"]
+           "sla_bicgstab_adjoint", "sla_fp64_fma_rate", "sla_wait_selftest"]
 
 
 class PcgOpts(C.Structure):
@@ -80,6 +80,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_spmv_dot_static.restype = C.c_int
     lib.sla_fp64_fma_rate.argtypes = [C.POINTER(C.c_double), _vp]
     lib.sla_fp64_fma_rate.restype = C.c_int
+    lib.sla_wait_selftest.argtypes = [C.c_int, C.c_double, _vp]
+    lib.sla_wait_selftest.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
     for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",

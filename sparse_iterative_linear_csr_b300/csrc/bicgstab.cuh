@@ -9,7 +9,8 @@
 // of the stored values, A^ = A D^-1 (D = diag(A)), built once per solve: the
 // iteration runs unpreconditioned on A^ y = b and returns x = D^-1 y, which
 // is the right-preconditioned iteration with p^ = D^-1 p and s^ = D^-1 s
-// folded into the products (the residual b - A x = b - A^ y is the same).
+// folded into the products (the residual b - A x = b - A^ y is the same up
+// to rounding; the stopping test is confirmed on b - A x itself).
 //
 // One iteration is five kernels, captured in a CUDA graph like the CG step:
 //   k_bicg_v:  v = A^ p, sigma = r^.v  (+ the true-residual check) -> alpha
@@ -144,11 +145,47 @@ __global__ void __launch_bounds__(NT) k_bicg_dir(Sys S, const double* __restrict
     if (grid_sum<1>(v, part, cnt, tot, red) && threadIdx.x == 0) bicg_start(st, S.ctl, tot[0]);
 }
 
-// v = A p, sigma = r^.v; with `check` set, ||b - A y||^2 first.
+// x_c = y_c / d_c: the iterate of the column-scaled iteration mapped back,
+// divided exactly as the returned x is (k_bicg_scale).
+struct GatherUnscaled {
+    const double* y;
+    const double* d;
+    __device__ __forceinline__ double operator()(int c) const { return ld_nc(y + c) / ld_nc(d + c); }
+};
+// ||b - A0 x||^2 over this CTA's rows with x = y / d (A0: the unscaled
+// values): the true residual of the x the solve returns.  Out of line for
+// the staged forms, like residual_staged.
+template <int FORM>
+__device__ __noinline__ double residual_unscaled_staged(const Mat& A, const double* __restrict__ a0,
+                                                        const double* y, const double* d,
+                                                        const double* __restrict__ b, double* dsm) {
+    double tr2 = 0.0;
+    spmv_rows<double, double>(A, a0, GatherUnscaled{y, d}, [&](int i) { return b[i]; },
+                              [&](int, double s, double bi) { sq_acc(tr2, resid(bi, s)); }, dsm);
+    return tr2;
+}
+template <int FORM>
+__device__ __forceinline__ double residual_unscaled(const Mat& A, const double* __restrict__ a0, const double* y,
+                                                    const double* d, const double* __restrict__ b, double* dsm) {
+    if constexpr (FORM == 5) {
+        double tr2 = 0.0;
+        spmv_direct<double, double>(A, a0, GatherUnscaled{y, d}, [&](int i) { return b[i]; },
+                                    [&](int, double s, double bi) { sq_acc(tr2, resid(bi, s)); });
+        return tr2;
+    } else {
+        return residual_unscaled_staged<FORM>(A, a0, y, d, b, dsm);
+    }
+}
+
+// v = A p, sigma = r^.v; with `check` set, the true residual first:
+// ||b - A y||^2, or with right Jacobi (dsc != nullptr, the iteration on the
+// column-scaled A D^-1) ||b - A0 x||^2 of the x = y / d the solve returns,
+// on the unscaled values a0, so the stopping test holds for that x.
 template <int FORM>
 __global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     k_bicg_v(Mat A, Sys S, const double* __restrict__ av, const double* __restrict__ p, double* __restrict__ v,
-             const double* __restrict__ rh, const double* __restrict__ y, const double* __restrict__ b) {
+             const double* __restrict__ rh, const double* __restrict__ y, const double* __restrict__ b,
+             const double* __restrict__ a0, const double* __restrict__ dsc) {
     SYS_PROLOGUE
     if (ld_cg(&st->done)) return;
     extern __shared__ __align__(16) double dsm[];
@@ -156,7 +193,10 @@ __global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     av += ao; p += vo; v += vo; rh += vo; y += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
     double tr2 = 0.0, sigma = 0.0;
-    if (check) tr2 = residual_pass<double, FORM>(A, av, y, b, dsm);
+    if (check) {
+        if (dsc) tr2 = residual_unscaled<FORM>(A, a0 + ao, y, dsc + vo, b, dsm);
+        else tr2 = residual_pass<double, FORM>(A, av, y, b, dsm);
+    }
     spmv_vec<double, FORM, double, double>(A, av, p, [&](int i) { return ld_vec(rh + i); },
                                            [&](int i, double s, double rhi) {
                                                st_vec(v + i, s);

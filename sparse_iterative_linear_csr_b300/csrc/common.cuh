@@ -291,12 +291,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Wait for phase `parity` of `bar` to complete; gives up (returns false)
 // after about WAIT_LIMIT_NS, so a copy that never lands cannot hang the GPU.
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity) {
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (unsigned k = 1; k < (1u << 30); ++k) {
         if (mbar_test(bar, parity)) return true;
-        if ((k & 255u) == 0 && global_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if ((k & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

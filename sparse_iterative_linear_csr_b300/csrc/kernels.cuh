@@ -1319,7 +1319,7 @@ struct GridSync {
 
 // Thread 0 of every CTA of a system: arrive and wait for the others.
 // Returns false (and records ERR_WAIT) after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool grid_arrive_wait(GridSync* g, int* err) {
+__device__ __forceinline__ bool grid_arrive_wait(GridSync* g, int* err, unsigned long long limit_ns = WAIT_LIMIT_NS) {
     volatile unsigned* vgen = &g->gen;
     const unsigned gen = *vgen;   // read before arriving: the last arrival advances it
     __threadfence();
@@ -1337,7 +1337,7 @@ __device__ __forceinline__ bool grid_arrive_wait(GridSync* g, int* err) {
             return true;
         }
         if (k > 32) __nanosleep(64);
-        if ((k & 63u) == 63u && global_ns() - t0 > WAIT_LIMIT_NS) break;
+        if ((k & 63u) == 63u && global_ns() - t0 > limit_ns) break;
     }
     atomicOr(err, ERR_GRID);
     note_wait(err + 2, 1 + (int)blockIdx.x, (int)gen, (int)arrived, (int)*((volatile unsigned*)&g->count));
@@ -1669,6 +1669,32 @@ __global__ void __launch_bounds__(NT) k_grad_A(Mat A, Sys S, const T* __restrict
             for (int k = rlo + sub; k < rhi; k += A.lanes) __stcs(dA + k, neg_prod(li, ld_nc(x + ld_stream(A.ci + k))));
         }
     }
+}
+
+// ----------------------------------------------------------------- self-test of the bounded waits
+// Makes one of the library's device waits run out on purpose, with a short
+// limit: which = 0, an mbarrier phase that never completes (nothing
+// arrives); which = 1, a grid barrier of two CTAs that only CTA 0 reaches
+// (CTA 1 returns at once).  The wait gives up, records its error bit and
+// location in `c` as the solver's waits do, and the kernel returns, so the
+// context stays usable.
+__global__ void k_wait_selftest(int which, unsigned long long limit_ns, Ctrl* c, GridSync* gs) {
+    if (which == 0) {
+        if (blockIdx.x != 0) return;
+        __shared__ unsigned long long bar;
+        if (threadIdx.x == 0) {
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+            if (!mbar_wait(&bar, 0, limit_ns)) {
+                atomicOr(&c->err, ERR_WAIT);
+                note_wait(c->diag, -1 - (int)blockIdx.x, 0, 1, 0);
+            }
+            mbar_inval(&bar);   // no arrival or copy is pending
+        }
+        return;
+    }
+    if (blockIdx.x != 0) return;   // never reaches the barrier
+    if (threadIdx.x == 0) grid_arrive_wait(gs, &c->err, limit_ns);
 }
 
 }  // namespace sla

@@ -196,8 +196,13 @@ struct sla_csr {
     int diag_err = 0;  // ERR_NO_DIAG | ERR_DIAG_SIGN
     DevBuf diag, dinv;
 
-    // SPAI factor (built on first use, per values)
+    // SPAI factor (patterns and layouts built on first use; values again
+    // after every sla_csr_update_values)
     bool spai_ready = false;
+    bool spai_stale = false;   // values of G, G^T older than the values of A
+    // reordered handles: the factors on the caller's ordering and the source
+    // entry of every permuted entry
+    DevBuf grp0, gci0, gv0, gtrp0, gtci0, gtv0, gsrc, gtsrc;
     long long nnzg = 0;
     long long gstride = 0;  // per-system stride of the G values (nnzg rounded up to even: 16-byte aligned)
     Layout LG, LGT;    // ... of G and G^T
@@ -955,45 +960,22 @@ static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
     return SLA_OK;
 }
 
-static void release_spai(sla_csr* h) {
-    h->spai_ready = false;
-    h->grp.release(); h->gci.release(); h->gv.release();
-    h->gtrp.release(); h->gtci.release(); h->gtv.release();
-    h->sG.release(); h->sGT.release();
-    h->t.release();
-    for (auto& g : h->graph) g.reset();
-}
 
 static sla_status ensure_pstride(sla_csr* h);
 
-static sla_status build_spai(sla_csr* h, cudaStream_t s) {
+// Values of G and G^T from the current values of A (on the caller's
+// ordering, where G is defined), then -- unless fill_only -- for a reordered
+// handle gathered into the permuted factors, and into their sliced copies.
+// The patterns, permutation maps and layouts were built once by build_spai
+// (which calls this with fill_only before the maps exist).
+static sla_status spai_values(sla_csr* h, cudaStream_t s, bool fill_only = false) {
     if (h->diag_err & ERR_NO_DIAG) return fail(SLA_ERR_INVALID, "SPAI needs every diagonal entry stored");
     if (h->diag_err & ERR_DIAG_SIGN) return fail(SLA_ERR_INVALID, "SPAI needs a positive diagonal");
     const int n = h->n;
-    TRY(h->grp.alloc(sizeof(int) * (size_t)(n + 1)));
-    TRY(h->gtrp.alloc(sizeof(int) * (size_t)(n + 1)));
     const int g = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
-    k_tri_count<<<g, 256, 0, s>>>(n, h->rp, h->ci, h->grp.as<int>(), h->gtrp.as<int>());
-    TRY(launched());
-    CU(cudaMemsetAsync(h->grp.as<int>() + n, 0, sizeof(int), s));
-    CU(cudaMemsetAsync(h->gtrp.as<int>() + n, 0, sizeof(int), s));
-    TRY(scan_exclusive(h->grp.as<int>(), n + 1, s));
-    TRY(scan_exclusive(h->gtrp.as<int>(), n + 1, s));
-    int ng = 0, ngt = 0;
-    TRY(read_int(h->grp.as<int>() + n, &ng, s));
-    TRY(read_int(h->gtrp.as<int>() + n, &ngt, s));
-    if (ng != ngt) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
-    h->nnzg = ng;
-    h->gstride = ((long long)ng + 1) & ~1LL;
-    TRY(h->gci.alloc(sizeof(int) * (size_t)ng));
-    TRY(h->gtci.alloc(sizeof(int) * (size_t)ng));
-    TRY(h->gv.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
-    TRY(h->gtv.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
     DevBuf err;
     TRY(err.alloc(sizeof(int)));
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
-    // G is defined on the caller's ordering (tril of A); with a reordered
-    // handle it is built there and then permuted like A.
     DevBuf dorig;
     const double* dbase = h->diag.as<double>();
     if (h->reordered) {
@@ -1001,51 +983,101 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
         TRY(gather_map(8, n, h->batch, h->iperm.as<int>(), h->diag.p, n, dorig.p, n, s));
         dbase = dorig.as<double>();
     }
+    // caller-ordered factors: the final ones, or the sources of the permuted ones
+    DevBuf& grp = h->reordered ? h->grp0 : h->grp;
+    DevBuf& gci = h->reordered ? h->gci0 : h->gci;
+    DevBuf& gvb = h->reordered ? h->gv0 : h->gv;
+    DevBuf& gtrp = h->reordered ? h->gtrp0 : h->gtrp;
+    DevBuf& gtci = h->reordered ? h->gtci0 : h->gtci;
+    DevBuf& gtvb = h->reordered ? h->gtv0 : h->gtv;
     for (int sy = 0; sy < h->batch; ++sy) {
         const double* dg = dbase + (size_t)sy * n;
-        double* gv = h->gv.as<double>() + (size_t)sy * h->gstride;     // 8-byte slots: fp64, or a
-        double* gtv = h->gtv.as<double>() + (size_t)sy * h->gstride;   // double-float pair for fp32
+        double* gv = gvb.as<double>() + (size_t)sy * h->gstride;     // 8-byte slots: fp64, or a
+        double* gtv = gtvb.as<double>() + (size_t)sy * h->gstride;   // double-float pair for fp32
         if (h->dt == SLA_F64) {
             const double* av = (const double*)h->vals + (size_t)sy * h->nnz;
-            k_fill_G<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(), gv);
+            k_fill_G<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, grp.as<int>(), gci.as<int>(), gv);
             TRY(launched());
-            k_fill_GT<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(), gtv,
-                                                err.as<int>());
+            k_fill_GT<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, gtrp.as<int>(), gtci.as<int>(), gtv,
+                                                        err.as<int>());
         } else {
             const float* av = (const float*)h->vals + (size_t)sy * h->nnz;
-            k_fill_G<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->grp.as<int>(), h->gci.as<int>(),
+            k_fill_G<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, grp.as<int>(), gci.as<int>(),
                                                       reinterpret_cast<float2*>(gv));
             TRY(launched());
-            k_fill_GT<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, h->gtrp.as<int>(), h->gtci.as<int>(),
-                                                       reinterpret_cast<float2*>(gtv),
-                                               err.as<int>());
+            k_fill_GT<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, gtrp.as<int>(), gtci.as<int>(),
+                                                       reinterpret_cast<float2*>(gtv), err.as<int>());
         }
         TRY(launched());
     }
     int e = 0;
     TRY(read_int(err.as<int>(), &e, s));
     if (e & ERR_ASYM) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
+    if (fill_only) return SLA_OK;
+    if (h->reordered) {
+        TRY(gather_map(8, h->nnzg, h->batch, h->gsrc.as<int>(), h->gv0.p, h->gstride, h->gv.p, h->gstride, s));
+        TRY(gather_map(8, h->nnzg, h->batch, h->gtsrc.as<int>(), h->gtv0.p, h->gstride, h->gtv.p, h->gstride, s));
+    }
+    if (sliced_form(h->LG.form)) TRY(sliced_values(h, h->sG, h->gv.p, h->gstride, 8, s));
+    if (sliced_form(h->LGT.form)) TRY(sliced_values(h, h->sGT, h->gtv.p, h->gstride, 8, s));
+    h->spai_stale = false;
+    return SLA_OK;
+}
+
+// The SPAI factor's patterns (G on tril(A) and its explicit transpose, on
+// the caller's ordering; for a reordered handle also permuted like A, with
+// the source entry of every permuted entry) and layouts, once per handle;
+// then its values.
+static sla_status build_spai(sla_csr* h, cudaStream_t s) {
+    if (h->diag_err & ERR_NO_DIAG) return fail(SLA_ERR_INVALID, "SPAI needs every diagonal entry stored");
+    if (h->diag_err & ERR_DIAG_SIGN) return fail(SLA_ERR_INVALID, "SPAI needs a positive diagonal");
+    const int n = h->n;
+    DevBuf& grp = h->reordered ? h->grp0 : h->grp;
+    DevBuf& gtrp = h->reordered ? h->gtrp0 : h->gtrp;
+    TRY(grp.alloc(sizeof(int) * (size_t)(n + 1)));
+    TRY(gtrp.alloc(sizeof(int) * (size_t)(n + 1)));
+    const int g = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    k_tri_count<<<g, 256, 0, s>>>(n, h->rp, h->ci, grp.as<int>(), gtrp.as<int>());
+    TRY(launched());
+    CU(cudaMemsetAsync(grp.as<int>() + n, 0, sizeof(int), s));
+    CU(cudaMemsetAsync(gtrp.as<int>() + n, 0, sizeof(int), s));
+    TRY(scan_exclusive(grp.as<int>(), n + 1, s));
+    TRY(scan_exclusive(gtrp.as<int>(), n + 1, s));
+    int ng = 0, ngt = 0;
+    TRY(read_int(grp.as<int>() + n, &ng, s));
+    TRY(read_int(gtrp.as<int>() + n, &ngt, s));
+    if (ng != ngt) return fail(SLA_ERR_INVALID, "SPAI needs a structurally symmetric matrix");
+    h->nnzg = ng;
+    h->gstride = ((long long)ng + 1) & ~1LL;
+    DevBuf& gci = h->reordered ? h->gci0 : h->gci;
+    DevBuf& gtci = h->reordered ? h->gtci0 : h->gtci;
+    TRY(gci.alloc(sizeof(int) * (size_t)ng));
+    TRY(gtci.alloc(sizeof(int) * (size_t)ng));
+    TRY(h->gv.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
+    TRY(h->gtv.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
+    if (h->reordered) {
+        TRY(h->gv0.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
+        TRY(h->gtv0.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
+    }
+    TRY(spai_values(h, s, true));   // fills the caller-ordered patterns too
     if (h->reordered) {
         std::vector<int> perm, iperm;
         TRY(to_host(perm, h->perm.as<int>(), (size_t)n));
         iperm.resize(n);
         for (int i = 0; i < n; ++i) iperm[perm[i]] = i;
-        DevBuf* pats[2][3] = {{&h->grp, &h->gci, &h->gv}, {&h->gtrp, &h->gtci, &h->gtv}};
-        for (auto& pt : pats) {
+        DevBuf* pats[2][4] = {{&h->grp0, &h->gci0, &h->grp, &h->gci}, {&h->gtrp0, &h->gtci0, &h->gtrp, &h->gtci}};
+        DevBuf* srcs[2] = {&h->gsrc, &h->gtsrc};
+        for (int f = 0; f < 2; ++f) {
             std::vector<int> rp, ci, rp2, ci2, src;
-            TRY(to_host(rp, pt[0]->as<int>(), (size_t)n + 1));
-            TRY(to_host(ci, pt[1]->as<int>(), (size_t)ng));
+            TRY(to_host(rp, pats[f][0]->as<int>(), (size_t)n + 1));
+            TRY(to_host(ci, pats[f][1]->as<int>(), (size_t)ng));
             permute_pattern(n, rp, ci, perm, iperm, rp2, ci2, src);
-            DevBuf dsrc, vals2;
-            TRY(to_device(dsrc, src));
-            TRY(vals2.alloc(sizeof(double) * (size_t)h->gstride * h->batch));
-            TRY(gather_map(8, ng, h->batch, dsrc.as<int>(), pt[2]->p, h->gstride, vals2.p, h->gstride, s));
-            CU(cudaStreamSynchronize(s));
-            TRY(to_device(*pt[0], rp2));
-            TRY(to_device(*pt[1], ci2));
-            std::swap(pt[2]->p, vals2.p);
-            std::swap(pt[2]->bytes, vals2.bytes);
+            TRY(to_device(*pats[f][2], rp2));
+            TRY(to_device(*pats[f][3], ci2));
+            TRY(to_device(*srcs[f], src));
         }
+        TRY(gather_map(8, ng, h->batch, h->gsrc.as<int>(), h->gv0.p, h->gstride, h->gv.p, h->gstride, s));
+        TRY(gather_map(8, ng, h->batch, h->gtsrc.as<int>(), h->gtv0.p, h->gstride, h->gtv.p, h->gstride, s));
     }
     TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, true, sizeof(double), s,
                       SLA_DIRECT_MAXROW_G));
@@ -1058,6 +1090,7 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     }
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
     h->spai_ready = true;
+    h->spai_stale = false;
     return ensure_pstride(h);
 }
 
@@ -1380,6 +1413,7 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
     if (pc == SLA_PC_JACOBI && (h->diag_err & ERR_NO_DIAG))
         return fail(SLA_ERR_INVALID, "Jacobi needs every diagonal entry stored");
     if (pc == SLA_PC_SPAI && !h->spai_ready) TRY(build_spai(h, s));
+    if (pc == SLA_PC_SPAI && h->spai_stale) TRY(spai_values(h, s));
     TRY(ensure_pstride(h));
     const int k = o->poll_k > 0 ? o->poll_k : 32;
     const double eps = pc == SLA_PC_SPAI ? o->eps : 0.0;
@@ -1524,9 +1558,11 @@ static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
 }
 
 // One BiCGStab iteration on the matrix (M, av): five kernels.
+// a0, dsc: the unscaled values and the diagonal when the iteration runs on
+// the column-scaled values (right Jacobi), else null.
 template <int W>
-static sla_status enqueue_bicg(sla_csr* h, const Mat& M, const Layout& L, const double* av, cudaStream_t s,
-                               int* nodes, cudaEvent_t ev0, cudaEvent_t ev1) {
+static sla_status enqueue_bicg(sla_csr* h, const Mat& M, const Layout& L, const double* av, const double* a0,
+                               const double* dsc, cudaStream_t s, int* nodes, cudaEvent_t ev0, cudaEvent_t ev1) {
     const Sys S = sys_of(h);
     double* y = h->x.as<double>();
     double* r = h->r.as<double>();   // r, and s over it
@@ -1537,7 +1573,7 @@ static sla_status enqueue_bicg(sla_csr* h, const Mat& M, const Layout& L, const 
     const dim3 gs(L.gx, h->batch), gv(gx_vec(h), h->batch);
     if (ev0) CU(cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal));
     with_form_rc(L.form, [&](auto f) {
-        k_bicg_v<decltype(f)::value><<<gs, NT, L.smem, s>>>(M, S, av, p, v, rh, y, h->bw.as<double>());
+        k_bicg_v<decltype(f)::value><<<gs, NT, L.smem, s>>>(M, S, av, p, v, rh, y, h->bw.as<double>(), a0, dsc);
     });
     TRY(launched());
     if (ev1) CU(cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal));
@@ -1591,8 +1627,10 @@ static sla_status bicg_impl(sla_csr* h, bool transposed, const double* b, double
     GraphCache& gc = h->graph[3 + 2 * (transposed ? 1 : 0) + (pc == SLA_PC_JACOBI ? 1 : 0)];
     TRY(capture_graph(h, gc, k, 0.0, h->time_product, [&](cudaStream_t cs, int* nodes, cudaEvent_t e0,
                                                             cudaEvent_t e1) {
-        return pairs_ok(h) ? enqueue_bicg<2>(h, M, L, itv, cs, nodes, e0, e1)
-                           : enqueue_bicg<1>(h, M, L, itv, cs, nodes, e0, e1);
+        const double* a0 = pc == SLA_PC_JACOBI ? uv : nullptr;
+        const double* dsc = pc == SLA_PC_JACOBI ? h->diag.as<double>() : nullptr;
+        return pairs_ok(h) ? enqueue_bicg<2>(h, M, L, itv, a0, dsc, cs, nodes, e0, e1)
+                           : enqueue_bicg<1>(h, M, L, itv, a0, dsc, cs, nodes, e0, e1);
     }));
 
     const dim3 gs(L.gx, h->batch), gv(gx_vec(h), h->batch);
@@ -1824,7 +1862,7 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
     if (!d_vals && h->nnz > 0) return fail(SLA_ERR_INVALID, "null values");
     cudaStream_t s = (cudaStream_t)stream;
     h->vals = d_vals;
-    release_spai(h);     // rebuilt on the next SPAI solve
+    h->spai_stale = true;   // G, G^T values recomputed by the next SPAI solve
     for (auto& g : h->graph) g.reset();
     if (vals_aligned(h, d_vals) != h->vals_aligned) {
         h->vals_aligned = !h->vals_aligned;
@@ -2038,6 +2076,27 @@ sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream) {
     TRY(st);
     if (!(best > 0.0f)) return fail(SLA_ERR_CUDA, "fp64 probe could not be timed");
     *fma_per_s = (double)grid * NT * iters * PROBE_CHAINS / (best * 1e-3);
+    return SLA_OK;
+}
+
+sla_status sla_wait_selftest(int which, double limit_s, void* stream) {
+    if (which != 0 && which != 1) return fail(SLA_ERR_INVALID, "which must be 0 (mbarrier) or 1 (grid barrier)");
+    if (!(limit_s > 0.0) || limit_s > 1.0) return fail(SLA_ERR_INVALID, "limit_s must be in (0, 1]");
+    cudaStream_t s = (cudaStream_t)stream;
+    DevBuf ctl, gs;
+    TRY(ctl.alloc(sizeof(Ctrl)));
+    TRY(gs.alloc(sizeof(GridSync)));
+    CU(cudaMemsetAsync(ctl.p, 0, sizeof(Ctrl), s));
+    CU(cudaMemsetAsync(gs.p, 0, sizeof(GridSync), s));
+    k_wait_selftest<<<2, 32, 0, s>>>(which, (unsigned long long)(limit_s * 1e9), ctl.as<Ctrl>(), gs.as<GridSync>());
+    TRY(launched());
+    Ctrl dc;
+    CU(cudaMemcpyAsync(&dc, ctl.p, sizeof(Ctrl), cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+    if (dc.err & (ERR_WAIT | ERR_GRID))
+        return fail(SLA_ERR_CUDA, "a device wait gave up (%s; at %d: %d %d %d)",
+                    (dc.err & ERR_GRID) ? "grid barrier" : "bulk copy", dc.diag[0], dc.diag[1], dc.diag[2],
+                    dc.diag[3]);
     return SLA_OK;
 }
 

@@ -303,6 +303,33 @@ def test_update_values(cuda_device):
     assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
 
 
+@pytest.mark.parametrize("reorder,sliced", [(False, False), (True, False), (False, True), (True, True)])
+def test_spai_follows_update_values(cuda_device, reorder, sliced):
+    """After a SPAI solve, new values (a symmetric scaling D A D, same
+    pattern) give the SPAI factor of the new matrix: the handle keeps G's
+    pattern, permutation and layout and recomputes only its values (also
+    for a reordered handle and for sliced factors)."""
+    w = build("c5", npoints=6000)
+    A = w.A
+    M = make(A, reorder=reorder, sliced=sliced)
+    assert M.layout()[2] == reorder
+    b = torch.from_numpy(w.b).to(cuda_device)
+    x1, i1 = M.solve(b, tol=1e-10, pc="spai", eps=1e-3)
+    xo1, io1 = oracle.pcg(A, w.b, 1e-10, pc="spai", eps=1e-3)
+    assert _iters_ok(i1[0].iters, io1["iters"]) and rel(x1.cpu().numpy(), xo1) <= 1e-6
+    d = 0.5 + np.random.default_rng(4).random(A.n)
+    v2 = A.vals * d[A.rows()] * d[A.col_idx]
+    A2 = CSR(A.n, A.row_ptr, A.col_idx, v2)
+    M.update_values(torch.from_numpy(v2).to(cuda_device))
+    x2, i2 = M.solve(b, tol=1e-10, pc="spai", eps=1e-3)
+    xo2, io2 = oracle.pcg(A2, w.b, 1e-10, pc="spai", eps=1e-3)
+    assert i2[0].status == "ok" and _iters_ok(i2[0].iters, io2["iters"])
+    assert rel(x2.cpu().numpy(), xo2) <= 1e-6
+    lam, dA, ai = M.adjoint(x2, torch.from_numpy(w.g).to(cuda_device), tol=1e-10, pc="spai", eps=1e-3)
+    lo, dAo, ao = oracle.adjoint(A2, x2.cpu().numpy(), w.g, 1e-10, pc="spai", eps=1e-3)
+    assert _iters_ok(ai[0].iters, ao["iters"]) and rel(lam.cpu().numpy(), lo) <= 1e-6
+
+
 @FUSED
 def test_launch_count_advances(cuda_device, fused):
     """Kernel-per-step solves launch three kernels per iteration; the
@@ -440,3 +467,24 @@ def test_scattered_pattern_is_reordered(cuda_device):
     x3, i3 = M.solve(bt, tol=1e-9, pc="jacobi", max_iter=20000)
     xo3, io3 = oracle.pcg(A3, b, 1e-9, pc="jacobi", max_iter=20000)
     assert _iters_ok(i3[0].iters, io3["iters"]) and rel(x3.cpu().numpy(), xo3) <= 1e-6
+
+
+@pytest.mark.parametrize("which,what", [(0, b"bulk copy"), (1, b"grid barrier")])
+def test_device_wait_gives_up_and_reports(cuda_device, which, what):
+    """A device wait that never ends (an mbarrier nothing arrives at; a grid
+    barrier one CTA never reaches) gives up after its limit (5 ms here),
+    records where, and lets the kernel return: the call returns
+    SLA_ERR_CUDA with the location, and the device stays usable."""
+    import ctypes as C
+    from sparse_iterative_linear_csr_b300 import _lib
+    lib = _lib.load()
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.sla_wait_selftest(which, 0.005, stream) == _lib.SLA_ERR_CUDA
+    msg = lib.sla_last_error()
+    assert b"gave up" in msg and what in msg, msg
+    assert lib.sla_wait_selftest(2, 0.005, stream) == _lib.SLA_ERR_INVALID
+    w = build("c1", N=16)
+    M = make(w.A)
+    x, info = M.solve(torch.from_numpy(w.b).to(cuda_device), tol=1e-10)
+    xo, _ = oracle.pcg(w.A, w.b, 1e-10)
+    assert info[0].status == "ok" and rel(x.cpu().numpy(), xo) <= 1e-6
