@@ -330,6 +330,62 @@ sla_status sla_spmv_dot_static(int n, long long nnz, int batch, sla_dtype dt, co
 sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream);
 
 /*
+ * Dense steps of the block eigensolver (torch-sla §3, .eigsh; here LOBPCG,
+ * Knyazev, SIAM J. Sci. Comput. 23(2), 2001: Rayleigh-Ritz over a basis of
+ * blocks, kept orthonormal).  A block of k vectors of length n is stored
+ * vector after vector (device double [k][n]); small matrices are row-major.
+ *
+ * sla_block_gram: G = A B^T, G[i][j] = A_i . B_j, for blocks A [ka][n] and
+ * B [kb][n] (1 <= ka, kb <= 64), into d_G (device double [ka][kb]).
+ * mode 0: every entry; mode 1 (B = A, ka = kb; d_B may be NULL): only
+ * i <= j, mirrored; mode 2 (B = A): only the diagonal, the squared norms of
+ * A's vectors, into d_G[0..ka).  Sums are fp64, split over CTAs and added in
+ * a fixed order (deterministic).  d_work: caller-owned device scratch of at
+ * least the number of doubles sla_block_gram_work returns for the same
+ * (ka, kb, mode, n).  Two kernels; does not synchronise.  SLA_ERR_INVALID
+ * for sizes out of range, an unknown mode, null pointers or too small a
+ * workspace.
+ */
+sla_status sla_block_gram_work(int ka, int kb, int mode, long long n, long long* doubles);
+sla_status sla_block_gram(int ka, int kb, long long n, const double* d_A, const double* d_B, int mode, double* d_G,
+                          double* d_work, long long work_doubles, void* stream);
+
+/*
+ * sla_block_update: Y[r] = sum_i C[i][r] S[i] (+ Yin[r]) for r < kc, i.e.
+ * Y = C^T S (+ Yin): the block S [ks][n] times the small matrix C (device
+ * double [ks][kc]), 1 <= ks, kc <= 64; d_Yin may be NULL or equal d_Y (an
+ * in-place update); d_Y must not overlap d_S.  fp64, one kernel; does not
+ * synchronise.
+ */
+sla_status sla_block_update(int ks, int kc, long long n, const double* d_C, const double* d_S, const double* d_Yin,
+                            double* d_Y, void* stream);
+
+/*
+ * dL/dA_k = -lambda_row(k) x_col(k) for every stored entry k of the handle's
+ * matrix (the matrix-gradient step of sla_adjoint, torch-sla §3.3 adjoint
+ * paragraph, on its own): d_lam, d_x [batch][n], d_dLdA [batch][nnz], the
+ * handle's dtype.  Used by the row-partitioned solve, where lambda and x come
+ * from a partitioned solve and x carries the halo.  Synchronises `stream`.
+ */
+sla_status sla_grad_A(sla_handle h, const void* d_lam, const void* d_x, void* d_dLdA, void* stream);
+
+/*
+ * Local steps of the row-partitioned CG (torch-sla §3.3, distributed CG:
+ * each rank updates its owned entries, and the inner products are all-reduced
+ * over the ranks by the caller).  fp64, device pointers, n owned entries.
+ * sla_cg_local_update: x += alpha p, r -= alpha q, z = dinv * r (z = r when
+ * d_dinv is NULL), and d_dots (device double[2]) = this rank's r.r and r.z
+ * (summed in a fixed order: deterministic); d_work: caller-owned scratch of
+ * at least sla_cg_local_work(n) doubles.  sla_cg_local_direction:
+ * p = z + beta p.  Neither synchronises.
+ */
+sla_status sla_cg_local_work(int n, long long* doubles);
+sla_status sla_cg_local_update(int n, double alpha, const double* d_p, const double* d_q, const double* d_dinv,
+                               double* d_x, double* d_r, double* d_z, double* d_dots, double* d_work,
+                               long long work_doubles, void* stream);
+sla_status sla_cg_local_direction(int n, double beta, const double* d_z, double* d_p, void* stream);
+
+/*
  * Self-test of the bounded device waits; the pages have no counterpart.
  * Every wait of this library's kernels (on an mbarrier phase, or on the
  * other CTAs at a grid barrier) gives up after a time limit, records where,

@@ -30,7 +30,8 @@ SLA_SLICED = 256
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
            "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_bicgstab_solve",
-           "sla_bicgstab_adjoint", "sla_fp64_fma_rate", "sla_wait_selftest"]
+           "sla_bicgstab_adjoint", "sla_fp64_fma_rate", "sla_wait_selftest", "sla_block_gram_work", "sla_block_gram",
+           "sla_block_update", "sla_grad_A", "sla_cg_local_work", "sla_cg_local_update", "sla_cg_local_direction"]
 
 
 class PcgOpts(C.Structure):
@@ -82,6 +83,20 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_fp64_fma_rate.restype = C.c_int
     lib.sla_wait_selftest.argtypes = [C.c_int, C.c_double, _vp]
     lib.sla_wait_selftest.restype = C.c_int
+    lib.sla_block_gram_work.argtypes = [C.c_int, C.c_int, C.c_int, C.c_longlong, C.POINTER(C.c_longlong)]
+    lib.sla_block_gram_work.restype = C.c_int
+    lib.sla_block_gram.argtypes = [C.c_int, C.c_int, C.c_longlong, _vp, _vp, C.c_int, _vp, _vp, C.c_longlong, _vp]
+    lib.sla_block_gram.restype = C.c_int
+    lib.sla_block_update.argtypes = [C.c_int, C.c_int, C.c_longlong, _vp, _vp, _vp, _vp, _vp]
+    lib.sla_block_update.restype = C.c_int
+    lib.sla_grad_A.argtypes = [_vp, _vp, _vp, _vp, _vp]
+    lib.sla_grad_A.restype = C.c_int
+    lib.sla_cg_local_work.argtypes = [C.c_int, C.POINTER(C.c_longlong)]
+    lib.sla_cg_local_work.restype = C.c_int
+    lib.sla_cg_local_update.argtypes = [C.c_int, C.c_double, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, C.c_longlong, _vp]
+    lib.sla_cg_local_update.restype = C.c_int
+    lib.sla_cg_local_direction.argtypes = [C.c_int, C.c_double, _vp, _vp, _vp]
+    lib.sla_cg_local_direction.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
     for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",

@@ -121,11 +121,41 @@ __device__ __forceinline__ DF afma(DF a, DF b, DF c) { return df_add(df_mul(a, b
 __device__ __forceinline__ double aneg(double a) { return -a; }
 __device__ __forceinline__ DF aneg(DF a) { return df_neg(a); }
 
+// Sums of products of fp32 systems are accumulated compensated (the Dot2
+// scheme of Ogita, Rump and Oishi, "Accurate sum and dot product", 2005):
+// the pair holds a running fp32 sum and a running fp32 sum of its rounding
+// errors (each exact by two-sum) and of the products' low parts, and is
+// normalised (acc_norm) once, when the sum is complete -- about 10 fp32
+// operations per term instead of a full double-float addition, with an
+// accuracy close to that of a sum carried in twice fp32's precision.
+__device__ __forceinline__ void acc_push(DF& s, DF p) {
+    const DF t = two_sum(s.hi, p.hi);
+    s.hi = t.hi;
+    s.lo = __fadd_rn(s.lo, __fadd_rn(t.lo, p.lo));
+}
+__device__ __forceinline__ void acc_norm(double&) {}
+__device__ __forceinline__ void acc_norm(DF& s) { s = two_sum(s.hi, s.lo); }
+// a * b for double-float a, b: the high parts' product exact, the cross
+// terms rounded into its low part (not normalised)
+__device__ __forceinline__ DF dprod(DF a, DF b) {
+    DF p = two_prod(a.hi, b.hi);
+    p.lo = __fmaf_rn(a.hi, b.lo, p.lo);
+    p.lo = __fmaf_rn(a.lo, b.hi, p.lo);
+    return p;
+}
+// s += a * b into an accumulator
+__device__ __forceinline__ void acc_fma(double& s, double a, double b) { s = fma(a, b, s); }
+__device__ __forceinline__ void acc_fma(DF& s, DF a, DF b) { acc_push(s, dprod(a, b)); }
+
 // acc += a * v
 __device__ __forceinline__ void mac(double& s, double a, double v) { s = fma(a, v, s); }
-__device__ __forceinline__ void mac(DF& s, float a, float v) { s = df_fma_ff(a, v, s); }
-__device__ __forceinline__ void mac(DF& s, float a, float2 v) { s = df_fma_df(DF{v.x, v.y}, a, s); }
-__device__ __forceinline__ void mac(DF& s, float2 g, float2 v) { s = df_add(s, df_mul(DF{g.x, g.y}, DF{v.x, v.y})); }
+__device__ __forceinline__ void mac(DF& s, float a, float v) { acc_push(s, two_prod(a, v)); }
+__device__ __forceinline__ void mac(DF& s, float a, float2 v) {
+    DF p = two_prod(a, v.x);
+    p.lo = __fmaf_rn(a, v.y, p.lo);
+    acc_push(s, p);
+}
+__device__ __forceinline__ void mac(DF& s, float2 g, float2 v) { acc_push(s, dprod(DF{g.x, g.y}, DF{v.x, v.y})); }
 
 // stored value nearest to an accumulator
 __device__ __forceinline__ double to_store(double s) { return s; }
@@ -207,6 +237,7 @@ __device__ __forceinline__ typename Prec<T>::acc unstaged_row(const Mat& A, cons
     acc_t s = Prec<T>::zero();
     if (rhi - rlo <= LONG_ROW)
         for (int k = rlo + sub; k < rhi; k += A.lanes) mac(s, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+    acc_norm(s);
     unsigned longs = __ballot_sync(0xffffffffu, rhi - rlo > LONG_ROW && sub == 0);
     while (longs) {
         const int src = __ffs(longs) - 1;
@@ -215,6 +246,7 @@ __device__ __forceinline__ typename Prec<T>::acc unstaged_row(const Mat& A, cons
         const int a1 = __shfl_sync(0xffffffffu, rhi, src);
         acc_t t = Prec<T>::zero();
         for (int k = a0 + lane; k < a1; k += 32) mac(t, ld_stream(av + k), gather(ld_stream(A.ci + k)));
+        acc_norm(t);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc_add(t, acc_xor(t, o));
         if (lane == src) s = t;
@@ -240,6 +272,7 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
         const auto carried = pre(row);
         acc_t s = Prec<T>::zero();
         for (int k = lo; k < hi; ++k) mac(s, ld_mat(av + k), gather(ld_mat(A.ci + k)));
+        acc_norm(s);
         epi(row, s, carried);
     }
 }
@@ -296,6 +329,7 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
             for (int u = 0; u < SLICE_U; ++u) mac(s, a[u], gather(cc[u]));
         }
         for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
+        acc_norm(s);
 #else
         // the last batch loads its missing entries again from the slice's
         // last entry (an L1 hit) and drops them, so no entry is summed alone
@@ -318,6 +352,7 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
 #endif
             }
         }
+        acc_norm(s);
 #endif
         if (live) epi(row, s, carried);
     }
@@ -386,6 +421,7 @@ __device__ __forceinline__ void spmv_rows(const Mat& A, const VT* __restrict__ a
         } else {
             s = unstaged_row<T>(A, av, gather, rlo, rhi);
         }
+        acc_norm(s);
         segment_sum(s, A.lanes);
         if (own) epi(row, s, carried);
     }
@@ -505,6 +541,7 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
             if (bufs == 2 && !early) issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
             s = unstaged_row<T>(A, av, GatherVec<XT, COH>{v}, rlo, rhi);
         }
+        acc_norm(s);
         segment_sum(s, A.lanes);
         __syncwarp();  // buffers free for reuse
         if (bufs == 1) issue_vc(grp + nwarps, 0, nk0, nk1);
@@ -680,6 +717,7 @@ __device__ __forceinline__ void spmv_pipe(const Mat& A, const VT* __restrict__ a
             const int lo = rlo - k0, hi = rhi - k0;
             if (lo >= 0 && hi <= hd->cnt[st])   // inside the staged range (always, unless ERR_STAGE)
                 for (int e = lo; e < hi; ++e) mac(s, cv[e], cx[e]);
+            acc_norm(s);
         }
         __syncwarp();   // stage st and gather buffer gb are free
         if (lane == 0 && i + S < m) {
@@ -852,6 +890,7 @@ __device__ __forceinline__ void spmv_ws(const Mat& A, const VT* __restrict__ av,
 #pragma unroll 4
                     for (int e = lo; e < hi; ++e) mac(s, cv[e], cx[e]);
                 }
+                acc_norm(s);
                 epi(row, s, car);
             }
             __syncwarp();
@@ -970,14 +1009,18 @@ __device__ __forceinline__ void start_state(State* s, Ctrl* c, double bb, double
 // ----------------------------------------------------------------- element-wise arithmetic
 // acc += a * b
 __device__ __forceinline__ void dot_acc(double& s, double a, double b) { s = fma(a, b, s); }
-__device__ __forceinline__ void dot_acc(DF& s, float a, float b) { s = df_fma_ff(a, b, s); }
-__device__ __forceinline__ void dot_acc(DF& s, float2 a, float2 b) { s = afma(ld_w(a), ld_w(b), s); }
+__device__ __forceinline__ void dot_acc(DF& s, float a, float b) { acc_push(s, two_prod(a, b)); }
+__device__ __forceinline__ void dot_acc(DF& s, float2 a, float2 b) { acc_push(s, dprod(ld_w(a), ld_w(b))); }
 
 // b - s for a row sum s
 __device__ __forceinline__ double resid(double b, double s) { return b - s; }
 __device__ __forceinline__ DF resid(float b, DF s) { return df_add_f(df_neg(s), b); }
 __device__ __forceinline__ void sq_acc(double& t, double e) { t = fma(e, e, t); }
-__device__ __forceinline__ void sq_acc(DF& t, DF e) { t = df_add(t, df_sqr(e)); }
+__device__ __forceinline__ void sq_acc(DF& t, DF e) {
+    DF p = two_prod(e.hi, e.hi);
+    p.lo = __fmaf_rn(__fmul_rn(2.0f, e.hi), e.lo, p.lo);
+    acc_push(t, p);
+}
 
 // -lambda_i x_j, rounded once
 __device__ __forceinline__ double neg_prod(double l, double x) { return -l * x; }
@@ -1105,11 +1148,11 @@ template <int PC, typename A, typename W, typename XW>
 __device__ __forceinline__ void update_r(A alpha, W& ri, W qi, XW di, W& zi, A& g, A& rz) {
     const A rn = afma(aneg(alpha), ld_w(qi), ld_w(ri));
     ri = to_w(rn);
-    g = afma(rn, rn, g);
+    acc_fma(g, rn, rn);
     if (PC == 1) {
         const A zz = amul(rn, ld_w(di));
         zi = to_w(zz);
-        rz = afma(rn, zz, rz);
+        acc_fma(rz, rn, zz);
     }
 }
 
@@ -1554,7 +1597,7 @@ __global__ void __launch_bounds__(NT, SPMV_MIN_CTAS)
                         const acc_t ri = resid(bi, s);
                         r[i] = to_w(ri);
                         dot_acc(bb, bi, bi);
-                        g = afma(ri, ri, g);
+                        acc_fma(g, ri, ri);
                     },
                     dsm);
     double v[2] = {Prec<T>::total(bb), Prec<T>::total(g)}, tot[2];

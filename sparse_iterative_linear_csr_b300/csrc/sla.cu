@@ -26,6 +26,7 @@
 #include "kernels.cuh"
 #include "bicgstab.cuh"
 #include "setup.cuh"
+#include "block.cuh"
 
 using namespace sla;
 
@@ -2077,6 +2078,110 @@ sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream) {
     if (!(best > 0.0f)) return fail(SLA_ERR_CUDA, "fp64 probe could not be timed");
     *fma_per_s = (double)grid * NT * iters * PROBE_CHAINS / (best * 1e-3);
     return SLA_OK;
+}
+
+// ===================================================================== block arithmetic
+static int gram_grid(long long n) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long chunks = (n + GRAM_COLS - 1) / GRAM_COLS;
+    long long g = 2LL * sms;
+    if (g > chunks) g = chunks;
+    return (int)(g < 1 ? 1 : g);
+}
+
+sla_status sla_block_gram_work(int ka, int kb, int mode, long long n, long long* doubles) {
+    if (!doubles) return fail(SLA_ERR_INVALID, "null output");
+    if (ka < 1 || kb < 1 || ka > GRAM_MAXK || kb > GRAM_MAXK)
+        return fail(SLA_ERR_INVALID, "block sizes must be in [1, %d] (got %d, %d)", GRAM_MAXK, ka, kb);
+    if (mode != GRAM_FULL && mode != GRAM_SYM && mode != GRAM_DIAG)
+        return fail(SLA_ERR_INVALID, "unknown mode %d", mode);
+    if (mode != GRAM_FULL && ka != kb) return fail(SLA_ERR_INVALID, "this mode needs ka == kb");
+    if (n < 0) return fail(SLA_ERR_INVALID, "n must be >= 0");
+    *doubles = (long long)gram_grid(n > 0 ? n : 1) * gram_pairs(ka, kb, mode);
+    return SLA_OK;
+}
+
+sla_status sla_block_gram(int ka, int kb, long long n, const double* d_A, const double* d_B, int mode, double* d_G,
+                          double* d_work, long long work_doubles, void* stream) {
+    long long need = 0;
+    TRY(sla_block_gram_work(ka, kb, mode, n, &need));
+    if (!d_A || !d_G || (mode == GRAM_FULL && !d_B) || !d_work) return fail(SLA_ERR_INVALID, "null pointer");
+    if (work_doubles < need) return fail(SLA_ERR_INVALID, "workspace too small (%lld < %lld doubles)", work_doubles, need);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (n == 0) {
+        CU(cudaMemsetAsync(d_G, 0, sizeof(double) * (size_t)(mode == GRAM_DIAG ? ka : ka * kb), s));
+        return SLA_OK;
+    }
+    const int grid = gram_grid(n);
+    k_gram_partial<<<grid, NT, 0, s>>>(ka, kb, n, d_A, mode == GRAM_FULL ? d_B : d_A, mode, d_work);
+    TRY(launched());
+    const int npairs = gram_pairs(ka, kb, mode);
+    k_gram_reduce<<<(npairs + NT - 1) / NT, NT, 0, s>>>(ka, kb, mode, grid, d_work, d_G);
+    return launched();
+}
+
+sla_status sla_block_update(int ks, int kc, long long n, const double* d_C, const double* d_S, const double* d_Yin,
+                            double* d_Y, void* stream) {
+    if (ks < 1 || kc < 1 || ks > GRAM_MAXK || kc > GRAM_MAXK)
+        return fail(SLA_ERR_INVALID, "block sizes must be in [1, %d] (got %d, %d)", GRAM_MAXK, ks, kc);
+    if (n < 0) return fail(SLA_ERR_INVALID, "n must be >= 0");
+    if (!d_C || !d_S || !d_Y) return fail(SLA_ERR_INVALID, "null pointer");
+    if (n == 0) return SLA_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0, sms = 148;
+    CU(cudaGetDevice(&dev));
+    CU(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    long long g = (n + NT - 1) / NT;
+    if (g > 8LL * sms) g = 8LL * sms;
+    k_block_update<<<(unsigned)g, NT, 0, s>>>(ks, kc, n, d_C, d_S, d_Yin, d_Y);
+    return launched();
+}
+
+// ===================================================================== partitioned CG steps
+static int local_grid(long long n) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long g = (n + NT - 1) / NT;
+    if (g > 2LL * sms) g = 2LL * sms;
+    return (int)(g < 1 ? 1 : g);
+}
+
+sla_status sla_cg_local_work(int n, long long* doubles) {
+    if (!doubles) return fail(SLA_ERR_INVALID, "null output");
+    if (n < 0) return fail(SLA_ERR_INVALID, "n must be >= 0");
+    *doubles = 2LL * local_grid(n);
+    return SLA_OK;
+}
+
+sla_status sla_cg_local_update(int n, double alpha, const double* d_p, const double* d_q, const double* d_dinv,
+                               double* d_x, double* d_r, double* d_z, double* d_dots, double* d_work,
+                               long long work_doubles, void* stream) {
+    long long need = 0;
+    TRY(sla_cg_local_work(n, &need));
+    if ((n > 0 && (!d_p || !d_q || !d_x || !d_r || !d_z)) || !d_dots || !d_work)
+        return fail(SLA_ERR_INVALID, "null pointer");
+    if (work_doubles < need) return fail(SLA_ERR_INVALID, "workspace too small (%lld < %lld doubles)", work_doubles, need);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int g = local_grid(n);
+    k_cg_local_update<<<g, NT, 0, s>>>(n, alpha, d_p, d_q, d_dinv, d_x, d_r, d_z, d_work);
+    TRY(launched());
+    k_pair_reduce<<<1, 32, 0, s>>>(g, d_work, d_dots);
+    return launched();
+}
+
+sla_status sla_cg_local_direction(int n, double beta, const double* d_z, double* d_p, void* stream) {
+    if (n < 0) return fail(SLA_ERR_INVALID, "n must be >= 0");
+    if (n > 0 && (!d_z || !d_p)) return fail(SLA_ERR_INVALID, "null pointer");
+    if (n == 0) return SLA_OK;
+    k_cg_local_direction<<<local_grid(n), NT, 0, (cudaStream_t)stream>>>(n, beta, d_z, d_p);
+    return launched();
+}
+
+sla_status sla_grad_A(sla_handle h, const void* d_lam, const void* d_x, void* d_dLdA, void* stream) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (!d_lam || !d_x || (!d_dLdA && h->nnz > 0)) return fail(SLA_ERR_INVALID, "null vector");
+    return grad_A(h, d_x, d_lam, d_dLdA, (cudaStream_t)stream);
 }
 
 sla_status sla_wait_selftest(int which, double limit_s, void* stream) {

@@ -20,11 +20,14 @@ amplifies rounding noise).  The block converges when each of its first k
 relative residuals is at most tol.
 
 Where the work runs: the block products A W go through the library's
-product kernels (sla_spmm); the tall-skinny products of the block with small
-matrices are plain GEMMs (torch), and the tiny Gram eigenproblems are solved
-on the host.  The gradient of eigenvalue j with respect to the stored
-entries is v_j[row] v_j[col] (first-order perturbation of a simple
-eigenvalue with unit eigenvector v_j).
+product kernels (sla_spmm); every product of a tall block with another
+block or with a small matrix -- the Gram matrices, the Rayleigh-Ritz matrix,
+Gram-Schmidt, the residual norms and the block updates -- through the
+library's block kernels (sla_block_gram, sla_block_update, fp64); the tiny
+Gram eigenproblems are solved on the host (one small copy each).  The
+gradient of eigenvalue j with respect to the stored entries is
+v_j[row] v_j[col] (first-order perturbation of a simple eigenvalue with
+unit eigenvector v_j).
 """
 from __future__ import annotations
 
@@ -36,7 +39,57 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
+import ctypes as C
+
 from . import CSRMatrix, _check, _lib_handle, _ptr, _stream
+
+GRAM_FULL, GRAM_SYM, GRAM_DIAG = 0, 1, 2
+
+
+def gram(A: torch.Tensor, B: torch.Tensor | None = None, mode: int | None = None) -> torch.Tensor:
+    """A B^T for blocks A [ka, n], B [kb, n] (fp64, CUDA) on the library:
+    mode GRAM_FULL (default with B), GRAM_SYM (B = A, the default without B)
+    or GRAM_DIAG (B = A: the squared norms of A's vectors, a [ka] vector)."""
+    if mode is None:
+        mode = GRAM_SYM if B is None else GRAM_FULL
+    A = A.contiguous()
+    ka, n = A.shape
+    kb = ka if B is None else B.shape[0]
+    shape = (ka,) if mode == GRAM_DIAG else (ka, kb)
+    if ka == 0 or kb == 0:
+        return torch.zeros(shape, dtype=torch.float64, device=A.device)
+    Bc = None if B is None else B.contiguous()
+    lib = _lib_handle()
+    need = C.c_longlong(0)
+    _check(lib.sla_block_gram_work(ka, kb, mode, n, C.byref(need)))
+    work = torch.empty(max(int(need.value), 1), dtype=torch.float64, device=A.device)
+    G = torch.empty(shape, dtype=torch.float64, device=A.device)
+    _check(lib.sla_block_gram(ka, kb, n, _ptr(A), None if Bc is None else _ptr(Bc), mode, _ptr(G), _ptr(work),
+                              int(need.value), _stream()))
+    return G
+
+
+def update(Cm: torch.Tensor, S: torch.Tensor, Yin: torch.Tensor | None = None,
+           out: torch.Tensor | None = None) -> torch.Tensor:
+    """C^T S (+ Yin) on the library: Y[r] = sum_i C[i, r] S[i] (+ Yin[r]) for
+    a block S [ks, n] and a small matrix C [ks, kc] (fp64, CUDA).  `out` may be
+    Yin (in place) but not S."""
+    ks, kc = Cm.shape
+    n = S.shape[1]
+    Y = out if out is not None else torch.empty((kc, n), dtype=torch.float64, device=S.device)
+    if kc == 0:
+        return Y
+    if ks == 0:
+        if Yin is None:
+            Y.zero_()
+        elif Yin.data_ptr() != Y.data_ptr():
+            Y.copy_(Yin)
+        return Y
+    Cd = Cm.to(device=S.device, dtype=torch.float64).contiguous()
+    S = S.contiguous()
+    _check(_lib_handle().sla_block_update(ks, kc, n, _ptr(Cd), _ptr(S), None if Yin is None else _ptr(Yin),
+                                          _ptr(Y), _stream()))
+    return Y
 
 
 def spmm(M: CSRMatrix, X: torch.Tensor, stream=None) -> torch.Tensor:
@@ -71,20 +124,25 @@ def _svqb(G: np.ndarray, eps: float) -> np.ndarray:
     return (V[:, keep] / np.sqrt(s[keep])).T / d[None, :]
 
 
-def _orth_against(B, AB, Qs):
+def _orth_against(B, AB, Qs, same=False):
     """B (and A B) minus their components along the orthonormal blocks
-    (Q, AQ) of Qs, twice (classical Gram-Schmidt with re-orthogonalisation)."""
+    (Q, AQ) of Qs, twice (classical Gram-Schmidt with re-orthogonalisation).
+    same: AB is B (only B is updated)."""
+    B = B.contiguous().clone()
+    AB = B if same else AB.contiguous().clone()
     for _ in range(2):
         for Q, AQ in Qs:
-            Cq = B @ Q.T
-            B = B - Cq @ Q
-            AB = AB - Cq @ AQ
+            Cq = gram(B, Q)                       # [kb, kq]
+            update(-Cq.T, Q, B, out=B)            # B -= Cq Q
+            if not same:
+                update(-Cq.T, AQ, AB, out=AB)     # AB -= Cq AQ
     return B, AB
 
 
-def _orthonormal(B, AB, eps):
-    T = torch.from_numpy(_svqb((B @ B.T).cpu().numpy(), eps)).to(B.device)
-    return T @ B, T @ AB
+def _orthonormal(B, AB, eps, same=False):
+    T = torch.from_numpy(_svqb(gram(B).cpu().numpy(), eps)).to(B.device)
+    Bn = update(T.T, B)
+    return Bn, (Bn if same else update(T.T, AB))
 
 
 def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_iter: int = 2000,
@@ -94,6 +152,8 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
     if not 1 <= k <= n:
         raise ValueError("need 1 <= k <= n")
     m = min(n, block or k + max(2, k // 2))
+    if 3 * m > 64:
+        raise ValueError("block too large: the Rayleigh-Ritz basis (3 x block) must be at most 64 vectors")
     dev, dt = M.values.device, torch.float64
     if M.dtype != torch.float64:
         raise ValueError("eigsh works on fp64 matrices")
@@ -117,19 +177,25 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
     else:
         g = torch.Generator(device="cpu").manual_seed(seed)
         X = torch.randn(m, n, generator=g, dtype=dt).to(dev)
-    T = torch.from_numpy(_svqb((X @ X.T).cpu().numpy(), eps)).to(dev)
-    X = T @ X
+    T = torch.from_numpy(_svqb(gram(X).cpu().numpy(), eps)).to(dev)
+    X = update(T.T, X)
     AX = Amul(X)
-    theta, C_ = np.linalg.eigh(((X @ AX.T).cpu().numpy() + (AX @ X.T).cpu().numpy()) / 2)
+    H0 = gram(X, AX).cpu().numpy()
+    theta, C_ = np.linalg.eigh((H0 + H0.T) / 2)
     Cd = torch.from_numpy(C_).to(dev)
-    X, AX = Cd.T @ X, Cd.T @ AX
+    X, AX = update(Cd, X), update(Cd, AX)
     theta = torch.from_numpy(theta).to(dev)
     P = AP = None
     it = 0
     res = None
+
+    def residual(X, AX, theta):
+        # R = AX - X diag(theta), and ||R_j|| / |theta_j|
+        R = update(-torch.diag(theta), X, AX)
+        return R, torch.sqrt(gram(R, mode=GRAM_DIAG)) / torch.clamp(theta.abs(), min=1e-300)
+
     for it in range(1, max_iter + 1):
-        R = AX - theta[:, None] * X
-        res = torch.linalg.norm(R, dim=1) / torch.clamp(theta.abs(), min=1e-300)
+        R, res = residual(X, AX, theta)
         if bool((res[:k] <= tol).all()):
             it -= 1
             break
@@ -137,8 +203,8 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
         W = R[active]
         if precondition:
             W = W * dinv[None, :]
-        W, _ = _orth_against(W, W, [(X, X)])
-        W, _ = _orthonormal(W, W, eps)
+        W, _ = _orth_against(W, W, [(X, X)], same=True)
+        W, _ = _orthonormal(W, W, eps, same=True)
         AW = Amul(W) if W.shape[0] else W
         blocks = [(X, AX), (W, AW)]
         if P is not None:
@@ -149,18 +215,15 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
                 blocks.append((P, AP))
         S = torch.cat([b for b, _ in blocks])
         AS = torch.cat([ab for _, ab in blocks])
-        H = (S @ AS.T).cpu().numpy()
+        H = gram(S, AS).cpu().numpy()
         th, Cn = np.linalg.eigh((H + H.T) / 2)
         Cn = torch.from_numpy(Cn[:, :m]).to(dev)
         # new directions: the update without its component in the old block
-        # (rows 0..m-1 of the basis are the old X)
-        Pc = Cn.clone()
-        Pc[:m] = 0.0
-        P, AP = Pc.T @ S, Pc.T @ AS
-        X, AX = Cn.T @ S, Cn.T @ AS
+        # (rows 0..m-1 of the basis are the old X); then X = C_top^T X + P
+        P, AP = update(Cn[m:], S[m:]), update(Cn[m:], AS[m:])
+        X, AX = update(Cn[:m], S[:m], P), update(Cn[:m], AS[:m], AP)
         theta = torch.from_numpy(th[:m]).to(dev)
-    R = AX - theta[:, None] * X
-    res = torch.linalg.norm(R, dim=1) / torch.clamp(theta.abs(), min=1e-300)
+    R, res = residual(X, AX, theta)
     info = EigInfo(it, bool((res[:k] <= tol).all()), [float(r) for r in res[:k]])
     return sign * theta[:k], X[:k], info
 
