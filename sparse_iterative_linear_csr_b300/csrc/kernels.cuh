@@ -1300,7 +1300,7 @@ __global__ void __launch_bounds__(NT) k_pupdate(Sys S, typename Prec<T>::w* __re
 // SPAI, first product: t = G^T r (explicit transposed CSR of G; G values
 // are per system, [batch][nnz(G)]).
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, (FORM >= 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_t(Mat GT, Sys S, long long nnzg,
+__global__ void __launch_bounds__(NT, (FORM >= 5 ? ProductCtas<T, FORM>::value : SPMV_MIN_CTAS)) k_spai_t(Mat GT, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gtv,
                                                               const typename Prec<T>::w* __restrict__ r,
                                                               typename Prec<T>::w* __restrict__ t) {
@@ -1316,7 +1316,7 @@ __global__ void __launch_bounds__(NT, (FORM >= 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CT
 
 // SPAI, second product: z = G t + eps r, rho' = r.z -> beta (or rho at set-up).
 template <typename T, int FORM>
-__global__ void __launch_bounds__(NT, (FORM >= 5 ? SLA_DIRECT_CTAS : SPMV_MIN_CTAS)) k_spai_z(Mat G, Sys S, long long nnzg,
+__global__ void __launch_bounds__(NT, (FORM >= 5 ? ProductCtas<T, FORM>::value : SPMV_MIN_CTAS)) k_spai_z(Mat G, Sys S, long long nnzg,
                                                               const typename Prec<T>::gv* __restrict__ gv,
                                                               const typename Prec<T>::w* __restrict__ t,
                                                               const typename Prec<T>::w* __restrict__ r,
