@@ -299,7 +299,13 @@ constexpr int SLICE_U = SLA_SLICE_U;
 #define SLA_SLICE_TAIL 0
 #endif
 
-template <typename T, typename VT, class Gather, class Pre, class Epi>
+// Batch of the short-row sliced form (7): measured on the 3D 7-point
+// product inside the running iteration, 7 (49.6 us) beat 2, 4, 6 and 8
+// (50.0, 51.3, 51.7, 50.8 us).
+#ifndef SLA_SLICE_U_SHORT
+#define SLA_SLICE_U_SHORT 7
+#endif
+template <typename T, typename VT, int U = SLICE_U, class Gather, class Pre, class Epi>
 __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__ sv, Gather gather, Pre pre,
                                             Epi epi) {
     using acc_t = typename Prec<T>::acc;
@@ -317,33 +323,33 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
         const int* c = A.scol + base + lane;
 #if SLA_SLICE_TAIL == 0
         int j = 0;
-        for (; j + SLICE_U <= w; j += SLICE_U) {
-            VT a[SLICE_U];
-            int cc[SLICE_U];
+        for (; j + U <= w; j += U) {
+            VT a[U];
+            int cc[U];
 #pragma unroll
-            for (int u = 0; u < SLICE_U; ++u) {
+            for (int u = 0; u < U; ++u) {
                 a[u] = ld_mat(v + (j + u) * 32);
                 cc[u] = ld_mat(c + (j + u) * 32);
             }
 #pragma unroll
-            for (int u = 0; u < SLICE_U; ++u) mac(s, a[u], gather(cc[u]));
+            for (int u = 0; u < U; ++u) mac(s, a[u], gather(cc[u]));
         }
         for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
         acc_norm(s);
 #else
         // the last batch loads its missing entries again from the slice's
         // last entry (an L1 hit) and drops them, so no entry is summed alone
-        for (int j = 0; j < w; j += SLICE_U) {
-            VT a[SLICE_U];
-            int cc[SLICE_U];
+        for (int j = 0; j < w; j += U) {
+            VT a[U];
+            int cc[U];
 #pragma unroll
-            for (int u = 0; u < SLICE_U; ++u) {
+            for (int u = 0; u < U; ++u) {
                 const int k = min(j + u, w - 1);
                 a[u] = ld_mat(v + k * 32);
                 cc[u] = ld_mat(c + k * 32);
             }
 #pragma unroll
-            for (int u = 0; u < SLICE_U; ++u) {
+            for (int u = 0; u < U; ++u) {
 #if SLA_SLICE_TAIL == 1
                 mac(s, j + u < w ? a[u] : VT{}, gather(cc[u]));
 #else
@@ -926,7 +932,8 @@ template <typename T, int FORM, typename VT, typename XT, bool COH = false, clas
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
     if constexpr (FORM == 5) spmv_direct<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
-    else if constexpr (sliced_form(FORM)) spmv_sliced<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
+    else if constexpr (sliced_form(FORM))
+        spmv_sliced<T, VT, (FORM == 7 ? SLA_SLICE_U_SHORT : SLICE_U)>(A, av, GatherVec<XT, COH>{v}, pre, epi);
     else if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
     else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
     else if constexpr (FORM == 4) spmv_ws<T, VT, XT>(A, av, v, pre, epi, wsm);

@@ -253,6 +253,9 @@ static constexpr int MAX_CAP = 864;  // staging capacity limit (larger groups ta
 #ifndef SLA_MIN_LANES_G
 #define SLA_MIN_LANES_G SLA_MIN_LANES   // the same for the SPAI factors
 #endif
+#ifndef SLA_MAX_CAP_G
+#define SLA_MAX_CAP_G 864   // staging capacity limit for the SPAI factors (larger groups go unstaged)
+#endif
 static int staging_form(int cap) {
     const size_t per_sm = 228 * 1024;
     if ((size_t)NWARP * async_smem_per_warp<double, double>(cap, 2) * SLA_STAGE_CTAS <= per_sm) return 2;
@@ -584,7 +587,7 @@ static constexpr int NEAR_WINDOW = 65536;
 
 static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, long long nnz, Layout* L,
                                 bool aligned, size_t vb, cudaStream_t s, int direct_maxrow = SLA_DIRECT_MAXROW,
-                                int min_lanes = SLA_MIN_LANES) {
+                                int min_lanes = SLA_MIN_LANES, int max_cap = MAX_CAP) {
     {
         DevBuf far;
         TRY(far.alloc(sizeof(unsigned long long)));
@@ -603,8 +606,8 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
         TRY(group_max(rp, h->n, 32 / lanes, &m, s));
         int cap = (m + 31) / 32 * 32;
         if (cap < 32) cap = 32;
-        if (cap <= MAX_CAP || lanes == 4) {
-            L->cap = cap > MAX_CAP ? MAX_CAP : cap;
+        if (cap <= max_cap || lanes == 4) {
+            L->cap = cap > max_cap ? max_cap : cap;
             L->lanes = lanes;
             break;
         }
@@ -1085,9 +1088,9 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
         TRY(gather_map(8, ng, h->batch, h->gtsrc.as<int>(), h->gtv0.p, h->gstride, h->gtv.p, h->gstride, s));
     }
     TRY(choose_layout(h, h->grp.as<int>(), h->gci.as<int>(), ng, &h->LG, true, sizeof(double), s,
-                      SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G));
+                      SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G, SLA_MAX_CAP_G));
     TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s,
-                      SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G));
+                      SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G, SLA_MAX_CAP_G));
     if (h->sliced) {   // only when asked: staged G and G^T measured faster (kNN Laplacian)
         TRY(make_sliced_any(h, h->grp.as<int>(), h->gci.as<int>(), ng, h->gv.p, h->gstride, 8, &h->LG, h->sG, s));
         TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
