@@ -290,6 +290,16 @@ def cpu_sample(w, calls=3):
     return oracle_summary(w, res, cpu, "bounded sample")
 
 
+def layouts_of(M, pc):
+    """Product form, CTAs per system and split group sums of the iteration
+    matrix and, under SPAI, of G and G^T (as the handle chose them)."""
+    out = {}
+    for which in (("A", "G", "GT") if pc == "spai" else ("A",)):
+        f, g, sp = M.layout_of(which)
+        out[which] = {"form": f, "ctas": g, "split": sp}
+    return out
+
+
 def config_of(name, w, poll_k, bm):
     """The `config` object, the same for both arms."""
     method = method_of(w)
@@ -502,6 +512,7 @@ def measure(args, name, dev, world, rank, stream, lib, with_cpu, e2e_steps, fma_
         "roofline": roof, "gpu_launches": int(launches), "clocks": clocks,
         "wall_s_timed": t_wall, "kernel_src": src, "product_form": M.layout()[0],
         "product_ctas_per_system": M.layout()[1], "metric": metric_of(w),
+        "layouts": layouts_of(M, w.pc),
     }
     if w.dtype == "f32":
         # the working vectors are 8-byte double-float slots; the same
@@ -631,7 +642,7 @@ def main():
             "e2e": m.get("e2e"), "gpu_launches": m["gpu_launches"], "clocks": m["clocks"],
             "cpu_baseline": m["cpu_baseline"], "wall_s_timed": m["wall_s_timed"], "kernel_src": m["kernel_src"],
             "product_form": m["product_form"], "product_ctas_per_system": m["product_ctas_per_system"],
-            "fp64_fma_rate_per_s": fma_rate,
+            "layouts": m["layouts"], "fp64_fma_rate_per_s": fma_rate,
         }
         if secondary:
             line["secondary"] = secondary

@@ -85,6 +85,10 @@ typedef enum {
 #define SLA_STAGED 128u      /* never use the direct product form (see sla_csr_layout) */
 #define SLA_SLICED 256u      /* use the sliced product form wherever it pads little, also for the
                                 SPAI factors (see sla_csr_layout) */
+#define SLA_SPLIT_ROWS 512u  /* staged forms 1 and 2 with one lane per row: always sum a group with
+                                its entries split evenly over the lanes (see sla_csr_layout) */
+#define SLA_ROW_WALK 1024u   /* never split a group's entries: every lane sums its own row
+                                (takes precedence over SLA_SPLIT_ROWS) */
 
 typedef struct {
     double tol;        /* stop when ||r||_2 <= tol ||b||_2 and the true residual of
@@ -164,12 +168,31 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         Costs (8 + value size) bytes per sliced entry of device memory,
  *         and the values are copied again by sla_csr_update_values.
  *         The SPAI factors G and G^T take their forms by the same rule;
- *         the BiCGStab products always take a staged form (0, 1 or 2);
+ *         the BiCGStab products always take a staged form (0, 1 or 2).
+ *         In forms 1 and 2 with one lane per row a warp sums its group of
+ *         32 rows either lane by lane (each lane its own row: as many
+ *         warp-wide fp64 steps as the group's longest row) or split (the
+ *         group's entries cut into 32 even runs, one per lane, the pieces of
+ *         cut rows joined by shuffles in lane order).  The split is taken
+ *         when the lane-per-row walk would cost at least 1.8 times as many
+ *         warp-wide fp64 steps over the whole matrix (groups holding a few
+ *         rows far longer than the rest), always with SLA_SPLIT_ROWS, never
+ *         with SLA_ROW_WALK;
  *  *ctas: CTAs per system of the product kernels;
  *  *reordered: 1 when the solves iterate on P A P^T.
  * Any pointer may be NULL.  SLA_ERR_INVALID for a null handle.
  */
 sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered);
+
+/*
+ * The same report for one matrix of the solves (no counterpart in the
+ * pages): which = 0 the iteration matrix, 1 the SPAI factor G, 2 its
+ * transpose G^T (built by the handle's first SPAI solve; SLA_ERR_INVALID
+ * before that).  *split: 1 when its staged groups are summed split (see
+ * sla_csr_layout).  Any output pointer may be NULL.  SLA_ERR_INVALID for a
+ * null handle or another `which`.
+ */
+sla_status sla_csr_layout_of(sla_handle h, int which, int* form, int* ctas, int* split);
 
 /*
  * Measurement hook; the pages have no counterpart.

@@ -91,12 +91,14 @@ class CSRMatrix:
     where the direct (thread-per-row) form would be the default;
     sliced=True uses the sliced product form (a handle-owned copy of the
     iteration matrix and of the SPAI factors in 32-row slices) where it
-    applies."""
+    applies; split=True / False forces / forbids summing the staged groups
+    with their entries split evenly over the lanes (default: chosen per
+    matrix from its row lengths)."""
 
     def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor,
                  validate: bool = True, pipeline: bool = False, fused: bool = False,
                  time_product: bool = False, producer_consumer: bool = False, reorder: bool | None = None,
-                 staged: bool = False, sliced: bool = False, stream=None):
+                 staged: bool = False, sliced: bool = False, split: bool | None = None, stream=None):
         lib = _lib_handle()
         for t, name in ((row_ptr, "row_ptr"), (col_idx, "col_idx"), (values, "values")):
             if not t.is_cuda:
@@ -124,6 +126,7 @@ class CSRMatrix:
                                   (_lib.SLA_PRODUCER_CONSUMER if producer_consumer else 0) |
                                   (_lib.SLA_STAGED if staged else 0) |
                                   (_lib.SLA_SLICED if sliced else 0) |
+                                  ({None: 0, True: _lib.SLA_SPLIT_ROWS, False: _lib.SLA_ROW_WALK}[split]) |
                                   ({None: 0, True: _lib.SLA_REORDER, False: _lib.SLA_NO_REORDER}[reorder]),
                                   _stream(stream),
                                   C.byref(self._h)))
@@ -178,6 +181,14 @@ class CSRMatrix:
         f, g, r = C.c_int(), C.c_int(), C.c_int()
         _check(_lib_handle().sla_csr_layout(self._h, C.byref(f), C.byref(g), C.byref(r)))
         return f.value, g.value, bool(r.value)
+
+    def layout_of(self, which: str = "A") -> tuple[int, int, bool]:
+        """(product form, CTAs per system, split group sums) of the iteration
+        matrix ("A") or, after a SPAI solve, of the factor "G" or "GT"."""
+        f, g, b = C.c_int(), C.c_int(), C.c_int()
+        _check(_lib_handle().sla_csr_layout_of(self._h, {"A": 0, "G": 1, "GT": 2}[which], C.byref(f), C.byref(g),
+                                               C.byref(b)))
+        return f.value, g.value, bool(b.value)
 
     def update_values(self, values: torch.Tensor, stream=None):
         if values.dtype != self.dtype or values.numel() != self.batch * self.nnz or not values.is_cuda:

@@ -25,11 +25,13 @@ SLA_REORDER = 32
 SLA_NO_REORDER = 64
 SLA_STAGED = 128
 SLA_SLICED = 256
+SLA_SPLIT_ROWS = 512
+SLA_ROW_WALK = 1024
 
 # every function the header declares
 EXPORTS = ["sla_pcg_opts_default", "sla_csr_create", "sla_csr_update_values", "sla_spmv", "sla_spmv_dot",
            "sla_pcg_solve", "sla_adjoint", "sla_csr_destroy", "sla_last_error", "sla_launch_count",
-           "sla_spmv_dot_static", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_bicgstab_solve",
+           "sla_spmv_dot_static", "sla_csr_layout", "sla_csr_layout_of", "sla_product_time", "sla_spmm", "sla_bicgstab_solve",
            "sla_bicgstab_adjoint", "sla_fp64_fma_rate", "sla_wait_selftest", "sla_block_gram_work", "sla_block_gram",
            "sla_block_update", "sla_grad_A", "sla_cg_local_work", "sla_cg_local_update", "sla_cg_local_direction"]
 
@@ -63,6 +65,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                    C.POINTER(_vp)]
     lib.sla_csr_update_values.argtypes = [_vp, _vp, _vp]
     lib.sla_csr_layout.argtypes = [_vp, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_int)]
+    lib.sla_csr_layout_of.argtypes = [_vp, C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_int)]
     lib.sla_product_time.argtypes = [_vp, C.POINTER(C.c_double), C.POINTER(C.c_longlong), C.c_int]
     lib.sla_spmv.argtypes = [_vp, _vp, _vp, _vp]
     lib.sla_spmm.argtypes = [_vp, _vp, _vp, C.c_int, _vp]
@@ -99,7 +102,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.sla_cg_local_direction.restype = C.c_int
     lib.sla_launch_count.argtypes = []
     lib.sla_launch_count.restype = C.c_ulonglong
-    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_product_time", "sla_spmm", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
+    for f in ["sla_csr_create", "sla_csr_update_values", "sla_csr_layout", "sla_csr_layout_of", "sla_product_time", "sla_spmm", "sla_spmv", "sla_spmv_dot", "sla_pcg_solve",
               "sla_adjoint", "sla_bicgstab_solve", "sla_bicgstab_adjoint", "sla_csr_destroy"]:
         getattr(lib, f).restype = C.c_int
     _lib = lib

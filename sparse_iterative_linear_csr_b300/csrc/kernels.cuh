@@ -64,6 +64,8 @@ struct Mat {
     int stages;       // warp pipeline: ring stages
     int* err;         // device error bits (Ctrl::err; Ctrl::diag follows at err + 2)
     int direct;       // 1: the layout's kernels run the direct form (no shared-memory staging)
+    int bal;          // 1: staged groups (one lane per row, cp.async forms) are summed with the
+                      //    entries split evenly over the lanes (balanced_group_sum)
     // Sliced form (FORM 6): the rows in slices of 32, each slice stored
     // column by column (entry j of the slice's 32 rows side by side), padded
     // to the slice's longest row.
@@ -191,6 +193,10 @@ __device__ __forceinline__ double acc_xor(double t, int o) { return __shfl_xor_s
 __device__ __forceinline__ DF acc_xor(DF t, int o) {
     return DF{__shfl_xor_sync(0xffffffffu, t.hi, o), __shfl_xor_sync(0xffffffffu, t.lo, o)};
 }
+__device__ __forceinline__ double acc_from(double t, int src) { return __shfl_sync(0xffffffffu, t, src); }
+__device__ __forceinline__ DF acc_from(DF t, int src) {
+    return DF{__shfl_sync(0xffffffffu, t.hi, src), __shfl_sync(0xffffffffu, t.lo, src)};
+}
 __device__ __forceinline__ void acc_add(double& a, double b) { a += b; }
 __device__ __forceinline__ void acc_add(DF& a, DF b) { a = df_add(a, b); }
 
@@ -295,9 +301,6 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
 #define SLA_SLICE_U 4
 #endif
 constexpr int SLICE_U = SLA_SLICE_U;
-#ifndef SLA_SLICE_TAIL
-#define SLA_SLICE_TAIL 0
-#endif
 
 // Batch of the short-row sliced form (7): measured on the 3D 7-point
 // product inside the running iteration, 7 (49.6 us) beat 2, 4, 6 and 8
@@ -321,7 +324,6 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
         acc_t s = Prec<T>::zero();
         const VT* v = sv + base + lane;
         const int* c = A.scol + base + lane;
-#if SLA_SLICE_TAIL == 0
         int j = 0;
         for (; j + U <= w; j += U) {
             VT a[U];
@@ -336,30 +338,6 @@ __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__
         }
         for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
         acc_norm(s);
-#else
-        // the last batch loads its missing entries again from the slice's
-        // last entry (an L1 hit) and drops them, so no entry is summed alone
-        for (int j = 0; j < w; j += U) {
-            VT a[U];
-            int cc[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = min(j + u, w - 1);
-                a[u] = ld_mat(v + k * 32);
-                cc[u] = ld_mat(c + k * 32);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-#if SLA_SLICE_TAIL == 1
-                mac(s, j + u < w ? a[u] : VT{}, gather(cc[u]));
-#else
-                const auto xv = gather(cc[u]);
-                if (j + u < w) mac(s, a[u], xv);
-#endif
-            }
-        }
-        acc_norm(s);
-#endif
         if (live) epi(row, s, carried);
     }
 }
@@ -457,6 +435,70 @@ __host__ __device__ constexpr size_t async_smem_per_warp(int cap, int bufs) {
     return (size_t)bufs * cap * (sizeof(VT) + sizeof(int)) + (size_t)cap * sizeof(T);
 }
 
+// Balanced sum of a staged group of 32 rows (one lane per row; Mat::bal).
+// A lane-per-row walk costs the warp as many fp64 steps as the group's
+// longest row, because a warp-wide fp64 instruction holds the fp64 pipe for
+// the whole warp however many lanes are active.  Here the group's cnt
+// staged entries are cut into 32 runs of C = ceil(cnt / 32) entries
+// (rounded up to odd, so that the lanes' shared-memory reads fall in
+// distinct banks), run l summed by lane l: the warp's fp64 steps are C plus
+// the rounds that join the pieces of rows cut by run boundaries.  A piece
+// that begins a row is left in the staged vector slot of the row's first
+// entry (already consumed by the lane that wrote it); a lane's first piece,
+// when it continues a row begun in an earlier run, is its carry, passed to
+// the row's lane by shuffles.  A row's sum is its first piece plus the
+// carries of the lanes whose runs start inside it, in lane order: a fixed
+// order, so the result is reproducible.
+// rend: 32 ints of scratch (the group's staged column indices, whose
+// gathers have all been issued); lo, hi: this lane's row relative to the
+// group's first entry.
+template <typename T, typename VT, typename XT>
+__device__ __forceinline__ typename Prec<T>::acc balanced_group_sum(const VT* __restrict__ cv, XT* sx, int* rend,
+                                                                   int cnt, int lo, int hi) {
+    using acc_t = typename Prec<T>::acc;
+    const int lane = threadIdx.x & 31;
+    rend[lane] = hi;
+    __syncwarp();
+    const int C = ((cnt + 31) >> 5) | 1;
+    int e = lane * C;
+    const int e1 = min(e + C, cnt);
+    acc_t s = Prec<T>::zero(), carry = Prec<T>::zero();
+    if (e < e1) {
+        int i = 0;   // row holding entry e: the number of rows that end at or before e
+#pragma unroll
+        for (int st = 16; st >= 1; st >>= 1)
+            if (rend[i + st - 1] <= e) i += st;
+        bool cont = e > (i > 0 ? rend[i - 1] : 0);   // the run starts inside row i
+        int head = e;                                // first entry of the current piece
+        int end = rend[i];
+        for (; e < e1; ++e) {
+            if (e == end) {
+                acc_norm(s);
+                if (cont) carry = s;
+                else sx[head] = to_w(s);
+                s = Prec<T>::zero();
+                cont = false;
+                head = e;
+                do end = rend[++i]; while (end == e);   // past empty rows
+            }
+            mac(s, cv[e], sx[e]);
+        }
+        acc_norm(s);
+        if (cont) carry = s;
+        else sx[head] = to_w(s);
+    }
+    __syncwarp();
+    acc_t tot = hi > lo ? acc_t(ld_w(sx[lo])) : Prec<T>::zero();
+    const int first = lo / C + 1;   // first lane whose run starts inside this row
+    const int joins = hi > lo ? (hi - 1) / C - lo / C : 0;
+    const int rounds = __reduce_max_sync(0xffffffffu, joins);
+    for (int k = 0; k < rounds; ++k) {
+        const acc_t t = acc_from(carry, min(first + k, 31));
+        if (k < joins) acc_add(tot, t);
+    }
+    return tot;
+}
+
 template <typename T, typename VT, typename XT, bool GASYNC, bool COH, class Pre, class Epi>
 __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restrict__ av, const XT* __restrict__ v,
                                                 Pre pre, Epi epi, double* wsm) {
@@ -542,7 +584,13 @@ __device__ __forceinline__ void spmv_rows_async(const Mat& A, const VT* __restri
             }
             __syncwarp();
             const VT* cv = sv + b * cap;
-            for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, cv[e], sx[e]);
+            // the balanced sum keeps a row's first piece in a staged vector slot
+            constexpr bool slot_fits = std::is_same<XT, decltype(to_w(acc_t{}))>::value;
+            if (slot_fits && A.bal) {
+                if constexpr (slot_fits) s = balanced_group_sum<T>(cv, sx, sc + b * cap, cnt, rlo - k0, rhi - k0);
+            } else {
+                for (int e = rlo - k0 + sub; e < rhi - k0; e += A.lanes) mac(s, cv[e], sx[e]);
+            }
         } else {
             if (bufs == 2 && !early) issue_vc(grp + nwarps, b ^ 1, nk0, nk1);
             s = unstaged_row<T>(A, av, GatherVec<XT, COH>{v}, rlo, rhi);

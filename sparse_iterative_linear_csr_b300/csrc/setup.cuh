@@ -95,6 +95,37 @@ __global__ void k_group_max(const int* __restrict__ rp, int n, int R, int* out) 
     if (m) atomicMax(out, m);
 }
 
+// Warp-wide fp64 steps of the two ways a staged warp can sum a group of 32
+// rows (one lane per row), summed over the groups:
+//   out[0]: a lane per row -- the group's longest row;
+//   out[1]: the entries split evenly, C = ceil(cnt / 32) rounded up to odd
+//           per lane, plus the shuffle-add rounds that join the pieces of
+//           split rows (the most pieces any row of the group has past its
+//           first).
+// (balanced_group_sum in kernels.cuh is the second way.)
+__global__ void k_walk_cost(const int* __restrict__ rp, int n, unsigned long long* out) {
+    const long long ng = ((long long)n + 31) / 32;
+    unsigned long long row_walk = 0, split_walk = 0;
+    for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < ng; g += (long long)gridDim.x * blockDim.x) {
+        const long long r0 = g * 32;
+        const long long r1 = r0 + 32 < n ? r0 + 32 : n;
+        const int k0 = rp[r0];
+        const int cnt = rp[r1] - k0;
+        if (cnt == 0) continue;
+        const int C = ((cnt + 31) >> 5) | 1;
+        int longest = 0, joins = 0;
+        for (long long r = r0; r < r1; ++r) {
+            const int lo = rp[r] - k0, hi = rp[r + 1] - k0;
+            longest = max(longest, hi - lo);
+            if (hi > lo) joins = max(joins, (hi - 1) / C - lo / C);
+        }
+        row_walk += longest;
+        split_walk += C + joins;
+    }
+    if (row_walk) atomicAdd(out, row_walk);
+    if (split_walk) atomicAdd(out + 1, split_walk);
+}
+
 // Largest staged range of a run of R consecutive rows (a warp-pipeline group
 // or a producer/consumer tile), the range's ends rounded out to multiples of
 // 4 entries as the bulk copies move it.

@@ -136,6 +136,7 @@ struct Layout {
     int form = 0;     // compiled form of the product kernels (spmv_vec)
     size_t smem = 0;  // their dynamic shared memory
     int maxrow = 0;   // longest row
+    int bal = 0;      // staged groups summed split over the lanes (forms 1 and 2, one lane per row)
     // sliced copy (form 6), owned by the handle's SellBufs
     const int* sptr = nullptr;
     const int* sperm = nullptr;
@@ -223,6 +224,7 @@ struct sla_csr {
 
     // sliced copies (form 6) of the iteration matrix and of G, G^T
     bool sliced = false;        // SLA_SLICED: sliced product form where it applies
+    int split = 0;              // SLA_SPLIT_ROWS: 1, SLA_ROW_WALK: -1, else chosen per matrix
     SellBufs sI, sG, sGT;
 
     // BiCGStab (built on first use): the iteration matrix's layout with the
@@ -516,6 +518,7 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     // doubles of shared memory per warp (L.smem / NWARP)
     m.wstride = (int)(L.smem / NWARP / sizeof(double));
     m.lanes = L.form == 3 ? 1 : L.lanes;
+    m.bal = L.bal && m.lanes == 1 && (L.form == 1 || L.form == 2) ? 1 : 0;
     m.lshift = m.lanes == 4 ? 2 : (m.lanes == 2 ? 1 : 0);
     if (L.form == 3) m.cap = L.ccap;   // every group stages in the register-staged passes too
     m.nnz = nnz;
@@ -585,6 +588,39 @@ static sla_status group_max(const int* rp, int n, int rows, int* out, cudaStream
 // columns from their row (a 512 KB window of an fp64 vector).
 static constexpr int NEAR_WINDOW = 65536;
 
+// Split sums of the staged groups (balanced_group_sum) when the lane-per-row
+// walk would take at least SLA_SPLIT_RATIO times the warp-wide fp64 steps
+// (k_walk_cost), one lane per row only.  Measured on B300 (product of 4M
+// rows, staged form 1): at ratios 1.36 and 1.54 the split product took 2-3%
+// longer (its serial chain per group -- row search, unrollable walk, joins
+// -- is longer, and the fp64 pipe is not what bounds these products), at
+// 2.0 2.5% less, at 2.7, 3.3 and 4.4 22%, 26% and 60% less (groups with a
+// few long rows).  The SPAI factors of the reordered kNN Laplacian (about
+// 1.3) keep the lane-per-row walk.
+#ifndef SLA_SPLIT_RATIO
+#define SLA_SPLIT_RATIO 1.8
+#endif
+static sla_status choose_split(const sla_csr* h, const int* rp, Layout* L, cudaStream_t s) {
+    L->bal = 0;
+    if (L->lanes != 1 || h->split < 0) return SLA_OK;
+    if (h->split > 0) {
+        L->bal = 1;
+        return SLA_OK;
+    }
+    DevBuf w;
+    TRY(w.alloc(2 * sizeof(unsigned long long)));
+    CU(cudaMemsetAsync(w.p, 0, 2 * sizeof(unsigned long long), s));
+    const long long ng = ((long long)h->n + 31) / 32;
+    const int g = (ng + 255) / 256 < 2048 ? (int)((ng + 255) / 256) : 2048;
+    k_walk_cost<<<g, 256, 0, s>>>(rp, h->n, w.as<unsigned long long>());
+    TRY(launched());
+    unsigned long long c[2] = {0, 0};
+    CU(cudaMemcpyAsync(c, w.p, sizeof c, cudaMemcpyDeviceToHost, s));
+    CU(cudaStreamSynchronize(s));
+    L->bal = c[1] > 0 && (double)c[0] >= SLA_SPLIT_RATIO * (double)c[1] ? 1 : 0;
+    return SLA_OK;
+}
+
 static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, long long nnz, Layout* L,
                                 bool aligned, size_t vb, cudaStream_t s, int direct_maxrow = SLA_DIRECT_MAXROW,
                                 int min_lanes = SLA_MIN_LANES, int max_cap = MAX_CAP) {
@@ -612,6 +648,7 @@ static sla_status choose_layout(const sla_csr* h, const int* rp, const int* ci, 
             break;
         }
     }
+    TRY(choose_split(h, rp, L, s));
     // warp pipeline: largest group of 32 rows, as staged
     L->ccap = 0;
     if (aligned16(rp) && aligned16(ci)) {
@@ -1036,6 +1073,37 @@ static sla_status spai_values(sla_csr* h, cudaStream_t s, bool fill_only = false
 // the caller's ordering; for a reordered handle also permuted like A, with
 // the source entry of every permuted entry) and layouts, once per handle;
 // then its values.
+// Work units (warps' groups, tiles, thread rows or slices, in CTAs of NT
+// threads) of a layout's product kernels.
+static long long layout_units(const sla_csr* h, const Layout& L) {
+    if (sliced_form(L.form)) return ((long long)L.nslices * 32 + NT - 1) / NT;
+    if (L.form == 5) return ((long long)h->n + NT - 1) / NT;
+    if (L.form == 4) return ((long long)h->n + WS_ROWS - 1) / WS_ROWS;
+    return group_ctas(h->n, L.form == 3 ? 1 : L.lanes);
+}
+
+// The SPAI products take their grids from their own kernels' occupancy,
+// at most SLA_SPAI_CTAS resident CTAs per SM.  Measured on B300 (SPAI
+// factors of the reordered kNN Laplacian, 4M rows, staged form 1): 3 CTAs
+// per SM 1.78k CG iterations/s; 4 (k_spai_t fits 4 by its own occupancy)
+// 1.73k -- the staging shared memory then leaves too little L1 for the
+// gathered vector; 2 1.66k.
+#ifndef SLA_SPAI_CTAS
+#define SLA_SPAI_CTAS 3
+#endif
+template <typename T>
+static sla_status spai_grids(sla_csr* h) {
+    int per = 1;
+    sla_status st = SLA_OK;
+    with_form(h->LGT.form, [&](auto f) { st = occupancy(k_spai_t<T, decltype(f)::value>, h->LGT.smem, &per); });
+    TRY(st);
+    h->LGT.gx = grid_x(h, layout_units(h, h->LGT), per < SLA_SPAI_CTAS ? per : SLA_SPAI_CTAS);
+    with_form(h->LG.form, [&](auto f) { st = occupancy(k_spai_z<T, decltype(f)::value>, h->LG.smem, &per); });
+    TRY(st);
+    h->LG.gx = grid_x(h, layout_units(h, h->LG), per < SLA_SPAI_CTAS ? per : SLA_SPAI_CTAS);
+    return SLA_OK;
+}
+
 static sla_status build_spai(sla_csr* h, cudaStream_t s) {
     if (h->diag_err & ERR_NO_DIAG) return fail(SLA_ERR_INVALID, "SPAI needs every diagonal entry stored");
     if (h->diag_err & ERR_DIAG_SIGN) return fail(SLA_ERR_INVALID, "SPAI needs a positive diagonal");
@@ -1096,6 +1164,7 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
         TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
                             s));
     }
+    TRY(h->dt == SLA_F64 ? spai_grids<double>(h) : spai_grids<float>(h));
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
     h->spai_ready = true;
     h->spai_stale = false;
@@ -1799,6 +1868,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt, const i
     h->time_product = (flags & SLA_TIME_PRODUCT) != 0;
     h->persistent = (flags & SLA_PERSISTENT) != 0;
     h->sliced = (flags & SLA_SLICED) != 0;
+    h->split = (flags & SLA_ROW_WALK) ? -1 : (flags & SLA_SPLIT_ROWS) ? 1 : 0;
     {
         int coop = 0;
         HCU(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
@@ -1862,6 +1932,17 @@ sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered) {
     if (form) *form = h->LI.form;
     if (ctas) *ctas = h->LI.gx;
     if (reordered) *reordered = h->reordered ? 1 : 0;
+    return SLA_OK;
+}
+
+sla_status sla_csr_layout_of(sla_handle h, int which, int* form, int* ctas, int* split) {
+    if (!h) return fail(SLA_ERR_INVALID, "null handle");
+    if (which < 0 || which > 2) return fail(SLA_ERR_INVALID, "which = %d: 0, 1 or 2", which);
+    if (which > 0 && !h->spai_ready) return fail(SLA_ERR_INVALID, "no SPAI factor yet");
+    const Layout& L = which == 0 ? h->LI : which == 1 ? h->LG : h->LGT;
+    if (form) *form = L.form;
+    if (ctas) *ctas = L.gx;
+    if (split) *split = L.bal && L.lanes == 1 && (L.form == 1 || L.form == 2) ? 1 : 0;
     return SLA_OK;
 }
 

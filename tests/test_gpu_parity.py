@@ -5,10 +5,12 @@ in seconds (many warp groups and CTAs and a ragged tail), plus edge cases.
 Every product test runs with the default form (the direct, thread-per-row
 form for patterns whose rows have at most 16 entries, else a warp-staged
 form), the warp-staged forms (staged=True), the warp pipeline
-(pipeline=True), the producer/consumer form (producer_consumer=True) and
-the sliced form (sliced=True), the last three wherever they apply; the solve tests run with one kernel per step in a CUDA graph (the
-default) and with the persistent iteration kernel (fused=True), each with
-every product form.
+(pipeline=True), the producer/consumer form (producer_consumer=True), the
+sliced form (sliced=True), the last three wherever they apply, and the
+warp-staged forms with every staged group summed split over the lanes
+(staged=True, split=True); the solve tests run with one kernel per step in
+a CUDA graph (the default) and with the persistent iteration kernel
+(fused=True), each with every product form.
 
 Tolerances: SpMV relative error <= 1e-12 (fp64) and <= 1e-5 (fp32);
 ||x - x_oracle|| / ||x_oracle|| <= 1e-6; iteration count within 2% of the
@@ -50,7 +52,8 @@ def _spmv_cases():
 
 
 FORMS = {"default": {}, "staged": {"staged": True}, "pipe": {"pipeline": True},
-         "pc": {"producer_consumer": True}, "sliced": {"sliced": True}}
+         "pc": {"producer_consumer": True}, "sliced": {"sliced": True},
+         "split": {"staged": True, "split": True}}
 # patterns whose sliced copy pads by at most 15% (the sliced form applies)
 SLICED = ("poisson2d_64", "poisson3d_24", "diffusion_96", "knn_3000")
 PIPE = pytest.mark.parametrize("mode", list(FORMS))
@@ -66,8 +69,10 @@ def test_spmv_parity(cuda_device, name, A, dtype, mode):
     x = np.random.default_rng(11).standard_normal(A.n).astype(dtype)
     M = make(A, **FORMS[mode])
     form = M.layout()[0]
-    if mode == "staged" or name == "dense_row":   # the dense row fits no bulk-copy form, nor the direct one
+    if mode in ("staged", "split") or name == "dense_row":   # the dense row fits no bulk-copy form, nor the direct one
         assert form in (0, 1, 2)
+        if mode == "split" and form in (1, 2) and name != "dense_row":
+            assert M.layout_of("A")[2]
     elif mode == "default" and name == "knn_3000":   # long rows: the sliced form
         assert form == 6, form
     elif mode == "default" and name == "poisson3d_24":   # 7-point rows: the sliced form for short rows
@@ -328,6 +333,104 @@ def test_spai_follows_update_values(cuda_device, reorder, sliced):
     lam, dA, ai = M.adjoint(x2, torch.from_numpy(w.g).to(cuda_device), tol=1e-10, pc="spai", eps=1e-3)
     lo, dAo, ao = oracle.adjoint(A2, x2.cpu().numpy(), w.g, 1e-10, pc="spai", eps=1e-3)
     assert _iters_ok(ai[0].iters, ao["iters"]) and rel(lam.cpu().numpy(), lo) <= 1e-6
+
+
+def _walk_costs(rp):
+    """Warp-wide fp64 steps of a staged product over 32-row groups, summed:
+    one lane per row (the longest row of every group) and with the group's
+    entries split into 32 runs of C = ceil(cnt / 32) entries rounded up to
+    odd, plus the rounds joining the pieces of cut rows."""
+    rp = np.asarray(rp, dtype=np.int64)
+    n = rp.size - 1
+    row = split = 0
+    for r0 in range(0, n, 32):
+        r1 = min(r0 + 32, n)
+        lo, hi = rp[r0:r1] - rp[r0], rp[r0 + 1:r1 + 1] - rp[r0]
+        cnt = int(hi[-1])
+        if cnt == 0:
+            continue
+        C = ((cnt + 31) // 32) | 1
+        ne = hi > lo
+        row += int((hi - lo).max())
+        split += C + int(((hi[ne] - 1) // C - lo[ne] // C).max())
+    return row, split
+
+
+def _lower_and_transpose(A):
+    rows = A.rows()
+    keep = A.col_idx <= rows
+    r, c = rows[keep], A.col_idx[keep]
+    rp_g = np.zeros(A.n + 1, np.int64)
+    rp_g[1:] = np.cumsum(np.bincount(r, minlength=A.n))
+    rp_t = np.zeros(A.n + 1, np.int64)
+    rp_t[1:] = np.cumsum(np.bincount(c, minlength=A.n))
+    return rp_g, rp_t
+
+
+def _skewed_spd(n, seed):
+    """Symmetric, strictly diagonally dominant matrix: every 32nd row holds
+    40 random columns of its own within 500 of the diagonal, the others 2,
+    each mirrored (so every 32-row group holds a few rows far longer than
+    the rest, and fits one lane per row)."""
+    g = np.random.default_rng(seed)
+    lens = np.full(n, 2)
+    lens[::32] = 40
+    r = np.repeat(np.arange(n), lens)
+    c = np.clip(r + g.integers(-500, 501, size=r.size), 0, n - 1)
+    r, c = np.concatenate([r, c]), np.concatenate([c, r])
+    off = r != c
+    key = np.unique(np.minimum(r[off], c[off]).astype(np.int64) * n + np.maximum(r[off], c[off]))
+    lo, hi = key // n, key % n
+    v = -(0.1 + g.random(key.size))
+    r = np.concatenate([lo, hi, np.arange(n)])
+    c = np.concatenate([hi, lo, np.arange(n)])
+    v = np.concatenate([v, v, np.zeros(n)])
+    v[-n:] = np.bincount(r[:-n], weights=np.abs(v[:-n]), minlength=n) + 1.0
+    order = np.lexsort((c, r))
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(np.bincount(r, minlength=n))
+    return CSR(n, rp, c[order].astype(np.int32), v[order])
+
+
+SPLIT_CASES = [("knn_20000", lambda: build("c5", npoints=20000).A), ("skewed_20000", lambda: _skewed_spd(20000, 5))]
+
+
+@pytest.mark.parametrize("name,mk", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_split_sums_follow_the_walk_cost(cuda_device, name, mk):
+    """The staged product splits its groups' entries over the lanes exactly
+    when the lane-per-row walk would cost at least 1.8 times the split one
+    (warp-wide fp64 steps summed over the matrix), recomputed here from the
+    patterns of A, G = tril(A) and G^T (caller order): on the skewed
+    pattern all three split, on the kNN Laplacian (row lengths too even)
+    none does.  By default and forced either way, the SPAI solve, the
+    adjoint and the product match the oracle."""
+    A = mk()
+    rp_g, rp_t = _lower_and_transpose(A)
+    gen = np.random.default_rng(21)
+    bh, gh = gen.standard_normal(A.n), gen.standard_normal(A.n)
+    b = torch.from_numpy(bh).to(cuda_device)
+    g = torch.from_numpy(gh).to(cuda_device)
+    xo, io = oracle.pcg(A, bh, 1e-10, pc="spai", eps=1e-3)
+    lo_, _, ao = oracle.adjoint(A, xo, gh, 1e-10, pc="spai", eps=1e-3)
+    for split in (None, True, False):
+        M = make(A, reorder=False, staged=True, split=split)
+        x, info = M.solve(b, tol=1e-10, pc="spai", eps=1e-3)
+        for which, rp in (("A", A.row_ptr), ("G", rp_g), ("GT", rp_t)):
+            form, _, sp = M.layout_of(which)
+            assert form in (1, 2), (which, form)
+            row, cut = _walk_costs(rp)
+            want = {None: row >= 1.8 * cut, True: True, False: False}[split]
+            assert sp == want, (which, split, row, cut, sp)
+            if split is None:
+                assert sp == (name == "skewed_20000"), (which, row, cut)
+        assert info[0].status == "ok" and _iters_ok(info[0].iters, io["iters"]), (info[0].iters, io["iters"])
+        assert rel(x.cpu().numpy(), xo) <= 1e-6
+        lam, dA, ai = M.adjoint(x, g, tol=1e-10, pc="spai", eps=1e-3)
+        assert _iters_ok(ai[0].iters, ao["iters"]) and rel(lam.cpu().numpy(), lo_) <= 1e-6
+        assert rel(dA.cpu().numpy(), oracle.grad_A(A, lo_, xo)) <= 1e-6
+        y = M.matvec(b).cpu().numpy()
+        scale = oracle.spmv(CSR(A.n, A.row_ptr, A.col_idx, np.abs(A.vals)), np.abs(bh))
+        assert np.all(np.abs(y - oracle.spmv(A, bh)) <= 1e-12 * scale)
 
 
 @FUSED
