@@ -160,14 +160,17 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         reordered by length within windows of 256, 1024 or 4096 rows when
  *         that pads less), used when padding adds at most 15% entries; one
  *         thread per row, coalesced value and column loads; 6 for rows of
- *         at least 12 entries on average, 7 (more resident CTAs) for
+ *         at least 7.5 entries on average, 7 (more resident CTAs) for
  *         shorter ones.  The default for the iteration matrix when some row
  *         has more than 16 entries and rows hold at least 12 on average, or
  *         when no row has more than 16 and rows hold at least 6 on average;
  *         with SLA_SLICED wherever it applies, the SPAI factors included.
  *         Costs (8 + value size) bytes per sliced entry of device memory,
  *         and the values are copied again by sla_csr_update_values.
- *         The SPAI factors G and G^T take their forms by the same rule;
+ *         The SPAI factor G takes its form by the same rule, but the sliced
+ *         form only with SLA_SLICED; G^T takes the sliced form whenever
+ *         rows sorted within windows of 256 rows pad it by at most 20%
+ *         (unless SLA_STAGED, SLA_WARP_PIPELINE or SLA_PRODUCER_CONSUMER);
  *         the BiCGStab products always take a staged form (0, 1 or 2).
  *         In forms 1 and 2 with one lane per row a warp sums its group of
  *         32 rows either lane by lane (each lane its own row: as many

@@ -486,15 +486,29 @@ static bool vals_aligned(const sla_csr* h, const void* vals) {
     return aligned16(vals) && (h->batch == 1 || ((size_t)h->nnz * h->es) % 16 == 0);
 }
 
-// Streaming kernels: two resident CTAs per SM.  Each warp-level fp64
-// reduction step costs a full warp issue on the slow fp64 pipe, so fewer,
-// longer-running threads (each with two pairs in flight per trip) beat a
-// fully occupied grid here.
+// Streaming kernels: two resident CTAs per SM, or SLA_VEC_CTAS_LARGE when
+// every thread still makes at least SLA_VEC_TRIPS trips (pairs) at that
+// occupancy.  Their per-CTA reduction tail and the fp64 work of each pair
+// favour few, long-running threads on small systems; on large ones more
+// loads in flight pay.  Measured on B300 inside the running iteration (it/s
+// at 2 / 4 / 8 CTAs per SM): 2D 5-point 1M rows 22.1k / 20.3k / 18.0k
+// (3.5 trips per thread at 4); 3D 7-point 2M rows 13.4k / 13.1k / 12.0k
+// (6.9 trips); kNN SPAI 4M rows 1.78k / 1.82k / 1.80k (13.8 trips).  Two
+// pairs per thread per trip (SLA_VU) did not help on any of them.
 #ifndef SLA_VEC_CTAS
 #define SLA_VEC_CTAS 2
 #endif
-static constexpr int VEC_CTAS_PER_SM = SLA_VEC_CTAS;
-static int gx_vec(const sla_csr* h) { return grid_x(h, vec_units(h), VEC_CTAS_PER_SM); }
+#ifndef SLA_VEC_CTAS_LARGE
+#define SLA_VEC_CTAS_LARGE 4
+#endif
+#ifndef SLA_VEC_TRIPS
+#define SLA_VEC_TRIPS 8
+#endif
+static int gx_vec(const sla_csr* h) {
+    const long long units = vec_units(h);   // CTAs if every thread took one pair
+    const int large = grid_x(h, units, SLA_VEC_CTAS_LARGE);
+    return units >= (long long)SLA_VEC_TRIPS * large ? large : grid_x(h, units, SLA_VEC_CTAS);
+}
 
 static Sys sys_of(sla_csr* h) {
     Sys s;
@@ -817,16 +831,30 @@ static sla_status gather_map(size_t eb, long long m, int batch, const int* map, 
 // A by 4%, but the SPAI factor (whose row lengths vary most) by 15.5%; 1024
 // rows pad it by 4%.
 static constexpr int SLICE_WINDOWS[3] = {NWARP * 32, 4 * NWARP * 32, 16 * NWARP * 32};
+#ifndef SLA_SLICE_WINDOW_LAST
+#define SLA_SLICE_WINDOW_LAST 2   // largest window tried (index into SLICE_WINDOWS)
+#endif
 static constexpr double SLICE_GOOD_PAD = 1.06;
-// Rows of at least this many entries on average take the sliced form for 4
-// resident CTAs per SM (6), shorter ones the one for 5 (7).
+// Patterns whose rows hold more than 16 entries take the sliced form by
+// default when they hold at least this many on average.
 #ifndef SLA_SLICED_MINAVG
 #define SLA_SLICED_MINAVG 12.0
 #endif
+// Sliced rows of at least this many entries on average take the form for 4
+// resident CTAs per SM and batches of 4 (6), shorter ones the one for 5 and
+// batches of 7 (7).  Measured on B300: 3D 7-point (6.97 entries) form 7;
+// kNN Laplacian (14.6) form 6; its SPAI factor G^T (7.8) form 6, 1.87k CG
+// iterations/s against 1.86k.
+#ifndef SLA_SLICED_FORM6_MINAVG
+#define SLA_SLICED_FORM6_MINAVG 7.5
+#endif
 // Largest padding (sliced entries / stored entries) for which the sliced
-// form is used.
+// form is used; for the SPAI factor G^T by default (windows of 256 rows).
 #ifndef SLA_SLICED_MAXPAD
 #define SLA_SLICED_MAXPAD 1.15
+#endif
+#ifndef SLA_SLICED_MAXPAD_GT
+#define SLA_SLICED_MAXPAD_GT 1.2
 #endif
 
 // values: the CSR values the sliced copy mirrors ([batch][is] of eb bytes).
@@ -853,7 +881,8 @@ static sla_status sliced_values(const sla_csr* h, SellBufs& B, const void* vals,
 // row, so the iteration order is unchanged.
 template <typename T>
 static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long long nnz, const void* vals,
-                              long long is, size_t eb, Layout* L, SellBufs& B, cudaStream_t s) {
+                              long long is, size_t eb, Layout* L, SellBufs& B, cudaStream_t s,
+                              int last_window, double max_pad) {
     const int n = h->n;
     if (nnz == 0 || n < 1) return SLA_OK;
     std::vector<int> rp;
@@ -871,7 +900,7 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     }
     std::vector<int> perm, sptr;
     long long pad_sorted = 0;
-    for (int wi = 0; wi < 3; ++wi) {
+    for (int wi = 0; wi <= last_window; ++wi) {
         const int window = SLICE_WINDOWS[wi];
         std::vector<int> pw(slots), sw(nslices + 1, 0);
         for (long long t = 0; t < slots; ++t) pw[t] = t < n ? (int)t : n;
@@ -893,7 +922,7 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     }
     const bool sorted = pad_sorted < pad_id && (double)pad_id > 1.02 * (double)nnz;
     const long long npad = sorted ? pad_sorted : pad_id;
-    if ((double)npad > SLA_SLICED_MAXPAD * (double)nnz || npad >= 0x7fffffffLL) return SLA_OK;
+    if ((double)npad > max_pad * (double)nnz || npad >= 0x7fffffffLL) return SLA_OK;
     if (!sorted) {
         for (int sl = 0; sl < nslices; ++sl) {
             int w = 0;
@@ -918,8 +947,8 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     TRY(B.sval.alloc(eb * (size_t)B.vstride * h->batch));
     TRY(sliced_values(h, B, vals, is, eb, s));
     // the sliced form for 4 resident CTAs per SM (6) for long rows, for 5 (7)
-    // for rows of fewer than 12 entries on average
-    const int form = (double)nnz >= SLA_SLICED_MINAVG * (double)n ? 6 : 7;
+    // for rows of fewer than SLA_SLICED_FORM6_MINAVG entries on average
+    const int form = (double)nnz >= SLA_SLICED_FORM6_MINAVG * (double)n ? 6 : 7;
     int per = 1;
     if (form == 6) TRY(occupancy(k_spmv_iter<T, 6>, 0, &per));
     else TRY(occupancy(k_spmv_iter<T, 7>, 0, &per));
@@ -953,9 +982,10 @@ static bool sliced_by_default(const sla_csr* h, const Layout& L, long long nnz) 
 }
 
 static sla_status make_sliced_any(sla_csr* h, const int* d_rp, const int* d_ci, long long nnz, const void* vals,
-                                  long long is, size_t eb, Layout* L, SellBufs& B, cudaStream_t s) {
-    return h->dt == SLA_F64 ? make_sliced<double>(h, d_rp, d_ci, nnz, vals, is, eb, L, B, s)
-                            : make_sliced<float>(h, d_rp, d_ci, nnz, vals, is, eb, L, B, s);
+                                  long long is, size_t eb, Layout* L, SellBufs& B, cudaStream_t s,
+                                  int last_window = SLA_SLICE_WINDOW_LAST, double max_pad = SLA_SLICED_MAXPAD) {
+    return h->dt == SLA_F64 ? make_sliced<double>(h, d_rp, d_ci, nnz, vals, is, eb, L, B, s, last_window, max_pad)
+                            : make_sliced<float>(h, d_rp, d_ci, nnz, vals, is, eb, L, B, s, last_window, max_pad);
 }
 
 // Iterate on P A P^T (reverse Cuthill-McKee): permuted pattern and values
@@ -1083,7 +1113,8 @@ static long long layout_units(const sla_csr* h, const Layout& L) {
 }
 
 // The SPAI products take their grids from their own kernels' occupancy,
-// at most SLA_SPAI_CTAS resident CTAs per SM.  Measured on B300 (SPAI
+// in the staged forms at most SLA_SPAI_CTAS resident CTAs per SM (their
+// staging shared memory competes with L1).  Measured on B300 (SPAI
 // factors of the reordered kNN Laplacian, 4M rows, staged form 1): 3 CTAs
 // per SM 1.78k CG iterations/s; 4 (k_spai_t fits 4 by its own occupancy)
 // 1.73k -- the staging shared memory then leaves too little L1 for the
@@ -1091,16 +1122,19 @@ static long long layout_units(const sla_csr* h, const Layout& L) {
 #ifndef SLA_SPAI_CTAS
 #define SLA_SPAI_CTAS 3
 #endif
+static int spai_ctas(const Layout& L, int per) {
+    return L.form <= 4 && per > SLA_SPAI_CTAS ? SLA_SPAI_CTAS : per;
+}
 template <typename T>
 static sla_status spai_grids(sla_csr* h) {
     int per = 1;
     sla_status st = SLA_OK;
     with_form(h->LGT.form, [&](auto f) { st = occupancy(k_spai_t<T, decltype(f)::value>, h->LGT.smem, &per); });
     TRY(st);
-    h->LGT.gx = grid_x(h, layout_units(h, h->LGT), per < SLA_SPAI_CTAS ? per : SLA_SPAI_CTAS);
+    h->LGT.gx = grid_x(h, layout_units(h, h->LGT), spai_ctas(h->LGT, per));
     with_form(h->LG.form, [&](auto f) { st = occupancy(k_spai_z<T, decltype(f)::value>, h->LG.smem, &per); });
     TRY(st);
-    h->LG.gx = grid_x(h, layout_units(h, h->LG), per < SLA_SPAI_CTAS ? per : SLA_SPAI_CTAS);
+    h->LG.gx = grid_x(h, layout_units(h, h->LG), spai_ctas(h->LG, per));
     return SLA_OK;
 }
 
@@ -1159,10 +1193,21 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
                       SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G, SLA_MAX_CAP_G));
     TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s,
                       SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G, SLA_MAX_CAP_G));
-    if (h->sliced) {   // only when asked: staged G and G^T measured faster (kNN Laplacian)
+    // Sliced factors: both with SLA_SLICED; by default G^T alone, its rows
+    // sorted by length within windows of at most 256 rows (its gathers stay
+    // near the row) when that pads at most SLA_SLICED_MAXPAD_GT.  Measured
+    // on B300 (SPAI factors of the reordered kNN Laplacian, 4M rows, CG
+    // iterations/s): both staged 1.80k; G^T sliced 1.85k; G sliced 1.72k
+    // (its kernel also reads r and reduces r.z at every row, which the
+    // sliced slot order scatters); both 1.75k (windows up to 1024 rows, as
+    // for the iteration matrix: 1.56k).
+    if (h->sliced) {
         TRY(make_sliced_any(h, h->grp.as<int>(), h->gci.as<int>(), ng, h->gv.p, h->gstride, 8, &h->LG, h->sG, s));
         TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
                             s));
+    } else if (!h->pipeline && !h->ws && !h->staged) {
+        TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
+                            s, 0, SLA_SLICED_MAXPAD_GT));
     }
     TRY(h->dt == SLA_F64 ? spai_grids<double>(h) : spai_grids<float>(h));
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
