@@ -66,6 +66,8 @@ struct Mat {
     int direct;       // 1: the layout's kernels run the direct form (no shared-memory staging)
     int bal;          // 1: staged groups (one lane per row, cp.async forms) are summed with the
                       //    entries split evenly over the lanes (balanced_group_sum)
+    int swin;         // 1: sliced rows sorted within windows of SLICE_WIN rows, run a warp per
+                      //    window with the epilogue in row order (spmv_sliced_win)
     // Sliced form (FORM 6): the rows in slices of 32, each slice stored
     // column by column (entry j of the slice's 32 rows side by side), padded
     // to the slice's longest row.
@@ -308,37 +310,87 @@ constexpr int SLICE_U = SLA_SLICE_U;
 #ifndef SLA_SLICE_U_SHORT
 #define SLA_SLICE_U_SHORT 7
 #endif
+// Sum of this lane's slot of slice sl: batches of U entries (loads before
+// gathers), then single entries.
+template <typename T, typename VT, int U, class Gather>
+__device__ __forceinline__ typename Prec<T>::acc slice_sum(const Mat& A, const VT* __restrict__ sv, Gather gather,
+                                                          int sl, int lane) {
+    using acc_t = typename Prec<T>::acc;
+    const int base = ld_nc(A.sptr + sl);
+    const int w = (ld_nc(A.sptr + sl + 1) - base) >> 5;
+    acc_t s = Prec<T>::zero();
+    const VT* v = sv + base + lane;
+    const int* c = A.scol + base + lane;
+    int j = 0;
+    for (; j + U <= w; j += U) {
+        VT a[U];
+        int cc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            a[u] = ld_mat(v + (j + u) * 32);
+            cc[u] = ld_mat(c + (j + u) * 32);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) mac(s, a[u], gather(cc[u]));
+    }
+    for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
+    acc_norm(s);
+    return s;
+}
+
 template <typename T, typename VT, int U = SLICE_U, class Gather, class Pre, class Epi>
 __device__ __forceinline__ void spmv_sliced(const Mat& A, const VT* __restrict__ sv, Gather gather, Pre pre,
                                             Epi epi) {
-    using acc_t = typename Prec<T>::acc;
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * NT) >> 5;
     for (int sl = (blockIdx.x * NT + threadIdx.x) >> 5; sl < A.nslices; sl += nwarps) {
-        const int base = ld_nc(A.sptr + sl);
-        const int w = (ld_nc(A.sptr + sl + 1) - base) >> 5;
         const int slot = (sl << 5) + lane;
         const int row = A.sperm ? ld_nc(A.sperm + slot) : slot;
         const bool live = row < A.n;
         const auto carried = live ? pre(row) : decltype(pre(0)){};
-        acc_t s = Prec<T>::zero();
-        const VT* v = sv + base + lane;
-        const int* c = A.scol + base + lane;
-        int j = 0;
-        for (; j + U <= w; j += U) {
-            VT a[U];
-            int cc[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                a[u] = ld_mat(v + (j + u) * 32);
-                cc[u] = ld_mat(c + (j + u) * 32);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) mac(s, a[u], gather(cc[u]));
-        }
-        for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
-        acc_norm(s);
+        const auto s = slice_sum<T, VT, U>(A, sv, gather, sl, lane);
         if (live) epi(row, s, carried);
+    }
+}
+
+// Sliced form with rows sorted within windows of SLICE_WIN rows (Mat::swin):
+// a warp takes whole windows (SLICE_WIN / 32 slices), parks the window's
+// slot sums in its shared-memory slice at their rows' places, and then runs
+// the epilogue for the window's rows in row order, so the epilogue's vector
+// accesses are coalesced instead of following the slot order.
+// Shared memory per warp: SLICE_WIN accumulators (wsm, A.wstride doubles).
+constexpr int SLICE_WIN = 256;
+template <typename T, typename VT, int U = SLICE_U, class Gather, class Pre, class Epi>
+__device__ __forceinline__ void spmv_sliced_win(const Mat& A, const VT* __restrict__ sv, Gather gather, Pre pre,
+                                                Epi epi, double* wsm) {
+    using acc_t = typename Prec<T>::acc;
+    using C = decltype(pre(0));
+    constexpr int SPW = SLICE_WIN / 32;   // slices per window
+    const int lane = threadIdx.x & 31;
+    acc_t* sums = reinterpret_cast<acc_t*>(wsm + (threadIdx.x >> 5) * A.wstride);
+    const int nwin = (A.nslices + SPW - 1) / SPW;
+    const int nwarps = (gridDim.x * NT) >> 5;
+    for (int win = (blockIdx.x * NT + threadIdx.x) >> 5; win < nwin; win += nwarps) {
+        const int row0 = win * SLICE_WIN;
+        const int sl1 = min((win + 1) * SPW, A.nslices);
+        for (int sl = win * SPW; sl < sl1; ++sl) {
+            const int row = ld_nc(A.sperm + (sl << 5) + lane);
+            const auto s = slice_sum<T, VT, U>(A, sv, gather, sl, lane);
+            if (row < A.n) sums[row - row0] = s;
+        }
+        __syncwarp();
+        C carried[SPW];
+#pragma unroll
+        for (int k = 0; k < SPW; ++k) {
+            const int row = row0 + k * 32 + lane;
+            carried[k] = row < A.n ? pre(row) : C{};
+        }
+#pragma unroll
+        for (int k = 0; k < SPW; ++k) {
+            const int row = row0 + k * 32 + lane;
+            if (row < A.n) epi(row, sums[k * 32 + lane], carried[k]);
+        }
+        __syncwarp();   // the sums are read before the next window writes them
     }
 }
 
@@ -980,8 +1032,11 @@ template <typename T, int FORM, typename VT, typename XT, bool COH = false, clas
 __device__ __forceinline__ void spmv_vec(const Mat& A, const VT* __restrict__ av, const XT* v, Pre pre,
                                          Epi epi, double* wsm) {
     if constexpr (FORM == 5) spmv_direct<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi);
-    else if constexpr (sliced_form(FORM))
-        spmv_sliced<T, VT, (FORM == 7 ? SLA_SLICE_U_SHORT : SLICE_U)>(A, av, GatherVec<XT, COH>{v}, pre, epi);
+    else if constexpr (sliced_form(FORM)) {
+        constexpr int U = FORM == 7 ? SLA_SLICE_U_SHORT : SLICE_U;
+        if (A.swin) spmv_sliced_win<T, VT, U>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
+        else spmv_sliced<T, VT, U>(A, av, GatherVec<XT, COH>{v}, pre, epi);
+    }
     else if constexpr (FORM == 0) spmv_rows<T, VT>(A, av, GatherVec<XT, COH>{v}, pre, epi, wsm);
     else if constexpr (FORM == 3) spmv_pipe<T, VT, XT>(A, av, v, pre, epi, wsm);
     else if constexpr (FORM == 4) spmv_ws<T, VT, XT>(A, av, v, pre, epi, wsm);

@@ -137,6 +137,7 @@ struct Layout {
     size_t smem = 0;  // their dynamic shared memory
     int maxrow = 0;   // longest row
     int bal = 0;      // staged groups summed split over the lanes (forms 1 and 2, one lane per row)
+    int swin = 0;     // sliced rows sorted within windows of SLICE_WIN rows: a warp per window
     // sliced copy (form 6), owned by the handle's SellBufs
     const int* sptr = nullptr;
     const int* sperm = nullptr;
@@ -533,6 +534,7 @@ static Mat mat_of(const int* rp, const int* ci, int n, long long nnz, const Layo
     m.wstride = (int)(L.smem / NWARP / sizeof(double));
     m.lanes = L.form == 3 ? 1 : L.lanes;
     m.bal = L.bal && m.lanes == 1 && (L.form == 1 || L.form == 2) ? 1 : 0;
+    m.swin = L.swin && sliced_form(L.form) ? 1 : 0;
     m.lshift = m.lanes == 4 ? 2 : (m.lanes == 2 ? 1 : 0);
     if (L.form == 3) m.cap = L.ccap;   // every group stages in the register-staged passes too
     m.nnz = nnz;
@@ -834,6 +836,10 @@ static constexpr int SLICE_WINDOWS[3] = {NWARP * 32, 4 * NWARP * 32, 16 * NWARP 
 #ifndef SLA_SLICE_WINDOW_LAST
 #define SLA_SLICE_WINDOW_LAST 2   // largest window tried (index into SLICE_WINDOWS)
 #endif
+#ifndef SLA_SLICE_WIN_EPI
+#define SLA_SLICE_WIN_EPI 1       // window-sorted sliced layouts run a warp per window (spmv_sliced_win)
+#endif
+static_assert(SLICE_WINDOWS[0] == SLICE_WIN, "the smallest sorting window is the kernels' window");
 static constexpr double SLICE_GOOD_PAD = 1.06;
 // Patterns whose rows hold more than 16 entries take the sliced form by
 // default when they hold at least this many on average.
@@ -900,6 +906,7 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     }
     std::vector<int> perm, sptr;
     long long pad_sorted = 0;
+    int sort_window = 0;
     for (int wi = 0; wi <= last_window; ++wi) {
         const int window = SLICE_WINDOWS[wi];
         std::vector<int> pw(slots), sw(nslices + 1, 0);
@@ -917,6 +924,7 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
             perm.swap(pw);
             sptr.swap(sw);
             pad_sorted = sptr[nslices];
+            sort_window = window;
         }
         if ((double)pad_sorted <= SLICE_GOOD_PAD * (double)nnz) break;
     }
@@ -949,11 +957,14 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
     // the sliced form for 4 resident CTAs per SM (6) for long rows, for 5 (7)
     // for rows of fewer than SLA_SLICED_FORM6_MINAVG entries on average
     const int form = (double)nnz >= SLA_SLICED_FORM6_MINAVG * (double)n ? 6 : 7;
+    // rows sorted within windows of SLICE_WIN rows: a warp per window, the
+    // epilogue in row order (spmv_sliced_win), SLICE_WIN sums per warp
+    L->swin = SLA_SLICE_WIN_EPI && sorted && sort_window == SLICE_WIN ? 1 : 0;
+    L->smem = L->swin ? (size_t)NWARP * SLICE_WIN * sizeof(double) : 0;
     int per = 1;
-    if (form == 6) TRY(occupancy(k_spmv_iter<T, 6>, 0, &per));
-    else TRY(occupancy(k_spmv_iter<T, 7>, 0, &per));
+    if (form == 6) TRY(occupancy(k_spmv_iter<T, 6>, L->smem, &per));
+    else TRY(occupancy(k_spmv_iter<T, 7>, L->smem, &per));
     L->form = form;
-    L->smem = 0;
     L->sptr = B.sptr.as<int>();
     L->sperm = sorted ? B.perm.as<int>() : nullptr;
     L->scol = B.scol.as<int>();
