@@ -167,10 +167,12 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         with SLA_SLICED wherever it applies, the SPAI factors included.
  *         Costs (8 + value size) bytes per sliced entry of device memory,
  *         and the values are copied again by sla_csr_update_values.
- *         The SPAI factor G takes its form by the same rule, but the sliced
- *         form only with SLA_SLICED; G^T takes the sliced form whenever
- *         rows sorted within windows of 256 rows pad it by at most 20%
- *         (unless SLA_STAGED, SLA_WARP_PIPELINE or SLA_PRODUCER_CONSUMER);
+ *         The SPAI factors G and G^T take the sliced form whenever rows
+ *         sorted within windows of 256 rows pad them by at most 20% (unless
+ *         SLA_STAGED, SLA_WARP_PIPELINE or SLA_PRODUCER_CONSUMER), else
+ *         their forms by the rule above; a sliced matrix whose rows are
+ *         sorted within windows of 256 rows runs a warp per window, with the
+ *         per-row work after the sums (the vector updates) in row order;
  *         the BiCGStab products always take a staged form (0, 1 or 2).
  *         In forms 1 and 2 with one lane per row a warp sums its group of
  *         32 rows either lane by lane (each lane its own row: as many

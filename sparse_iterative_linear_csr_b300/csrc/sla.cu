@@ -855,12 +855,12 @@ static constexpr double SLICE_GOOD_PAD = 1.06;
 #define SLA_SLICED_FORM6_MINAVG 7.5
 #endif
 // Largest padding (sliced entries / stored entries) for which the sliced
-// form is used; for the SPAI factor G^T by default (windows of 256 rows).
+// form is used; for the SPAI factors by default (windows of 256 rows).
 #ifndef SLA_SLICED_MAXPAD
 #define SLA_SLICED_MAXPAD 1.15
 #endif
-#ifndef SLA_SLICED_MAXPAD_GT
-#define SLA_SLICED_MAXPAD_GT 1.2
+#ifndef SLA_SLICED_MAXPAD_FACTORS
+#define SLA_SLICED_MAXPAD_FACTORS 1.2
 #endif
 
 // values: the CSR values the sliced copy mirrors ([batch][is] of eb bytes).
@@ -1204,21 +1204,26 @@ static sla_status build_spai(sla_csr* h, cudaStream_t s) {
                       SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G, SLA_MAX_CAP_G));
     TRY(choose_layout(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, &h->LGT, true, sizeof(double), s,
                       SLA_DIRECT_MAXROW_G, SLA_MIN_LANES_G, SLA_MAX_CAP_G));
-    // Sliced factors: both with SLA_SLICED; by default G^T alone, its rows
-    // sorted by length within windows of at most 256 rows (its gathers stay
-    // near the row) when that pads at most SLA_SLICED_MAXPAD_GT.  Measured
-    // on B300 (SPAI factors of the reordered kNN Laplacian, 4M rows, CG
-    // iterations/s): both staged 1.80k; G^T sliced 1.85k; G sliced 1.72k
-    // (its kernel also reads r and reduces r.z at every row, which the
-    // sliced slot order scatters); both 1.75k (windows up to 1024 rows, as
-    // for the iteration matrix: 1.56k).
+    // Sliced factors.  By default G and G^T take the sliced form with rows
+    // sorted by length within windows of 256 rows (a warp per window, the
+    // epilogue in row order; the gathers stay near the row) when that pads
+    // at most SLA_SLICED_MAXPAD_FACTORS; with SLA_SLICED in the iteration
+    // matrix's windows (up to 4096 rows, least padding).  Measured on B300
+    // (SPAI factors of the reordered kNN Laplacian, 4M rows, CG
+    // iterations/s): both staged 1.80k.  With the epilogue in slot order:
+    // G^T sliced 1.86k, G sliced 1.72k (G's kernel also reads r and reduces
+    // r.z at every row, which the slot order scatters), both 1.75k, both in
+    // windows of up to 1024 rows 1.56k.  With the window epilogue (and the
+    // iteration matrix's product on it too): G^T sliced 1.96k, both 2.04k.
     if (h->sliced) {
         TRY(make_sliced_any(h, h->grp.as<int>(), h->gci.as<int>(), ng, h->gv.p, h->gstride, 8, &h->LG, h->sG, s));
         TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
                             s));
     } else if (!h->pipeline && !h->ws && !h->staged) {
+        TRY(make_sliced_any(h, h->grp.as<int>(), h->gci.as<int>(), ng, h->gv.p, h->gstride, 8, &h->LG, h->sG, s, 0,
+                            SLA_SLICED_MAXPAD_FACTORS));
         TRY(make_sliced_any(h, h->gtrp.as<int>(), h->gtci.as<int>(), ng, h->gtv.p, h->gstride, 8, &h->LGT, h->sGT,
-                            s, 0, SLA_SLICED_MAXPAD_GT));
+                            s, 0, SLA_SLICED_MAXPAD_FACTORS));
     }
     TRY(h->dt == SLA_F64 ? spai_grids<double>(h) : spai_grids<float>(h));
     TRY(h->t.alloc(WORK_BYTES * (size_t)n * h->batch));
