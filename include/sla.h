@@ -160,7 +160,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         reordered by length within windows of 256, 1024 or 4096 rows when
  *         that pads less), used when padding adds at most 15% entries; one
  *         thread per row, coalesced value and column loads; 6 for rows of
- *         at least 7.5 entries on average, 7 (more resident CTAs) for
+ *         at least 8 entries on average, 7 (more resident CTAs) for
  *         shorter ones.  The default for the iteration matrix when some row
  *         has more than 16 entries and rows hold at least 12 on average, or
  *         when no row has more than 16 and rows hold at least 6 on average;

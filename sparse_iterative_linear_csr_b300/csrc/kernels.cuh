@@ -293,14 +293,17 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
 // entries go in batches of SLICE_U -- all loads of a batch issued before its
 // gathers -- then one at a time.  Padding entries hold the value 0 and a
 // valid column.  Rows are summed in stored order (one fp64 FMA per entry
-// for fp64 systems).  No shared memory.
+// for fp64 systems).  No shared memory (but see spmv_sliced_win).
 // Measured on B300 inside the running iteration (kNN Laplacian; 3D and 2D
-// grids): plain batches of 4 beat batches of 6 or 8 predicated on the
-// width, batches of 3 or 4 software-pipelined (the next batch's values and
-// columns loaded before this batch's FMAs), and 3 resident CTAs per SM
-// (kNN product 191 us against 204-282 us).
+// grids): plain batches beat batches predicated on the width, batches of 3
+// or 4 software-pipelined (the next batch's values and columns loaded
+// before this batch's FMAs), and 3 resident CTAs per SM (kNN product 191 us
+// against 204-282 us).  With the window epilogue and both SPAI factors
+// sliced (kNN SPAI-PCG, CG iterations/s): batches of 2 / 4 / 5 / 6 / 7 / 8
+// 2.01k / 2.04k / 2.12k / 2.13k / 2.08k / 2.09k (the A product 198 / 186 /
+// 179 / 179 / 180 / 181 us).
 #ifndef SLA_SLICE_U
-#define SLA_SLICE_U 4
+#define SLA_SLICE_U 6
 #endif
 constexpr int SLICE_U = SLA_SLICE_U;
 

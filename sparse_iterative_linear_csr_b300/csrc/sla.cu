@@ -847,12 +847,14 @@ static constexpr double SLICE_GOOD_PAD = 1.06;
 #define SLA_SLICED_MINAVG 12.0
 #endif
 // Sliced rows of at least this many entries on average take the form for 4
-// resident CTAs per SM and batches of 4 (6), shorter ones the one for 5 and
-// batches of 7 (7).  Measured on B300: 3D 7-point (6.97 entries) form 7;
-// kNN Laplacian (14.6) form 6; its SPAI factor G^T (7.8) form 6, 1.87k CG
-// iterations/s against 1.86k.
+// resident CTAs per SM and batches of SLICE_U (6), shorter ones the one for
+// 5 and batches of 7 (7).  Measured on B300: 3D 7-point (6.97 entries) form
+// 7; kNN Laplacian (14.6) form 6; its SPAI factors (7.8 entries): with form
+// 6 in batches of 4, G^T alone sliced, form 6 1.87k CG iterations/s against
+// 1.86k; with batches of 6 and both factors sliced, form 7 2.15k against
+// 2.12-2.13k.
 #ifndef SLA_SLICED_FORM6_MINAVG
-#define SLA_SLICED_FORM6_MINAVG 7.5
+#define SLA_SLICED_FORM6_MINAVG 8.0
 #endif
 // Largest padding (sliced entries / stored entries) for which the sliced
 // form is used; for the SPAI factors by default (windows of 256 rows).
