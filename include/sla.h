@@ -152,8 +152,9 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         takes precedence over SLA_WARP_PIPELINE);
  *         5 direct: one thread per row, no shared-memory staging, kernels
  *         built for high occupancy -- the default whenever no row has more
- *         than 16 entries, unless SLA_STAGED, SLA_WARP_PIPELINE or
- *         SLA_PRODUCER_CONSUMER asks otherwise; otherwise 0, 1 or 2;
+ *         than 16 entries and the sliced form (below) does not apply, unless
+ *         SLA_STAGED, SLA_WARP_PIPELINE or SLA_PRODUCER_CONSUMER asks
+ *         otherwise; otherwise 0, 1 or 2;
  *         6 and 7 sliced (not with SLA_STAGED, SLA_WARP_PIPELINE or
  *         SLA_PRODUCER_CONSUMER): a handle-owned copy of the iteration
  *         matrix in slices of 32 rows stored column by column (rows
@@ -163,7 +164,7 @@ sla_status sla_csr_create(int n, long long nnz, int batch, sla_dtype dt,
  *         at least 8 entries on average, 7 (more resident CTAs) for
  *         shorter ones.  The default for the iteration matrix when some row
  *         has more than 16 entries and rows hold at least 12 on average, or
- *         when no row has more than 16 and rows hold at least 6 on average;
+ *         when no row has more than 16 and rows hold at least 4.5 on average;
  *         with SLA_SLICED wherever it applies, the SPAI factors included.
  *         Costs (8 + value size) bytes per sliced entry of device memory,
  *         and the values are copied again by sla_csr_update_values.

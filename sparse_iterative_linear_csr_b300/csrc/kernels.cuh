@@ -305,6 +305,9 @@ __device__ __forceinline__ void spmv_direct(const Mat& A, const VT* __restrict__
 #ifndef SLA_SLICE_U
 #define SLA_SLICE_U 6
 #endif
+#ifndef SLA_SLICE_REST
+#define SLA_SLICE_REST 1   // the last w % U entries of a slot as one batch (0: one at a time)
+#endif
 constexpr int SLICE_U = SLA_SLICE_U;
 
 // Batch of the short-row sliced form (7): measured on the 3D 7-point
@@ -313,8 +316,31 @@ constexpr int SLICE_U = SLA_SLICE_U;
 #ifndef SLA_SLICE_U_SHORT
 #define SLA_SLICE_U_SHORT 7
 #endif
-// Sum of this lane's slot of slice sl: batches of U entries (loads before
-// gathers), then single entries.
+// K entries j .. j + K - 1 of a slot: all loads of values and columns
+// issued before the gathers, then the FMAs in order.
+template <int K, typename VT, typename ACC, class Gather>
+__device__ __forceinline__ void slice_batch(ACC& s, const VT* v, const int* c, int j, Gather gather) {
+    VT a[K];
+    int cc[K];
+#pragma unroll
+    for (int u = 0; u < K; ++u) {
+        a[u] = ld_mat(v + (j + u) * 32);
+        cc[u] = ld_mat(c + (j + u) * 32);
+    }
+#pragma unroll
+    for (int u = 0; u < K; ++u) mac(s, a[u], gather(cc[u]));
+}
+// The last w % U entries as one batch of their own size (R < U).
+template <int R, typename VT, typename ACC, class Gather>
+__device__ __forceinline__ void slice_rest(ACC& s, const VT* v, const int* c, int j, int r, Gather gather) {
+    if constexpr (R > 0) {
+        if (r == R) slice_batch<R>(s, v, c, j, gather);
+        else slice_rest<R - 1>(s, v, c, j, r, gather);
+    }
+}
+
+// Sum of this lane's slot of slice sl: batches of U entries, then the rest
+// as one batch.
 template <typename T, typename VT, int U, class Gather>
 __device__ __forceinline__ typename Prec<T>::acc slice_sum(const Mat& A, const VT* __restrict__ sv, Gather gather,
                                                           int sl, int lane) {
@@ -325,18 +351,12 @@ __device__ __forceinline__ typename Prec<T>::acc slice_sum(const Mat& A, const V
     const VT* v = sv + base + lane;
     const int* c = A.scol + base + lane;
     int j = 0;
-    for (; j + U <= w; j += U) {
-        VT a[U];
-        int cc[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            a[u] = ld_mat(v + (j + u) * 32);
-            cc[u] = ld_mat(c + (j + u) * 32);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) mac(s, a[u], gather(cc[u]));
-    }
+    for (; j + U <= w; j += U) slice_batch<U>(s, v, c, j, gather);
+#if SLA_SLICE_REST
+    slice_rest<U - 1>(s, v, c, j, w - j, gather);
+#else
     for (; j < w; ++j) mac(s, ld_mat(v + j * 32), gather(ld_mat(c + j * 32)));
+#endif
     acc_norm(s);
     return s;
 }

@@ -980,13 +980,15 @@ static sla_status make_sliced(sla_csr* h, const int* d_rp, const int* d_ci, long
 // Default choice of the sliced form for the iteration matrix (measured on
 // B300 inside the running iteration): rows too long for the direct form and
 // long enough on average (the kNN Laplacian, 14.6 entries per row: 192
-// against 238 us staged), or short rows of at least 6 on average (the 3D
-// 7-point grid: 51.4 against 55.7 us direct, at 5 CTAs per SM); the direct
-// form stays for shorter rows (the 2D 5-point grid: 26.2 against 26.9 us),
-// and the SPAI factors stay staged (the kNN Laplacian's, 7.8 per row, runs
-// faster staged).
+// against 238 us staged), or short rows of at least 4.5 on average (the 3D
+// 7-point grid: 51.4 against 55.7 us direct, at 5 CTAs per SM; the 2D
+// 5-point grid, once a slot's last entries went as one batch: 25.0 against
+// 26.6 us, and 53.9 against 68.5 us for 64 fp32 systems on one 256^2 grid);
+// the direct form stays for shorter rows.  (The 64^2 5-point grid, launch
+// bound, measured 57.2k against 58.2k CG iterations/s sliced.)  The SPAI
+// factors take their own rule (build_spai).
 #ifndef SLA_SLICED_MINAVG_SHORT
-#define SLA_SLICED_MINAVG_SHORT 6.0
+#define SLA_SLICED_MINAVG_SHORT 4.5
 #endif
 static bool sliced_by_default(const sla_csr* h, const Layout& L, long long nnz) {
     const double avg = (double)nnz / (double)h->n;

@@ -2,9 +2,8 @@
 on the same seeded inputs, element by element, at sizes the oracle finishes
 in seconds (many warp groups and CTAs and a ragged tail), plus edge cases.
 
-Every product test runs with the default form (the direct, thread-per-row
-form for patterns whose rows have at most 16 entries, else a warp-staged
-form), the warp-staged forms (staged=True), the warp pipeline
+Every product test runs with the default form (by the row lengths the
+sliced, the direct thread-per-row or a warp-staged form), the warp-staged forms (staged=True), the warp pipeline
 (pipeline=True), the producer/consumer form (producer_consumer=True), the
 sliced form (sliced=True), the last three wherever they apply, and the
 warp-staged forms with every staged group summed split over the lanes
@@ -35,6 +34,7 @@ def _iters_ok(a, b):
 
 
 def _spmv_cases():
+    yield "poisson1d_5000", poisson_grid((5000,))
     yield "poisson2d_64", poisson_grid((64, 64))
     yield "poisson3d_24", poisson_grid((24, 24, 24))
     yield "diffusion_96", build("c2", N=96).A
@@ -77,7 +77,9 @@ def test_spmv_parity(cuda_device, name, A, dtype, mode):
         assert form == 6, form
     elif mode == "default" and name == "poisson3d_24":   # 7-point rows: the sliced form for short rows
         assert form == 7, form
-    elif mode == "default" and name in ("poisson2d_64", "diffusion_96"):   # 5-point rows: the direct form
+    elif mode == "default" and name in ("poisson2d_64", "diffusion_96"):   # 5-point rows: the short-row sliced form
+        assert form == 7, form
+    elif mode == "default" and name == "poisson1d_5000":   # 3-point rows: the direct form
         assert form == 5, form
     elif mode == "pipe" and name != "knn_3000":   # groups of 32 short rows fit the warp pipeline
         assert form == 3, form
