@@ -39,10 +39,19 @@ template <> struct IterMinCtas<float> { static constexpr int value = 4; };
 #define SLA_SLICED_CTAS_SHORT 5
 #endif
 __host__ __device__ constexpr bool sliced_form(int form) { return form == 6 || form == 7; }
+// fp32 systems (fp32 values, double-float vectors) in the short-row form
+// take 8 (32 registers, a few spilled): measured on 64 fp32 systems on one
+// 256^2 5-point grid, 5 / 6 / 8 CTAs per SM 570k / 578k / 595k
+// system-iterations/s (product 53.7 / 52.5 / 49.5 us; 7 compiles to the
+// same 32 registers as 8).  fp64 keeps 5 (6 slowed the 2D and 3D grids by
+// 6% and 3%).
+#ifndef SLA_SLICED_CTAS_SHORT_F32
+#define SLA_SLICED_CTAS_SHORT_F32 8
+#endif
 template <typename T, int FORM> struct ProductCtas {
     static constexpr int value = FORM == 5   ? SLA_DIRECT_CTAS
                                  : FORM == 6 ? SLA_SLICED_CTAS
-                                 : FORM == 7 ? SLA_SLICED_CTAS_SHORT
+                                 : FORM == 7 ? (sizeof(T) == 4 ? SLA_SLICED_CTAS_SHORT_F32 : SLA_SLICED_CTAS_SHORT)
                                              : IterMinCtas<T>::value;
 };
 
