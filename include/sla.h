@@ -193,10 +193,12 @@ sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered);
 /*
  * The same report for one matrix of the solves (no counterpart in the
  * pages): which = 0 the iteration matrix, 1 the SPAI factor G, 2 its
- * transpose G^T (built by the handle's first SPAI solve; SLA_ERR_INVALID
- * before that).  *split: 1 when its staged groups are summed split (see
- * sla_csr_layout).  Any output pointer may be NULL.  SLA_ERR_INVALID for a
- * null handle or another `which`.
+ * transpose G^T (built by the handle's first SPAI solve), 3 the matrix the
+ * BiCGStab products iterate on (built by the first BiCGStab solve), 4 its
+ * explicit transpose (built by the first BiCGStab adjoint); SLA_ERR_INVALID
+ * before those are built.  *split: 1 when its staged groups are summed
+ * split (see sla_csr_layout).  Any output pointer may be NULL.
+ * SLA_ERR_INVALID for a null handle or another `which`.
  */
 sla_status sla_csr_layout_of(sla_handle h, int which, int* form, int* ctas, int* split);
 

@@ -184,10 +184,11 @@ class CSRMatrix:
 
     def layout_of(self, which: str = "A") -> tuple[int, int, bool]:
         """(product form, CTAs per system, split group sums) of the iteration
-        matrix ("A") or, after a SPAI solve, of the factor "G" or "GT"."""
+        matrix ("A"); after a SPAI solve of the factor "G" or "GT"; after a
+        BiCGStab solve of its matrix "B", after its adjoint of "BT"."""
         f, g, b = C.c_int(), C.c_int(), C.c_int()
-        _check(_lib_handle().sla_csr_layout_of(self._h, {"A": 0, "G": 1, "GT": 2}[which], C.byref(f), C.byref(g),
-                                               C.byref(b)))
+        _check(_lib_handle().sla_csr_layout_of(self._h, {"A": 0, "G": 1, "GT": 2, "B": 3, "BT": 4}[which],
+                                               C.byref(f), C.byref(g), C.byref(b)))
         return f.value, g.value, bool(b.value)
 
     def update_values(self, values: torch.Tensor, stream=None):

@@ -167,7 +167,7 @@ __device__ __noinline__ double residual_unscaled_staged(const Mat& A, const doub
 template <int FORM>
 __device__ __forceinline__ double residual_unscaled(const Mat& A, const double* __restrict__ a0, const double* y,
                                                     const double* d, const double* __restrict__ b, double* dsm) {
-    if constexpr (FORM == 5) {
+    if constexpr (FORM == 5 || sliced_form(FORM)) {   // on the CSR arrays (a0 is CSR-ordered)
         double tr2 = 0.0;
         spmv_direct<double, double>(A, a0, GatherUnscaled{y, d}, [&](int i) { return b[i]; },
                                     [&](int, double s, double bi) { sq_acc(tr2, resid(bi, s)); });
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     if (ld_cg(&st->done)) return;
     extern __shared__ __align__(16) double dsm[];
     __shared__ double red[RED_DOUBLES];
-    av += ao; p += vo; v += vo; rh += vo; y += vo; b += vo;
+    av += val_offset<FORM>(A, sys, S.nnz); p += vo; v += vo; rh += vo; y += vo; b += vo;
     const bool check = ld_cg(&st->check) != 0;
     double tr2 = 0.0, sigma = 0.0;
     if (check) {
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(NT, (ProductCtas<double, FORM>::value))
     if (ld_cg(&st->done)) return;
     extern __shared__ __align__(16) double dsm[];
     __shared__ double red[RED_DOUBLES];
-    av += ao; s += vo; t += vo;
+    av += val_offset<FORM>(A, sys, S.nnz); s += vo; t += vo;
     double tt = 0.0, ts = 0.0;
     spmv_vec<double, FORM, double, double>(A, av, s, [&](int i) { return ld_vec(s + i); },
                                            [&](int i, double q, double si) {

@@ -227,6 +227,7 @@ struct sla_csr {
     bool sliced = false;        // SLA_SLICED: sliced product form where it applies
     int split = 0;              // SLA_SPLIT_ROWS: 1, SLA_ROW_WALK: -1, else chosen per matrix
     SellBufs sI, sG, sGT;
+    SellBufs sB, sT;            // sliced copies of the BiCGStab matrices (values refilled per solve)
 
     // BiCGStab (built on first use): the iteration matrix's layout with the
     // register / cp.async forms only (its values may be a handle-owned
@@ -1641,14 +1642,16 @@ static sla_status solve_impl(sla_csr* h, const T* b, T* x_user, const sla_pcg_op
 }
 
 // ===================================================================== BiCGStab
-// Dispatch over the register / cp.async staging forms and the direct form
-// (the BiCGStab product kernels are built for these only).
+// Dispatch over the register / cp.async staging forms, the direct form and
+// the sliced forms (the BiCGStab product kernels are built for these only).
 template <class F>
 static void with_form_rc(int form, F&& f) {
     switch (form) {
         case 0: f(std::integral_constant<int, 0>{}); break;
         case 1: f(std::integral_constant<int, 1>{}); break;
         case 5: f(std::integral_constant<int, 5>{}); break;
+        case 6: f(std::integral_constant<int, 6>{}); break;
+        case 7: f(std::integral_constant<int, 7>{}); break;
         default: f(std::integral_constant<int, 2>{}); break;
     }
 }
@@ -1673,14 +1676,25 @@ static void transpose_pattern(int n, const std::vector<int>& rp, const std::vect
 
 // Workspace of BiCGStab (and, for `transposed`, the explicit transpose of
 // the iteration matrix); built once per handle.  Its products take the
-// staged forms: on the 3D convection-diffusion system the direct form's
-// product was slower inside the BiCGStab iteration (71.9 against 65.1 us,
-// measured on B300), unlike in the CG iteration.
+// staged forms, or the sliced form where the CG products' default would
+// (a handle-owned sliced copy whose values bicg_impl refills from the
+// iterated values every solve).  Measured on B300, 3D convection-diffusion
+// system: the direct form's product was slower than the staged one inside
+// the BiCGStab iteration (71.9 against 65.1 us), unlike in the CG iteration.
+#ifndef SLA_BICG_SLICED
+#define SLA_BICG_SLICED 1
+#endif
+static bool bicg_sliced(const sla_csr* h, const Layout& L) {
+    return h->dt == SLA_F64 && SLA_BICG_SLICED && !h->pipeline && !h->ws && !h->staged &&
+           (h->sliced || sliced_by_default(h, L, h->nnz));
+}
 static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
     if (!h->bicg_ready) {
         TRY(h->rh.alloc(sizeof(double) * (size_t)h->n * h->batch));
-        h->LB = h->LI;
+        h->LB = h->LI;   // the CG layout's pattern analysis; its own form (and sliced copy) below
         TRY(set_form_any(h, &h->LB, false, sizeof(double), 0));
+        if (bicg_sliced(h, h->LB))
+            TRY(make_sliced_any(h, h->irp, h->ici, h->nnz, h->ivals, h->nnz, 8, &h->LB, h->sB, s));
         h->bicg_ready = true;
     }
     if (transposed && !h->tr_ready) {
@@ -1694,6 +1708,9 @@ static sla_status ensure_bicg(sla_csr* h, bool transposed, cudaStream_t s) {
         TRY(to_device(h->tsrc, src));
         TRY(h->tvals.alloc(sizeof(double) * (size_t)h->nnz * h->batch));
         TRY(choose_layout(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, &h->LT, false, sizeof(double), s, 0));
+        if (bicg_sliced(h, h->LT))
+            TRY(make_sliced_any(h, h->trp.as<int>(), h->tci.as<int>(), h->nnz, h->ivals, h->nnz, 8, &h->LT, h->sT,
+                                s));
         h->tr_ready = true;
     }
     return ensure_pstride(h);
@@ -1765,6 +1782,10 @@ static sla_status bicg_impl(sla_csr* h, bool transposed, const double* b, double
             TRY(launched());
         }
         itv = h->bvals.as<double>();
+    }
+    if (sliced_form(L.form)) {   // the sliced copy holds this solve's iterated values
+        TRY(sliced_values(h, transposed ? h->sT : h->sB, itv, h->nnz, 8, s));
+        itv = (const double*)L.sval;
     }
     GraphCache& gc = h->graph[3 + 2 * (transposed ? 1 : 0) + (pc == SLA_PC_JACOBI ? 1 : 0)];
     TRY(capture_graph(h, gc, k, 0.0, h->time_product, [&](cudaStream_t cs, int* nodes, cudaEvent_t e0,
@@ -2002,9 +2023,11 @@ sla_status sla_csr_layout(sla_handle h, int* form, int* ctas, int* reordered) {
 
 sla_status sla_csr_layout_of(sla_handle h, int which, int* form, int* ctas, int* split) {
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
-    if (which < 0 || which > 2) return fail(SLA_ERR_INVALID, "which = %d: 0, 1 or 2", which);
-    if (which > 0 && !h->spai_ready) return fail(SLA_ERR_INVALID, "no SPAI factor yet");
-    const Layout& L = which == 0 ? h->LI : which == 1 ? h->LG : h->LGT;
+    if (which < 0 || which > 4) return fail(SLA_ERR_INVALID, "which = %d: 0 to 4", which);
+    if ((which == 1 || which == 2) && !h->spai_ready) return fail(SLA_ERR_INVALID, "no SPAI factor yet");
+    if (which == 3 && !h->bicg_ready) return fail(SLA_ERR_INVALID, "no BiCGStab solve yet");
+    if (which == 4 && !h->tr_ready) return fail(SLA_ERR_INVALID, "no BiCGStab adjoint yet");
+    const Layout& L = which == 0 ? h->LI : which == 1 ? h->LG : which == 2 ? h->LGT : which == 3 ? h->LB : h->LT;
     if (form) *form = L.form;
     if (ctas) *ctas = L.gx;
     if (split) *split = L.bal && L.lanes == 1 && (L.form == 1 || L.form == 2) ? 1 : 0;

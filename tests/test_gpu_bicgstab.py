@@ -57,13 +57,23 @@ def _cases():
 CASES = list(_cases())
 
 
+# grid patterns whose BiCGStab products take the sliced form by default
+SLICED = ("convdiff2d_rot_96", "convdiff3d_25_odd", "cd3_24")
+
+
+@pytest.mark.parametrize("staged", [False, True], ids=["default", "staged"])
 @pytest.mark.parametrize("pc", ["none", "jacobi"])
 @pytest.mark.parametrize("name,A", CASES, ids=[c[0] for c in CASES])
-def test_bicgstab_parity(cuda_device, name, A, pc):
+def test_bicgstab_parity(cuda_device, name, A, pc, staged):
     tol = 1e-10
     b = rng.normal(21, 1, A.n)
-    M = make(A)
+    M = make(A, staged=staged)
     x, info = M.solve(torch.from_numpy(b).to(cuda_device), tol=tol, max_iter=20000, pc=pc, method="bicgstab")
+    form = M.layout_of("B")[0]
+    if staged:
+        assert form in (0, 1, 2), form
+    elif name in SLICED:
+        assert form in (6, 7), form
     xo, io = oracle.bicgstab(A, b, tol, max_iter=20000, pc=pc)
     assert io["status"] == "ok"
     assert info[0].status == "ok", info[0]
@@ -94,15 +104,17 @@ def test_bicgstab_batch_with_a_zero_rhs(cuda_device):
         assert info[1].iters == 0 and not xh[1].any()
 
 
+@pytest.mark.parametrize("staged", [False, True], ids=["default", "staged"])
 @pytest.mark.parametrize("pc", ["none", "jacobi"])
-def test_bicgstab_adjoint_parity(cuda_device, pc):
+def test_bicgstab_adjoint_parity(cuda_device, pc, staged):
     w = build("cd3", N=24)
-    M = make(w.A)
+    M = make(w.A, staged=staged)
     b = torch.from_numpy(w.b).to(cuda_device)
     g = torch.from_numpy(w.g).to(cuda_device)
     tol = 1e-10
     x, _ = M.solve(b, tol=tol, max_iter=20000, pc=pc, method="bicgstab")
     dldb, dlda, info = M.adjoint(x, g, tol=tol, max_iter=20000, pc=pc, method="bicgstab")
+    assert (M.layout_of("BT")[0] in (0, 1, 2)) == staged
     xh = x.cpu().numpy()
     lb_o, la_o, io = oracle.bicgstab_adjoint(w.A, xh, w.g, tol, max_iter=20000, pc=pc)
     lb, la = dldb.cpu().numpy(), dlda.cpu().numpy()
