@@ -370,7 +370,9 @@ sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream);
  * B [kb][n] (1 <= ka, kb <= 64), into d_G (device double [ka][kb]).
  * mode 0: every entry; mode 1 (B = A, ka = kb; d_B may be NULL): only
  * i <= j, mirrored; mode 2 (B = A): only the diagonal, the squared norms of
- * A's vectors, into d_G[0..ka).  Sums are fp64, split over CTAs and added in
+ * A's vectors, into d_G[0..ka); mode 3 (ka = kb, for blocks whose product
+ * is symmetric, such as S and A S for a symmetric A): only i <= j of A B^T,
+ * mirrored.  Sums are fp64, split over CTAs and added in
  * a fixed order (deterministic).  d_work: caller-owned device scratch of at
  * least the number of doubles sla_block_gram_work returns for the same
  * (ka, kb, mode, n).  Two kernels; does not synchronise.  SLA_ERR_INVALID

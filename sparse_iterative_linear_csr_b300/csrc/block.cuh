@@ -20,14 +20,19 @@ constexpr int GRAM_MAXK = 64;    // largest block of either operand
 constexpr int GRAM_PER_THREAD = (GRAM_MAXK * GRAM_MAXK + NT - 1) / NT;
 
 // Modes of the Gram kernels: every entry, the upper triangle (A = B,
-// mirrored), or the diagonal only (A = B: the squared norms of A's vectors).
-enum : int { GRAM_FULL = 0, GRAM_SYM = 1, GRAM_DIAG = 2 };
+// mirrored), the diagonal only (A = B: the squared norms of A's vectors), or
+// the upper triangle of A B^T for two blocks whose product is symmetric
+// (such as S^T (A S) for a symmetric A), mirrored.
+enum : int { GRAM_FULL = 0, GRAM_SYM = 1, GRAM_DIAG = 2, GRAM_UPPER = 3 };
+__host__ __device__ constexpr bool gram_triangle(int mode) { return mode == GRAM_SYM || mode == GRAM_UPPER; }
+__host__ __device__ constexpr bool gram_one_block(int mode) { return mode == GRAM_SYM || mode == GRAM_DIAG; }
 __host__ __device__ constexpr int gram_pairs(int ka, int kb, int mode) {
-    return mode == GRAM_FULL ? ka * kb : mode == GRAM_SYM ? ka * (ka + 1) / 2 : ka;
+    return mode == GRAM_FULL ? ka * kb : gram_triangle(mode) ? ka * (ka + 1) / 2 : ka;
 }
 
-// Entry p of the result: (i, j) = (p / kb, p % kb); in GRAM_SYM mode only
-// i <= j, enumerated row by row; in GRAM_DIAG mode (p, p).
+// Entry p of the result: (i, j) = (p / kb, p % kb); in GRAM_SYM and
+// GRAM_UPPER modes only i <= j, enumerated row by row; in GRAM_DIAG mode
+// (p, p).
 __device__ __forceinline__ void gram_pair(int p, int ka, int kb, int mode, int& i, int& j) {
     if (mode == GRAM_FULL) {
         i = p / kb;
@@ -55,7 +60,7 @@ __global__ void __launch_bounds__(NT) k_gram_partial(int ka, int kb, long long n
                                                       double* __restrict__ part) {
     __shared__ double sA[GRAM_MAXK][GRAM_COLS + 1];
     __shared__ double sB[GRAM_MAXK][GRAM_COLS + 1];
-    const bool sym = mode != GRAM_FULL;   // one operand: B = A
+    const bool sym = gram_one_block(mode);   // one operand: B = A
     const int npairs = gram_pairs(ka, kb, mode);
     double acc[GRAM_PER_THREAD];
     int pi[GRAM_PER_THREAD], pj[GRAM_PER_THREAD];
@@ -102,7 +107,8 @@ __global__ void __launch_bounds__(NT) k_gram_partial(int ka, int kb, long long n
 }
 
 // G = the sum of the partials over the CTAs, in CTA order (deterministic);
-// GRAM_SYM mirrors the upper triangle; GRAM_DIAG writes G[i] (a vector).
+// GRAM_SYM and GRAM_UPPER mirror the upper triangle; GRAM_DIAG writes G[i]
+// (a vector).
 __global__ void __launch_bounds__(NT) k_gram_reduce(int ka, int kb, int mode, int nparts,
                                                      const double* __restrict__ part, double* __restrict__ G) {
     const int npairs = gram_pairs(ka, kb, mode);
@@ -116,7 +122,7 @@ __global__ void __launch_bounds__(NT) k_gram_reduce(int ka, int kb, int mode, in
         int i, j;
         gram_pair(p, ka, kb, mode, i, j);
         G[i * kb + j] = s;
-        if (mode == GRAM_SYM) G[j * kb + i] = s;
+        if (gram_triangle(mode)) G[j * kb + i] = s;
     }
 }
 

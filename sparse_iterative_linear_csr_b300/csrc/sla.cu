@@ -2270,7 +2270,7 @@ sla_status sla_block_gram_work(int ka, int kb, int mode, long long n, long long*
     if (!doubles) return fail(SLA_ERR_INVALID, "null output");
     if (ka < 1 || kb < 1 || ka > GRAM_MAXK || kb > GRAM_MAXK)
         return fail(SLA_ERR_INVALID, "block sizes must be in [1, %d] (got %d, %d)", GRAM_MAXK, ka, kb);
-    if (mode != GRAM_FULL && mode != GRAM_SYM && mode != GRAM_DIAG)
+    if (mode != GRAM_FULL && mode != GRAM_SYM && mode != GRAM_DIAG && mode != GRAM_UPPER)
         return fail(SLA_ERR_INVALID, "unknown mode %d", mode);
     if (mode != GRAM_FULL && ka != kb) return fail(SLA_ERR_INVALID, "this mode needs ka == kb");
     if (n < 0) return fail(SLA_ERR_INVALID, "n must be >= 0");
@@ -2282,7 +2282,7 @@ sla_status sla_block_gram(int ka, int kb, long long n, const double* d_A, const 
                           double* d_work, long long work_doubles, void* stream) {
     long long need = 0;
     TRY(sla_block_gram_work(ka, kb, mode, n, &need));
-    if (!d_A || !d_G || (mode == GRAM_FULL && !d_B) || !d_work) return fail(SLA_ERR_INVALID, "null pointer");
+    if (!d_A || !d_G || (!gram_one_block(mode) && !d_B) || !d_work) return fail(SLA_ERR_INVALID, "null pointer");
     if (work_doubles < need) return fail(SLA_ERR_INVALID, "workspace too small (%lld < %lld doubles)", work_doubles, need);
     cudaStream_t s = (cudaStream_t)stream;
     if (n == 0) {
@@ -2290,7 +2290,7 @@ sla_status sla_block_gram(int ka, int kb, long long n, const double* d_A, const 
         return SLA_OK;
     }
     const int grid = gram_grid(n);
-    k_gram_partial<<<grid, NT, 0, s>>>(ka, kb, n, d_A, mode == GRAM_FULL ? d_B : d_A, mode, d_work);
+    k_gram_partial<<<grid, NT, 0, s>>>(ka, kb, n, d_A, gram_one_block(mode) ? d_A : d_B, mode, d_work);
     TRY(launched());
     const int npairs = gram_pairs(ka, kb, mode);
     k_gram_reduce<<<(npairs + NT - 1) / NT, NT, 0, s>>>(ka, kb, mode, grid, d_work, d_G);

@@ -43,13 +43,15 @@ import ctypes as C
 
 from . import CSRMatrix, _check, _lib_handle, _ptr, _stream
 
-GRAM_FULL, GRAM_SYM, GRAM_DIAG = 0, 1, 2
+GRAM_FULL, GRAM_SYM, GRAM_DIAG, GRAM_UPPER = 0, 1, 2, 3
 
 
 def gram(A: torch.Tensor, B: torch.Tensor | None = None, mode: int | None = None) -> torch.Tensor:
     """A B^T for blocks A [ka, n], B [kb, n] (fp64, CUDA) on the library:
-    mode GRAM_FULL (default with B), GRAM_SYM (B = A, the default without B)
-    or GRAM_DIAG (B = A: the squared norms of A's vectors, a [ka] vector)."""
+    mode GRAM_FULL (default with B), GRAM_SYM (B = A, the default without B),
+    GRAM_DIAG (B = A: the squared norms of A's vectors, a [ka] vector) or
+    GRAM_UPPER (ka = kb, A B^T known to be symmetric: the upper triangle,
+    mirrored)."""
     if mode is None:
         mode = GRAM_SYM if B is None else GRAM_FULL
     A = A.contiguous()
@@ -215,7 +217,7 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
                 blocks.append((P, AP))
         S = torch.cat([b for b, _ in blocks])
         AS = torch.cat([ab for _, ab in blocks])
-        H = gram(S, AS).cpu().numpy()
+        H = gram(S, AS, mode=GRAM_UPPER).cpu().numpy()   # S^T A S is symmetric
         th, Cn = np.linalg.eigh((H + H.T) / 2)
         Cn = torch.from_numpy(Cn[:, :m]).to(dev)
         # new directions: the update without its component in the old block

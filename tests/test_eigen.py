@@ -110,9 +110,10 @@ def test_eigenvalue_gradient_against_finite_differences(cuda_device):
 @pytest.mark.parametrize("ka,kb,n", [(1, 1, 1), (5, 7, 1000), (12, 36, 33333), (64, 64, 257), (36, 36, 100000)])
 def test_block_gram_and_update_match_numpy(cuda_device, ka, kb, n):
     """The library's block kernels against numpy's fp64 products: G = A B^T
-    (full, upper triangle mirrored, diagonal) and Y = C^T S + Yin, in place
-    too; ragged column counts exercise the staged chunks' tails."""
-    from sparse_iterative_linear_csr_b300.eigen import GRAM_DIAG, gram, update
+    (full, upper triangle mirrored for one block and for two, diagonal) and
+    Y = C^T S + Yin, in place too; ragged column counts exercise the staged
+    chunks' tails."""
+    from sparse_iterative_linear_csr_b300.eigen import GRAM_DIAG, GRAM_UPPER, gram, update
     g = np.random.default_rng(ka * 1000 + kb)
     A = g.standard_normal((ka, n))
     B = g.standard_normal((kb, n))
@@ -125,6 +126,12 @@ def test_block_gram_and_update_match_numpy(cuda_device, ka, kb, n):
     assert np.array_equal(Gs, Gs.T) and np.abs(Gs - A @ A.T).max() <= 1e-12 * scale * 10
     d = gram(Ad, mode=GRAM_DIAG).cpu().numpy()
     assert np.abs(d - (A * A).sum(1)).max() <= 1e-12 * scale * 10
+    if ka == kb:
+        Gu = gram(Ad, Bd, mode=GRAM_UPPER).cpu().numpy()
+        full = A @ B.T
+        iu = np.triu_indices(ka)
+        assert np.array_equal(Gu, Gu.T)
+        assert np.abs(Gu[iu] - full[iu]).max() <= 1e-12 * scale * 10
     Cm = g.standard_normal((kb, ka))
     Y = update(torch.from_numpy(Cm).to(cuda_device), Bd).cpu().numpy()
     assert np.abs(Y - Cm.T @ B).max() <= 1e-12 * kb
@@ -142,4 +149,5 @@ def test_block_kernels_reject_bad_sizes(cuda_device):
     assert lib.sla_block_gram_work(65, 1, 0, 10, C.byref(need)) == _lib.SLA_ERR_INVALID
     assert lib.sla_block_gram_work(3, 4, 1, 10, C.byref(need)) == _lib.SLA_ERR_INVALID
     assert lib.sla_block_gram_work(3, 3, 7, 10, C.byref(need)) == _lib.SLA_ERR_INVALID
+    assert lib.sla_block_gram_work(3, 4, 3, 10, C.byref(need)) == _lib.SLA_ERR_INVALID
     assert lib.sla_block_update(0, 3, 10, None, None, None, None, None) == _lib.SLA_ERR_INVALID
