@@ -2092,16 +2092,22 @@ sla_status sla_spmm(sla_handle h, const void* d_X, void* d_Y, int k, void* strea
     cudaStream_t s = (cudaStream_t)stream;
     Sys S = sys_of(h);
     S.nnz = 0;   // every column of the block is multiplied by the same values
-    const Mat A = mat_A(h);
-    const dim3 g(h->LA.gx, k);
-    const size_t sm = h->LA.smem;
-    with_form(h->LA.form, [&](auto f) {
+    // the sliced copy of the iteration matrix serves A itself when the
+    // handle does not reorder (as in sla_spmv)
+    const bool sl = !h->reordered && sliced_form(h->LI.form);
+    const Layout& L = sl ? h->LI : h->LA;
+    Mat A = sl ? mat_I(h) : mat_A(h);
+    A.vstride = 0;   // likewise for the sliced values
+    const void* vals = sl ? L.sval : h->vals;
+    const dim3 g(L.gx, k);
+    const size_t sm = L.smem;
+    with_form(L.form, [&](auto f) {
         constexpr int F = decltype(f)::value;
         if (h->dt == SLA_F64)
-            k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)h->vals, (const double*)d_X, (double*)d_Y,
+            k_spmv<double, F><<<g, NT, sm, s>>>(A, S, (const double*)vals, (const double*)d_X, (double*)d_Y,
                                                 nullptr);
         else
-            k_spmv<float, F><<<g, NT, sm, s>>>(A, S, (const float*)h->vals, (const float*)d_X, (float*)d_Y,
+            k_spmv<float, F><<<g, NT, sm, s>>>(A, S, (const float*)vals, (const float*)d_X, (float*)d_Y,
                                                nullptr);
     });
     return launched();

@@ -210,10 +210,12 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
         AW = Amul(W) if W.shape[0] else W
         blocks = [(X, AX), (W, AW)]
         if P is not None:
-            P, AP = P[active], AP[active]
-            P, AP = _orth_against(P, AP, blocks)
-            P, AP = _orthonormal(P, AP, eps)
+            # P alone through the corrections, then A P by one block product
+            # (cheaper than carrying A P through every correction, and exact)
+            P, _ = _orth_against(P[active], None, blocks, same=True)
+            P, _ = _orthonormal(P, None, eps, same=True)
             if P.shape[0]:
+                AP = Amul(P)
                 blocks.append((P, AP))
         S = torch.cat([b for b, _ in blocks])
         AS = torch.cat([ab for _, ab in blocks])
