@@ -310,6 +310,43 @@ def test_update_values(cuda_device):
     assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
 
 
+def test_sliced_windows_batched(cuda_device):
+    """Three systems on one kNN pattern (rows sorted by length within
+    256-row windows, so the sliced products run a warp per window): the
+    product, the fused product and dot, the Jacobi-PCG solve and BiCGStab
+    per system against the oracle.  BiCGStab's iteration count on this
+    symmetric problem moves with the rounding order (system 0: oracle 132,
+    sliced 133, staged 142 iterations, measured), so for it x, the status
+    and the true residual are checked, not the count."""
+    A1 = build("c5", npoints=5000).A
+    scale = np.array([1.0, 1.25, 1.5])
+    A = CSR(A1.n, A1.row_ptr, A1.col_idx, np.stack([A1.vals * s for s in scale]))
+    M = make(A)
+    assert M.layout()[0] == 6
+    g = np.random.default_rng(17)
+    x = g.standard_normal((3, A.n))
+    xd = torch.from_numpy(x).to(cuda_device)
+    y = M.matvec(xd).cpu().numpy()
+    yd, dots = M.matvec_dot(xd)
+    assert np.array_equal(yd.cpu().numpy(), y)
+    for s in range(3):
+        yo = oracle.spmv(A, x[s], system=s)
+        ref = oracle.spmv(CSR(A.n, A.row_ptr, A.col_idx, np.abs(A.vals[s])), np.abs(x[s]))
+        assert np.all(np.abs(y[s] - yo) <= 1e-12 * ref)
+        assert abs(dots[s].item() - float(x[s] @ y[s])) <= 1e-12 * float(np.abs(x[s]) @ np.abs(y[s]))
+    b = g.standard_normal((3, A.n))
+    bd = torch.from_numpy(b).to(cuda_device)
+    for method in ("cg", "bicgstab"):
+        xs, info = M.solve(bd, tol=1e-10, max_iter=5000, pc="jacobi", method=method)
+        xo, io = (oracle.pcg if method == "cg" else oracle.bicgstab)(A, b, 1e-10, max_iter=5000, pc="jacobi")
+        for s in range(3):
+            assert info[s].status == "ok" and info[s].rel_res_true <= 1e-10, (method, s)
+            if method == "cg":
+                assert _iters_ok(info[s].iters, io[s]["iters"]), (method, s)
+            assert rel(xs[s].cpu().numpy(), xo[s]) <= 1e-6
+    assert M.layout_of("B")[0] == 6
+
+
 @pytest.mark.parametrize("reorder,sliced", [(False, False), (True, False), (False, True), (True, True)])
 def test_spai_follows_update_values(cuda_device, reorder, sliced):
     """After a SPAI solve, new values (a symmetric scaling D A D, same
