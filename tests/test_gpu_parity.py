@@ -310,6 +310,28 @@ def test_update_values(cuda_device):
     assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
 
 
+@pytest.mark.parametrize("pc", ["none", "jacobi"])
+def test_batch_with_a_frozen_system(cuda_device, pc):
+    """A batch of 8 fp32 systems on one 5-point grid (the short-row sliced
+    form).  System 3 has b = 0 and freezes at the start while the others
+    iterate; every system's x and iteration count against the oracle, and
+    its reported true residual."""
+    w = build("c3", N=40, batch=8)
+    b = w.b.copy()
+    b[3] = 0.0
+    M = make(w.A)
+    assert M.layout()[0] in (6, 7)
+    x, info = M.solve(torch.from_numpy(b).to(cuda_device), tol=w.tol, max_iter=20000, pc=pc, poll_k=16)
+    xo, io = oracle.pcg(w.A, b, w.tol, max_iter=20000, pc=pc)
+    xh = x.cpu().numpy()
+    assert info[3].iters == 0 and not xh[3].any()
+    for s in range(8):
+        assert info[s].status == "ok" and io[s]["status"] == "ok"
+        assert _iters_ok(info[s].iters, io[s]["iters"]), (s, info[s].iters, io[s]["iters"])
+        assert rel(xh[s], xo[s]) <= 1e-6
+        assert info[s].rel_res_true <= w.tol
+
+
 def test_sliced_windows_batched(cuda_device):
     """Three systems on one kNN pattern (rows sorted by length within
     256-row windows, so the sliced products run a warp per window): the
