@@ -212,8 +212,14 @@ def test_bicgstab_breakdown_and_invalid(cuda_device):
     A = convection_diffusion((8, 8), (1.0, 1.0))
     M = make(A)
     tb = torch.ones(A.n, dtype=torch.float64, device=cuda_device)
+    for which in ("B", "BT", "G", "GT"):   # not built before their first solve
+        with pytest.raises(SLAError):
+            M.layout_of(which)
     with pytest.raises(SLAError):      # SPAI is for SPD systems
         M.solve(tb, pc="spai", method="bicgstab")
+    x, _ = M.solve(tb, method="bicgstab")
+    M.adjoint(x, tb, method="bicgstab")
+    assert M.layout_of("B")[0] in (0, 1, 2, 5, 6, 7) and M.layout_of("BT")[0] in (0, 1, 2, 5, 6, 7)
     A32 = CSR(A.n, A.row_ptr, A.col_idx, A.vals.astype(np.float32))
     M32 = make(A32)
     with pytest.raises(SLAError):      # fp64 only
