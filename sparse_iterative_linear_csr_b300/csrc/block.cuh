@@ -55,6 +55,9 @@ __device__ __forceinline__ void gram_pair(int p, int ka, int kb, int mode, int& 
 
 // Partial Gram matrices: CTA c sums the column chunks c, c + gridDim.x, ...
 // and writes its ka x kb (or upper-triangle) partial sums to part[c][...].
+// PT: result entries per thread; the launch takes the fewest that cover the
+// pairs, so small Gram matrices hold fewer registers and more CTAs fit.
+template <int PT>
 __global__ void __launch_bounds__(NT) k_gram_partial(int ka, int kb, long long n, const double* __restrict__ A,
                                                       const double* __restrict__ B, int mode,
                                                       double* __restrict__ part) {
@@ -62,10 +65,10 @@ __global__ void __launch_bounds__(NT) k_gram_partial(int ka, int kb, long long n
     __shared__ double sB[GRAM_MAXK][GRAM_COLS + 1];
     const bool sym = gram_one_block(mode);   // one operand: B = A
     const int npairs = gram_pairs(ka, kb, mode);
-    double acc[GRAM_PER_THREAD];
-    int pi[GRAM_PER_THREAD], pj[GRAM_PER_THREAD];
+    double acc[PT];
+    int pi[PT], pj[PT];
 #pragma unroll
-    for (int q = 0; q < GRAM_PER_THREAD; ++q) {
+    for (int q = 0; q < PT; ++q) {
         acc[q] = 0.0;
         const int p = threadIdx.x + q * NT;
         if (p < npairs) gram_pair(p, ka, kb, mode, pi[q], pj[q]);
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(NT) k_gram_partial(int ka, int kb, long long n
         __syncthreads();
         const double(*tb)[GRAM_COLS + 1] = sym ? sA : sB;
 #pragma unroll
-        for (int q = 0; q < GRAM_PER_THREAD; ++q) {
+        for (int q = 0; q < PT; ++q) {
             if (threadIdx.x + q * NT >= npairs) break;
             const double* ra = sA[pi[q]];
             const double* rb = tb[pj[q]];
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(NT) k_gram_partial(int ka, int kb, long long n
         }
     }
 #pragma unroll
-    for (int q = 0; q < GRAM_PER_THREAD; ++q) {
+    for (int q = 0; q < PT; ++q) {
         const int p = threadIdx.x + q * NT;
         if (p < npairs) part[(size_t)blockIdx.x * npairs + p] = acc[q];
     }

@@ -2263,11 +2263,18 @@ sla_status sla_fp64_fma_rate(double* fma_per_s, void* stream) {
 }
 
 // ===================================================================== block arithmetic
+// CTAs per SM of the Gram kernel's grid.  Measured on B300 (LOBPCG on the
+// 128^3 Laplacian, k = 8, block kept full, ms per iteration): 2 / 3 / 4 CTAs
+// per SM 24.9 / 22.8 / 22.3 (the Gram matrices of LOBPCG need at most 4
+// result entries per thread: 64 registers, 4 CTAs resident).
+#ifndef SLA_GRAM_CTAS
+#define SLA_GRAM_CTAS 4
+#endif
 static int gram_grid(long long n) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long chunks = (n + GRAM_COLS - 1) / GRAM_COLS;
-    long long g = 2LL * sms;
+    long long g = (long long)SLA_GRAM_CTAS * sms;
     if (g > chunks) g = chunks;
     return (int)(g < 1 ? 1 : g);
 }
@@ -2296,7 +2303,12 @@ sla_status sla_block_gram(int ka, int kb, long long n, const double* d_A, const 
         return SLA_OK;
     }
     const int grid = gram_grid(n);
-    k_gram_partial<<<grid, NT, 0, s>>>(ka, kb, n, d_A, gram_one_block(mode) ? d_A : d_B, mode, d_work);
+    const double* B = gram_one_block(mode) ? d_A : d_B;
+    const int ppt = (gram_pairs(ka, kb, mode) + NT - 1) / NT;   // result entries per thread
+    if (ppt <= 2) k_gram_partial<2><<<grid, NT, 0, s>>>(ka, kb, n, d_A, B, mode, d_work);
+    else if (ppt <= 4) k_gram_partial<4><<<grid, NT, 0, s>>>(ka, kb, n, d_A, B, mode, d_work);
+    else if (ppt <= 8) k_gram_partial<8><<<grid, NT, 0, s>>>(ka, kb, n, d_A, B, mode, d_work);
+    else k_gram_partial<GRAM_PER_THREAD><<<grid, NT, 0, s>>>(ka, kb, n, d_A, B, mode, d_work);
     TRY(launched());
     const int npairs = gram_pairs(ka, kb, mode);
     k_gram_reduce<<<(npairs + NT - 1) / NT, NT, 0, s>>>(ka, kb, mode, grid, d_work, d_G);
