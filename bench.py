@@ -523,34 +523,61 @@ def measure(args, name, dev, world, rank, stream, lib, with_cpu, e2e_steps, fma_
             it4 / A.batch * iters / (ms * 1e-3) / 1e9) / peak
 
     if e2e_steps > 0:
-        # end to end through the public API with host buffers: H2D of the
-        # step's inputs (values, b, g) from pinned memory, solve + adjoint,
-        # D2H of x, dL/db and dL/dA into pinned memory, all inside the timed
-        # region.
+        # end to end through the public API with host buffers: every step
+        # copies its inputs (values, b, g) in from pinned memory and its
+        # results (x, dL/db, dL/dA) out into pinned memory, all inside the
+        # timed region.  The copies run on their own streams into and out of
+        # double buffers: step k+1's inputs go in while step k computes, and
+        # step k's results come out while step k+1 computes (a solve returns
+        # once it has finished, so only the first upload and the last
+        # download are not overlapped).
         h_vals = vals.cpu().pin_memory()
         h_b = b.cpu().pin_memory()
         h_g = g.cpu().pin_memory()
-        d_vals2 = torch.empty_like(vals)
-        o_x = torch.empty_like(h_b).pin_memory()
-        o_lb = torch.empty_like(h_b).pin_memory()
-        o_la = torch.empty_like(h_vals).pin_memory()
+        d_in = [(torch.empty_like(vals), torch.empty_like(b), torch.empty_like(g)) for _ in range(2)]
+        o_out = [(torch.empty_like(h_b).pin_memory(), torch.empty_like(h_b).pin_memory(),
+                  torch.empty_like(h_vals).pin_memory()) for _ in range(2)]
         h2d = h_vals.numel() * h_vals.element_size() + 2 * h_b.numel() * h_b.element_size()
         d2h = 2 * h_b.numel() * h_b.element_size() + h_vals.numel() * h_vals.element_size()
+        up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        comp_s = torch.cuda.current_stream(dev)
+
+        def upload(k):
+            dv, dbk, dgk = d_in[k % 2]
+            with torch.cuda.stream(up_s):
+                dv.copy_(h_vals, non_blocking=True)
+                dbk.copy_(h_b, non_blocking=True)
+                dgk.copy_(h_g, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(up_s)
+            return ev
+
         barrier()
         t0 = time.perf_counter()
         e2e_iters = 0
-        for _ in range(e2e_steps):
-            d_vals2.copy_(h_vals, non_blocking=True)
-            db = h_b.to(dev, non_blocking=True)
-            dg = h_g.to(dev, non_blocking=True)
-            M.update_values(d_vals2)
-            xx, i1 = M.solve(db, **kw)
-            lb, la, i2 = M.adjoint(xx, dg, **kw)
-            o_x.copy_(xx, non_blocking=True)
-            o_lb.copy_(lb, non_blocking=True)
-            o_la.copy_(la, non_blocking=True)
-            torch.cuda.synchronize()
+        ev_next = upload(0)
+        for k in range(e2e_steps):
+            ev_in = ev_next
+            if k + 1 < e2e_steps:   # into the other buffers (step k-1 has finished with them)
+                ev_next = upload(k + 1)
+            comp_s.wait_event(ev_in)
+            dv, dbk, dgk = d_in[k % 2]
+            M.update_values(dv)
+            xx, i1 = M.solve(dbk, **kw)
+            lb, la, i2 = M.adjoint(xx, dgk, **kw)
+            ox, olb, ola = o_out[k % 2]
+            down_s.wait_stream(comp_s)
+            with torch.cuda.stream(down_s):
+                ox.copy_(xx, non_blocking=True)
+                olb.copy_(lb, non_blocking=True)
+                ola.copy_(la, non_blocking=True)
+            # the results' memory is reused only once their copies are done
+            # (downloads into one host buffer are ordered on down_s)
+            for t_ in (xx, lb, la):
+                t_.record_stream(down_s)
+            del xx, lb, la
             e2e_iters += sum(i.iters for i in i1) + sum(i.iters for i in i2)
+        torch.cuda.synchronize()
         e2e_ms, e2e_iters_all = aggregate((time.perf_counter() - t0) * 1000.0, e2e_iters, world, dev)
         out["e2e"] = {"value": e2e_iters_all / (e2e_ms / 1000.0), "unit": "iterations/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -573,7 +600,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--poll-k", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--warp-pipeline", action="store_true",
                     help="use the warp-pipeline product where it applies")
     ap.add_argument("--producer-consumer", action="store_true",

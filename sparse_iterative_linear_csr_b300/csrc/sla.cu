@@ -185,6 +185,11 @@ struct sla_csr {
     DevBuf perm, iperm;        // int[n]: new -> old row, old -> new row
     DevBuf prp, pci, psrc;     // permuted pattern; source entry of every permuted entry
     DevBuf pvals;              // permuted values [batch][nnz]
+    // Scratch of a values update and the SPAI refresh, kept across calls: a
+    // buffer freed per call (cudaFree) would synchronise the whole device,
+    // also the caller's copies in flight on other streams.
+    DevBuf derr;               // one int: error bits of the diagonal and SPAI value kernels
+    DevBuf dorig;              // [batch][n] diagonal in the caller's order (SPAI, reordered handles)
     DevBuf ptmp;               // 2 x [batch][n] values: permuted right-hand side / initial guess, result
     bool vals_aligned = false;  // values 16-byte aligned for every system (bulk-copy forms)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
@@ -1032,8 +1037,8 @@ static sla_status make_reordered(sla_csr* h, cudaStream_t s) {
 }
 
 static sla_status compute_diag(sla_csr* h, cudaStream_t s) {
-    DevBuf err;
-    TRY(err.alloc(sizeof(int)));
+    if (!h->derr.p) TRY(h->derr.alloc(sizeof(int)));
+    DevBuf& err = h->derr;
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
     const int g = (h->n + 255) / 256 < 4096 ? (h->n + 255) / 256 : 4096;
     if (h->dt == SLA_F64)
@@ -1064,13 +1069,13 @@ static sla_status spai_values(sla_csr* h, cudaStream_t s, bool fill_only = false
     if (h->diag_err & ERR_DIAG_SIGN) return fail(SLA_ERR_INVALID, "SPAI needs a positive diagonal");
     const int n = h->n;
     const int g = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
-    DevBuf err;
-    TRY(err.alloc(sizeof(int)));
+    if (!h->derr.p) TRY(h->derr.alloc(sizeof(int)));
+    DevBuf& err = h->derr;
     CU(cudaMemsetAsync(err.p, 0, sizeof(int), s));
-    DevBuf dorig;
+    DevBuf& dorig = h->dorig;
     const double* dbase = h->diag.as<double>();
     if (h->reordered) {
-        TRY(dorig.alloc(sizeof(double) * (size_t)n * h->batch));
+        if (dorig.bytes < sizeof(double) * (size_t)n * h->batch) TRY(dorig.alloc(sizeof(double) * (size_t)n * h->batch));
         TRY(gather_map(8, n, h->batch, h->iperm.as<int>(), h->diag.p, n, dorig.p, n, s));
         dbase = dorig.as<double>();
     }
@@ -2038,10 +2043,24 @@ sla_status sla_csr_update_values(sla_handle h, const void* d_vals, void* stream)
     if (!h) return fail(SLA_ERR_INVALID, "null handle");
     if (!d_vals && h->nnz > 0) return fail(SLA_ERR_INVALID, "null values");
     cudaStream_t s = (cudaStream_t)stream;
+    const bool moved = d_vals != h->vals;
     h->vals = d_vals;
     h->spai_stale = true;   // G, G^T values recomputed by the next SPAI solve
-    for (auto& g : h->graph) g.reset();
+    // The CUDA graphs hold the pointers their kernels read.  Rebuilt: all of
+    // them when the layout changes (below); when the caller's values moved,
+    // those that read them -- CG on neither a permuted nor a sliced copy,
+    // BiCGStab on A (its unsliced product and its Jacobi residual check)
+    // unless the handle reorders.  The handle's own copies (permuted,
+    // sliced, G, G^T, the transpose) keep their buffers and are refreshed
+    // in place.
+    if (moved && !h->reordered) {
+        if (!sliced_form(h->LI.form))
+            for (int g = 0; g < 3; ++g) h->graph[g].reset();
+        h->graph[3].reset();
+        h->graph[4].reset();
+    }
     if (vals_aligned(h, d_vals) != h->vals_aligned) {
+        for (auto& g : h->graph) g.reset();
         h->vals_aligned = !h->vals_aligned;
         TRY(set_form_any(h, &h->LA, h->vals_aligned, h->es));
         if (!h->reordered) {

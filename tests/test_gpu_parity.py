@@ -298,16 +298,24 @@ def test_repeat_solves_are_deterministic(cuda_device, pc):
     assert i1[0].iters == i2[0].iters and torch.equal(x1, x2)
 
 
-def test_update_values(cuda_device):
+@pytest.mark.parametrize("staged", [False, True], ids=["sliced", "staged"])
+def test_update_values(cuda_device, staged):
+    """New values at a new address after a solve (the CUDA graphs that read
+    the caller's values are rebuilt: the staged form's; the sliced copy's
+    are refreshed in place): the next solve follows the new matrix."""
     w = build("c2", N=48)
-    M = make(w.A)
+    M = make(w.A, staged=staged)
+    assert (M.layout()[0] in (0, 1, 2)) == staged
     b = torch.from_numpy(w.b).to(cuda_device)
+    for pc in ("jacobi", "spai"):        # graphs captured on the first values
+        M.solve(b, tol=1e-10, pc=pc)
     v2 = M.values * 2.0
     M.update_values(v2)
-    x, info = M.solve(b, tol=1e-10, pc="spai")
     A2 = CSR(w.A.n, w.A.row_ptr, w.A.col_idx, w.A.vals * 2.0)
-    xo, io = oracle.pcg(A2, w.b, 1e-10, pc="spai", eps=1e-3)
-    assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6
+    for pc in ("jacobi", "spai"):
+        x, info = M.solve(b, tol=1e-10, pc=pc)
+        xo, io = oracle.pcg(A2, w.b, 1e-10, pc=pc, eps=1e-3)
+        assert _iters_ok(info[0].iters, io["iters"]) and rel(x.cpu().numpy(), xo) <= 1e-6, pc
 
 
 @pytest.mark.parametrize("pc", ["none", "jacobi"])
