@@ -280,38 +280,46 @@ __global__ void k_tri_count(int n, const int* __restrict__ rp, const int* __rest
     }
 }
 
+// rs[i] = 1 / sqrt(A_ii): the factor's entries are G_ii = rs_i and
+// G_ij = -A_ij rs_i rs_j / 2, so each entry costs two products instead of a
+// square root and a division (both long sequences on the fp64 pipe).
+__global__ void k_rsqrt_diag(int n, const double* __restrict__ diag, double* __restrict__ rs) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        rs[i] = 1.0 / sqrt(diag[i]);
+}
+
 template <typename T, typename GV>
 __global__ void k_fill_G(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
-                         const double* __restrict__ diag, const int* __restrict__ grp, int* gci, GV* gv) {
+                         const double* __restrict__ rs, const int* __restrict__ grp, int* gci, GV* gv) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         int m = grp[i];
         const int end = grp[i + 1];
-        const double di = diag[i];
+        const double ri = rs[i];
         for (int k = rp[i]; m < end; ++k, ++m) {
             const int j = ci[k];
             gci[m] = j;
-            put(gv + m, (j == i) ? 1.0 / sqrt(di) : -(double)av[k] / (2.0 * sqrt(di * diag[j])));
+            put(gv + m, (j == i) ? ri : -0.5 * (double)av[k] * ri * rs[j]);
         }
     }
 }
 
 template <typename T, typename GV>
 __global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
-                          const double* __restrict__ diag, const int* __restrict__ gtrp, int* gtci, GV* gtv,
+                          const double* __restrict__ rs, const int* __restrict__ gtrp, int* gtci, GV* gtv,
                           int* err) {
     int bits = 0;
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
         int m = gtrp[j];
         const int end = gtrp[j + 1];
-        const double dj = diag[j];
+        const double rj = rs[j];
         const int b = rp[j + 1];
         for (int k = b - (end - m); k < b; ++k, ++m) {
             const int i = ci[k];   // i >= j
             gtci[m] = i;
-            if (i == j) { put(gtv + m, 1.0 / sqrt(dj)); continue; }
+            if (i == j) { put(gtv + m, rj); continue; }
             const int pos = find_col(ci, rp[i], rp[i + 1], j);
             if (pos < 0) { bits |= ERR_ASYM; put(gtv + m, 0.0); continue; }
-            put(gtv + m, -(double)av[pos] / (2.0 * sqrt(diag[i] * dj)));
+            put(gtv + m, -0.5 * (double)av[pos] * rs[i] * rj);
         }
     }
     if (bits) atomicOr(err, bits);

@@ -190,6 +190,7 @@ struct sla_csr {
     // also the caller's copies in flight on other streams.
     DevBuf derr;               // one int: error bits of the diagonal and SPAI value kernels
     DevBuf dorig;              // [batch][n] diagonal in the caller's order (SPAI, reordered handles)
+    DevBuf drs;                // [batch][n] 1 / sqrt(A_ii) in the caller's order (SPAI)
     DevBuf ptmp;               // 2 x [batch][n] values: permuted right-hand side / initial guess, result
     bool vals_aligned = false;  // values 16-byte aligned for every system (bulk-copy forms)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
@@ -1086,8 +1087,15 @@ static sla_status spai_values(sla_csr* h, cudaStream_t s, bool fill_only = false
     DevBuf& gtrp = h->reordered ? h->gtrp0 : h->gtrp;
     DevBuf& gtci = h->reordered ? h->gtci0 : h->gtci;
     DevBuf& gtvb = h->reordered ? h->gtv0 : h->gtv;
+    if (h->drs.bytes < sizeof(double) * (size_t)n * h->batch) TRY(h->drs.alloc(sizeof(double) * (size_t)n * h->batch));
+    {
+        const long long m = (long long)n * h->batch;
+        const int gr = (int)std::min<long long>((m + 255) / 256, 4096);
+        k_rsqrt_diag<<<gr, 256, 0, s>>>((int)m, dbase, h->drs.as<double>());
+        TRY(launched());
+    }
     for (int sy = 0; sy < h->batch; ++sy) {
-        const double* dg = dbase + (size_t)sy * n;
+        const double* dg = h->drs.as<double>() + (size_t)sy * n;
         double* gv = gvb.as<double>() + (size_t)sy * h->gstride;     // 8-byte slots: fp64, or a
         double* gtv = gtvb.as<double>() + (size_t)sy * h->gstride;   // double-float pair for fp32
         if (h->dt == SLA_F64) {
