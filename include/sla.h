@@ -82,7 +82,8 @@ typedef enum {
 #define SLA_PRODUCER_CONSUMER 16u /* use the producer/consumer product where it applies (see sla_csr_layout) */
 #define SLA_REORDER 32u      /* always iterate on the reordered matrix (see sla_pcg_solve) */
 #define SLA_NO_REORDER 64u   /* never reorder */
-#define SLA_STAGED 128u      /* never use the direct product form (see sla_csr_layout) */
+#define SLA_STAGED 128u      /* never use the direct or sliced product forms, for any matrix of the
+                                solves (see sla_csr_layout) */
 #define SLA_SLICED 256u      /* use the sliced product form wherever it pads little, also for the
                                 SPAI factors (see sla_csr_layout) */
 #define SLA_SPLIT_ROWS 512u  /* staged forms 1 and 2 with one lane per row: always sum a group with

@@ -88,7 +88,8 @@ class CSRMatrix:
     product where it applies; reorder=True / False forces / forbids
     iterating on a reverse Cuthill-McKee reordering (default: reorder
     scattered patterns); staged=True keeps the warp-staged product forms
-    where the direct (thread-per-row) form would be the default;
+    where the direct (thread-per-row) or the sliced form would be the
+    default, for every matrix of the solves;
     sliced=True uses the sliced product form (a handle-owned copy of the
     iteration matrix and of the SPAI factors in 32-row slices) where it
     applies; split=True / False forces / forbids summing the staged groups
