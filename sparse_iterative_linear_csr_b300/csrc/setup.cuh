@@ -303,10 +303,14 @@ __global__ void k_fill_G(int n, const int* __restrict__ rp, const int* __restric
     }
 }
 
+// gtpos[m]: the entry of A whose value G^T's entry m takes (row i, column
+// j of A for G^T's row j, column i; -1 for the diagonal).  The first fill
+// (have_pos false) finds it by a search of row i and records it; later
+// fills, after a values update, read it.
 template <typename T, typename GV>
 __global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restrict__ ci, const T* __restrict__ av,
                           const double* __restrict__ rs, const int* __restrict__ gtrp, int* gtci, GV* gtv,
-                          int* err) {
+                          int* gtpos, bool have_pos, int* err) {
     int bits = 0;
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
         int m = gtrp[j];
@@ -316,8 +320,18 @@ __global__ void k_fill_GT(int n, const int* __restrict__ rp, const int* __restri
         for (int k = b - (end - m); k < b; ++k, ++m) {
             const int i = ci[k];   // i >= j
             gtci[m] = i;
-            if (i == j) { put(gtv + m, rj); continue; }
-            const int pos = find_col(ci, rp[i], rp[i + 1], j);
+            if (i == j) {
+                if (!have_pos) gtpos[m] = -1;
+                put(gtv + m, rj);
+                continue;
+            }
+            int pos;
+            if (have_pos) {
+                pos = gtpos[m];
+            } else {
+                pos = find_col(ci, rp[i], rp[i + 1], j);
+                gtpos[m] = pos;
+            }
             if (pos < 0) { bits |= ERR_ASYM; put(gtv + m, 0.0); continue; }
             put(gtv + m, -0.5 * (double)av[pos] * rs[i] * rj);
         }

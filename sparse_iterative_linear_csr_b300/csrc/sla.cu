@@ -191,6 +191,7 @@ struct sla_csr {
     DevBuf derr;               // one int: error bits of the diagonal and SPAI value kernels
     DevBuf dorig;              // [batch][n] diagonal in the caller's order (SPAI, reordered handles)
     DevBuf drs;                // [batch][n] 1 / sqrt(A_ii) in the caller's order (SPAI)
+    DevBuf gtpos;              // [nnz(G)] entry of A behind each entry of G^T (caller's order)
     DevBuf ptmp;               // 2 x [batch][n] values: permuted right-hand side / initial guess, result
     bool vals_aligned = false;  // values 16-byte aligned for every system (bulk-copy forms)
     bool pipeline = false;      // SLA_WARP_PIPELINE: warp-pipeline product where it applies
@@ -1094,6 +1095,9 @@ static sla_status spai_values(sla_csr* h, cudaStream_t s, bool fill_only = false
         k_rsqrt_diag<<<gr, 256, 0, s>>>((int)m, dbase, h->drs.as<double>());
         TRY(launched());
     }
+    // positions of G^T's values in A, found by the first fill (system 0)
+    const bool have_pos = h->gtpos.p != nullptr && h->gtpos.bytes >= sizeof(int) * (size_t)h->nnzg;
+    if (!have_pos) TRY(h->gtpos.alloc(sizeof(int) * (size_t)(h->nnzg > 0 ? h->nnzg : 1)));
     for (int sy = 0; sy < h->batch; ++sy) {
         const double* dg = h->drs.as<double>() + (size_t)sy * n;
         double* gv = gvb.as<double>() + (size_t)sy * h->gstride;     // 8-byte slots: fp64, or a
@@ -1103,14 +1107,14 @@ static sla_status spai_values(sla_csr* h, cudaStream_t s, bool fill_only = false
             k_fill_G<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, grp.as<int>(), gci.as<int>(), gv);
             TRY(launched());
             k_fill_GT<double, double><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, gtrp.as<int>(), gtci.as<int>(), gtv,
-                                                        err.as<int>());
+                                                        h->gtpos.as<int>(), have_pos, err.as<int>());
         } else {
             const float* av = (const float*)h->vals + (size_t)sy * h->nnz;
             k_fill_G<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, grp.as<int>(), gci.as<int>(),
                                                       reinterpret_cast<float2*>(gv));
             TRY(launched());
             k_fill_GT<float, float2><<<g, 256, 0, s>>>(n, h->rp, h->ci, av, dg, gtrp.as<int>(), gtci.as<int>(),
-                                                       reinterpret_cast<float2*>(gtv), err.as<int>());
+                                                       reinterpret_cast<float2*>(gtv), h->gtpos.as<int>(), have_pos, err.as<int>());
         }
         TRY(launched());
     }
