@@ -377,6 +377,64 @@ def test_sliced_windows_batched(cuda_device):
     assert M.layout_of("B")[0] == 6
 
 
+def _window_pattern(n, lo, hi, seed):
+    """Rows of lo..hi random columns, 2% of them empty, plus an empty block
+    of 100 rows inside the third 256-row window and 7 empty rows at the end."""
+    g = np.random.default_rng(seed)
+    lens = g.integers(lo, hi + 1, n)
+    lens[g.random(n) < 0.02] = 0
+    lens[512:612] = 0
+    lens[-7:] = 0
+    rp = np.zeros(n + 1, np.int64)
+    rp[1:] = np.cumsum(lens)
+    ci = np.concatenate([np.sort(g.choice(n, size=k, replace=False)) for k in lens])
+    return CSR(n, rp.astype(np.int32), ci.astype(np.int32), g.standard_normal(int(rp[-1])))
+
+
+def _slice_widths(lens, window):
+    """Widths of the 32-row slices with the rows in their own order and with
+    the rows of every window sorted by decreasing length."""
+    n = lens.size
+    ns = (n + 31) // 32
+
+    def widths(v):
+        return np.concatenate([v, np.zeros(ns * 32 - n, v.dtype)]).reshape(ns, 32).max(1)
+    return widths(lens), widths(np.concatenate([np.sort(lens[w:w + window])[::-1] for w in range(0, n, window)]))
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("sliced", [False, True], ids=["default", "sliced"])
+@pytest.mark.parametrize("lo,hi,form", [(12, 18, 6), (5, 7, 7)], ids=["long", "short"])
+def test_sliced_windows_with_empty_rows(cuda_device, lo, hi, form, sliced, dtype):
+    """The sliced products on rows sorted by length within 256-row windows
+    (a warp per window, its sums written in row order) where windows hold
+    empty rows, whole slices of them, and the last window and slice are
+    ragged (3001 rows): y = A x and p.Ap against the oracle."""
+    A = _window_pattern(3001, lo, hi, seed=lo)
+    lens = np.diff(A.row_ptr.astype(np.int64))
+    w_rows, w_sorted = _slice_widths(lens, 256)
+    pad_rows, pad_sorted = 32 * int(w_rows.sum()), 32 * int(w_sorted.sum())
+    # the layout these rows get: sorted within 256-row windows (sorting pads
+    # less, and at most 6% over nnz at the smallest window), within the
+    # sliced form's padding limit, with whole slices of empty rows
+    assert pad_sorted <= 1.06 * A.nnz < pad_rows and pad_rows > 1.02 * A.nnz
+    assert (w_sorted == 0).sum() >= 3
+    A = CSR(A.n, A.row_ptr, A.col_idx, A.vals.astype(dtype))
+    M = make(A, reorder=False, sliced=sliced)
+    assert M.layout()[0] == form, M.layout()
+    x = np.random.default_rng(23).standard_normal(A.n).astype(dtype)
+    xd = torch.from_numpy(x).to(cuda_device)
+    y = M.matvec(xd).cpu().numpy()
+    y_o = oracle.spmv(A, x.astype(np.float64))
+    scale = oracle.spmv(CSR(A.n, A.row_ptr, A.col_idx, np.abs(A.vals)), np.abs(x.astype(np.float64)))
+    assert np.all(np.abs(y - y_o) <= SPMV_TOL[dtype] * np.maximum(scale, 1e-300) + (0 if dtype == np.float64 else 1e-30))
+    assert np.all(y[lens == 0] == 0)
+    yd, dot = M.matvec_dot(xd)
+    assert np.array_equal(yd.cpu().numpy(), y)
+    d_o = float(x.astype(np.float64) @ y.astype(np.float64))
+    assert abs(dot.item() - d_o) <= 1e-12 * max(1.0, float(np.abs(x) @ np.abs(y)))
+
+
 @pytest.mark.parametrize("reorder,sliced", [(False, False), (True, False), (False, True), (True, True)])
 def test_spai_follows_update_values(cuda_device, reorder, sliced):
     """After a SPAI solve, new values (a symmetric scaling D A D, same
