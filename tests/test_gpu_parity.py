@@ -462,6 +462,41 @@ def test_spai_follows_update_values(cuda_device, reorder, sliced):
     assert _iters_ok(ai[0].iters, ao["iters"]) and rel(lam.cpu().numpy(), lo) <= 1e-6
 
 
+@pytest.mark.parametrize("cfg", ["c5", "c3"])
+def test_spai_batch_follows_update_values(cuda_device, cfg):
+    """Three systems on one pattern with SPAI (the kNN Laplacian in fp64,
+    the 2D grid in fp32): after new values for every system (D_s A_s D_s,
+    a different scaling per system) each system's factor is that of its new
+    matrix -- the positions of G^T's values in A found at the first fill
+    serve all systems and every later fill -- so every solve matches the
+    oracle's on the new values."""
+    g = np.random.default_rng(9)
+    if cfg == "c5":
+        A1 = build("c5", npoints=4000).A
+        A = CSR(A1.n, A1.row_ptr, A1.col_idx, np.stack([A1.vals * s for s in (1.0, 1.5, 0.75)]))
+        b, tol = g.standard_normal((3, A.n)), 1e-10
+    else:
+        w = build("c3", N=32, batch=3)
+        A, b, tol = w.A, w.b, w.tol
+    bd = torch.from_numpy(b).to(cuda_device)
+    M = make(A)
+
+    def check(Ak):
+        x, info = M.solve(bd, tol=tol, max_iter=20000, pc="spai", eps=1e-3)
+        xo, io = oracle.pcg(Ak, b, tol, max_iter=20000, pc="spai", eps=1e-3)
+        for s in range(3):
+            assert info[s].status == "ok" and io[s]["status"] == "ok"
+            assert _iters_ok(info[s].iters, io[s]["iters"]), (s, info[s].iters, io[s]["iters"])
+            assert rel(x[s].cpu().numpy(), xo[s]) <= 1e-6
+            assert info[s].rel_res_true <= tol
+    check(A)
+    r = A.rows()
+    v2 = np.stack([A.vals[s] * d[r] * d[A.col_idx] for s, d in enumerate(0.5 + g.random((3, A.n)))])
+    A2 = CSR(A.n, A.row_ptr, A.col_idx, v2.astype(A.vals.dtype))
+    M.update_values(torch.from_numpy(A2.vals).to(cuda_device))
+    check(A2)
+
+
 def _walk_costs(rp):
     """Warp-wide fp64 steps of a staged product over 32-row groups, summed:
     one lane per row (the longest row of every group) and with the group's
