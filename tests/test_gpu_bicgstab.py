@@ -104,6 +104,62 @@ def test_bicgstab_batch_with_a_zero_rhs(cuda_device):
         assert info[1].iters == 0 and not xh[1].any()
 
 
+def _skewed_nonsym(n, seed):
+    """Nonsymmetric, strictly diagonally dominant by rows: every 32nd row
+    holds 40 random columns within 500 of the diagonal, the others 2, plus
+    the diagonal (every 32-row group of A holds one row far longer than the
+    rest; the rows of A^T are even)."""
+    g = np.random.default_rng(seed)
+    lens = np.full(n, 2)
+    lens[::32] = 40
+    r = np.repeat(np.arange(n), lens)
+    c = np.clip(r + g.integers(-500, 501, size=r.size), 0, n - 1)
+    key = np.unique(r.astype(np.int64) * n + c)
+    r, c = key // n, key % n
+    off = r != c
+    r = np.concatenate([r[off], np.arange(n)])
+    c = np.concatenate([c[off], np.arange(n)])
+    v = np.concatenate([g.standard_normal(r.size - n), np.zeros(n)])
+    v[-n:] = np.bincount(r[:-n], weights=np.abs(v[:-n]), minlength=n) * 1.2 + 0.5
+    order = np.lexsort((c, r))
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(np.bincount(r, minlength=n))
+    return CSR(n, rp, c[order].astype(np.int32), v[order])
+
+
+@pytest.mark.parametrize("split", [None, True, False], ids=["auto", "split", "rows"])
+def test_bicgstab_split_group_sums(cuda_device, split):
+    """BiCGStab (right Jacobi) and its transpose adjoint on staged products
+    of a pattern whose 32-row groups each hold one row far longer than the
+    rest: by default A's groups are summed split over the lanes (the
+    lane-per-row walk costs 3.2 times the split one) and A^T's are not
+    (1.3); forced either way.  x, lambda and dL/dA against the oracle."""
+    A = _skewed_nonsym(20000, 5)
+    tol = 1e-10
+    gen = np.random.default_rng(31)
+    bh, gh = gen.standard_normal(A.n), gen.standard_normal(A.n)
+    M = make(A, reorder=False, staged=True, split=split)
+    x, info = M.solve(torch.from_numpy(bh).to(cuda_device), tol=tol, max_iter=20000, pc="jacobi", method="bicgstab")
+    form, _, sp = M.layout_of("B")
+    assert form in (1, 2) and sp == (split is not False), (form, sp)
+    xo, io = oracle.bicgstab(A, bh, tol, max_iter=20000, pc="jacobi")
+    xh = x.cpu().numpy()
+    assert info[0].status == io["status"] == "ok"
+    assert _iters_ok(info[0].iters, io["iters"]), (info[0].iters, io["iters"])
+    assert rel(xh, xo) <= 1e-6
+    assert info[0].rel_res_true <= tol
+    dldb, dlda, ai = M.adjoint(x, torch.from_numpy(gh).to(cuda_device), tol=tol, max_iter=20000, pc="jacobi",
+                               method="bicgstab")
+    form, _, sp = M.layout_of("BT")
+    assert form in (1, 2) and sp == bool(split), (form, sp)
+    lb_o, la_o, ao = oracle.bicgstab_adjoint(A, xh, gh, tol, max_iter=20000, pc="jacobi")
+    lb, la = dldb.cpu().numpy(), dlda.cpu().numpy()
+    assert ai[0].status == ao["status"] == "ok"
+    assert _iters_ok(ai[0].iters, ao["iters"]), (ai[0].iters, ao["iters"])
+    assert rel(lb, lb_o) <= 1e-6 and rel(la, la_o) <= 1e-6
+    assert np.array_equal(la, -lb[A.rows()] * xh[A.col_idx])
+
+
 @pytest.mark.parametrize("staged", [False, True], ids=["default", "staged"])
 @pytest.mark.parametrize("pc", ["none", "jacobi"])
 def test_bicgstab_adjoint_parity(cuda_device, pc, staged):
