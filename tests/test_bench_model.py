@@ -85,3 +85,14 @@ def test_reference_arm_prints_one_contract_line():
     for key in ("workload", "n", "nnz", "batch", "pc", "tol", "poll_k", "step", "l2"):
         assert key in d["config"], key
     assert d["config"]["workload"].startswith("c1:")
+
+
+def test_l2_rule_follows_the_working_set():
+    """A workload whose iteration touches more than L2 (126 MiB) is timed
+    with no flush; one that fits (the 64x64 Poisson grid, and the
+    profiler-capture sizes) gets an L2 flush before every timed step."""
+    for name, kw, resident in (("c1", {}, True), ("c2", {}, False), ("c4", {"N": 24}, True)):
+        w = build(name, **kw)
+        bm = bench.byte_model(w, bench.nnzg_of(w))
+        assert bench.l2_resident(bm) == resident, name
+        assert bench.l2_rule(bm).startswith("L2 flushed" if resident else "inputs larger than L2"), name
