@@ -50,6 +50,13 @@ def test_host_only_calls(lib):
     assert b"n must be" in lib.sla_last_error()
     assert lib.sla_pcg_solve(None, None, None, C.byref(o), None, None) == _lib.SLA_ERR_INVALID
     assert lib.sla_csr_destroy(None) == _lib.SLA_ERR_INVALID
+    f, g, sp = C.c_int(-1), C.c_int(-1), C.c_int(-1)
+    for fn, args in ((lib.sla_csr_layout_of, (None, 0, C.byref(f), C.byref(g), C.byref(sp))),
+                     (lib.sla_csr_layout, (None, C.byref(f), C.byref(g), C.byref(sp))),
+                     (lib.sla_csr_update_values, (None, None, None))):
+        assert fn(*args) == _lib.SLA_ERR_INVALID
+        assert b"null handle" in lib.sla_last_error()
+    assert (f.value, g.value, sp.value) == (-1, -1, -1)
 
 
 def test_struct_layouts_match_header():
