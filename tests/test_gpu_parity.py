@@ -377,6 +377,26 @@ def test_sliced_windows_batched(cuda_device):
     assert M.layout_of("B")[0] == 6
 
 
+def test_matrix_without_entries(cuda_device):
+    """A pattern with no stored entries (nnz = 0, every row empty): the
+    product and p.Ap are zero, and CG returns x = 0 as the oracle does --
+    after 0 iterations with status ok for b = 0, and with status breakdown
+    (p.Ap = 0 at the first step) otherwise."""
+    n = 1000
+    A = CSR(n, np.zeros(n + 1, np.int32), np.zeros(0, np.int32), np.zeros(0))
+    M = make(A)
+    assert M.layout()[0] == 5
+    x = torch.from_numpy(np.random.default_rng(2).standard_normal(n)).to(cuda_device)
+    assert not M.matvec(x).cpu().numpy().any()
+    y, dot = M.matvec_dot(x)
+    assert not y.cpu().numpy().any() and dot.item() == 0.0
+    for b in (np.zeros(n), np.random.default_rng(3).standard_normal(n)):
+        xs, info = M.solve(torch.from_numpy(b).to(cuda_device), tol=1e-8, max_iter=100)
+        xo, io = oracle.pcg(A, b, 1e-8, max_iter=100, pc="none")
+        assert (info[0].status, info[0].iters) == (io["status"], io["iters"]), (info[0], io)
+        assert not xs.cpu().numpy().any()
+
+
 def _window_pattern(n, lo, hi, seed):
     """Rows of lo..hi random columns, 2% of them empty, plus an empty block
     of 100 rows inside the third 256-row window and 7 empty rows at the end."""
